@@ -1,1 +1,263 @@
-"""GB300-native GGUF block-quantized matmul (placeholder; binding added below)."""
+"""GB300-native GGUF block-quantized matmul: thin Python binding of libgguf_gb300.
+
+Each function has the name of the C-ABI entry point it calls and only
+marshals arguments (torch CUDA tensors -> device pointers, the current CUDA
+stream, workspace allocation through torch's caching allocator).  Every step
+of the computation runs in the library's CUDA kernels; there is no fallback:
+if the library is missing or the device is not a CUDA GPU, the calls raise.
+
+Packed weights and q8_1 activations are ``torch.uint8`` tensors of shape
+``[rows, row_size]``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+F32, F16, Q8_0, Q8_1, Q4_K, Q6_K, BF16 = 0, 1, 8, 9, 12, 14, 30
+GATE_UP_SWIGLU, DOWN_WEIGHTED_SUM = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgguf_gb300.so")
+
+_DTYPE_OF = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}
+_TYPE_OF = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+
+_STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED_TYPE", 3: "SHAPE", 4: "ALIGNMENT", 5: "WORKSPACE", 6: "CUDA"}
+
+
+class GgufError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class MoeArgs(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("wt", ctypes.c_int), ("n_experts", ctypes.c_int64),
+                ("expert_stride", ctypes.c_int64), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("x", ctypes.c_void_p), ("xt", ctypes.c_int), ("n_tokens", ctypes.c_int64),
+                ("ldx", ctypes.c_int64), ("ids", ctypes.c_void_p), ("top_k", ctypes.c_int64),
+                ("route_w", ctypes.c_void_p), ("mode", ctypes.c_int), ("y", ctypes.c_void_p),
+                ("yt", ctypes.c_int), ("dev_status", ctypes.c_void_p)]
+
+
+class MoeFfnArgs(ctypes.Structure):
+    _fields_ = [("w_gate_up", ctypes.c_void_p), ("gate_up_type", ctypes.c_int), ("gate_up_stride", ctypes.c_int64),
+                ("w_down", ctypes.c_void_p), ("down_type", ctypes.c_int), ("down_stride", ctypes.c_int64),
+                ("n_experts", ctypes.c_int64), ("hidden", ctypes.c_int64), ("inter", ctypes.c_int64),
+                ("x", ctypes.c_void_p), ("xt", ctypes.c_int), ("n_tokens", ctypes.c_int64), ("ldx", ctypes.c_int64),
+                ("ids", ctypes.c_void_p), ("top_k", ctypes.c_int64), ("route_w", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("yt", ctypes.c_int), ("dev_status", ctypes.c_void_p)]
+
+
+# name -> (restype, argtypes); the exported C-ABI of include/gguf_gb300.h
+_i, _i64, _p, _sz = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+SIGNATURES = {
+    "gguf_last_error": (ctypes.c_char_p, []),
+    "gguf_type_block_elems": (_i64, [_i]),
+    "gguf_type_block_bytes": (_i64, [_i]),
+    "gguf_row_size": (_i64, [_i, _i64]),
+    "gguf_quantize_q8_1": (_i, [_p, _i, _i64, _i64, _i64, _p, _p]),
+    "gguf_dequantize": (_i, [_p, _i, _i64, _i64, _p, _i, _p]),
+    "gguf_get_rows": (_i, [_p, _i, _i64, _i64, _p, _i64, _p, _i, _p]),
+    "gguf_mul_mat_ws_size": (_sz, [_i, _i64, _i64, _i, _i64]),
+    "gguf_mul_mat": (_i, [_p, _i, _i64, _i64, _p, _i, _i64, _i64, _p, _i, _i64, _p, _sz, _p]),
+    "gguf_mul_mat_id_ws_size": (_sz, [ctypes.POINTER(MoeArgs)]),
+    "gguf_mul_mat_id": (_i, [ctypes.POINTER(MoeArgs), _p, _sz, _p]),
+    "gguf_moe_ffn_ws_size": (_sz, [ctypes.POINTER(MoeFfnArgs)]),
+    "gguf_moe_ffn": (_i, [ctypes.POINTER(MoeFfnArgs), _p, _sz, _p]),
+    "gguf_debug_block_dots": (_i, [_p, _i, _i64, _i64, _p, _i64, _p, _p]),
+    "gguf_set_option": (_i, [ctypes.c_char_p, _i64]),
+    "gguf_get_option": (_i64, [ctypes.c_char_p]),
+}
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libgguf_gb300.so (built by ``build.build()``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libgguf_gb300.so is not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(st: int):
+    if st != 0:
+        raise GgufError(st, load_library().gguf_last_error().decode())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("gguf: tensors must live on a CUDA device")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor | None:
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def gguf_row_size(t: int, k: int) -> int:
+    return int(load_library().gguf_row_size(t, k))
+
+
+def gguf_set_option(key: str, value: int):
+    _check(load_library().gguf_set_option(key.encode(), int(value)))
+
+
+def gguf_get_option(key: str) -> int:
+    return int(load_library().gguf_get_option(key.encode()))
+
+
+def gguf_quantize_q8_1(x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """x [m, k] (fp32 / bf16 / fp16, rows may be strided) -> q8_1 bytes [m, k/32*36]."""
+    m, k = x.shape
+    if x.stride(1) != 1:
+        raise ValueError("gguf_quantize_q8_1: rows must be contiguous")
+    rs = gguf_row_size(Q8_1, k)
+    if out is None:
+        out = torch.empty((m, max(rs, 0)), dtype=torch.uint8, device=x.device)
+    _check(load_library().gguf_quantize_q8_1(_ptr(x), _TYPE_OF[x.dtype], m, k, x.stride(0), _ptr(out), _stream()))
+    return out
+
+
+def gguf_dequantize(w: torch.Tensor, wt: int, rows: int, k: int, out_dtype=torch.float32,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty((rows, k), dtype=out_dtype, device=w.device)
+    _check(load_library().gguf_dequantize(_ptr(w), wt, rows, k, _ptr(out), _TYPE_OF[out.dtype], _stream()))
+    return out
+
+
+def gguf_get_rows(table: torch.Tensor, tt: int, rows: int, k: int, ids: torch.Tensor, out_dtype=torch.float32,
+                  out: torch.Tensor | None = None) -> torch.Tensor:
+    n = ids.numel()
+    if out is None:
+        out = torch.empty((n, k), dtype=out_dtype, device=ids.device)
+    _check(load_library().gguf_get_rows(_ptr(table), tt, rows, k, _ptr(ids), n, _ptr(out), _TYPE_OF[out.dtype],
+                                        _stream()))
+    return out
+
+
+def gguf_mul_mat_ws_size(wt: int, n: int, k: int, xt: int, m: int) -> int:
+    return int(load_library().gguf_mul_mat_ws_size(wt, n, k, xt, m))
+
+
+def gguf_mul_mat(w: torch.Tensor, wt: int, n: int, k: int, x: torch.Tensor, xt: int | None = None,
+                 m: int | None = None, out: torch.Tensor | None = None, out_dtype=None,
+                 ws: torch.Tensor | None = None) -> torch.Tensor:
+    """y[m, n] = x[m, k] @ W[n, k]^T.  ``x`` is a float tensor, or q8_1 bytes
+    with ``xt=Q8_1`` (then ``m`` = rows of x).  ``out`` may be a column slice of
+    a wider row-major tensor (its row stride becomes ldy)."""
+    if xt is None:
+        xt = _TYPE_OF[x.dtype]
+    if m is None:
+        m = x.shape[0]
+    ldx = x.stride(0) if xt != Q8_1 else gguf_row_size(Q8_1, k)
+    if out is None:
+        if out_dtype is None:
+            out_dtype = x.dtype if xt != Q8_1 else torch.float32
+        out = torch.empty((m, n), dtype=out_dtype, device=x.device)
+    if out.stride(1) != 1:
+        raise ValueError("gguf_mul_mat: output rows must be contiguous")
+    need = gguf_mul_mat_ws_size(wt, n, k, xt, m)
+    if ws is None:
+        ws = _workspace(need, x.device)
+    _check(load_library().gguf_mul_mat(_ptr(w), wt, n, k, _ptr(x), xt, m, ldx, _ptr(out), _TYPE_OF[out.dtype],
+                                       out.stride(0), _ptr(ws), 0 if ws is None else ws.numel(), _stream()))
+    return out
+
+
+def moe_args(w, wt, n_experts, expert_stride, n, k, x, xt, n_tokens, ldx, ids, top_k, route_w, mode, y, yt,
+             dev_status=None) -> MoeArgs:
+    return MoeArgs(w.data_ptr(), wt, n_experts, expert_stride, n, k, x.data_ptr(), xt, n_tokens, ldx,
+                   ids.data_ptr(), top_k, 0 if route_w is None else route_w.data_ptr(), mode, y.data_ptr(), yt,
+                   0 if dev_status is None else dev_status.data_ptr())
+
+
+def gguf_mul_mat_id_ws_size(args: MoeArgs) -> int:
+    return int(load_library().gguf_mul_mat_id_ws_size(ctypes.byref(args)))
+
+
+def gguf_mul_mat_id(w: torch.Tensor, wt: int, n_experts: int, expert_stride: int, n: int, k: int, x: torch.Tensor,
+                    ids: torch.Tensor, mode: int, route_w: torch.Tensor | None = None, xt: int | None = None,
+                    out_type: int | None = None, out: torch.Tensor | None = None,
+                    dev_status: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
+    """MoE expert product (see include/gguf_gb300.h for the two modes)."""
+    n_tokens, top_k = ids.shape
+    if xt is None:
+        xt = _TYPE_OF[x.dtype]
+    ldx = x.stride(0) if xt != Q8_1 else gguf_row_size(Q8_1, k)
+    if out is None:
+        if mode == GATE_UP_SWIGLU:
+            yt = BF16 if out_type is None else out_type
+            i_dim = n // 2
+            out = (torch.empty((n_tokens * top_k, i_dim), dtype=torch.bfloat16, device=x.device) if yt == BF16 else
+                   torch.empty((n_tokens * top_k, gguf_row_size(Q8_1, i_dim)), dtype=torch.uint8, device=x.device))
+        else:
+            yt = BF16 if out_type is None else out_type
+            out = torch.empty((n_tokens, n), dtype=_DTYPE_OF[yt], device=x.device)
+    else:
+        yt = out_type if out_type is not None else (Q8_1 if out.dtype == torch.uint8 else _TYPE_OF[out.dtype])
+    args = moe_args(w, wt, n_experts, expert_stride, n, k, x, xt, n_tokens, ldx, ids, top_k, route_w, mode, out,
+                    yt, dev_status)
+    need = gguf_mul_mat_id_ws_size(args)
+    if ws is None:
+        ws = _workspace(need, x.device)
+    _check(load_library().gguf_mul_mat_id(ctypes.byref(args), _ptr(ws), 0 if ws is None else ws.numel(), _stream()))
+    return out
+
+
+def moe_ffn_args(w_gate_up, gate_up_type, gate_up_stride, w_down, down_type, down_stride, n_experts, hidden, inter,
+                 x, xt, ids, top_k, route_w, y, yt, dev_status=None) -> MoeFfnArgs:
+    return MoeFfnArgs(w_gate_up.data_ptr(), gate_up_type, gate_up_stride, w_down.data_ptr(), down_type, down_stride,
+                      n_experts, hidden, inter, x.data_ptr(), xt, ids.shape[0], x.stride(0) if xt != Q8_1 else 0,
+                      ids.data_ptr(), top_k, 0 if route_w is None else route_w.data_ptr(), y.data_ptr(), yt,
+                      0 if dev_status is None else dev_status.data_ptr())
+
+
+def gguf_moe_ffn_ws_size(args: MoeFfnArgs) -> int:
+    return int(load_library().gguf_moe_ffn_ws_size(ctypes.byref(args)))
+
+
+def gguf_moe_ffn(w_gate_up: torch.Tensor, gate_up_type: int, gate_up_stride: int, w_down: torch.Tensor,
+                 down_type: int, down_stride: int, n_experts: int, hidden: int, inter: int, x: torch.Tensor,
+                 ids: torch.Tensor, route_w: torch.Tensor | None, out: torch.Tensor | None = None,
+                 dev_status: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
+    """The whole MoE expert block: y = sum_k w_k * down_e(silu(gate_e x) * up_e x)."""
+    n_tokens, top_k = ids.shape
+    xt = _TYPE_OF[x.dtype] if x.dtype != torch.uint8 else Q8_1
+    if out is None:
+        out = torch.empty((n_tokens, hidden), dtype=x.dtype if xt != Q8_1 else torch.bfloat16, device=x.device)
+    args = moe_ffn_args(w_gate_up, gate_up_type, gate_up_stride, w_down, down_type, down_stride, n_experts, hidden,
+                        inter, x, xt, ids, top_k, route_w, out, _TYPE_OF[out.dtype], dev_status)
+    need = gguf_moe_ffn_ws_size(args)
+    if ws is None:
+        ws = _workspace(need, x.device)
+    _check(load_library().gguf_moe_ffn(ctypes.byref(args), _ptr(ws), 0 if ws is None else ws.numel(), _stream()))
+    return out
+
+
+def gguf_debug_block_dots(w: torch.Tensor, wt: int, n: int, k: int, xq: torch.Tensor, m: int) -> torch.Tensor:
+    sub = 16 if wt == Q6_K else 32
+    out = torch.empty((m, n, k // sub), dtype=torch.int32, device=xq.device)
+    _check(load_library().gguf_debug_block_dots(_ptr(w), wt, n, k, _ptr(xq), m, _ptr(out), _stream()))
+    return out

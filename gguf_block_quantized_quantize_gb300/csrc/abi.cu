@@ -1,0 +1,359 @@
+// C ABI of libgguf_gb300: argument validation, path dispatch and error
+// reporting.  Every entry point validates on the host, returns a status code
+// and never aborts; kernels are launched asynchronously on the caller's stream.
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gg {
+
+static thread_local std::string g_last_error;
+
+static gguf_status fail(gguf_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+static gguf_status cuda_status(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return GGUF_OK;
+    return fail(GGUF_ERR_CUDA, "%s: CUDA error %d (%s)", what, (int)e, cudaGetErrorString(e));
+}
+
+const DeviceInfo &device_info() {
+    static DeviceInfo infos[64];
+    static bool have[64];
+    static std::mutex mu;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        DeviceInfo di{};
+        cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&di.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        int optin = 0;
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        di.smem_optin = (size_t)optin;
+        if (di.sm_count <= 0) di.sm_count = 1;
+        infos[dev] = di;
+        have[dev] = true;
+    }
+    return infos[dev];
+}
+
+// tunables
+static int64_t g_mmvq_max_m = 8;
+static int64_t g_mmq_enable = 1;
+
+static bool is_float(int t) { return t == GGUF_F32 || t == GGUF_F16 || t == GGUF_BF16; }
+static bool is_weight(int t) { return t == GGUF_Q8_0 || t == GGUF_Q4_K || t == GGUF_Q6_K; }
+static int64_t esize(int t) { return t == GGUF_F32 ? 4 : 2; }
+static int64_t row_size(int t, int64_t k) {
+    const int64_t be = block_elems(t);
+    if (be == 0 || k < 0 || k % be) return -1;
+    return k / be * block_bytes(t);
+}
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Which engine runs a dense product of m activation rows of length k: MMVQ
+// holds one 32-value piece per thread (k <= 16384); MMQ takes the rest.
+static bool use_mmq(int64_t m, int64_t k) { return k > 16384 || (g_mmq_enable != 0 && m > g_mmvq_max_m); }
+
+}  // namespace gg
+
+using namespace gg;
+
+extern "C" {
+
+const char *gguf_last_error(void) { return g_last_error.c_str(); }
+
+int64_t gguf_type_block_elems(int type) { return block_elems(type); }
+int64_t gguf_type_block_bytes(int type) { return block_bytes(type); }
+int64_t gguf_row_size(int type, int64_t k) { return row_size(type, k); }
+
+gguf_status gguf_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int64_t ldx, void *xq,
+                               gguf_stream_t stream) {
+    if (!is_float(xt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "quantize_q8_1: x type %d is not F32/BF16/F16", xt);
+    if (m < 0 || k < 0) return fail(GGUF_ERR_INVALID_ARG, "quantize_q8_1: negative size");
+    if (k % 32) return fail(GGUF_ERR_SHAPE, "quantize_q8_1: k=%lld is not a multiple of 32", (long long)k);
+    if (ldx < k) return fail(GGUF_ERR_INVALID_ARG, "quantize_q8_1: ldx=%lld < k=%lld", (long long)ldx, (long long)k);
+    if (m == 0 || k == 0) return GGUF_OK;
+    if (!x || !xq) return fail(GGUF_ERR_INVALID_ARG, "quantize_q8_1: null pointer");
+    if (!aligned(x, esize(xt)) || !aligned(xq, 4))
+        return fail(GGUF_ERR_ALIGNMENT, "quantize_q8_1: x must be element-aligned and xq 4-byte aligned");
+    return cuda_status(launch_quantize_q8_1(x, xt, m, k, ldx, (uint8_t *)xq, nullptr, (cudaStream_t)stream),
+                       "quantize_q8_1");
+}
+
+gguf_status gguf_dequantize(const void *w, int wt, int64_t rows, int64_t k, void *out, int ot, gguf_stream_t stream) {
+    if (!is_float(ot)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "dequantize: out type %d is not F32/BF16/F16", ot);
+    if (!is_weight(wt) && wt != GGUF_Q8_1 && !is_float(wt))
+        return fail(GGUF_ERR_UNSUPPORTED_TYPE, "dequantize: no converter for type %d", wt);
+    if (rows < 0 || k < 0) return fail(GGUF_ERR_INVALID_ARG, "dequantize: negative size");
+    if (row_size(wt, k) < 0) return fail(GGUF_ERR_SHAPE, "dequantize: k=%lld not a multiple of the block of type %d", (long long)k, wt);
+    if (rows == 0 || k == 0) return GGUF_OK;
+    if (!w || !out) return fail(GGUF_ERR_INVALID_ARG, "dequantize: null pointer");
+    if (is_float(wt)) {
+        if (!aligned(w, esize(wt)) || !aligned(out, esize(ot))) return fail(GGUF_ERR_ALIGNMENT, "dequantize: misaligned float buffer");
+        if (wt == ot)
+            return cuda_status(cudaMemcpyAsync(out, w, (size_t)(rows * k * esize(wt)), cudaMemcpyDeviceToDevice,
+                                               (cudaStream_t)stream), "dequantize copy");
+        return cuda_status(launch_convert_float(w, wt, rows * k, out, ot, (cudaStream_t)stream), "dequantize convert");
+    }
+    if (!aligned(w, 16) || !aligned(out, 16)) return fail(GGUF_ERR_ALIGNMENT, "dequantize: w and out must be 16-byte aligned");
+    return cuda_status(launch_dequantize((const uint8_t *)w, wt, rows, k, nullptr, rows, out, ot, (cudaStream_t)stream),
+                       "dequantize");
+}
+
+gguf_status gguf_get_rows(const void *table, int tt, int64_t rows, int64_t k, const int32_t *ids, int64_t n_ids,
+                          void *out, int ot, gguf_stream_t stream) {
+    if (!is_float(ot)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "get_rows: out type %d is not F32/BF16/F16", ot);
+    if (!is_weight(tt) && tt != GGUF_Q8_1) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "get_rows: table type %d not supported", tt);
+    if (rows < 0 || k < 0 || n_ids < 0) return fail(GGUF_ERR_INVALID_ARG, "get_rows: negative size");
+    if (row_size(tt, k) < 0) return fail(GGUF_ERR_SHAPE, "get_rows: k=%lld not a multiple of the block", (long long)k);
+    if (n_ids == 0 || k == 0) return GGUF_OK;
+    if (!ids || !out || (rows > 0 && !table)) return fail(GGUF_ERR_INVALID_ARG, "get_rows: null pointer");
+    if ((rows > 0 && !aligned(table, 16)) || !aligned(out, 16) || !aligned(ids, 4))
+        return fail(GGUF_ERR_ALIGNMENT, "get_rows: table and out must be 16-byte aligned");
+    if (rows == 0)  // every id is out of range: all rows are zero
+        return cuda_status(cudaMemsetAsync(out, 0, (size_t)(n_ids * k * esize(ot)), (cudaStream_t)stream), "get_rows");
+    return cuda_status(launch_dequantize((const uint8_t *)table, tt, n_ids, k, ids, rows, out, ot, (cudaStream_t)stream),
+                       "get_rows");
+}
+
+size_t gguf_mul_mat_ws_size(int wt, int64_t n, int64_t k, int xt, int64_t m) {
+    (void)wt;
+    (void)n;
+    if (m <= 0 || k <= 0 || k % 32) return 0;
+    if (use_mmq(m, k)) return align256((size_t)(m * k * 2));              // fp16 operand rows
+    if (xt == GGUF_Q8_1) return 0;
+    return align256((size_t)(m * row_size(GGUF_Q8_1, k)));             // q8_1 rows
+}
+
+gguf_status gguf_mul_mat(const void *w, int wt, int64_t n, int64_t k, const void *x, int xt, int64_t m, int64_t ldx,
+                         void *y, int yt, int64_t ldy, void *ws, size_t ws_bytes, gguf_stream_t stream) {
+    if (!is_weight(wt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat: weight type %d not supported", wt);
+    if (!is_float(xt) && xt != GGUF_Q8_1) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat: x type %d not supported", xt);
+    if (!is_float(yt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat: y type %d is not F32/BF16/F16", yt);
+    if (n < 0 || k < 0 || m < 0) return fail(GGUF_ERR_INVALID_ARG, "mul_mat: negative size");
+    if (row_size(wt, k) < 0) return fail(GGUF_ERR_SHAPE, "mul_mat: k=%lld not a multiple of the block of type %d", (long long)k, wt);
+    if (ldy < n) return fail(GGUF_ERR_INVALID_ARG, "mul_mat: ldy=%lld < n=%lld", (long long)ldy, (long long)n);
+    if (is_float(xt) && ldx < k) return fail(GGUF_ERR_INVALID_ARG, "mul_mat: ldx=%lld < k=%lld", (long long)ldx, (long long)k);
+    if (m == 0 || n == 0) return GGUF_OK;
+    if (k == 0) return fail(GGUF_ERR_SHAPE, "mul_mat: k must be positive");
+    if (!w || !x || !y) return fail(GGUF_ERR_INVALID_ARG, "mul_mat: null pointer");
+    if (!aligned(w, 16)) return fail(GGUF_ERR_ALIGNMENT, "mul_mat: weight base must be 16-byte aligned");
+    if (!aligned(y, esize(yt)) || (is_float(xt) && !aligned(x, esize(xt))) || (xt == GGUF_Q8_1 && !aligned(x, 4)))
+        return fail(GGUF_ERR_ALIGNMENT, "mul_mat: misaligned x or y");
+    const size_t need = gguf_mul_mat_ws_size(wt, n, k, xt, m);
+    if (ws_bytes < need || (need > 0 && !ws))
+        return fail(GGUF_ERR_WORKSPACE, "mul_mat: workspace of %zu bytes < required %zu", ws_bytes, need);
+    if (need > 0 && !aligned(ws, 16)) return fail(GGUF_ERR_ALIGNMENT, "mul_mat: workspace must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+
+    if (use_mmq(m, k)) {
+        uint16_t *xh = (uint16_t *)ws;
+        cudaError_t e = xt == GGUF_Q8_1 ? launch_q8_1_to_f16((const uint8_t *)x, m, k, xh, s)
+                                        : launch_quantize_q8_1(x, xt, m, k, ldx, nullptr, xh, s);
+        if (e != cudaSuccess) return cuda_status(e, "mul_mat quantize");
+        return cuda_status(launch_mmq((const uint8_t *)w, wt, n, k, xh, m, y, yt, ldy, s), "mul_mat mmq");
+    }
+    const uint8_t *xq = (const uint8_t *)x;
+    if (xt != GGUF_Q8_1) {
+        cudaError_t e = launch_quantize_q8_1(x, xt, m, k, ldx, (uint8_t *)ws, nullptr, s);
+        if (e != cudaSuccess) return cuda_status(e, "mul_mat quantize");
+        xq = (const uint8_t *)ws;
+    }
+    const int64_t xrb = row_size(GGUF_Q8_1, k);
+    const int64_t ysz = esize(yt);
+    for (int64_t m0 = 0; m0 < m; m0 += 8) {  // MMVQ handles up to 8 rows per launch
+        const int64_t mc = m - m0 < 8 ? m - m0 : 8;
+        cudaError_t e = launch_mmvq((const uint8_t *)w, wt, n, k, xq + m0 * xrb, mc,
+                                    (uint8_t *)y + m0 * ldy * ysz, yt, ldy, s);
+        if (e != cudaSuccess) return cuda_status(e, "mul_mat mmvq");
+    }
+    return GGUF_OK;
+}
+
+// ---------------------------------------------------------------- MoE
+
+static gguf_status check_bank(const char *what, const void *w, int wt, int64_t E, int64_t stride, int64_t n, int64_t k) {
+    if (!is_weight(wt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "%s: weight type %d not supported", what, wt);
+    if (E <= 0 || n <= 0 || k <= 0) return fail(GGUF_ERR_INVALID_ARG, "%s: experts, n and k must be positive", what);
+    if (row_size(wt, k) < 0) return fail(GGUF_ERR_SHAPE, "%s: k=%lld not a multiple of the block of type %d", what, (long long)k, wt);
+    if (stride < n * row_size(wt, k)) return fail(GGUF_ERR_INVALID_ARG, "%s: expert stride %lld < n * row_size", what, (long long)stride);
+    if (stride % 16) return fail(GGUF_ERR_ALIGNMENT, "%s: expert stride must be a multiple of 16 bytes", what);
+    if (!w) return fail(GGUF_ERR_INVALID_ARG, "%s: null weight bank", what);
+    if (!aligned(w, 16)) return fail(GGUF_ERR_ALIGNMENT, "%s: weight bank must be 16-byte aligned", what);
+    return GGUF_OK;
+}
+
+// workspace of one mul_mat_id call
+static MoeWs moe_call_layout(const gguf_moe_args *a, void *base) {
+    const int64_t R = a->n_tokens * a->top_k;
+    if (a->mode == GGUF_MOE_GATE_UP_SWIGLU) return moe_ws_layout(base, a->n_experts, R, a->n_tokens * a->k, 0, 0);
+    return moe_ws_layout(base, a->n_experts, R, R * a->k, a->n_tokens * a->n, 0);
+}
+
+static gguf_status check_moe(const gguf_moe_args *a) {
+    if (!a) return fail(GGUF_ERR_INVALID_ARG, "mul_mat_id: null args");
+    gguf_status st = check_bank("mul_mat_id", a->w, a->wt, a->n_experts, a->expert_stride, a->n, a->k);
+    if (st != GGUF_OK) return st;
+    if (a->n_tokens < 0 || a->top_k <= 0) return fail(GGUF_ERR_INVALID_ARG, "mul_mat_id: bad n_tokens / top_k");
+    if (a->n_tokens * a->top_k > INT32_MAX) return fail(GGUF_ERR_INVALID_ARG, "mul_mat_id: too many routes");
+    if (!is_float(a->xt) && a->xt != GGUF_Q8_1) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat_id: x type %d", a->xt);
+    if (is_float(a->xt) && a->ldx < a->k) return fail(GGUF_ERR_INVALID_ARG, "mul_mat_id: ldx < k");
+    if (a->k % 8) return fail(GGUF_ERR_SHAPE, "mul_mat_id: k must be a multiple of 8");
+    if (a->mode == GGUF_MOE_GATE_UP_SWIGLU) {
+        if (a->n % 128) return fail(GGUF_ERR_SHAPE, "mul_mat_id gate_up: n = 2*I must be a multiple of 128");
+        if (a->yt != GGUF_BF16 && a->yt != GGUF_Q8_1 && a->yt != GGUF_F16)
+            return fail(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat_id gate_up: out type %d is not BF16/Q8_1/F16", a->yt);
+    } else if (a->mode == GGUF_MOE_DOWN_WEIGHTED_SUM) {
+        if (!is_float(a->yt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat_id down: out type %d", a->yt);
+    } else {
+        return fail(GGUF_ERR_INVALID_ARG, "mul_mat_id: unknown mode %d", a->mode);
+    }
+    if (a->n_tokens > 0 && (!a->x || !a->ids || !a->y)) return fail(GGUF_ERR_INVALID_ARG, "mul_mat_id: null pointer");
+    if (a->n_tokens > 0 && (!aligned(a->ids, 4) || !aligned(a->x, a->xt == GGUF_Q8_1 ? 4 : esize(a->xt)) ||
+                            !aligned(a->y, a->yt == GGUF_F32 ? 4 : 2)))
+        return fail(GGUF_ERR_ALIGNMENT, "mul_mat_id: misaligned x, ids or y");
+    return GGUF_OK;
+}
+
+static cudaError_t to_f16_operand(const void *x, int xt, int64_t rows, int64_t k, int64_t ldx, uint16_t *xh,
+                                  cudaStream_t s) {
+    return xt == GGUF_Q8_1 ? launch_q8_1_to_f16((const uint8_t *)x, rows, k, xh, s)
+                           : launch_quantize_q8_1(x, xt, rows, k, ldx, nullptr, xh, s);
+}
+
+size_t gguf_mul_mat_id_ws_size(const gguf_moe_args *args) {
+    if (!args || args->n_experts <= 0 || args->top_k <= 0 || args->n_tokens < 0) return 0;
+    return moe_call_layout(args, nullptr).bytes;
+}
+
+gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, gguf_stream_t stream) {
+    gguf_status st = check_moe(a);
+    if (st != GGUF_OK) return st;
+    if (a->n_tokens == 0) return GGUF_OK;
+    const size_t need = moe_call_layout(a, nullptr).bytes;
+    if (!ws || ws_bytes < need) return fail(GGUF_ERR_WORKSPACE, "mul_mat_id: workspace of %zu bytes < required %zu", ws_bytes, need);
+    if (!aligned(ws, 256)) return fail(GGUF_ERR_ALIGNMENT, "mul_mat_id: workspace must be 256-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    const MoeWs w = moe_call_layout(a, ws);
+    const int64_t R = a->n_tokens * a->top_k;
+    const int bn = moe_bn(R, a->n_experts);
+    cudaError_t e;
+    if (a->mode == GGUF_MOE_GATE_UP_SWIGLU) {
+        const int64_t idim = a->n / 2;
+        const size_t ybytes = a->yt == GGUF_Q8_1 ? (size_t)(R * row_size(GGUF_Q8_1, idim)) : (size_t)(R * idim * 2);
+        if ((e = cudaMemsetAsync(a->y, 0, ybytes, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id");
+        if ((e = to_f16_operand(a->x, a->xt, a->n_tokens, a->k, a->ldx, w.xh, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id quantize");
+        if ((e = moe_group(a->ids, nullptr, R, a->n_experts, false, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id grouping");
+        e = launch_moe_gate_up((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, a->top_k, R,
+                               a->n_experts, w, a->yt == GGUF_Q8_1 ? (uint8_t *)a->y : nullptr,
+                               a->yt == GGUF_BF16 ? (uint16_t *)a->y : nullptr,
+                               a->yt == GGUF_F16 ? (uint16_t *)a->y : nullptr, s);
+        return cuda_status(e, "mul_mat_id gate_up");
+    }
+    if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id quantize");
+    if ((e = moe_group(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id grouping");
+    if ((e = cudaMemsetAsync(w.yacc, 0, sizeof(float) * (size_t)(a->n_tokens * a->n), s)) != cudaSuccess) return cuda_status(e, "mul_mat_id");
+    if ((e = launch_moe_down((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, a->top_k, R,
+                             a->n_experts, a->route_w, w, w.yacc, s)) != cudaSuccess)
+        return cuda_status(e, "mul_mat_id down");
+    return cuda_status(launch_moe_finalize(w.yacc, a->n_tokens * a->n, a->y, a->yt, s), "mul_mat_id finalize");
+}
+
+static MoeWs ffn_layout(const gguf_moe_ffn_args *a, void *base) {
+    const int64_t R = a->n_tokens * a->top_k;
+    return moe_ws_layout(base, a->n_experts, R, a->n_tokens * a->hidden, a->n_tokens * a->hidden, R * a->inter);
+}
+
+size_t gguf_moe_ffn_ws_size(const gguf_moe_ffn_args *a) {
+    if (!a || a->n_experts <= 0 || a->top_k <= 0 || a->n_tokens < 0) return 0;
+    return ffn_layout(a, nullptr).bytes;
+}
+
+gguf_status gguf_moe_ffn(const gguf_moe_ffn_args *a, void *ws, size_t ws_bytes, gguf_stream_t stream) {
+    if (!a) return fail(GGUF_ERR_INVALID_ARG, "moe_ffn: null args");
+    gguf_status st = check_bank("moe_ffn gate_up", a->w_gate_up, a->gate_up_type, a->n_experts, a->gate_up_stride,
+                                2 * a->inter, a->hidden);
+    if (st != GGUF_OK) return st;
+    st = check_bank("moe_ffn down", a->w_down, a->down_type, a->n_experts, a->down_stride, a->hidden, a->inter);
+    if (st != GGUF_OK) return st;
+    if (a->inter % 64) return fail(GGUF_ERR_SHAPE, "moe_ffn: intermediate size must be a multiple of 64");
+    if (a->hidden % 8) return fail(GGUF_ERR_SHAPE, "moe_ffn: hidden size must be a multiple of 8");
+    if (a->n_tokens < 0 || a->top_k <= 0 || a->n_tokens * a->top_k > INT32_MAX) return fail(GGUF_ERR_INVALID_ARG, "moe_ffn: bad n_tokens / top_k");
+    if (!is_float(a->xt) && a->xt != GGUF_Q8_1) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "moe_ffn: x type %d", a->xt);
+    if (!is_float(a->yt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "moe_ffn: y type %d", a->yt);
+    if (is_float(a->xt) && a->ldx < a->hidden) return fail(GGUF_ERR_INVALID_ARG, "moe_ffn: ldx < hidden");
+    if (a->n_tokens == 0) return GGUF_OK;
+    if (!a->x || !a->ids || !a->y) return fail(GGUF_ERR_INVALID_ARG, "moe_ffn: null pointer");
+    const size_t need = ffn_layout(a, nullptr).bytes;
+    if (!ws || ws_bytes < need) return fail(GGUF_ERR_WORKSPACE, "moe_ffn: workspace of %zu bytes < required %zu", ws_bytes, need);
+    if (!aligned(ws, 256)) return fail(GGUF_ERR_ALIGNMENT, "moe_ffn: workspace must be 256-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    const MoeWs w = ffn_layout(a, ws);
+    const int64_t R = a->n_tokens * a->top_k;
+    const int bn = moe_bn(R, a->n_experts);
+    cudaError_t e;
+    if ((e = to_f16_operand(a->x, a->xt, a->n_tokens, a->hidden, a->ldx, w.xh, s)) != cudaSuccess) return cuda_status(e, "moe_ffn quantize");
+    // one grouping serves both GEMMs; a route of weight 0 contributes nothing and is skipped by both
+    if ((e = moe_group(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "moe_ffn grouping");
+    if ((e = launch_moe_gate_up((const uint8_t *)a->w_gate_up, a->gate_up_type, a->gate_up_stride, 2 * a->inter,
+                                a->hidden, w.xh, a->top_k, R, a->n_experts, w, nullptr, nullptr, w.h16, s)) != cudaSuccess)
+        return cuda_status(e, "moe_ffn gate_up");
+    if ((e = cudaMemsetAsync(w.yacc, 0, sizeof(float) * (size_t)(a->n_tokens * a->hidden), s)) != cudaSuccess) return cuda_status(e, "moe_ffn");
+    if ((e = launch_moe_down((const uint8_t *)a->w_down, a->down_type, a->down_stride, a->hidden, a->inter, w.h16,
+                             a->top_k, R, a->n_experts, a->route_w, w, w.yacc, s)) != cudaSuccess)
+        return cuda_status(e, "moe_ffn down");
+    return cuda_status(launch_moe_finalize(w.yacc, a->n_tokens * a->hidden, a->y, a->yt, s), "moe_ffn finalize");
+}
+
+gguf_status gguf_debug_block_dots(const void *w, int wt, int64_t n, int64_t k, const void *xq, int64_t m,
+                                  int32_t *sums, gguf_stream_t stream) {
+    if (!is_weight(wt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "debug_block_dots: weight type %d not supported", wt);
+    if (n < 0 || k < 0 || m < 0) return fail(GGUF_ERR_INVALID_ARG, "debug_block_dots: negative size");
+    if (row_size(wt, k) < 0) return fail(GGUF_ERR_SHAPE, "debug_block_dots: k not a multiple of the block");
+    if (n == 0 || m == 0 || k == 0) return GGUF_OK;
+    if (!w || !xq || !sums) return fail(GGUF_ERR_INVALID_ARG, "debug_block_dots: null pointer");
+    return cuda_status(launch_block_dots((const uint8_t *)w, wt, n, k, (const uint8_t *)xq, m, sums, (cudaStream_t)stream),
+                       "debug_block_dots");
+}
+
+gguf_status gguf_set_option(const char *key, int64_t value) {
+    if (!key) return fail(GGUF_ERR_INVALID_ARG, "set_option: null key");
+    if (!strcmp(key, "mmvq_max_m")) {
+        if (value < 0) return fail(GGUF_ERR_INVALID_ARG, "set_option: mmvq_max_m must be >= 0");
+        g_mmvq_max_m = value;
+        return GGUF_OK;
+    }
+    if (!strcmp(key, "mmq_enable")) {
+        g_mmq_enable = value != 0;
+        return GGUF_OK;
+    }
+    return fail(GGUF_ERR_INVALID_ARG, "set_option: unknown key '%s'", key);
+}
+
+int64_t gguf_get_option(const char *key) {
+    if (!key) return -1;
+    if (!strcmp(key, "mmvq_max_m")) return g_mmvq_max_m;
+    if (!strcmp(key, "mmq_enable")) return g_mmq_enable;
+    return -1;
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// Device helpers shared by the CUDA kernels of libgguf_gb300 (sm_103a only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gguf_gb300.h"
+
+namespace gg {
+
+// block geometry (public GGUF convention)
+constexpr int QK8 = 32;            // values per Q8_0 / q8_1 block
+constexpr int QKK = 256;           // values per K-quant super-block
+constexpr int Q8_0_BYTES = 34;     // fp16 d, int8 q[32]
+constexpr int Q8_1_BYTES = 36;     // fp16 d, fp16 s, int8 q[32]
+constexpr int Q4_K_BYTES = 144;    // fp16 d, fp16 dmin, scales[12], qs[128]
+constexpr int Q6_K_BYTES = 210;    // ql[128], qh[64], scales[16], fp16 d
+
+__device__ __forceinline__ float h2f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+__device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
+
+__device__ __forceinline__ uint16_t f2h_rn(float f) { return __half_as_ushort(__float2half_rn(f)); }
+__device__ __forceinline__ uint16_t f2bf_rn(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+
+// store one fp32 value as F32 / BF16 / F16 (round to nearest even)
+__device__ __forceinline__ void store_out(void *out, int ot, int64_t idx, float v) {
+    if (ot == GGUF_F32) reinterpret_cast<float *>(out)[idx] = v;
+    else if (ot == GGUF_BF16) reinterpret_cast<uint16_t *>(out)[idx] = f2bf_rn(v);
+    else reinterpret_cast<uint16_t *>(out)[idx] = f2h_rn(v);
+}
+
+// signed x signed 4-way byte dot product with accumulate
+__device__ __forceinline__ int dp4a_ss(int a, int b, int c) { return __dp4a(a, b, c); }
+// unsigned (a) x signed (b) 4-way byte dot product with accumulate
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t ld_u32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
+__device__ __forceinline__ uint16_t ld_u16(const uint8_t *p) { return *reinterpret_cast<const uint16_t *>(p); }
+
+// Read 8 bytes at a 2-byte-aligned address as two words, touching only bytes
+// in [p - 2, p + 10): aligned words plus a funnel shift when p % 4 == 2.
+__device__ __forceinline__ void ld8_a2(const uint8_t *p, uint32_t &lo, uint32_t &hi) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint8_t *base = reinterpret_cast<const uint8_t *>(a & ~uintptr_t(3));
+    uint32_t w0 = ld_u32(base), w1 = ld_u32(base + 4);
+    if (a & 2) {
+        uint32_t w2 = ld_u32(base + 8);
+        lo = __funnelshift_r(w0, w1, 16);
+        hi = __funnelshift_r(w1, w2, 16);
+    } else {
+        lo = w0;
+        hi = w1;
+    }
+}
+
+// 6-bit (scale, min) of Q4_K sub-block j from the 12 scale bytes held in three
+// little-endian words sc[0..2] (bytes 0..11).
+__device__ __forceinline__ int sc_byte(const uint32_t sc[3], int i) { return (sc[i >> 2] >> (8 * (i & 3))) & 0xff; }
+__device__ __forceinline__ void q4k_scale_min(const uint32_t sc[3], int j, int &s, int &m) {
+    if (j < 4) {
+        s = sc_byte(sc, j) & 63;
+        m = sc_byte(sc, j + 4) & 63;
+    } else {
+        s = (sc_byte(sc, j + 4) & 15) | ((sc_byte(sc, j - 4) >> 6) << 4);
+        m = (sc_byte(sc, j + 4) >> 4) | ((sc_byte(sc, j) >> 6) << 4);
+    }
+}
+
+__host__ __device__ constexpr int64_t block_elems(int t) {
+    return (t == GGUF_Q8_0 || t == GGUF_Q8_1) ? 32 : (t == GGUF_Q4_K || t == GGUF_Q6_K) ? 256
+         : (t == GGUF_F32 || t == GGUF_F16 || t == GGUF_BF16) ? 1 : 0;
+}
+__host__ __device__ constexpr int64_t block_bytes(int t) {
+    return t == GGUF_Q8_0 ? 34 : t == GGUF_Q8_1 ? 36 : t == GGUF_Q4_K ? 144 : t == GGUF_Q6_K ? 210
+         : t == GGUF_F32 ? 4 : (t == GGUF_F16 || t == GGUF_BF16) ? 2 : 0;
+}
+
+}  // namespace gg

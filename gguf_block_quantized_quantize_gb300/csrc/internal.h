@@ -1,0 +1,60 @@
+// Host-side launch interface between the C-ABI layer (abi.cu) and the kernel
+// translation units.  Every launcher returns the cudaError_t of its launch and
+// assumes its arguments were validated by abi.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gg {
+
+struct DeviceInfo {
+    int sm_count;
+    int cc_major, cc_minor;
+    size_t smem_optin;
+};
+const DeviceInfo &device_info();
+
+// q8_1 quantization; also writes the fp16 tensor-core operand xh[m][k] (d16*q)
+// when xh != nullptr.
+cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int64_t ldx, uint8_t *xq,
+                                 uint16_t *xh, cudaStream_t s);
+// fp16 operand xh[m][k] from q8_1 rows (d16*q rounded to fp16).
+cudaError_t launch_q8_1_to_f16(const uint8_t *xq, int64_t m, int64_t k, uint16_t *xh, cudaStream_t s);
+
+cudaError_t launch_dequantize(const uint8_t *w, int wt, int64_t rows, int64_t k, const int32_t *ids,
+                              int64_t table_rows, void *out, int ot, cudaStream_t s);
+cudaError_t launch_convert_float(const void *x, int xt, int64_t count, void *out, int ot, cudaStream_t s);
+cudaError_t launch_block_dots(const uint8_t *w, int wt, int64_t n, int64_t k, const uint8_t *xq, int64_t m,
+                              int32_t *sums, cudaStream_t s);
+
+// y[m][ldy] (yt) = W[n][k] (wt) . q8_1 rows xq[m] ; m <= 8
+cudaError_t launch_mmvq(const uint8_t *w, int wt, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y,
+                        int yt, int64_t ldy, cudaStream_t s);
+
+// tensor-core MMQ: y[m][ldy] = W[n][k] . xh[m][k] (fp16 operand rows)
+cudaError_t launch_mmq(const uint8_t *w, int wt, int64_t n, int64_t k, const uint16_t *xh, int64_t m, void *y,
+                       int yt, int64_t ldy, cudaStream_t s);
+
+// ---- MoE (moe.cu)
+struct MoeWs {
+    int32_t *counts, *offsets, *pos, *route_list, *tile_expert, *tile_start, *n_tiles;
+    uint16_t *xh;
+    float *yacc;
+    uint16_t *h16;
+    size_t bytes;
+};
+// base == nullptr computes only the size
+MoeWs moe_ws_layout(void *base, int64_t E, int64_t R, int64_t xh_elems, int64_t yacc_elems, int64_t h16_elems);
+int moe_bn(int64_t routes, int64_t experts);
+cudaError_t moe_group(const int32_t *ids, const float *rw, int64_t R, int64_t E, bool skip_zero_w, int32_t *status,
+                      const MoeWs &w, int bn, cudaStream_t s);
+cudaError_t launch_moe_gate_up(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
+                               const uint16_t *xh, int64_t top_k, int64_t R, int64_t E, const MoeWs &ws,
+                               uint8_t *hq, uint16_t *hbf, uint16_t *h16, cudaStream_t s);
+cudaError_t launch_moe_down(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
+                            const uint16_t *xh, int64_t top_k, int64_t R, int64_t E, const float *route_w,
+                            const MoeWs &ws, float *yacc, cudaStream_t s);
+cudaError_t launch_moe_finalize(const float *yacc, int64_t count, void *y, int yt, cudaStream_t s);
+
+}  // namespace gg

@@ -1,0 +1,145 @@
+// q8_1 activation quantization (FreeToken PR #690 "serve GGUF checkpoints on
+// vendored ggml-cuda kernels", section "Vendored ggml": fp32 / bf16 / fp16
+// activations go straight to q8_1).
+//
+// One thread handles 8 consecutive values, four threads one block of 32:
+//   d = amax / 127 (IEEE division), q = roundf(x / d) (ties away from zero),
+//   s = fp16(d * sum(q)) with the fp32 d, and d is stored as fp16(d).
+// The kernel is HBM-bound: 2 or 4 bytes read and 1.125 bytes written per value.
+#include "common.cuh"
+#include "internal.h"
+
+namespace gg {
+
+template <int XT, bool VEC>
+__device__ __forceinline__ void load8(const void *x, int64_t off, float v[8]) {
+    if (XT == GGUF_F32) {
+        const float *p = reinterpret_cast<const float *>(x) + off;
+        if (VEC) {
+            float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; i++) v[i] = p[i];
+        }
+    } else {
+        const uint16_t *p = reinterpret_cast<const uint16_t *>(x) + off;
+        uint16_t h[8];
+        if (VEC) {
+            uint4 a = *reinterpret_cast<const uint4 *>(p);
+            uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int i = 0; i < 4; i++) { h[2 * i] = w[i] & 0xffff; h[2 * i + 1] = w[i] >> 16; }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; i++) h[i] = p[i];
+        }
+#pragma unroll
+        for (int i = 0; i < 8; i++) v[i] = (XT == GGUF_BF16) ? bf2f(h[i]) : h2f(h[i]);
+    }
+}
+
+template <int XT, bool VEC>
+__global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restrict__ x, int64_t m, int64_t k,
+                                                            int64_t ldx, uint8_t *__restrict__ xq,
+                                                            uint16_t *__restrict__ xh) {
+    const int64_t nb = k / QK8;
+    const int64_t total = m * nb;
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t blk = g >> 2;
+    const int j = (int)(g & 3);
+    const bool active = blk < total;
+    const int64_t row = active ? blk / nb : 0;
+    const int64_t b = active ? blk - row * nb : 0;
+
+    float v[8];
+    if (active) load8<XT, VEC>(x, row * ldx + b * QK8 + 8 * j, v);
+    else {
+#pragma unroll
+        for (int i = 0; i < 8; i++) v[i] = 0.0f;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float d = __fdiv_rn(amax, 127.0f);
+
+    int q[8];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        q[i] = (d != 0.0f) ? (int)roundf(__fdiv_rn(v[i], d)) : 0;
+        sum += q[i];
+    }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    if (!active) return;
+
+    const uint16_t dh = f2h_rn(d);
+    if (xq != nullptr) {
+        uint8_t *o = xq + blk * Q8_1_BYTES;
+        uint32_t w0 = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) | ((uint32_t)(q[3] & 0xff) << 24);
+        uint32_t w1 = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) | ((uint32_t)(q[7] & 0xff) << 24);
+        reinterpret_cast<uint32_t *>(o + 4 + 8 * j)[0] = w0;
+        reinterpret_cast<uint32_t *>(o + 4 + 8 * j)[1] = w1;
+        if (j == 0) {
+            const uint16_t sh = f2h_rn(__fmul_rn(d, (float)sum));
+            *reinterpret_cast<uint32_t *>(o) = (uint32_t)dh | ((uint32_t)sh << 16);
+        }
+    }
+    if (xh != nullptr) {
+        // fp16 tensor-core operand: the dequantized q8_1 value d16 * q, rounded once
+        const float d16 = h2f(dh);
+        uint32_t hw[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            hw[i] = (uint32_t)f2h_rn(d16 * (float)q[2 * i]) | ((uint32_t)f2h_rn(d16 * (float)q[2 * i + 1]) << 16);
+        *reinterpret_cast<uint4 *>(xh + row * k + b * QK8 + 8 * j) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    }
+}
+
+__global__ void __launch_bounds__(256) q8_1_to_f16_kernel(const uint8_t *__restrict__ xq, int64_t m, int64_t k,
+                                                          uint16_t *__restrict__ xh) {
+    const int64_t nb = k / QK8;
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t blk = g >> 2;
+    const int j = (int)(g & 3);
+    if (blk >= m * nb) return;
+    const uint8_t *p = xq + blk * Q8_1_BYTES;
+    const float d16 = h2f(ld_u16(p));
+    const uint32_t w0 = ld_u32(p + 4 + 8 * j), w1 = ld_u32(p + 8 + 8 * j);
+    int8_t q[8];
+#pragma unroll
+    for (int i = 0; i < 4; i++) { q[i] = (int8_t)(w0 >> (8 * i)); q[4 + i] = (int8_t)(w1 >> (8 * i)); }
+    uint32_t hw[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        hw[i] = (uint32_t)f2h_rn(d16 * (float)q[2 * i]) | ((uint32_t)f2h_rn(d16 * (float)q[2 * i + 1]) << 16);
+    const int64_t row = blk / nb, b = blk - row * nb;
+    *reinterpret_cast<uint4 *>(xh + row * k + b * QK8 + 8 * j) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+}
+
+cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int64_t ldx, uint8_t *xq,
+                                 uint16_t *xh, cudaStream_t s) {
+    const int64_t threads = m * (k / QK8) * 4;
+    if (threads == 0) return cudaSuccess;
+    const int64_t grid = (threads + 255) / 256;
+    const int esz = xt == GGUF_F32 ? 4 : 2;
+    const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && ((ldx * esz) % 16 == 0);
+#define QLAUNCH(XT, V) quantize_q8_1_kernel<XT, V><<<(unsigned)grid, 256, 0, s>>>(x, m, k, ldx, xq, xh)
+    if (xt == GGUF_F32) { if (vec) QLAUNCH(GGUF_F32, true); else QLAUNCH(GGUF_F32, false); }
+    else if (xt == GGUF_BF16) { if (vec) QLAUNCH(GGUF_BF16, true); else QLAUNCH(GGUF_BF16, false); }
+    else { if (vec) QLAUNCH(GGUF_F16, true); else QLAUNCH(GGUF_F16, false); }
+#undef QLAUNCH
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q8_1_to_f16(const uint8_t *xq, int64_t m, int64_t k, uint16_t *xh, cudaStream_t s) {
+    const int64_t threads = m * (k / QK8) * 4;
+    if (threads == 0) return cudaSuccess;
+    q8_1_to_f16_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(xq, m, k, xh);
+    return cudaGetLastError();
+}
+
+}  // namespace gg

@@ -1,0 +1,271 @@
+/*
+ * gguf_gb300.h -- C ABI of the GB300 (sm_103a) GGUF block-quantized matmul
+ * library (libgguf_gb300.so).
+ *
+ * The library computes the hot path of a GGUF serving engine: activations in
+ * fp32 / bf16 / fp16 are quantized to q8_1 blocks of 32 and multiplied against
+ * Q8_0 / Q4_K / Q6_K weight blocks with per-block integer dot products and an
+ * fp32 scale / min combination; results come back in the activation dtype
+ * with fp32 accumulation (FreeToken PR #690 "serve GGUF checkpoints on
+ * vendored ggml-cuda kernels", section "Vendored ggml", list "What the ggml
+ * patch changes").  The entry points are that page's op list: mul_mat,
+ * mul_mat_id with the fused GLU and the MoE weighted sum, get_rows and
+ * dequantize (same section, paragraph "Our own code next to it").
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named w, x, xq, y, out, table, ids, ws are DEVICE pointers of
+ *     the current CUDA device, owned by the caller.  The library allocates no
+ *     device memory per call; scratch comes from the caller's workspace `ws`,
+ *     sized by the matching *_ws_size query.
+ *   - Every call is asynchronous and ordered on `stream` (a cudaStream_t;
+ *     NULL is the legacy default stream).  No call synchronizes the host; in
+ *     particular mul_mat_id groups its routes on the device and launches work
+ *     only for the (expert, tile) pairs that have routes, without the host
+ *     learning the counts (FreeToken PR #690, section "Vendored ggml").
+ *   - Argument errors are reported synchronously as a status code; the
+ *     library never aborts the process and never faults on bad arguments; the
+ *     prior art turned such faults into errors (FreeToken issue #671 "MoE cache,
+ *     CPU experts and GGUF support", section "Known issues").  gguf_last_error() returns a
+ *     thread-local message for the last non-OK status.  CUDA launch errors
+ *     come back as GGUF_ERR_CUDA.
+ *   - Weight buffers must start on a 16-byte boundary.  Rows are packed back
+ *     to back ([rows][row_size] bytes).  K must be a multiple of the type's
+ *     block (32 for Q8_0 / q8_1, 256 for Q4_K / Q6_K: K-quant super-blocks span
+ *     256 values, 1Cat-vLLM "GGUF on V100: implementation and acceptance control",
+ *     section "TP/EP decision").  Offsets are 64-bit: no 2^31-block limit
+ *     (FreeToken issue #671, "Known issues").  No kernel reads past the last
+ *     byte of a weight view, so no tail padding is needed (unlike the MMQ tail
+ *     read described in FreeToken PR #690, comment "GGUF experts in the offload
+ *     slot cache have no MMQ tail padding").
+ *
+ * Block layouts (public GGUF convention; the pages name the formats but do not
+ * print their bytes):
+ *   Q8_0  34 B / 32 values : fp16 d, int8 q[32]                 v = d*q
+ *   q8_1  36 B / 32 values : fp16 d, fp16 s = d*sum(q), int8 q[32]
+ *   Q4_K 144 B / 256 values: fp16 d, fp16 dmin, 12 B of 6-bit (scale, min)
+ *                            for 8 sub-blocks of 32, 128 B of 4-bit quants
+ *                            v = d*scale_j*q - dmin*min_j
+ *   Q6_K 210 B / 256 values: 128 B low 4 bits, 64 B high 2 bits, 16 int8
+ *                            scales (sub-blocks of 16), fp16 d
+ *                            v = d*scale_j*(q - 32)
+ */
+#ifndef GGUF_GB300_H
+#define GGUF_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *gguf_stream_t; /* a cudaStream_t */
+
+/* ggml type numbering (public GGUF convention). */
+typedef enum {
+    GGUF_F32 = 0,
+    GGUF_F16 = 1,
+    GGUF_Q8_0 = 8,
+    GGUF_Q8_1 = 9,
+    GGUF_Q4_K = 12,
+    GGUF_Q6_K = 14,
+    GGUF_BF16 = 30
+} gguf_type;
+
+typedef enum {
+    GGUF_OK = 0,
+    GGUF_ERR_INVALID_ARG = 1,      /* null pointer, negative size, bad mode/stride */
+    GGUF_ERR_UNSUPPORTED_TYPE = 2, /* type not handled by this entry point */
+    GGUF_ERR_SHAPE = 3,            /* K not a multiple of the block, or sizes inconsistent */
+    GGUF_ERR_ALIGNMENT = 4,        /* a buffer or stride breaks the alignment rule */
+    GGUF_ERR_WORKSPACE = 5,        /* ws smaller than the *_ws_size query */
+    GGUF_ERR_CUDA = 6              /* a CUDA runtime / launch error; see gguf_last_error() */
+} gguf_status;
+
+/* Thread-local message describing the last non-OK status of this thread. */
+const char *gguf_last_error(void);
+
+/* Values per block (1 for float types, 0 for unknown types). */
+int64_t gguf_type_block_elems(int type);
+/* Bytes per block (element size for float types, 0 for unknown types). */
+int64_t gguf_type_block_bytes(int type);
+/* Bytes of one row of k values ("ggml_row_size", FreeToken PR #690, comment on
+ * MMQ tail padding); -1 if k is not a multiple of the block. */
+int64_t gguf_row_size(int type, int64_t k);
+
+/*
+ * gguf_quantize_q8_1 -- activations to q8_1 (FreeToken PR #690, section
+ * "Vendored ggml": fp32 / bf16 / fp16 activations go straight to q8_1).
+ *   x   : [m][ldx] values of type xt (GGUF_F32, GGUF_BF16 or GGUF_F16); only
+ *         the first k of each row are read.  ldx >= k.
+ *   xq  : [m][k/32] q8_1 blocks (m * gguf_row_size(GGUF_Q8_1, k) bytes).
+ * Per block of 32: d = amax/127 (IEEE fp32 division), q = roundf(x/d) (ties
+ * away from zero; 0 when d == 0), s = fp16(d * sum(q)) with the fp32 d, and d
+ * stored as fp16(d).  Bit-exact and deterministic.  |x| must stay below
+ * 65504 * 127 so that d fits in fp16; NaN / Inf inputs give unspecified
+ * blocks (no fault).  Requires k % 32 == 0.
+ */
+gguf_status gguf_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int64_t ldx, void *xq,
+                               gguf_stream_t stream);
+
+/*
+ * gguf_dequantize -- packed weights to float (FreeToken PR #690, op
+ * "dequantize"; same-type float inputs are copied, types without a converter
+ * are rejected: same page, summary of the later commits under "Validation").
+ *   w   : [rows][row_size(wt, k)] bytes, wt in {Q8_0, Q4_K, Q6_K, Q8_1, F32, F16, BF16}
+ *   out : [rows][k] of type ot in {F32, F16, BF16}
+ * Values are computed in fp32 in the order  Q4_K: a = d*s; b = dmin*m; a*q - b;
+ * Q6_K: (d*sc)*(q-32);  Q8_0 / q8_1: d*q;  then rounded to ot with
+ * round-to-nearest-even.  Bit-exact.  Float-to-float calls convert (RNE).
+ */
+gguf_status gguf_dequantize(const void *w, int wt, int64_t rows, int64_t k, void *out, int ot,
+                            gguf_stream_t stream);
+
+/*
+ * gguf_get_rows -- out[i][:] = dequantize(table[ids[i]][:]) (FreeToken PR #690,
+ * op "get_rows", used for the token embedding and the PLE table).
+ *   table : [rows][row_size(tt, k)] bytes; ids : [n_ids] int32 device array;
+ *   out   : [n_ids][k] of type ot (F32, F16, BF16).
+ * An id outside [0, rows) yields a zero row (never an out-of-bounds read).
+ */
+gguf_status gguf_get_rows(const void *table, int tt, int64_t rows, int64_t k, const int32_t *ids, int64_t n_ids,
+                          void *out, int ot, gguf_stream_t stream);
+
+/*
+ * gguf_mul_mat -- y[m][n] = sum_k W[n][k] * X[m][k] for a packed weight W
+ * [n][k] (wt in {Q8_0, Q4_K, Q6_K}) and activations X [m][k].
+ *   x  : [m][ldx] of type xt in {F32, BF16, F16} (quantized to q8_1 inside,
+ *        into ws), or xt = GGUF_Q8_1: pre-quantized rows of row_size(Q8_1,k)
+ *        bytes (ldx is then ignored) -- the way one q8_1 quantization serves
+ *        several weight segments (FreeToken PR #690, section "Vendored ggml").
+ *   y  : [m][ldy] of type yt in {F32, BF16, F16}; columns [0, n) of each row
+ *        are written, so segments of a fused Linear can write column slices.
+ *   ws : device workspace of at least gguf_mul_mat_ws_size(...) bytes
+ *        (may be NULL when that size is 0).
+ * Path: small m (<= option "mmvq_max_m", default 8) runs the bandwidth-bound
+ * MMVQ kernel (per-block int8 dot products, exact int32 block sums, fp32
+ * combination); larger m runs the tensor-core MMQ kernel.  Accuracy: MMVQ is
+ * within 1e-6 relative of the fp64 blockwise formula; MMQ feeds the tcgen05
+ * tensor cores fp16 operands (dequantized weight and q8_1 values) with fp32
+ * accumulation, within 3e-3 relative to the row rms.
+ */
+size_t gguf_mul_mat_ws_size(int wt, int64_t n, int64_t k, int xt, int64_t m);
+gguf_status gguf_mul_mat(const void *w, int wt, int64_t n, int64_t k, const void *x, int xt, int64_t m,
+                         int64_t ldx, void *y, int yt, int64_t ldy, void *ws, size_t ws_bytes, gguf_stream_t stream);
+
+/* mul_mat_id modes */
+#define GGUF_MOE_GATE_UP_SWIGLU 0   /* h[r] = silu(gate) * up, rounded to bf16, out as BF16 or Q8_1 */
+#define GGUF_MOE_DOWN_WEIGHTED_SUM 1 /* y[t] = sum_k route_w[t][k] * (W[e] . x[route]) */
+
+/*
+ * Arguments of gguf_mul_mat_id (MoE experts).
+ *   w, wt           : expert bank base; expert e's packed [n][k] matrix starts at
+ *                     w + e * expert_stride bytes (a flat [n_experts, stride]
+ *                     bank as in FreeToken PR #196's bank geometry discussion);
+ *                     expert_stride >= n * row_size and a multiple of 16.
+ *   n, k            : rows and columns of one expert matrix.  GATE_UP: n = 2*I,
+ *                     gate rows [0, I) first, then up rows [I, 2I) (the merged
+ *                     gate_up layout of transformers PR #45977 "GgufExperts").
+ *   x, xt, ldx      : GATE_UP: token rows [n_tokens][ldx] (F32 / BF16 / F16) or
+ *                     q8_1 rows [n_tokens][row_size(Q8_1, k)];
+ *                     DOWN: route rows [n_tokens * top_k][ldx] (BF16) or q8_1
+ *                     rows [n_tokens * top_k][row_size(Q8_1, k)], route
+ *                     r = t * top_k + j.
+ *   ids             : [n_tokens][top_k] int32 expert ids; id < 0 or >= n_experts
+ *                     marks an inactive route (skipped, never read), and a token
+ *                     may name the same expert more than once (FreeToken issue
+ *                     #671, "Known issues").
+ *   route_w         : [n_tokens][top_k] fp32 weights (DOWN; NULL means 1.0).
+ *                     A route whose weight is 0 is skipped.
+ *   y, yt           : GATE_UP: [n_tokens * top_k][n/2] of yt = BF16, Q8_1 (q8_1
+ *                     rows of row_size(Q8_1, n/2) bytes) or F16 (the dequantized
+ *                     q8_1 values d16*q, the form the down GEMM consumes);
+ *                     inactive routes get zero rows.  n must be a multiple of 128.
+ *                     DOWN: [n_tokens][n] of yt = F32, BF16 or F16.
+ *   workspace       : 256-byte aligned, gguf_mul_mat_id_ws_size(args) bytes.
+ *   dev_status      : optional device int32; the count of ids >= n_experts is
+ *                     added to it (never a trap, never a host sync).
+ * The intermediate h is kept in the activation dtype (bf16) and then quantized
+ * to q8_1 (FreeToken PR #690, section "Changes": the intermediates stay in the
+ * activation dtype).
+ */
+typedef struct {
+    const void *w;
+    int wt;
+    int64_t n_experts;
+    int64_t expert_stride;
+    int64_t n;
+    int64_t k;
+    const void *x;
+    int xt;
+    int64_t n_tokens;
+    int64_t ldx;
+    const int32_t *ids;
+    int64_t top_k;
+    const float *route_w;
+    int mode;
+    void *y;
+    int yt;
+    int32_t *dev_status;
+} gguf_moe_args;
+
+size_t gguf_mul_mat_id_ws_size(const gguf_moe_args *args);
+gguf_status gguf_mul_mat_id(const gguf_moe_args *args, void *ws, size_t ws_bytes, gguf_stream_t stream);
+
+/*
+ * gguf_moe_ffn -- the whole MoE expert block in one call: q8_1 quantization of
+ * the token rows, gate_up mul_mat_id with the fused SwiGLU (h kept in bf16,
+ * then quantized to q8_1), and the down mul_mat_id with the fused
+ * expert-weighted sum.  One device-side route grouping serves both GEMMs and
+ * the intermediate stays in the workspace.  Same conventions as
+ * gguf_mul_mat_id; banks hold [2*inter][hidden] (gate rows, then up rows) and
+ * [hidden][inter] matrices per expert.  y : [n_tokens][hidden] of yt (F32, BF16
+ * or F16).  Routes with weight 0 are skipped by both GEMMs.
+ */
+typedef struct {
+    const void *w_gate_up;
+    int gate_up_type;
+    int64_t gate_up_stride;
+    const void *w_down;
+    int down_type;
+    int64_t down_stride;
+    int64_t n_experts;
+    int64_t hidden;
+    int64_t inter;
+    const void *x;
+    int xt;
+    int64_t n_tokens;
+    int64_t ldx;
+    const int32_t *ids;
+    int64_t top_k;
+    const float *route_w;
+    void *y;
+    int yt;
+    int32_t *dev_status;
+} gguf_moe_ffn_args;
+
+size_t gguf_moe_ffn_ws_size(const gguf_moe_ffn_args *args);
+gguf_status gguf_moe_ffn(const gguf_moe_ffn_args *args, void *ws, size_t ws_bytes, gguf_stream_t stream);
+
+/*
+ * gguf_debug_block_dots -- test hook: the exact int32 dot product of every
+ * weight sub-block (32 values for Q8_0 / Q4_K, 16 for Q6_K) with the matching
+ * q8_1 activation quants.  sums : [m][n][k / sub] int32.  Bit-exact.
+ */
+gguf_status gguf_debug_block_dots(const void *w, int wt, int64_t n, int64_t k, const void *xq, int64_t m,
+                                  int32_t *sums, gguf_stream_t stream);
+
+/*
+ * Tunables (host-global, not thread-safe against concurrent calls):
+ *   "mmvq_max_m"  : largest m routed to MMVQ (default 8; FreeToken issue #671,
+ *                   "Known issues": MMQ takes over above 8 tokens).
+ *   "mmq_enable"  : 0 routes every m through MMVQ (default 1).
+ * Returns GGUF_ERR_INVALID_ARG for an unknown key.
+ */
+gguf_status gguf_set_option(const char *key, int64_t value);
+int64_t gguf_get_option(const char *key);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GGUF_GB300_H */

@@ -1,0 +1,95 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point that include/gguf_gb300.h declares, and rejects bad
+arguments with the documented status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gguf_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def g():
+    from gguf_block_quantized_quantize_gb300 import build
+
+    build.build()
+    import gguf_block_quantized_quantize_gb300 as g
+
+    g.load_library()
+    return g
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gguf_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(g):
+    names = _declared()
+    assert "gguf_mul_mat" in names and "gguf_mul_mat_id" in names and "gguf_quantize_q8_1" in names
+    lib = ctypes.CDLL(g.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in g.SIGNATURES, f"binding lacks {n}"
+
+
+def test_type_table(g):
+    L = g.load_library()
+    assert L.gguf_type_block_elems(g.Q4_K) == 256 and L.gguf_type_block_bytes(g.Q4_K) == 144
+    assert L.gguf_type_block_elems(g.Q6_K) == 256 and L.gguf_type_block_bytes(g.Q6_K) == 210
+    assert L.gguf_type_block_elems(g.Q8_0) == 32 and L.gguf_type_block_bytes(g.Q8_0) == 34
+    assert L.gguf_type_block_elems(g.Q8_1) == 32 and L.gguf_type_block_bytes(g.Q8_1) == 36
+    assert g.gguf_row_size(g.Q4_K, 4096) == 2304 and g.gguf_row_size(g.Q6_K, 3072) == 2520
+    assert g.gguf_row_size(g.Q4_K, 100) == -1 and L.gguf_type_block_bytes(99) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)    # never dereferenced: validation fails first
+
+
+def _mm(g, **kw):
+    a = dict(w=FAKE, wt=g.Q4_K, n=16, k=256, x=FAKE, xt=g.F32, m=4, ldx=256, y=FAKE, yt=g.F32, ldy=16,
+             ws=FAKE, ws_bytes=1 << 20)
+    a.update(kw)
+    L = g.load_library()
+    return L.gguf_mul_mat(a["w"], a["wt"], a["n"], a["k"], a["x"], a["xt"], a["m"], a["ldx"], a["y"], a["yt"],
+                          a["ldy"], a["ws"], a["ws_bytes"], None)
+
+
+def test_mul_mat_rejects_bad_arguments(g):
+    assert _mm(g, wt=2) == 2                       # Q4_0: unsupported type
+    assert _mm(g, xt=g.Q6_K) == 2
+    assert _mm(g, yt=g.Q8_0) == 2
+    assert _mm(g, k=100) == 3                      # not a multiple of 256
+    assert _mm(g, n=-1) == 1
+    assert _mm(g, ldy=8) == 1
+    assert _mm(g, ldx=128) == 1
+    assert _mm(g, w=None) == 1
+    assert _mm(g, w=ctypes.c_void_p(0x10008)) == 4  # weight base not 16-byte aligned
+    assert _mm(g, ws=None, ws_bytes=0) == 5         # float x needs a q8_1 workspace
+    assert _mm(g, ws_bytes=16) == 5
+    assert "workspace" in g.load_library().gguf_last_error().decode()
+    assert _mm(g, m=0) == 0 and _mm(g, n=0) == 0     # empty products are no-ops
+
+
+def test_workspace_sizes(g):
+    assert g.gguf_mul_mat_ws_size(g.Q4_K, 4096, 4096, g.Q8_1, 8) == 0
+    assert g.gguf_mul_mat_ws_size(g.Q4_K, 4096, 4096, g.BF16, 8) >= 8 * 4096 // 32 * 36
+    assert g.gguf_mul_mat_ws_size(g.Q4_K, 4096, 4096, g.BF16, 64) >= 64 * 4096 * 2
+
+
+def test_other_entry_points_reject_bad_arguments(g):
+    L = g.load_library()
+    assert L.gguf_quantize_q8_1(FAKE, g.Q8_0, 4, 64, 64, FAKE, None) == 2
+    assert L.gguf_quantize_q8_1(FAKE, g.F32, 4, 40, 40, FAKE, None) == 3
+    assert L.gguf_quantize_q8_1(FAKE, g.F32, 4, 64, 32, FAKE, None) == 1
+    assert L.gguf_dequantize(FAKE, 2, 4, 64, FAKE, g.F32, None) == 2
+    assert L.gguf_dequantize(FAKE, g.Q6_K, 4, 300, FAKE, g.F32, None) == 3
+    assert L.gguf_dequantize(FAKE, g.Q6_K, 4, 256, FAKE, g.Q8_0, None) == 2
+    assert L.gguf_get_rows(FAKE, g.Q6_K, 4, 256, None, 3, FAKE, g.F32, None) == 1
+    assert L.gguf_debug_block_dots(FAKE, g.F32, 4, 256, FAKE, 1, FAKE, None) == 2
+    assert L.gguf_set_option(b"no_such_key", 1) == 1
+    assert L.gguf_set_option(b"mmvq_max_m", 8) == 0 and L.gguf_get_option(b"mmvq_max_m") == 8

@@ -1,0 +1,125 @@
+"""GPU parity of the tensor-core MMQ path (m above the MMVQ threshold).
+
+MMQ feeds tcgen05 fp16 operands that hold the dequantized weight and q8_1
+values (each rounded once from the exact fp32 value of the blockwise
+formula), accumulating over K in fp32.  bf16 outputs are held to the 1e-2
+bound; fp32 outputs to 3e-3 of max(|r|, row rms): two fp16 roundings of
+relative size <= 2^-11 per product give an error of ~3e-4 of the row rms per
+output (standard deviation), and the bound leaves room for the tail of a few
+million outputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _util import TOL_BF16, assert_close
+from gguf_block_quantized_quantize_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL_MMQ_F32 = 3e-3
+
+
+@pytest.fixture(scope="module")
+def g():
+    from gguf_block_quantized_quantize_gb300 import build
+
+    build.build()
+    import gguf_block_quantized_quantize_gb300 as g
+
+    g.load_library()
+    return g
+
+
+def _u8(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _weights(wt, n, k, seed, safe=False):
+    if safe:
+        return synth.safe_blocks(wt, n, k, seed)
+    return oracle.quantize_weights(wt, synth.normal((n, k), 0.02, seed))
+
+
+@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0])
+@pytest.mark.parametrize("m", [9, 16, 17, 32, 64, 100, 128, 256, 300])
+def test_mmq_bf16_shapes(g, wt, m):
+    n, k = 300, 1024 if wt != oracle.Q8_0 else 1056     # ragged n; Q8_0 k % 64 == 32
+    w = _weights(wt, n, k, seed=m, safe=(m % 2 == 1))
+    x = synth.activations(m, k, seed=m + 1, dtype=torch.bfloat16)
+    ref = oracle.mul_mat(wt, w, k, oracle.quantize_q8_1(x.float().numpy()))
+    y = g.gguf_mul_mat(_u8(w), wt, n, k, x.to(DEV))
+    assert y.dtype == torch.bfloat16
+    assert_close(y.float().cpu().numpy(), ref, TOL_BF16, f"mmq type {wt} m {m}")
+
+
+@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K])
+def test_mmq_fp32_output(g, wt):
+    n, m, k = 257, 200, 2048
+    w = _weights(wt, n, k, seed=3)
+    x = synth.activations(m, k, seed=4, dtype=torch.float32)
+    ref = oracle.mul_mat(wt, w, k, oracle.quantize_q8_1(x.numpy()))
+    y = g.gguf_mul_mat(_u8(w), wt, n, k, x.to(DEV))
+    assert_close(y.cpu().numpy(), ref, TOL_MMQ_F32, f"mmq fp32 type {wt}")
+
+
+def test_mmq_prequantized_and_column_slices(g):
+    k, m = 2048, 96
+    x = synth.activations(m, k, seed=7, dtype=torch.bfloat16)
+    xq = g.gguf_quantize_q8_1(x.to(DEV))
+    xq_ref = oracle.quantize_q8_1(x.float().numpy())
+    out = torch.zeros(m, 512 + 256, dtype=torch.bfloat16, device=DEV)
+    w1, w2 = _weights(oracle.Q4_K, 512, k, 8), _weights(oracle.Q6_K, 256, k, 9)
+    g.gguf_mul_mat(_u8(w1), oracle.Q4_K, 512, k, xq, xt=oracle.Q8_1, m=m, out=out[:, :512])
+    g.gguf_mul_mat(_u8(w2), oracle.Q6_K, 256, k, xq, xt=oracle.Q8_1, m=m, out=out[:, 512:])
+    ref = np.concatenate([oracle.mul_mat(oracle.Q4_K, w1, k, xq_ref), oracle.mul_mat(oracle.Q6_K, w2, k, xq_ref)], 1)
+    assert_close(out.float().cpu().numpy(), ref, TOL_BF16, "mmq segments")
+
+
+def test_mmq_threshold_option(g):
+    """m = 8 runs MMVQ by default; with mmvq_max_m = 4 it runs MMQ; both agree."""
+    n, k, m = 256, 512, 8
+    w = _weights(oracle.Q4_K, n, k, 10)
+    x = synth.activations(m, k, seed=11, dtype=torch.bfloat16).to(DEV)
+    a = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x).float()
+    g.gguf_set_option("mmvq_max_m", 4)
+    try:
+        b = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x).float()
+    finally:
+        g.gguf_set_option("mmvq_max_m", 8)
+    ref = oracle.mul_mat(oracle.Q4_K, w, k, oracle.quantize_q8_1(x.float().cpu().numpy()))
+    assert_close(a.cpu().numpy(), ref, TOL_BF16, "mmvq")
+    assert_close(b.cpu().numpy(), ref, TOL_BF16, "mmq")
+
+
+def test_mmq_prefill_q4_k_full_size_sampled(g):
+    # prefill MMQ: Q4_K weight 8192 x 2048, bf16 activations M = 8192, bf16 out
+    n, k, m = 8192, 2048, 8192
+    w = _weights(oracle.Q4_K, n, k, seed=20)
+    x = synth.activations(m, k, seed=21, dtype=torch.bfloat16)
+    y = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x.to(DEV))
+    rng = np.random.default_rng(22)
+    rows = np.sort(rng.choice(n, 48, replace=False))
+    toks = np.sort(rng.choice(m, 24, replace=False))
+    rows[0], rows[-1], toks[0], toks[-1] = 0, n - 1, 0, m - 1
+    ref = oracle.mul_mat(oracle.Q4_K, w[rows], k, oracle.quantize_q8_1(x[toks].float().numpy()))
+    got = y[torch.from_numpy(toks).to(DEV)][:, torch.from_numpy(rows).to(DEV)].float().cpu().numpy()
+    # row rms for the tolerance floor comes from a full oracle row of the sampled tokens
+    assert_close(got, ref, TOL_BF16, "Q4_K 8192x2048 @ 8192")
+
+
+def test_mmq_lm_head_q6_k_full_size_sampled(g):
+    # prefill MMQ: Q6_K weight 248320 x 2048, M = 2048 tokens, bf16 out
+    n, k, m = 248320, 2048, 2048
+    w = synth.safe_blocks(oracle.Q6_K, n, k, seed=30)
+    x = synth.activations(m, k, seed=31, dtype=torch.bfloat16)
+    y = g.gguf_mul_mat(_u8(w), oracle.Q6_K, n, k, x.to(DEV))
+    rng = np.random.default_rng(32)
+    rows = np.sort(rng.choice(n, 40, replace=False))
+    toks = np.sort(rng.choice(m, 16, replace=False))
+    rows[0], rows[-1], toks[-1] = 0, n - 1, m - 1
+    ref = oracle.mul_mat(oracle.Q6_K, w[rows], k, oracle.quantize_q8_1(x[toks].float().numpy()))
+    got = y[torch.from_numpy(toks).to(DEV)][:, torch.from_numpy(rows).to(DEV)].float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    assert_close(got, ref, TOL_BF16, "Q6_K 248320x2048 @ 2048")

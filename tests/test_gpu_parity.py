@@ -1,0 +1,241 @@
+"""GPU parity of the CUDA path against the oracle (through the C ABI).
+
+Bit-exact: q8_1 quantization, dequantize / get_rows, per-block int32 dots.
+Within tolerance (fp32 1e-3, bf16 1e-2 of max(|r|, row rms)): mul_mat.
+Shapes span several CTAs and ragged tails; the full-size decode shapes are
+checked on a sampled subset of output rows that the oracle computes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _util import TOL_BF16, TOL_F32, assert_close
+from gguf_block_quantized_quantize_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def g():
+    from gguf_block_quantized_quantize_gb300 import build
+
+    build.build()
+    import gguf_block_quantized_quantize_gb300 as g
+
+    g.load_library()
+    assert torch.cuda.is_available()
+    return g
+
+
+def _u8(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _bits(t):
+    """uint16 bit patterns of a bf16 / f16 CUDA tensor."""
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------- quantize
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("m,k", [(1, 32), (37, 4096), (8, 14336), (300, 2048)])
+def test_quantize_q8_1_bit_exact(g, dtype, m, k):
+    x = synth.activations(m, k, seed=m + k, dtype=dtype)
+    x[0, :32] = 0                       # all-zero block
+    if k >= 64:
+        x[0, 32:64] = torch.linspace(-3.5, 3.5, 32).to(dtype)   # ties after scaling
+    ref = oracle.quantize_q8_1(x.float().numpy())
+    got = g.gguf_quantize_q8_1(x.to(DEV)).cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_quantize_q8_1_strided_rows(g):
+    base = synth.activations(16, 1024 + 64, seed=5, dtype=torch.bfloat16)
+    x = base[:, 32:32 + 1024]           # row stride 1088, misaligned start
+    ref = oracle.quantize_q8_1(x.float().contiguous().numpy())
+    got = g.gguf_quantize_q8_1(base.to(DEV)[:, 32:32 + 1024]).cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_quantize_q8_1_hand_values(g):
+    x = torch.zeros(1, 64)
+    x[0, 0], x[0, 1], x[0, 2], x[0, 7] = 127.0, 2.5, -2.5, 126.5
+    x[0, 32 + 5], x[0, 32 + 6] = -254.0, 1.0
+    got = g.gguf_quantize_q8_1(x.to(DEV)).cpu().numpy()
+    np.testing.assert_array_equal(got, oracle.quantize_q8_1(x.numpy()))
+    d, s, q = oracle.q8_1_fields(got)
+    assert d[0, 0] == 0x3C00 and q[0, 0, 1] == 3 and q[0, 0, 2] == -3 and q[0, 0, 7] == 127
+    assert d[0, 1] == 0x4000 and q[0, 1, 5] == -127 and q[0, 1, 6] == 1
+
+
+# ---------------------------------------------------------------- dequantize / get_rows
+
+def _weights(wt, n, k, seed, safe=False):
+    if safe:
+        return synth.safe_blocks(wt, n, k, seed)
+    return oracle.quantize_weights(wt, synth.normal((n, k), 0.02, seed) * synth.lognormal_row_scale(n, seed + 1))
+
+
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K])
+@pytest.mark.parametrize("safe", [False, True])
+@pytest.mark.parametrize("ot", [oracle.F32, oracle.BF16, oracle.F16])
+def test_dequantize_bit_exact(g, wt, safe, ot):
+    n, k = 37, 768 if wt != oracle.Q8_0 else 800
+    w = _weights(wt, n, k, seed=7, safe=safe)
+    ref = oracle.dequantize(wt, w, k, ot)
+    out = g.gguf_dequantize(_u8(w), wt, n, k, out_dtype={0: torch.float32, 30: torch.bfloat16, 1: torch.float16}[ot])
+    got = out.cpu().numpy() if ot == oracle.F32 else _bits(out)
+    np.testing.assert_array_equal(got.view(np.uint32) if ot == oracle.F32 else got,
+                                  ref.view(np.uint32) if ot == oracle.F32 else ref)
+
+
+@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0])
+def test_dequantize_odd_rows_unaligned_blocks(g, wt):
+    # K = one block per row: Q6_K (210 B) and Q8_0 (34 B) rows alternate alignment
+    k = 256 if wt != oracle.Q8_0 else 32
+    w = _weights(wt, 33, k, seed=8, safe=True)
+    ref = oracle.dequantize(wt, w, k, oracle.F32)
+    got = g.gguf_dequantize(_u8(w), wt, 33, k).cpu().numpy()
+    np.testing.assert_array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("wt", [oracle.Q6_K, oracle.Q4_K, oracle.Q8_0])
+def test_get_rows_bit_exact(g, wt):
+    rows, k = 1000, 512
+    w = _weights(wt, rows, k, seed=9, safe=True)
+    ids = np.array([0, 999, 3, 3, -1, 1000, 517, 42], dtype=np.int32)
+    ref = oracle.get_rows(wt, w, k, ids, oracle.BF16)
+    got = _bits(g.gguf_get_rows(_u8(w), wt, rows, k, _u8(ids), out_dtype=torch.bfloat16))
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_get_rows_llama_embedding_shape(g):
+    # tied embedding table 128256 x 3072 (Q6_K), ids at both ends
+    rows, k = 128256, 3072
+    w = synth.safe_blocks(oracle.Q6_K, rows, k, seed=10)
+    ids = np.array([0, 128255, 64000, 1, 77777, 128254, 5, 99999], dtype=np.int32)
+    ref = oracle.get_rows(oracle.Q6_K, w, k, ids, oracle.BF16)
+    got = _bits(g.gguf_get_rows(_u8(w), oracle.Q6_K, rows, k, _u8(ids), out_dtype=torch.bfloat16))
+    np.testing.assert_array_equal(got, ref)
+
+
+# ---------------------------------------------------------------- block dots
+
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K])
+def test_block_dots_bit_exact(g, wt):
+    n, k, m = 19, 1024, 3
+    w = _weights(wt, n, k, seed=11, safe=True)
+    x = synth.activations(m, k, seed=12, dtype=torch.float32)
+    xq = oracle.quantize_q8_1(x.numpy())
+    ref = oracle.block_dots(wt, w, k, xq)
+    got = g.gguf_debug_block_dots(_u8(w), wt, n, k, _u8(xq), m).cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
+# ---------------------------------------------------------------- mul_mat (MMVQ)
+
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K])
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("safe", [False, True])
+def test_mmvq_fp32(g, wt, m, safe):
+    n, k = 301, 2048
+    w = _weights(wt, n, k, seed=20 + m, safe=safe)
+    x = synth.activations(m, k, seed=30 + m, dtype=torch.float32)
+    ref = oracle.mul_mat(wt, w, k, oracle.quantize_q8_1(x.numpy()))
+    y = g.gguf_mul_mat(_u8(w), wt, n, k, x.to(DEV)).cpu().numpy()
+    assert_close(y, ref, TOL_F32, f"mmvq type {wt} m {m}")
+
+
+@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K])
+@pytest.mark.parametrize("k", [256, 768, 3072, 8192, 16384])
+def test_mmvq_k_range_bf16(g, wt, k):
+    n, m = 129, 4
+    w = _weights(wt, n, k, seed=k, safe=True)
+    x = synth.activations(m, k, seed=k + 1, dtype=torch.bfloat16)
+    ref = oracle.mul_mat(wt, w, k, oracle.quantize_q8_1(x.float().numpy()))
+    y = g.gguf_mul_mat(_u8(w), wt, n, k, x.to(DEV))
+    assert y.dtype == torch.bfloat16        # output in the activation dtype
+    assert_close(y.float().cpu().numpy(), ref, TOL_BF16, f"mmvq bf16 type {wt} k {k}")
+
+
+def test_mmvq_q8_0_config(g):
+    # Q8_0 512 x 1024, X 8 x 1024 fp32 ~ N(0,1), output 8 x 512 fp32
+    wf = synth.normal((512, 1024), 0.02, seed=0)
+    w = oracle.quantize_weights(oracle.Q8_0, wf)
+    x = synth.activations(8, 1024, seed=1, dtype=torch.float32)
+    xq = oracle.quantize_q8_1(x.numpy())
+    ref = oracle.mul_mat(oracle.Q8_0, w, 1024, xq)
+    y = g.gguf_mul_mat(_u8(w), oracle.Q8_0, 512, 1024, x.to(DEV))
+    assert y.shape == (8, 512) and y.dtype == torch.float32
+    assert_close(y.cpu().numpy(), ref, TOL_F32, "Q8_0 512x1024 m=8")
+
+
+@pytest.mark.parametrize("n", [4096, 14336])
+@pytest.mark.parametrize("m", [1, 2, 4, 8])
+def test_mmvq_q4_k_decode_full_size_sampled(g, n, m):
+    # decode MMVQ shapes: Q4_K n x 4096 from N(0, 0.02), bf16 activations
+    k = 4096
+    w = oracle.quantize_weights(oracle.Q4_K, synth.normal((n, k), 0.02, seed=n))
+    x = synth.activations(m, k, seed=n + m, dtype=torch.bfloat16)
+    xq = oracle.quantize_q8_1(x.float().numpy())
+    y = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x.to(DEV)).float().cpu().numpy()
+    rows = np.sort(np.random.default_rng(n + m).choice(n, 256, replace=False))
+    rows[0], rows[-1] = 0, n - 1
+    ref = oracle.mul_mat(oracle.Q4_K, w[rows], k, xq)
+    assert_close(y[:, rows], ref, TOL_BF16, f"Q4_K {n}x{k} m={m}")
+
+
+def test_mmvq_prequantized_segments(g):
+    """One q8_1 quantization reused by three weight segments that write column
+    slices of one output (the fused-Linear use)."""
+    k, m = 3072, 8
+    x = synth.activations(m, k, seed=40, dtype=torch.bfloat16)
+    xq_ref = oracle.quantize_q8_1(x.float().numpy())
+    xq = g.gguf_quantize_q8_1(x.to(DEV))
+    segs = [(oracle.Q4_K, 3072), (oracle.Q4_K, 1024), (oracle.Q6_K, 1024)]
+    out = torch.zeros(m, sum(n for _, n in segs), dtype=torch.bfloat16, device=DEV)
+    col = 0
+    refs = []
+    for i, (wt, n) in enumerate(segs):
+        w = _weights(wt, n, k, seed=41 + i)
+        g.gguf_mul_mat(_u8(w), wt, n, k, xq, xt=oracle.Q8_1, m=m, out=out[:, col:col + n])
+        refs.append(oracle.mul_mat(wt, w, k, xq_ref))
+        col += n
+    assert_close(out.float().cpu().numpy(), np.concatenate(refs, axis=1), TOL_BF16, "segments")
+
+
+def test_mmvq_edge_cases(g):
+    w = _weights(oracle.Q4_K, 1, 256, seed=50)
+    x = synth.activations(1, 256, seed=51, dtype=torch.float32)
+    y = g.gguf_mul_mat(_u8(w), oracle.Q4_K, 1, 256, x.to(DEV)).cpu().numpy()
+    assert_close(y, oracle.mul_mat(oracle.Q4_K, w, 256, oracle.quantize_q8_1(x.numpy())), TOL_F32, "1x256")
+    # zero activations give exact zeros
+    w = _weights(oracle.Q6_K, 7, 512, seed=52, safe=True)
+    y = g.gguf_mul_mat(_u8(w), oracle.Q6_K, 7, 512, torch.zeros(3, 512, device=DEV)).cpu().numpy()
+    assert np.all(y == 0)
+    # m = 0 is a no-op
+    y = g.gguf_mul_mat(_u8(w), oracle.Q6_K, 7, 512, torch.zeros(0, 512, device=DEV))
+    assert y.shape == (0, 7)
+
+
+def test_no_read_past_weight_view(g):
+    """A weight view fenced on both sides by 0xFF bytes (NaN fp16 scales) gives
+    the same result as a clean copy: no kernel reads outside the view."""
+    for wt, n, k in [(oracle.Q6_K, 9, 256), (oracle.Q8_0, 7, 96), (oracle.Q4_K, 5, 512)]:
+        w = _weights(wt, n, k, seed=60, safe=True)
+        nb = w.nbytes
+        off = 4096
+        fenced = torch.full((off + nb + 4096,), 0xFF, dtype=torch.uint8, device=DEV)
+        fenced[off:off + nb] = _u8(w.reshape(-1))
+        view = fenced[off:off + nb]
+        x = synth.activations(3, k, seed=61, dtype=torch.float32).to(DEV)
+        y = g.gguf_mul_mat(view, wt, n, k, x).cpu().numpy()
+        assert np.all(np.isfinite(y))
+        ref = oracle.mul_mat(wt, w, k, oracle.quantize_q8_1(x.cpu().numpy()))
+        assert_close(y, ref, TOL_F32, f"fenced type {wt}")
+        d = g.gguf_dequantize(view, wt, n, k).cpu().numpy()
+        np.testing.assert_array_equal(d.view(np.uint32), oracle.dequantize(wt, w, k, oracle.F32).view(np.uint32))
