@@ -62,7 +62,7 @@ SIGNATURES = {
     "gguf_quantize_q8_1": (_i, [_p, _i, _i64, _i64, _i64, _p, _p]),
     "gguf_dequantize": (_i, [_p, _i, _i64, _i64, _p, _i, _p]),
     "gguf_get_rows": (_i, [_p, _i, _i64, _i64, _p, _i64, _p, _i, _p]),
-    "gguf_mul_mat_ws_size": (_sz, [_i, _i64, _i64, _i, _i64]),
+    "gguf_mul_mat_ws_size": (_sz, [_i, _i64, _i64, _i, _i64, _i]),
     "gguf_mul_mat": (_i, [_p, _i, _i64, _i64, _p, _i, _i64, _i64, _p, _i, _i64, _p, _sz, _p]),
     "gguf_mul_mat_id_ws_size": (_sz, [ctypes.POINTER(MoeArgs)]),
     "gguf_mul_mat_id": (_i, [ctypes.POINTER(MoeArgs), _p, _sz, _p]),
@@ -157,8 +157,8 @@ def gguf_get_rows(table: torch.Tensor, tt: int, rows: int, k: int, ids: torch.Te
     return out
 
 
-def gguf_mul_mat_ws_size(wt: int, n: int, k: int, xt: int, m: int) -> int:
-    return int(load_library().gguf_mul_mat_ws_size(wt, n, k, xt, m))
+def gguf_mul_mat_ws_size(wt: int, n: int, k: int, xt: int, m: int, yt: int = BF16) -> int:
+    return int(load_library().gguf_mul_mat_ws_size(wt, n, k, xt, m, yt))
 
 
 def gguf_mul_mat(w: torch.Tensor, wt: int, n: int, k: int, x: torch.Tensor, xt: int | None = None,
@@ -178,7 +178,7 @@ def gguf_mul_mat(w: torch.Tensor, wt: int, n: int, k: int, x: torch.Tensor, xt: 
         out = torch.empty((m, n), dtype=out_dtype, device=x.device)
     if out.stride(1) != 1:
         raise ValueError("gguf_mul_mat: output rows must be contiguous")
-    need = gguf_mul_mat_ws_size(wt, n, k, xt, m)
+    need = gguf_mul_mat_ws_size(wt, n, k, xt, m, _TYPE_OF[out.dtype])
     if ws is None:
         ws = _workspace(need, x.device)
     _check(load_library().gguf_mul_mat(_ptr(w), wt, n, k, _ptr(x), xt, m, ldx, _ptr(out), _TYPE_OF[out.dtype],

@@ -26,6 +26,12 @@ static gguf_status fail(gguf_status st, const char *fmt, ...) {
     return st;
 }
 
+// for the other translation units of the C ABI
+gguf_status report(gguf_status st, const char *msg) {
+    g_last_error = msg;
+    return st;
+}
+
 static gguf_status cuda_status(cudaError_t e, const char *what) {
     if (e == cudaSuccess) return GGUF_OK;
     return fail(GGUF_ERR_CUDA, "%s: CUDA error %d (%s)", what, (int)e, cudaGetErrorString(e));
@@ -95,7 +101,7 @@ gguf_status gguf_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int6
     if (!x || !xq) return fail(GGUF_ERR_INVALID_ARG, "quantize_q8_1: null pointer");
     if (!aligned(x, esize(xt)) || !aligned(xq, 4))
         return fail(GGUF_ERR_ALIGNMENT, "quantize_q8_1: x must be element-aligned and xq 4-byte aligned");
-    return cuda_status(launch_quantize_q8_1(x, xt, m, k, ldx, (uint8_t *)xq, nullptr, (cudaStream_t)stream),
+    return cuda_status(launch_quantize_q8_1(x, xt, m, k, ldx, (uint8_t *)xq, nullptr, nullptr, (cudaStream_t)stream),
                        "quantize_q8_1");
 }
 
@@ -135,11 +141,17 @@ gguf_status gguf_get_rows(const void *table, int tt, int64_t rows, int64_t k, co
                        "get_rows");
 }
 
-size_t gguf_mul_mat_ws_size(int wt, int64_t n, int64_t k, int xt, int64_t m) {
-    (void)wt;
-    (void)n;
+size_t gguf_mul_mat_ws_size(int wt, int64_t n, int64_t k, int xt, int64_t m, int yt) {
     if (m <= 0 || k <= 0 || k % 32) return 0;
-    if (use_mmq(m, k)) return align256((size_t)(m * k * 2));              // fp16 operand rows
+    if (use_mmq(m, k)) {
+        // fp16 operand rows (plus their low parts for fp32 outputs), plus fp32
+        // partial sums when K is split across CTAs (small m)
+        const int64_t kx = op_pitch(wt, k);
+        size_t b = align256((size_t)(m * kx * 2));
+        if (yt == GGUF_F32) b += align256((size_t)(m * kx * 2));
+        if (m <= 256) b += align256((size_t)(m * n * 4));
+        return b;
+    }
     if (xt == GGUF_Q8_1) return 0;
     return align256((size_t)(m * row_size(GGUF_Q8_1, k)));             // q8_1 rows
 }
@@ -159,22 +171,31 @@ gguf_status gguf_mul_mat(const void *w, int wt, int64_t n, int64_t k, const void
     if (!aligned(w, 16)) return fail(GGUF_ERR_ALIGNMENT, "mul_mat: weight base must be 16-byte aligned");
     if (!aligned(y, esize(yt)) || (is_float(xt) && !aligned(x, esize(xt))) || (xt == GGUF_Q8_1 && !aligned(x, 4)))
         return fail(GGUF_ERR_ALIGNMENT, "mul_mat: misaligned x or y");
-    const size_t need = gguf_mul_mat_ws_size(wt, n, k, xt, m);
+    const size_t need = gguf_mul_mat_ws_size(wt, n, k, xt, m, yt);
     if (ws_bytes < need || (need > 0 && !ws))
         return fail(GGUF_ERR_WORKSPACE, "mul_mat: workspace of %zu bytes < required %zu", ws_bytes, need);
     if (need > 0 && !aligned(ws, 16)) return fail(GGUF_ERR_ALIGNMENT, "mul_mat: workspace must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
 
     if (use_mmq(m, k)) {
-        uint16_t *xh = (uint16_t *)ws;
-        cudaError_t e = xt == GGUF_Q8_1 ? launch_q8_1_to_f16((const uint8_t *)x, m, k, xh, s)
-                                        : launch_quantize_q8_1(x, xt, m, k, ldx, nullptr, xh, s);
+        const int64_t kx = op_pitch(wt, k);
+        uint8_t *wp = (uint8_t *)ws;
+        uint16_t *xh = (uint16_t *)wp;
+        wp += align256((size_t)(m * kx * 2));
+        uint16_t *xl = nullptr;
+        if (yt == GGUF_F32) {
+            xl = (uint16_t *)wp;
+            wp += align256((size_t)(m * kx * 2));
+        }
+        float *yacc = m <= 256 ? (float *)wp : nullptr;
+        cudaError_t e = xt == GGUF_Q8_1 ? launch_q8_1_to_f16((const uint8_t *)x, m, k, xh, xl, s, kx)
+                                        : launch_quantize_q8_1(x, xt, m, k, ldx, nullptr, xh, xl, s, kx);
         if (e != cudaSuccess) return cuda_status(e, "mul_mat quantize");
-        return cuda_status(launch_mmq((const uint8_t *)w, wt, n, k, xh, m, y, yt, ldy, s), "mul_mat mmq");
+        return cuda_status(launch_mmq((const uint8_t *)w, wt, n, k, xh, xl, m, y, yt, ldy, yacc, s), "mul_mat mmq");
     }
     const uint8_t *xq = (const uint8_t *)x;
     if (xt != GGUF_Q8_1) {
-        cudaError_t e = launch_quantize_q8_1(x, xt, m, k, ldx, (uint8_t *)ws, nullptr, s);
+        cudaError_t e = launch_quantize_q8_1(x, xt, m, k, ldx, (uint8_t *)ws, nullptr, nullptr, s);
         if (e != cudaSuccess) return cuda_status(e, "mul_mat quantize");
         xq = (const uint8_t *)ws;
     }
@@ -205,8 +226,9 @@ static gguf_status check_bank(const char *what, const void *w, int wt, int64_t E
 // workspace of one mul_mat_id call
 static MoeWs moe_call_layout(const gguf_moe_args *a, void *base) {
     const int64_t R = a->n_tokens * a->top_k;
-    if (a->mode == GGUF_MOE_GATE_UP_SWIGLU) return moe_ws_layout(base, a->n_experts, R, a->n_tokens * a->k, 0, 0);
-    return moe_ws_layout(base, a->n_experts, R, R * a->k, a->n_tokens * a->n, 0);
+    const int64_t kx = op_pitch(a->wt, a->k);
+    if (a->mode == GGUF_MOE_GATE_UP_SWIGLU) return moe_ws_layout(base, a->n_experts, R, a->n_tokens * kx, 0, 0, false);
+    return moe_ws_layout(base, a->n_experts, R, R * kx, a->n_tokens * a->n, 0, false);
 }
 
 static gguf_status check_moe(const gguf_moe_args *a) {
@@ -235,9 +257,9 @@ static gguf_status check_moe(const gguf_moe_args *a) {
 }
 
 static cudaError_t to_f16_operand(const void *x, int xt, int64_t rows, int64_t k, int64_t ldx, uint16_t *xh,
-                                  cudaStream_t s) {
-    return xt == GGUF_Q8_1 ? launch_q8_1_to_f16((const uint8_t *)x, rows, k, xh, s)
-                           : launch_quantize_q8_1(x, xt, rows, k, ldx, nullptr, xh, s);
+                                  uint16_t *xl, int64_t pitch, cudaStream_t s) {
+    return xt == GGUF_Q8_1 ? launch_q8_1_to_f16((const uint8_t *)x, rows, k, xh, xl, s, pitch)
+                           : launch_quantize_q8_1(x, xt, rows, k, ldx, nullptr, xh, xl, s, pitch);
 }
 
 size_t gguf_mul_mat_id_ws_size(const gguf_moe_args *args) {
@@ -261,26 +283,27 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
         const int64_t idim = a->n / 2;
         const size_t ybytes = a->yt == GGUF_Q8_1 ? (size_t)(R * row_size(GGUF_Q8_1, idim)) : (size_t)(R * idim * 2);
         if ((e = cudaMemsetAsync(a->y, 0, ybytes, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id");
-        if ((e = to_f16_operand(a->x, a->xt, a->n_tokens, a->k, a->ldx, w.xh, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id quantize");
+        if ((e = to_f16_operand(a->x, a->xt, a->n_tokens, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), s)) != cudaSuccess) return cuda_status(e, "mul_mat_id quantize");
         if ((e = moe_group(a->ids, nullptr, R, a->n_experts, false, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id grouping");
-        e = launch_moe_gate_up((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, a->top_k, R,
+        e = launch_moe_gate_up((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, w.xl, a->top_k, R,
                                a->n_experts, w, a->yt == GGUF_Q8_1 ? (uint8_t *)a->y : nullptr,
                                a->yt == GGUF_BF16 ? (uint16_t *)a->y : nullptr,
-                               a->yt == GGUF_F16 ? (uint16_t *)a->y : nullptr, s);
+                               a->yt == GGUF_F16 ? (uint16_t *)a->y : nullptr, nullptr, a->n / 2, s);
         return cuda_status(e, "mul_mat_id gate_up");
     }
-    if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id quantize");
+    if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), s)) != cudaSuccess) return cuda_status(e, "mul_mat_id quantize");
     if ((e = moe_group(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id grouping");
     if ((e = cudaMemsetAsync(w.yacc, 0, sizeof(float) * (size_t)(a->n_tokens * a->n), s)) != cudaSuccess) return cuda_status(e, "mul_mat_id");
-    if ((e = launch_moe_down((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, a->top_k, R,
-                             a->n_experts, a->route_w, w, w.yacc, s)) != cudaSuccess)
+    if ((e = launch_moe_down((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, w.xl, a->top_k, R,
+                             a->n_experts, a->route_w, w, w.yacc, a->yt == GGUF_F32, s)) != cudaSuccess)
         return cuda_status(e, "mul_mat_id down");
     return cuda_status(launch_moe_finalize(w.yacc, a->n_tokens * a->n, a->y, a->yt, s), "mul_mat_id finalize");
 }
 
 static MoeWs ffn_layout(const gguf_moe_ffn_args *a, void *base) {
     const int64_t R = a->n_tokens * a->top_k;
-    return moe_ws_layout(base, a->n_experts, R, a->n_tokens * a->hidden, a->n_tokens * a->hidden, R * a->inter);
+    return moe_ws_layout(base, a->n_experts, R, a->n_tokens * op_pitch(a->gate_up_type, a->hidden),
+                         a->n_tokens * a->hidden, R * op_pitch(a->down_type, a->inter), a->yt == GGUF_F32);
 }
 
 size_t gguf_moe_ffn_ws_size(const gguf_moe_ffn_args *a) {
@@ -311,15 +334,16 @@ gguf_status gguf_moe_ffn(const gguf_moe_ffn_args *a, void *ws, size_t ws_bytes, 
     const int64_t R = a->n_tokens * a->top_k;
     const int bn = moe_bn(R, a->n_experts);
     cudaError_t e;
-    if ((e = to_f16_operand(a->x, a->xt, a->n_tokens, a->hidden, a->ldx, w.xh, s)) != cudaSuccess) return cuda_status(e, "moe_ffn quantize");
+    if ((e = to_f16_operand(a->x, a->xt, a->n_tokens, a->hidden, a->ldx, w.xh, w.xl, op_pitch(a->gate_up_type, a->hidden), s)) != cudaSuccess) return cuda_status(e, "moe_ffn quantize");
     // one grouping serves both GEMMs; a route of weight 0 contributes nothing and is skipped by both
     if ((e = moe_group(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "moe_ffn grouping");
     if ((e = launch_moe_gate_up((const uint8_t *)a->w_gate_up, a->gate_up_type, a->gate_up_stride, 2 * a->inter,
-                                a->hidden, w.xh, a->top_k, R, a->n_experts, w, nullptr, nullptr, w.h16, s)) != cudaSuccess)
+                                a->hidden, w.xh, w.xl, a->top_k, R, a->n_experts, w, nullptr, nullptr, w.h16, w.h16lo,
+                                op_pitch(a->down_type, a->inter), s)) != cudaSuccess)
         return cuda_status(e, "moe_ffn gate_up");
     if ((e = cudaMemsetAsync(w.yacc, 0, sizeof(float) * (size_t)(a->n_tokens * a->hidden), s)) != cudaSuccess) return cuda_status(e, "moe_ffn");
     if ((e = launch_moe_down((const uint8_t *)a->w_down, a->down_type, a->down_stride, a->hidden, a->inter, w.h16,
-                             a->top_k, R, a->n_experts, a->route_w, w, w.yacc, s)) != cudaSuccess)
+                             w.h16lo, a->top_k, R, a->n_experts, a->route_w, w, w.yacc, a->yt == GGUF_F32, s)) != cudaSuccess)
         return cuda_status(e, "moe_ffn down");
     return cuda_status(launch_moe_finalize(w.yacc, a->n_tokens * a->hidden, a->y, a->yt, s), "moe_ffn finalize");
 }
@@ -357,3 +381,4 @@ int64_t gguf_get_option(const char *key) {
 }
 
 }  // extern "C"
+

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/gguf_gb300.h"
+
 namespace gg {
 
 struct DeviceInfo {
@@ -14,13 +16,21 @@ struct DeviceInfo {
     size_t smem_optin;
 };
 const DeviceInfo &device_info();
+// sets the thread-local message returned by gguf_last_error() and returns st
+gguf_status report(gguf_status st, const char *msg);
 
-// q8_1 quantization; also writes the fp16 tensor-core operand xh[m][k] (d16*q)
-// when xh != nullptr.
+// q8_1 quantization (xq may be null); also writes the fp16 tensor-core operand
+// xh[m][pitch] = fp16(d16*q) when xh != nullptr, and its low part
+// xl = fp16(d16*q - xh) when xl != nullptr.  pitch > k appends the Q4_K
+// min-term correction columns (see op_pitch) and zero padding.
 cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int64_t ldx, uint8_t *xq,
-                                 uint16_t *xh, cudaStream_t s);
-// fp16 operand xh[m][k] from q8_1 rows (d16*q rounded to fp16).
-cudaError_t launch_q8_1_to_f16(const uint8_t *xq, int64_t m, int64_t k, uint16_t *xh, cudaStream_t s);
+                                 uint16_t *xh, uint16_t *xl, cudaStream_t s, int64_t pitch = 0);
+// the same fp16 operand(s) from q8_1 rows
+cudaError_t launch_q8_1_to_f16(const uint8_t *xq, int64_t m, int64_t k, uint16_t *xh, uint16_t *xl, cudaStream_t s,
+                               int64_t pitch = 0);
+// Row length of the tensor-core operand for weight type wt: k, plus for Q4_K
+// one min-term correction column per 32-block, rounded up to the 64-value K step.
+inline int64_t op_pitch(int wt, int64_t k) { return wt == GGUF_Q4_K ? (k + k / 32 + 63) / 64 * 64 : k; }
 
 cudaError_t launch_dequantize(const uint8_t *w, int wt, int64_t rows, int64_t k, const int32_t *ids,
                               int64_t table_rows, void *out, int ot, cudaStream_t s);
@@ -32,29 +42,34 @@ cudaError_t launch_block_dots(const uint8_t *w, int wt, int64_t n, int64_t k, co
 cudaError_t launch_mmvq(const uint8_t *w, int wt, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y,
                         int yt, int64_t ldy, cudaStream_t s);
 
-// tensor-core MMQ: y[m][ldy] = W[n][k] . xh[m][k] (fp16 operand rows)
-cudaError_t launch_mmq(const uint8_t *w, int wt, int64_t n, int64_t k, const uint16_t *xh, int64_t m, void *y,
-                       int yt, int64_t ldy, cudaStream_t s);
+// tensor-core MMQ: y[m][ldy] = W[n][k] . xh[m][k] (fp16 operand rows; fp32
+// outputs also need the low parts xl).  yacc (optional, fp32 [m][n]) lets small
+// m split K across CTAs.
+cudaError_t launch_mmq(const uint8_t *w, int wt, int64_t n, int64_t k, const uint16_t *xh, const uint16_t *xl,
+                       int64_t m, void *y, int yt, int64_t ldy, float *yacc, cudaStream_t s);
+cudaError_t launch_convert_rows(const float *yacc, int64_t m, int64_t n, void *y, int yt, int64_t ldy, cudaStream_t s);
 
 // ---- MoE (moe.cu)
 struct MoeWs {
     int32_t *counts, *offsets, *pos, *route_list, *tile_expert, *tile_start, *n_tiles;
-    uint16_t *xh;
+    uint16_t *xh, *xl;
     float *yacc;
-    uint16_t *h16;
+    uint16_t *h16, *h16lo;
     size_t bytes;
 };
 // base == nullptr computes only the size
-MoeWs moe_ws_layout(void *base, int64_t E, int64_t R, int64_t xh_elems, int64_t yacc_elems, int64_t h16_elems);
+MoeWs moe_ws_layout(void *base, int64_t E, int64_t R, int64_t xh_elems, int64_t yacc_elems, int64_t h16_elems,
+                    bool with_lo);
 int moe_bn(int64_t routes, int64_t experts);
 cudaError_t moe_group(const int32_t *ids, const float *rw, int64_t R, int64_t E, bool skip_zero_w, int32_t *status,
                       const MoeWs &w, int bn, cudaStream_t s);
 cudaError_t launch_moe_gate_up(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
-                               const uint16_t *xh, int64_t top_k, int64_t R, int64_t E, const MoeWs &ws,
-                               uint8_t *hq, uint16_t *hbf, uint16_t *h16, cudaStream_t s);
+                               const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
+                               const MoeWs &ws, uint8_t *hq, uint16_t *hbf, uint16_t *h16, uint16_t *h16lo,
+                               int64_t hpitch, cudaStream_t s);
 cudaError_t launch_moe_down(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
-                            const uint16_t *xh, int64_t top_k, int64_t R, int64_t E, const float *route_w,
-                            const MoeWs &ws, float *yacc, cudaStream_t s);
+                            const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
+                            const float *route_w, const MoeWs &ws, float *yacc, bool precise, cudaStream_t s);
 cudaError_t launch_moe_finalize(const float *yacc, int64_t count, void *y, int yt, cudaStream_t s);
 
 }  // namespace gg

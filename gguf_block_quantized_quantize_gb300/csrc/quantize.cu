@@ -39,10 +39,50 @@ __device__ __forceinline__ void load8(const void *x, int64_t off, float v[8]) {
     }
 }
 
+// fp16 tensor-core operand of 8 q8_1 values: hi = fp16(d16 * q) (d16 * q is
+// exact in fp32), and optionally lo = fp16(d16 * q - hi), which makes hi + lo
+// equal to d16 * q (the 3-term product of the precise mode needs it).
+__device__ __forceinline__ void write_f16_operand(float d16, const int q[8], uint16_t *hi, uint16_t *lo) {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float v0 = d16 * (float)q[2 * i], v1 = d16 * (float)q[2 * i + 1];
+        const uint16_t h0 = f2h_rn(v0), h1 = f2h_rn(v1);
+        hw[i] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        lw[i] = (uint32_t)f2h_rn(v0 - h2f(h0)) | ((uint32_t)f2h_rn(v1 - h2f(h1)) << 16);
+    }
+    *reinterpret_cast<uint4 *>(hi) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    if (lo) *reinterpret_cast<uint4 *>(lo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
+// Min-term correction columns of the operand rows (Q4_K weights).  The fp16
+// operand d16 * q gives the min term of a 32-block as dmin * m * d16 * sum(q);
+// the blockwise formula uses the stored s instead.  Column k + b of a row
+// holds c_b = d16 * sum(q) - s (the weight side holds dmin * m for that
+// sub-block), so the product adds exactly the difference.  Columns past
+// k + k/32 up to the row pitch are zero, and so are all low parts there.
+__device__ __forceinline__ void write_correction(uint16_t *hi_row, uint16_t *lo_row, int64_t k, int64_t pitch,
+                                                 int64_t b, int j, float d16, int sum, uint16_t s16) {
+    const int64_t nb = k / QK8;
+    if (j == 0) hi_row[k + b] = f2h_rn(d16 * (float)sum - h2f(s16));
+    if (j == 1 && lo_row) lo_row[k + b] = 0;
+    // zero padding [k + nb, pitch): column k + nb + 4 * b + j, then every 4 * nb
+    for (int64_t c = k + nb + 4 * b + j; c < pitch; c += 4 * nb) {
+        hi_row[c] = 0;
+        if (lo_row) lo_row[c] = 0;
+    }
+}
+
 template <int XT, bool VEC>
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restrict__ x, int64_t m, int64_t k,
                                                             int64_t ldx, uint8_t *__restrict__ xq,
-                                                            uint16_t *__restrict__ xh) {
+                                                            uint16_t *__restrict__ xh, uint16_t *__restrict__ xl,
+                                                            int64_t pitch) {
+    // launched as a programmatic dependent: let the next kernel start its own
+    // independent prefetch, and wait for the previous kernel before touching
+    // memory it may still read or write
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t nb = k / QK8;
     const int64_t total = m * nb;
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -89,18 +129,16 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restri
         }
     }
     if (xh != nullptr) {
-        // fp16 tensor-core operand: the dequantized q8_1 value d16 * q, rounded once
-        const float d16 = h2f(dh);
-        uint32_t hw[4];
-#pragma unroll
-        for (int i = 0; i < 4; i++)
-            hw[i] = (uint32_t)f2h_rn(d16 * (float)q[2 * i]) | ((uint32_t)f2h_rn(d16 * (float)q[2 * i + 1]) << 16);
-        *reinterpret_cast<uint4 *>(xh + row * k + b * QK8 + 8 * j) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        write_f16_operand(h2f(dh), q, xh + row * pitch + b * QK8 + 8 * j, xl ? xl + row * pitch + b * QK8 + 8 * j : nullptr);
+        if (pitch > k)
+            write_correction(xh + row * pitch, xl ? xl + row * pitch : nullptr, k, pitch, b, j, h2f(dh), sum,
+                             f2h_rn(__fmul_rn(d, (float)sum)));
     }
 }
 
 __global__ void __launch_bounds__(256) q8_1_to_f16_kernel(const uint8_t *__restrict__ xq, int64_t m, int64_t k,
-                                                          uint16_t *__restrict__ xh) {
+                                                          uint16_t *__restrict__ xh, uint16_t *__restrict__ xl,
+                                                          int64_t pitch) {
     const int64_t nb = k / QK8;
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t blk = g >> 2;
@@ -109,25 +147,36 @@ __global__ void __launch_bounds__(256) q8_1_to_f16_kernel(const uint8_t *__restr
     const uint8_t *p = xq + blk * Q8_1_BYTES;
     const float d16 = h2f(ld_u16(p));
     const uint32_t w0 = ld_u32(p + 4 + 8 * j), w1 = ld_u32(p + 8 + 8 * j);
-    int8_t q[8];
+    int q[8];
 #pragma unroll
     for (int i = 0; i < 4; i++) { q[i] = (int8_t)(w0 >> (8 * i)); q[4 + i] = (int8_t)(w1 >> (8 * i)); }
-    uint32_t hw[4];
-#pragma unroll
-    for (int i = 0; i < 4; i++)
-        hw[i] = (uint32_t)f2h_rn(d16 * (float)q[2 * i]) | ((uint32_t)f2h_rn(d16 * (float)q[2 * i + 1]) << 16);
     const int64_t row = blk / nb, b = blk - row * nb;
-    *reinterpret_cast<uint4 *>(xh + row * k + b * QK8 + 8 * j) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    write_f16_operand(d16, q, xh + row * pitch + b * QK8 + 8 * j, xl ? xl + row * pitch + b * QK8 + 8 * j : nullptr);
+    if (pitch > k) {
+        int sum = 0;
+        for (int t = 0; t < 32; t++) sum += (int8_t)p[4 + t];
+        write_correction(xh + row * pitch, xl ? xl + row * pitch : nullptr, k, pitch, b, j, d16, sum, ld_u16(p + 2));
+    }
 }
 
 cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int64_t ldx, uint8_t *xq,
-                                 uint16_t *xh, cudaStream_t s) {
+                                 uint16_t *xh, uint16_t *xl, cudaStream_t s, int64_t pitch) {
+    if (pitch < k) pitch = k;
     const int64_t threads = m * (k / QK8) * 4;
     if (threads == 0) return cudaSuccess;
     const int64_t grid = (threads + 255) / 256;
     const int esz = xt == GGUF_F32 ? 4 : 2;
     const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && ((ldx * esz) % 16 == 0);
-#define QLAUNCH(XT, V) quantize_q8_1_kernel<XT, V><<<(unsigned)grid, 256, 0, s>>>(x, m, k, ldx, xq, xh)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+#define QLAUNCH(XT, V) (void)cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<XT, V>, x, m, k, ldx, xq, xh, xl, pitch)
     if (xt == GGUF_F32) { if (vec) QLAUNCH(GGUF_F32, true); else QLAUNCH(GGUF_F32, false); }
     else if (xt == GGUF_BF16) { if (vec) QLAUNCH(GGUF_BF16, true); else QLAUNCH(GGUF_BF16, false); }
     else { if (vec) QLAUNCH(GGUF_F16, true); else QLAUNCH(GGUF_F16, false); }
@@ -135,10 +184,12 @@ cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, in
     return cudaGetLastError();
 }
 
-cudaError_t launch_q8_1_to_f16(const uint8_t *xq, int64_t m, int64_t k, uint16_t *xh, cudaStream_t s) {
+cudaError_t launch_q8_1_to_f16(const uint8_t *xq, int64_t m, int64_t k, uint16_t *xh, uint16_t *xl, cudaStream_t s,
+                               int64_t pitch) {
+    if (pitch < k) pitch = k;
     const int64_t threads = m * (k / QK8) * 4;
     if (threads == 0) return cudaSuccess;
-    q8_1_to_f16_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(xq, m, k, xh);
+    q8_1_to_f16_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(xq, m, k, xh, xl, pitch);
     return cudaGetLastError();
 }
 

@@ -176,3 +176,192 @@ __device__ __forceinline__ void store_sw128_row(uint8_t *tile, int row, const ui
 }
 
 }  // namespace gg
+
+namespace gg {
+
+// ---------------------------------------------------------------- half-row units
+//
+// A K-step of 64 values of one weight row, split in two halves of 32 values
+// (one 32-value sub-block, or two 16-value Q6_K sub-blocks, or one Q8_0
+// block), each produced by its own thread.  `H2` selects packed-half math
+// (two fp16 roundings per value instead of one; used when the product is
+// rounded to a 16-bit output anyway).
+
+// (1024 + byte) as fp16 for bytes 2i and 2i+1 of w (i = 0, 1)
+__device__ __forceinline__ uint32_t bytes_to_h2_1024(uint32_t w, int i) {
+    return __byte_perm(w, 0x64646464u, i == 0 ? 0x4140u : 0x4342u);
+}
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t v) { return *reinterpret_cast<const __half2 *>(&v); }
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<const uint32_t *>(&h); }
+
+template <int WT>
+struct KHalf;
+
+template <>
+struct KHalf<GGUF_Q4_K> {
+    uint4 hdr, q0, q1;
+    __device__ __forceinline__ void load(const uint8_t *row, int ks, int) {
+        const uint8_t *blk = row + (int64_t)(ks >> 2) * Q4_K_BYTES;
+        const int c = ks & 3;
+        hdr = *reinterpret_cast<const uint4 *>(blk);
+        q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
+        q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
+    }
+    // half 0: low nibbles (sub-block 2c), half 1: high nibbles (sub-block 2c+1)
+    __device__ __forceinline__ void scales(int ks, int half, float &a, float &b) const {
+        const uint32_t sc[3] = {hdr.y, hdr.z, hdr.w};
+        int s, m;
+        q4k_scale_min(sc, 2 * (ks & 3) + half, s, m);
+        a = __fmul_rn(h2f(hdr.x & 0xffff), (float)s);
+        b = __fmul_rn(h2f(hdr.x >> 16), (float)m);
+    }
+    __device__ __forceinline__ uint32_t nibbles(int i, int half) const {
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        return half ? ((w[i] >> 4) & 0x0F0F0F0Fu) : (w[i] & 0x0F0F0F0Fu);
+    }
+    // exact fp32 block values (a*q is exact; the subtraction rounds once)
+    __device__ __forceinline__ void unpack_f32(int ks, int half, float (&v)[32]) const {
+        float a, b;
+        scales(ks, half, a, b);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const uint32_t nib = nibbles(i, half);
+#pragma unroll
+            for (int j = 0; j < 4; j++) v[4 * i + j] = fmaf(a, byte_to_f(nib, j, -8388608.0f), -b);
+        }
+    }
+    __device__ __forceinline__ void unpack_h2(int ks, int half, uint32_t (&out)[16]) const {
+        float a, b;
+        scales(ks, half, a, b);
+        const __half2 a2 = __float2half2_rn(a), nb2 = __float2half2_rn(-b), k1024 = __float2half2_rn(1024.0f);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const uint32_t nib = nibbles(i, half);
+#pragma unroll
+            for (int p = 0; p < 2; p++) {
+                const __half2 q = __hsub2(u32_as_h2(bytes_to_h2_1024(nib, p)), k1024);
+                out[2 * i + p] = h2_as_u32(__hfma2(q, a2, nb2));
+            }
+        }
+    }
+};
+
+template <>
+struct KHalf<GGUF_Q6_K> {
+    uint32_t ql[8], qh[8], sc, dw;
+    // K-step ks: super-block ks/4, half h = (ks%4)/2, j = ks%2; this thread's
+    // half gg is run g = 2j + gg: ql bytes [64h + 32gg, +32), nibble j.
+    __device__ __forceinline__ void load(const uint8_t *row, int ks, int gg) {
+        const uint8_t *blk = row + (int64_t)(ks >> 2) * Q6_K_BYTES;
+        const int h = (ks >> 1) & 1, j = ks & 1;
+        ldw_a2<8>(blk + 64 * h + 32 * gg, ql);
+        ldw_a2<8>(blk + 128 + 32 * h, qh);
+        sc = ld_u16(blk + 192 + 8 * h + 2 * (2 * j + gg));   // scales of l < 16 and l >= 16
+        dw = ld_u16(blk + 208);
+    }
+    __device__ __forceinline__ uint32_t quants(int ks, int gg, int i) const {
+        const int j = ks & 1;
+        return ((ql[i] >> (4 * j)) & 0x0F0F0F0Fu) | (((qh[i] >> (4 * j + 2 * gg)) & 0x03030303u) << 4);
+    }
+    __device__ __forceinline__ void dscales(float &ds0, float &ds1) const {
+        const float d = h2f(dw & 0xffff);
+        ds0 = __fmul_rn(d, (float)(int)(int8_t)(sc & 0xff));
+        ds1 = __fmul_rn(d, (float)(int)(int8_t)((sc >> 8) & 0xff));
+    }
+    // exact fp32 values (d*sc*(q-32) fits in 24 bits)
+    __device__ __forceinline__ void unpack_f32(int ks, int gg, float (&v)[32]) const {
+        float ds0, ds1;
+        dscales(ds0, ds1);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const uint32_t q4 = quants(ks, gg, i);
+#pragma unroll
+            for (int t = 0; t < 4; t++) v[4 * i + t] = __fmul_rn(i < 4 ? ds0 : ds1, byte_to_f(q4, t, -8388640.0f));
+        }
+    }
+    __device__ __forceinline__ void unpack_h2(int ks, int gg, uint32_t (&out)[16]) const {
+        float ds0, ds1;
+        dscales(ds0, ds1);
+        const __half2 d0 = __float2half2_rn(ds0), d1 = __float2half2_rn(ds1), k1056 = __float2half2_rn(1056.0f);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const uint32_t q4 = quants(ks, gg, i);
+#pragma unroll
+            for (int p = 0; p < 2; p++) {
+                const __half2 q = __hsub2(u32_as_h2(bytes_to_h2_1024(q4, p)), k1056);  // q - 32
+                out[2 * i + p] = h2_as_u32(__hmul2(q, i < 4 ? d0 : d1));
+            }
+        }
+    }
+};
+
+template <>
+struct KHalf<GGUF_Q8_0> {
+    uint32_t q[8];
+    uint32_t dw;
+    int64_t kblocks;
+    // half t of K-step ks is block 2*ks + t (absent past the end when k % 64 == 32)
+    __device__ __forceinline__ void load(const uint8_t *row, int ks, int t) {
+        const int64_t b = 2 * (int64_t)ks + t;
+        if (b < kblocks) {
+            const uint8_t *blk = row + b * Q8_0_BYTES;
+            dw = ld_u16(blk);
+            ldw_a2<8>(blk + 2, q);
+        } else {
+            dw = 0;
+#pragma unroll
+            for (int i = 0; i < 8; i++) q[i] = 0u;
+        }
+    }
+    __device__ __forceinline__ void unpack_f32(int, int, float (&v)[32]) const {
+        const float d = h2f((uint16_t)dw);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const uint32_t u = q[i] ^ 0x80808080u;  // signed byte + 128
+#pragma unroll
+            for (int b = 0; b < 4; b++) v[4 * i + b] = __fmul_rn(d, byte_to_f(u, b, -8388736.0f));
+        }
+    }
+    // d * q is exact in fp32 and rounded once to fp16 either way
+    __device__ __forceinline__ void unpack_h2(int, int, uint32_t (&out)[16]) const {
+        const __half2 d2 = __halves2half2(__ushort_as_half((uint16_t)dw), __ushort_as_half((uint16_t)dw));
+        const __half2 k1152 = __float2half2_rn(1152.0f);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const uint32_t u = q[i] ^ 0x80808080u;
+#pragma unroll
+            for (int p = 0; p < 2; p++) {
+                const __half2 qq = __hsub2(u32_as_h2(bytes_to_h2_1024(u, p)), k1152);
+                out[2 * i + p] = h2_as_u32(__hmul2(qq, d2));
+            }
+        }
+    }
+};
+
+// fp32 values -> one fp16 operand (single rounding)
+__device__ __forceinline__ void pack_single(const float (&v)[32], uint32_t (&hi)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; i++) hi[i] = pack_h2(v[2 * i], v[2 * i + 1]);
+}
+// fp32 values -> hi + lo fp16 operands with hi + lo = v to ~2^-22
+__device__ __forceinline__ void pack_split(const float (&v)[32], uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+        const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+        const float2 hf = __half22float2(h);
+        hi[i] = h2_as_u32(h);
+        lo[i] = pack_h2(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
+    }
+}
+
+// store 32 fp16 (16 words) as chunks [4*half, 4*half + 4) of a 128-byte swizzled row
+__device__ __forceinline__ void store_sw128_half(uint8_t *tile, int row, int half, const uint32_t (&v)[16]) {
+    uint8_t *base = tile + row * 128;
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        const int pc = (4 * half + c) ^ (row & 7);
+        *reinterpret_cast<uint4 *>(base + pc * 16) = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    }
+}
+
+}  // namespace gg

@@ -97,3 +97,28 @@ def lognormal_row_scale(rows: int, seed: int, sigma: float = 1.0) -> np.ndarray:
     """Per-row multiplicative scale exp(N(0, sigma^2)), used to spread block
     scales over a wider range than uniform N(0, 0.02) weights give."""
     return np.exp(normal((rows, 1), sigma, seed)).astype(np.float32)
+
+
+def safe_blocks_device(t: int, rows: int, k: int, seed: int, device) -> torch.Tensor:
+    """Random-but-safe packed blocks generated on the device (for multi-GB
+    benchmark weights): random bytes, then the fp16 scale fields overwritten
+    with a few safe values of the size quantized N(0, 0.02) weights have."""
+    nb = k // BLOCK_ELEMS[t]
+    bb = BLOCK_BYTES[t]
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    blk = torch.randint(0, 256, (rows, nb, bb), dtype=torch.uint8, device=device, generator=g)
+    def field(vals, lo, hi):
+        bits = torch.from_numpy(_f16_bits(np.asarray(vals, dtype=np.float64)).view(np.uint8).reshape(-1, 2))
+        choice = torch.randint(0, len(vals), (rows, nb), device=device, generator=g)
+        blk[:, :, lo:hi] = bits.to(device)[choice]
+    if t == Q8_0:
+        field([1.5e-4, -2.5e-4, 3.5e-4, -4.5e-4], 0, 2)
+    elif t == Q4_K:
+        field([3.0e-5, 6.0e-5, 1.1e-4, 1.6e-4], 0, 2)
+        field([0.0, 3.0e-4, 6.0e-4, 9.0e-4], 2, 4)
+    elif t == Q6_K:
+        field([7.0e-6, -1.1e-5, 1.4e-5, -1.8e-5], 208, 210)
+    else:
+        raise ValueError(f"unsupported type {t}")
+    return blk.reshape(rows, nb * bb)

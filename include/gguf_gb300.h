@@ -144,12 +144,13 @@ gguf_status gguf_get_rows(const void *table, int tt, int64_t rows, int64_t k, co
  *        (may be NULL when that size is 0).
  * Path: small m (<= option "mmvq_max_m", default 8) runs the bandwidth-bound
  * MMVQ kernel (per-block int8 dot products, exact int32 block sums, fp32
- * combination); larger m runs the tensor-core MMQ kernel.  Accuracy: MMVQ is
- * within 1e-6 relative of the fp64 blockwise formula; MMQ feeds the tcgen05
- * tensor cores fp16 operands (dequantized weight and q8_1 values) with fp32
- * accumulation, within 3e-3 relative to the row rms.
+ * combination); larger m runs the tensor-core MMQ kernel, which feeds tcgen05
+ * fp16 operands (the exact fp32 block value of each weight and d16*q of each
+ * activation) with fp32 accumulation: one fp16 operand per side for 16-bit
+ * outputs (about 3e-4 of the row rms from the two roundings), hi + lo
+ * operands on both sides for fp32 outputs (about 1e-6).
  */
-size_t gguf_mul_mat_ws_size(int wt, int64_t n, int64_t k, int xt, int64_t m);
+size_t gguf_mul_mat_ws_size(int wt, int64_t n, int64_t k, int xt, int64_t m, int yt);
 gguf_status gguf_mul_mat(const void *w, int wt, int64_t n, int64_t k, const void *x, int xt, int64_t m,
                          int64_t ldx, void *y, int yt, int64_t ldy, void *ws, size_t ws_bytes, gguf_stream_t stream);
 

@@ -79,6 +79,8 @@ def test_workspace_sizes(g):
     assert g.gguf_mul_mat_ws_size(g.Q4_K, 4096, 4096, g.Q8_1, 8) == 0
     assert g.gguf_mul_mat_ws_size(g.Q4_K, 4096, 4096, g.BF16, 8) >= 8 * 4096 // 32 * 36
     assert g.gguf_mul_mat_ws_size(g.Q4_K, 4096, 4096, g.BF16, 64) >= 64 * 4096 * 2
+    # fp32 outputs of the tensor-core path also hold the low fp16 parts
+    assert g.gguf_mul_mat_ws_size(g.Q4_K, 4096, 4096, g.BF16, 64, g.F32) >= 2 * 64 * 4096 * 2
 
 
 def test_other_entry_points_reject_bad_arguments(g):

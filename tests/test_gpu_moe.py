@@ -1,11 +1,12 @@
 """GPU parity of mul_mat_id (MoE) against the oracle.
 
   * gate_up + SwiGLU: h (bf16) within 1e-2 of max(|r|, row rms); the q8_1
-    form within one quantization step per value (the GPU's g, u come from the
-    fp16 tensor-core product, so h may sit on the other side of a rounding
-    boundary -- a q differs by at most 1);
+    form within half a quantization step of each side plus one bf16 ulp (g, u
+    come from the precise hi + lo tensor-core product, so a bf16 rounding of h
+    can still land on the other side of a tie);
   * down + weighted sum fed with the ORACLE's h_q8_1 rows: within 1e-2;
-  * the fused FFN end to end against the full oracle chain: within 1e-2;
+  * the fused FFN end to end against the full oracle chain: norm-wise per
+    token within 1e-2 (the re-quantized intermediate, see _util.py);
   * repeated expert ids, id -1, ids >= E (counted in the status word) and
     weight-0 routes; the full-size configuration (E = 256, top-8, H = 2048,
     I = 512, 8192 tokens) on sampled tokens.
@@ -15,7 +16,7 @@ import pytest
 import torch
 
 import oracle
-from _util import TOL_BF16, assert_close
+from _util import TOL_BF16, TOL_F32, assert_close, assert_close_moe_e2e
 from gguf_block_quantized_quantize_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -72,12 +73,17 @@ def test_gate_up_swiglu_bf16_and_q8_1(g):
     np.testing.assert_array_equal(hb[0], hb[2])
     hq = g.gguf_mul_mat_id(_u8(bank_gu), g.Q4_K, E, sgu, 2 * I, H, x.to(DEV), _u8(ids), g.GATE_UP_SWIGLU,
                            out_type=g.Q8_1).cpu().numpy()
-    d1, _, q1 = oracle.q8_1_fields(hq)
-    d0, _, q0 = oracle.q8_1_fields(hq_ref)
-    assert np.all(np.abs(q1.astype(int) - q0.astype(int))[active] <= 1)
-    dd1, dd0 = d1.view(np.float16).astype(np.float64), d0.view(np.float16).astype(np.float64)
-    assert np.all(np.abs(dd1 - dd0)[active] <= 0.02 * np.abs(dd0)[active] + 1e-12)
+    # The two h differ by the tensor-core rounding and at most one bf16 ulp
+    # (2^-7 relative); each q8_1 dequantization is within d/2 of its h.  So the
+    # dequantized values agree within d_gpu/2 + d_ref/2 + |h| 2^-7 + 2e-3 rms.
     assert np.all(hq[~active] == 0)
+    d1 = oracle.q8_1_fields(hq)[0].view(np.float16).astype(np.float64)
+    d0 = oracle.q8_1_fields(hq_ref)[0].view(np.float16).astype(np.float64)
+    v1 = oracle.dequantize_f64(oracle.Q8_1, hq, I)
+    v0 = oracle.dequantize_f64(oracle.Q8_1, hq_ref, I)
+    rms = np.sqrt((h_ref.astype(np.float64) ** 2).mean(axis=1, keepdims=True))
+    bound = (np.repeat(d1, 32, axis=1) + np.repeat(d0, 32, axis=1)) / 2 + np.abs(h_ref) * 2.0 ** -7 + 2e-3 * rms
+    assert np.all((np.abs(v1 - v0) <= bound * 1.0001)[active])
 
 
 def test_down_weighted_sum_from_oracle_h(g):
@@ -95,8 +101,8 @@ def test_down_weighted_sum_from_oracle_h(g):
     y = g.gguf_mul_mat_id(_u8(bank_d), g.Q6_K, E, sd, H, I, _u8(hq), _u8(ids), g.DOWN_WEIGHTED_SUM,
                           route_w=_u8(rw), xt=g.Q8_1, out_type=g.F32)
     assert y.shape == (T, H)
-    # the fp16 operand path: 3e-3 of the row rms for fp32 outputs (see test_gpu_mmq)
-    assert_close(y.cpu().numpy(), ref, 3e-3, "down weighted sum")
+    # fp32 output: the precise (hi + lo) operand mode
+    assert_close(y.cpu().numpy(), ref, TOL_F32, "down weighted sum")
 
 
 @pytest.mark.parametrize("safe", [False, True])
@@ -119,7 +125,7 @@ def test_moe_ffn_end_to_end_small(g, safe):
     y = g.gguf_moe_ffn(_u8(bank_gu), g.Q4_K, sgu, _u8(bank_d), g.Q6_K, sd, E, H, I, x.to(DEV), _u8(ids),
                        _u8(rw), dev_status=status)
     assert y.dtype == torch.bfloat16
-    assert_close(y.float().cpu().numpy(), ref, TOL_BF16, "moe ffn")
+    assert_close_moe_e2e(y.float().cpu().numpy(), ref, "moe ffn")
     assert int(status.item()) == 1
 
 
@@ -155,4 +161,56 @@ def test_moe_full_size_sampled(g):
         _, hq = oracle.moe_gate_up(oracle.Q4_K, bank_gu, E, sgu, 2 * I, H, xq, ids, routes=(t * K, t * K + K),
                                    nthreads=8)
         ref = oracle.moe_down(oracle.Q6_K, bank_d, E, sd, H, I, hq, ids, rw, tokens=(t, t + 1), nthreads=8)
-        assert_close(y[t:t + 1], ref[t:t + 1], TOL_BF16, f"moe token {t}")
+        assert_close_moe_e2e(y[t:t + 1], ref[t:t + 1], f"moe token {t}")
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_moe_ffn_q4_k_down_bank(g, out_dtype):
+    """Both banks Q4_K: the down GEMM needs the min-term correction columns of
+    the q8_1 intermediate; fp32 output runs the precise down product."""
+    E, K, H, T, I = 4, 2, 512, 23, 256
+    bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 800, False)
+    bank_d = _bank(oracle.Q4_K, E, H, I, 801, False)
+    sgu, sd = bank_gu.nbytes // E, bank_d.nbytes // E
+    ids, rw = synth.routes(T, E, K, seed=9)
+    ids[0] = [1, 1]
+    x = synth.activations(T, H, seed=10, dtype=torch.float32)
+    xq = oracle.quantize_q8_1(x.numpy())
+    _, hq = oracle.moe_gate_up(oracle.Q4_K, bank_gu, E, sgu, 2 * I, H, xq, ids)
+    ref = oracle.moe_down(oracle.Q4_K, bank_d, E, sd, H, I, hq, ids, rw)
+    out = torch.empty(T, H, dtype=out_dtype, device=DEV)
+    y = g.gguf_moe_ffn(_u8(bank_gu), g.Q4_K, sgu, _u8(bank_d), g.Q4_K, sd, E, H, I, x.to(DEV), _u8(ids), _u8(rw),
+                       out=out)
+    assert_close_moe_e2e(y.float().cpu().numpy(), ref, f"moe ffn q4_k down {out_dtype}")
+
+
+@pytest.mark.parametrize("out_type", ["f32", "bf16"])
+def test_down_q4_k_from_oracle_h(g, out_type):
+    """Q4_K down bank through the DOWN mode (q8_1 rows from the oracle): the
+    operand conversion appends the min-term correction columns."""
+    E, K, H, T, I = 4, 2, 512, 23, 256
+    bank_d = _bank(oracle.Q4_K, E, H, I, 801, False)
+    sd = bank_d.nbytes // E
+    ids, rw = synth.routes(T, E, K, seed=9)
+    ids[0] = [1, 1]
+    hq = oracle.quantize_q8_1(synth.normal((T * K, I), 1.0, seed=12))
+    ref = oracle.moe_down(oracle.Q4_K, bank_d, E, sd, H, I, hq, ids, rw)
+    yt = g.F32 if out_type == "f32" else g.BF16
+    y = g.gguf_mul_mat_id(_u8(bank_d), g.Q4_K, E, sd, H, I, _u8(hq), _u8(ids), g.DOWN_WEIGHTED_SUM,
+                          route_w=_u8(rw), xt=g.Q8_1, out_type=yt)
+    assert_close(y.float().cpu().numpy(), ref, TOL_F32 if yt == g.F32 else TOL_BF16, f"down q4_k {out_type}")
+
+
+def test_gate_up_h512(g):
+    E, K, H, T, I = 4, 2, 512, 23, 256
+    bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 800, False)
+    sgu = bank_gu.nbytes // E
+    ids, _ = synth.routes(T, E, K, seed=9)
+    x = synth.activations(T, H, seed=10, dtype=torch.float32)
+    h_ref, _ = oracle.moe_gate_up(oracle.Q4_K, bank_gu, E, sgu, 2 * I, H, oracle.quantize_q8_1(x.numpy()), ids)
+    hb = g.gguf_mul_mat_id(_u8(bank_gu), g.Q4_K, E, sgu, 2 * I, H, x.to(DEV), _u8(ids), g.GATE_UP_SWIGLU)
+    assert_close(hb.float().cpu().numpy(), h_ref, TOL_BF16, "gate_up H=512")
+    # precise gate_up: the bf16 h agrees bit for bit with the oracle's except
+    # near rounding ties (fp32 accumulation, ~1e-6 relative: ~0.1% of values)
+    same = (hb.float().cpu().numpy() == h_ref)
+    assert same.mean() > 0.995, same.mean()
