@@ -64,6 +64,7 @@ SIGNATURES = {
     "gguf_get_rows": (_i, [_p, _i, _i64, _i64, _p, _i64, _p, _i, _p]),
     "gguf_mul_mat_ws_size": (_sz, [_i, _i64, _i64, _i, _i64, _i]),
     "gguf_mul_mat": (_i, [_p, _i, _i64, _i64, _p, _i, _i64, _i64, _p, _i, _i64, _p, _sz, _p]),
+    "gguf_mul_mat_noalloc": (_i, [_p, _i, _i64, _i64, _p, _i, _i64, _i64, _p, _i, _i64, _p]),
     "gguf_mul_mat_id_ws_size": (_sz, [ctypes.POINTER(MoeArgs)]),
     "gguf_mul_mat_id": (_i, [ctypes.POINTER(MoeArgs), _p, _sz, _p]),
     "gguf_moe_ffn_ws_size": (_sz, [ctypes.POINTER(MoeFfnArgs)]),
@@ -183,6 +184,22 @@ def gguf_mul_mat(w: torch.Tensor, wt: int, n: int, k: int, x: torch.Tensor, xt: 
         ws = _workspace(need, x.device)
     _check(load_library().gguf_mul_mat(_ptr(w), wt, n, k, _ptr(x), xt, m, ldx, _ptr(out), _TYPE_OF[out.dtype],
                                        out.stride(0), _ptr(ws), 0 if ws is None else ws.numel(), _stream()))
+    return out
+
+
+def gguf_mul_mat_noalloc(w: torch.Tensor, wt: int, n: int, k: int, x: torch.Tensor,
+                         out: torch.Tensor | None = None, out_dtype=None) -> torch.Tensor:
+    """y[m, n] = x[m, k] @ W[n, k]^T for m <= 8, k <= 16384, with the q8_1
+    scratch in the library's fixed device array (no workspace, no allocation
+    inside the call; calls that overlap on one device race on the scratch)."""
+    xt = _TYPE_OF[x.dtype]
+    m = x.shape[0]
+    if out is None:
+        out = torch.empty((m, n), dtype=out_dtype or x.dtype, device=x.device)
+    if out.stride(1) != 1:
+        raise ValueError("gguf_mul_mat_noalloc: output rows must be contiguous")
+    _check(load_library().gguf_mul_mat_noalloc(_ptr(w), wt, n, k, _ptr(x), xt, m, x.stride(0), _ptr(out),
+                                               _TYPE_OF[out.dtype], out.stride(0), _stream()))
     return out
 
 

@@ -154,6 +154,30 @@ size_t gguf_mul_mat_ws_size(int wt, int64_t n, int64_t k, int xt, int64_t m, int
 gguf_status gguf_mul_mat(const void *w, int wt, int64_t n, int64_t k, const void *x, int xt, int64_t m,
                          int64_t ldx, void *y, int yt, int64_t ldy, void *ws, size_t ws_bytes, gguf_stream_t stream);
 
+/*
+ * gguf_mul_mat_noalloc -- gguf_mul_mat for decode-sized products (m <= 8 rows
+ * of float activations, k <= 16384), with no workspace argument and no device
+ * allocation.  The pages have no counterpart of this entry point: it is for
+ * callers that cannot hand over device memory at the call site, such as an
+ * engine that launches from inside its own memory-pool callbacks, or one whose
+ * allocator is not reachable from the code that issues the matmul.  The q8_1
+ * copy of x lives in a fixed 256 KB device array inside this library instead
+ * (m * k/32 * 36 bytes are used: 147,456 at the limits).
+ *
+ * Arguments, layouts and output are those of gguf_mul_mat with xt in
+ * {F32, BF16, F16}; the result is the same MMVQ computation that gguf_mul_mat
+ * runs for these sizes under the default options.
+ * Errors: GGUF_ERR_WORKSPACE when m > 8 or k > 16384 (use gguf_mul_mat);
+ * otherwise as gguf_mul_mat.  Nothing has to be cleared between calls: every
+ * scratch byte that is read was written by the same call.
+ * The first call on each device looks up the scratch address; make it before
+ * any stream capture.  The scratch is shared by every caller on the device:
+ * calls that overlap in time (other streams, other host threads) race on it
+ * and must be serialized by the caller.
+ */
+gguf_status gguf_mul_mat_noalloc(const void *w, int wt, int64_t n, int64_t k, const void *x, int xt, int64_t m,
+                                 int64_t ldx, void *y, int yt, int64_t ldy, gguf_stream_t stream);
+
 /* mul_mat_id modes */
 #define GGUF_MOE_GATE_UP_SWIGLU 0   /* h[r] = silu(gate) * up, rounded to bf16, out as BF16 or Q8_1 */
 #define GGUF_MOE_DOWN_WEIGHTED_SUM 1 /* y[t] = sum_k route_w[t][k] * (W[e] . x[route]) */
