@@ -2,14 +2,19 @@
 
 Default workload (one "step"): the decode MMVQ configuration -- Q4_K weights of
 shape 4096 x 4096 and 14336 x 4096, bf16 activations with M in {1, 2, 4, 8};
-each of the 8 products runs the whole path (bf16 -> q8_1 quantization, then the
-MMVQ kernel) through the library's C ABI.  The metric is the HBM bandwidth of
+for each M the activations are quantized once (bf16 -> q8_1) and both weight
+matrices run the MMVQ kernel on that copy, all through the library's C ABI.  The metric is the HBM bandwidth of
 the path in GB/s: algorithmic bytes (packed weights + activations + q8_1 +
 outputs; the weights are >99% of them) / step time.  Weight copies rotate so
 that no launch finds its weights in L2 (the rotation set is > 4x L2).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload decode|mmq|moe|llama]
+                  [--no-secondary] [--no-cpu-baseline]
+
+Beside the headline, the line carries "secondary" results measured in the same
+run: the Q8_0 512x1024 product, the two prefill MMQ products (TOPS), the MoE
+FFN (TOPS on routed rows) and a Llama-3.2-3B-shaped decode step of all 196
+linears plus the tied LM head at M = 1, 8, 32 (GB/s of weights).
 
 Under torchrun each rank runs the same per-GPU workload (replicas, weak
 scaling); rank 0 prints one JSON line with the whole-job value.
@@ -100,7 +105,7 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------
-# decode workload (MMVQ)
+# decode workload (MMVQ) -- the headline
 # --------------------------------------------------------------------------
 
 def _l2_bytes(torch):
@@ -110,36 +115,89 @@ def _l2_bytes(torch):
         return 126 * 2 ** 20
 
 
-def decode_setup(torch, g, synth, dev):
-    """Weight copies (random-but-safe Q4_K blocks), activations and outputs."""
-    l2 = _l2_bytes(torch)
-    plan = []
-    pools = {}
-    for (n, k) in DECODE_SHAPES:
-        rb = g.gguf_row_size(g.Q4_K, k)
-        nbytes = n * rb
-        copies = max(4, -(-4 * l2 // nbytes))
-        base = torch.from_numpy(synth.safe_blocks(g.Q4_K, n, k, seed=n)).to(dev)
-        pool = torch.empty((copies, n, rb), dtype=torch.uint8, device=dev)
-        for c in range(copies):
-            pool[c].copy_(base)
-        pools[(n, k)] = pool
-    xs, ys = {}, {}
-    for (n, k) in DECODE_SHAPES:
+class Decode:
+    """Q4_K 4096x4096 and 14336x4096 with bf16 activations, M in {1, 2, 4, 8}.
+
+    One step quantizes each M's activations once (bf16 -> q8_1) and runs both
+    weight matrices on that q8_1 copy (the quantization is shared by every
+    weight that reads the same activations).  Weight copies rotate over more
+    than 4x L2 per shape, so no launch finds its weights in L2."""
+
+    def __init__(self, torch, g, synth, dev):
+        self.g = g
+        l2 = _l2_bytes(torch)
+        self.pools, self.counters = {}, {}
+        for (n, k) in DECODE_SHAPES:
+            rb = g.gguf_row_size(g.Q4_K, k)
+            copies = max(4, -(-4 * l2 // (n * rb)))
+            base = torch.from_numpy(synth.safe_blocks(g.Q4_K, n, k, seed=n)).to(dev)
+            pool = torch.empty((copies, n, rb), dtype=torch.uint8, device=dev)
+            for c in range(copies):
+                pool[c].copy_(base)
+            self.pools[(n, k)] = pool
+            self.counters[(n, k)] = 0
+        k = DECODE_SHAPES[0][1]
+        self.k = k
+        self.xs = {m: synth.activations(m, k, seed=100 + m, dtype=torch.bfloat16).to(dev) for m in DECODE_MS}
+        self.xqs = {m: torch.empty((m, g.gguf_row_size(g.Q8_1, k)), dtype=torch.uint8, device=dev) for m in DECODE_MS}
+        self.ys = {(n, m): torch.empty((m, n), dtype=torch.bfloat16, device=dev) for (n, _) in DECODE_SHAPES
+                   for m in DECODE_MS}
+        self.n_phase = max(p.shape[0] for p in self.pools.values())
+
+    def weight(self, n, k):
+        pool = self.pools[(n, k)]
+        c = self.counters[(n, k)]
+        self.counters[(n, k)] = (c + 1) % pool.shape[0]
+        return pool[c]
+
+    def step(self, quantize=True, xs=None):
+        g = self.g
+        xs = self.xs if xs is None else xs
         for m in DECODE_MS:
-            xs[(n, k, m)] = synth.activations(m, k, seed=100 + m, dtype=torch.bfloat16).to(dev)
-            ys[(n, k, m)] = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-            plan.append((n, k, m))
-    ws = torch.empty(g.gguf_mul_mat_ws_size(g.Q4_K, 14336, 4096, g.BF16, 8) + 4096, dtype=torch.uint8, device=dev)
-    xqs = {key: torch.empty((key[2], g.gguf_row_size(g.Q8_1, key[1])), dtype=torch.uint8, device=dev) for key in plan}
-    return plan, pools, xs, ys, ws, xqs
+            if quantize:
+                g.gguf_quantize_q8_1(xs[m], out=self.xqs[m])
+            for (n, k) in DECODE_SHAPES:
+                g.gguf_mul_mat(self.weight(n, k), g.Q4_K, n, k, self.xqs[m], xt=g.Q8_1, m=m, out=self.ys[(n, m)])
+
+    def launches_per_step(self, quantize=True):
+        return len(DECODE_MS) * (len(DECODE_SHAPES) + (1 if quantize else 0))
+
+    def bytes_per_step(self):
+        """Algorithmic bytes: packed weights + bf16 x read + q8_1 write + q8_1 read per product + y write."""
+        g, k = self.g, self.k
+        tot = wts = mmvq = 0
+        for m in DECODE_MS:
+            xq = m * g.gguf_row_size(g.Q8_1, k)
+            tot += m * k * 2 + xq
+            for (n, _) in DECODE_SHAPES:
+                w = n * g.gguf_row_size(g.Q4_K, k)
+                tot += w + xq + m * n * 2
+                wts += w
+                mmvq += w + xq + m * n * 2
+        return tot, wts, mmvq
 
 
-def decode_bytes(g, n, k, m):
-    w = n * g.gguf_row_size(g.Q4_K, k)
-    xq = m * g.gguf_row_size(g.Q8_1, k)
-    return {"weights": w, "x_bf16": m * k * 2, "xq_write": xq, "xq_read": xq, "y": m * n * 2,
-            "mmvq": w + xq + m * n * 2}
+def _capture(torch, stream, fn, count):
+    graphs = []
+    for _ in range(count):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            fn()
+        graphs.append(gr)
+    return graphs
+
+
+def _time_graphs(torch, stream, graphs, reps, warm=3):
+    with torch.cuda.stream(stream):
+        for i in range(warm):
+            graphs[i % len(graphs)].replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(reps):
+            graphs[i % len(graphs)].replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
 
 
 def run_ours(args, rank, world, torch, dev):
@@ -147,52 +205,19 @@ def run_ours(args, rank, world, torch, dev):
     from gguf_block_quantized_quantize_gb300 import synth
 
     g.load_library()
-    hbm_peak, _, peak_kind = _peaks()
-    plan, pools, xs, ys, ws, xqs = decode_setup(torch, g, synth, dev)
-    counters = {key: 0 for key in pools}
-
-    def weight(n, k):
-        pool = pools[(n, k)]
-        c = counters[(n, k)]
-        counters[(n, k)] = (c + 1) % pool.shape[0]
-        return pool[c]
-
-    # one step = 8 products, each quantize + MMVQ through the C ABI
-    def step():
-        for (n, k, m) in plan:
-            g.gguf_mul_mat(weight(n, k), g.Q4_K, n, k, xs[(n, k, m)], out=ys[(n, k, m)], ws=ws)
-
-    # the MMVQ kernels alone (pre-quantized q8_1 input), for the roofline
-    for (n, k, m) in plan:
-        g.gguf_quantize_q8_1(xs[(n, k, m)], out=xqs[(n, k, m)])
-
-    def mmvq_only():
-        for (n, k, m) in plan:
-            g.gguf_mul_mat(weight(n, k), g.Q4_K, n, k, xqs[(n, k, m)], xt=g.Q8_1, m=m, out=ys[(n, k, m)])
-
+    hbm_peak, tf_peak, peak_kind = _peaks()
     stream = torch.cuda.Stream()
-    torch.cuda.synchronize()
-    # CUDA graphs: one graph per rotation phase so that every replay reads new copies
-    n_phase = max(p.shape[0] for p in pools.values())
-    graphs, mgraphs = [], []
     with torch.cuda.stream(stream):
+        dec = Decode(torch, g, synth, dev)
         for _ in range(2):   # warm the launch path before capture
-            step()
-        torch.cuda.synchronize()
-        for i in range(min(n_phase, 8)):
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=stream):
-                step()
-            graphs.append(gr)
-        for i in range(min(n_phase, 8)):
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=stream):
-                mmvq_only()
-            mgraphs.append(gr)
+            dec.step()
     torch.cuda.synchronize()
-
-    per_step = sum(sum(v for kk, v in decode_bytes(g, n, k, m).items() if kk in ("weights", "x_bf16", "xq_write", "xq_read", "y")) for (n, k, m) in plan)
-    weight_bytes = sum(decode_bytes(g, n, k, m)["weights"] for (n, k, m) in plan)
+    nph = min(dec.n_phase, 8)
+    with torch.cuda.stream(stream):
+        graphs = _capture(torch, stream, dec.step, nph)
+        mgraphs = _capture(torch, stream, lambda: dec.step(quantize=False), nph)
+    torch.cuda.synchronize()
+    per_step, weight_bytes, mmvq_bytes = dec.bytes_per_step()
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -210,46 +235,31 @@ def run_ours(args, rank, world, torch, dev):
         ev1.record(stream)
     torch.cuda.synchronize()
     ms_total = ev0.elapsed_time(ev1)
-    # dominant kernel: MMVQ launches alone, same stream, same rotation
-    reps = max(args.steps, 20)
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            mgraphs[i % len(mgraphs)].replay()
-        m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        m0.record(stream)
-        for i in range(reps):
-            mgraphs[i % len(mgraphs)].replay()
-        m1.record(stream)
-    torch.cuda.synchronize()
+    # the dominant kernel alone (MMVQ on the same q8_1 inputs, same rotation, same stream)
+    ms_mmvq_step = _time_graphs(torch, stream, mgraphs, max(args.steps, 20))
     clk = clocks.stop()
-    ms_mmvq = m0.elapsed_time(m1) / (reps * len(plan))
+    n_mmvq = len(DECODE_MS) * len(DECODE_SHAPES)
+    ms_mmvq = ms_mmvq_step / n_mmvq
     ms_total = _max_over_ranks(ms_total, world, torch, dev)
     ms_step = ms_total / args.steps
     value = per_step * world / (ms_step * 1e-3) / 1e9
-    mmvq_bytes = sum(decode_bytes(g, n, k, m)["mmvq"] for (n, k, m) in plan) / len(plan)
-    achieved = mmvq_bytes / (ms_mmvq * 1e-3) / 1e9
+    achieved = (mmvq_bytes / n_mmvq) / (ms_mmvq * 1e-3) / 1e9
 
-    # per-shape detail: each (shape, m) MMVQ alone
+    # per (shape, M) detail: each MMVQ alone, 16 launches per graph
     detail = []
-    for (n, k, m) in plan:
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(gr, stream=stream):
+    for m in DECODE_MS:
+        for (n, k) in DECODE_SHAPES:
+            def one(n=n, k=k, m=m):
                 for _ in range(16):
-                    g.gguf_mul_mat(weight(n, k), g.Q4_K, n, k, xqs[(n, k, m)], xt=g.Q8_1, m=m, out=ys[(n, k, m)])
-            gr.replay()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(5):
-                gr.replay()
-            b.record(stream)
-        torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / 80
-        by = decode_bytes(g, n, k, m)["mmvq"]
-        detail.append({"n": n, "k": k, "m": m, "us": round(us, 3), "gbs": round(by / us / 1e3, 1),
-                       "frac": round(by / us / 1e3 / hbm_peak, 3)})
+                    g.gguf_mul_mat(dec.weight(n, k), g.Q4_K, n, k, dec.xqs[m], xt=g.Q8_1, m=m, out=dec.ys[(n, m)])
+            with torch.cuda.stream(stream):
+                gr = _capture(torch, stream, one, 1)
+            us = _time_graphs(torch, stream, gr, 5, warm=1) * 1e3 / 16
+            by = n * g.gguf_row_size(g.Q4_K, k) + m * g.gguf_row_size(g.Q8_1, k) + m * n * 2
+            detail.append({"n": n, "k": k, "m": m, "us": round(us, 3), "gbs": round(by / us / 1e3, 1),
+                           "frac": round(by / us / 1e3 / hbm_peak, 3)})
 
-    e2e = run_e2e(args, g, torch, dev, plan, xs, ys, weight, per_step, ws)
+    e2e = run_e2e(args, g, torch, dev, dec, per_step)
 
     result = {
         "metric": "GGUF matmul: weight-read HBM GB/s (MMVQ) and int8 TOPS (MMQ/MoE) on 1 GB300",
@@ -257,38 +267,47 @@ def run_ours(args, rank, world, torch, dev):
         "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u8", "data": "synthetic",
         "config": {"workload": "decode MMVQ: Q4_K 4096x4096 and 14336x4096, bf16 activations M in {1,2,4,8}; "
-                               "step = 8 x (bf16->q8_1 quantize + MMVQ)",
+                               "step = per M one bf16->q8_1 quantize shared by the two MMVQ products",
                    "l2": "weight copies rotate over >4x L2 per shape (inputs larger than L2)",
                    "weights": "random-but-safe packed Q4_K blocks", "parallelism": f"replicas x{world}"},
         "weight_bytes_per_step": weight_bytes, "bytes_per_step": per_step,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": None, "kernel": "mmvq_kernel (Q4_K)",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": MMVQ_TRAFFIC,
+                     "kernel": "mmvq_kernel<Q4KPiece> (8 launches per step, mean)",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "detail": detail,
-        "gpu_launches": args.steps * 2 * len(plan),
+        "gpu_launches": args.steps * dec.launches_per_step(),
         "clocks": clk,
         "e2e": e2e,
     }
+    if not args.no_secondary:
+        result["secondary"] = secondary(torch, g, synth, dev, stream, hbm_peak, tf_peak, peak_kind)
     return result
 
 
-def run_e2e(args, g, torch, dev, plan, xs, ys, weight, per_step, ws):
-    """Same workload through the public API with host buffers: the step's
-    activations are copied from pinned host memory and its outputs read back."""
-    hx = {key: xs[key].cpu().pin_memory() for key in plan}
-    hy = {key: torch.empty(ys[key].shape, dtype=ys[key].dtype).pin_memory() for key in plan}
-    dx = {key: torch.empty_like(xs[key]) for key in plan}
+# Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# decode MMVQ launches, averaged over the step's 8 launches, from the ncu
+# capture summarized in profiles/mmvq_q4_k_decode.md (set to None whenever the
+# kernel changes, until it is captured again).
+MMVQ_TRAFFIC = 21271840
+
+
+def run_e2e(args, g, torch, dev, dec, per_step):
+    """Same workload through the public API with host buffers: each step copies
+    its activations from pinned host memory and reads its outputs back."""
+    hx = {m: dec.xs[m].cpu().pin_memory() for m in DECODE_MS}
+    hy = {key: torch.empty(y.shape, dtype=y.dtype).pin_memory() for key, y in dec.ys.items()}
+    dx = {m: torch.empty_like(dec.xs[m]) for m in DECODE_MS}
     stream = torch.cuda.Stream()
-    h2d = sum(hx[k].numel() * hx[k].element_size() for k in plan)
-    d2h = sum(hy[k].numel() * hy[k].element_size() for k in plan)
+    h2d = sum(t.numel() * t.element_size() for t in hx.values())
+    d2h = sum(t.numel() * t.element_size() for t in hy.values())
 
     def step():
-        for key in plan:
-            dx[key].copy_(hx[key], non_blocking=True)
-        for (n, k, m) in plan:
-            g.gguf_mul_mat(weight(n, k), g.Q4_K, n, k, dx[(n, k, m)], out=ys[(n, k, m)], ws=ws)
-        for key in plan:
-            hy[key].copy_(ys[key], non_blocking=True)
+        for m in DECODE_MS:
+            dx[m].copy_(hx[m], non_blocking=True)
+        dec.step(xs=dx)
+        for key in dec.ys:
+            hy[key].copy_(dec.ys[key], non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -303,6 +322,156 @@ def run_e2e(args, g, torch, dev, plan, xs, ys, weight, per_step, ws):
     ms = a.elapsed_time(b) / args.steps
     return {"value": round(per_step / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5)}
+
+
+# --------------------------------------------------------------------------
+# secondary workloads (reported beside the headline, not part of its step)
+# --------------------------------------------------------------------------
+
+def _time_eager(torch, stream, fn, reps, flush=None, warm=2):
+    """Mean device time of fn() over reps calls, CUDA events on `stream` around
+    each call only; `flush` (an L2-sized write) runs between calls, untimed."""
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            fn()
+        evs = []
+        for _ in range(reps):
+            if flush is not None:
+                flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / reps
+
+
+def secondary(torch, g, synth, dev, stream, hbm_peak, tf_peak, peak_kind):
+    out = {}
+    l2 = _l2_bytes(torch)
+    scrub = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def flush():
+        scrub.fill_(1)
+
+    def u8(a):
+        return torch.from_numpy(a).to(dev)
+
+    with torch.cuda.stream(stream):
+        # Q8_0 512 x 1024, fp32 activations M = 8, fp32 out (a few hundred KB: launch-latency bound)
+        n, k, m = 512, 1024, 8
+        w = u8(synth.safe_blocks(g.Q8_0, n, k, seed=1))
+        x = synth.activations(m, k, seed=2, dtype=torch.float32).to(dev)
+        y = torch.empty((m, n), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(g.gguf_mul_mat_ws_size(g.Q8_0, n, k, g.F32, m, g.F32), 16), dtype=torch.uint8, device=dev)
+        ms = _time_eager(torch, stream, lambda: g.gguf_mul_mat(w, g.Q8_0, n, k, x, out=y, ws=ws), 20, flush)
+        out["q8_0_512x1024_m8_f32"] = {"us": round(ms * 1e3, 2), "note": "quantize + MMVQ, L2 flushed between calls"}
+        del w
+
+        # prefill MMQ: Q4_K 8192x2048 @ 8192 bf16 tokens, Q6_K 248320x2048 @ 2048, bf16 out
+        for name, wt, n, k, m in (("mmq_q4_k_8192x2048_m8192", g.Q4_K, 8192, 2048, 8192),
+                                  ("mmq_q6_k_248320x2048_m2048", g.Q6_K, 248320, 2048, 2048)):
+            w = synth.safe_blocks_device(wt, n, k, seed=n, device=dev)
+            x = synth.activations(m, k, seed=3, dtype=torch.bfloat16).to(dev)
+            y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(max(g.gguf_mul_mat_ws_size(wt, n, k, g.BF16, m, g.BF16), 16), dtype=torch.uint8,
+                             device=dev)
+            ms = _time_eager(torch, stream, lambda: g.gguf_mul_mat(w, wt, n, k, x, out=y, ws=ws), 5, flush)
+            tops = 2.0 * m * n * k / (ms * 1e-3) / 1e12
+            out[name] = {"ms": round(ms, 4), "tops": round(tops, 1),
+                         "roofline": {"bound": "tensor", "achieved": round(tops, 1), "peak": tf_peak,
+                                      "unit": "TFLOP/s", "frac": round(tops / tf_peak, 4),
+                                      "note": f"fp16 tcgen05 MMA; peak = {peak_kind} bf16 (same rate as fp16)"}}
+            del w, x, y, ws
+
+        # MoE FFN: E=256, top-8, H=2048, I=512, 8192 bf16 tokens; gate_up Q4_K, down Q6_K
+        E, H, I, T, K_ = 256, 2048, 512, 8192, 8
+        wgu = synth.safe_blocks_device(g.Q4_K, E * 2 * I, H, seed=5, device=dev)
+        wdn = synth.safe_blocks_device(g.Q6_K, E * H, I, seed=6, device=dev)
+        ids_np, rw_np = synth.routes(T, E, K_, seed=7)
+        ids, rw = torch.from_numpy(ids_np).to(dev), torch.from_numpy(rw_np).to(dev)
+        x = synth.activations(T, H, seed=8, dtype=torch.bfloat16).to(dev)
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        gu_stride, dn_stride = 2 * I * g.gguf_row_size(g.Q4_K, H), H * g.gguf_row_size(g.Q6_K, I)
+        args = g.moe_ffn_args(wgu, g.Q4_K, gu_stride, wdn, g.Q6_K, dn_stride, E, H, I, x, g.BF16, ids, K_, rw, y,
+                              g.BF16, None)
+        ws = torch.empty(max(g.gguf_moe_ffn_ws_size(args), 16), dtype=torch.uint8, device=dev)
+
+        def moe():
+            g.gguf_moe_ffn(wgu, g.Q4_K, gu_stride, wdn, g.Q6_K, dn_stride, E, H, I, x, ids, rw, out=y, ws=ws)
+        ms = _time_eager(torch, stream, moe, 5, flush)
+        ops = 2.0 * T * K_ * (2 * I * H + H * I)
+        out["moe_ffn_e256_top8_h2048_i512_t8192"] = {
+            "ms": round(ms, 4), "tops": round(ops / (ms * 1e-3) / 1e12, 1),
+            "note": "routed-row int8-equivalent ops 2*T*top_k*(2I*H + H*I) / time; gate_up Q4_K + SwiGLU + q8_1, "
+                    "down Q6_K + weighted sum"}
+        del wgu, wdn, x, y, ws
+
+        # Llama-3.2-3B-shaped decode step: 28 layers of q/k/o/gate/up (Q4_K) and v/down (Q6_K), tied
+        # Q6_K embedding / LM head 128256 x 3072 via get_rows + MMVQ; all linears at M in {1, 8, 32}
+        out["llama32_3b_decode_linears"] = llama_decode(torch, g, synth, dev, stream, hbm_peak)
+    torch.cuda.synchronize()
+    return out
+
+
+def llama_decode(torch, g, synth, dev, stream, hbm_peak):
+    L, D, F, V, KV = 28, 3072, 8192, 128256, 1024
+    Q4, Q6 = g.Q4_K, g.Q6_K
+    layer_shapes = [("q", Q4, D, D), ("k", Q4, KV, D), ("v", Q6, KV, D), ("o", Q4, D, D),
+                    ("gate", Q4, F, D), ("up", Q4, F, D), ("down", Q6, D, F)]
+    layers = []
+    seed = 1000
+    for _ in range(L):
+        ly = {}
+        for nm, wt, n, k in layer_shapes:
+            ly[nm] = synth.safe_blocks_device(wt, n, k, seed=seed, device=dev)
+            seed += 1
+        layers.append(ly)
+    emb = synth.safe_blocks_device(Q6, V, D, seed=seed, device=dev)
+    wbytes = sum(t.numel() for ly in layers for t in ly.values()) + emb.numel()
+    res = []
+    for m in (1, 8, 32):
+        ids = torch.randint(0, V, (m,), dtype=torch.int32, device=dev)
+        h = torch.empty((m, D), dtype=torch.bfloat16, device=dev)
+        act_d = synth.activations(m, D, seed=m, dtype=torch.bfloat16).to(dev)
+        act_f = synth.activations(m, F, seed=m + 1, dtype=torch.bfloat16).to(dev)
+        xq_d = torch.empty((m, g.gguf_row_size(g.Q8_1, D)), dtype=torch.uint8, device=dev)
+        xq_f = torch.empty((m, g.gguf_row_size(g.Q8_1, F)), dtype=torch.uint8, device=dev)
+        outs = {nm: torch.empty((m, n), dtype=torch.bfloat16, device=dev) for nm, _, n, _ in layer_shapes}
+        logits = torch.empty((m, V), dtype=torch.bfloat16, device=dev)
+        wsz = max(g.gguf_mul_mat_ws_size(wt, n, k, g.Q8_1, m, g.BF16) for _, wt, n, k in layer_shapes)
+        wsz = max(wsz, g.gguf_mul_mat_ws_size(Q6, V, D, g.Q8_1, m, g.BF16), 16)
+        ws = torch.empty(wsz, dtype=torch.uint8, device=dev)
+
+        def mm(w, wt, n, k, xq, out):
+            g.gguf_mul_mat(w, wt, n, k, xq, xt=g.Q8_1, m=m, out=out, ws=ws)
+
+        def step():
+            g.gguf_get_rows(emb, Q6, V, D, ids, out=h)           # token embedding rows
+            for ly in layers:
+                g.gguf_quantize_q8_1(act_d, out=xq_d)              # attention input, shared by q, k, v
+                for nm in ("q", "k", "v"):
+                    _, wt, n, k = next(s for s in layer_shapes if s[0] == nm)
+                    mm(ly[nm], wt, n, k, xq_d, outs[nm])
+                g.gguf_quantize_q8_1(act_d, out=xq_d)              # attention output
+                mm(ly["o"], Q4, D, D, xq_d, outs["o"])
+                g.gguf_quantize_q8_1(act_d, out=xq_d)              # FFN input, shared by gate and up
+                mm(ly["gate"], Q4, F, D, xq_d, outs["gate"])
+                mm(ly["up"], Q4, F, D, xq_d, outs["up"])
+                g.gguf_quantize_q8_1(act_f, out=xq_f)              # FFN hidden
+                mm(ly["down"], Q6, D, F, xq_f, outs["down"])
+            g.gguf_quantize_q8_1(act_d, out=xq_d)
+            mm(emb, Q6, V, D, xq_d, logits)                        # tied LM head
+
+        step()
+        torch.cuda.synchronize()
+        gr = _capture(torch, stream, step, 1)
+        ms = _time_graphs(torch, stream, gr, 10, warm=2)
+        gbs = wbytes / (ms * 1e-3) / 1e9
+        res.append({"m": m, "ms": round(ms, 4), "weight_gb": round(wbytes / 1e9, 3), "gbs": round(gbs, 1),
+                    "frac": round(gbs / hbm_peak, 3), "path": "MMVQ" if m <= 8 else "MMQ"})
+    return res
 
 
 # --------------------------------------------------------------------------
@@ -375,6 +544,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the MMQ / MoE / Llama-shaped results")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -3,8 +3,8 @@
 
 namespace gg {
 
-// One 32-value piece per thread: K <= 32 * 512 = 16384 (longer rows take the
-// tensor-core path, which has no K limit).
+// One piece per thread and at most 512 threads per CTA: K <= 16384 (longer
+// rows take the tensor-core path, which has no K limit).
 constexpr int64_t MMVQ_MAX_PIECES = 512;
 
 cudaError_t launch_mmvq(const uint8_t *w, int wt, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y,

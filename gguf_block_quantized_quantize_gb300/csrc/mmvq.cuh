@@ -11,24 +11,24 @@
 // GB300 design.  The kernel is bound by the HBM read of the packed weights
 // (transformers PR #45977 "GgufLinear ...", section "What made it fast": a
 // bandwidth-bound decode), so every weight byte is read exactly once, with
-// coalesced loads, and all compute hides under those loads:
-//   * K is split across the threads of a CTA: thread t owns the 32-value
-//     "pieces" t, t + blockDim, ... of every row.  Its q8_1 activation quants
-//     for those pieces (all m rows) are loaded once into registers and reused
-//     for every weight row the CTA visits, so activations cost no bandwidth in
-//     the row loop.
-//   * A persistent grid (a few CTAs per SM) walks the rows R at a time; the R
-//     rows' loads are issued together to keep enough bytes in flight.
+// coalesced loads, and the arithmetic per byte is kept small enough to hide
+// under those loads:
+//   * K is split across the threads of a CTA: thread t owns "piece" t of every
+//     row (64 values for Q4_K / Q6_K, 32 for Q8_0).  Its q8_1 activation quants
+//     for that piece are loaded once into registers and reused for every row
+//     the CTA visits, so activations cost no bandwidth in the row loop.  For
+//     8 tokens, two threads share a piece and take 4 tokens each, which halves
+//     the activation registers.
+//   * A persistent grid (as many CTAs as fit on the SMs) walks the rows R at a
+//     time.  The weights of the next R rows are loaded into registers before
+//     the current R rows are computed (two register sets used in turn), so a
+//     load is always in flight; the first rows are requested before the kernel
+//     waits for the kernel that produced the activations (programmatic
+//     dependent launch).
 //   * Per-piece int32 sums use dp4a; partial sums of the R x M outputs are
-//     reduced with a butterfly (one shuffle per value and level) and then
-//     across warps through shared memory.
-// Piece p of a row (32 values):
-//   Q8_0: block p.
-//   Q4_K: super-block p/8, 16 quant bytes at chunk c = (p%8)/2, half h = p%2:
-//         values [64c+16h, +16) (low nibbles, sub-block 2c) and
-//         [64c+32+16h, +16) (high nibbles, sub-block 2c+1).
-//   Q6_K: super-block p/8, half h = (p%8)/4, l0 = 8*(p%4): the runs
-//         [128h + 32g + l0, +8) for g = 0..3.
+//     reduced with a butterfly (one shuffle per value and level) and across
+//     warps through shared memory in a fixed order, so results are
+//     deterministic.
 #pragma once
 
 #include "common.cuh"
@@ -37,6 +37,14 @@
 
 namespace gg {
 
+// ---------------------------------------------------------------- 32-value pieces
+// Piece p of a row (32 values):
+//   Q8_0: block p.
+//   Q4_K: super-block p/8, 16 quant bytes at chunk c = (p%8)/2, half h = p%2:
+//         values [64c+16h, +16) (low nibbles, sub-block 2c) and
+//         [64c+32+16h, +16) (high nibbles, sub-block 2c+1).
+//   Q6_K: super-block p/8, half h = (p%8)/4, l0 = 8*(p%4): the runs
+//         [128h + 32g + l0, +8) for g = 0..3.
 template <int M>
 struct ActPiece {
     int q[M][8];      // activation quants of the piece, 4 per word, in piece order
@@ -259,229 +267,420 @@ __device__ __forceinline__ float butterfly(float (&v)[V], int lane) {
     return r;
 }
 
-// Streaming design.  A CTA owns the contiguous rows [r0, r1) of W, which are
-// one contiguous byte range in HBM.  One thread streams that range through a
-// ring of NS shared-memory stages with TMA bulk copies (cp.async.bulk), so
-// tens of KB per CTA are in flight no matter how many registers the compute
-// warps use; the compute threads read their piece of each row from shared
-// memory.  Stage c holds rows [r0 + c*SR, r0 + (c+1)*SR) (SR = G*R rows, G
-// sub-groups of R rows); the copy starts at the 16-byte boundary at or below
-// the stage's first byte, so shared memory keeps each byte's address modulo 16
-// and the same aligned loads work on it.  A tail that ends off a 16-byte
-// boundary at the very end of the view is copied byte by byte (never past the
-// view).  Per-row results go to shared-memory accumulators with atomics, so
-// no block barrier sits in the row loop.
-constexpr int MMVQ_STAGES = 4;
 
-struct MmvqShape {
-    int64_t rows_per_cta;
-    int sub_groups;  // G
-    int stage_bytes;
-};
 
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(tc::smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
-                 : "memory");
-}
-
-template <int WT, int M, int R, int MAXT>
-__global__ void __launch_bounds__(MAXT) mmvq_kernel(const uint8_t *__restrict__ w, int64_t n, int64_t k, int64_t rb,
-                                                   const uint8_t *__restrict__ xq, int m_act, void *__restrict__ y,
-                                                   int yt, int64_t ldy, MmvqShape shp) {
-    constexpr int V = R * M;
-    constexpr int LOG = V == 1 ? 0 : V == 2 ? 1 : V == 4 ? 2 : V == 8 ? 3 : V == 16 ? 4 : 5;
-    static_assert((1 << LOG) == V && V <= 32, "R*M must be a power of two <= 32");
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    const int SB = shp.stage_bytes;  // multiple of 16
-    uint8_t *stage = smem_raw;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw + MMVQ_STAGES * SB);
-    uint64_t *empty = full + MMVQ_STAGES;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + MMVQ_STAGES);
-    float *s_acc = reinterpret_cast<float *>(empty + MMVQ_STAGES + 2);  // [rows_per_cta][M]
-
-    const int tid = threadIdx.x, lane = tid & 31, nwarps = blockDim.x >> 5;
-    const int64_t P = k / 32;
-    const int64_t xrb = P * Q8_1_BYTES;
-    const int64_t r0 = (int64_t)blockIdx.x * shp.rows_per_cta;
-    const int64_t r1 = r0 + shp.rows_per_cta < n ? r0 + shp.rows_per_cta : n;
-    const int64_t SR = (int64_t)shp.sub_groups * R;
-    const int nst = (int)((r1 - r0 + SR - 1) / SR);  // stages of this CTA
-    const int64_t piece = tid;
-    const bool valid = piece < P;
-    const uintptr_t wbase = reinterpret_cast<uintptr_t>(w);
-    const uintptr_t wend = wbase + (uintptr_t)(n * rb);
-
-    if (tid == 0) {
-        for (int s = 0; s < MMVQ_STAGES; s++) {
-            tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], nwarps);
-        }
-        *abort_flag = 0;
-        tc::fence_barrier_init();
-    }
-    __syncthreads();
-    // the next kernel on the stream may launch now; weights never change, so
-    // their streaming starts before waiting for the previous kernel
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-    // stage c: byte range [g0, g1) of the view, copied from a16 = g0 rounded down to 16
-    auto issue = [&](int c) {
-        const int s = c % MMVQ_STAGES;
-        const int64_t ra = r0 + (int64_t)c * SR;
-        const int64_t rz = ra + SR < r1 ? ra + SR : r1;
-        const uintptr_t g0 = wbase + (uintptr_t)(ra * rb), g1 = wbase + (uintptr_t)(rz * rb);
-        const uintptr_t a16 = g0 & ~uintptr_t(15);
-        const uintptr_t b16 = (g1 + 15) & ~uintptr_t(15);
-        const uintptr_t bulk_end = b16 <= wend ? b16 : (wend & ~uintptr_t(15));
-        uint8_t *dst = stage + s * SB;
-        const uint32_t bytes = (uint32_t)(bulk_end - a16);
-        // the view's last bytes when it does not end on a 16-byte boundary
-        // (written before the arrive below publishes the stage)
-        for (uintptr_t p = bulk_end; p < g1; p++) dst[p - a16] = *reinterpret_cast<const uint8_t *>(p);
-        tc::mbar_arrive_expect_tx(&full[s], bytes);
-        if (bytes) bulk_g2s(dst, reinterpret_cast<const void *>(a16), bytes, &full[s]);
-    };
-    if (tid == 0) {
-        for (int c = 0; c < MMVQ_STAGES && c < nst; c++) issue(c);
-    }
-
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int i = tid; i < shp.rows_per_cta * M; i += blockDim.x) s_acc[i] = 0.0f;
-    ActPiece<M> act;
-    load_act<WT, M>(act, xq, xrb, m_act, valid ? piece : 0, valid);
-    __syncthreads();
-
-    for (int c = 0; c < nst; c++) {
-        const int s = c % MMVQ_STAGES;
-        const uint32_t ph = (uint32_t)(c / MMVQ_STAGES) & 1u;
-        if (*abort_flag) break;
-        if (!tc::mbar_wait(&full[s], ph)) { *abort_flag = 1; break; }
-        const int64_t ra = r0 + (int64_t)c * SR;
-        const uintptr_t a16 = (wbase + (uintptr_t)(ra * rb)) & ~uintptr_t(15);
-        // shared-memory address of global byte p is stage + s*SB + (p - a16)
-        const uint8_t *srow0 = stage + s * SB + ((wbase + (uintptr_t)(ra * rb)) - a16);
-        for (int g = 0; g < shp.sub_groups; g++) {
-            const int64_t g0 = ra + (int64_t)g * R;
-            if (g0 >= r1) break;
-            WPiece<WT> wp[R];
+// Butterfly over the lanes that share lane % TG (offsets 16 .. TG): V values in,
+// one total out; `idx` receives the value index whose total this lane holds.
+template <int V, int TG>
+__device__ __forceinline__ float butterfly_tg(float (&v)[V], int lane, int &idx) {
+    idx = 0;
+    int c = V;
 #pragma unroll
-            for (int r = 0; r < R; r++) {
-                const int64_t rr = g0 + r < r1 ? (int64_t)g * R + r : (r1 - 1 - ra);  // stay inside the stage
-                if (valid) load_w<WT>(wp[r], srow0 + rr * rb, piece);
-            }
-            float part[V];
+    for (int o = 16; o >= TG; o >>= 1) {
+        if (c > 1) {
+            const bool upper = (lane & o) != 0;
 #pragma unroll
-            for (int i = 0; i < V; i++) part[i] = 0.0f;
-            if (valid) {
-#pragma unroll
-                for (int r = 0; r < R; r++) {
-                    float acc[M];
-#pragma unroll
-                    for (int mm = 0; mm < M; mm++) acc[mm] = 0.0f;
-                    dot_piece<WT, M>(wp[r], act, piece, acc);
-#pragma unroll
-                    for (int mm = 0; mm < M; mm++) part[r * M + mm] = acc[mm];
+            for (int j = 0; j < V / 2; j++) {
+                if (j < c / 2) {
+                    const float send = upper ? v[j] : v[j + c / 2];
+                    const float keep = upper ? v[j + c / 2] : v[j];
+                    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
                 }
             }
-            const float tot = butterfly<V>(part, lane);
-            if ((lane & ((32 >> LOG) - 1)) == 0) {
-                const int idx = lane >> (5 - LOG);
-                const int r = idx / M, mm = idx % M;
-                if (g0 + r < r1) atomicAdd(&s_acc[(g0 - r0 + r) * M + mm], tot);
+            if (upper) idx += c / 2;
+            c /= 2;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        }
+    }
+    return v[0];
+}
+
+// lanes that write the totals after butterfly_tg: the lane bits used by the
+// plain (non-splitting) levels are zero
+template <int V, int TG>
+__device__ __forceinline__ bool butterfly_writer(int lane) {
+    int c = V, mask = 0;
+#pragma unroll
+    for (int o = 16; o >= TG; o >>= 1) {
+        if (c > 1) c /= 2;
+        else mask |= o;
+    }
+    return (lane & mask) == 0;
+}
+
+// ---------------------------------------------------------------- piece traits
+// Each traits type describes one thread's piece of a weight row: where its
+// bytes are (Pos, computed once), the raw bytes of one row (W, loaded before
+// any arithmetic so several rows are in flight), the activation values of the
+// piece for M tokens (A, loaded once), and the block-dot arithmetic.
+
+// 32-value pieces (Q8_0, and the fallback for rows that do not split into
+// 64-value pieces) reuse the building blocks above.
+template <int WT>
+struct ThinPiece {
+    static constexpr int VALUES = 32;
+    struct Pos { int64_t p; };
+    using W = WPiece<WT>;
+    template <int M> using A = ActPiece<M>;
+    static __device__ __forceinline__ Pos pos(int64_t p) { return Pos{p}; }
+    static __device__ __forceinline__ void load(W &w, const uint8_t *row, const Pos &q) { load_w<WT>(w, row, q.p); }
+    template <int M>
+    static __device__ __forceinline__ void load_act(A<M> &a, const uint8_t *xq, int64_t xrb, int m_act,
+                                                    const Pos &q, bool valid) {
+        gg::load_act<WT, M>(a, xq, xrb, m_act, valid ? q.p : 0, valid);
+    }
+    template <int M>
+    static __device__ __forceinline__ void dot(const W &w, const A<M> &a, const Pos &q, float (&acc)[M]) {
+        dot_piece<WT, M>(w, a, q.p, acc);
+    }
+};
+
+// Q4_K, 64-value pieces: piece p is chunk c = p%4 of super-block p/4, i.e. the
+// 32 quant bytes at 16 + 32c whose low nibbles are sub-block 2c and whose high
+// nibbles are sub-block 2c+1 (values 64c .. 64c+63).  One thread loads the
+// 16-byte header and the 32 quant bytes with three 16-byte loads.
+struct Q4KPiece {
+    static constexpr int VALUES = 64;
+    struct Pos {
+        int64_t off;               // byte offset of the super-block in the row
+        int c;                     // chunk
+        uint32_t sel_r, sel_w;     // byte_perm selectors for the scale bytes
+        uint32_t m1, m2, m3, m4;   // masks that assemble (s0, s1, m0, m1) for this c
+    };
+    struct W { uint4 h, a, b; };
+    template <int M>
+    struct A {
+        int q[M][16];     // quants of q8_1 blocks 2c and 2c+1 of the super-block
+        float f[M][4];    // d_a0, d_a1, s_a0, s_a1
+    };
+    static __device__ __forceinline__ Pos pos(int64_t p) {
+        Pos q;
+        q.off = (p >> 2) * Q4_K_BYTES;
+        q.c = (int)(p & 3);
+        const uint32_t cc = (uint32_t)(q.c & 1);
+        // sub-blocks j = 2c, 2c+1 take their 6-bit scale / min from the scale
+        // bytes sc[0..11] (header words y = sc[0..3], z = sc[4..7], w = sc[8..11]):
+        //   j < 4: s = sc[j] & 63, m = sc[j+4] & 63
+        //   j >= 4: s = (sc[j+4] & 15) | (sc[j-4] >> 6) << 4,
+        //           m = (sc[j+4] >> 4) | (sc[j] >> 6) << 4
+        // r = (y[2cc], y[2cc+1], z[2cc], z[2cc+1]) and wq = (w[2cc], w[2cc+1]) x 2
+        // hold every byte either case needs.
+        q.sel_r = (2 * cc) | ((2 * cc + 1) << 4) | ((4 + 2 * cc) << 8) | ((5 + 2 * cc) << 12);
+        q.sel_w = (2 * cc) | ((2 * cc + 1) << 4) | ((2 * cc) << 8) | ((2 * cc + 1) << 12);
+        const bool lo = q.c < 2;
+        q.m1 = lo ? 0x3F3F3F3Fu : 0u;
+        q.m2 = lo ? 0u : 0x30303030u;
+        q.m3 = lo ? 0u : 0x00000F0Fu;
+        q.m4 = lo ? 0u : 0x0F0F0000u;
+        return q;
+    }
+    static __device__ __forceinline__ void load(W &w, const uint8_t *row, const Pos &q) {
+        const uint8_t *blk = row + q.off;
+        w.h = __ldg(reinterpret_cast<const uint4 *>(blk));
+        w.a = __ldg(reinterpret_cast<const uint4 *>(blk + 16 + 32 * q.c));
+        w.b = __ldg(reinterpret_cast<const uint4 *>(blk + 32 + 32 * q.c));
+    }
+    template <int M>
+    static __device__ __forceinline__ void load_act(A<M> &a, const uint8_t *xq, int64_t xrb, int m_act,
+                                                    const Pos &q, bool valid) {
+        const int64_t b0 = (q.off / Q4_K_BYTES) * 8 + 2 * q.c;
+#pragma unroll
+        for (int mm = 0; mm < M; mm++) {
+            const bool on = valid && mm < m_act;
+            const uint8_t *p0 = xq + mm * xrb + b0 * Q8_1_BYTES, *p1 = p0 + Q8_1_BYTES;
+            const uint32_t ds0 = on ? ld_u32(p0) : 0u, ds1 = on ? ld_u32(p1) : 0u;
+            a.f[mm][0] = h2f(ds0 & 0xffff);
+            a.f[mm][1] = h2f(ds1 & 0xffff);
+            a.f[mm][2] = h2f(ds0 >> 16);
+            a.f[mm][3] = h2f(ds1 >> 16);
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                a.q[mm][i] = on ? (int)ld_u32(p0 + 4 + 4 * i) : 0;
+                a.q[mm][8 + i] = on ? (int)ld_u32(p1 + 4 + 4 * i) : 0;
             }
         }
-        // this warp is done reading stage s
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&empty[s]);
-        if (tid == 0 && c + MMVQ_STAGES < nst) {
-            if (!tc::mbar_wait(&empty[s], ph)) { *abort_flag = 1; }
-            else issue(c + MMVQ_STAGES);
+    }
+    template <int M>
+    static __device__ __forceinline__ void dot(const W &w, const A<M> &a, const Pos &q, float (&acc)[M]) {
+        const float d = h2f(w.h.x & 0xffff), dmin = h2f(w.h.x >> 16);
+        const uint32_t r = __byte_perm(w.h.y, w.h.z, q.sel_r);
+        const uint32_t wq = __byte_perm(w.h.w, 0u, q.sel_w);
+        // bytes (s0, s1, m0, m1), each 6 bits
+        const uint32_t sm = (r & q.m1) | ((r >> 2) & q.m2) | (wq & q.m3) | ((wq >> 4) & q.m4);
+        const float ds0 = d * (float)(sm & 0xff);
+        // high nibbles are used in place (16 * q), so their scale carries 1/16 (exact)
+        const float ds1 = d * (float)((sm >> 8) & 0xff) * 0.0625f;
+        const float fm0 = (float)((sm >> 16) & 0xff), fm1 = (float)(sm >> 24);
+        const uint32_t raw[8] = {w.a.x, w.a.y, w.a.z, w.a.w, w.b.x, w.b.y, w.b.z, w.b.w};
+        uint32_t lo[8], hi[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            lo[i] = raw[i] & 0x0F0F0F0Fu;
+            hi[i] = raw[i] & 0xF0F0F0F0u;
+        }
+#pragma unroll
+        for (int mm = 0; mm < M; mm++) {
+            int S0 = 0, S1 = 0;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                S0 = dp4a_us(lo[i], a.q[mm][i], S0);
+                S1 = dp4a_us(hi[i], a.q[mm][8 + i], S1);
+            }
+            float v = ds0 * (a.f[mm][0] * (float)S0);
+            v = fmaf(ds1, a.f[mm][1] * (float)S1, v);
+            v = fmaf(-dmin, fmaf(fm0, a.f[mm][2], fm1 * a.f[mm][3]), v);
+            acc[mm] += v;
         }
     }
-    // copies still in flight (only after an abort) land before the CTA exits
-    if (tid == 0 && *abort_flag) {
-        for (int c = 0; c < nst; c++) tc::mbar_wait(&full[c % MMVQ_STAGES], (uint32_t)(c / MMVQ_STAGES) & 1u);
-    }
-    __syncthreads();
-    const int64_t nr = r1 - r0;
-    for (int64_t i = tid; i < nr * M; i += blockDim.x) {
-        const int64_t mm = i / nr, r = i - mm * nr;
-        if (mm < m_act) store_out(y, yt, mm * ldy + r0 + r, s_acc[r * M + mm]);
+};
+
+// Read 16 bytes at a 2-byte-aligned address as four words (aligned loads plus
+// a funnel shift when p % 4 == 2; touches only [p - 2, p + 18)).
+__device__ __forceinline__ void ld16_a2(const uint8_t *p, uint32_t (&o)[4]) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint8_t *base = reinterpret_cast<const uint8_t *>(a & ~uintptr_t(3));
+    uint32_t w[5];
+#pragma unroll
+    for (int i = 0; i < 4; i++) w[i] = __ldg(reinterpret_cast<const uint32_t *>(base) + i);
+    if (a & 2) {
+        w[4] = __ldg(reinterpret_cast<const uint32_t *>(base) + 4);
+#pragma unroll
+        for (int i = 0; i < 4; i++) o[i] = __funnelshift_r(w[i], w[i + 1], 16);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; i++) o[i] = w[i];
     }
 }
 
-template <int WT, int M, int R, int MAXT>
-inline cudaError_t launch_mmvq_t(const uint8_t *w, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y,
-                                 int yt, int64_t ldy, cudaStream_t s) {
-    const int64_t P = k / 32;
-    const int nthr = (int)(((P + 31) / 32) * 32);
-    const int64_t rb = k / block_elems(WT) * block_bytes(WT);
-    auto kern = mmvq_kernel<WT, M, R, MAXT>;
-    // stage = G sub-groups of R rows, about 16 KB
-    int G = (int)(16384 / (R * rb));
-    if (G < 1) G = 1;
-    if (G > 8) G = 8;
-    const int stage_bytes = (int)(((G * R * rb + 32) + 15) / 16 * 16);
-    // one wave of CTAs, each owning a contiguous range of rows
-    const int64_t groups = (n + R - 1) / R;
-    const int sms = device_info().sm_count;
-    const size_t fixed = (size_t)MMVQ_STAGES * stage_bytes + 8 * (2 * MMVQ_STAGES + 2);
-    // raise the dynamic shared-memory limit before asking for the occupancy
-    // (the query counts a kernel whose request exceeds the limit as unlaunchable)
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(device_info().smem_optin));
-    if (e != cudaSuccess) return e;
+// Q6_K, 64-value pieces: piece p of super-block p/4 is half h = (p/2)%2 and
+// l0 = 16*(p%2): the runs [128h + 32g + l0, +16) for g = 0..3, i.e. ql bytes
+// [64h + l0, +16) (g = 0 low nibbles, g = 2 high), [64h + 32 + l0, +16)
+// (g = 1, g = 3) and qh bytes [32h + l0, +16) (two bits per g).  Run g is the
+// 16-value sub-block 8h + 2g + l0/16 (scale sc[8h + 2g + l0/16]) and half
+// l0/16 of q8_1 block 4h + g.  Quants are used as unsigned 0..63 and the
+// offset is applied through the activation sums: sum (u - 32) a = sum u a - 32 sum a.
+struct Q6KPiece {
+    static constexpr int VALUES = 64;
+    struct Pos { int64_t off; int h, l0; };
+    struct W { uint32_t ql0[4], ql1[4], qh[4]; uint32_t sc; uint32_t d; };
+    template <int M>
+    struct A {
+        int q[M][16];    // run g quants: words 4g .. 4g+3
+        float f[M][4];   // d_a of run g
+        int sum[M][4];   // 32 * sum of the run's 16 quants
+    };
+    static __device__ __forceinline__ Pos pos(int64_t p) {
+        return Pos{(p >> 2) * Q6_K_BYTES, (int)((p >> 1) & 1), 16 * (int)(p & 1)};
+    }
+    static __device__ __forceinline__ void load(W &w, const uint8_t *row, const Pos &q) {
+        const uint8_t *blk = row + q.off;
+        ld16_a2(blk + 64 * q.h + q.l0, w.ql0);
+        ld16_a2(blk + 64 * q.h + 32 + q.l0, w.ql1);
+        ld16_a2(blk + 128 + 32 * q.h + q.l0, w.qh);
+        uint32_t s0, s1;
+        ld8_a2(blk + 192 + 8 * q.h, s0, s1);  // sc[8h .. 8h+7]
+        // scales of runs g = 0..3: sc[8h + l0/16 + 2g]
+        w.sc = q.l0 ? __byte_perm(s0, s1, 0x7531) : __byte_perm(s0, s1, 0x6420);
+        w.d = ld_u16(blk + 208);
+    }
+    template <int M>
+    static __device__ __forceinline__ void load_act(A<M> &a, const uint8_t *xq, int64_t xrb, int m_act,
+                                                    const Pos &q, bool valid) {
+        const int64_t b0 = (q.off / Q6_K_BYTES) * 8 + 4 * q.h;
+#pragma unroll
+        for (int mm = 0; mm < M; mm++) {
+            const bool on = valid && mm < m_act;
+#pragma unroll
+            for (int g = 0; g < 4; g++) {
+                const uint8_t *blk = xq + mm * xrb + (b0 + g) * Q8_1_BYTES;
+                a.f[mm][g] = on ? h2f(ld_u16(blk)) : 0.0f;
+                int sum = 0;
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int v = on ? (int)ld_u32(blk + 4 + q.l0 + 4 * i) : 0;
+                    a.q[mm][4 * g + i] = v;
+                    sum = dp4a_ss(v, 0x01010101, sum);
+                }
+                a.sum[mm][g] = 32 * sum;
+            }
+        }
+    }
+    template <int M>
+    static __device__ __forceinline__ void dot(const W &w, const A<M> &a, const Pos &, float (&acc)[M]) {
+        const float d = h2f((uint16_t)w.d);
+        float dsc[4];
+#pragma unroll
+        for (int g = 0; g < 4; g++) dsc[g] = d * (float)(int)(int8_t)((w.sc >> (8 * g)) & 0xff);
+        uint32_t u[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint32_t A0 = w.ql0[i], A1 = w.ql1[i], H = w.qh[i];
+            u[0][i] = (A0 & 0x0F0F0F0Fu) | ((H << 4) & 0x30303030u);
+            u[1][i] = (A1 & 0x0F0F0F0Fu) | ((H << 2) & 0x30303030u);
+            u[2][i] = ((A0 >> 4) & 0x0F0F0F0Fu) | (H & 0x30303030u);
+            u[3][i] = ((A1 >> 4) & 0x0F0F0F0Fu) | ((H >> 2) & 0x30303030u);
+        }
+#pragma unroll
+        for (int mm = 0; mm < M; mm++) {
+            float v = 0.0f;
+#pragma unroll
+            for (int g = 0; g < 4; g++) {
+                int S = -a.sum[mm][g];
+#pragma unroll
+                for (int i = 0; i < 4; i++) S = dp4a_us(u[g][i], a.q[mm][4 * g + i], S);
+                v = fmaf(dsc[g], a.f[mm][g] * (float)S, v);
+            }
+            acc[mm] += v;
+        }
+    }
+};
+
+// ---------------------------------------------------------------- the kernel
+// Thread t of a CTA owns piece t / TG of every row and the tokens
+// [(t % TG) * M, +M).  The CTA walks rows [n0, n0 + R) for n0 = blockIdx.x * R,
+// + gridDim.x * R, ...
+template <class PT, int M, int TG, int R, int MAXT>
+__global__ void __launch_bounds__(MAXT) mmvq_kernel(const uint8_t *__restrict__ w, int64_t n, int64_t k, int64_t rb,
+                                                   const uint8_t *__restrict__ xq, int m_act, void *__restrict__ y,
+                                                   int yt, int64_t ldy) {
+    constexpr int V = R * M;
+    static_assert(V * TG <= 32 && (V & (V - 1)) == 0, "R*M must be a power of two <= 32/TG");
+    __shared__ float red[2][MAXT / 32][TG * V];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    const int tg = tid % TG;
+    const int64_t piece = tid / TG;
+    const int64_t P = k / PT::VALUES;
+    const bool valid = piece < P;
+    const typename PT::Pos pos = PT::pos(valid ? piece : 0);
+    const int64_t stride = (int64_t)gridDim.x * R;
+    int64_t n0 = (int64_t)blockIdx.x * R;
+
+    typename PT::W wa[R], wb[R];
+    auto load_rows = [&](typename PT::W (&dst)[R], int64_t base) {
+        if (!valid) return;
+#pragma unroll
+        for (int r = 0; r < R; r++) PT::load(dst[r], w + (base + r < n ? base + r : n - 1) * rb, pos);
+    };
+    // weights never change: the first rows are requested before waiting for
+    // the kernel that wrote the activations
+    if (n0 < n) load_rows(wa, n0);
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    typename PT::template A<M> act;
+    const int m_mine = m_act - tg * M;  // tokens of this thread (may be <= 0)
+    PT::template load_act<M>(act, xq + (int64_t)tg * M * ((k / 32) * Q8_1_BYTES), (k / 32) * Q8_1_BYTES,
+                             m_mine, pos, valid);
+
+    int buf = 0;
+    auto process = [&](const typename PT::W (&cur)[R], int64_t r0) {
+        float part[V];
+#pragma unroll
+        for (int i = 0; i < V; i++) part[i] = 0.0f;
+        if (valid) {
+#pragma unroll
+            for (int r = 0; r < R; r++) {
+                float acc[M];
+#pragma unroll
+                for (int mm = 0; mm < M; mm++) acc[mm] = 0.0f;
+                PT::template dot<M>(cur[r], act, pos, acc);
+#pragma unroll
+                for (int mm = 0; mm < M; mm++) part[r * M + mm] = acc[mm];
+            }
+        }
+        int idx;
+        const float tot = butterfly_tg<V, TG>(part, lane, idx);
+        const bool writer = butterfly_writer<V, TG>(lane);
+        if (nw == 1) {
+            if (writer) {
+                const int r = idx / M, tok = tg * M + idx % M;
+                if (r0 + r < n && tok < m_act) store_out(y, yt, (int64_t)tok * ldy + r0 + r, tot);
+            }
+        } else {
+            if (writer) red[buf][warp][tg * V + idx] = tot;
+            __syncthreads();
+            if (tid < TG * V) {
+                float sum = 0.0f;
+                for (int j = 0; j < nw; j++) sum += red[buf][j][tid];
+                const int g = tid / V, i = tid % V, r = i / M, tok = g * M + i % M;
+                if (r0 + r < n && tok < m_act) store_out(y, yt, (int64_t)tok * ldy + r0 + r, sum);
+            }
+            buf ^= 1;
+        }
+    };
+    // two register sets in turn: the next rows load while the current compute
+    while (n0 < n) {
+        if (n0 + stride < n) load_rows(wb, n0 + stride);
+        process(wa, n0);
+        n0 += stride;
+        if (n0 >= n) break;
+        if (n0 + stride < n) load_rows(wa, n0 + stride);
+        process(wb, n0);
+        n0 += stride;
+    }
+}
+
+template <class PT, int M, int TG, int R, int MAXT>
+inline cudaError_t launch_mmvq_cfg(const uint8_t *w, int64_t n, int64_t k, int64_t rb, const uint8_t *xq, int64_t m,
+                                   void *y, int yt, int64_t ldy, cudaStream_t s) {
+    const int64_t P = k / PT::VALUES;
+    const int nthr = (int)((P * TG + 31) / 32 * 32);
+    if (nthr > MAXT) return cudaErrorInvalidValue;
+    auto kern = mmvq_kernel<PT, M, TG, R, MAXT>;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nthr, fixed + 4096);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nthr, 0);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
-    int64_t grid = (int64_t)sms * per_sm;
+    const int64_t groups = (n + R - 1) / R;
+    int64_t grid = (int64_t)device_info().sm_count * per_sm;
     if (grid > groups) grid = groups;
-    const int64_t rows_per_cta = (groups + grid - 1) / grid * R;
-    grid = (n + rows_per_cta - 1) / rows_per_cta;
-    MmvqShape shp{rows_per_cta, G, stage_bytes};
-    const size_t smem = fixed + (size_t)rows_per_cta * M * sizeof(float);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3((unsigned)nthr);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, w, n, k, rb, xq, (int)m, y, yt, ldy, shp);
+    return cudaLaunchKernelEx(&cfg, kern, w, n, k, rb, xq, (int)m, y, yt, ldy);
 }
 
-// Threads per CTA = pieces per row (rounded to a warp): K <= 8192 fits in 256
-// threads with the full register budget; longer rows use 512-thread CTAs.
-// Rows per sub-group R: the default keeps R * M = 16 (8 for m = 1); rows
-// longer than 3 KB use R = 1 so that a stage stays within ~20 KB of shared
-// memory.  Threads per CTA = pieces per row rounded to a warp: K <= 8192 fits
-// 256-thread CTAs with the full register budget, longer rows use 512.
-template <int WT, int MAXT>
-inline cudaError_t launch_mmvq_mt(const uint8_t *w, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y,
-                                  int yt, int64_t ldy, cudaStream_t s) {
-    const int64_t rb = k / block_elems(WT) * block_bytes(WT);
-    if (MAXT == 256 && rb <= 3072) {
-        if (m <= 1) return launch_mmvq_t<WT, 1, 8, MAXT>(w, n, k, xq, m, y, yt, ldy, s);
-        if (m <= 2) return launch_mmvq_t<WT, 2, 8, MAXT>(w, n, k, xq, m, y, yt, ldy, s);
-        if (m <= 4) return launch_mmvq_t<WT, 4, 4, MAXT>(w, n, k, xq, m, y, yt, ldy, s);
-        return launch_mmvq_t<WT, 8, 2, MAXT>(w, n, k, xq, m, y, yt, ldy, s);
+// Configuration by token count (measured on GB300, Q4_K / Q6_K rows of 3072 ..
+// 8192 values): up to 4 tokens per thread with the next R rows prefetched;
+// 5..8 tokens either as two threads per piece with 4 tokens each (Q4_K) or 8
+// tokens per thread (Q6_K, whose wider loads leave fewer registers).  Rows of
+// more than 256 pieces (32-value pieces of K > 8192) use 512-thread CTAs.
+struct MmvqTune {
+    bool r4_m1;        // M = 1: R = 4 instead of 2
+    bool r1_m1;        // M = 1: R = 1 (overrides r4_m1)
+    bool tg2_m8;       // 5..8 tokens: two threads per piece
+};
+
+template <class PT>
+inline cudaError_t launch_mmvq_pt(const uint8_t *w, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y,
+                                  int yt, int64_t ldy, cudaStream_t s, int64_t rb, MmvqTune t) {
+    const int64_t P = k / PT::VALUES;
+    if (P <= 256) {
+        if (m <= 1) {
+            if (t.r1_m1) return launch_mmvq_cfg<PT, 1, 1, 1, 256>(w, n, k, rb, xq, m, y, yt, ldy, s);
+            if (t.r4_m1) return launch_mmvq_cfg<PT, 1, 1, 4, 256>(w, n, k, rb, xq, m, y, yt, ldy, s);
+            return launch_mmvq_cfg<PT, 1, 1, 2, 256>(w, n, k, rb, xq, m, y, yt, ldy, s);
+        }
+        if (m <= 2) return launch_mmvq_cfg<PT, 2, 1, 2, 256>(w, n, k, rb, xq, m, y, yt, ldy, s);
+        if (m <= 4) return launch_mmvq_cfg<PT, 4, 1, 2, 256>(w, n, k, rb, xq, m, y, yt, ldy, s);
+        if (t.tg2_m8 && P <= 128) return launch_mmvq_cfg<PT, 4, 2, 2, 256>(w, n, k, rb, xq, m, y, yt, ldy, s);
+        return launch_mmvq_cfg<PT, 8, 1, 1, 256>(w, n, k, rb, xq, m, y, yt, ldy, s);
     }
-    if (m <= 1) return launch_mmvq_t<WT, 1, 1, MAXT>(w, n, k, xq, m, y, yt, ldy, s);
-    if (m <= 2) return launch_mmvq_t<WT, 2, 1, MAXT>(w, n, k, xq, m, y, yt, ldy, s);
-    if (m <= 4) return launch_mmvq_t<WT, 4, 1, MAXT>(w, n, k, xq, m, y, yt, ldy, s);
-    return launch_mmvq_t<WT, 8, 1, MAXT>(w, n, k, xq, m, y, yt, ldy, s);
-}
-
-template <int WT>
-inline cudaError_t launch_mmvq_type(const uint8_t *w, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y,
-                                    int yt, int64_t ldy, cudaStream_t s) {
-    if (k <= 8192) return launch_mmvq_mt<WT, 256>(w, n, k, xq, m, y, yt, ldy, s);
-    return launch_mmvq_mt<WT, 512>(w, n, k, xq, m, y, yt, ldy, s);
+    if constexpr (PT::VALUES == 32) {
+        if (m <= 1) return launch_mmvq_cfg<PT, 1, 1, 2, 512>(w, n, k, rb, xq, m, y, yt, ldy, s);
+        if (m <= 2) return launch_mmvq_cfg<PT, 2, 1, 2, 512>(w, n, k, rb, xq, m, y, yt, ldy, s);
+        if (m <= 4) return launch_mmvq_cfg<PT, 4, 1, 1, 512>(w, n, k, rb, xq, m, y, yt, ldy, s);
+        return launch_mmvq_cfg<PT, 8, 1, 1, 512>(w, n, k, rb, xq, m, y, yt, ldy, s);
+    }
+    return cudaErrorInvalidValue;  // 64-value pieces: K <= 16384 gives at most 256 pieces
 }
 
 cudaError_t launch_mmvq_q8_0(const uint8_t *w, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y, int yt,

@@ -150,16 +150,32 @@ def test_mmvq_fp32(g, wt, m, safe):
     assert_close(y, ref, TOL_F32, f"mmvq type {wt} m {m}")
 
 
-@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K])
+@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0])
 @pytest.mark.parametrize("k", [256, 768, 3072, 8192, 16384])
-def test_mmvq_k_range_bf16(g, wt, k):
-    n, m = 129, 4
+@pytest.mark.parametrize("m", [1, 4, 7])
+def test_mmvq_k_range_bf16(g, wt, k, m):
+    # covers every CTA shape: 64-value pieces up to 256 threads, 32-value
+    # pieces up to 512 threads, 1 or 2 threads per piece, ragged warps
+    n = 129
     w = _weights(wt, n, k, seed=k, safe=True)
     x = synth.activations(m, k, seed=k + 1, dtype=torch.bfloat16)
     ref = oracle.mul_mat(wt, w, k, oracle.quantize_q8_1(x.float().numpy()))
     y = g.gguf_mul_mat(_u8(w), wt, n, k, x.to(DEV))
     assert y.dtype == torch.bfloat16        # output in the activation dtype
-    assert_close(y.float().cpu().numpy(), ref, TOL_BF16, f"mmvq bf16 type {wt} k {k}")
+    assert_close(y.float().cpu().numpy(), ref, TOL_BF16, f"mmvq bf16 type {wt} k {k} m {m}")
+
+
+@pytest.mark.parametrize("wt,n,k", [(oracle.Q6_K, 40000, 3072), (oracle.Q4_K, 20000, 3072)])
+@pytest.mark.parametrize("m", [1, 2, 8])
+def test_mmvq_tall_sampled(g, wt, n, k, m):
+    # tall matrices take the R = 1 / R = 4 row groupings; rows sampled for the oracle
+    w = synth.safe_blocks(wt, n, k, seed=n + m)
+    x = synth.activations(m, k, seed=m, dtype=torch.float32)
+    y = g.gguf_mul_mat(_u8(w), wt, n, k, x.to(DEV)).cpu().numpy()
+    rows = np.sort(np.random.default_rng(m).choice(n, 64, replace=False))
+    rows[0], rows[-1] = 0, n - 1
+    ref = oracle.mul_mat(wt, w[rows], k, oracle.quantize_q8_1(x.numpy()))
+    assert_close(y[:, rows], ref, TOL_F32, f"mmvq tall type {wt} m {m}")
 
 
 def test_mmvq_q8_0_config(g):
