@@ -63,6 +63,8 @@ const DeviceInfo &device_info() {
 // tunables
 static int64_t g_mmvq_max_m = 8;
 static int64_t g_mmq_enable = 1;
+static int64_t g_mmvq_tc = 1;
+int64_t option_mmvq_tc() { return g_mmvq_tc; }
 
 static bool is_float(int t) { return t == GGUF_F32 || t == GGUF_F16 || t == GGUF_BF16; }
 static bool is_weight(int t) { return t == GGUF_Q8_0 || t == GGUF_Q4_K || t == GGUF_Q6_K; }
@@ -366,6 +368,10 @@ gguf_status gguf_set_option(const char *key, int64_t value) {
         g_mmvq_max_m = value;
         return GGUF_OK;
     }
+    if (!strcmp(key, "mmvq_tc")) {
+        g_mmvq_tc = value != 0;
+        return GGUF_OK;
+    }
     if (!strcmp(key, "mmq_enable")) {
         g_mmq_enable = value != 0;
         return GGUF_OK;
@@ -377,6 +383,7 @@ int64_t gguf_get_option(const char *key) {
     if (!key) return -1;
     if (!strcmp(key, "mmvq_max_m")) return g_mmvq_max_m;
     if (!strcmp(key, "mmq_enable")) return g_mmq_enable;
+    if (!strcmp(key, "mmvq_tc")) return g_mmvq_tc;
     return -1;
 }
 

@@ -38,6 +38,9 @@ cudaError_t launch_convert_float(const void *x, int xt, int64_t count, void *out
 cudaError_t launch_block_dots(const uint8_t *w, int wt, int64_t n, int64_t k, const uint8_t *xq, int64_t m,
                               int32_t *sums, cudaStream_t s);
 
+// option "mmvq_tc": 5..8 tokens of Q4_K rows run on the tensor-core MMVQ (1, default) or dp4a (0)
+int64_t option_mmvq_tc();
+
 // y[m][ldy] (yt) = W[n][k] (wt) . q8_1 rows xq[m] ; m <= 8
 cudaError_t launch_mmvq(const uint8_t *w, int wt, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y,
                         int yt, int64_t ldy, cudaStream_t s);

@@ -1,0 +1,274 @@
+// Tensor-core MMVQ for 5..8 tokens (Q4_K weights): the per-block int32 dot
+// products of the blockwise formula run on warp-level int8 MMAs
+// (mma.sync m16n8k32 s8 x s8 -> s32).  One MMA is one 32-value block of 16
+// weight rows against 8 tokens, so its s32 accumulator is exactly the block
+// dot S_j of each (row, token) pair; scales are then applied per block in
+// fp32 as in the dp4a kernel:
+//   y += d * sum_j s_j * d_a,j * S_j  -  dmin * sum_j m_j * s_a,j
+// At 8 tokens the dp4a form needs 16 dp4a per token per 64 weights, which
+// GB300's int8 rate cannot issue as fast as HBM delivers the weights; here the
+// operands need one LOP3 per 4 weights (Q4_K nibbles are non-negative int8)
+// and the q8_1 quants are the B fragments as they are.
+// The min term of a super-block is one fp16 MMA: A = the rows' 8 six-bit
+// mins, B = the 8 blocks' stored fp16 s_a (products exact in fp32).
+//
+// Work split.  A CTA of NW warps owns 16-row tiles; warp w takes super-blocks
+// [w * nsb / NW, (w + 1) * nsb / NW) of every tile and the warps' partial
+// results are summed through shared memory in a fixed order (deterministic).
+// The q8_1 rows (8 tokens) are copied once per CTA into shared memory with the
+// 32 quants of each block on an 8-byte boundary; the weights of the next
+// (tile, super-block) item load into registers while the current one computes.
+#pragma once
+
+#include "mmvq.cuh"
+
+namespace gg {
+
+__device__ __forceinline__ void mma_16832_s8(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0));
+}
+
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// Shared-memory layout (bytes) for rows of nblk = K/32 q8_1 blocks.
+struct MmaSmem {
+    int64_t xs, xs_pitch, da, saf, red, total;
+};
+__host__ __device__ inline MmaSmem mma_smem_layout(int64_t k, int nw) {
+    const int64_t nblk = k / 32, nsb = k / 256;
+    MmaSmem L;
+    L.xs = 0;                                               // 8 token rows of nblk x 32 quants (+8 B pad)
+    L.xs_pitch = (nblk * 40 + 127) / 128 * 128 + 32;        // 40 B per block; pitch = 32 mod 128 bytes
+    L.da = L.xs + 8 * L.xs_pitch;                           // float [nblk][8]: d_a
+    L.saf = L.da + nblk * 8 * 4;                            // uint32 [nsb][32]: s_a pairs for the min MMA
+    L.red = L.saf + nsb * 32 * 4;                           // float4 [2][nw][32]
+    L.total = L.red + 2 * (int64_t)nw * 32 * 16;
+    return L;
+}
+
+struct MmaW {
+    uint4 h0, h1;        // headers of rows g and g+8
+    uint2 q0[4], q1[4];  // bytes [32c + 8t, +8) of each chunk c, rows g and g+8
+};
+
+__global__ void __launch_bounds__(512, 1) mmvq_mma_q4k_kernel(const uint8_t *__restrict__ w, int64_t n, int64_t k,
+                                                             int64_t rb, const uint8_t *__restrict__ xq, int m_act,
+                                                             void *__restrict__ y, int yt, int64_t ldy) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int nw = blockDim.x >> 5;
+    const MmaSmem L = mma_smem_layout(k, nw);
+    uint8_t *xs = smem + L.xs;
+    float *da = reinterpret_cast<float *>(smem + L.da);
+    uint32_t *saf = reinterpret_cast<uint32_t *>(smem + L.saf);
+    float4 *red = reinterpret_cast<float4 *>(smem + L.red);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int nblk = (int)(k / 32), nsb = (int)(k / 256);
+    const int64_t xrb = (int64_t)nblk * Q8_1_BYTES;
+    const int pitch = (int)L.xs_pitch;
+    const int64_t n_tiles = (n + 15) / 16;
+    const int sb_lo = warp * nsb / nw, sb_hi = (warp + 1) * nsb / nw;
+
+    // per-thread Q4_K scale selectors for sub-blocks 2t, 2t+1 (see Q4KPiece::pos)
+    const Q4KPiece::Pos sel = Q4KPiece::pos(t);
+
+    auto load_item = [&](MmaW &W, int64_t tile, int sb) {
+        const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
+        const uint8_t *b0 = w + (r0 < n ? r0 : n - 1) * rb + sb * Q4_K_BYTES;
+        const uint8_t *b1 = w + (r1 < n ? r1 : n - 1) * rb + sb * Q4_K_BYTES;
+        W.h0 = __ldg(reinterpret_cast<const uint4 *>(b0));
+        W.h1 = __ldg(reinterpret_cast<const uint4 *>(b1));
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+            W.q0[c] = __ldg(reinterpret_cast<const uint2 *>(b0 + 16 + 32 * c + 8 * t));
+            W.q1[c] = __ldg(reinterpret_cast<const uint2 *>(b1 + 16 + 32 * c + 8 * t));
+        }
+    };
+
+    // the first item's weights are requested before waiting for the kernel
+    // that wrote the activations
+    int64_t tile = blockIdx.x;
+    MmaW wa, wb;
+    if (sb_lo < sb_hi && tile < n_tiles) load_item(wa, tile, sb_lo);
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // ---- q8_1 rows into shared memory (quants of block b at b * 40 + 8), d_a and s_a pairs
+    for (int i = tid; i < 8 * nblk; i += blockDim.x) {
+        const int tok = i / nblk, b = i - tok * nblk;
+        uint32_t *dst = reinterpret_cast<uint32_t *>(xs + tok * pitch + b * 40 + 8);
+        if (tok < m_act) {
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + tok * xrb + (int64_t)b * Q8_1_BYTES + 4);
+#pragma unroll
+            for (int j = 0; j < 8; j++) dst[j] = src[j];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; j++) dst[j] = 0u;
+        }
+    }
+    for (int i = tid; i < nblk * 8; i += blockDim.x) {
+        const int b = i >> 3, tok = i & 7;
+        da[i] = tok < m_act ? h2f(ld_u16(xq + tok * xrb + (int64_t)b * Q8_1_BYTES)) : 0.0f;
+    }
+    for (int i = tid; i < nsb * 32; i += blockDim.x) {
+        const int s = i >> 5, l = i & 31, tok = l >> 2, tt = l & 3;
+        uint32_t v = 0u;
+        if (tok < m_act) {
+            const uint8_t *b = xq + tok * xrb + (int64_t)(s * 8 + 2 * tt) * Q8_1_BYTES;
+            v = (uint32_t)ld_u16(b + 2) | ((uint32_t)ld_u16(b + Q8_1_BYTES + 2) << 16);
+        }
+        saf[i] = v;
+    }
+    __syncthreads();
+
+    const uint8_t *xg = xs + g * pitch + 8 + 8 * t;   // this lane's B bytes: token g, values 8t .. 8t+7
+    const __half2 bias = __floats2half2_rn(-1024.0f, -1024.0f);
+
+    // one (tile, super-block) item; partial sums of rows g, g+8 x tokens 2t, 2t+1 into acc
+    auto process = [&](const MmaW &W, int sb, float (&acc)[4]) {
+        const float d0 = h2f(W.h0.x & 0xffff), dm0 = h2f(W.h0.x >> 16);
+        const float d1 = h2f(W.h1.x & 0xffff), dm1 = h2f(W.h1.x >> 16);
+        // (s, m) of sub-blocks 2t, 2t+1 for rows g and g+8 as bytes (s0, s1, m0, m1)
+        const uint32_t r0 = __byte_perm(W.h0.y, W.h0.z, sel.sel_r), r1 = __byte_perm(W.h1.y, W.h1.z, sel.sel_r);
+        const uint32_t w0 = __byte_perm(W.h0.w, 0u, sel.sel_w), w1 = __byte_perm(W.h1.w, 0u, sel.sel_w);
+        const uint32_t sm0 = (r0 & sel.m1) | ((r0 >> 2) & sel.m2) | (w0 & sel.m3) | ((w0 >> 4) & sel.m4);
+        const uint32_t sm1 = (r1 & sel.m1) | ((r1 >> 2) & sel.m2) | (w1 & sel.m3) | ((w1 >> 4) & sel.m4);
+        // the scales of chunk c are decoded by lane t = c of the quad
+        const uint32_t sp = __byte_perm(sm0, sm1, 0x5410);   // s_2t(g), s_2t+1(g), s_2t(g+8), s_2t+1(g+8)
+        float u[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+            const uint32_t sc = __shfl_sync(0xffffffffu, sp, (lane & ~3) | c);
+            const float sl0 = (float)(sc & 0xff), sh0 = (float)((sc >> 8) & 0xff);
+            const float sl1 = (float)((sc >> 16) & 0xff), sh1 = (float)(sc >> 24);
+            const int bl = sb * 8 + 2 * c;   // block of the low nibbles; bl + 1 of the high ones
+            const uint2 bL = *reinterpret_cast<const uint2 *>(xg + bl * 40);
+            const uint2 bH = *reinterpret_cast<const uint2 *>(xg + (bl + 1) * 40);
+            const uint2 x0 = W.q0[c], x1 = W.q1[c];
+            int sL[4], sH[4];
+            mma_16832_s8(sL, x0.x & 0x0F0F0F0Fu, x1.x & 0x0F0F0F0Fu, x0.y & 0x0F0F0F0Fu, x1.y & 0x0F0F0F0Fu,
+                         bL.x, bL.y);
+            mma_16832_s8(sH, (x0.x >> 4) & 0x0F0F0F0Fu, (x1.x >> 4) & 0x0F0F0F0Fu, (x0.y >> 4) & 0x0F0F0F0Fu,
+                         (x1.y >> 4) & 0x0F0F0F0Fu, bH.x, bH.y);
+            const float2 dL = *reinterpret_cast<const float2 *>(da + bl * 8 + 2 * t);
+            const float2 dH = *reinterpret_cast<const float2 *>(da + (bl + 1) * 8 + 2 * t);
+            // accumulator i: row g (i < 2) or g+8, token 2t + (i & 1)
+            u[0] = fmaf(sl0, dL.x * (float)sL[0], u[0]);
+            u[1] = fmaf(sl0, dL.y * (float)sL[1], u[1]);
+            u[2] = fmaf(sl1, dL.x * (float)sL[2], u[2]);
+            u[3] = fmaf(sl1, dL.y * (float)sL[3], u[3]);
+            u[0] = fmaf(sh0, dH.x * (float)sH[0], u[0]);
+            u[1] = fmaf(sh0, dH.y * (float)sH[1], u[1]);
+            u[2] = fmaf(sh1, dH.x * (float)sH[2], u[2]);
+            u[3] = fmaf(sh1, dH.y * (float)sH[3], u[3]);
+        }
+        // min term: A = m_2t, m_2t+1 of rows g, g+8 at k-slots 2t, 2t+1 (exact fp16 integers)
+        uint32_t ma0 = __byte_perm(sm0, 0x64u, 0x4342), ma1 = __byte_perm(sm1, 0x64u, 0x4342);
+        {
+            __half2 h0 = __hadd2(*reinterpret_cast<__half2 *>(&ma0), bias);
+            __half2 h1 = __hadd2(*reinterpret_cast<__half2 *>(&ma1), bias);
+            ma0 = *reinterpret_cast<uint32_t *>(&h0);
+            ma1 = *reinterpret_cast<uint32_t *>(&h1);
+        }
+        float mv[4];
+        mma_16816_f16(mv, ma0, ma1, 0u, 0u, saf[sb * 32 + lane], 0u);
+        acc[0] = fmaf(d0, u[0], acc[0]);
+        acc[1] = fmaf(d0, u[1], acc[1]);
+        acc[2] = fmaf(d1, u[2], acc[2]);
+        acc[3] = fmaf(d1, u[3], acc[3]);
+        acc[0] = fmaf(-dm0, mv[0], acc[0]);
+        acc[1] = fmaf(-dm0, mv[1], acc[1]);
+        acc[2] = fmaf(-dm1, mv[2], acc[2]);
+        acc[3] = fmaf(-dm1, mv[3], acc[3]);
+    };
+
+    int buf = 0;
+    for (; tile < n_tiles; tile += gridDim.x) {
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // items of this tile, two register sets in turn; the item after the
+        // last one of the tile is the first of the next tile
+        for (int sb = sb_lo; sb < sb_hi; sb += 2) {
+            {
+                const bool more = sb + 1 < sb_hi;
+                const int64_t nt = more ? tile : tile + gridDim.x;
+                if (nt < n_tiles) load_item(wb, nt, more ? sb + 1 : sb_lo);
+            }
+            process(wa, sb, acc);
+            if (sb + 1 >= sb_hi) {
+                wa = wb;   // odd count: the next tile's first item is in wb
+                break;
+            }
+            {
+                const bool more = sb + 2 < sb_hi;
+                const int64_t nt = more ? tile : tile + gridDim.x;
+                if (nt < n_tiles) load_item(wa, nt, more ? sb + 2 : sb_lo);
+            }
+            process(wb, sb + 1, acc);
+        }
+        // sum the warps' partial results of this tile in a fixed order
+        red[(buf * nw + warp) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        __syncthreads();
+        for (int i = tid; i < 128; i += blockDim.x) {   // 16 rows x 8 tokens
+            const int l = i >> 2, e = i & 3;
+            float s = 0.0f;
+            for (int j = 0; j < nw; j++) {
+                const float4 v = red[(buf * nw + j) * 32 + l];
+                s += e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+            }
+            const int64_t row = tile * 16 + (l >> 2) + 8 * (e >> 1);
+            const int tok = 2 * (l & 3) + (e & 1);
+            if (row < n && tok < m_act) store_out(y, yt, (int64_t)tok * ldy + row, s);
+        }
+        buf ^= 1;
+    }
+}
+
+inline int mma_q4k_warps(int64_t k) {
+    int nw = (int)(k / 256 / 2);
+    return nw < 1 ? 1 : nw > 16 ? 16 : nw;
+}
+// whether the q8_1 rows fit in shared memory (K <= 16384)
+inline bool mma_q4k_fits(int64_t k) {
+    return mma_smem_layout(k, mma_q4k_warps(k)).total <= (int64_t)device_info().smem_optin;
+}
+
+inline cudaError_t launch_mmvq_mma_q4k(const uint8_t *w, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y,
+                                       int yt, int64_t ldy, cudaStream_t s) {
+    const int nw = mma_q4k_warps(k);
+    const MmaSmem L = mma_smem_layout(k, nw);
+    if (L.total > (int64_t)device_info().smem_optin) return cudaErrorInvalidValue;
+    auto kern = mmvq_mma_q4k_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nw * 32, (size_t)L.total);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t n_tiles = (n + 15) / 16;
+    int64_t grid = (int64_t)device_info().sm_count * per_sm;
+    if (grid > n_tiles) grid = n_tiles;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)(nw * 32));
+    cfg.dynamicSmemBytes = (size_t)L.total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, w, n, k, k / 256 * (int64_t)Q4_K_BYTES, xq, (int)m, y, yt, ldy);
+}
+
+}  // namespace gg

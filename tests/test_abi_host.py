@@ -95,3 +95,4 @@ def test_other_entry_points_reject_bad_arguments(g):
     assert L.gguf_debug_block_dots(FAKE, g.F32, 4, 256, FAKE, 1, FAKE, None) == 2
     assert L.gguf_set_option(b"no_such_key", 1) == 1
     assert L.gguf_set_option(b"mmvq_max_m", 8) == 0 and L.gguf_get_option(b"mmvq_max_m") == 8
+    assert L.gguf_get_option(b"mmvq_tc") == 1

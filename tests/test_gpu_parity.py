@@ -165,6 +165,25 @@ def test_mmvq_k_range_bf16(g, wt, k, m):
     assert_close(y.float().cpu().numpy(), ref, TOL_BF16, f"mmvq bf16 type {wt} k {k} m {m}")
 
 
+@pytest.mark.parametrize("k", [256, 1024, 3072, 8192])
+@pytest.mark.parametrize("m", [5, 8])
+def test_mmvq_tensor_core_vs_dp4a(g, k, m):
+    # 5..8 tokens of Q4_K rows (n >= 2048) run on the tensor-core MMVQ by
+    # default; the dp4a kernel (option mmvq_tc = 0) computes the same formula
+    n = 2100
+    w = _weights(oracle.Q4_K, n, k, seed=k + m)
+    x = synth.activations(m, k, seed=k, dtype=torch.float32)
+    ref = oracle.mul_mat(oracle.Q4_K, w, k, oracle.quantize_q8_1(x.numpy()))
+    a = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x.to(DEV)).cpu().numpy()
+    g.gguf_set_option("mmvq_tc", 0)
+    try:
+        b = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x.to(DEV)).cpu().numpy()
+    finally:
+        g.gguf_set_option("mmvq_tc", 1)
+    assert_close(a, ref, TOL_F32, f"tensor-core mmvq k {k} m {m}")
+    assert_close(b, ref, TOL_F32, f"dp4a mmvq k {k} m {m}")
+
+
 @pytest.mark.parametrize("wt,n,k", [(oracle.Q6_K, 40000, 3072), (oracle.Q4_K, 20000, 3072)])
 @pytest.mark.parametrize("m", [1, 2, 8])
 def test_mmvq_tall_sampled(g, wt, n, k, m):
