@@ -230,7 +230,7 @@ static MoeWs moe_call_layout(const gguf_moe_args *a, void *base) {
     const int64_t R = a->n_tokens * a->top_k;
     const int64_t kx = op_pitch(a->wt, a->k);
     if (a->mode == GGUF_MOE_GATE_UP_SWIGLU) return moe_ws_layout(base, a->n_experts, R, a->n_tokens * kx, 0, 0, false);
-    return moe_ws_layout(base, a->n_experts, R, R * kx, a->n_tokens * a->n, 0, false);
+    return moe_ws_layout(base, a->n_experts, R, R * kx, R * a->n, 0, false);
 }
 
 static gguf_status check_moe(const gguf_moe_args *a) {
@@ -295,17 +295,17 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
     }
     if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), s)) != cudaSuccess) return cuda_status(e, "mul_mat_id quantize");
     if ((e = moe_group(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id grouping");
-    if ((e = cudaMemsetAsync(w.yacc, 0, sizeof(float) * (size_t)(a->n_tokens * a->n), s)) != cudaSuccess) return cuda_status(e, "mul_mat_id");
     if ((e = launch_moe_down((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, w.xl, a->top_k, R,
-                             a->n_experts, a->route_w, w, w.yacc, a->yt == GGUF_F32, s)) != cudaSuccess)
+                             a->n_experts, w, w.z, a->yt == GGUF_F32, s)) != cudaSuccess)
         return cuda_status(e, "mul_mat_id down");
-    return cuda_status(launch_moe_finalize(w.yacc, a->n_tokens * a->n, a->y, a->yt, s), "mul_mat_id finalize");
+    return cuda_status(launch_moe_finalize(w.z, w.pos, a->route_w, a->n_tokens, a->top_k, a->n, a->y, a->yt, s),
+                       "mul_mat_id finalize");
 }
 
 static MoeWs ffn_layout(const gguf_moe_ffn_args *a, void *base) {
     const int64_t R = a->n_tokens * a->top_k;
     return moe_ws_layout(base, a->n_experts, R, a->n_tokens * op_pitch(a->gate_up_type, a->hidden),
-                         a->n_tokens * a->hidden, R * op_pitch(a->down_type, a->inter), a->yt == GGUF_F32);
+                         R * a->hidden, R * op_pitch(a->down_type, a->inter), a->yt == GGUF_F32);
 }
 
 size_t gguf_moe_ffn_ws_size(const gguf_moe_ffn_args *a) {
@@ -343,11 +343,11 @@ gguf_status gguf_moe_ffn(const gguf_moe_ffn_args *a, void *ws, size_t ws_bytes, 
                                 a->hidden, w.xh, w.xl, a->top_k, R, a->n_experts, w, nullptr, nullptr, w.h16, w.h16lo,
                                 op_pitch(a->down_type, a->inter), s)) != cudaSuccess)
         return cuda_status(e, "moe_ffn gate_up");
-    if ((e = cudaMemsetAsync(w.yacc, 0, sizeof(float) * (size_t)(a->n_tokens * a->hidden), s)) != cudaSuccess) return cuda_status(e, "moe_ffn");
     if ((e = launch_moe_down((const uint8_t *)a->w_down, a->down_type, a->down_stride, a->hidden, a->inter, w.h16,
-                             w.h16lo, a->top_k, R, a->n_experts, a->route_w, w, w.yacc, a->yt == GGUF_F32, s)) != cudaSuccess)
+                             w.h16lo, a->top_k, R, a->n_experts, w, w.z, a->yt == GGUF_F32, s)) != cudaSuccess)
         return cuda_status(e, "moe_ffn down");
-    return cuda_status(launch_moe_finalize(w.yacc, a->n_tokens * a->hidden, a->y, a->yt, s), "moe_ffn finalize");
+    return cuda_status(launch_moe_finalize(w.z, w.pos, a->route_w, a->n_tokens, a->top_k, a->hidden, a->y, a->yt, s),
+                       "moe_ffn finalize");
 }
 
 gguf_status gguf_debug_block_dots(const void *w, int wt, int64_t n, int64_t k, const void *xq, int64_t m,

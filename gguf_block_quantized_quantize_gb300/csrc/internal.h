@@ -56,12 +56,12 @@ cudaError_t launch_convert_rows(const float *yacc, int64_t m, int64_t n, void *y
 struct MoeWs {
     int32_t *counts, *offsets, *pos, *route_list, *tile_expert, *tile_start, *n_tiles;
     uint16_t *xh, *xl;
-    float *yacc;
+    float *z;  // per-route outputs of the down GEMM [R][n]
     uint16_t *h16, *h16lo;
     size_t bytes;
 };
 // base == nullptr computes only the size
-MoeWs moe_ws_layout(void *base, int64_t E, int64_t R, int64_t xh_elems, int64_t yacc_elems, int64_t h16_elems,
+MoeWs moe_ws_layout(void *base, int64_t E, int64_t R, int64_t xh_elems, int64_t z_elems, int64_t h16_elems,
                     bool with_lo);
 int moe_bn(int64_t routes, int64_t experts);
 cudaError_t moe_group(const int32_t *ids, const float *rw, int64_t R, int64_t E, bool skip_zero_w, int32_t *status,
@@ -72,7 +72,8 @@ cudaError_t launch_moe_gate_up(const uint8_t *w, int wt, int64_t expert_stride, 
                                int64_t hpitch, cudaStream_t s);
 cudaError_t launch_moe_down(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
                             const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
-                            const float *route_w, const MoeWs &ws, float *yacc, bool precise, cudaStream_t s);
-cudaError_t launch_moe_finalize(const float *yacc, int64_t count, void *y, int yt, cudaStream_t s);
+                            const MoeWs &ws, float *z, bool precise, cudaStream_t s);
+cudaError_t launch_moe_finalize(const float *z, const int32_t *pos, const float *route_w, int64_t T, int64_t top_k,
+                                int64_t n, void *y, int yt, cudaStream_t s);
 
 }  // namespace gg

@@ -18,17 +18,18 @@
 // The GEMM is launched with an upper bound of tiles (routes / BN + experts);
 // CTAs past the device-side tile count exit at once.
 //
-// GEMM tile: 128 weight rows x BN routes x 64 K per stage (4 stages), the same
-// fp16 tcgen05 engine as the dense MMQ.  The activation rows of a tile are
-// gathered with cp.async (token rows for gate_up, route rows for down); the
-// last tile of an expert issues the MMA with N rounded up to 16 only.
+// GEMM tile: 128 weight rows x BN routes x 64 K per stage, the same fp16
+// tcgen05 engine as the dense MMQ.  The activation rows of a tile are gathered
+// by TMA tile::gather4 (token rows for gate_up, route rows for down); the last
+// tile of an expert issues the MMA with N rounded up to 16 only.
 //   gate_up : the A tile holds 64 gate rows i and the 64 matching up rows I+i,
 //             so the epilogue has g and u of the same (route, i): it computes
 //             h = silu(g) * u in fp32, rounds it to bf16 (the activation dtype),
 //             quantizes each 32 consecutive i (one warp) to a q8_1 block, and
 //             writes q8_1 / bf16 / fp16 (d16*q, the operand of the down GEMM).
-//   down    : y_acc[t][n] += route_w * (W_down[e] . h_route) with fp32 atomics;
-//             a last pass converts y_acc to the output dtype.
+//   down    : z[route][n] = W_down[e] . h_route (fp32, plain stores); a last
+//             pass sums each token's routes in slot order, y[t] = sum_k w_k z,
+//             so the result is deterministic and needs no atomics.
 #include <mutex>
 
 #include "tcgemm.cuh"
@@ -108,10 +109,36 @@ __global__ void moe_scatter_kernel(const int32_t *__restrict__ ids, const int32_
     if (p >= 0) route_list[offsets[ids[r]] + p] = (int32_t)r;
 }
 
-// y[t][n] (out dtype) from the fp32 accumulator
-__global__ void moe_finalize_kernel(const float *__restrict__ yacc, int64_t count, void *__restrict__ y, int yt) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < count) store_out(y, yt, i, yacc[i]);
+// y[t][c] = sum over the token's route slots k (in order) of w_k * z[t*top_k + k][c];
+// routes that were not grouped (inactive id, or weight 0) have pos = -1 and no z row
+// V consecutive columns per thread (V = 4 when n % 4 == 0: 16-byte loads)
+template <int V>
+__global__ void moe_finalize_kernel(const float *__restrict__ z, const int32_t *__restrict__ pos,
+                                    const float *__restrict__ route_w, int64_t T, int64_t top_k, int64_t n,
+                                    void *__restrict__ y, int yt) {
+    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * V;
+    if (i >= T * n) return;
+    const int64_t t = i / n, c = i - t * n;
+    float acc[V];
+#pragma unroll
+    for (int v = 0; v < V; v++) acc[v] = 0.0f;
+    for (int64_t k = 0; k < top_k; k++) {
+        const int64_t r = t * top_k + k;
+        if (pos[r] < 0) continue;
+        const float w = route_w ? route_w[r] : 1.0f;
+        if (V == 4) {
+            const float4 zv = *reinterpret_cast<const float4 *>(z + r * n + c);
+            acc[0] = fmaf(w, zv.x, acc[0]);
+            acc[1] = fmaf(w, zv.y, acc[1]);
+            acc[2] = fmaf(w, zv.z, acc[2]);
+            acc[3] = fmaf(w, zv.w, acc[3]);
+        } else {
+#pragma unroll
+            for (int v = 0; v < V; v++) acc[v] = fmaf(w, z[r * n + c + v], acc[v]);
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < V; v++) store_out(y, yt, i + v, acc[v]);
 }
 
 // ---------------------------------------------------------------- host side
@@ -125,9 +152,9 @@ int moe_bn(int64_t routes, int64_t experts) {
 }
 
 // Carve the workspace (base == nullptr: only compute the size): grouping
-// tables, the fp16 activation operand (hi and lo parts), the fp32 output
-// accumulator and the fp16 intermediate (each optional: 0 elements).
-MoeWs moe_ws_layout(void *base, int64_t E, int64_t R, int64_t xh_elems, int64_t yacc_elems, int64_t h16_elems,
+// tables, the fp16 activation operand (hi and lo parts), the fp32 per-route
+// outputs of the down GEMM and the fp16 intermediate (each optional: 0 elements).
+MoeWs moe_ws_layout(void *base, int64_t E, int64_t R, int64_t xh_elems, int64_t z_elems, int64_t h16_elems,
                     bool with_lo) {
     MoeWs w{};
     uint8_t *p = reinterpret_cast<uint8_t *>(base);
@@ -148,7 +175,7 @@ MoeWs moe_ws_layout(void *base, int64_t E, int64_t R, int64_t xh_elems, int64_t 
     w.n_tiles = (int32_t *)take(sizeof(int32_t));
     w.xh = (uint16_t *)take(sizeof(uint16_t) * (size_t)xh_elems);
     w.xl = (uint16_t *)take(sizeof(uint16_t) * (size_t)xh_elems);  // low parts: the gate_up is always precise
-    w.yacc = (float *)take(sizeof(float) * (size_t)yacc_elems);
+    w.z = (float *)take(sizeof(float) * (size_t)z_elems);
     w.h16 = (uint16_t *)take(sizeof(uint16_t) * (size_t)h16_elems);
     w.h16lo = (uint16_t *)take(sizeof(uint16_t) * (size_t)(with_lo ? h16_elems : 0));
     w.bytes = off;
@@ -166,14 +193,19 @@ cudaError_t moe_group(const int32_t *ids, const float *rw, int64_t R, int64_t E,
     return cudaGetLastError();
 }
 
+// rows: operand rows (tokens for gate_up, routes for down), each p.kx fp16;
+// the gather reads one-row boxes of 64 values
 template <int MODE, bool PRECISE>
-static cudaError_t launch_moe_mode(int wt, const TgParams &p, cudaStream_t s) {
-    CUtensorMap dummy{};
+static cudaError_t launch_moe_mode(int wt, const TgParams &p, int64_t rows, cudaStream_t s) {
+    CUtensorMap mh{}, ml{};
+    cudaError_t e = tg_make_map(&mh, p.xh, rows, p.kx, 1);
+    if (e == cudaSuccess && PRECISE) e = tg_make_map(&ml, p.xl, rows, p.kx, 1);
+    if (e != cudaSuccess) return e;
     const int grid = device_info().sm_count;  // persistent; CTAs beyond the device-side tile count exit
     switch (wt) {
-    case GGUF_Q4_K: return tg_launch<GGUF_Q4_K, MOE_BN, PRECISE, MODE, GGUF_F32>(dummy, dummy, p, grid, s);
-    case GGUF_Q6_K: return tg_launch<GGUF_Q6_K, MOE_BN, PRECISE, MODE, GGUF_F32>(dummy, dummy, p, grid, s);
-    case GGUF_Q8_0: return tg_launch<GGUF_Q8_0, MOE_BN, PRECISE, MODE, GGUF_F32>(dummy, dummy, p, grid, s);
+    case GGUF_Q4_K: return tg_launch<GGUF_Q4_K, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, p, grid, s);
+    case GGUF_Q6_K: return tg_launch<GGUF_Q6_K, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, p, grid, s);
+    case GGUF_Q8_0: return tg_launch<GGUF_Q8_0, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, p, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -214,26 +246,33 @@ cudaError_t launch_moe_gate_up(const uint8_t *w, int wt, int64_t expert_stride, 
     p.hbf = hbf;
     p.h16 = h16;
     p.h16lo = h16lo;
-    return launch_moe_mode<TG_MOE_GATE_UP, true>(wt, p, s);
+    p.m = R / top_k;  // token rows of the operand
+    return launch_moe_mode<TG_MOE_GATE_UP, true>(wt, p, p.m, s);
 }
 
-// down + weighted sum: yacc[T][n] += route_w * (W[e] . x[route]); xh / xl:
-// route rows [R][k] (xl only in the precise mode)
+// down: z[R][n] = W[e] . x[route] for every grouped route; xh / xl: route
+// rows [R][kx] (xl only in the precise mode)
 cudaError_t launch_moe_down(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
                             const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
-                            const float *route_w, const MoeWs &ws, float *yacc, bool precise, cudaStream_t s) {
+                            const MoeWs &ws, float *z, bool precise, cudaStream_t s) {
     (void)E;
     if (R == 0) return cudaSuccess;
     TgParams p = moe_params(w, wt, expert_stride, n, k, xh, xl, top_k, ws);
     p.tiles_x = (int)((n + TG_BM - 1) / TG_BM);
-    p.route_w = route_w;
-    p.yacc = yacc;
-    return precise ? launch_moe_mode<TG_MOE_DOWN, true>(wt, p, s) : launch_moe_mode<TG_MOE_DOWN, false>(wt, p, s);
+    p.yacc = z;
+    p.m = R / top_k;  // tokens; the operand has R = top_k * m rows
+    return precise ? launch_moe_mode<TG_MOE_DOWN, true>(wt, p, R, s) : launch_moe_mode<TG_MOE_DOWN, false>(wt, p, R, s);
 }
 
-cudaError_t launch_moe_finalize(const float *yacc, int64_t count, void *y, int yt, cudaStream_t s) {
+// y[T][n] = the route-weighted sum of each token's z rows (out dtype)
+cudaError_t launch_moe_finalize(const float *z, const int32_t *pos, const float *route_w, int64_t T, int64_t top_k,
+                                int64_t n, void *y, int yt, cudaStream_t s) {
+    const int64_t count = T * n;
     if (count == 0) return cudaSuccess;
-    moe_finalize_kernel<<<(unsigned)((count + 255) / 256), 256, 0, s>>>(yacc, count, y, yt);
+    if (n % 4 == 0)   // z rows are 16-byte aligned (workspace base 256-aligned, n % 4 == 0)
+        moe_finalize_kernel<4><<<(unsigned)((count / 4 + 255) / 256), 256, 0, s>>>(z, pos, route_w, T, top_k, n, y, yt);
+    else
+        moe_finalize_kernel<1><<<(unsigned)((count + 255) / 256), 256, 0, s>>>(z, pos, route_w, T, top_k, n, y, yt);
     return cudaGetLastError();
 }
 

@@ -4,9 +4,11 @@
 //
 // Operands (all fp16, K-major, 128-byte swizzled rows of 64 values):
 //   A = weight rows, unpacked in registers from the packed GGUF blocks
-//       (unpack.cuh) by 8 producer warps, each thread half a row per K-step;
-//   B = activation rows (the fp16 form d16 * q of q8_1 values), loaded by TMA
-//       (dense) or gathered row by row with cp.async (MoE).
+//       (unpack.cuh) by 8 producer warps; per K-step a thread takes one part
+//       (half or quarter) of one or two rows, consecutive lanes sharing a
+//       row, so that each warp-wide load reads 16 (8) rows of contiguous bytes;
+//   B = activation rows (the fp16 form d16 * q of q8_1 values), loaded by TMA:
+//       tiles (dense) or tile::gather4 of the routed rows (MoE; 4 rows per copy).
 // Precision modes:
 //   FAST    one fp16 operand per side (packed-half unpack for 16-bit outputs);
 //           the product differs from the exact blockwise value by two fp16
@@ -16,7 +18,7 @@
 //           result matches the exact blockwise value to about 1e-6.  Used for
 //           fp32 outputs and for the MoE intermediate, which is re-quantized.
 // Roles (448 threads):
-//   warp 0      B producer (TMA: one elected lane; gather: all 32 lanes)
+//   warp 0      B producer (dense: one elected lane; MoE: lane i gathers rows 4i .. 4i+3)
 //   warp 1      TMEM allocator + the MMA-issuing thread (two accumulators)
 //   warps 2-9   A producers
 //   warps 10-13 epilogue (TMEM lane quadrant = warp % 4), overlapping the next
@@ -52,7 +54,7 @@ struct TgParams {
     void *y;
     int yt;
     int64_t ldy;
-    float *yacc;  // split-K partial sums [m][n] (dense) or the MoE output accumulator [T][n] (down)
+    float *yacc;  // split-K partial sums [m][n] (dense) or the per-route outputs [R][n] (MoE down)
     // gathered activation rows (MoE)
     const uint16_t *xh, *xl;
     int64_t top_k;
@@ -65,24 +67,20 @@ struct TgParams {
     int64_t hpitch;  // row length of h16 / h16lo: I, plus correction columns when the down weights are Q4_K
 };
 
-template <int BN, bool PRECISE>
+template <int BN, bool PRECISE, int MODE>
 struct TgShape {
     static constexpr int OPS = PRECISE ? 2 : 1;
     static constexpr int A_STAGE = OPS * TG_A_BYTES;
     static constexpr int B_STAGE = OPS * BN * TG_BK * 2;
-    static constexpr int XBUF = 64 * 32 * 4;  // gate_up exchange: 64 rows x 32 columns of fp32
-    static constexpr int STAGES_RAW = (200 * 1024 - XBUF) / (A_STAGE + B_STAGE);
+    // gate_up exchange: gate and up values of 64 rows x 32 routes, fp32
+    static constexpr int XBUF = MODE == TG_MOE_GATE_UP ? 2 * 64 * 32 * 4 : 0;
+    static constexpr int FIXED = 1024 + XBUF + 512 + BN * 8;
+    static constexpr int STAGES_RAW = (220 * 1024 - FIXED) / (A_STAGE + B_STAGE);
     static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
-    static constexpr int SMEM = 1024 + STAGES * (A_STAGE + B_STAGE) + XBUF + 512 + BN * 8;
+    static constexpr int SMEM = FIXED + STAGES * (A_STAGE + B_STAGE);
     static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
 };
 
-__device__ __forceinline__ void tg_cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void tg_cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void tg_cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void tg_named_bar(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -123,7 +121,7 @@ template <int WT, int BN, bool PRECISE, int MODE, int OT>
 __global__ void __launch_bounds__(TG_THREADS, 1)
     tg_kernel(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo, const TgParams p,
               int *err) {
-    using S = TgShape<BN, PRECISE>;
+    using S = TgShape<BN, PRECISE, MODE>;
     constexpr int ST = S::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -145,7 +143,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
     if (tid == 0) {
         for (int s = 0; s < ST; s++) {
             tc::mbar_init(&full_a[s], TG_PRODUCERS);
-            tc::mbar_init(&full_b[s], MODE == TG_DENSE ? 1 : 32);
+            tc::mbar_init(&full_b[s], 1);
             tc::mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; b++) {
@@ -154,10 +152,8 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
         }
         *abort_flag = 0;
         tc::fence_barrier_init();
-        if (MODE == TG_DENSE) {
-            tc::prefetch_tmap(&map_hi);
-            if (PRECISE) tc::prefetch_tmap(&map_lo);
-        }
+        tc::prefetch_tmap(&map_hi);
+        if (PRECISE) tc::prefetch_tmap(&map_lo);
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, S::TMEM_COLS);
@@ -174,7 +170,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
 
     if (warp == 0) {
         // ================= B producer
-        if (MODE == TG_DENSE) {
+        if constexpr (MODE == TG_DENSE) {
             if (lane == 0) {
                 int it = 0, last = 0;
                 for (int t = blockIdx.x; t < tiles_total && !*abort_flag; t += gridDim.x) {
@@ -196,54 +192,43 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                         tc::mbar_wait(&full_b[i % ST], (uint32_t)(i / ST) & 1u);
             }
         } else {
-            // gather: lane handles rows lane, lane + 32, ... of the tile
-            constexpr int RPL = (BN + 31) / 32;
-            constexpr int LAG = 2;  // cp.async groups in flight per lane
-            int it = 0;
+            // gather: lane i loads rows 4i .. 4i+3 of the tile with one
+            // tile::gather4 per operand; slots past the routes read row
+            // `rows` of the operand, out of range, i.e. zeros
+            static_assert(BN == 128, "the MoE gather assigns 4 rows to each of 32 lanes");
+            const int32_t oob = (int32_t)(MODE == TG_MOE_GATE_UP ? p.m : p.top_k * p.m);
+            int it = 0, last = 0;
             for (int t = blockIdx.x; t < tiles_total && !*abort_flag; t += gridDim.x) {
                 const TgTile d = tg_tile<MODE, BN>(p, t, KS);
-                int64_t srow[RPL];
+                int32_t rows[4];
 #pragma unroll
-                for (int i = 0; i < RPL; i++) {
-                    const int j = lane + 32 * i;
-                    const int r = (j < BN && j < d.n_eff) ? p.route_list[d.route0 + j] : -1;
-                    srow[i] = r < 0 ? -1 : (MODE == TG_MOE_GATE_UP ? r / p.top_k : r);
+                for (int i = 0; i < 4; i++) {
+                    const int j = 4 * lane + i;
+                    const int r = j < d.n_eff ? p.route_list[d.route0 + j] : -1;
+                    rows[i] = r < 0 ? oob : (int32_t)(MODE == TG_MOE_GATE_UP ? r / p.top_k : r);
                 }
-                const int it0 = it;
                 for (int ks = 0; ks < KS; ks++, it++) {
                     const int s = it % ST;
                     const uint32_t ph = (uint32_t)(it / ST) & 1u;
                     if (*abort_flag) break;
-                    if (!tc::mbar_wait(&empty[s], ph ^ 1u)) { fail(1); break; }
-                    const uint32_t bbase = tc::smem_u32(sB + s * S::B_STAGE);
-#pragma unroll
-                    for (int i = 0; i < RPL; i++) {
-                        const int j = lane + 32 * i;
-                        if (j >= BN) continue;
-#pragma unroll
-                        for (int c = 0; c < 8; c++) {
-                            const int64_t kk = (int64_t)ks * TG_BK + 8 * c;
-                            const bool v = srow[i] >= 0 && kk < p.kx;
-                            const uint32_t off = (uint32_t)(j * 128 + ((c ^ (j & 7)) * 16));
-                            tg_cp_async16(bbase + off, v ? (const void *)(p.xh + srow[i] * p.kx + kk) : (const void *)p.xh,
-                                          v ? 16u : 0u);
-                            if (PRECISE)
-                                tg_cp_async16(bbase + BN * TG_BK * 2 + off,
-                                              v ? (const void *)(p.xl + srow[i] * p.kx + kk) : (const void *)p.xl,
-                                              v ? 16u : 0u);
-                        }
+                    bool ok = true;
+                    if (lane == 0) {
+                        ok = tc::mbar_wait(&empty[s], ph ^ 1u);
+                        if (ok) tc::mbar_arrive_expect_tx(&full_b[s], (uint32_t)S::B_STAGE);
                     }
-                    tg_cp_commit();
-                    if (it - it0 >= LAG) {
-                        tg_cp_wait<LAG>();
-                        tc::fence_proxy_async_smem();
-                        tc::mbar_arrive(&full_b[(it - LAG) % ST]);
-                    }
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                    if (!ok) { if (lane == 0) fail(1); break; }
+                    uint8_t *dst = sB + s * S::B_STAGE + lane * 4 * 128;
+                    tc::tma_gather4(dst, &map_hi, &full_b[s], ks * TG_BK, rows[0], rows[1], rows[2], rows[3]);
+                    if (PRECISE)
+                        tc::tma_gather4(dst + BN * TG_BK * 2, &map_lo, &full_b[s], ks * TG_BK, rows[0], rows[1], rows[2],
+                                        rows[3]);
+                    last = it + 1;
                 }
-                tg_cp_wait<0>();
-                tc::fence_proxy_async_smem();
-                for (int i = (it - LAG > it0 ? it - LAG : it0); i < it; i++) tc::mbar_arrive(&full_b[i % ST]);
             }
+            if (*abort_flag && lane == 0)  // copies already issued land before the CTA exits
+                for (int i = last - ST < 0 ? 0 : last - ST; i < last; i++)
+                    tc::mbar_wait(&full_b[i % ST], (uint32_t)(i / ST) & 1u);
         }
     } else if (warp == 1) {
         // ================= MMA issuer
@@ -283,76 +268,116 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             }
         }
     } else if (warp < 2 + TG_PRODUCERS / 32) {
-        // ================= A producers: thread p -> row p % 128, half p / 128
-        const int pidx = tid - 64;
-        const int r = pidx & (TG_BM - 1), half = pidx >> 7;
+        // ================= A producers: thread p takes part p % PARTS of tile
+        // rows p / PARTS + RP * i (RP = 256 / PARTS rows per pass); one
+        // warp-wide load covers 32 / PARTS rows of contiguous bytes
+        using U = KQ<WT>;
+        constexpr int PARTS = U::PARTS, RP = TG_PRODUCERS / PARTS, TPT = TG_BM / RP;
+        constexpr int VW = 8 * U::CHUNKS;  // fp32 values per task
+        constexpr int DEPTH = 2;           // K-steps loaded ahead (deeper unrolling costs i-cache)
+        // lane -> (row, part): each group of 8 lanes takes one part of 8
+        // different rows, so a 16-byte swizzled store is conflict-free within
+        // every 8-lane phase, and the parts of a row are in the same warp so a
+        // warp-wide load still reads whole 32-byte sectors
+        const int pw = warp - 2, pl = lane;
+        const int part = (pl >> 3) % PARTS;
+        const int r0 = (32 / PARTS) * pw + (pl & 7) + 8 * (pl / (8 * PARTS));
+        const int64_t kblocks = p.k / 32;
         int it = 0;
         for (int t = blockIdx.x; t < tiles_total && !*abort_flag; t += gridDim.x) {
             const TgTile d = tg_tile<MODE, BN>(p, t, KS);
-            int64_t row;
-            if (MODE == TG_MOE_GATE_UP) row = r < 64 ? d.row0 + r : p.n / 2 + d.row0 + (r - 64);
-            else row = d.row0 + r;
-            const bool live = row < p.n;
-            const uint8_t *wrow = p.w + (MODE == TG_DENSE ? 0 : (int64_t)d.e * p.expert_stride) + (live ? row : 0) * p.rb;
-            KHalf<WT> u0, u1;
-            if constexpr (WT == GGUF_Q8_0) { u0.kblocks = p.k / 32; u1.kblocks = p.k / 32; }
-            const int kw1 = d.k1 < KS_W ? d.k1 : KS_W;  // weight K steps of this tile
-            if (live) {
-                if (d.k0 < kw1) u0.load(wrow, d.k0, half);
-                if (d.k0 + 1 < kw1) u1.load(wrow, d.k0 + 1, half);
+            bool live[TPT];
+            const uint8_t *wrow[TPT];
+            const uint8_t *wbase = p.w + (MODE == TG_DENSE ? 0 : (int64_t)d.e * p.expert_stride);
+#pragma unroll
+            for (int i = 0; i < TPT; i++) {
+                const int r = r0 + RP * i;
+                // gate_up tiles: rows 0..63 are gate rows, 64..127 the matching up rows
+                int64_t row;
+                if (MODE == TG_MOE_GATE_UP) {
+                    row = r < 64 ? d.row0 + r : p.n / 2 + d.row0 + (r - 64);
+                    live[i] = (r < 64 ? d.row0 + r : d.row0 + (r - 64)) < p.n / 2;
+                } else {
+                    row = d.row0 + r;
+                    live[i] = row < p.n;
+                }
+                wrow[i] = wbase + (live[i] ? row : 0) * p.rb;
             }
-            // one K step: unpack (weight steps) or the min-term correction values
-            // dmin * m_j of 32 sub-blocks (Q4_K steps past the weights), then store
-            auto produce = [&](const KHalf<WT> &u, int ks) -> bool {
-                const int s = it % ST;
-                const uint32_t ph = (uint32_t)(it / ST) & 1u;
-                it++;
-                uint32_t hi[16], lo[16];
+            const int kw1 = d.k1 < KS_W ? d.k1 : KS_W;  // weight K steps of this tile
+            U u[DEPTH][TPT];                             // tasks of steps ks .. ks + DEPTH - 1
+            auto load_step = [&](U (&uu)[TPT], int ks) {
+                if (ks >= kw1) return;
 #pragma unroll
-                for (int i = 0; i < 16; i++) { hi[i] = 0u; lo[i] = 0u; }
-                if (live && ks < KS_W) {
-                    if (H2) u.unpack_h2(ks, half, hi);
-                    else {
-                        float v[32];
-                        u.unpack_f32(ks, half, v);
-                        if (PRECISE) pack_split(v, hi, lo);
-                        else pack_single(v, hi);
+                for (int i = 0; i < TPT; i++)
+                    if (live[i]) uu[i].load(wrow[i], ks, part, kblocks);
+            };
+#pragma unroll
+            for (int dd = 0; dd < DEPTH; dd++) load_step(u[dd], d.k0 + dd);
+            // one task: unpack (weight steps) or the Q4_K min-term correction
+            // values dmin * m_j of 8 sub-blocks per chunk (steps past the weights)
+            auto task = [&](const U &u, int i, int ks, uint32_t (&hi)[VW / 2], uint32_t (&lo)[VW / 2]) {
+#pragma unroll
+                for (int w = 0; w < VW / 2; w++) { hi[w] = 0u; lo[w] = 0u; }
+                if (!live[i]) return;
+                if (ks < KS_W) {
+                    if (H2) {
+                        u.unpack_h2(ks, hi);
+                    } else {
+                        float v[VW];
+                        u.unpack_f32(ks, v);
+                        if (PRECISE) pack_split<VW>(v, hi, lo);
+                        else pack_single<VW>(v, hi);
                     }
-                } else if (live && WT == GGUF_Q4_K) {
-                    const int64_t j0 = (int64_t)ks * TG_BK - p.k + 32 * half;  // first sub-block of this half
-                    const int64_t nsub = p.k / 32;
-                    float v[32];
+                } else if (WT == GGUF_Q4_K) {
+                    // chunk c of this step holds the corrections of super-block
+                    // (ks * 64 - k) / 64 + c of the row
+                    const int64_t nsb = p.k / 256;
+                    const int64_t sb0 = ((int64_t)ks * TG_BK - p.k) / 8;
+                    float v[VW];
 #pragma unroll
-                    for (int g4 = 0; g4 < 4; g4++) {  // 8 sub-blocks per super-block header
-                        const int64_t sb = j0 / 8 + g4;
+                    for (int e = 0; e < U::CHUNKS; e++) {
+                        const int64_t sb = sb0 + U::chunk(part, e);
                         uint4 hdr = make_uint4(0, 0, 0, 0);
-                        if (sb * 8 < nsub) hdr = *reinterpret_cast<const uint4 *>(wrow + sb * Q4_K_BYTES);
+                        if (sb < nsb) hdr = *reinterpret_cast<const uint4 *>(wrow[i] + sb * Q4_K_BYTES);
                         const uint32_t sc[3] = {hdr.y, hdr.z, hdr.w};
                         const float dmin = h2f(hdr.x >> 16);
 #pragma unroll
                         for (int jj = 0; jj < 8; jj++) {
                             int sv, mv;
                             q4k_scale_min(sc, jj, sv, mv);
-                            v[8 * g4 + jj] = (sb * 8 + jj < nsub) ? __fmul_rn(dmin, (float)mv) : 0.0f;
+                            v[8 * e + jj] = sb < nsb ? __fmul_rn(dmin, (float)mv) : 0.0f;
                         }
                     }
-                    pack_single(v, hi);
+                    pack_single<VW>(v, hi);
                 }
+            };
+            auto produce = [&](const U (&uu)[TPT], int ks) -> bool {
+                const int s = it % ST;
+                const uint32_t ph = (uint32_t)(it / ST) & 1u;
+                it++;
+                uint32_t hi[TPT][VW / 2], lo[TPT][VW / 2];
+#pragma unroll
+                for (int i = 0; i < TPT; i++) task(uu[i], i, ks, hi[i], lo[i]);
                 if (*abort_flag) return false;
                 if (!tc::mbar_wait(&empty[s], ph ^ 1u)) { fail(4); return false; }
-                store_sw128_half(sA + s * S::A_STAGE, r, half, hi);
-                if (PRECISE) store_sw128_half(sA + s * S::A_STAGE + TG_A_BYTES, r, half, lo);
+                uint8_t *tile = sA + s * S::A_STAGE;
+#pragma unroll
+                for (int i = 0; i < TPT; i++) {
+                    store_sw128_task<U>(tile, r0 + RP * i, part, hi[i]);
+                    if (PRECISE) store_sw128_task<U>(tile + TG_A_BYTES, r0 + RP * i, part, lo[i]);
+                }
                 tc::fence_proxy_async_smem();
                 tc::mbar_arrive(&full_a[s]);
                 return true;
             };
             bool ok = true;
-            for (int ks = d.k0; ks < d.k1 && ok; ks += 2) {
-                ok = produce(u0, ks);
-                if (live && ks + 2 < kw1) u0.load(wrow, ks + 2, half);  // two K-steps ahead
-                if (ok && ks + 1 < d.k1) {
-                    ok = produce(u1, ks + 1);
-                    if (live && ks + 3 < kw1) u1.load(wrow, ks + 3, half);
+            for (int ks = d.k0; ks < d.k1 && ok; ks += DEPTH) {
+#pragma unroll
+                for (int dd = 0; dd < DEPTH; dd++) {
+                    if (ok && ks + dd < d.k1) {
+                        ok = produce(u[dd], ks + dd);
+                        load_step(u[dd], ks + dd + DEPTH);  // DEPTH K-steps ahead
+                    }
                 }
             }
             if (!ok) break;
@@ -398,79 +423,83 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                         for (int jj = 0; jj < 32; jj++) {
                             const int j = 32 * c + jj;
                             if (j < d.n_eff) {
+                                // route rt's output row; the weighted sum over a token's
+                                // routes is taken afterwards in a fixed order
                                 const int rt = p.route_list[d.route0 + j];
-                                const float wgt = p.route_w ? p.route_w[rt] : 1.0f;
-                                atomicAdd(&p.yacc[(int64_t)(rt / p.top_k) * p.n + orow], wgt * __uint_as_float(rr[jj]));
+                                p.yacc[(int64_t)rt * p.n + orow] = __uint_as_float(rr[jj]);
                             }
                         }
                     }
                 }
             } else {
-                // gate rows in TMEM lanes 0..63 (q = 0, 1), up rows in 64..127 (q = 2, 3)
+                // gate rows in TMEM lanes 0..63 (q = 0, 1), up rows in 64..127 (q = 2, 3).
+                // Per chunk of 32 routes: all four warps park their values in
+                // xbuf[gate/up][route][i], then warp q finishes routes q, q+4, ...:
+                // lane l takes h columns i = l and 32 + l, one q8_1 block each.
                 const int64_t idim = p.n / 2;
                 const int64_t hrb = idim / 32 * Q8_1_BYTES;
-                const int il = 32 * (q & 1) + lane;          // i within the 64-row slice
-                const int64_t icol = d.row0 + il;             // column of h
+                float *xg = xbuf, *xu = xbuf + 32 * 64;
 #pragma unroll 1
                 for (int c = 0; c * 32 < BN; c++) {
                     const bool any = go && 32 * c < d.n_eff;  // uniform across the 4 warps
-                    uint32_t rr[32];
                     if (any) {
+                        uint32_t rr[32];
                         tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + 32 * c), rr);
                         tc::tmem_ld_wait();
-                        if (q >= 2) {
+                        float *dst = (q < 2 ? xg : xu) + 32 * (q & 1) + lane;
 #pragma unroll
-                            for (int jj = 0; jj < 32; jj++) xbuf[jj * 64 + il] = __uint_as_float(rr[jj]);
-                        }
+                        for (int jj = 0; jj < 32; jj++) dst[jj * 64] = __uint_as_float(rr[jj]);
                     }
                     tg_named_bar(1, 128);
-                    if (any && q < 2) {
-#pragma unroll 1
-                        for (int jj = 0; jj < 32; jj++) {
+                    if (any) {
+#pragma unroll 2
+                        for (int jj = q; jj < 32; jj += 4) {
                             const int j = 32 * c + jj;
-                            if (j >= d.n_eff) break;
+                            if (j >= d.n_eff) break;  // uniform within the warp
                             const int64_t rt = p.route_list[d.route0 + j];
-                            const float gv = __uint_as_float(rr[jj]);
-                            const float uv = xbuf[jj * 64 + il];
-                            const float hf = gv / (1.0f + expf(-gv)) * uv;
-                            const uint16_t hb = f2bf_rn(hf);
-                            const float hx = bf2f(hb);  // the intermediate in the activation dtype
-                            if (p.hbf) p.hbf[rt * idim + icol] = hb;
-                            float amax = fabsf(hx);
 #pragma unroll
-                            for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-                            const float dq = __fdiv_rn(amax, 127.0f);
-                            const int qv = dq != 0.0f ? (int)roundf(__fdiv_rn(hx, dq)) : 0;
-                            int sum = qv;
-#pragma unroll
-                            for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-                            const uint16_t dh = f2h_rn(dq);
-                            if (p.hq) {
-                                uint8_t *blk = p.hq + rt * hrb + (icol / 32) * Q8_1_BYTES;
-                                blk[4 + lane] = (uint8_t)(int8_t)qv;
-                                if (lane == 0) {
-                                    const uint16_t sh = f2h_rn(__fmul_rn(dq, (float)sum));
-                                    *reinterpret_cast<uint32_t *>(blk) = (uint32_t)dh | ((uint32_t)sh << 16);
-                                }
-                            }
-                            if (p.h16) {
-                                const float v = h2f(dh) * (float)qv;
-                                const uint16_t vh = f2h_rn(v);
-                                p.h16[rt * p.hpitch + icol] = vh;
-                                if (p.h16lo) p.h16lo[rt * p.hpitch + icol] = f2h_rn(v - h2f(vh));
-                                if (p.hpitch > idim) {
-                                    // min-term correction column of this q8_1 block (Q4_K down weights),
-                                    // and the zero padding of the row (written once, by the first column tile)
+                            for (int hb = 0; hb < 2; hb++) {
+                                const int il = 32 * hb + lane;
+                                const int64_t icol = d.row0 + il;  // column of h
+                                const float gv = xg[jj * 64 + il], uv = xu[jj * 64 + il];
+                                const float hf = gv / (1.0f + expf(-gv)) * uv;
+                                const uint16_t hbits = f2bf_rn(hf);
+                                const float hx = bf2f(hbits);  // the intermediate in the activation dtype
+                                if (p.hbf) p.hbf[rt * idim + icol] = hbits;
+                                // q8_1 of the 32 columns of this warp: amax on the (non-negative) float bits
+                                const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hx))));
+                                const float dq = __fdiv_rn(amax, 127.0f);
+                                const int qv = dq != 0.0f ? (int)roundf(__fdiv_rn(hx, dq)) : 0;
+                                const int sum = __reduce_add_sync(0xffffffffu, qv);
+                                const uint16_t dh = f2h_rn(dq);
+                                if (p.hq) {
+                                    uint8_t *blk = p.hq + rt * hrb + (icol / 32) * Q8_1_BYTES;
+                                    blk[4 + lane] = (uint8_t)(int8_t)qv;
                                     if (lane == 0) {
                                         const uint16_t sh = f2h_rn(__fmul_rn(dq, (float)sum));
-                                        p.h16[rt * p.hpitch + idim + icol / 32] = f2h_rn(h2f(dh) * (float)sum - h2f(sh));
-                                        if (p.h16lo) p.h16lo[rt * p.hpitch + idim + icol / 32] = 0;
+                                        *reinterpret_cast<uint32_t *>(blk) = (uint32_t)dh | ((uint32_t)sh << 16);
                                     }
-                                    if (d.row0 == 0 && q == 0)
-                                        for (int64_t c2 = idim + idim / 32 + lane; c2 < p.hpitch; c2 += 32) {
-                                            p.h16[rt * p.hpitch + c2] = 0;
-                                            if (p.h16lo) p.h16lo[rt * p.hpitch + c2] = 0;
+                                }
+                                if (p.h16) {
+                                    const float v = h2f(dh) * (float)qv;
+                                    const uint16_t vh = f2h_rn(v);
+                                    p.h16[rt * p.hpitch + icol] = vh;
+                                    if (p.h16lo) p.h16lo[rt * p.hpitch + icol] = f2h_rn(v - h2f(vh));
+                                    if (p.hpitch > idim) {
+                                        // min-term correction column of this q8_1 block (Q4_K down
+                                        // weights), and the zero padding of the row (written once,
+                                        // by the first column tile)
+                                        if (lane == 0) {
+                                            const uint16_t sh = f2h_rn(__fmul_rn(dq, (float)sum));
+                                            p.h16[rt * p.hpitch + idim + icol / 32] = f2h_rn(h2f(dh) * (float)sum - h2f(sh));
+                                            if (p.h16lo) p.h16lo[rt * p.hpitch + idim + icol / 32] = 0;
                                         }
+                                        if (d.row0 == 0 && hb == 0)
+                                            for (int64_t c2 = idim + idim / 32 + lane; c2 < p.hpitch; c2 += 32) {
+                                                p.h16[rt * p.hpitch + c2] = 0;
+                                                if (p.h16lo) p.h16lo[rt * p.hpitch + c2] = 0;
+                                            }
+                                    }
                                 }
                             }
                         }
@@ -511,7 +540,7 @@ int *tg_error_word();
 template <int WT, int BN, bool PRECISE, int MODE, int OT>
 inline cudaError_t tg_launch(const CUtensorMap &mh, const CUtensorMap &ml, const TgParams &p, int grid,
                              cudaStream_t s) {
-    using S = TgShape<BN, PRECISE>;
+    using S = TgShape<BN, PRECISE, MODE>;
     auto kern = tg_kernel<WT, BN, PRECISE, MODE, OT>;
     static bool attr_set[64] = {};
     int dev = 0;
