@@ -274,7 +274,10 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
         using U = KQ<WT>;
         constexpr int PARTS = U::PARTS, RP = TG_PRODUCERS / PARTS, TPT = TG_BM / RP;
         constexpr int VW = 8 * U::CHUNKS;  // fp32 values per task
-        constexpr int DEPTH = 2;           // K-steps loaded ahead (deeper unrolling costs i-cache)
+        // K-steps loaded ahead: 4 for the MoE GEMMs (latency-bound gathers of
+        // expert rows); 2 for the dense MMQ, where deeper unrolling cost more
+        // in instruction-cache misses than it hid
+        constexpr int DEPTH = MODE == TG_DENSE ? 2 : 4;
         // lane -> (row, part): each group of 8 lanes takes one part of 8
         // different rows, so a 16-byte swizzled store is conflict-free within
         // every 8-lane phase, and the parts of a row are in the same warp so a
@@ -416,18 +419,17 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
 #pragma unroll 1
                 for (int c = 0; c * 32 < d.n_eff && go; c++) {
                     uint32_t rr[32];
+                    // the chunk's 32 route ids, one per lane, loaded together
+                    const int rt_l = 32 * c + lane < d.n_eff ? p.route_list[d.route0 + 32 * c + lane] : 0;
                     tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + 32 * c), rr);
                     tc::tmem_ld_wait();
-                    if (orow < p.n) {
-#pragma unroll 4
-                        for (int jj = 0; jj < 32; jj++) {
-                            const int j = 32 * c + jj;
-                            if (j < d.n_eff) {
-                                // route rt's output row; the weighted sum over a token's
-                                // routes is taken afterwards in a fixed order
-                                const int rt = p.route_list[d.route0 + j];
-                                p.yacc[(int64_t)rt * p.n + orow] = __uint_as_float(rr[jj]);
-                            }
+#pragma unroll
+                    for (int jj = 0; jj < 32; jj++) {
+                        if (32 * c + jj < d.n_eff) {  // uniform within the warp
+                            // route rt's output row; the weighted sum over a token's
+                            // routes is taken afterwards in a fixed order
+                            const int rt = __shfl_sync(0xffffffffu, rt_l, jj);
+                            if (orow < p.n) p.yacc[(int64_t)rt * p.n + orow] = __uint_as_float(rr[jj]);
                         }
                     }
                 }
@@ -452,11 +454,13 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                     }
                     tg_named_bar(1, 128);
                     if (any) {
+                        // the chunk's 32 route ids, one per lane, loaded together
+                        const int rt_l = 32 * c + lane < d.n_eff ? p.route_list[d.route0 + 32 * c + lane] : 0;
 #pragma unroll 2
                         for (int jj = q; jj < 32; jj += 4) {
                             const int j = 32 * c + jj;
                             if (j >= d.n_eff) break;  // uniform within the warp
-                            const int64_t rt = p.route_list[d.route0 + j];
+                            const int64_t rt = __shfl_sync(0xffffffffu, rt_l, jj);
 #pragma unroll
                             for (int hb = 0; hb < 2; hb++) {
                                 const int il = 32 * hb + lane;
