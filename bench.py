@@ -164,7 +164,7 @@ class Decode:
         if quantize:
             g.gguf_quantize_q8_1(self.x_all if x_all is None else x_all, out=self.xq_all)
         for m in DECODE_MS:
-            for (n, k) in DECODE_SHAPES:
+            for (n, k) in DECODE_SHAPES:   # both weight matrices read this M's q8_1 slice
                 g.gguf_mul_mat(self.weight(n, k), g.Q4_K, n, k, self.xqs[m], xt=g.Q8_1, m=m, out=self.ys[(n, m)])
 
     def launches_per_step(self, quantize=True):
@@ -282,7 +282,7 @@ def run_ours(args, rank, world, torch, dev):
         "weight_bytes_per_step": weight_bytes, "bytes_per_step": per_step,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": MMVQ_TRAFFIC,
-                     "kernel": "mmvq_kernel<Q4KPiece> (8 launches per step, mean)",
+                     "kernel": "MMVQ (dp4a mmvq_kernel for M<=4, int8 tensor-core for M=8); 8 launches per step, mean",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "detail": detail,
         "gpu_launches": args.steps * dec.launches_per_step(),
@@ -295,10 +295,10 @@ def run_ours(args, rank, world, torch, dev):
 
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# decode MMVQ launches, averaged over the step's 8 launches, from the ncu
-# capture summarized in profiles/mmvq_q4_k_decode.md (set to None whenever the
-# kernel changes, until it is captured again).
-MMVQ_TRAFFIC = 21271840
+# decode MMVQ launches, averaged over the step's launches, from the ncu capture
+# summarized in profiles/mmvq_q4_k_decode.md; None whenever the kernel has
+# changed since the capture.
+MMVQ_TRAFFIC = None
 
 
 def run_e2e(args, g, torch, dev, dec, per_step):
@@ -355,8 +355,22 @@ def _time_eager(torch, stream, fn, reps, flush=None, warm=2):
     return sum(a.elapsed_time(b) for a, b in evs) / reps
 
 
+def int8_mma_peak_tops(torch):
+    """The int8 warp-MMA (mma.sync m16n8k32 s8) peak: 512 ops per clock per SM
+    (ncu's sm__ops_path_tensor_op_imma_src_int8 peak_sustained on GB300) x SMs x
+    the maximum SM clock from the measured-peaks file."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f)["sm_max_mhz"])
+    except Exception:
+        mhz = 2070.0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return 512.0 * sms * mhz * 1e6 / 1e12
+
+
 def secondary(torch, g, synth, dev, stream, hbm_peak, tf_peak, peak_kind):
     out = {}
+    p_int8 = int8_mma_peak_tops(torch)
     l2 = _l2_bytes(torch)
     scrub = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
 
@@ -390,7 +404,8 @@ def secondary(torch, g, synth, dev, stream, hbm_peak, tf_peak, peak_kind):
             out[name] = {"ms": round(ms, 4), "tops": round(tops, 1),
                          "roofline": {"bound": "tensor", "achieved": round(tops, 1), "peak": tf_peak,
                                       "unit": "TFLOP/s", "frac": round(tops / tf_peak, 4),
-                                      "note": f"fp16 tcgen05 MMA; peak = {peak_kind} bf16 (same rate as fp16)"}}
+                                      "note": f"fp16 tcgen05 MMA; peak = {peak_kind} bf16 (same rate as fp16)"},
+                         "frac_of_int8_mma_peak": round(tops / p_int8, 3), "int8_mma_peak_tops": round(p_int8, 1)}
             del w, x, y, ws
 
         # MoE FFN: E=256, top-8, H=2048, I=512, 8192 bf16 tokens; gate_up Q4_K, down Q6_K
@@ -412,6 +427,8 @@ def secondary(torch, g, synth, dev, stream, hbm_peak, tf_peak, peak_kind):
         ops = 2.0 * T * K_ * (2 * I * H + H * I)
         out["moe_ffn_e256_top8_h2048_i512_t8192"] = {
             "ms": round(ms, 4), "tops": round(ops / (ms * 1e-3) / 1e12, 1),
+            "frac_of_bf16_peak": round(ops / (ms * 1e-3) / 1e12 / tf_peak, 4),
+            "frac_of_int8_mma_peak": round(ops / (ms * 1e-3) / 1e12 / p_int8, 3),
             "note": "routed-row int8-equivalent ops 2*T*top_k*(2I*H + H*I) / time; gate_up Q4_K + SwiGLU + q8_1, "
                     "down Q6_K + weighted sum"}
         del wgu, wdn, x, y, ws

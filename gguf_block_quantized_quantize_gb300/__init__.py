@@ -34,6 +34,13 @@ class GgufError(RuntimeError):
         self.status = status
 
 
+MAX_SEGMENTS = 8
+
+
+class Segment(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("n", ctypes.c_int64), ("y", ctypes.c_void_p), ("ldy", ctypes.c_int64)]
+
+
 class MoeArgs(ctypes.Structure):
     _fields_ = [("w", ctypes.c_void_p), ("wt", ctypes.c_int), ("n_experts", ctypes.c_int64),
                 ("expert_stride", ctypes.c_int64), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
@@ -65,6 +72,8 @@ SIGNATURES = {
     "gguf_mul_mat_ws_size": (_sz, [_i, _i64, _i64, _i, _i64, _i]),
     "gguf_mul_mat": (_i, [_p, _i, _i64, _i64, _p, _i, _i64, _i64, _p, _i, _i64, _p, _sz, _p]),
     "gguf_mul_mat_noalloc": (_i, [_p, _i, _i64, _i64, _p, _i, _i64, _i64, _p, _i, _i64, _p]),
+    "gguf_mul_mat_segments_ws_size": (_sz, [_i, ctypes.POINTER(Segment), _i, _i64, _i, _i64, _i]),
+    "gguf_mul_mat_segments": (_i, [_i, ctypes.POINTER(Segment), _i, _i64, _p, _i, _i64, _i64, _i, _p, _sz, _p]),
     "gguf_mul_mat_id_ws_size": (_sz, [ctypes.POINTER(MoeArgs)]),
     "gguf_mul_mat_id": (_i, [ctypes.POINTER(MoeArgs), _p, _sz, _p]),
     "gguf_moe_ffn_ws_size": (_sz, [ctypes.POINTER(MoeFfnArgs)]),
@@ -185,6 +194,30 @@ def gguf_mul_mat(w: torch.Tensor, wt: int, n: int, k: int, x: torch.Tensor, xt: 
     _check(load_library().gguf_mul_mat(_ptr(w), wt, n, k, _ptr(x), xt, m, ldx, _ptr(out), _TYPE_OF[out.dtype],
                                        out.stride(0), _ptr(ws), 0 if ws is None else ws.numel(), _stream()))
     return out
+
+
+def gguf_mul_mat_segments(wt: int, k: int, x: torch.Tensor, segments, xt: int | None = None, m: int | None = None,
+                          ws: torch.Tensor | None = None):
+    """y_s = x @ W_s^T for each (w, n, out) in ``segments``, with x quantized once
+    (one MMVQ launch for all segments when m is small).  ``out`` tensors must
+    have contiguous rows and share one dtype; they are returned."""
+    if xt is None:
+        xt = _TYPE_OF[x.dtype]
+    if m is None:
+        m = x.shape[0]
+    ldx = x.stride(0) if xt != Q8_1 else gguf_row_size(Q8_1, k)
+    outs = [o for (_, _, o) in segments]
+    yt = _TYPE_OF[outs[0].dtype]
+    for o in outs:
+        if o.stride(1) != 1 or _TYPE_OF[o.dtype] != yt:
+            raise ValueError("gguf_mul_mat_segments: outputs need contiguous rows and one dtype")
+    arr = (Segment * len(segments))(*[Segment(_ptr(w), n, _ptr(o), o.stride(0)) for (w, n, o) in segments])
+    need = int(load_library().gguf_mul_mat_segments_ws_size(wt, arr, len(segments), k, xt, m, yt))
+    if ws is None:
+        ws = _workspace(need, x.device)
+    _check(load_library().gguf_mul_mat_segments(wt, arr, len(segments), k, _ptr(x), xt, m, ldx, yt, _ptr(ws),
+                                                0 if ws is None else ws.numel(), _stream()))
+    return outs
 
 
 def gguf_mul_mat_noalloc(w: torch.Tensor, wt: int, n: int, k: int, x: torch.Tensor,

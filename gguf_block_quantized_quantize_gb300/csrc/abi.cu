@@ -158,25 +158,43 @@ size_t gguf_mul_mat_ws_size(int wt, int64_t n, int64_t k, int xt, int64_t m, int
     return align256((size_t)(m * row_size(GGUF_Q8_1, k)));             // q8_1 rows
 }
 
-gguf_status gguf_mul_mat(const void *w, int wt, int64_t n, int64_t k, const void *x, int xt, int64_t m, int64_t ldx,
-                         void *y, int yt, int64_t ldy, void *ws, size_t ws_bytes, gguf_stream_t stream) {
-    if (!is_weight(wt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat: weight type %d not supported", wt);
-    if (!is_float(xt) && xt != GGUF_Q8_1) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat: x type %d not supported", xt);
-    if (!is_float(yt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat: y type %d is not F32/BF16/F16", yt);
-    if (n < 0 || k < 0 || m < 0) return fail(GGUF_ERR_INVALID_ARG, "mul_mat: negative size");
-    if (row_size(wt, k) < 0) return fail(GGUF_ERR_SHAPE, "mul_mat: k=%lld not a multiple of the block of type %d", (long long)k, wt);
-    if (ldy < n) return fail(GGUF_ERR_INVALID_ARG, "mul_mat: ldy=%lld < n=%lld", (long long)ldy, (long long)n);
-    if (is_float(xt) && ldx < k) return fail(GGUF_ERR_INVALID_ARG, "mul_mat: ldx=%lld < k=%lld", (long long)ldx, (long long)k);
-    if (m == 0 || n == 0) return GGUF_OK;
-    if (k == 0) return fail(GGUF_ERR_SHAPE, "mul_mat: k must be positive");
-    if (!w || !x || !y) return fail(GGUF_ERR_INVALID_ARG, "mul_mat: null pointer");
-    if (!aligned(w, 16)) return fail(GGUF_ERR_ALIGNMENT, "mul_mat: weight base must be 16-byte aligned");
-    if (!aligned(y, esize(yt)) || (is_float(xt) && !aligned(x, esize(xt))) || (xt == GGUF_Q8_1 && !aligned(x, 4)))
-        return fail(GGUF_ERR_ALIGNMENT, "mul_mat: misaligned x or y");
-    const size_t need = gguf_mul_mat_ws_size(wt, n, k, xt, m, yt);
+// The body shared by gguf_mul_mat and gguf_mul_mat_segments: x is quantized
+// once for every segment; in the MMVQ range one launch covers all segments.
+static gguf_status mul_mat_impl(int wt, const gguf_segment *segs, int nseg, int64_t k, const void *x, int xt,
+                                int64_t m, int64_t ldx, int yt, void *ws, size_t ws_bytes, gguf_stream_t stream,
+                                const char *what) {
+    if (!is_weight(wt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "%s: weight type %d not supported", what, wt);
+    if (!is_float(xt) && xt != GGUF_Q8_1) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "%s: x type %d not supported", what, xt);
+    if (!is_float(yt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "%s: y type %d is not F32/BF16/F16", what, yt);
+    if (nseg < 1 || nseg > GGUF_MAX_SEGMENTS || !segs)
+        return fail(GGUF_ERR_INVALID_ARG, "%s: %d segments (1..%d)", what, nseg, GGUF_MAX_SEGMENTS);
+    if (k < 0 || m < 0) return fail(GGUF_ERR_INVALID_ARG, "%s: negative size", what);
+    if (row_size(wt, k) < 0) return fail(GGUF_ERR_SHAPE, "%s: k=%lld not a multiple of the block of type %d", what, (long long)k, wt);
+    if (is_float(xt) && ldx < k) return fail(GGUF_ERR_INVALID_ARG, "%s: ldx=%lld < k=%lld", what, (long long)ldx, (long long)k);
+    int64_t n_max = 0, n_tot = 0;
+    for (int i = 0; i < nseg; i++) {
+        const gguf_segment &g = segs[i];
+        if (g.n < 0) return fail(GGUF_ERR_INVALID_ARG, "%s: negative size", what);
+        if (g.ldy < g.n) return fail(GGUF_ERR_INVALID_ARG, "%s: ldy=%lld < n=%lld", what, (long long)g.ldy, (long long)g.n);
+        n_max = g.n > n_max ? g.n : n_max;
+        n_tot += g.n;
+    }
+    if (m == 0 || n_tot == 0) return GGUF_OK;   // nothing to compute: pointers are not looked at
+    for (int i = 0; i < nseg; i++) {
+        const gguf_segment &g = segs[i];
+        if (g.n == 0) continue;
+        if (!g.w || !g.y) return fail(GGUF_ERR_INVALID_ARG, "%s: null pointer", what);
+        if (!aligned(g.w, 16)) return fail(GGUF_ERR_ALIGNMENT, "%s: weight base must be 16-byte aligned", what);
+        if (!aligned(g.y, esize(yt))) return fail(GGUF_ERR_ALIGNMENT, "%s: misaligned y", what);
+    }
+    if (k == 0) return fail(GGUF_ERR_SHAPE, "%s: k must be positive", what);
+    if (!x) return fail(GGUF_ERR_INVALID_ARG, "%s: null pointer", what);
+    if ((is_float(xt) && !aligned(x, esize(xt))) || (xt == GGUF_Q8_1 && !aligned(x, 4)))
+        return fail(GGUF_ERR_ALIGNMENT, "%s: misaligned x", what);
+    const size_t need = gguf_mul_mat_ws_size(wt, n_max, k, xt, m, yt);
     if (ws_bytes < need || (need > 0 && !ws))
-        return fail(GGUF_ERR_WORKSPACE, "mul_mat: workspace of %zu bytes < required %zu", ws_bytes, need);
-    if (need > 0 && !aligned(ws, 16)) return fail(GGUF_ERR_ALIGNMENT, "mul_mat: workspace must be 16-byte aligned");
+        return fail(GGUF_ERR_WORKSPACE, "%s: workspace of %zu bytes < required %zu", what, ws_bytes, need);
+    if (need > 0 && !aligned(ws, 16)) return fail(GGUF_ERR_ALIGNMENT, "%s: workspace must be 16-byte aligned", what);
     cudaStream_t s = (cudaStream_t)stream;
 
     if (use_mmq(m, k)) {
@@ -192,24 +210,58 @@ gguf_status gguf_mul_mat(const void *w, int wt, int64_t n, int64_t k, const void
         float *yacc = m <= 256 ? (float *)wp : nullptr;
         cudaError_t e = xt == GGUF_Q8_1 ? launch_q8_1_to_f16((const uint8_t *)x, m, k, xh, xl, s, kx)
                                         : launch_quantize_q8_1(x, xt, m, k, ldx, nullptr, xh, xl, s, kx);
-        if (e != cudaSuccess) return cuda_status(e, "mul_mat quantize");
-        return cuda_status(launch_mmq((const uint8_t *)w, wt, n, k, xh, xl, m, y, yt, ldy, yacc, s), "mul_mat mmq");
+        if (e != cudaSuccess) return cuda_status(e, what);
+        for (int i = 0; i < nseg; i++) {
+            if (segs[i].n == 0) continue;
+            e = launch_mmq((const uint8_t *)segs[i].w, wt, segs[i].n, k, xh, xl, m, segs[i].y, yt, segs[i].ldy, yacc, s);
+            if (e != cudaSuccess) return cuda_status(e, what);
+        }
+        return GGUF_OK;
     }
     const uint8_t *xq = (const uint8_t *)x;
     if (xt != GGUF_Q8_1) {
         cudaError_t e = launch_quantize_q8_1(x, xt, m, k, ldx, (uint8_t *)ws, nullptr, nullptr, s);
-        if (e != cudaSuccess) return cuda_status(e, "mul_mat quantize");
+        if (e != cudaSuccess) return cuda_status(e, what);
         xq = (const uint8_t *)ws;
     }
     const int64_t xrb = row_size(GGUF_Q8_1, k);
     const int64_t ysz = esize(yt);
     for (int64_t m0 = 0; m0 < m; m0 += 8) {  // MMVQ handles up to 8 rows per launch
         const int64_t mc = m - m0 < 8 ? m - m0 : 8;
-        cudaError_t e = launch_mmvq((const uint8_t *)w, wt, n, k, xq + m0 * xrb, mc,
-                                    (uint8_t *)y + m0 * ldy * ysz, yt, ldy, s);
-        if (e != cudaSuccess) return cuda_status(e, "mul_mat mmvq");
+        MmvqSegs sg{};
+        for (int i = 0; i < MMVQ_MAX_SEGS; i++) sg.end[i] = INT64_MAX;
+        int64_t acc = 0;
+        for (int i = 0; i < nseg; i++) {
+            if (segs[i].n == 0) continue;
+            acc += segs[i].n;
+            sg.end[sg.nseg] = acc;
+            sg.w[sg.nseg] = (const uint8_t *)segs[i].w;
+            sg.y[sg.nseg] = (uint8_t *)segs[i].y + m0 * segs[i].ldy * ysz;
+            sg.ldy[sg.nseg] = segs[i].ldy;
+            sg.nseg++;
+        }
+        cudaError_t e = launch_mmvq(sg, wt, k, xq + m0 * xrb, mc, yt, s);
+        if (e != cudaSuccess) return cuda_status(e, what);
     }
     return GGUF_OK;
+}
+
+gguf_status gguf_mul_mat(const void *w, int wt, int64_t n, int64_t k, const void *x, int xt, int64_t m, int64_t ldx,
+                         void *y, int yt, int64_t ldy, void *ws, size_t ws_bytes, gguf_stream_t stream) {
+    const gguf_segment seg = {w, n, y, ldy};
+    return mul_mat_impl(wt, &seg, 1, k, x, xt, m, ldx, yt, ws, ws_bytes, stream, "mul_mat");
+}
+
+size_t gguf_mul_mat_segments_ws_size(int wt, const gguf_segment *segs, int nseg, int64_t k, int xt, int64_t m, int yt) {
+    if (!segs || nseg < 1 || nseg > GGUF_MAX_SEGMENTS) return 0;
+    int64_t n_max = 0;
+    for (int i = 0; i < nseg; i++) n_max = segs[i].n > n_max ? segs[i].n : n_max;
+    return gguf_mul_mat_ws_size(wt, n_max, k, xt, m, yt);
+}
+
+gguf_status gguf_mul_mat_segments(int wt, const gguf_segment *segs, int nseg, int64_t k, const void *x, int xt,
+                                  int64_t m, int64_t ldx, int yt, void *ws, size_t ws_bytes, gguf_stream_t stream) {
+    return mul_mat_impl(wt, segs, nseg, k, x, xt, m, ldx, yt, ws, ws_bytes, stream, "mul_mat_segments");
 }
 
 // ---------------------------------------------------------------- MoE

@@ -41,9 +41,23 @@ cudaError_t launch_block_dots(const uint8_t *w, int wt, int64_t n, int64_t k, co
 // option "mmvq_tc": 5..8 tokens of Q4_K rows run on the tensor-core MMVQ (1, default) or dp4a (0)
 int64_t option_mmvq_tc();
 
-// y[m][ldy] (yt) = W[n][k] (wt) . q8_1 rows xq[m] ; m <= 8
-cudaError_t launch_mmvq(const uint8_t *w, int wt, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y,
-                        int yt, int64_t ldy, cudaStream_t s);
+// Weight segments that read the same activations; one MMVQ launch covers all
+// of them.  Row r of the launch is row r - end[s-1] of segment s (end[-1] = 0);
+// end[] is cumulative and padded with INT64_MAX past nseg.
+constexpr int MMVQ_MAX_SEGS = 8;
+struct MmvqSegs {
+    int nseg;
+    int64_t end[MMVQ_MAX_SEGS];
+    const uint8_t *w[MMVQ_MAX_SEGS];
+    void *y[MMVQ_MAX_SEGS];
+    int64_t ldy[MMVQ_MAX_SEGS];
+    __host__ __device__ int64_t rows() const { return end[nseg - 1]; }
+};
+// one segment: W[n][k] -> y[.][ldy]
+MmvqSegs mmvq_one_segment(const void *w, int64_t n, void *y, int64_t ldy);
+
+// for every segment s: y_s[m][ldy_s] (yt) = W_s (wt) . q8_1 rows xq[m] ; m <= 8
+cudaError_t launch_mmvq(const MmvqSegs &sg, int wt, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
 
 // tensor-core MMQ: y[m][ldy] = W[n][k] . xh[m][k] (fp16 operand rows; fp32
 // outputs also need the low parts xl).  yacc (optional, fp32 [m][n]) lets small

@@ -7,14 +7,25 @@ namespace gg {
 // rows take the tensor-core path, which has no K limit).
 constexpr int64_t MMVQ_MAX_PIECES = 512;
 
-cudaError_t launch_mmvq(const uint8_t *w, int wt, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y,
-                        int yt, int64_t ldy, cudaStream_t s) {
-    if (n == 0 || m == 0) return cudaSuccess;
+MmvqSegs mmvq_one_segment(const void *w, int64_t n, void *y, int64_t ldy) {
+    MmvqSegs sg{};
+    sg.nseg = 1;
+    for (int i = 0; i < MMVQ_MAX_SEGS; i++) sg.end[i] = INT64_MAX;
+    sg.end[0] = n;
+    sg.w[0] = (const uint8_t *)w;
+    sg.y[0] = y;
+    sg.ldy[0] = ldy;
+    return sg;
+}
+
+cudaError_t launch_mmvq(const MmvqSegs &sg, int wt, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s) {
+    if (sg.nseg < 1 || sg.nseg > MMVQ_MAX_SEGS) return cudaErrorInvalidValue;
+    if (sg.rows() == 0 || m == 0) return cudaSuccess;
     if (k / 32 > MMVQ_MAX_PIECES || m > 8) return cudaErrorInvalidValue;
     switch (wt) {
-    case GGUF_Q8_0: return launch_mmvq_q8_0(w, n, k, xq, m, y, yt, ldy, s);
-    case GGUF_Q4_K: return launch_mmvq_q4_k(w, n, k, xq, m, y, yt, ldy, s);
-    case GGUF_Q6_K: return launch_mmvq_q6_k(w, n, k, xq, m, y, yt, ldy, s);
+    case GGUF_Q8_0: return launch_mmvq_q8_0(sg, k, xq, m, yt, s);
+    case GGUF_Q4_K: return launch_mmvq_q4_k(sg, k, xq, m, yt, s);
+    case GGUF_Q6_K: return launch_mmvq_q6_k(sg, k, xq, m, yt, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -309,6 +309,24 @@ __device__ __forceinline__ bool butterfly_writer(int lane) {
     return (lane & mask) == 0;
 }
 
+// ---------------------------------------------------------------- weight segments
+
+// segment of launch row r (end[] is padded with INT64_MAX, so no bound check)
+__device__ __forceinline__ int seg_index(const MmvqSegs &sg, int64_t r) {
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < MMVQ_MAX_SEGS - 1; i++) s += r >= sg.end[i] ? 1 : 0;
+    return s;
+}
+__device__ __forceinline__ const uint8_t *seg_row(const MmvqSegs &sg, int64_t r, int64_t rb) {
+    const int s = seg_index(sg, r);
+    return sg.w[s] + (r - (s ? sg.end[s - 1] : 0)) * rb;
+}
+__device__ __forceinline__ void seg_store(const MmvqSegs &sg, int yt, int tok, int64_t r, float v) {
+    const int s = seg_index(sg, r);
+    store_out(sg.y[s], yt, (int64_t)tok * sg.ldy[s] + (r - (s ? sg.end[s - 1] : 0)), v);
+}
+
 // ---------------------------------------------------------------- piece traits
 // Each traits type describes one thread's piece of a weight row: where its
 // bytes are (Pos, computed once), the raw bytes of one row (W, loaded before
@@ -540,10 +558,15 @@ struct Q6KPiece {
 // Thread t of a CTA owns piece t / TG of every row and the tokens
 // [(t % TG) * M, +M).  The CTA walks rows [n0, n0 + R) for n0 = blockIdx.x * R,
 // + gridDim.x * R, ...
-template <class PT, int M, int TG, int R, int MAXT>
-__global__ void __launch_bounds__(MAXT) mmvq_kernel(const uint8_t *__restrict__ w, int64_t n, int64_t k, int64_t rb,
-                                                   const uint8_t *__restrict__ xq, int m_act, void *__restrict__ y,
-                                                   int yt, int64_t ldy) {
+// MULTI: more than one weight segment (row addresses looked up per row group);
+// a single segment keeps its pointers in registers.
+template <class PT, int M, int TG, int R, int MAXT, bool MULTI>
+__global__ void __launch_bounds__(MAXT) mmvq_kernel(const MmvqSegs sg, int64_t k, int64_t rb,
+                                                   const uint8_t *__restrict__ xq, int m_act, int yt) {
+    const int64_t n = sg.rows();
+    const uint8_t *const w0 = sg.w[0];
+    void *const y0 = sg.y[0];
+    const int64_t ldy0 = sg.ldy[0];
     constexpr int V = R * M;
     static_assert(V * TG <= 32 && (V & (V - 1)) == 0, "R*M must be a power of two <= 32/TG");
     __shared__ float red[2][MAXT / 32][TG * V];
@@ -559,8 +582,26 @@ __global__ void __launch_bounds__(MAXT) mmvq_kernel(const uint8_t *__restrict__ 
     typename PT::W wa[R], wb[R];
     auto load_rows = [&](typename PT::W (&dst)[R], int64_t base) {
         if (!valid) return;
+        if constexpr (!MULTI) {
 #pragma unroll
-        for (int r = 0; r < R; r++) PT::load(dst[r], w + (base + r < n ? base + r : n - 1) * rb, pos);
+            for (int r = 0; r < R; r++) PT::load(dst[r], w0 + (base + r < n ? base + r : n - 1) * rb, pos);
+        } else {
+            // one lookup per group; a group that crosses a segment end (or the
+            // last row) takes the per-row lookup
+            const int sgi = seg_index(sg, base);
+            if (base + R <= sg.end[sgi]) {
+                const uint8_t *row0 = sg.w[sgi] + (base - (sgi ? sg.end[sgi - 1] : 0)) * rb;
+#pragma unroll
+                for (int r = 0; r < R; r++) PT::load(dst[r], row0 + r * rb, pos);
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; r++) PT::load(dst[r], seg_row(sg, base + r < n ? base + r : n - 1, rb), pos);
+            }
+        }
+    };
+    auto store_row = [&](int tok, int64_t r, float v) {
+        if constexpr (!MULTI) store_out(y0, yt, (int64_t)tok * ldy0 + r, v);
+        else seg_store(sg, yt, tok, r, v);
     };
     // weights never change: the first rows are requested before waiting for
     // the kernel that wrote the activations
@@ -595,7 +636,7 @@ __global__ void __launch_bounds__(MAXT) mmvq_kernel(const uint8_t *__restrict__ 
         if (nw == 1) {
             if (writer) {
                 const int r = idx / M, tok = tg * M + idx % M;
-                if (r0 + r < n && tok < m_act) store_out(y, yt, (int64_t)tok * ldy + r0 + r, tot);
+                if (r0 + r < n && tok < m_act) store_row(tok, r0 + r, tot);
             }
         } else {
             if (writer) red[buf][warp][tg * V + idx] = tot;
@@ -604,7 +645,7 @@ __global__ void __launch_bounds__(MAXT) mmvq_kernel(const uint8_t *__restrict__ 
                 float sum = 0.0f;
                 for (int j = 0; j < nw; j++) sum += red[buf][j][tid];
                 const int g = tid / V, i = tid % V, r = i / M, tok = g * M + i % M;
-                if (r0 + r < n && tok < m_act) store_out(y, yt, (int64_t)tok * ldy + r0 + r, sum);
+                if (r0 + r < n && tok < m_act) store_row(tok, r0 + r, sum);
             }
             buf ^= 1;
         }
@@ -622,12 +663,13 @@ __global__ void __launch_bounds__(MAXT) mmvq_kernel(const uint8_t *__restrict__ 
 }
 
 template <class PT, int M, int TG, int R, int MAXT>
-inline cudaError_t launch_mmvq_cfg(const uint8_t *w, int64_t n, int64_t k, int64_t rb, const uint8_t *xq, int64_t m,
-                                   void *y, int yt, int64_t ldy, cudaStream_t s) {
+inline cudaError_t launch_mmvq_cfg(const MmvqSegs &sg, int64_t k, int64_t rb, const uint8_t *xq, int64_t m, int yt,
+                                   cudaStream_t s) {
+    const int64_t n = sg.rows();
     const int64_t P = k / PT::VALUES;
     const int nthr = (int)((P * TG + 31) / 32 * 32);
     if (nthr > MAXT) return cudaErrorInvalidValue;
-    auto kern = mmvq_kernel<PT, M, TG, R, MAXT>;
+    auto kern = sg.nseg > 1 ? mmvq_kernel<PT, M, TG, R, MAXT, true> : mmvq_kernel<PT, M, TG, R, MAXT, false>;
     int per_sm = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nthr, 0);
     if (e != cudaSuccess) return e;
@@ -645,7 +687,7 @@ inline cudaError_t launch_mmvq_cfg(const uint8_t *w, int64_t n, int64_t k, int64
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, w, n, k, rb, xq, (int)m, y, yt, ldy);
+    return cudaLaunchKernelEx(&cfg, kern, sg, k, rb, xq, (int)m, yt);
 }
 
 // Configuration by token count (measured on GB300, Q4_K / Q6_K rows of 3072 ..
@@ -660,34 +702,31 @@ struct MmvqTune {
 };
 
 template <class PT>
-inline cudaError_t launch_mmvq_pt(const uint8_t *w, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y,
-                                  int yt, int64_t ldy, cudaStream_t s, int64_t rb, MmvqTune t) {
+inline cudaError_t launch_mmvq_pt(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s,
+                                  int64_t rb, MmvqTune t) {
     const int64_t P = k / PT::VALUES;
     if (P <= 256) {
         if (m <= 1) {
-            if (t.r1_m1) return launch_mmvq_cfg<PT, 1, 1, 1, 256>(w, n, k, rb, xq, m, y, yt, ldy, s);
-            if (t.r4_m1) return launch_mmvq_cfg<PT, 1, 1, 4, 256>(w, n, k, rb, xq, m, y, yt, ldy, s);
-            return launch_mmvq_cfg<PT, 1, 1, 2, 256>(w, n, k, rb, xq, m, y, yt, ldy, s);
+            if (t.r1_m1) return launch_mmvq_cfg<PT, 1, 1, 1, 256>(sg, k, rb, xq, m, yt, s);
+            if (t.r4_m1) return launch_mmvq_cfg<PT, 1, 1, 4, 256>(sg, k, rb, xq, m, yt, s);
+            return launch_mmvq_cfg<PT, 1, 1, 2, 256>(sg, k, rb, xq, m, yt, s);
         }
-        if (m <= 2) return launch_mmvq_cfg<PT, 2, 1, 2, 256>(w, n, k, rb, xq, m, y, yt, ldy, s);
-        if (m <= 4) return launch_mmvq_cfg<PT, 4, 1, 2, 256>(w, n, k, rb, xq, m, y, yt, ldy, s);
-        if (t.tg2_m8 && P <= 128) return launch_mmvq_cfg<PT, 4, 2, 2, 256>(w, n, k, rb, xq, m, y, yt, ldy, s);
-        return launch_mmvq_cfg<PT, 8, 1, 1, 256>(w, n, k, rb, xq, m, y, yt, ldy, s);
+        if (m <= 2) return launch_mmvq_cfg<PT, 2, 1, 2, 256>(sg, k, rb, xq, m, yt, s);
+        if (m <= 4) return launch_mmvq_cfg<PT, 4, 1, 2, 256>(sg, k, rb, xq, m, yt, s);
+        if (t.tg2_m8 && P <= 128) return launch_mmvq_cfg<PT, 4, 2, 2, 256>(sg, k, rb, xq, m, yt, s);
+        return launch_mmvq_cfg<PT, 8, 1, 1, 256>(sg, k, rb, xq, m, yt, s);
     }
     if constexpr (PT::VALUES == 32) {
-        if (m <= 1) return launch_mmvq_cfg<PT, 1, 1, 2, 512>(w, n, k, rb, xq, m, y, yt, ldy, s);
-        if (m <= 2) return launch_mmvq_cfg<PT, 2, 1, 2, 512>(w, n, k, rb, xq, m, y, yt, ldy, s);
-        if (m <= 4) return launch_mmvq_cfg<PT, 4, 1, 1, 512>(w, n, k, rb, xq, m, y, yt, ldy, s);
-        return launch_mmvq_cfg<PT, 8, 1, 1, 512>(w, n, k, rb, xq, m, y, yt, ldy, s);
+        if (m <= 1) return launch_mmvq_cfg<PT, 1, 1, 2, 512>(sg, k, rb, xq, m, yt, s);
+        if (m <= 2) return launch_mmvq_cfg<PT, 2, 1, 2, 512>(sg, k, rb, xq, m, yt, s);
+        if (m <= 4) return launch_mmvq_cfg<PT, 4, 1, 1, 512>(sg, k, rb, xq, m, yt, s);
+        return launch_mmvq_cfg<PT, 8, 1, 1, 512>(sg, k, rb, xq, m, yt, s);
     }
     return cudaErrorInvalidValue;  // 64-value pieces: K <= 16384 gives at most 256 pieces
 }
 
-cudaError_t launch_mmvq_q8_0(const uint8_t *w, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y, int yt,
-                             int64_t ldy, cudaStream_t s);
-cudaError_t launch_mmvq_q4_k(const uint8_t *w, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y, int yt,
-                             int64_t ldy, cudaStream_t s);
-cudaError_t launch_mmvq_q6_k(const uint8_t *w, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y, int yt,
-                             int64_t ldy, cudaStream_t s);
+cudaError_t launch_mmvq_q8_0(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
+cudaError_t launch_mmvq_q4_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
+cudaError_t launch_mmvq_q6_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
 
 }  // namespace gg

@@ -13,8 +13,9 @@
 // mins, B = the 8 blocks' stored fp16 s_a (products exact in fp32).
 //
 // Work split.  A CTA of NW warps owns 16-row tiles; warp w takes super-blocks
-// [w * nsb / NW, (w + 1) * nsb / NW) of every tile and the warps' partial
-// results are summed through shared memory in a fixed order (deterministic).
+// [w * nsb / NW, (w + 1) * nsb / NW) of every tile; the warps' partial results
+// of up to 4 tiles are kept in shared memory and then summed in a fixed order
+// (deterministic; one CTA barrier per group of tiles).
 // The q8_1 rows (8 tokens) are copied once per CTA into shared memory with the
 // 32 quants of each block on an 8-byte boundary; the weights of the next
 // (tile, super-block) item load into registers while the current one computes.
@@ -40,19 +41,20 @@ __device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
-// Shared-memory layout (bytes) for rows of nblk = K/32 q8_1 blocks.
+// Shared-memory layout (bytes) for rows of nblk = K/32 q8_1 blocks; the
+// warps' partial sums of up to `grp` tiles are kept before one reduction.
 struct MmaSmem {
     int64_t xs, xs_pitch, da, saf, red, total;
 };
-__host__ __device__ inline MmaSmem mma_smem_layout(int64_t k, int nw) {
+__host__ __device__ inline MmaSmem mma_smem_layout(int64_t k, int nw, int grp) {
     const int64_t nblk = k / 32, nsb = k / 256;
     MmaSmem L;
     L.xs = 0;                                               // 8 token rows of nblk x 32 quants (+8 B pad)
     L.xs_pitch = (nblk * 40 + 127) / 128 * 128 + 32;        // 40 B per block; pitch = 32 mod 128 bytes
     L.da = L.xs + 8 * L.xs_pitch;                           // float [nblk][8]: d_a
     L.saf = L.da + nblk * 8 * 4;                            // uint32 [nsb][32]: s_a pairs for the min MMA
-    L.red = L.saf + nsb * 32 * 4;                           // float4 [2][nw][32]
-    L.total = L.red + 2 * (int64_t)nw * 32 * 16;
+    L.red = L.saf + nsb * 32 * 4;                           // float4 [2][grp][nw][32]
+    L.total = L.red + 2 * (int64_t)grp * nw * 32 * 16;
     return L;
 }
 
@@ -61,12 +63,13 @@ struct MmaW {
     uint2 q0[4], q1[4];  // bytes [32c + 8t, +8) of each chunk c, rows g and g+8
 };
 
-__global__ void __launch_bounds__(512, 1) mmvq_mma_q4k_kernel(const uint8_t *__restrict__ w, int64_t n, int64_t k,
-                                                             int64_t rb, const uint8_t *__restrict__ xq, int m_act,
-                                                             void *__restrict__ y, int yt, int64_t ldy) {
+__global__ void __launch_bounds__(512, 1) mmvq_mma_q4k_kernel(const MmvqSegs sg, int64_t k, int64_t rb,
+                                                             const uint8_t *__restrict__ xq, int m_act, int yt,
+                                                             int grp) {
+    const int64_t n = sg.rows();
     extern __shared__ __align__(16) uint8_t smem[];
     const int nw = blockDim.x >> 5;
-    const MmaSmem L = mma_smem_layout(k, nw);
+    const MmaSmem L = mma_smem_layout(k, nw, grp);
     uint8_t *xs = smem + L.xs;
     float *da = reinterpret_cast<float *>(smem + L.da);
     uint32_t *saf = reinterpret_cast<uint32_t *>(smem + L.saf);
@@ -83,10 +86,18 @@ __global__ void __launch_bounds__(512, 1) mmvq_mma_q4k_kernel(const uint8_t *__r
     // per-thread Q4_K scale selectors for sub-blocks 2t, 2t+1 (see Q4KPiece::pos)
     const Q4KPiece::Pos sel = Q4KPiece::pos(t);
 
+    // row base pointers of the tile being loaded (looked up once per tile)
+    int64_t cached_tile = -1;
+    const uint8_t *base0 = nullptr, *base1 = nullptr;
     auto load_item = [&](MmaW &W, int64_t tile, int sb) {
-        const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
-        const uint8_t *b0 = w + (r0 < n ? r0 : n - 1) * rb + sb * Q4_K_BYTES;
-        const uint8_t *b1 = w + (r1 < n ? r1 : n - 1) * rb + sb * Q4_K_BYTES;
+        if (tile != cached_tile) {
+            const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
+            base0 = seg_row(sg, r0 < n ? r0 : n - 1, rb);
+            base1 = seg_row(sg, r1 < n ? r1 : n - 1, rb);
+            cached_tile = tile;
+        }
+        const uint8_t *b0 = base0 + sb * Q4_K_BYTES;
+        const uint8_t *b1 = base1 + sb * Q4_K_BYTES;
         W.h0 = __ldg(reinterpret_cast<const uint4 *>(b0));
         W.h1 = __ldg(reinterpret_cast<const uint4 *>(b1));
 #pragma unroll
@@ -193,7 +204,7 @@ __global__ void __launch_bounds__(512, 1) mmvq_mma_q4k_kernel(const uint8_t *__r
         acc[3] = fmaf(-dm1, mv[3], acc[3]);
     };
 
-    int buf = 0;
+    int buf = 0, gi = 0;   // gi: tiles held in the current group
     for (; tile < n_tiles; tile += gridDim.x) {
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         // items of this tile, two register sets in turn; the item after the
@@ -216,21 +227,27 @@ __global__ void __launch_bounds__(512, 1) mmvq_mma_q4k_kernel(const uint8_t *__r
             }
             process(wb, sb + 1, acc);
         }
-        // sum the warps' partial results of this tile in a fixed order
-        red[(buf * nw + warp) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        __syncthreads();
-        for (int i = tid; i < 128; i += blockDim.x) {   // 16 rows x 8 tokens
-            const int l = i >> 2, e = i & 3;
-            float s = 0.0f;
-            for (int j = 0; j < nw; j++) {
-                const float4 v = red[(buf * nw + j) * 32 + l];
-                s += e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+        red[((buf * grp + gi) * nw + warp) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        gi++;
+        // every `grp` tiles (and after the last), sum the warps' partial results
+        // of the group's tiles in a fixed order
+        if (gi == grp || tile + gridDim.x >= n_tiles) {
+            __syncthreads();
+            for (int i = tid; i < gi * 128; i += blockDim.x) {   // per tile: 16 rows x 8 tokens
+                const int tt = i >> 7, l = (i >> 2) & 31, e = i & 3;
+                float s = 0.0f;
+                for (int j = 0; j < nw; j++) {
+                    const float4 v = red[((buf * grp + tt) * nw + j) * 32 + l];
+                    s += e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+                }
+                const int64_t t_of = tile - (int64_t)(gi - 1 - tt) * gridDim.x;
+                const int64_t row = t_of * 16 + (l >> 2) + 8 * (e >> 1);
+                const int tok = 2 * (l & 3) + (e & 1);
+                if (row < n && tok < m_act) seg_store(sg, yt, tok, row, s);
             }
-            const int64_t row = tile * 16 + (l >> 2) + 8 * (e >> 1);
-            const int tok = 2 * (l & 3) + (e & 1);
-            if (row < n && tok < m_act) store_out(y, yt, (int64_t)tok * ldy + row, s);
+            buf ^= 1;
+            gi = 0;
         }
-        buf ^= 1;
     }
 }
 
@@ -238,16 +255,21 @@ inline int mma_q4k_warps(int64_t k) {
     int nw = (int)(k / 256 / 2);
     return nw < 1 ? 1 : nw > 16 ? 16 : nw;
 }
-// whether the q8_1 rows fit in shared memory (K <= 16384)
-inline bool mma_q4k_fits(int64_t k) {
-    return mma_smem_layout(k, mma_q4k_warps(k)).total <= (int64_t)device_info().smem_optin;
+// tiles per reduction group: 4 when shared memory allows, else fewer (0: does not fit)
+inline int mma_q4k_group(int64_t k) {
+    for (int grp = 4; grp >= 1; grp /= 2)
+        if (mma_smem_layout(k, mma_q4k_warps(k), grp).total <= (int64_t)device_info().smem_optin) return grp;
+    return 0;
 }
+// whether the q8_1 rows fit in shared memory (K <= 16384)
+inline bool mma_q4k_fits(int64_t k) { return mma_q4k_group(k) > 0; }
 
-inline cudaError_t launch_mmvq_mma_q4k(const uint8_t *w, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y,
-                                       int yt, int64_t ldy, cudaStream_t s) {
-    const int nw = mma_q4k_warps(k);
-    const MmaSmem L = mma_smem_layout(k, nw);
-    if (L.total > (int64_t)device_info().smem_optin) return cudaErrorInvalidValue;
+inline cudaError_t launch_mmvq_mma_q4k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt,
+                                       cudaStream_t s) {
+    const int64_t n = sg.rows();
+    const int nw = mma_q4k_warps(k), grp = mma_q4k_group(k);
+    if (grp == 0) return cudaErrorInvalidValue;
+    const MmaSmem L = mma_smem_layout(k, nw, grp);
     auto kern = mmvq_mma_q4k_kernel;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
     if (e != cudaSuccess) return e;
@@ -268,7 +290,7 @@ inline cudaError_t launch_mmvq_mma_q4k(const uint8_t *w, int64_t n, int64_t k, c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, w, n, k, k / 256 * (int64_t)Q4_K_BYTES, xq, (int)m, y, yt, ldy);
+    return cudaLaunchKernelEx(&cfg, kern, sg, k, k / 256 * (int64_t)Q4_K_BYTES, xq, (int)m, yt, grp);
 }
 
 }  // namespace gg

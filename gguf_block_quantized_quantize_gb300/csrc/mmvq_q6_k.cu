@@ -3,9 +3,9 @@
 
 namespace gg {
 
-cudaError_t launch_mmvq_q6_k(const uint8_t *w, int64_t n, int64_t k, const uint8_t *xq, int64_t m, void *y, int yt,
-                             int64_t ldy, cudaStream_t s) {
-    return launch_mmvq_pt<Q6KPiece>(w, n, k, xq, m, y, yt, ldy, s, k / 256 * Q6_K_BYTES, MmvqTune{n >= 8192 && n < 32768, n >= 32768, false});
+cudaError_t launch_mmvq_q6_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s) {
+    const int64_t n = sg.rows();
+    return launch_mmvq_pt<Q6KPiece>(sg, k, xq, m, yt, s, k / 256 * Q6_K_BYTES, MmvqTune{n >= 8192 && n < 32768, n >= 32768, false});
 }
 
 }  // namespace gg

@@ -79,7 +79,7 @@ extern "C" gguf_status gguf_mul_mat_noalloc(const void *w, int wt, int64_t n, in
     // nothing has to be cleared between calls
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = launch_quantize_q8_1(x, xt, m, k, ldx, xq, nullptr, nullptr, s);
-    if (e == cudaSuccess) e = launch_mmvq((const uint8_t *)w, wt, n, k, xq, m, y, yt, ldy, s);
+    if (e == cudaSuccess) e = launch_mmvq(mmvq_one_segment(w, n, y, ldy), wt, k, xq, m, yt, s);
     if (e != cudaSuccess) {
         char msg[256];
         snprintf(msg, sizeof(msg), "mul_mat_noalloc: CUDA error %d (%s)", (int)e, cudaGetErrorString(e));

@@ -155,6 +155,34 @@ gguf_status gguf_mul_mat(const void *w, int wt, int64_t n, int64_t k, const void
                          int64_t ldx, void *y, int yt, int64_t ldy, void *ws, size_t ws_bytes, gguf_stream_t stream);
 
 /*
+ * gguf_mul_mat_segments -- several weight matrices ("segments") that read the
+ * same activations, e.g. the q/k/v or gate/up parts of a fused Linear:
+ * y_s[m][n_s] = X . W_s^T for every segment s.  FreeToken PR #690 (section
+ * "Vendored ggml") keeps one q8_1 quantization of the input for all segments;
+ * here X is quantized once and, in the MMVQ range, one kernel launch covers
+ * every segment (a row index runs through the segments in order).  The MMQ
+ * range shares the quantized operand and runs one GEMM per segment.
+ *   wt, k, x, xt, m, ldx, yt : as in gguf_mul_mat, common to all segments;
+ *   segs[nseg]               : host array, 1 <= nseg <= GGUF_MAX_SEGMENTS; each
+ *                              segment's w is 16-byte aligned [n][row_size(wt,k)]
+ *                              bytes, y is [m][ldy] of type yt (columns [0, n)
+ *                              written); n may be 0 (the segment is skipped).
+ *   ws                       : gguf_mul_mat_segments_ws_size(...) bytes.
+ * Errors as gguf_mul_mat; GGUF_ERR_INVALID_ARG for a bad segment count.
+ */
+#define GGUF_MAX_SEGMENTS 8
+typedef struct gguf_segment {
+    const void *w;  /* packed weight rows */
+    int64_t n;      /* rows (output columns) */
+    void *y;        /* output rows */
+    int64_t ldy;    /* output row stride in elements (>= n) */
+} gguf_segment;
+size_t gguf_mul_mat_segments_ws_size(int wt, const gguf_segment *segs, int nseg, int64_t k, int xt, int64_t m,
+                                     int yt);
+gguf_status gguf_mul_mat_segments(int wt, const gguf_segment *segs, int nseg, int64_t k, const void *x, int xt,
+                                  int64_t m, int64_t ldx, int yt, void *ws, size_t ws_bytes, gguf_stream_t stream);
+
+/*
  * gguf_mul_mat_noalloc -- gguf_mul_mat for decode-sized products (m <= 8 rows
  * of float activations, k <= 16384), with no workspace argument and no device
  * allocation.  The pages have no counterpart of this entry point: it is for

@@ -1,0 +1,83 @@
+"""GPU parity of gguf_mul_mat_segments: several weight matrices on one input.
+
+Each segment's output must equal the oracle's product for that weight, in
+every path: dp4a MMVQ (1..4 tokens), the int8 tensor-core MMVQ (5..8 tokens of
+Q4_K, where 16-row tiles straddle segment boundaries), MMVQ in 8-row chunks,
+and MMQ (one GEMM per segment on the shared operand).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _util import TOL_BF16, TOL_F32, assert_close
+from gguf_block_quantized_quantize_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def g():
+    from gguf_block_quantized_quantize_gb300 import build
+
+    build.build()
+    import gguf_block_quantized_quantize_gb300 as g
+
+    g.load_library()
+    return g
+
+
+def _u8(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0])
+@pytest.mark.parametrize("m", [1, 3, 6, 8, 40])
+def test_segments_match_oracle(g, wt, m):
+    k = 1024
+    ns = [2100, 0, 517, 64] if wt == oracle.Q4_K else [300, 0, 517, 64]
+    ws_ = [oracle.quantize_weights(wt, synth.normal((n, k), 0.02, seed=11 + i)) if n else None for i, n in enumerate(ns)]
+    x = synth.activations(m, k, seed=m, dtype=torch.float32)
+    xq = oracle.quantize_q8_1(x.numpy())
+    # outputs: column slices of one wide row-major tensor
+    wide = torch.zeros(m, sum(ns) + 5, dtype=torch.float32, device=DEV)
+    segs, c0 = [], 0
+    for w, n in zip(ws_, ns):
+        segs.append((_u8(w) if n else torch.zeros(16, dtype=torch.uint8, device=DEV), n, wide[:, c0:c0 + n]))
+        c0 += n
+    g.gguf_mul_mat_segments(wt, k, x.to(DEV), segs)
+    got = wide.cpu().numpy()
+    c0 = 0
+    for i, (w, n) in enumerate(zip(ws_, ns)):
+        if n:
+            ref = oracle.mul_mat(wt, w, k, xq)
+            assert_close(got[:, c0:c0 + n], ref, TOL_F32, f"segment {i} type {wt} m {m}")
+        c0 += n
+    assert np.all(got[:, c0:] == 0)   # columns past the segments untouched
+
+
+def test_segments_equal_separate_calls_bf16(g):
+    # the decode shape: two Q4_K matrices on one q8_1 copy, bf16 out
+    k = 4096
+    w1 = _u8(synth.safe_blocks(oracle.Q4_K, 4096, k, seed=1))
+    w2 = _u8(synth.safe_blocks(oracle.Q4_K, 2560, k, seed=2))   # both >= 2048 rows: same kernel at 8 tokens
+    for m in (1, 2, 4, 8):
+        x = synth.activations(m, k, seed=m, dtype=torch.bfloat16).to(DEV)
+        xq = g.gguf_quantize_q8_1(x)
+        y1 = torch.empty(m, 4096, dtype=torch.bfloat16, device=DEV)
+        y2 = torch.empty(m, 2560, dtype=torch.bfloat16, device=DEV)
+        g.gguf_mul_mat_segments(oracle.Q4_K, k, xq, [(w1, 4096, y1), (w2, 2560, y2)], xt=oracle.Q8_1, m=m)
+        r1 = g.gguf_mul_mat(w1, oracle.Q4_K, 4096, k, xq, xt=oracle.Q8_1, m=m, out_dtype=torch.bfloat16)
+        r2 = g.gguf_mul_mat(w2, oracle.Q4_K, 2560, k, xq, xt=oracle.Q8_1, m=m, out_dtype=torch.bfloat16)
+        # same kernels, same per-row arithmetic and reduction order
+        assert torch.equal(y1, r1) and torch.equal(y2, r2), m
+
+
+def test_segments_reject_bad_count(g):
+    x = torch.zeros(1, 256, dtype=torch.bfloat16, device=DEV)
+    y = torch.zeros(1, 8, dtype=torch.bfloat16, device=DEV)
+    w = torch.zeros(8 * 144, dtype=torch.uint8, device=DEV)
+    with pytest.raises(g.GgufError) as e:
+        g.gguf_mul_mat_segments(oracle.Q4_K, 256, x, [(w, 8, y)] * 9)
+    assert e.value.status == 1
