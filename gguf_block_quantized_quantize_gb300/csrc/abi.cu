@@ -64,7 +64,9 @@ const DeviceInfo &device_info() {
 static int64_t g_mmvq_max_m = 8;
 static int64_t g_mmq_enable = 1;
 static int64_t g_mmvq_tc = 1;
+static int64_t g_mmvq_tc_max_m = 16;   // 9..16 tokens: 2 n-tiles beat MMQ; 4 n-tiles do not
 int64_t option_mmvq_tc() { return g_mmvq_tc; }
+int64_t option_mmvq_tc_max_m() { return g_mmvq_tc_max_m; }
 
 static bool is_float(int t) { return t == GGUF_F32 || t == GGUF_F16 || t == GGUF_BF16; }
 static bool is_weight(int t) { return t == GGUF_Q8_0 || t == GGUF_Q4_K || t == GGUF_Q6_K; }
@@ -79,7 +81,13 @@ static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_
 
 // Which engine runs a dense product of m activation rows of length k: MMVQ
 // holds one 32-value piece per thread (k <= 16384); MMQ takes the rest.
-static bool use_mmq(int64_t m, int64_t k) { return k > 16384 || (g_mmq_enable != 0 && m > g_mmvq_max_m); }
+// MMQ above mmvq_max_m tokens (and for K > 16384), except Q4_K products that
+// the tensor-core MMVQ takes in one launch (up to mmvq_tc_max_m tokens)
+static bool use_mmq(int wt, int64_t m, int64_t k) {
+    if (k > 16384) return true;
+    if (m <= g_mmvq_max_m || g_mmq_enable == 0) return false;
+    return !mmvq_tc_wide(wt, k, m);
+}
 
 }  // namespace gg
 
@@ -145,7 +153,7 @@ gguf_status gguf_get_rows(const void *table, int tt, int64_t rows, int64_t k, co
 
 size_t gguf_mul_mat_ws_size(int wt, int64_t n, int64_t k, int xt, int64_t m, int yt) {
     if (m <= 0 || k <= 0 || k % 32) return 0;
-    if (use_mmq(m, k)) {
+    if (use_mmq(wt, m, k)) {
         // fp16 operand rows (plus their low parts for fp32 outputs), plus fp32
         // partial sums when K is split across CTAs (small m)
         const int64_t kx = op_pitch(wt, k);
@@ -197,7 +205,7 @@ static gguf_status mul_mat_impl(int wt, const gguf_segment *segs, int nseg, int6
     if (need > 0 && !aligned(ws, 16)) return fail(GGUF_ERR_ALIGNMENT, "%s: workspace must be 16-byte aligned", what);
     cudaStream_t s = (cudaStream_t)stream;
 
-    if (use_mmq(m, k)) {
+    if (use_mmq(wt, m, k)) {
         const int64_t kx = op_pitch(wt, k);
         uint8_t *wp = (uint8_t *)ws;
         uint16_t *xh = (uint16_t *)wp;
@@ -226,8 +234,10 @@ static gguf_status mul_mat_impl(int wt, const gguf_segment *segs, int nseg, int6
     }
     const int64_t xrb = row_size(GGUF_Q8_1, k);
     const int64_t ysz = esize(yt);
-    for (int64_t m0 = 0; m0 < m; m0 += 8) {  // MMVQ handles up to 8 rows per launch
-        const int64_t mc = m - m0 < 8 ? m - m0 : 8;
+    // MMVQ handles up to 8 rows per launch, or all of them on the wide tensor-core path
+    const int64_t chunk = mmvq_tc_wide(wt, k, m) ? m : 8;
+    for (int64_t m0 = 0; m0 < m; m0 += chunk) {
+        const int64_t mc = m - m0 < chunk ? m - m0 : chunk;
         MmvqSegs sg{};
         for (int i = 0; i < MMVQ_MAX_SEGS; i++) sg.end[i] = INT64_MAX;
         int64_t acc = 0;
@@ -424,6 +434,11 @@ gguf_status gguf_set_option(const char *key, int64_t value) {
         g_mmvq_tc = value != 0;
         return GGUF_OK;
     }
+    if (!strcmp(key, "mmvq_tc_max_m")) {
+        if (value < 8 || value > 32) return fail(GGUF_ERR_INVALID_ARG, "set_option: mmvq_tc_max_m must be in [8, 32]");
+        g_mmvq_tc_max_m = value;
+        return GGUF_OK;
+    }
     if (!strcmp(key, "mmq_enable")) {
         g_mmq_enable = value != 0;
         return GGUF_OK;
@@ -436,6 +451,7 @@ int64_t gguf_get_option(const char *key) {
     if (!strcmp(key, "mmvq_max_m")) return g_mmvq_max_m;
     if (!strcmp(key, "mmq_enable")) return g_mmq_enable;
     if (!strcmp(key, "mmvq_tc")) return g_mmvq_tc;
+    if (!strcmp(key, "mmvq_tc_max_m")) return g_mmvq_tc_max_m;
     return -1;
 }
 

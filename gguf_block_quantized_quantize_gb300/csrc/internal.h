@@ -40,6 +40,11 @@ cudaError_t launch_block_dots(const uint8_t *w, int wt, int64_t n, int64_t k, co
 
 // option "mmvq_tc": 5..8 tokens of Q4_K rows run on the tensor-core MMVQ (1, default) or dp4a (0)
 int64_t option_mmvq_tc();
+// option "mmvq_tc_max_m" (default 32): Q4_K products of 9..this many tokens run
+// as one tensor-core MMVQ launch instead of MMQ
+int64_t option_mmvq_tc_max_m();
+// whether m (> 8) tokens of K-long Q4_K rows take the tensor-core MMVQ
+bool mmvq_tc_wide(int wt, int64_t k, int64_t m);
 
 // Weight segments that read the same activations; one MMVQ launch covers all
 // of them.  Row r of the launch is row r - end[s-1] of segment s (end[-1] = 0);
@@ -56,7 +61,8 @@ struct MmvqSegs {
 // one segment: W[n][k] -> y[.][ldy]
 MmvqSegs mmvq_one_segment(const void *w, int64_t n, void *y, int64_t ldy);
 
-// for every segment s: y_s[m][ldy_s] (yt) = W_s (wt) . q8_1 rows xq[m] ; m <= 8
+// for every segment s: y_s[m][ldy_s] (yt) = W_s (wt) . q8_1 rows xq[m] ; m <= 8,
+// or m <= 32 when mmvq_tc_wide(wt, k, m)
 cudaError_t launch_mmvq(const MmvqSegs &sg, int wt, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
 
 // tensor-core MMQ: y[m][ldy] = W[n][k] . xh[m][k] (fp16 operand rows; fp32

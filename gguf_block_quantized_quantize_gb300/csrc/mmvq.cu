@@ -21,7 +21,7 @@ MmvqSegs mmvq_one_segment(const void *w, int64_t n, void *y, int64_t ldy) {
 cudaError_t launch_mmvq(const MmvqSegs &sg, int wt, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s) {
     if (sg.nseg < 1 || sg.nseg > MMVQ_MAX_SEGS) return cudaErrorInvalidValue;
     if (sg.rows() == 0 || m == 0) return cudaSuccess;
-    if (k / 32 > MMVQ_MAX_PIECES || m > 8) return cudaErrorInvalidValue;
+    if (k / 32 > MMVQ_MAX_PIECES || (m > 8 && !mmvq_tc_wide(wt, k, m))) return cudaErrorInvalidValue;
     switch (wt) {
     case GGUF_Q8_0: return launch_mmvq_q8_0(sg, k, xq, m, yt, s);
     case GGUF_Q4_K: return launch_mmvq_q4_k(sg, k, xq, m, yt, s);

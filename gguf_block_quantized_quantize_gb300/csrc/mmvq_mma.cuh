@@ -1,7 +1,8 @@
-// Tensor-core MMVQ for 5..8 tokens (Q4_K weights): the per-block int32 dot
+// Tensor-core MMVQ for 5..32 tokens (Q4_K weights): the per-block int32 dot
 // products of the blockwise formula run on warp-level int8 MMAs
 // (mma.sync m16n8k32 s8 x s8 -> s32).  One MMA is one 32-value block of 16
-// weight rows against 8 tokens, so its s32 accumulator is exactly the block
+// weight rows against 8 tokens (one n-tile; 2 or 4 n-tiles share the weight
+// fragments for 9..32 tokens), so its s32 accumulator is exactly the block
 // dot S_j of each (row, token) pair; scales are then applied per block in
 // fp32 as in the dp4a kernel:
 //   y += d * sum_j s_j * d_a,j * S_j  -  dmin * sum_j m_j * s_a,j
@@ -46,15 +47,15 @@ __device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32
 struct MmaSmem {
     int64_t xs, xs_pitch, da, saf, red, total;
 };
-__host__ __device__ inline MmaSmem mma_smem_layout(int64_t k, int nw, int grp) {
-    const int64_t nblk = k / 32, nsb = k / 256;
+__host__ __device__ inline MmaSmem mma_smem_layout(int64_t k, int nw, int grp, int nt) {
+    const int64_t nblk = k / 32, nsb = k / 256, tok = 8 * (int64_t)nt;
     MmaSmem L;
-    L.xs = 0;                                               // 8 token rows of nblk x 32 quants (+8 B pad)
+    L.xs = 0;                                               // 8*nt token rows of nblk x 32 quants (+8 B pad)
     L.xs_pitch = (nblk * 40 + 127) / 128 * 128 + 32;        // 40 B per block; pitch = 32 mod 128 bytes
-    L.da = L.xs + 8 * L.xs_pitch;                           // float [nblk][8]: d_a
-    L.saf = L.da + nblk * 8 * 4;                            // uint32 [nsb][32]: s_a pairs for the min MMA
-    L.red = L.saf + nsb * 32 * 4;                           // float4 [2][grp][nw][32]
-    L.total = L.red + 2 * (int64_t)grp * nw * 32 * 16;
+    L.da = L.xs + tok * L.xs_pitch;                         // float [nblk][8*nt]: d_a
+    L.saf = L.da + nblk * tok * 4;                          // uint32 [nsb][nt][32]: s_a pairs for the min MMA
+    L.red = L.saf + nsb * nt * 32 * 4;                      // float4 [2][grp][nw][nt][32]
+    L.total = L.red + 2 * (int64_t)grp * nw * nt * 32 * 16;
     return L;
 }
 
@@ -63,13 +64,16 @@ struct MmaW {
     uint2 q0[4], q1[4];  // bytes [32c + 8t, +8) of each chunk c, rows g and g+8
 };
 
-__global__ void __launch_bounds__(512, 1) mmvq_mma_q4k_kernel(const MmvqSegs sg, int64_t k, int64_t rb,
-                                                             const uint8_t *__restrict__ xq, int m_act, int yt,
-                                                             int grp) {
+// NT: n-tiles of 8 tokens (8*NT tokens at most)
+template <int NT>
+__global__ void __launch_bounds__(NT == 1 ? 512 : 256, 1)
+    mmvq_mma_q4k_kernel(const MmvqSegs sg, int64_t k, int64_t rb, const uint8_t *__restrict__ xq, int m_act, int yt,
+                        int grp) {
+    constexpr int TOK = 8 * NT;
     const int64_t n = sg.rows();
     extern __shared__ __align__(16) uint8_t smem[];
     const int nw = blockDim.x >> 5;
-    const MmaSmem L = mma_smem_layout(k, nw, grp);
+    const MmaSmem L = mma_smem_layout(k, nw, grp, NT);
     uint8_t *xs = smem + L.xs;
     float *da = reinterpret_cast<float *>(smem + L.da);
     uint32_t *saf = reinterpret_cast<uint32_t *>(smem + L.saf);
@@ -116,7 +120,7 @@ __global__ void __launch_bounds__(512, 1) mmvq_mma_q4k_kernel(const MmvqSegs sg,
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- q8_1 rows into shared memory (quants of block b at b * 40 + 8), d_a and s_a pairs
-    for (int i = tid; i < 8 * nblk; i += blockDim.x) {
+    for (int i = tid; i < TOK * nblk; i += blockDim.x) {
         const int tok = i / nblk, b = i - tok * nblk;
         uint32_t *dst = reinterpret_cast<uint32_t *>(xs + tok * pitch + b * 40 + 8);
         if (tok < m_act) {
@@ -128,12 +132,12 @@ __global__ void __launch_bounds__(512, 1) mmvq_mma_q4k_kernel(const MmvqSegs sg,
             for (int j = 0; j < 8; j++) dst[j] = 0u;
         }
     }
-    for (int i = tid; i < nblk * 8; i += blockDim.x) {
-        const int b = i >> 3, tok = i & 7;
+    for (int i = tid; i < nblk * TOK; i += blockDim.x) {
+        const int b = i / TOK, tok = i % TOK;
         da[i] = tok < m_act ? h2f(ld_u16(xq + tok * xrb + (int64_t)b * Q8_1_BYTES)) : 0.0f;
     }
-    for (int i = tid; i < nsb * 32; i += blockDim.x) {
-        const int s = i >> 5, l = i & 31, tok = l >> 2, tt = l & 3;
+    for (int i = tid; i < nsb * NT * 32; i += blockDim.x) {   // [sb][nt][lane]
+        const int s = i / (NT * 32), l = i & 31, tok = 8 * ((i >> 5) % NT) + (l >> 2), tt = l & 3;
         uint32_t v = 0u;
         if (tok < m_act) {
             const uint8_t *b = xq + tok * xrb + (int64_t)(s * 8 + 2 * tt) * Q8_1_BYTES;
@@ -143,11 +147,11 @@ __global__ void __launch_bounds__(512, 1) mmvq_mma_q4k_kernel(const MmvqSegs sg,
     }
     __syncthreads();
 
-    const uint8_t *xg = xs + g * pitch + 8 + 8 * t;   // this lane's B bytes: token g, values 8t .. 8t+7
+    const uint8_t *xg = xs + g * pitch + 8 + 8 * t;   // this lane's B bytes: token 8nt + g, values 8t .. 8t+7
     const __half2 bias = __floats2half2_rn(-1024.0f, -1024.0f);
 
-    // one (tile, super-block) item; partial sums of rows g, g+8 x tokens 2t, 2t+1 into acc
-    auto process = [&](const MmaW &W, int sb, float (&acc)[4]) {
+    // one (tile, super-block) item; partial sums of rows g, g+8 x tokens 8nt + 2t, +1 into acc[nt]
+    auto process = [&](const MmaW &W, int sb, float (&acc)[NT][4]) {
         const float d0 = h2f(W.h0.x & 0xffff), dm0 = h2f(W.h0.x >> 16);
         const float d1 = h2f(W.h1.x & 0xffff), dm1 = h2f(W.h1.x >> 16);
         // (s, m) of sub-blocks 2t, 2t+1 for rows g and g+8 as bytes (s0, s1, m0, m1)
@@ -157,32 +161,41 @@ __global__ void __launch_bounds__(512, 1) mmvq_mma_q4k_kernel(const MmvqSegs sg,
         const uint32_t sm1 = (r1 & sel.m1) | ((r1 >> 2) & sel.m2) | (w1 & sel.m3) | ((w1 >> 4) & sel.m4);
         // the scales of chunk c are decoded by lane t = c of the quad
         const uint32_t sp = __byte_perm(sm0, sm1, 0x5410);   // s_2t(g), s_2t+1(g), s_2t(g+8), s_2t+1(g+8)
-        float u[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float u[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+            for (int i = 0; i < 4; i++) u[nt][i] = 0.0f;
 #pragma unroll
         for (int c = 0; c < 4; c++) {
             const uint32_t sc = __shfl_sync(0xffffffffu, sp, (lane & ~3) | c);
             const float sl0 = (float)(sc & 0xff), sh0 = (float)((sc >> 8) & 0xff);
             const float sl1 = (float)((sc >> 16) & 0xff), sh1 = (float)(sc >> 24);
             const int bl = sb * 8 + 2 * c;   // block of the low nibbles; bl + 1 of the high ones
-            const uint2 bL = *reinterpret_cast<const uint2 *>(xg + bl * 40);
-            const uint2 bH = *reinterpret_cast<const uint2 *>(xg + (bl + 1) * 40);
             const uint2 x0 = W.q0[c], x1 = W.q1[c];
-            int sL[4], sH[4];
-            mma_16832_s8(sL, x0.x & 0x0F0F0F0Fu, x1.x & 0x0F0F0F0Fu, x0.y & 0x0F0F0F0Fu, x1.y & 0x0F0F0F0Fu,
-                         bL.x, bL.y);
-            mma_16832_s8(sH, (x0.x >> 4) & 0x0F0F0F0Fu, (x1.x >> 4) & 0x0F0F0F0Fu, (x0.y >> 4) & 0x0F0F0F0Fu,
-                         (x1.y >> 4) & 0x0F0F0F0Fu, bH.x, bH.y);
-            const float2 dL = *reinterpret_cast<const float2 *>(da + bl * 8 + 2 * t);
-            const float2 dH = *reinterpret_cast<const float2 *>(da + (bl + 1) * 8 + 2 * t);
-            // accumulator i: row g (i < 2) or g+8, token 2t + (i & 1)
-            u[0] = fmaf(sl0, dL.x * (float)sL[0], u[0]);
-            u[1] = fmaf(sl0, dL.y * (float)sL[1], u[1]);
-            u[2] = fmaf(sl1, dL.x * (float)sL[2], u[2]);
-            u[3] = fmaf(sl1, dL.y * (float)sL[3], u[3]);
-            u[0] = fmaf(sh0, dH.x * (float)sH[0], u[0]);
-            u[1] = fmaf(sh0, dH.y * (float)sH[1], u[1]);
-            u[2] = fmaf(sh1, dH.x * (float)sH[2], u[2]);
-            u[3] = fmaf(sh1, dH.y * (float)sH[3], u[3]);
+            const uint32_t lo00 = x0.x & 0x0F0F0F0Fu, lo10 = x1.x & 0x0F0F0F0Fu;
+            const uint32_t lo01 = x0.y & 0x0F0F0F0Fu, lo11 = x1.y & 0x0F0F0F0Fu;
+            const uint32_t hi00 = (x0.x >> 4) & 0x0F0F0F0Fu, hi10 = (x1.x >> 4) & 0x0F0F0F0Fu;
+            const uint32_t hi01 = (x0.y >> 4) & 0x0F0F0F0Fu, hi11 = (x1.y >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) {
+                const uint2 bL = *reinterpret_cast<const uint2 *>(xg + 8 * nt * pitch + bl * 40);
+                const uint2 bH = *reinterpret_cast<const uint2 *>(xg + 8 * nt * pitch + (bl + 1) * 40);
+                int sL[4], sH[4];
+                mma_16832_s8(sL, lo00, lo10, lo01, lo11, bL.x, bL.y);
+                mma_16832_s8(sH, hi00, hi10, hi01, hi11, bH.x, bH.y);
+                const float2 dL = *reinterpret_cast<const float2 *>(da + bl * TOK + 8 * nt + 2 * t);
+                const float2 dH = *reinterpret_cast<const float2 *>(da + (bl + 1) * TOK + 8 * nt + 2 * t);
+                // accumulator i: row g (i < 2) or g+8, token 8nt + 2t + (i & 1)
+                u[nt][0] = fmaf(sl0, dL.x * (float)sL[0], u[nt][0]);
+                u[nt][1] = fmaf(sl0, dL.y * (float)sL[1], u[nt][1]);
+                u[nt][2] = fmaf(sl1, dL.x * (float)sL[2], u[nt][2]);
+                u[nt][3] = fmaf(sl1, dL.y * (float)sL[3], u[nt][3]);
+                u[nt][0] = fmaf(sh0, dH.x * (float)sH[0], u[nt][0]);
+                u[nt][1] = fmaf(sh0, dH.y * (float)sH[1], u[nt][1]);
+                u[nt][2] = fmaf(sh1, dH.x * (float)sH[2], u[nt][2]);
+                u[nt][3] = fmaf(sh1, dH.y * (float)sH[3], u[nt][3]);
+            }
         }
         // min term: A = m_2t, m_2t+1 of rows g, g+8 at k-slots 2t, 2t+1 (exact fp16 integers)
         uint32_t ma0 = __byte_perm(sm0, 0x64u, 0x4342), ma1 = __byte_perm(sm1, 0x64u, 0x4342);
@@ -192,21 +205,28 @@ __global__ void __launch_bounds__(512, 1) mmvq_mma_q4k_kernel(const MmvqSegs sg,
             ma0 = *reinterpret_cast<uint32_t *>(&h0);
             ma1 = *reinterpret_cast<uint32_t *>(&h1);
         }
-        float mv[4];
-        mma_16816_f16(mv, ma0, ma1, 0u, 0u, saf[sb * 32 + lane], 0u);
-        acc[0] = fmaf(d0, u[0], acc[0]);
-        acc[1] = fmaf(d0, u[1], acc[1]);
-        acc[2] = fmaf(d1, u[2], acc[2]);
-        acc[3] = fmaf(d1, u[3], acc[3]);
-        acc[0] = fmaf(-dm0, mv[0], acc[0]);
-        acc[1] = fmaf(-dm0, mv[1], acc[1]);
-        acc[2] = fmaf(-dm1, mv[2], acc[2]);
-        acc[3] = fmaf(-dm1, mv[3], acc[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+            float mv[4];
+            mma_16816_f16(mv, ma0, ma1, 0u, 0u, saf[(sb * NT + nt) * 32 + lane], 0u);
+            acc[nt][0] = fmaf(d0, u[nt][0], acc[nt][0]);
+            acc[nt][1] = fmaf(d0, u[nt][1], acc[nt][1]);
+            acc[nt][2] = fmaf(d1, u[nt][2], acc[nt][2]);
+            acc[nt][3] = fmaf(d1, u[nt][3], acc[nt][3]);
+            acc[nt][0] = fmaf(-dm0, mv[0], acc[nt][0]);
+            acc[nt][1] = fmaf(-dm0, mv[1], acc[nt][1]);
+            acc[nt][2] = fmaf(-dm1, mv[2], acc[nt][2]);
+            acc[nt][3] = fmaf(-dm1, mv[3], acc[nt][3]);
+        }
     };
 
     int buf = 0, gi = 0;   // gi: tiles held in the current group
     for (; tile < n_tiles; tile += gridDim.x) {
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+            for (int i = 0; i < 4; i++) acc[nt][i] = 0.0f;
         // items of this tile, two register sets in turn; the item after the
         // last one of the tile is the first of the next tile
         for (int sb = sb_lo; sb < sb_hi; sb += 2) {
@@ -227,22 +247,25 @@ __global__ void __launch_bounds__(512, 1) mmvq_mma_q4k_kernel(const MmvqSegs sg,
             }
             process(wb, sb + 1, acc);
         }
-        red[((buf * grp + gi) * nw + warp) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+            red[(((buf * grp + gi) * nw + warp) * NT + nt) * 32 + lane] =
+                make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
         gi++;
         // every `grp` tiles (and after the last), sum the warps' partial results
         // of the group's tiles in a fixed order
         if (gi == grp || tile + gridDim.x >= n_tiles) {
             __syncthreads();
-            for (int i = tid; i < gi * 128; i += blockDim.x) {   // per tile: 16 rows x 8 tokens
-                const int tt = i >> 7, l = (i >> 2) & 31, e = i & 3;
+            for (int i = tid; i < gi * 128 * NT; i += blockDim.x) {   // per tile: 16 rows x 8*NT tokens
+                const int tt = i / (128 * NT), rem = i % (128 * NT), nt = rem >> 7, l = (rem >> 2) & 31, e = rem & 3;
                 float s = 0.0f;
                 for (int j = 0; j < nw; j++) {
-                    const float4 v = red[((buf * grp + tt) * nw + j) * 32 + l];
+                    const float4 v = red[(((buf * grp + tt) * nw + j) * NT + nt) * 32 + l];
                     s += e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
                 }
                 const int64_t t_of = tile - (int64_t)(gi - 1 - tt) * gridDim.x;
                 const int64_t row = t_of * 16 + (l >> 2) + 8 * (e >> 1);
-                const int tok = 2 * (l & 3) + (e & 1);
+                const int tok = 8 * nt + 2 * (l & 3) + (e & 1);
                 if (row < n && tok < m_act) seg_store(sg, yt, tok, row, s);
             }
             buf ^= 1;
@@ -251,26 +274,30 @@ __global__ void __launch_bounds__(512, 1) mmvq_mma_q4k_kernel(const MmvqSegs sg,
     }
 }
 
-inline int mma_q4k_warps(int64_t k) {
+inline int mma_q4k_warps(int64_t k, int nt) {
+    const int cap = nt == 1 ? 16 : 8;   // 512 / 256 threads
     int nw = (int)(k / 256 / 2);
-    return nw < 1 ? 1 : nw > 16 ? 16 : nw;
+    return nw < 1 ? 1 : nw > cap ? cap : nw;
 }
 // tiles per reduction group: 4 when shared memory allows, else fewer (0: does not fit)
-inline int mma_q4k_group(int64_t k) {
+inline int mma_q4k_group(int64_t k, int nt) {
     for (int grp = 4; grp >= 1; grp /= 2)
-        if (mma_smem_layout(k, mma_q4k_warps(k), grp).total <= (int64_t)device_info().smem_optin) return grp;
+        if (mma_smem_layout(k, mma_q4k_warps(k, nt), grp, nt).total <= (int64_t)device_info().smem_optin) return grp;
     return 0;
 }
-// whether the q8_1 rows fit in shared memory (K <= 16384)
-inline bool mma_q4k_fits(int64_t k) { return mma_q4k_group(k) > 0; }
+inline int mma_q4k_ntiles(int64_t m) { return m <= 8 ? 1 : m <= 16 ? 2 : 4; }
+// whether the tensor-core MMVQ takes m tokens of K-long Q4_K rows (the q8_1
+// rows must fit in shared memory; m <= 32)
+inline bool mma_q4k_fits(int64_t k, int64_t m) { return m <= 32 && mma_q4k_group(k, mma_q4k_ntiles(m)) > 0; }
 
-inline cudaError_t launch_mmvq_mma_q4k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt,
-                                       cudaStream_t s) {
+template <int NT>
+inline cudaError_t launch_mmvq_mma_q4k_nt(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt,
+                                          cudaStream_t s) {
     const int64_t n = sg.rows();
-    const int nw = mma_q4k_warps(k), grp = mma_q4k_group(k);
+    const int nw = mma_q4k_warps(k, NT), grp = mma_q4k_group(k, NT);
     if (grp == 0) return cudaErrorInvalidValue;
-    const MmaSmem L = mma_smem_layout(k, nw, grp);
-    auto kern = mmvq_mma_q4k_kernel;
+    const MmaSmem L = mma_smem_layout(k, nw, grp, NT);
+    auto kern = mmvq_mma_q4k_kernel<NT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
@@ -291,6 +318,15 @@ inline cudaError_t launch_mmvq_mma_q4k(const MmvqSegs &sg, int64_t k, const uint
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, sg, k, k / 256 * (int64_t)Q4_K_BYTES, xq, (int)m, yt, grp);
+}
+
+inline cudaError_t launch_mmvq_mma_q4k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt,
+                                       cudaStream_t s) {
+    switch (mma_q4k_ntiles(m)) {
+    case 1: return launch_mmvq_mma_q4k_nt<1>(sg, k, xq, m, yt, s);
+    case 2: return launch_mmvq_mma_q4k_nt<2>(sg, k, xq, m, yt, s);
+    default: return launch_mmvq_mma_q4k_nt<4>(sg, k, xq, m, yt, s);
+    }
 }
 
 }  // namespace gg

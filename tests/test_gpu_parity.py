@@ -184,6 +184,27 @@ def test_mmvq_tensor_core_vs_dp4a(g, k, m):
     assert_close(b, ref, TOL_F32, f"dp4a mmvq k {k} m {m}")
 
 
+@pytest.mark.parametrize("m", [9, 12, 16, 17, 24, 32])
+@pytest.mark.parametrize("n,k", [(300, 256), (2100, 3072), (700, 4096)])
+def test_mmvq_wide_tensor_core(g, m, n, k):
+    # 9..32 tokens of Q4_K rows: one tensor-core MMVQ launch with 2 or 4
+    # n-tiles (option mmvq_tc_max_m at 32); with the option at 8 the same
+    # product runs on MMQ, and both match the oracle
+    w = _weights(oracle.Q4_K, n, k, seed=m + n)
+    x = synth.activations(m, k, seed=k + m, dtype=torch.float32)
+    ref = oracle.mul_mat(oracle.Q4_K, w, k, oracle.quantize_q8_1(x.numpy()))
+    saved = g.gguf_get_option("mmvq_tc_max_m")
+    try:
+        g.gguf_set_option("mmvq_tc_max_m", 32)
+        a = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x.to(DEV)).cpu().numpy()
+        g.gguf_set_option("mmvq_tc_max_m", 8)
+        b = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x.to(DEV)).cpu().numpy()
+    finally:
+        g.gguf_set_option("mmvq_tc_max_m", saved)
+    assert_close(a, ref, TOL_F32, f"wide mmvq m {m} n {n} k {k}")
+    assert_close(b, ref, TOL_F32, f"mmq m {m} n {n} k {k}")
+
+
 @pytest.mark.parametrize("wt,n,k", [(oracle.Q6_K, 40000, 3072), (oracle.Q4_K, 20000, 3072)])
 @pytest.mark.parametrize("m", [1, 2, 8])
 def test_mmvq_tall_sampled(g, wt, n, k, m):
