@@ -65,7 +65,9 @@ static int64_t g_mmvq_max_m = 8;
 static int64_t g_mmq_enable = 1;
 static int64_t g_mmvq_tc = 1;
 static int64_t g_mmvq_tc_max_m = 16;   // 9..16 tokens: 2 n-tiles beat MMQ; 4 n-tiles do not
+static int64_t g_mmvq_tc_min_m = 5;
 int64_t option_mmvq_tc() { return g_mmvq_tc; }
+int64_t option_mmvq_tc_min_m() { return g_mmvq_tc_min_m; }
 int64_t option_mmvq_tc_max_m() { return g_mmvq_tc_max_m; }
 
 static bool is_float(int t) { return t == GGUF_F32 || t == GGUF_F16 || t == GGUF_BF16; }
@@ -434,6 +436,11 @@ gguf_status gguf_set_option(const char *key, int64_t value) {
         g_mmvq_tc = value != 0;
         return GGUF_OK;
     }
+    if (!strcmp(key, "mmvq_tc_min_m")) {
+        if (value < 1 || value > 8) return fail(GGUF_ERR_INVALID_ARG, "set_option: mmvq_tc_min_m must be in [1, 8]");
+        g_mmvq_tc_min_m = value;
+        return GGUF_OK;
+    }
     if (!strcmp(key, "mmvq_tc_max_m")) {
         if (value < 8 || value > 32) return fail(GGUF_ERR_INVALID_ARG, "set_option: mmvq_tc_max_m must be in [8, 32]");
         g_mmvq_tc_max_m = value;
@@ -451,6 +458,7 @@ int64_t gguf_get_option(const char *key) {
     if (!strcmp(key, "mmvq_max_m")) return g_mmvq_max_m;
     if (!strcmp(key, "mmq_enable")) return g_mmq_enable;
     if (!strcmp(key, "mmvq_tc")) return g_mmvq_tc;
+    if (!strcmp(key, "mmvq_tc_min_m")) return g_mmvq_tc_min_m;
     if (!strcmp(key, "mmvq_tc_max_m")) return g_mmvq_tc_max_m;
     return -1;
 }

@@ -40,6 +40,7 @@ cudaError_t launch_block_dots(const uint8_t *w, int wt, int64_t n, int64_t k, co
 
 // option "mmvq_tc": 5..8 tokens of Q4_K rows run on the tensor-core MMVQ (1, default) or dp4a (0)
 int64_t option_mmvq_tc();
+int64_t option_mmvq_tc_min_m();
 // option "mmvq_tc_max_m" (default 32): Q4_K products of 9..this many tokens run
 // as one tensor-core MMVQ launch instead of MMQ
 int64_t option_mmvq_tc_max_m();

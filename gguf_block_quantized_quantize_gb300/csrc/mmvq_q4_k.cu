@@ -6,11 +6,12 @@ namespace gg {
 cudaError_t launch_mmvq_q4_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s) {
     const int64_t n = sg.rows();
     // 9..32 tokens: the tensor-core kernel with 2 or 4 n-tiles (the caller
-    // checked mmvq_tc_wide); 5..8 tokens: the tensor-core kernel when the q8_1
-    // rows fit in shared memory and there are enough 16-row tiles to fill the
-    // GPU (below 2048 rows the per-CTA staging of the activations outweighs it)
+    // checked mmvq_tc_wide); mmvq_tc_min_m..8 tokens: the tensor-core kernel
+    // when the q8_1 rows fit in shared memory and there are enough 16-row
+    // tiles to fill the GPU (below 2048 rows the per-CTA staging of the
+    // activations outweighs it)
     if (m > 8) return mma_q4k_fits(k, m) ? launch_mmvq_mma_q4k(sg, k, xq, m, yt, s) : cudaErrorInvalidValue;
-    if (m >= 5 && n >= 2048 && option_mmvq_tc() && mma_q4k_fits(k, m))
+    if (m >= option_mmvq_tc_min_m() && n >= 2048 && option_mmvq_tc() && mma_q4k_fits(k, m))
         return launch_mmvq_mma_q4k(sg, k, xq, m, yt, s);
     return launch_mmvq_pt<Q4KPiece>(sg, k, xq, m, yt, s, k / 256 * Q4_K_BYTES,
                                     MmvqTune{n >= 8192, false, true});

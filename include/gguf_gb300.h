@@ -144,7 +144,8 @@ gguf_status gguf_get_rows(const void *table, int tt, int64_t rows, int64_t k, co
  *        (may be NULL when that size is 0).
  * Path: small m (<= option "mmvq_max_m", default 8; Q4_K up to option
  * "mmvq_tc_max_m", default 16) runs the bandwidth-bound MMVQ kernel
- * (per-block int8 dot products, exact int32 block sums, fp32 combination);
+ * (exact int32 block sums from dp4a or int8 tensor-core MMAs, then the fp32
+ * combination of the scales);
  * larger m runs the tensor-core MMQ kernel, which feeds tcgen05
  * fp16 operands (the exact fp32 block value of each weight and d16*q of each
  * activation) with fp32 accumulation: one fp16 operand per side for 16-bit
@@ -314,10 +315,13 @@ gguf_status gguf_debug_block_dots(const void *w, int wt, int64_t n, int64_t k, c
  *   "mmvq_max_m"  : largest m routed to MMVQ (default 8; FreeToken issue #671,
  *                   "Known issues": MMQ takes over above 8 tokens).
  *   "mmq_enable"  : 0 routes every m through MMVQ (default 1).
- *   "mmvq_tc"     : 1 (default) lets 5..8 tokens of Q4_K rows (n >= 2048) run
- *                   the int8 tensor-core MMVQ; 0 keeps them on the dp4a MMVQ.
+ *   "mmvq_tc"     : 1 (default) lets mmvq_tc_min_m..8 tokens of Q4_K rows
+ *                   (n >= 2048) run the tensor-core MMVQ; 0 keeps them on the
+ *                   dp4a MMVQ.
+ *   "mmvq_tc_min_m": fewest tokens that take the tensor-core MMVQ, 1 .. 8
+ *                   (default 5).
  *   "mmvq_tc_max_m": Q4_K products of 9 up to this many tokens stay on the
- *                   int8 tensor-core MMVQ (2 or 4 n-tiles of 8 tokens) instead
+ *                   tensor-core MMVQ (2 or 4 n-tiles of 8 tokens) instead
  *                   of MMQ; 8 .. 32, default 16 (the measured crossover on
  *                   GB300: 4 n-tiles are not faster than MMQ).
  * Returns GGUF_ERR_INVALID_ARG for an unknown key or a value out of range.

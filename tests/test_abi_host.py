@@ -96,5 +96,7 @@ def test_other_entry_points_reject_bad_arguments(g):
     assert L.gguf_set_option(b"no_such_key", 1) == 1
     assert L.gguf_set_option(b"mmvq_max_m", 8) == 0 and L.gguf_get_option(b"mmvq_max_m") == 8
     assert L.gguf_get_option(b"mmvq_tc") == 1
+    assert L.gguf_get_option(b"mmvq_tc_min_m") == 5
+    assert L.gguf_set_option(b"mmvq_tc_min_m", 0) != 0 and L.gguf_get_option(b"mmvq_tc_min_m") == 5
     assert L.gguf_get_option(b"mmvq_tc_max_m") == 16
     assert L.gguf_set_option(b"mmvq_tc_max_m", 64) != 0 and L.gguf_get_option(b"mmvq_tc_max_m") == 16

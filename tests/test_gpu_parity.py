@@ -205,6 +205,42 @@ def test_mmvq_wide_tensor_core(g, m, n, k):
     assert_close(b, ref, TOL_F32, f"mmq m {m} n {n} k {k}")
 
 
+def _q4_k_plain_nibbles(nib):
+    # Q4_K rows with d = 1, dmin = 0 and every sub-block scale 1, min 0: the
+    # blocks hold the nibbles themselves (chunk c of 64 values: byte i has
+    # value 64c + i in its low and 64c + 32 + i in its high nibble)
+    n, k = nib.shape
+    blk = np.zeros((n, k // 256, 144), np.uint8)
+    blk[:, :, 1] = 0x3C                                   # d = fp16 1.0 (0x3C00)
+    blk[:, :, 4:8] = 1                                    # scales of sub-blocks 0..3
+    blk[:, :, 12:16] = 1                                  # scales of sub-blocks 4..7 (low bits)
+    q = nib.reshape(n, k // 256, 4, 2, 32).astype(np.uint8)
+    blk[:, :, 16:] = (q[:, :, :, 0, :] | (q[:, :, :, 1, :] << 4)).reshape(n, k // 256, 128)
+    return blk.reshape(n, -1)
+
+
+@pytest.mark.parametrize("m", [5, 8, 16])
+def test_mmvq_tensor_core_exact_integer_sums(g, m):
+    # With plain-nibble Q4_K rows and integer activations whose every 32-block
+    # reaches 127 (so d_a = 1 and q = x), y is the integer product W . X, below
+    # 2^24 and so exact in fp32.  The tensor-core MMVQ sums every block exactly
+    # and combines the sums in fp32 without rounding here, so y must match the
+    # int64 product bit for bit (5..8 tokens: one n-tile; 16 tokens: two).
+    n, k = 2048, 4096
+    rng = np.random.default_rng(m)
+    nib = rng.integers(0, 16, size=(n, k), dtype=np.int64)
+    xi = rng.integers(-127, 128, size=(m, k), dtype=np.int64)
+    xi[:, ::32] = 127
+    w = _q4_k_plain_nibbles(nib)
+    assert np.array_equal(oracle.dequantize_f32(oracle.Q4_K, w, k), nib.astype(np.float32))
+    want = (xi @ nib.T).astype(np.float64)
+    assert np.abs(want).max() < 2 ** 24
+    x = torch.from_numpy(xi.astype(np.float32))
+    assert np.array_equal(oracle.mul_mat(oracle.Q4_K, w, k, oracle.quantize_q8_1(xi.astype(np.float32))), want)
+    y = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x.to(DEV)).cpu().numpy()
+    assert np.array_equal(y.astype(np.float64), want), f"max diff {np.abs(y - want).max()}"
+
+
 @pytest.mark.parametrize("wt,n,k", [(oracle.Q6_K, 40000, 3072), (oracle.Q4_K, 20000, 3072)])
 @pytest.mark.parametrize("m", [1, 2, 8])
 def test_mmvq_tall_sampled(g, wt, n, k, m):
