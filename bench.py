@@ -123,7 +123,12 @@ class Decode:
     matrix; one quantize pass turns all of them into q8_1, and each batch's
     row slice feeds both weight matrices (every weight that reads the same
     activations shares one quantization).  Weight copies rotate over more
-    than 4x L2 per shape, so no launch finds its weights in L2."""
+    than 4x L2 per shape, so no launch finds its weights in L2.
+
+    The eight products depend only on the quantized rows, so a step runs them
+    on two CUDA streams (M = 8 and 2 beside M = 4 and 1), which overlaps the
+    start and end of one launch with the other stream's; `serial` keeps them
+    on one stream (the per-kernel roofline is timed that way)."""
 
     def __init__(self, torch, g, synth, dev):
         self.g = g
@@ -149,9 +154,18 @@ class Decode:
             r0 += m
         self.xs = {m: self.x_all[a:b] for m, (a, b) in self.rows.items()}
         self.xqs = {m: self.xq_all[a:b] for m, (a, b) in self.rows.items()}
-        self.ys = {(n, m): torch.empty((m, n), dtype=torch.bfloat16, device=dev) for (n, _) in DECODE_SHAPES
-                   for m in DECODE_MS}
+        # all outputs in one buffer (one device-to-host read in the e2e loop)
+        sizes = [(n, m) for m in DECODE_MS for (n, _) in DECODE_SHAPES]
+        self.y_all = torch.empty(sum(n * m for n, m in sizes), dtype=torch.bfloat16, device=dev)
+        self.ys, off = {}, 0
+        for (n, m) in sizes:
+            self.ys[(n, m)] = self.y_all[off:off + n * m].view(m, n)
+            off += n * m
         self.n_phase = max(p.shape[0] for p in self.pools.values())
+        self.torch = torch
+        self.side = torch.cuda.Stream(device=dev)
+        # MMVQ on q8_1 input needs no workspace; passing one skips the size query
+        self.ws = torch.empty(256, dtype=torch.uint8, device=dev)
 
     def weight(self, n, k):
         pool = self.pools[(n, k)]
@@ -159,13 +173,37 @@ class Decode:
         self.counters[(n, k)] = (c + 1) % pool.shape[0]
         return pool[c]
 
-    def step(self, quantize=True, x_all=None):
+    def _products(self, ms):
         g = self.g
+        for m in ms:
+            for (n, k) in DECODE_SHAPES:   # both weight matrices read this M's q8_1 slice
+                g.gguf_mul_mat(self.weight(n, k), g.Q4_K, n, k, self.xqs[m], xt=g.Q8_1, m=m, out=self.ys[(n, m)],
+                               ws=self.ws)
+
+    def _segments(self, ms):   # one call (and launch) per M for both weight matrices
+        g = self.g
+        for m in ms:
+            segs = [(self.weight(n, k), n, self.ys[(n, m)]) for (n, k) in DECODE_SHAPES]
+            g.gguf_mul_mat_segments(g.Q4_K, self.k, self.xqs[m], segs, xt=g.Q8_1, m=m, ws=self.ws)
+
+    def step(self, quantize=True, x_all=None, serial=False, segments=False):
+        g, torch = self.g, self.torch
         if quantize:
             g.gguf_quantize_q8_1(self.x_all if x_all is None else x_all, out=self.xq_all)
-        for m in DECODE_MS:
-            for (n, k) in DECODE_SHAPES:   # both weight matrices read this M's q8_1 slice
-                g.gguf_mul_mat(self.weight(n, k), g.Q4_K, n, k, self.xqs[m], xt=g.Q8_1, m=m, out=self.ys[(n, m)])
+        run = self._segments if segments else self._products
+        if serial:
+            run(DECODE_MS)
+            return
+        main = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(main)
+        self.side.wait_event(fork)
+        with torch.cuda.stream(self.side):
+            run((8, 2))
+        run((4, 1))
+        join = torch.cuda.Event()
+        join.record(self.side)
+        main.wait_event(join)
 
     def launches_per_step(self, quantize=True):
         return len(DECODE_MS) * len(DECODE_SHAPES) + (1 if quantize else 0)
@@ -223,7 +261,7 @@ def run_ours(args, rank, world, torch, dev):
     nph = min(dec.n_phase, 8)
     with torch.cuda.stream(stream):
         graphs = _capture(torch, stream, dec.step, nph)
-        mgraphs = _capture(torch, stream, lambda: dec.step(quantize=False), nph)
+        mgraphs = _capture(torch, stream, lambda: dec.step(quantize=False, serial=True), nph)
     torch.cuda.synchronize()
     per_step, weight_bytes, mmvq_bytes = dec.bytes_per_step()
 
@@ -276,7 +314,8 @@ def run_ours(args, rank, world, torch, dev):
         "dtype": "u8", "data": "synthetic",
         "config": {"workload": "decode MMVQ: Q4_K 4096x4096 and 14336x4096, bf16 activations M in {1,2,4,8}; "
                                "step = one bf16->q8_1 quantize of the 15 activation rows, then 8 MMVQ products "
-                               "(each M-row slice shared by both weight matrices)",
+                               "(each M-row slice shared by both weight matrices), on 2 CUDA streams "
+                               "(M=8,2 | M=4,1) after the quantize",
                    "l2": "weight copies rotate over >4x L2 per shape (inputs larger than L2)",
                    "weights": "random-but-safe packed Q4_K blocks", "parallelism": f"replicas x{world}"},
         "weight_bytes_per_step": weight_bytes, "bytes_per_step": per_step,
@@ -303,19 +342,22 @@ MMVQ_TRAFFIC = 21277344
 
 def run_e2e(args, g, torch, dev, dec, per_step):
     """Same workload through the public API with host buffers: each step copies
-    its activations from pinned host memory and reads its outputs back."""
+    its activations from pinned host memory and reads its outputs back.  The
+    loop is bound by host calls, so it issues the fewest: one quantize, one
+    gguf_mul_mat_segments call per M (both weight matrices), one copy each way,
+    all on one stream (a second stream's events cost more host time than the
+    overlap saves here)."""
     hx = dec.x_all.cpu().pin_memory()
-    hy = {key: torch.empty(y.shape, dtype=y.dtype).pin_memory() for key, y in dec.ys.items()}
+    hy = torch.empty(dec.y_all.shape, dtype=dec.y_all.dtype).pin_memory()
     dx = torch.empty_like(dec.x_all)
     stream = torch.cuda.Stream()
     h2d = hx.numel() * hx.element_size()
-    d2h = sum(t.numel() * t.element_size() for t in hy.values())
+    d2h = hy.numel() * hy.element_size()
 
     def step():
         dx.copy_(hx, non_blocking=True)
-        dec.step(x_all=dx)
-        for key in dec.ys:
-            hy[key].copy_(dec.ys[key], non_blocking=True)
+        dec.step(x_all=dx, serial=True, segments=True)
+        hy.copy_(dec.y_all, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):

@@ -18,6 +18,7 @@ import torch
 
 F32, F16, Q8_0, Q8_1, Q4_K, Q6_K, BF16 = 0, 1, 8, 9, 12, 14, 30
 GATE_UP_SWIGLU, DOWN_WEIGHTED_SUM = 0, 1
+Q8_1_BYTES = 36   # one q8_1 block: fp16 d, fp16 s, 32 int8 quants (a q8_1 row is k / 32 blocks)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgguf_gb300.so")
@@ -107,8 +108,19 @@ def _check(st: int):
         raise GgufError(st, load_library().gguf_last_error().decode())
 
 
+# the current stream's raw handle without building a Stream object (the
+# public call is the fallback)
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream():
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if _RAW_STREAM is not None:
+        return _RAW_STREAM(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _lib_fast():
+    return _lib if _lib is not None else load_library()
 
 
 def _ptr(t: torch.Tensor | None):
@@ -116,7 +128,7 @@ def _ptr(t: torch.Tensor | None):
         return None
     if not t.is_cuda:
         raise ValueError("gguf: tensors must live on a CUDA device")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def _workspace(nbytes: int, device) -> torch.Tensor | None:
@@ -142,10 +154,9 @@ def gguf_quantize_q8_1(x: torch.Tensor, out: torch.Tensor | None = None) -> torc
     m, k = x.shape
     if x.stride(1) != 1:
         raise ValueError("gguf_quantize_q8_1: rows must be contiguous")
-    rs = gguf_row_size(Q8_1, k)
     if out is None:
-        out = torch.empty((m, max(rs, 0)), dtype=torch.uint8, device=x.device)
-    _check(load_library().gguf_quantize_q8_1(_ptr(x), _TYPE_OF[x.dtype], m, k, x.stride(0), _ptr(out), _stream()))
+        out = torch.empty((m, max(gguf_row_size(Q8_1, k), 0)), dtype=torch.uint8, device=x.device)
+    _check(_lib_fast().gguf_quantize_q8_1(_ptr(x), _TYPE_OF[x.dtype], m, k, x.stride(0), _ptr(out), _stream()))
     return out
 
 
@@ -181,18 +192,18 @@ def gguf_mul_mat(w: torch.Tensor, wt: int, n: int, k: int, x: torch.Tensor, xt: 
         xt = _TYPE_OF[x.dtype]
     if m is None:
         m = x.shape[0]
-    ldx = x.stride(0) if xt != Q8_1 else gguf_row_size(Q8_1, k)
+    ldx = x.stride(0) if xt != Q8_1 else k // 32 * Q8_1_BYTES
     if out is None:
         if out_dtype is None:
             out_dtype = x.dtype if xt != Q8_1 else torch.float32
         out = torch.empty((m, n), dtype=out_dtype, device=x.device)
     if out.stride(1) != 1:
         raise ValueError("gguf_mul_mat: output rows must be contiguous")
-    need = gguf_mul_mat_ws_size(wt, n, k, xt, m, _TYPE_OF[out.dtype])
-    if ws is None:
-        ws = _workspace(need, x.device)
-    _check(load_library().gguf_mul_mat(_ptr(w), wt, n, k, _ptr(x), xt, m, ldx, _ptr(out), _TYPE_OF[out.dtype],
-                                       out.stride(0), _ptr(ws), 0 if ws is None else ws.numel(), _stream()))
+    yt = _TYPE_OF[out.dtype]
+    if ws is None:   # a caller's workspace is checked against the need by the library
+        ws = _workspace(gguf_mul_mat_ws_size(wt, n, k, xt, m, yt), x.device)
+    _check(_lib_fast().gguf_mul_mat(_ptr(w), wt, n, k, _ptr(x), xt, m, ldx, _ptr(out), yt, out.stride(0), _ptr(ws),
+                                    0 if ws is None else ws.numel(), _stream()))
     return out
 
 
@@ -205,18 +216,18 @@ def gguf_mul_mat_segments(wt: int, k: int, x: torch.Tensor, segments, xt: int | 
         xt = _TYPE_OF[x.dtype]
     if m is None:
         m = x.shape[0]
-    ldx = x.stride(0) if xt != Q8_1 else gguf_row_size(Q8_1, k)
+    ldx = x.stride(0) if xt != Q8_1 else k // 32 * Q8_1_BYTES
     outs = [o for (_, _, o) in segments]
     yt = _TYPE_OF[outs[0].dtype]
     for o in outs:
         if o.stride(1) != 1 or _TYPE_OF[o.dtype] != yt:
             raise ValueError("gguf_mul_mat_segments: outputs need contiguous rows and one dtype")
     arr = (Segment * len(segments))(*[Segment(_ptr(w), n, _ptr(o), o.stride(0)) for (w, n, o) in segments])
-    need = int(load_library().gguf_mul_mat_segments_ws_size(wt, arr, len(segments), k, xt, m, yt))
-    if ws is None:
-        ws = _workspace(need, x.device)
-    _check(load_library().gguf_mul_mat_segments(wt, arr, len(segments), k, _ptr(x), xt, m, ldx, yt, _ptr(ws),
-                                                0 if ws is None else ws.numel(), _stream()))
+    lib = _lib_fast()
+    if ws is None:   # a caller's workspace is checked against the need by the library
+        ws = _workspace(int(lib.gguf_mul_mat_segments_ws_size(wt, arr, len(segments), k, xt, m, yt)), x.device)
+    _check(lib.gguf_mul_mat_segments(wt, arr, len(segments), k, _ptr(x), xt, m, ldx, yt, _ptr(ws),
+                                     0 if ws is None else ws.numel(), _stream()))
     return outs
 
 

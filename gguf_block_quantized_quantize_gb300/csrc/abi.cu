@@ -6,8 +6,10 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <map>
 #include <mutex>
 #include <string>
+#include <tuple>
 
 #include "common.cuh"
 #include "internal.h"
@@ -58,6 +60,40 @@ const DeviceInfo &device_info() {
         have[dev] = true;
     }
     return infos[dev];
+}
+
+int kernel_occupancy(const void *kern, int threads, size_t smem, cudaError_t *err) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void *, int, size_t>, int> cache;
+    static std::map<std::pair<int, const void *>, size_t> smem_limit;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *err = e;
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_tuple(dev, kern, threads, smem);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    size_t &lim = smem_limit[std::make_pair(dev, kern)];
+    if (smem > lim) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) {
+            *err = e;
+            return 0;
+        }
+        lim = smem;
+    }
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    if (e != cudaSuccess) {
+        *err = e;
+        return 0;
+    }
+    if (per_sm < 1) per_sm = 1;
+    cache[key] = per_sm;
+    return per_sm;
 }
 
 // tunables

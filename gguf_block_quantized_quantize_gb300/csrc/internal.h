@@ -16,6 +16,12 @@ struct DeviceInfo {
     size_t smem_optin;
 };
 const DeviceInfo &device_info();
+// Resident CTAs per SM of kernel `kern` at `threads` per CTA and `smem` bytes
+// of dynamic shared memory on the current device (at least 1).  Queried once
+// per (device, kernel, threads, smem) and cached, so a launch costs no driver
+// query after the first; the kernel's dynamic shared-memory limit is raised
+// to the largest smem asked for.  0 with the CUDA error in *err on failure.
+int kernel_occupancy(const void *kern, int threads, size_t smem, cudaError_t *err);
 // sets the thread-local message returned by gguf_last_error() and returns st
 gguf_status report(gguf_status st, const char *msg);
 

@@ -670,10 +670,9 @@ inline cudaError_t launch_mmvq_cfg(const MmvqSegs &sg, int64_t k, int64_t rb, co
     const int nthr = (int)((P * TG + 31) / 32 * 32);
     if (nthr > MAXT) return cudaErrorInvalidValue;
     auto kern = sg.nseg > 1 ? mmvq_kernel<PT, M, TG, R, MAXT, true> : mmvq_kernel<PT, M, TG, R, MAXT, false>;
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nthr, 0);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
+    cudaError_t e = cudaSuccess;
+    const int per_sm = kernel_occupancy(reinterpret_cast<const void *>(kern), nthr, 0, &e);
+    if (per_sm == 0) return e;
     const int64_t groups = (n + R - 1) / R;
     int64_t grid = (int64_t)device_info().sm_count * per_sm;
     if (grid > groups) grid = groups;

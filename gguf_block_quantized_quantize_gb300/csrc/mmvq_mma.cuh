@@ -298,12 +298,9 @@ inline cudaError_t launch_mmvq_mma_q4k_nt(const MmvqSegs &sg, int64_t k, const u
     if (grp == 0) return cudaErrorInvalidValue;
     const MmaSmem L = mma_smem_layout(k, nw, grp, NT);
     auto kern = mmvq_mma_q4k_kernel<NT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nw * 32, (size_t)L.total);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
+    cudaError_t e = cudaSuccess;
+    const int per_sm = kernel_occupancy(reinterpret_cast<const void *>(kern), nw * 32, (size_t)L.total, &e);
+    if (per_sm == 0) return e;
     const int64_t n_tiles = (n + 15) / 16;
     int64_t grid = (int64_t)device_info().sm_count * per_sm;
     if (grid > n_tiles) grid = n_tiles;
