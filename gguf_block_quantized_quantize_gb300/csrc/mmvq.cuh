@@ -338,6 +338,8 @@ __device__ __forceinline__ void seg_store(const MmvqSegs &sg, int yt, int tok, i
 template <int WT>
 struct ThinPiece {
     static constexpr int VALUES = 32;
+    static constexpr bool STAGED = false;   // each thread loads its own piece
+    static constexpr int STAGE_CHUNKS = 1;
     struct Pos { int64_t p; };
     using W = WPiece<WT>;
     template <int M> using A = ActPiece<M>;
@@ -360,6 +362,8 @@ struct ThinPiece {
 // 16-byte header and the 32 quant bytes with three 16-byte loads.
 struct Q4KPiece {
     static constexpr int VALUES = 64;
+    static constexpr bool STAGED = false;
+    static constexpr int STAGE_CHUNKS = 1;
     struct Pos {
         int64_t off;               // byte offset of the super-block in the row
         int c;                     // chunk
@@ -453,54 +457,98 @@ struct Q4KPiece {
     }
 };
 
-// Read 16 bytes at a 2-byte-aligned address as four words (aligned loads plus
-// a funnel shift when p % 4 == 2; touches only [p - 2, p + 18)).
-__device__ __forceinline__ void ld16_a2(const uint8_t *p, uint32_t (&o)[4]) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint8_t *base = reinterpret_cast<const uint8_t *>(a & ~uintptr_t(3));
+// 16 bytes at a 2-byte-aligned shared-memory address as four words (aligned
+// words plus a funnel shift when p % 4 == 2)
+__device__ __forceinline__ void lds16_a2(const uint8_t *p, uint32_t (&o)[4]) {
+    const uint32_t *b = reinterpret_cast<const uint32_t *>(reinterpret_cast<uintptr_t>(p) & ~uintptr_t(3));
+    const int sh = (reinterpret_cast<uintptr_t>(p) & 2) ? 16 : 0;
     uint32_t w[5];
 #pragma unroll
-    for (int i = 0; i < 4; i++) w[i] = __ldg(reinterpret_cast<const uint32_t *>(base) + i);
-    if (a & 2) {
-        w[4] = __ldg(reinterpret_cast<const uint32_t *>(base) + 4);
+    for (int i = 0; i < 5; i++) w[i] = b[i];
 #pragma unroll
-        for (int i = 0; i < 4; i++) o[i] = __funnelshift_r(w[i], w[i + 1], 16);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 4; i++) o[i] = w[i];
-    }
+    for (int i = 0; i < 4; i++) o[i] = __funnelshift_r(w[i], w[i + 1], sh);
 }
 
-// Q6_K, 64-value pieces: piece p of super-block p/4 is half h = (p/2)%2 and
-// l0 = 16*(p%2): the runs [128h + 32g + l0, +16) for g = 0..3, i.e. ql bytes
-// [64h + l0, +16) (g = 0 low nibbles, g = 2 high), [64h + 32 + l0, +16)
-// (g = 1, g = 3) and qh bytes [32h + l0, +16) (two bits per g).  Run g is the
-// 16-value sub-block 8h + 2g + l0/16 (scale sc[8h + 2g + l0/16]) and half
-// l0/16 of q8_1 block 4h + g.  Quants are used as unsigned 0..63 and the
-// offset is applied through the activation sums: sum (u - 32) a = sum u a - 32 sum a.
+// Q6_K blocks (210 bytes) are only 2-byte aligned, so per-thread loads of a
+// piece's fields cost many narrow, scattered requests.  Instead the warp's
+// span of 8 consecutive blocks of a row (1680 contiguous bytes) is read with
+// 16-byte loads of its 16-byte-aligned cover (lane l takes chunks l + 32 i),
+// plus 2-byte loads of a tail that does not fill a chunk; `prepare` writes the
+// span to the warp's shared-memory buffer and every lane reads its piece's
+// fields from there.  Nothing outside the span's row is read except bytes of
+// the same aligned chunk before the span start, which belong to the view.
 struct Q6KPiece {
     static constexpr int VALUES = 64;
-    struct Pos { int64_t off; int h, l0; };
-    struct W { uint32_t ql0[4], ql1[4], qh[4]; uint32_t sc; uint32_t d; };
+    static constexpr bool STAGED = true;
+    static constexpr int STAGE_CHUNKS = 108;   // 16-byte chunks of a warp's buffer (1680 + 15 bytes)
+    struct Pos {
+        int64_t off;     // byte offset of the piece's block in the row
+        int h, l0;       // half of the block, 16-value offset
+        int lane;        // lane in the warp
+        int span_off;    // byte offset of the warp's span in the row
+        int span_len;    // bytes of the span (8 blocks, fewer at the end of the row)
+        int fld;         // byte offset of the piece's block in the span
+    };
+    struct Wf { uint32_t ql0[4], ql1[4], qh[4]; uint32_t sc; uint32_t d; };   // one piece's fields
+    struct W { uint4 c[4]; uint32_t t; uint32_t head; };                       // the lane's share of the span
     template <int M>
     struct A {
         int q[M][16];    // run g quants: words 4g .. 4g+3
         float f[M][4];   // d_a of run g
         int sum[M][4];   // 32 * sum of the run's 16 quants
     };
-    static __device__ __forceinline__ Pos pos(int64_t p) {
-        return Pos{(p >> 2) * Q6_K_BYTES, (int)((p >> 1) & 1), 16 * (int)(p & 1)};
+    static __device__ __forceinline__ Pos pos(int64_t p, int64_t k) {
+        const int64_t left = k / 256 - 8 * (p >> 5);   // blocks of the row from the span start
+        Pos q;
+        q.off = (p >> 2) * Q6_K_BYTES;
+        q.h = (int)((p >> 1) & 1);
+        q.l0 = 16 * (int)(p & 1);
+        q.lane = (int)(p & 31);
+        q.span_off = (int)((p >> 5) * 8 * Q6_K_BYTES);
+        q.span_len = (int)((left < 8 ? (left > 0 ? left : 0) : 8) * Q6_K_BYTES);
+        q.fld = (q.lane >> 2) * Q6_K_BYTES;
+        return q;
     }
     static __device__ __forceinline__ void load(W &w, const uint8_t *row, const Pos &q) {
-        const uint8_t *blk = row + q.off;
-        ld16_a2(blk + 64 * q.h + q.l0, w.ql0);
-        ld16_a2(blk + 64 * q.h + 32 + q.l0, w.ql1);
-        ld16_a2(blk + 128 + 32 * q.h + q.l0, w.qh);
-        uint32_t s0, s1;
-        ld8_a2(blk + 192 + 8 * q.h, s0, s1);  // sc[8h .. 8h+7]
+        const uint8_t *a = row + q.span_off;
+        const uint32_t head = (uint32_t)(reinterpret_cast<uintptr_t>(a) & 15);
+        const uint4 *c0 = reinterpret_cast<const uint4 *>(a - head);
+        const int full = (int)(head + q.span_len) >> 4;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int c = q.lane + 32 * i;
+            w.c[i] = c < full ? __ldg(c0 + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        const int tail = (int)((head + q.span_len) & 15) >> 1;
+        w.t = q.lane < tail ? ld_u16(reinterpret_cast<const uint8_t *>(c0 + full) + 2 * q.lane) : 0u;
+        w.head = head;
+    }
+    // the span into the warp's buffer, then this lane's fields out of it
+    static __device__ __forceinline__ void prepare(const W &w, const Pos &q, uint4 *buf, Wf &f) {
+        const int full = (int)(w.head + q.span_len) >> 4;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int c = q.lane + 32 * i;
+            if (c < full) buf[c] = w.c[i];
+        }
+        const int tail = (int)((w.head + q.span_len) & 15) >> 1;
+        if (q.lane < tail) reinterpret_cast<uint16_t *>(buf + full)[q.lane] = (uint16_t)w.t;
+        __syncwarp();
+        const uint8_t *blk = reinterpret_cast<const uint8_t *>(buf) + w.head + q.fld;
+        lds16_a2(blk + 64 * q.h + q.l0, f.ql0);
+        lds16_a2(blk + 64 * q.h + 32 + q.l0, f.ql1);
+        lds16_a2(blk + 128 + 32 * q.h + q.l0, f.qh);
+        uint32_t s[3];
+        const uint8_t *sp = blk + 192 + 8 * q.h;   // sc[8h .. 8h+7]
+        const uint32_t *sb = reinterpret_cast<const uint32_t *>(reinterpret_cast<uintptr_t>(sp) & ~uintptr_t(3));
+#pragma unroll
+        for (int i = 0; i < 3; i++) s[i] = sb[i];
+        const int sh = (reinterpret_cast<uintptr_t>(sp) & 2) ? 16 : 0;
+        const uint32_t s0 = __funnelshift_r(s[0], s[1], sh), s1 = __funnelshift_r(s[1], s[2], sh);
         // scales of runs g = 0..3: sc[8h + l0/16 + 2g]
-        w.sc = q.l0 ? __byte_perm(s0, s1, 0x7531) : __byte_perm(s0, s1, 0x6420);
-        w.d = ld_u16(blk + 208);
+        f.sc = q.l0 ? __byte_perm(s0, s1, 0x7531) : __byte_perm(s0, s1, 0x6420);
+        f.d = *reinterpret_cast<const uint16_t *>(blk + 208);
+        __syncwarp();   // every lane holds its fields before the buffer is rewritten
     }
     template <int M>
     static __device__ __forceinline__ void load_act(A<M> &a, const uint8_t *xq, int64_t xrb, int m_act,
@@ -525,7 +573,7 @@ struct Q6KPiece {
         }
     }
     template <int M>
-    static __device__ __forceinline__ void dot(const W &w, const A<M> &a, const Pos &, float (&acc)[M]) {
+    static __device__ __forceinline__ void dot(const Wf &w, const A<M> &a, const Pos &, float (&acc)[M]) {
         const float d = h2f((uint16_t)w.d);
         float dsc[4];
 #pragma unroll
@@ -569,19 +617,24 @@ __global__ void __launch_bounds__(MAXT) mmvq_kernel(const MmvqSegs sg, int64_t k
     const int64_t ldy0 = sg.ldy[0];
     constexpr int V = R * M;
     static_assert(V * TG <= 32 && (V & (V - 1)) == 0, "R*M must be a power of two <= 32/TG");
+    static_assert(!PT::STAGED || TG == 1, "staged pieces: one thread per piece, so a warp is 32 pieces");
     __shared__ float red[2][MAXT / 32][TG * V];
+    __shared__ uint4 stage[PT::STAGED ? MAXT / 32 : 1][PT::STAGE_CHUNKS];   // warp buffers of staged pieces
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     const int tg = tid % TG;
     const int64_t piece = tid / TG;
     const int64_t P = k / PT::VALUES;
     const bool valid = piece < P;
-    const typename PT::Pos pos = PT::pos(valid ? piece : 0);
+    const typename PT::Pos pos = [&] {
+        if constexpr (PT::STAGED) return PT::pos(piece, k);   // lanes past the row still copy their share
+        else return PT::pos(valid ? piece : 0);
+    }();
     const int64_t stride = (int64_t)gridDim.x * R;
     int64_t n0 = (int64_t)blockIdx.x * R;
 
     typename PT::W wa[R], wb[R];
     auto load_rows = [&](typename PT::W (&dst)[R], int64_t base) {
-        if (!valid) return;
+        if (!valid && !PT::STAGED) return;
         if constexpr (!MULTI) {
 #pragma unroll
             for (int r = 0; r < R; r++) PT::load(dst[r], w0 + (base + r < n ? base + r : n - 1) * rb, pos);
@@ -619,7 +672,21 @@ __global__ void __launch_bounds__(MAXT) mmvq_kernel(const MmvqSegs sg, int64_t k
         float part[V];
 #pragma unroll
         for (int i = 0; i < V; i++) part[i] = 0.0f;
-        if (valid) {
+        if constexpr (PT::STAGED) {
+#pragma unroll
+            for (int r = 0; r < R; r++) {
+                typename PT::Wf f;
+                PT::prepare(cur[r], pos, stage[warp], f);   // every lane of the warp takes part
+                if (valid) {
+                    float acc[M];
+#pragma unroll
+                    for (int mm = 0; mm < M; mm++) acc[mm] = 0.0f;
+                    PT::template dot<M>(f, act, pos, acc);
+#pragma unroll
+                    for (int mm = 0; mm < M; mm++) part[r * M + mm] = acc[mm];
+                }
+            }
+        } else if (valid) {
 #pragma unroll
             for (int r = 0; r < R; r++) {
                 float acc[M];
@@ -720,7 +787,8 @@ inline cudaError_t launch_mmvq_pt(const MmvqSegs &sg, int64_t k, const uint8_t *
             if (t.r4_m24) return launch_mmvq_cfg<PT, 4, 1, 4, 256>(sg, k, rb, xq, m, yt, s);
             return launch_mmvq_cfg<PT, 4, 1, 2, 256>(sg, k, rb, xq, m, yt, s);
         }
-        if (t.tg2_m8 && P <= 128) return launch_mmvq_cfg<PT, 4, 2, 2, 256>(sg, k, rb, xq, m, yt, s);
+        if constexpr (!PT::STAGED)   // staged pieces take one thread per piece
+            if (t.tg2_m8 && P <= 128) return launch_mmvq_cfg<PT, 4, 2, 2, 256>(sg, k, rb, xq, m, yt, s);
         return launch_mmvq_cfg<PT, 8, 1, 1, 256>(sg, k, rb, xq, m, yt, s);
     }
     if constexpr (PT::VALUES == 32) {
