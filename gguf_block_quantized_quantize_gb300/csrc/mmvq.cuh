@@ -758,7 +758,7 @@ inline cudaError_t launch_mmvq_cfg(const MmvqSegs &sg, int64_t k, int64_t rb, co
 
 // Configuration by token count (measured on GB300, Q4_K / Q6_K rows of 3072 ..
 // 8192 values): up to 4 tokens per thread with the next R rows prefetched
-// (R = 4 for 2..4 tokens of Q4_K rows);
+// (R = 4 for 2..4 tokens of Q4_K rows and 2 tokens of Q6_K rows);
 // 5..8 tokens either as two threads per piece with 4 tokens each (Q4_K) or 8
 // tokens per thread (Q6_K, whose wider loads leave fewer registers).  Rows of
 // more than 256 pieces (32-value pieces of K > 8192) use 512-thread CTAs.
@@ -766,7 +766,8 @@ struct MmvqTune {
     bool r4_m1;        // M = 1: R = 4 instead of 2
     bool r1_m1;        // M = 1: R = 1 (overrides r4_m1)
     bool tg2_m8;       // 5..8 tokens: two threads per piece
-    bool r4_m24;       // 2..4 tokens: R = 4 instead of 2
+    bool r4_m2;        // 2 tokens: R = 4 instead of 2
+    bool r4_m4;        // 3..4 tokens: R = 4 instead of 2
 };
 
 template <class PT>
@@ -780,11 +781,11 @@ inline cudaError_t launch_mmvq_pt(const MmvqSegs &sg, int64_t k, const uint8_t *
             return launch_mmvq_cfg<PT, 1, 1, 2, 256>(sg, k, rb, xq, m, yt, s);
         }
         if (m <= 2) {
-            if (t.r4_m24) return launch_mmvq_cfg<PT, 2, 1, 4, 256>(sg, k, rb, xq, m, yt, s);
+            if (t.r4_m2) return launch_mmvq_cfg<PT, 2, 1, 4, 256>(sg, k, rb, xq, m, yt, s);
             return launch_mmvq_cfg<PT, 2, 1, 2, 256>(sg, k, rb, xq, m, yt, s);
         }
         if (m <= 4) {
-            if (t.r4_m24) return launch_mmvq_cfg<PT, 4, 1, 4, 256>(sg, k, rb, xq, m, yt, s);
+            if (t.r4_m4) return launch_mmvq_cfg<PT, 4, 1, 4, 256>(sg, k, rb, xq, m, yt, s);
             return launch_mmvq_cfg<PT, 4, 1, 2, 256>(sg, k, rb, xq, m, yt, s);
         }
         if constexpr (!PT::STAGED)   // staged pieces take one thread per piece

@@ -14,7 +14,7 @@ cudaError_t launch_mmvq_q4_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, i
     if (m >= option_mmvq_tc_min_m() && n >= 2048 && option_mmvq_tc() && mma_q4k_fits(k, m))
         return launch_mmvq_mma_q4k(sg, k, xq, m, yt, s);
     return launch_mmvq_pt<Q4KPiece>(sg, k, xq, m, yt, s, k / 256 * Q4_K_BYTES,
-                                    MmvqTune{n >= 8192, false, true, true});
+                                    MmvqTune{n >= 8192, false, true, true, true});
 }
 
 bool mmvq_tc_wide(int wt, int64_t k, int64_t m) {
