@@ -37,216 +37,31 @@
 
 namespace gg {
 
-// ---------------------------------------------------------------- 32-value pieces
-// Piece p of a row (32 values):
-//   Q8_0: block p.
-//   Q4_K: super-block p/8, 16 quant bytes at chunk c = (p%8)/2, half h = p%2:
-//         values [64c+16h, +16) (low nibbles, sub-block 2c) and
-//         [64c+32+16h, +16) (high nibbles, sub-block 2c+1).
-//   Q6_K: super-block p/8, half h = (p%8)/4, l0 = 8*(p%4): the runs
-//         [128h + 32g + l0, +8) for g = 0..3.
+// ---------------------------------------------------------------- Q8_0 pieces
+// A Q8_0 piece is one 32-value block; its activations are the matching q8_1
+// block: 8 quant words and d_a.
 template <int M>
 struct ActPiece {
     int q[M][8];      // activation quants of the piece, 4 per word, in piece order
-    float f[M][4];    // Q8_0: d_a | Q4_K: d_a0, d_a1, s_a0, s_a1 | Q6_K: d_a of runs 0..3
-    int sum[M][4];    // Q6_K: sum of the 8 activation quants of each run
+    float f[M];       // d_a
 };
 
-// q8_1 block fields
-__device__ __forceinline__ void q81_load(const uint8_t *blk, float &d, float &s) {
-    const uint32_t ds = ld_u32(blk);
-    d = h2f(ds & 0xffff);
-    s = h2f(ds >> 16);
-}
-
-__device__ __forceinline__ int bsum4(int w) {
-    return (int)(int8_t)(w) + (int)(int8_t)(w >> 8) + (int)(int8_t)(w >> 16) + (int)(int8_t)(w >> 24);
-}
-
-template <int WT, int M>
-__device__ __forceinline__ void load_act(ActPiece<M> &a, const uint8_t *xq, int64_t xrb, int m_act, int64_t p,
-                                         bool valid) {
+template <int M>
+__device__ __forceinline__ void load_act_q8_0(ActPiece<M> &a, const uint8_t *xq, int64_t xrb, int m_act, int64_t p,
+                                              bool valid) {
 #pragma unroll
     for (int mm = 0; mm < M; mm++) {
 #pragma unroll
         for (int i = 0; i < 8; i++) a.q[mm][i] = 0;
-#pragma unroll
-        for (int i = 0; i < 4; i++) { a.f[mm][i] = 0.0f; a.sum[mm][i] = 0; }
+        a.f[mm] = 0.0f;
         if (!valid || mm >= m_act) continue;
-        const uint8_t *row = xq + mm * xrb;
-        if (WT == GGUF_Q8_0) {
-            const uint8_t *blk = row + p * Q8_1_BYTES;
-            float d, s;
-            q81_load(blk, d, s);
-            a.f[mm][0] = d;
+        const uint8_t *blk = xq + mm * xrb + p * Q8_1_BYTES;
+        a.f[mm] = h2f(ld_u16(blk));
 #pragma unroll
-            for (int i = 0; i < 8; i++) a.q[mm][i] = (int)ld_u32(blk + 4 + 4 * i);
-        } else if (WT == GGUF_Q4_K) {
-            const int64_t sb = p >> 3;
-            const int pp = (int)(p & 7), c = pp >> 1, h = pp & 1;
-            const uint8_t *b0 = row + (sb * 8 + 2 * c) * Q8_1_BYTES;
-            const uint8_t *b1 = b0 + Q8_1_BYTES;
-            q81_load(b0, a.f[mm][0], a.f[mm][2]);
-            q81_load(b1, a.f[mm][1], a.f[mm][3]);
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                a.q[mm][i] = (int)ld_u32(b0 + 4 + 16 * h + 4 * i);
-                a.q[mm][4 + i] = (int)ld_u32(b1 + 4 + 16 * h + 4 * i);
-            }
-        } else {  // Q6_K
-            const int64_t sb = p >> 3;
-            const int pp = (int)(p & 7), h = pp >> 2, l0 = 8 * (pp & 3);
-#pragma unroll
-            for (int g = 0; g < 4; g++) {
-                const uint8_t *b = row + (sb * 8 + 4 * h + g) * Q8_1_BYTES;
-                float d, s;
-                q81_load(b, d, s);
-                a.f[mm][g] = d;
-                a.q[mm][2 * g] = (int)ld_u32(b + 4 + l0);
-                a.q[mm][2 * g + 1] = (int)ld_u32(b + 8 + l0);
-                a.sum[mm][g] = bsum4(a.q[mm][2 * g]) + bsum4(a.q[mm][2 * g + 1]);
-            }
-        }
+        for (int i = 0; i < 8; i++) a.q[mm][i] = (int)ld_u32(blk + 4 + 4 * i);
     }
 }
 
-// raw weight bytes of one piece, loaded before any arithmetic so that the
-// loads of several rows are in flight together
-template <int WT>
-struct WPiece {
-    uint32_t a[8];
-    uint32_t b[4];
-};
-
-template <int WT>
-__device__ __forceinline__ void load_w(WPiece<WT> &wp, const uint8_t *row, int64_t p) {
-    if (WT == GGUF_Q8_0) {
-        // d at +0 (2-aligned), quants at +2; blocks are 34 bytes, so 2-aligned
-        const uint8_t *blk = row + p * Q8_0_BYTES;
-        const uintptr_t qa = reinterpret_cast<uintptr_t>(blk + 2);
-        if (qa & 2) {
-            // quants start 2 bytes into an aligned word: words cover [blk, blk+32),
-            // the last two quant bytes come from a 16-bit load (no read past the block)
-            const uint8_t *base = blk;
-#pragma unroll
-            for (int i = 0; i < 8; i++) wp.a[i] = ld_u32(base + 4 * i);
-            wp.b[0] = ld_u16(blk + 32);
-            wp.b[1] = 1;  // misaligned marker
-        } else {
-            wp.b[0] = ld_u16(blk);  // d
-#pragma unroll
-            for (int i = 0; i < 8; i++) wp.a[i] = ld_u32(blk + 2 + 4 * i);
-            wp.b[1] = 0;
-        }
-    } else if (WT == GGUF_Q4_K) {
-        const int64_t sb = p >> 3;
-        const int pp = (int)(p & 7), c = pp >> 1, h = pp & 1;
-        const uint8_t *blk = row + sb * Q4_K_BYTES;
-        const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
-        const uint4 qv = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c + 16 * h);
-        wp.a[0] = qv.x; wp.a[1] = qv.y; wp.a[2] = qv.z; wp.a[3] = qv.w;
-        wp.b[0] = hdr.x; wp.b[1] = hdr.y; wp.b[2] = hdr.z; wp.b[3] = hdr.w;
-    } else {  // Q6_K
-        const int64_t sb = p >> 3;
-        const int pp = (int)(p & 7), h = pp >> 2, l0 = 8 * (pp & 3);
-        const uint8_t *blk = row + sb * Q6_K_BYTES;
-        ld8_a2(blk + 64 * h + l0, wp.a[0], wp.a[1]);
-        ld8_a2(blk + 64 * h + 32 + l0, wp.a[2], wp.a[3]);
-        ld8_a2(blk + 128 + 32 * h + l0, wp.a[4], wp.a[5]);
-        ld8_a2(blk + 192 + 8 * h, wp.b[0], wp.b[1]);
-        wp.b[2] = ld_u16(blk + 208);
-        wp.b[3] = (uint32_t)l0;
-    }
-}
-
-template <int WT, int M>
-__device__ __forceinline__ void dot_piece(const WPiece<WT> &wp, const ActPiece<M> &a, int64_t p, float acc[M]) {
-    if (WT == GGUF_Q8_0) {
-        uint32_t q[8];
-        float d;
-        if (wp.b[1]) {
-            d = h2f(wp.a[0] & 0xffff);
-#pragma unroll
-            for (int i = 0; i < 7; i++) q[i] = __funnelshift_r(wp.a[i], wp.a[i + 1], 16);
-            q[7] = __funnelshift_r(wp.a[7], wp.b[0], 16);
-        } else {
-            d = h2f(wp.b[0]);
-#pragma unroll
-            for (int i = 0; i < 8; i++) q[i] = wp.a[i];
-        }
-#pragma unroll
-        for (int mm = 0; mm < M; mm++) {
-            int S = 0;
-#pragma unroll
-            for (int i = 0; i < 8; i++) S = dp4a_ss((int)q[i], a.q[mm][i], S);
-            acc[mm] = fmaf(d * a.f[mm][0], (float)S, acc[mm]);
-        }
-    } else if (WT == GGUF_Q4_K) {
-        const int pp = (int)(p & 7), c = pp >> 1, h = pp & 1;
-        const uint32_t sc[3] = {wp.b[1], wp.b[2], wp.b[3]};
-        const float d = h2f(wp.b[0] & 0xffff), dmin = h2f(wp.b[0] >> 16);
-        int s0, m0, s1, m1;
-        q4k_scale_min(sc, 2 * c, s0, m0);
-        q4k_scale_min(sc, 2 * c + 1, s1, m1);
-        const float ds0 = d * (float)s0, ds1 = d * (float)s1;
-        // the min term of a 32-value sub-block is counted once, by its h == 0 piece
-        const float dm = h == 0 ? dmin : 0.0f;
-        const float fm0 = (float)m0, fm1 = (float)m1;
-        uint32_t lo[4], hi[4];
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            lo[i] = wp.a[i] & 0x0F0F0F0Fu;
-            hi[i] = (wp.a[i] >> 4) & 0x0F0F0F0Fu;
-        }
-#pragma unroll
-        for (int mm = 0; mm < M; mm++) {
-            int S0 = 0, S1 = 0;
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                S0 = dp4a_us(lo[i], a.q[mm][i], S0);
-                S1 = dp4a_us(hi[i], a.q[mm][4 + i], S1);
-            }
-            float v = ds0 * (a.f[mm][0] * (float)S0);
-            v = fmaf(ds1, a.f[mm][1] * (float)S1, v);
-            v = fmaf(-dm, fmaf(fm0, a.f[mm][2], fm1 * a.f[mm][3]), v);
-            acc[mm] += v;
-        }
-    } else {  // Q6_K
-        const int l0 = (int)wp.b[3];
-        const float d = h2f(wp.b[2] & 0xffff);
-        float dsc[4];
-#pragma unroll
-        for (int g = 0; g < 4; g++) {
-            const int si = (l0 >> 4) + 2 * g;
-            const int sc = (int)(int8_t)((wp.b[si >> 2] >> (8 * (si & 3))) & 0xff);
-            dsc[g] = d * (float)sc;
-        }
-        uint32_t q[4][2];
-#pragma unroll
-        for (int i = 0; i < 2; i++) {
-            const uint32_t A = wp.a[i], B = wp.a[2 + i], H = wp.a[4 + i];
-            q[0][i] = (A & 0x0F0F0F0Fu) | ((H << 4) & 0x30303030u);
-            q[1][i] = (B & 0x0F0F0F0Fu) | ((H << 2) & 0x30303030u);
-            q[2][i] = ((A >> 4) & 0x0F0F0F0Fu) | (H & 0x30303030u);
-            q[3][i] = ((B >> 4) & 0x0F0F0F0Fu) | ((H >> 2) & 0x30303030u);
-        }
-#pragma unroll
-        for (int mm = 0; mm < M; mm++) {
-            float v = 0.0f;
-#pragma unroll
-            for (int g = 0; g < 4; g++) {
-                int S = dp4a_us(q[g][0], a.q[mm][2 * g], 0);
-                S = dp4a_us(q[g][1], a.q[mm][2 * g + 1], S);
-                S -= 32 * a.sum[mm][g];
-                v = fmaf(dsc[g], a.f[mm][g] * (float)S, v);
-            }
-            acc[mm] += v;
-        }
-    }
-}
-
-// Butterfly reduction of V values across the 32 lanes of a warp; afterwards
-// lane l holds the warp total of value index l >> (5 - log2 V).
 template <int V>
 __device__ __forceinline__ float butterfly(float (&v)[V], int lane) {
     constexpr int LOG = V == 1 ? 0 : V == 2 ? 1 : V == 4 ? 2 : V == 8 ? 3 : V == 16 ? 4 : 5;
@@ -333,26 +148,96 @@ __device__ __forceinline__ void seg_store(const MmvqSegs &sg, int yt, int tok, i
 // any arithmetic so several rows are in flight), the activation values of the
 // piece for M tokens (A, loaded once), and the block-dot arithmetic.
 
-// 32-value pieces (Q8_0, and the fallback for rows that do not split into
-// 64-value pieces) reuse the building blocks above.
-template <int WT>
-struct ThinPiece {
+// 16 bytes at a 2-byte-aligned shared-memory address as four words (aligned
+// words plus a funnel shift when p % 4 == 2)
+__device__ __forceinline__ void lds16_a2(const uint8_t *p, uint32_t (&o)[4]) {
+    const uint32_t *b = reinterpret_cast<const uint32_t *>(reinterpret_cast<uintptr_t>(p) & ~uintptr_t(3));
+    const int sh = (reinterpret_cast<uintptr_t>(p) & 2) ? 16 : 0;
+    uint32_t w[5];
+#pragma unroll
+    for (int i = 0; i < 5; i++) w[i] = b[i];
+#pragma unroll
+    for (int i = 0; i < 4; i++) o[i] = __funnelshift_r(w[i], w[i + 1], sh);
+}
+
+// Q8_0 with staged loads: a warp's 32 pieces are 32 consecutive blocks, one
+// contiguous span of up to 1088 bytes.  As for Q6_K (below), the span is read
+// with 16-byte loads of its 16-byte-aligned cover plus 2-byte loads of a tail,
+// written to the warp's shared-memory buffer, and each lane takes its block's
+// d and quants from there.
+struct Q80Piece {
     static constexpr int VALUES = 32;
-    static constexpr bool STAGED = false;   // each thread loads its own piece
-    static constexpr int STAGE_CHUNKS = 1;
-    struct Pos { int64_t p; };
-    using W = WPiece<WT>;
+    static constexpr bool STAGED = true;
+    static constexpr int STAGE_CHUNKS = 70;   // 16-byte chunks of a warp's buffer (1088 + 15 bytes)
+    struct Pos {
+        int64_t p;       // piece = block index in the row
+        int lane;
+        int span_off;    // byte offset of the warp's span in the row
+        int span_len;    // bytes of the span (32 blocks, fewer at the end of the row)
+    };
+    struct W { uint4 c[3]; uint32_t t; uint32_t head; };
+    struct Wf { uint32_t q[8]; uint32_t d; };
     template <int M> using A = ActPiece<M>;
-    static __device__ __forceinline__ Pos pos(int64_t p) { return Pos{p}; }
-    static __device__ __forceinline__ void load(W &w, const uint8_t *row, const Pos &q) { load_w<WT>(w, row, q.p); }
+    static __device__ __forceinline__ Pos pos(int64_t p, int64_t k) {
+        const int64_t left = k / 32 - 32 * (p >> 5);
+        Pos q;
+        q.p = p;
+        q.lane = (int)(p & 31);
+        q.span_off = (int)((p >> 5) * 32 * Q8_0_BYTES);
+        q.span_len = (int)((left < 32 ? (left > 0 ? left : 0) : 32) * Q8_0_BYTES);
+        return q;
+    }
+    static __device__ __forceinline__ void load(W &w, const uint8_t *row, const Pos &q) {
+        const uint8_t *a = row + q.span_off;
+        const uint32_t head = (uint32_t)(reinterpret_cast<uintptr_t>(a) & 15);
+        const uint4 *c0 = reinterpret_cast<const uint4 *>(a - head);
+        const int full = (int)(head + q.span_len) >> 4;
+#pragma unroll
+        for (int i = 0; i < 3; i++) {
+            const int c = q.lane + 32 * i;
+            w.c[i] = c < full ? __ldg(c0 + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        const int tail = (int)((head + q.span_len) & 15) >> 1;
+        w.t = q.lane < tail ? ld_u16(reinterpret_cast<const uint8_t *>(c0 + full) + 2 * q.lane) : 0u;
+        w.head = head;
+    }
+    static __device__ __forceinline__ void prepare(const W &w, const Pos &q, uint4 *buf, Wf &f) {
+        const int full = (int)(w.head + q.span_len) >> 4;
+#pragma unroll
+        for (int i = 0; i < 3; i++) {
+            const int c = q.lane + 32 * i;
+            if (c < full) buf[c] = w.c[i];
+        }
+        const int tail = (int)((w.head + q.span_len) & 15) >> 1;
+        if (q.lane < tail) reinterpret_cast<uint16_t *>(buf + full)[q.lane] = (uint16_t)w.t;
+        __syncwarp();
+        const uint8_t *blk = reinterpret_cast<const uint8_t *>(buf) + w.head + q.lane * Q8_0_BYTES;
+        f.d = *reinterpret_cast<const uint16_t *>(blk);
+        uint32_t lo[4], hi[4];
+        lds16_a2(blk + 2, lo);
+        lds16_a2(blk + 18, hi);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            f.q[i] = lo[i];
+            f.q[4 + i] = hi[i];
+        }
+        __syncwarp();   // every lane holds its block before the buffer is rewritten
+    }
     template <int M>
     static __device__ __forceinline__ void load_act(A<M> &a, const uint8_t *xq, int64_t xrb, int m_act,
                                                     const Pos &q, bool valid) {
-        gg::load_act<WT, M>(a, xq, xrb, m_act, valid ? q.p : 0, valid);
+        load_act_q8_0<M>(a, xq, xrb, m_act, valid ? q.p : 0, valid);
     }
     template <int M>
-    static __device__ __forceinline__ void dot(const W &w, const A<M> &a, const Pos &q, float (&acc)[M]) {
-        dot_piece<WT, M>(w, a, q.p, acc);
+    static __device__ __forceinline__ void dot(const Wf &w, const A<M> &a, const Pos &, float (&acc)[M]) {
+        const float d = h2f((uint16_t)w.d);
+#pragma unroll
+        for (int mm = 0; mm < M; mm++) {
+            int S = 0;
+#pragma unroll
+            for (int i = 0; i < 8; i++) S = dp4a_ss((int)w.q[i], a.q[mm][i], S);
+            acc[mm] = fmaf(d * a.f[mm], (float)S, acc[mm]);
+        }
     }
 };
 
@@ -456,18 +341,6 @@ struct Q4KPiece {
         }
     }
 };
-
-// 16 bytes at a 2-byte-aligned shared-memory address as four words (aligned
-// words plus a funnel shift when p % 4 == 2)
-__device__ __forceinline__ void lds16_a2(const uint8_t *p, uint32_t (&o)[4]) {
-    const uint32_t *b = reinterpret_cast<const uint32_t *>(reinterpret_cast<uintptr_t>(p) & ~uintptr_t(3));
-    const int sh = (reinterpret_cast<uintptr_t>(p) & 2) ? 16 : 0;
-    uint32_t w[5];
-#pragma unroll
-    for (int i = 0; i < 5; i++) w[i] = b[i];
-#pragma unroll
-    for (int i = 0; i < 4; i++) o[i] = __funnelshift_r(w[i], w[i + 1], sh);
-}
 
 // Q6_K blocks (210 bytes) are only 2-byte aligned, so per-thread loads of a
 // piece's fields cost many narrow, scattered requests.  Instead the warp's

@@ -4,8 +4,7 @@
 namespace gg {
 
 cudaError_t launch_mmvq_q8_0(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s) {
-    const int64_t n = sg.rows();
-    return launch_mmvq_pt<ThinPiece<GGUF_Q8_0>>(sg, k, xq, m, yt, s, k / 32 * Q8_0_BYTES, MmvqTune{false, false, true});
+    return launch_mmvq_pt<Q80Piece>(sg, k, xq, m, yt, s, k / 32 * Q8_0_BYTES, MmvqTune{false, false, true});
 }
 
 }  // namespace gg
