@@ -173,18 +173,23 @@ struct Q80Piece {
         int64_t p;       // piece = block index in the row
         int lane;
         int span_off;    // byte offset of the warp's span in the row
-        int span_len;    // bytes of the span (32 blocks, fewer at the end of the row)
+        int span_len;    // bytes of the span (32 / TG blocks, fewer at the end of the row)
+        int fld;         // byte offset of the piece's block in the span
     };
     struct W { uint4 c[3]; uint32_t t; uint32_t head; };
     struct Wf { uint32_t q[8]; uint32_t d; };
     template <int M> using A = ActPiece<M>;
-    static __device__ __forceinline__ Pos pos(int64_t p, int64_t k) {
-        const int64_t left = k / 32 - 32 * (p >> 5);
+    // piece p, thread tg of its TG: the warp holds pieces [PW w, PW w + PW), PW = 32 / TG
+    template <int TG>
+    static __device__ __forceinline__ Pos pos(int64_t p, int tg, int64_t k) {
+        constexpr int PW = 32 / TG;
+        const int64_t w = p / PW, left = k / 32 - PW * w;
         Pos q;
         q.p = p;
-        q.lane = (int)(p & 31);
-        q.span_off = (int)((p >> 5) * 32 * Q8_0_BYTES);
-        q.span_len = (int)((left < 32 ? (left > 0 ? left : 0) : 32) * Q8_0_BYTES);
+        q.lane = (int)((p * TG + tg) & 31);
+        q.span_off = (int)(w * PW * Q8_0_BYTES);
+        q.span_len = (int)((left < PW ? (left > 0 ? left : 0) : PW) * Q8_0_BYTES);
+        q.fld = (int)(p % PW) * Q8_0_BYTES;
         return q;
     }
     static __device__ __forceinline__ void load(W &w, const uint8_t *row, const Pos &q) {
@@ -211,7 +216,7 @@ struct Q80Piece {
         const int tail = (int)((w.head + q.span_len) & 15) >> 1;
         if (q.lane < tail) reinterpret_cast<uint16_t *>(buf + full)[q.lane] = (uint16_t)w.t;
         __syncwarp();
-        const uint8_t *blk = reinterpret_cast<const uint8_t *>(buf) + w.head + q.lane * Q8_0_BYTES;
+        const uint8_t *blk = reinterpret_cast<const uint8_t *>(buf) + w.head + q.fld;
         f.d = *reinterpret_cast<const uint16_t *>(blk);
         uint32_t lo[4], hi[4];
         lds16_a2(blk + 2, lo);
@@ -359,7 +364,7 @@ struct Q6KPiece {
         int h, l0;       // half of the block, 16-value offset
         int lane;        // lane in the warp
         int span_off;    // byte offset of the warp's span in the row
-        int span_len;    // bytes of the span (8 blocks, fewer at the end of the row)
+        int span_len;    // bytes of the span (8 / TG blocks, fewer at the end of the row)
         int fld;         // byte offset of the piece's block in the span
     };
     struct Wf { uint32_t ql0[4], ql1[4], qh[4]; uint32_t sc; uint32_t d; };   // one piece's fields
@@ -370,16 +375,20 @@ struct Q6KPiece {
         float f[M][4];   // d_a of run g
         int sum[M][4];   // 32 * sum of the run's 16 quants
     };
-    static __device__ __forceinline__ Pos pos(int64_t p, int64_t k) {
-        const int64_t left = k / 256 - 8 * (p >> 5);   // blocks of the row from the span start
+    // piece p, thread tg of its TG: the warp holds pieces [PW w, PW w + PW), PW = 32 / TG,
+    // i.e. blocks [PW w / 4, +PW / 4)
+    template <int TG>
+    static __device__ __forceinline__ Pos pos(int64_t p, int tg, int64_t k) {
+        constexpr int PW = 32 / TG, BW = PW / 4;
+        const int64_t w = p / PW, left = k / 256 - BW * w;   // blocks of the row from the span start
         Pos q;
         q.off = (p >> 2) * Q6_K_BYTES;
         q.h = (int)((p >> 1) & 1);
         q.l0 = 16 * (int)(p & 1);
-        q.lane = (int)(p & 31);
-        q.span_off = (int)((p >> 5) * 8 * Q6_K_BYTES);
-        q.span_len = (int)((left < 8 ? (left > 0 ? left : 0) : 8) * Q6_K_BYTES);
-        q.fld = (q.lane >> 2) * Q6_K_BYTES;
+        q.lane = (int)((p * TG + tg) & 31);
+        q.span_off = (int)(w * BW * Q6_K_BYTES);
+        q.span_len = (int)((left < BW ? (left > 0 ? left : 0) : BW) * Q6_K_BYTES);
+        q.fld = (int)((p % PW) >> 2) * Q6_K_BYTES;
         return q;
     }
     static __device__ __forceinline__ void load(W &w, const uint8_t *row, const Pos &q) {
@@ -490,7 +499,6 @@ __global__ void __launch_bounds__(MAXT) mmvq_kernel(const MmvqSegs sg, int64_t k
     const int64_t ldy0 = sg.ldy[0];
     constexpr int V = R * M;
     static_assert(V * TG <= 32 && (V & (V - 1)) == 0, "R*M must be a power of two <= 32/TG");
-    static_assert(!PT::STAGED || TG == 1, "staged pieces: one thread per piece, so a warp is 32 pieces");
     __shared__ float red[2][MAXT / 32][TG * V];
     __shared__ uint4 stage[PT::STAGED ? MAXT / 32 : 1][PT::STAGE_CHUNKS];   // warp buffers of staged pieces
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
@@ -499,7 +507,7 @@ __global__ void __launch_bounds__(MAXT) mmvq_kernel(const MmvqSegs sg, int64_t k
     const int64_t P = k / PT::VALUES;
     const bool valid = piece < P;
     const typename PT::Pos pos = [&] {
-        if constexpr (PT::STAGED) return PT::pos(piece, k);   // lanes past the row still copy their share
+        if constexpr (PT::STAGED) return PT::template pos<TG>(piece, tg, k);   // lanes past the row still copy their share
         else return PT::pos(valid ? piece : 0);
     }();
     const int64_t stride = (int64_t)gridDim.x * R;
@@ -632,9 +640,9 @@ inline cudaError_t launch_mmvq_cfg(const MmvqSegs &sg, int64_t k, int64_t rb, co
 // Configuration by token count (measured on GB300, Q4_K / Q6_K rows of 3072 ..
 // 8192 values): up to 4 tokens per thread with the next R rows prefetched
 // (R = 4 for 2..4 tokens of Q4_K rows and 2 tokens of Q6_K rows);
-// 5..8 tokens either as two threads per piece with 4 tokens each (Q4_K) or 8
-// tokens per thread (Q6_K, whose wider loads leave fewer registers).  Rows of
-// more than 256 pieces (32-value pieces of K > 8192) use 512-thread CTAs.
+// 5..8 tokens either as two threads per piece with 4 tokens each (Q4_K; Q6_K
+// and Q8_0 on small matrices) or 8 tokens per thread.  Rows of more than 256
+// pieces (32-value pieces of K > 8192) use 512-thread CTAs.
 struct MmvqTune {
     bool r4_m1;        // M = 1: R = 4 instead of 2
     bool r1_m1;        // M = 1: R = 1 (overrides r4_m1)
@@ -661,8 +669,7 @@ inline cudaError_t launch_mmvq_pt(const MmvqSegs &sg, int64_t k, const uint8_t *
             if (t.r4_m4) return launch_mmvq_cfg<PT, 4, 1, 4, 256>(sg, k, rb, xq, m, yt, s);
             return launch_mmvq_cfg<PT, 4, 1, 2, 256>(sg, k, rb, xq, m, yt, s);
         }
-        if constexpr (!PT::STAGED)   // staged pieces take one thread per piece
-            if (t.tg2_m8 && P <= 128) return launch_mmvq_cfg<PT, 4, 2, 2, 256>(sg, k, rb, xq, m, yt, s);
+        if (t.tg2_m8 && P <= 128) return launch_mmvq_cfg<PT, 4, 2, 2, 256>(sg, k, rb, xq, m, yt, s);
         return launch_mmvq_cfg<PT, 8, 1, 1, 256>(sg, k, rb, xq, m, yt, s);
     }
     if constexpr (PT::VALUES == 32) {
