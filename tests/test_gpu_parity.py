@@ -165,23 +165,27 @@ def test_mmvq_k_range_bf16(g, wt, k, m):
     assert_close(y.float().cpu().numpy(), ref, TOL_BF16, f"mmvq bf16 type {wt} k {k} m {m}")
 
 
+@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K])
 @pytest.mark.parametrize("k", [256, 1024, 3072, 8192])
 @pytest.mark.parametrize("m", [5, 8])
-def test_mmvq_tensor_core_vs_dp4a(g, k, m):
-    # 5..8 tokens of Q4_K rows (n >= 2048) run on the tensor-core MMVQ by
-    # default; the dp4a kernel (option mmvq_tc = 0) computes the same formula
-    n = 2100
-    w = _weights(oracle.Q4_K, n, k, seed=k + m)
+def test_mmvq_tensor_core_vs_dp4a(g, wt, k, m):
+    # 5..8 tokens of Q4_K rows (n >= 2048) and of Q6_K rows (n >= 32768) run on
+    # the tensor-core MMVQ by default; the dp4a kernel (option mmvq_tc = 0)
+    # computes the same formula
+    n = 2100 if wt == oracle.Q4_K else 32768 + 37
+    if wt == oracle.Q6_K and k > 1024:
+        pytest.skip("tall Q6_K rows: k up to 1024 keeps the oracle fast")
+    w = _weights(wt, n, k, seed=k + m)
     x = synth.activations(m, k, seed=k, dtype=torch.float32)
-    ref = oracle.mul_mat(oracle.Q4_K, w, k, oracle.quantize_q8_1(x.numpy()))
-    a = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x.to(DEV)).cpu().numpy()
+    ref = oracle.mul_mat(wt, w, k, oracle.quantize_q8_1(x.numpy()))
+    a = g.gguf_mul_mat(_u8(w), wt, n, k, x.to(DEV)).cpu().numpy()
     g.gguf_set_option("mmvq_tc", 0)
     try:
-        b = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x.to(DEV)).cpu().numpy()
+        b = g.gguf_mul_mat(_u8(w), wt, n, k, x.to(DEV)).cpu().numpy()
     finally:
         g.gguf_set_option("mmvq_tc", 1)
-    assert_close(a, ref, TOL_F32, f"tensor-core mmvq k {k} m {m}")
-    assert_close(b, ref, TOL_F32, f"dp4a mmvq k {k} m {m}")
+    assert_close(a, ref, TOL_F32, f"tensor-core mmvq type {wt} k {k} m {m}")
+    assert_close(b, ref, TOL_F32, f"dp4a mmvq type {wt} k {k} m {m}")
 
 
 @pytest.mark.parametrize("m", [9, 12, 16, 17, 24, 32])
@@ -238,6 +242,47 @@ def test_mmvq_tensor_core_exact_integer_sums(g, m):
     x = torch.from_numpy(xi.astype(np.float32))
     assert np.array_equal(oracle.mul_mat(oracle.Q4_K, w, k, oracle.quantize_q8_1(xi.astype(np.float32))), want)
     y = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x.to(DEV)).cpu().numpy()
+    assert np.array_equal(y.astype(np.float64), want), f"max diff {np.abs(y - want).max()}"
+
+
+def _q6_k_plain(q6):
+    # Q6_K rows with d = 1 and every scale 1: the blocks hold q6 - 32 (q6 in
+    # 0..63); value 128h + 32q + l of a block takes its low 4 bits from
+    # ql[64h + 32(q & 1) + l] (low nibble for q < 2, high for q >= 2) and its
+    # high 2 bits from bits 2q, 2q + 1 of qh[32h + l]
+    n, k = q6.shape
+    v = q6.reshape(n, k // 256, 2, 4, 32).astype(np.uint8)     # [row][sb][h][q][l]
+    ql = np.zeros((n, k // 256, 2, 2, 32), np.uint8)            # [row][sb][h][q & 1][l]
+    qh = np.zeros((n, k // 256, 2, 32), np.uint8)
+    for q in range(4):
+        ql[:, :, :, q & 1, :] |= (v[:, :, :, q, :] & 15) << (4 * (q >> 1))
+        qh |= (v[:, :, :, q, :] >> 4) << (2 * q)
+    blk = np.zeros((n, k // 256, 210), np.uint8)
+    blk[:, :, :128] = ql.reshape(n, k // 256, 128)
+    blk[:, :, 128:192] = qh.reshape(n, k // 256, 64)
+    blk[:, :, 192:208] = 1
+    blk[:, :, 209] = 0x3C                                      # d = fp16 1.0 (0x3C00)
+    return blk.reshape(n, -1)
+
+
+@pytest.mark.parametrize("m", [5, 8])
+@pytest.mark.parametrize("n", [32768, 32781])
+def test_mmvq_tensor_core_q6_k_exact_integer_sums(g, m, n):
+    # Q6_K rows with unit scales and integer activations whose every 32-block
+    # reaches 127 (d_a = 1, q = x): y is the integer product (q6 - 32) . X,
+    # below 2^24, so the tensor-core MMVQ (u8 quants, the 32 * sum correction,
+    # int32 scale sums) must match the int64 product bit for bit.  32781 rows:
+    # a ragged last tile and the guarded end of the view.
+    k = 512
+    rng = np.random.default_rng(m + n)
+    q6 = rng.integers(0, 64, size=(n, k), dtype=np.int64)
+    xi = rng.integers(-127, 128, size=(m, k), dtype=np.int64)
+    xi[:, ::32] = 127
+    w = _q6_k_plain(q6)
+    assert np.array_equal(oracle.dequantize_f32(oracle.Q6_K, w, k), (q6 - 32).astype(np.float32))
+    want = (xi @ (q6 - 32).T).astype(np.float64)
+    assert np.abs(want).max() < 2 ** 24
+    y = g.gguf_mul_mat(_u8(w), oracle.Q6_K, n, k, torch.from_numpy(xi.astype(np.float32)).to(DEV)).cpu().numpy()
     assert np.array_equal(y.astype(np.float64), want), f"max diff {np.abs(y - want).max()}"
 
 
