@@ -475,6 +475,28 @@ def secondary(torch, g, synth, dev, stream, hbm_peak, tf_peak, peak_kind):
                     "down Q6_K + weighted sum"}
         del wgu, wdn, x, y, ws
 
+        # dequantize (a whole Q4_K / Q6_K matrix to bf16) and get_rows (8192 random rows of a Q6_K
+        # embedding table to bf16): HBM-bound, reported as GB/s of packed bytes read + values written
+        for name, wt, n, k in (("dequantize_q4_k_14336x4096_bf16", g.Q4_K, 14336, 4096),
+                               ("dequantize_q6_k_14336x4096_bf16", g.Q6_K, 14336, 4096)):
+            w = synth.safe_blocks_device(wt, n, k, seed=9, device=dev)
+            y = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
+            ms = _time_eager(torch, stream, lambda: g.gguf_dequantize(w, wt, n, k, out=y), 10, flush)
+            by = w.numel() + y.numel() * 2
+            out[name] = {"us": round(ms * 1e3, 2), "gbs": round(by / (ms * 1e-3) / 1e9, 1),
+                         "frac": round(by / (ms * 1e-3) / 1e9 / hbm_peak, 3), "bytes": by}
+            del w, y
+        V, D, NI = 128256, 3072, 8192
+        table = synth.safe_blocks_device(g.Q6_K, V, D, seed=10, device=dev)
+        ids = torch.randint(0, V, (NI,), dtype=torch.int32, device=dev)
+        y = torch.empty((NI, D), dtype=torch.bfloat16, device=dev)
+        ms = _time_eager(torch, stream, lambda: g.gguf_get_rows(table, g.Q6_K, V, D, ids, out=y), 10, flush)
+        by = NI * g.gguf_row_size(g.Q6_K, D) + NI * 4 + y.numel() * 2
+        out["get_rows_q6_k_128256x3072_8192ids_bf16"] = {
+            "us": round(ms * 1e3, 2), "gbs": round(by / (ms * 1e-3) / 1e9, 1),
+            "frac": round(by / (ms * 1e-3) / 1e9 / hbm_peak, 3), "bytes": by}
+        del table, ids, y
+
         # Llama-3.2-3B-shaped decode step: 28 layers of q/k/o/gate/up (Q4_K) and v/down (Q6_K), tied
         # Q6_K embedding / LM head 128256 x 3072 via get_rows + MMVQ; all linears at M in {1, 8, 32}
         out["llama32_3b_decode_linears"] = llama_decode(torch, g, synth, dev, stream, hbm_peak)

@@ -9,8 +9,8 @@
 //
 // One thread produces one 32-value piece of a row:
 //   Q8_0 / q8_1 : one block (one run of 32 values)
-//   Q4_K        : 16 quant bytes -> runs [64c+16h, +16) (low nibbles) and
-//                 [64c+32+16h, +16) (high nibbles) of a super-block
+//   Q4_K        : sub-block j of a super-block (values [32j, +32): the low or
+//                 high nibbles of the 32 quant bytes of chunk j / 2)
 //   Q6_K        : runs [128h + 32g + l0, +8) for g = 0..3 of a super-block
 #include "common.cuh"
 #include "internal.h"
@@ -72,28 +72,28 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
         if (zero) for (int i = 0; i < 32; i++) v[i] = 0.0f;
         store_run<OT>(out, obase + p * 32, v, 32);
     } else if (WT == GGUF_Q4_K) {
+        // sub-block j = p % 8 of super-block p / 8: the low (j even) or high
+        // (j odd) nibbles of the 32 quant bytes of chunk j / 2, written as one
+        // contiguous run of 32 values
         const int64_t sb = p >> 3;
-        const int pp = (int)(p & 7), c = pp >> 1, h = pp & 1;
+        const int j = (int)(p & 7), c = j >> 1, sh = 4 * (j & 1);
         const uint8_t *blk = row + sb * Q4_K_BYTES;
         const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
-        const uint4 qv = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c + 16 * h);
+        const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
+        const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
         const uint32_t sc[3] = {hdr.y, hdr.z, hdr.w};
         const float d = h2f(hdr.x & 0xffff), dmin = h2f(hdr.x >> 16);
-        int s0, m0, s1, m1;
-        q4k_scale_min(sc, 2 * c, s0, m0);
-        q4k_scale_min(sc, 2 * c + 1, s1, m1);
-        const float a0 = __fmul_rn(d, (float)s0), b0 = __fmul_rn(dmin, (float)m0);
-        const float a1 = __fmul_rn(d, (float)s1), b1 = __fmul_rn(dmin, (float)m1);
-        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+        int s, m;
+        q4k_scale_min(sc, j, s, m);
+        const float a = __fmul_rn(d, (float)s), b = __fmul_rn(dmin, (float)m);
+        const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-            const int byte = (qw[i >> 2] >> (8 * (i & 3))) & 0xff;
-            v[i] = __fsub_rn(__fmul_rn(a0, (float)(byte & 15)), b0);
-            v[16 + i] = __fsub_rn(__fmul_rn(a1, (float)(byte >> 4)), b1);
+        for (int i = 0; i < 32; i++) {
+            const int nib = (qw[i >> 2] >> (8 * (i & 3) + sh)) & 15;
+            v[i] = __fsub_rn(__fmul_rn(a, (float)nib), b);
         }
         if (zero) for (int i = 0; i < 32; i++) v[i] = 0.0f;
-        store_run<OT>(out, obase + sb * 256 + 64 * c + 16 * h, v, 16);
-        store_run<OT>(out, obase + sb * 256 + 64 * c + 32 + 16 * h, v + 16, 16);
+        store_run<OT>(out, obase + sb * 256 + 32 * j, v, 32);
     } else {  // Q6_K
         const int64_t sb = p >> 3;
         const int pp = (int)(p & 7), h = pp >> 2, l0 = 8 * (pp & 3);
