@@ -57,6 +57,43 @@ def test_segments_match_oracle(g, wt, m):
     assert np.all(got[:, c0:] == 0)   # columns past the segments untouched
 
 
+@pytest.mark.parametrize("m", [5, 8])
+def test_segments_q6_k_tensor_core_tall(g, m):
+    # tall Q6_K segments (>= 32768 rows in all) take the tensor-core Q6_K
+    # MMVQ; the 16-row tiles straddle the segment boundaries at 20001 and
+    # 20001 + 12799, and the last row of every segment is the guarded end of
+    # its view.  Each segment's output is checked against the oracle on
+    # sampled rows (the boundary rows included) and against the dp4a kernel.
+    k = 512
+    ns = [20001, 12799, 37]
+    ws_ = [synth.safe_blocks(oracle.Q6_K, n, k, seed=31 + i) for i, n in enumerate(ns)]
+    x = synth.activations(m, k, seed=m + 50, dtype=torch.float32)
+    xq = oracle.quantize_q8_1(x.numpy())
+    wide = torch.zeros(m, sum(ns), dtype=torch.float32, device=DEV)
+    segs, c0 = [], 0
+    for w, n in zip(ws_, ns):
+        segs.append((_u8(w), n, wide[:, c0:c0 + n]))
+        c0 += n
+    g.gguf_mul_mat_segments(oracle.Q6_K, k, x.to(DEV), segs)
+    got = wide.cpu().numpy()
+    g.gguf_set_option("mmvq_tc", 0)
+    try:
+        wide2 = torch.zeros_like(wide)
+        segs2 = [(w_, n, wide2[:, c:c + n]) for (w_, n, _), c in zip(segs, np.cumsum([0] + ns[:-1]))]
+        g.gguf_mul_mat_segments(oracle.Q6_K, k, x.to(DEV), segs2)
+        dp4a = wide2.cpu().numpy()
+    finally:
+        g.gguf_set_option("mmvq_tc", 1)
+    assert_close(got, dp4a, TOL_F32, f"tensor-core vs dp4a m {m}")
+    c0 = 0
+    rng = np.random.default_rng(m)
+    for i, (w, n) in enumerate(zip(ws_, ns)):
+        rows = np.unique(np.concatenate([[0, n - 1], rng.choice(n, min(n, 48), replace=False)]))
+        ref = oracle.mul_mat(oracle.Q6_K, w[rows], k, xq)
+        assert_close(got[:, c0 + rows], ref, TOL_F32, f"segment {i} m {m}")
+        c0 += n
+
+
 def test_segments_equal_separate_calls_bf16(g):
     # the decode shape: two Q4_K matrices on one q8_1 copy, bf16 out
     k = 4096
