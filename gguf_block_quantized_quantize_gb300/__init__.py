@@ -271,8 +271,10 @@ def gguf_mul_mat_id(w: torch.Tensor, wt: int, n_experts: int, expert_stride: int
         if mode == GATE_UP_SWIGLU:
             yt = BF16 if out_type is None else out_type
             i_dim = n // 2
-            out = (torch.empty((n_tokens * top_k, i_dim), dtype=torch.bfloat16, device=x.device) if yt == BF16 else
-                   torch.empty((n_tokens * top_k, gguf_row_size(Q8_1, i_dim)), dtype=torch.uint8, device=x.device))
+            if yt in (BF16, F16):
+                out = torch.empty((n_tokens * top_k, i_dim), dtype=_DTYPE_OF[yt], device=x.device)
+            else:
+                out = torch.empty((n_tokens * top_k, gguf_row_size(Q8_1, i_dim)), dtype=torch.uint8, device=x.device)
         else:
             yt = BF16 if out_type is None else out_type
             out = torch.empty((n_tokens, n), dtype=_DTYPE_OF[yt], device=x.device)

@@ -102,6 +102,10 @@ static int64_t g_mmq_enable = 1;
 static int64_t g_mmvq_tc = 1;
 static int64_t g_mmvq_tc_max_m = 16;   // 9..16 tokens: 2 n-tiles beat MMQ; 4 n-tiles do not
 static int64_t g_mmvq_tc_min_m = 5;
+// MoE calls of at most this many tokens take the route-batched MMVQ (vector)
+// path; the workspace reserves its buffers up to MOE_VEC_CAP tokens
+constexpr int64_t MOE_VEC_CAP = 256;
+static int64_t g_moe_vec_max_tokens = 128;
 int64_t option_mmvq_tc() { return g_mmvq_tc; }
 int64_t option_mmvq_tc_min_m() { return g_mmvq_tc_min_m; }
 int64_t option_mmvq_tc_max_m() { return g_mmvq_tc_max_m; }
@@ -329,8 +333,15 @@ static gguf_status check_bank(const char *what, const void *w, int wt, int64_t E
 static MoeWs moe_call_layout(const gguf_moe_args *a, void *base) {
     const int64_t R = a->n_tokens * a->top_k;
     const int64_t kx = op_pitch(a->wt, a->k);
-    if (a->mode == GGUF_MOE_GATE_UP_SWIGLU) return moe_ws_layout(base, a->n_experts, R, a->n_tokens * kx, 0, 0, false);
+    if (a->mode == GGUF_MOE_GATE_UP_SWIGLU)
+        return moe_ws_layout(base, a->n_experts, R, a->n_tokens * kx, 0, 0, false,
+                             a->n_tokens <= MOE_VEC_CAP ? a->n : 0);
     return moe_ws_layout(base, a->n_experts, R, R * kx, R * a->n, 0, false);
+}
+
+// the route-batched MMVQ path: few tokens, and weight rows it takes
+static bool moe_vec(int64_t n_tokens, int wt, int64_t k) {
+    return n_tokens <= g_moe_vec_max_tokens && mmvq_routes_supported(wt, k);
 }
 
 static gguf_status check_moe(const gguf_moe_args *a) {
@@ -381,6 +392,37 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
     const int64_t R = a->n_tokens * a->top_k;
     const int bn = moe_bn(R, a->n_experts);
     cudaError_t e;
+    const bool vec = moe_vec(a->n_tokens, a->wt, a->k);
+    if (vec) {
+        // route-batched MMVQ: each active route reads its expert's rows once
+        const int64_t rows = a->mode == GGUF_MOE_GATE_UP_SWIGLU ? a->n_tokens : R;
+        const uint8_t *xq = (const uint8_t *)a->x;
+        if (a->xt != GGUF_Q8_1) {
+            if ((e = launch_quantize_q8_1(a->x, a->xt, rows, a->k, a->ldx, (uint8_t *)w.xh, nullptr, nullptr, s)) != cudaSuccess)
+                return cuda_status(e, "mul_mat_id quantize");
+            xq = (const uint8_t *)w.xh;
+        }
+        const bool gu = a->mode == GGUF_MOE_GATE_UP_SWIGLU;
+        if ((e = moe_mark(a->ids, gu ? nullptr : a->route_w, R, a->n_experts, !gu, a->dev_status, w.pos, s)) != cudaSuccess)
+            return cuda_status(e, "mul_mat_id routes");
+        const MmvqRoutes rt{a->ids, w.pos, a->expert_stride, a->top_k, gu ? 0 : 1};
+        if (!gu) {
+            if ((e = launch_mmvq_routes(a->wt, (const uint8_t *)a->w, rt, a->n, a->k, xq, R, w.z, s)) != cudaSuccess)
+                return cuda_status(e, "mul_mat_id down");
+            return cuda_status(launch_moe_finalize(w.z, w.pos, a->route_w, a->n_tokens, a->top_k, a->n, a->y, a->yt, s),
+                               "mul_mat_id finalize");
+        }
+        const int64_t idim = a->n / 2;
+        if ((e = launch_mmvq_routes(a->wt, (const uint8_t *)a->w, rt, a->n, a->k, xq, R, w.zv, s)) != cudaSuccess)
+            return cuda_status(e, "mul_mat_id gate_up");
+        uint16_t *h = a->yt == GGUF_BF16 ? (uint16_t *)a->y : w.hb;
+        if ((e = launch_moe_swiglu(w.zv, w.pos, R, idim, h, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id swiglu");
+        if (a->yt == GGUF_Q8_1)
+            e = launch_quantize_q8_1(h, GGUF_BF16, R, idim, idim, (uint8_t *)a->y, nullptr, nullptr, s);
+        else if (a->yt == GGUF_F16 && (e = launch_quantize_q8_1(h, GGUF_BF16, R, idim, idim, w.hqv, nullptr, nullptr, s)) == cudaSuccess)
+            e = launch_q8_1_to_f16(w.hqv, R, idim, (uint16_t *)a->y, nullptr, s, idim);
+        return cuda_status(e, "mul_mat_id gate_up output");
+    }
     if (a->mode == GGUF_MOE_GATE_UP_SWIGLU) {
         const int64_t idim = a->n / 2;
         const size_t ybytes = a->yt == GGUF_Q8_1 ? (size_t)(R * row_size(GGUF_Q8_1, idim)) : (size_t)(R * idim * 2);
@@ -405,7 +447,8 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
 static MoeWs ffn_layout(const gguf_moe_ffn_args *a, void *base) {
     const int64_t R = a->n_tokens * a->top_k;
     return moe_ws_layout(base, a->n_experts, R, a->n_tokens * op_pitch(a->gate_up_type, a->hidden),
-                         R * a->hidden, R * op_pitch(a->down_type, a->inter), a->yt == GGUF_F32);
+                         R * a->hidden, R * op_pitch(a->down_type, a->inter), a->yt == GGUF_F32,
+                         a->n_tokens <= MOE_VEC_CAP ? 2 * a->inter : 0);
 }
 
 size_t gguf_moe_ffn_ws_size(const gguf_moe_ffn_args *a) {
@@ -436,6 +479,31 @@ gguf_status gguf_moe_ffn(const gguf_moe_ffn_args *a, void *ws, size_t ws_bytes, 
     const int64_t R = a->n_tokens * a->top_k;
     const int bn = moe_bn(R, a->n_experts);
     cudaError_t e;
+    if (moe_vec(a->n_tokens, a->gate_up_type, a->hidden) && mmvq_routes_supported(a->down_type, a->inter)) {
+        // route-batched MMVQ for both products: x -> q8_1, gate_up rows per
+        // route, SwiGLU -> bf16 -> q8_1, down rows per route, weighted sum
+        const uint8_t *xq = (const uint8_t *)a->x;
+        if (a->xt != GGUF_Q8_1) {
+            if ((e = launch_quantize_q8_1(a->x, a->xt, a->n_tokens, a->hidden, a->ldx, (uint8_t *)w.xh, nullptr, nullptr, s)) != cudaSuccess)
+                return cuda_status(e, "moe_ffn quantize");
+            xq = (const uint8_t *)w.xh;
+        }
+        if ((e = moe_mark(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w.pos, s)) != cudaSuccess)
+            return cuda_status(e, "moe_ffn routes");
+        uint8_t *hq = (uint8_t *)w.h16;   // q8_1 rows of h ([R][I / 32] blocks fit in the fp16 operand buffer)
+        if ((e = launch_mmvq_routes(a->gate_up_type, (const uint8_t *)a->w_gate_up,
+                                    MmvqRoutes{a->ids, w.pos, a->gate_up_stride, a->top_k, 0}, 2 * a->inter, a->hidden,
+                                    xq, R, w.zv, s)) != cudaSuccess ||
+            (e = launch_moe_swiglu(w.zv, w.pos, R, a->inter, w.hb, s)) != cudaSuccess ||
+            (e = launch_quantize_q8_1(w.hb, GGUF_BF16, R, a->inter, a->inter, hq, nullptr, nullptr, s)) != cudaSuccess)
+            return cuda_status(e, "moe_ffn gate_up");
+        if ((e = launch_mmvq_routes(a->down_type, (const uint8_t *)a->w_down,
+                                    MmvqRoutes{a->ids, w.pos, a->down_stride, a->top_k, 1}, a->hidden, a->inter, hq, R,
+                                    w.z, s)) != cudaSuccess)
+            return cuda_status(e, "moe_ffn down");
+        return cuda_status(launch_moe_finalize(w.z, w.pos, a->route_w, a->n_tokens, a->top_k, a->hidden, a->y, a->yt, s),
+                           "moe_ffn finalize");
+    }
     if ((e = to_f16_operand(a->x, a->xt, a->n_tokens, a->hidden, a->ldx, w.xh, w.xl, op_pitch(a->gate_up_type, a->hidden), s)) != cudaSuccess) return cuda_status(e, "moe_ffn quantize");
     // one grouping serves both GEMMs; a route of weight 0 contributes nothing and is skipped by both
     if ((e = moe_group(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "moe_ffn grouping");
@@ -472,6 +540,11 @@ gguf_status gguf_set_option(const char *key, int64_t value) {
         g_mmvq_tc = value != 0;
         return GGUF_OK;
     }
+    if (!strcmp(key, "moe_vec_max_tokens")) {
+        if (value < 0 || value > MOE_VEC_CAP) return fail(GGUF_ERR_INVALID_ARG, "set_option: moe_vec_max_tokens must be in [0, 256]");
+        g_moe_vec_max_tokens = value;
+        return GGUF_OK;
+    }
     if (!strcmp(key, "mmvq_tc_min_m")) {
         if (value < 1 || value > 8) return fail(GGUF_ERR_INVALID_ARG, "set_option: mmvq_tc_min_m must be in [1, 8]");
         g_mmvq_tc_min_m = value;
@@ -495,6 +568,7 @@ int64_t gguf_get_option(const char *key) {
     if (!strcmp(key, "mmq_enable")) return g_mmq_enable;
     if (!strcmp(key, "mmvq_tc")) return g_mmvq_tc;
     if (!strcmp(key, "mmvq_tc_min_m")) return g_mmvq_tc_min_m;
+    if (!strcmp(key, "moe_vec_max_tokens")) return g_moe_vec_max_tokens;
     if (!strcmp(key, "mmvq_tc_max_m")) return g_mmvq_tc_max_m;
     return -1;
 }

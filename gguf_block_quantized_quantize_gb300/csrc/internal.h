@@ -68,6 +68,22 @@ struct MmvqSegs {
 // one segment: W[n][k] -> y[.][ldy]
 MmvqSegs mmvq_one_segment(const void *w, int64_t n, void *y, int64_t ldy);
 
+// MoE routes of the route-batched MMVQ: grid row blockIdx.y is route slot r
+struct MmvqRoutes {
+    const int32_t *ids;      // expert of each route slot
+    const int32_t *pos;      // < 0: the route is skipped (inactive, out-of-range id or weight 0)
+    int64_t expert_stride;   // bytes between the experts' matrices
+    int64_t top_k;           // route slots per token
+    int x_per_route;         // activation row of route r: r (1) or its token r / top_k (0)
+};
+// z[r][n] (fp32) = W[ids[r]] . q8_1 activation row of route r, for every route
+// slot r < routes with pos[r] >= 0 (W: the expert bank, [n][k] of type wt per
+// expert); one launch, one token per route
+cudaError_t launch_mmvq_routes(int wt, const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k,
+                               const uint8_t *xq, int64_t routes, float *z, cudaStream_t s);
+// whether launch_mmvq_routes takes rows of k values of type wt
+bool mmvq_routes_supported(int wt, int64_t k);
+
 // for every segment s: y_s[m][ldy_s] (yt) = W_s (wt) . q8_1 rows xq[m] ; m <= 8,
 // or m <= 32 when mmvq_tc_wide(wt, k, m)
 cudaError_t launch_mmvq(const MmvqSegs &sg, int wt, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
@@ -85,14 +101,25 @@ struct MoeWs {
     uint16_t *xh, *xl;
     float *z;  // per-route outputs of the down GEMM [R][n]
     uint16_t *h16, *h16lo;
+    // route-batched (vector) gate_up: per-route g | u rows [R][2I], h [R][I] bf16, h as q8_1
+    float *zv;
+    uint16_t *hb;
+    uint8_t *hqv;
     size_t bytes;
 };
-// base == nullptr computes only the size
+// base == nullptr computes only the size; vec_n2 = 2I reserves the vector
+// gate_up buffers (0: none)
 MoeWs moe_ws_layout(void *base, int64_t E, int64_t R, int64_t xh_elems, int64_t z_elems, int64_t h16_elems,
-                    bool with_lo);
+                    bool with_lo, int64_t vec_n2 = 0);
+// h[r][j] = bf16(silu(g) * u) of the vector gate_up rows z[r] = (g[0..I), u[0..I));
+// zeros for skipped routes (pos[r] < 0)
+cudaError_t launch_moe_swiglu(const float *z, const int32_t *pos, int64_t R, int64_t I, uint16_t *h, cudaStream_t s);
 int moe_bn(int64_t routes, int64_t experts);
 cudaError_t moe_group(const int32_t *ids, const float *rw, int64_t R, int64_t E, bool skip_zero_w, int32_t *status,
                       const MoeWs &w, int bn, cudaStream_t s);
+// route marks only (pos[r] = r or -1), for the route-batched path
+cudaError_t moe_mark(const int32_t *ids, const float *rw, int64_t R, int64_t E, bool skip_zero_w, int32_t *status,
+                     int32_t *pos, cudaStream_t s);
 cudaError_t launch_moe_gate_up(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
                                const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
                                const MoeWs &ws, uint8_t *hq, uint16_t *hbf, uint16_t *h16, uint16_t *h16lo,

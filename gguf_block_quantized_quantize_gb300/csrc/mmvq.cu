@@ -30,4 +30,19 @@ cudaError_t launch_mmvq(const MmvqSegs &sg, int wt, int64_t k, const uint8_t *xq
     }
 }
 
+bool mmvq_routes_supported(int wt, int64_t k) {
+    const int64_t values = wt == GGUF_Q8_0 ? 32 : 64;
+    return (wt == GGUF_Q8_0 || wt == GGUF_Q4_K || wt == GGUF_Q6_K) && k > 0 && k / values <= 256;
+}
+
+cudaError_t launch_mmvq_routes(int wt, const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k,
+                               const uint8_t *xq, int64_t routes, float *z, cudaStream_t s) {
+    if (!mmvq_routes_supported(wt, k)) return cudaErrorInvalidValue;
+    switch (wt) {
+    case GGUF_Q8_0: return launch_mmvq_routes_q8_0(bank, rt, n, k, xq, routes, z, s);
+    case GGUF_Q4_K: return launch_mmvq_routes_q4_k(bank, rt, n, k, xq, routes, z, s);
+    default: return launch_mmvq_routes_q6_k(bank, rt, n, k, xq, routes, z, s);
+    }
+}
+
 }  // namespace gg

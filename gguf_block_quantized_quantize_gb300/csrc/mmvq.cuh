@@ -490,13 +490,28 @@ struct Q6KPiece {
 // + gridDim.x * R, ...
 // MULTI: more than one weight segment (row addresses looked up per row group);
 // a single segment keeps its pointers in registers.
-template <class PT, int M, int TG, int R, int MAXT, bool MULTI>
+// ROUTES: MoE route slots, one per grid row (blockIdx.y = r): the weights are
+// expert ids[r] of the bank sg.w[0], the activations the q8_1 row of route r
+// (or of its token), the fp32 output row r of sg.y[0]; skipped routes
+// (pos[r] < 0) exit at once.  M = 1, one segment.
+template <class PT, int M, int TG, int R, int MAXT, bool MULTI, bool ROUTES = false>
 __global__ void __launch_bounds__(MAXT) mmvq_kernel(const MmvqSegs sg, int64_t k, int64_t rb,
-                                                   const uint8_t *__restrict__ xq, int m_act, int yt) {
+                                                   const uint8_t *__restrict__ xq, int m_act, int yt,
+                                                   const MmvqRoutes rt) {
     const int64_t n = sg.rows();
-    const uint8_t *const w0 = sg.w[0];
-    void *const y0 = sg.y[0];
+    const uint8_t *w0 = sg.w[0];
+    void *y0 = sg.y[0];
     const int64_t ldy0 = sg.ldy[0];
+    if constexpr (ROUTES) {
+        static_assert(M == 1 && !MULTI, "routes: one token, one segment");
+        // the route table and the activations come from earlier kernels
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        const int64_t r = blockIdx.y;
+        if (rt.pos[r] < 0) return;
+        w0 += (int64_t)rt.ids[r] * rt.expert_stride;
+        y0 = reinterpret_cast<float *>(y0) + r * n;
+        xq += (rt.x_per_route ? r : r / rt.top_k) * ((k / 32) * Q8_1_BYTES);
+    }
     constexpr int V = R * M;
     static_assert(V * TG <= 32 && (V & (V - 1)) == 0, "R*M must be a power of two <= 32/TG");
     __shared__ float red[2][MAXT / 32][TG * V];
@@ -634,7 +649,38 @@ inline cudaError_t launch_mmvq_cfg(const MmvqSegs &sg, int64_t k, int64_t rb, co
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, sg, k, rb, xq, (int)m, yt);
+    return cudaLaunchKernelEx(&cfg, kern, sg, k, rb, xq, (int)m, yt, MmvqRoutes{});
+}
+
+// the route-batched launch: CTAs of one route over its rows (two per group),
+// as many per route as fill the GPU once
+template <class PT>
+inline cudaError_t launch_mmvq_routes_pt(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k,
+                                         int64_t rb, const uint8_t *xq, int64_t routes, float *z, cudaStream_t s) {
+    if (routes <= 0 || n <= 0) return cudaSuccess;
+    const int64_t P = k / PT::VALUES;
+    if (P > 256 || routes > 65535) return cudaErrorInvalidValue;
+    const int nthr = (int)((P + 31) / 32 * 32);
+    auto kern = mmvq_kernel<PT, 1, 1, 2, 256, false, true>;
+    cudaError_t e = cudaSuccess;
+    const int per_sm = kernel_occupancy(reinterpret_cast<const void *>(kern), nthr, 0, &e);
+    if (per_sm == 0) return e;
+    const int64_t groups = (n + 1) / 2;
+    int64_t bx = ((int64_t)device_info().sm_count * per_sm + routes - 1) / routes;
+    if (bx > groups) bx = groups;
+    if (bx < 1) bx = 1;
+    const MmvqSegs sg = mmvq_one_segment(bank, n, z, n);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)bx, (unsigned)routes);
+    cfg.blockDim = dim3((unsigned)nthr);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, sg, k, rb, xq, 1, (int)GGUF_F32, rt);
 }
 
 // Configuration by token count (measured on GB300, Q4_K / Q6_K rows of 3072 ..
@@ -684,5 +730,11 @@ inline cudaError_t launch_mmvq_pt(const MmvqSegs &sg, int64_t k, const uint8_t *
 cudaError_t launch_mmvq_q8_0(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
 cudaError_t launch_mmvq_q4_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
 cudaError_t launch_mmvq_q6_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
+cudaError_t launch_mmvq_routes_q8_0(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,
+                                    int64_t routes, float *z, cudaStream_t s);
+cudaError_t launch_mmvq_routes_q4_k(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,
+                                    int64_t routes, float *z, cudaStream_t s);
+cudaError_t launch_mmvq_routes_q6_k(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,
+                                    int64_t routes, float *z, cudaStream_t s);
 
 }  // namespace gg

@@ -22,4 +22,9 @@ bool mmvq_tc_wide(int wt, int64_t k, int64_t m) {
            mma_q4k_fits(k, m);
 }
 
+cudaError_t launch_mmvq_routes_q4_k(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,
+                                    int64_t routes, float *z, cudaStream_t s) {
+    return launch_mmvq_routes_pt<Q4KPiece>(bank, rt, n, k, k / 256 * Q4_K_BYTES, xq, routes, z, s);
+}
+
 }  // namespace gg

@@ -15,4 +15,9 @@ cudaError_t launch_mmvq_q6_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, i
     return launch_mmvq_pt<Q6KPiece>(sg, k, xq, m, yt, s, k / 256 * Q6_K_BYTES, MmvqTune{false, false, n < 2048, n >= 2048, false});
 }
 
+cudaError_t launch_mmvq_routes_q6_k(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,
+                                    int64_t routes, float *z, cudaStream_t s) {
+    return launch_mmvq_routes_pt<Q6KPiece>(bank, rt, n, k, k / 256 * Q6_K_BYTES, xq, routes, z, s);
+}
+
 }  // namespace gg

@@ -51,6 +51,18 @@ __global__ void moe_count_kernel(const int32_t *__restrict__ ids, const float *_
     pos[r] = ok ? atomicAdd(&counts[e], 1) : -1;
 }
 
+// the route marks of the route-batched path: pos[r] = r for an active route,
+// -1 for a skipped one (same rules as moe_count_kernel; no grouping needed)
+__global__ void moe_mark_kernel(const int32_t *__restrict__ ids, const float *__restrict__ rw, int64_t R, int64_t E,
+                                int skip_zero_w, int32_t *__restrict__ pos, int32_t *__restrict__ dev_status) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= R) return;
+    const int32_t e = ids[r];
+    const bool ok = e >= 0 && e < E && !(skip_zero_w && rw != nullptr && rw[r] == 0.0f);
+    if (e >= E && dev_status != nullptr) atomicAdd(dev_status, 1);
+    pos[r] = ok ? (int32_t)r : -1;
+}
+
 // single CTA of 1024 threads: exclusive scans of counts and of tiles per expert
 __global__ void __launch_bounds__(1024) moe_scan_kernel(const int32_t *__restrict__ counts, int64_t E, int bn,
                                                         int32_t *__restrict__ offsets,
@@ -141,6 +153,21 @@ __global__ void moe_finalize_kernel(const float *__restrict__ z, const int32_t *
     for (int v = 0; v < V; v++) store_out(y, yt, i + v, acc[v]);
 }
 
+// SwiGLU of the route-batched gate_up: h = silu(g) * u in fp32 (the formula
+// of the tensor-core epilogue), rounded to bf16, the activation dtype
+__global__ void moe_swiglu_kernel(const float *__restrict__ z, const int32_t *__restrict__ pos, int64_t R, int64_t I,
+                                  uint16_t *__restrict__ h) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= R * I) return;
+    const int64_t r = i / I, j = i - r * I;
+    uint16_t bits = 0;
+    if (pos[r] >= 0) {
+        const float g = z[r * 2 * I + j], u = z[r * 2 * I + I + j];
+        bits = f2bf_rn(g / (1.0f + expf(-g)) * u);
+    }
+    h[i] = bits;
+}
+
 // ---------------------------------------------------------------- host side
 
 static size_t a256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -155,7 +182,7 @@ int moe_bn(int64_t routes, int64_t experts) {
 // tables, the fp16 activation operand (hi and lo parts), the fp32 per-route
 // outputs of the down GEMM and the fp16 intermediate (each optional: 0 elements).
 MoeWs moe_ws_layout(void *base, int64_t E, int64_t R, int64_t xh_elems, int64_t z_elems, int64_t h16_elems,
-                    bool with_lo) {
+                    bool with_lo, int64_t vec_n2) {
     MoeWs w{};
     uint8_t *p = reinterpret_cast<uint8_t *>(base);
     size_t off = 0;
@@ -178,6 +205,9 @@ MoeWs moe_ws_layout(void *base, int64_t E, int64_t R, int64_t xh_elems, int64_t 
     w.z = (float *)take(sizeof(float) * (size_t)z_elems);
     w.h16 = (uint16_t *)take(sizeof(uint16_t) * (size_t)h16_elems);
     w.h16lo = (uint16_t *)take(sizeof(uint16_t) * (size_t)(with_lo ? h16_elems : 0));
+    w.zv = (float *)take(sizeof(float) * (size_t)(R * vec_n2));
+    w.hb = (uint16_t *)take(sizeof(uint16_t) * (size_t)(R * vec_n2 / 2));
+    w.hqv = (uint8_t *)take((size_t)(R * (vec_n2 / 2 / 32) * Q8_1_BYTES));
     w.bytes = off;
     return w;
 }
@@ -273,6 +303,20 @@ cudaError_t launch_moe_finalize(const float *z, const int32_t *pos, const float 
         moe_finalize_kernel<4><<<(unsigned)((count / 4 + 255) / 256), 256, 0, s>>>(z, pos, route_w, T, top_k, n, y, yt);
     else
         moe_finalize_kernel<1><<<(unsigned)((count + 255) / 256), 256, 0, s>>>(z, pos, route_w, T, top_k, n, y, yt);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_moe_swiglu(const float *z, const int32_t *pos, int64_t R, int64_t I, uint16_t *h, cudaStream_t s) {
+    const int64_t count = R * I;
+    if (count == 0) return cudaSuccess;
+    moe_swiglu_kernel<<<(unsigned)((count + 255) / 256), 256, 0, s>>>(z, pos, R, I, h);
+    return cudaGetLastError();
+}
+
+cudaError_t moe_mark(const int32_t *ids, const float *rw, int64_t R, int64_t E, bool skip_zero_w, int32_t *status,
+                     int32_t *pos, cudaStream_t s) {
+    if (R == 0) return cudaSuccess;
+    moe_mark_kernel<<<(unsigned)((R + 255) / 256), 256, 0, s>>>(ids, rw, R, E, skip_zero_w ? 1 : 0, pos, status);
     return cudaGetLastError();
 }
 

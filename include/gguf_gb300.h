@@ -243,6 +243,14 @@ gguf_status gguf_mul_mat_noalloc(const void *w, int wt, int64_t n, int64_t k, co
  * The intermediate h is kept in the activation dtype (bf16) and then quantized
  * to q8_1 (FreeToken PR #690, section "Changes": the intermediates stay in the
  * activation dtype).
+ * Path: up to option "moe_vec_max_tokens" tokens (default 128) the call runs
+ * the route-batched MMVQ (one launch over all route slots, each reading its
+ * expert's rows once with exact int32 block sums; FreeToken PR #690, section
+ * "Changes": MoE takes MMVQ for small batches and MMQ above, with the
+ * grouped-MMQ-vs-vec crossover at 16 tokens on sm_120 in FreeToken PR #196,
+ * "Dispatch thresholds"), else the tensor-core grouped GEMM over the (expert,
+ * 128-route tile) pairs that hold routes.  Rows longer than 16384
+ * values (8192 for Q8_0) always take the grouped GEMM.
  */
 typedef struct {
     const void *w;
@@ -275,7 +283,8 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *args, void *ws, size_t ws_bytes
  * the intermediate stays in the workspace.  Same conventions as
  * gguf_mul_mat_id; banks hold [2*inter][hidden] (gate rows, then up rows) and
  * [hidden][inter] matrices per expert.  y : [n_tokens][hidden] of yt (F32, BF16
- * or F16).  Routes with weight 0 are skipped by both GEMMs.
+ * or F16).  Routes with weight 0 are skipped by both GEMMs.  The same
+ * "moe_vec_max_tokens" option selects the route-batched MMVQ for both products.
  */
 typedef struct {
     const void *w_gate_up;
@@ -320,6 +329,11 @@ gguf_status gguf_debug_block_dots(const void *w, int wt, int64_t n, int64_t k, c
  *                   dp4a MMVQ.
  *   "mmvq_tc_min_m": fewest tokens that take the tensor-core MMVQ, 1 .. 8
  *                   (default 5).
+ *   "moe_vec_max_tokens": mul_mat_id / moe_ffn calls of at most this many
+ *                   tokens take the route-batched MMVQ; 0 .. 256, default 128
+ *                   (the measured crossover with the grouped GEMM on GB300
+ *                   for the E=256, top-8 expert block: 3x faster at 1..16
+ *                   tokens, even at 128, slower from 192).
  *   "mmvq_tc_max_m": Q4_K products of 9 up to this many tokens stay on the
  *                   tensor-core MMVQ (2 or 4 n-tiles of 8 tokens) instead
  *                   of MMQ; 8 .. 32, default 16 (the measured crossover on

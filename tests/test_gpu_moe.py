@@ -9,7 +9,10 @@
     token within 1e-2 (the re-quantized intermediate, see _util.py);
   * repeated expert ids, id -1, ids >= E (counted in the status word) and
     weight-0 routes; the full-size configuration (E = 256, top-8, H = 2048,
-    I = 512, 8192 tokens) on sampled tokens.
+    I = 512, 8192 tokens) on sampled tokens;
+  * the route-batched MMVQ (vector) path of small token counts (option
+    moe_vec_max_tokens): the same checks, and agreement with the tensor-core
+    path on the same inputs.
 """
 import numpy as np
 import pytest
@@ -38,6 +41,17 @@ def _u8(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
+@pytest.fixture(params=["tensor_core", "vector"])
+def path(request, g):
+    """Runs the test through the tensor-core grouped GEMM (option
+    moe_vec_max_tokens = 0) and through the route-batched MMVQ (option at
+    its maximum), whatever the token count."""
+    saved = g.gguf_get_option("moe_vec_max_tokens")
+    g.gguf_set_option("moe_vec_max_tokens", 0 if request.param == "tensor_core" else 256)
+    yield request.param
+    g.gguf_set_option("moe_vec_max_tokens", saved)
+
+
 def _bank(wt, E, rows, cols, seed, safe):
     if safe:
         return np.ascontiguousarray(synth.safe_blocks(wt, E * rows, cols, seed))
@@ -57,7 +71,7 @@ def _small_case(safe=False):
     return E, K, H, I, T, bank_gu, bank_d, ids, rw, x
 
 
-def test_gate_up_swiglu_bf16_and_q8_1(g):
+def test_gate_up_swiglu_bf16_and_q8_1(g, path):
     E, K, H, I, T, bank_gu, _, ids, rw, x = _small_case()
     sgu = bank_gu.nbytes // E
     xq = oracle.quantize_q8_1(x.float().numpy())
@@ -86,7 +100,7 @@ def test_gate_up_swiglu_bf16_and_q8_1(g):
     assert np.all((np.abs(v1 - v0) <= bound * 1.0001)[active])
 
 
-def test_down_weighted_sum_from_oracle_h(g):
+def test_down_weighted_sum_from_oracle_h(g, path):
     E, K, H, T = 4, 3, 512, 29
     I = 256
     bank_d = _bank(oracle.Q6_K, E, H, I, 300, safe=False)
@@ -106,7 +120,7 @@ def test_down_weighted_sum_from_oracle_h(g):
 
 
 @pytest.mark.parametrize("safe", [False, True])
-def test_moe_ffn_end_to_end_small(g, safe):
+def test_moe_ffn_end_to_end_small(g, path, safe):
     E, K, H, T = 6, 4, 256, 41
     I = 256
     bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 400, safe)
@@ -129,7 +143,7 @@ def test_moe_ffn_end_to_end_small(g, safe):
     assert int(status.item()) == 1
 
 
-def test_moe_empty_and_all_inactive(g):
+def test_moe_empty_and_all_inactive(g, path):
     E, H, I = 2, 256, 256
     bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 600, True)
     bank_d = _bank(oracle.Q6_K, E, H, I, 601, True)
@@ -165,7 +179,7 @@ def test_moe_full_size_sampled(g):
 
 
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
-def test_moe_ffn_q4_k_down_bank(g, out_dtype):
+def test_moe_ffn_q4_k_down_bank(g, path, out_dtype):
     """Both banks Q4_K: the down GEMM needs the min-term correction columns of
     the q8_1 intermediate; fp32 output runs the precise down product."""
     E, K, H, T, I = 4, 2, 512, 23, 256
@@ -185,7 +199,7 @@ def test_moe_ffn_q4_k_down_bank(g, out_dtype):
 
 
 @pytest.mark.parametrize("out_type", ["f32", "bf16"])
-def test_down_q4_k_from_oracle_h(g, out_type):
+def test_down_q4_k_from_oracle_h(g, path, out_type):
     """Q4_K down bank through the DOWN mode (q8_1 rows from the oracle): the
     operand conversion appends the min-term correction columns."""
     E, K, H, T, I = 4, 2, 512, 23, 256
@@ -201,7 +215,7 @@ def test_down_q4_k_from_oracle_h(g, out_type):
     assert_close(y.float().cpu().numpy(), ref, TOL_F32 if yt == g.F32 else TOL_BF16, f"down q4_k {out_type}")
 
 
-def test_gate_up_h512(g):
+def test_gate_up_h512(g, path):
     E, K, H, T, I = 4, 2, 512, 23, 256
     bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 800, False)
     sgu = bank_gu.nbytes // E
@@ -210,7 +224,132 @@ def test_gate_up_h512(g):
     h_ref, _ = oracle.moe_gate_up(oracle.Q4_K, bank_gu, E, sgu, 2 * I, H, oracle.quantize_q8_1(x.numpy()), ids)
     hb = g.gguf_mul_mat_id(_u8(bank_gu), g.Q4_K, E, sgu, 2 * I, H, x.to(DEV), _u8(ids), g.GATE_UP_SWIGLU)
     assert_close(hb.float().cpu().numpy(), h_ref, TOL_BF16, "gate_up H=512")
-    # precise gate_up: the bf16 h agrees bit for bit with the oracle's except
-    # near rounding ties (fp32 accumulation, ~1e-6 relative: ~0.1% of values)
+    # precise gate_up (tensor-core hi + lo, or the exact block sums of the
+    # vector path): the bf16 h agrees bit for bit with the oracle's except near
+    # rounding ties (fp32 accumulation, ~1e-6 relative: ~0.1% of values)
     same = (hb.float().cpu().numpy() == h_ref)
     assert same.mean() > 0.995, same.mean()
+
+
+# ---------------------------------------------------------------- vector path (few tokens)
+
+class _vec_off:
+    """Runs the block with the tensor-core path for every token count."""
+
+    def __init__(self, g):
+        self.g = g
+
+    def __enter__(self):
+        self.saved = self.g.gguf_get_option("moe_vec_max_tokens")
+        self.g.gguf_set_option("moe_vec_max_tokens", 0)
+
+    def __exit__(self, *a):
+        self.g.gguf_set_option("moe_vec_max_tokens", self.saved)
+
+
+def _q8_1_close(hq, hq_ref, h_ref, active, I):
+    # as in test_gate_up_swiglu_bf16_and_q8_1: each dequantized value within
+    # d/2 of its h on each side, plus one bf16 ulp of h and 2e-3 of the row rms
+    d1 = oracle.q8_1_fields(hq)[0].view(np.float16).astype(np.float64)
+    d0 = oracle.q8_1_fields(hq_ref)[0].view(np.float16).astype(np.float64)
+    v1 = oracle.dequantize_f64(oracle.Q8_1, hq, I)
+    v0 = oracle.dequantize_f64(oracle.Q8_1, hq_ref, I)
+    rms = np.sqrt((h_ref.astype(np.float64) ** 2).mean(axis=1, keepdims=True))
+    bound = (np.repeat(d1, 32, axis=1) + np.repeat(d0, 32, axis=1)) / 2 + np.abs(h_ref) * 2.0 ** -7 + 2e-3 * rms
+    return bool(np.all((np.abs(v1 - v0) <= bound * 1.0001)[active]))
+
+
+@pytest.mark.parametrize("T", [1, 3, 16])
+def test_vec_gate_up_outputs(g, T):
+    E, K, H, I = 5, 3, 512, 128
+    bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 900 + T, False)
+    sgu = bank_gu.nbytes // E
+    ids, _ = synth.routes(T, E, K, seed=T)
+    ids[0, 1] = ids[0, 0]                 # a repeated expert
+    if T > 1:
+        ids[1, 2] = -1                    # an inactive slot
+    x = synth.activations(T, H, seed=T + 1, dtype=torch.bfloat16)
+    xq = oracle.quantize_q8_1(x.float().numpy())
+    h_ref, hq_ref = oracle.moe_gate_up(oracle.Q4_K, bank_gu, E, sgu, 2 * I, H, xq, ids)
+    active = ids.reshape(-1) >= 0
+    args = (_u8(bank_gu), g.Q4_K, E, sgu, 2 * I, H, x.to(DEV), _u8(ids), g.GATE_UP_SWIGLU)
+    hb = g.gguf_mul_mat_id(*args).float().cpu().numpy()
+    assert np.all(hb[~active] == 0)
+    assert_close(hb[active], h_ref[active], TOL_BF16, f"vec gate_up bf16 T {T}")
+    np.testing.assert_array_equal(hb[0], hb[1])
+    hq = g.gguf_mul_mat_id(*args, out_type=g.Q8_1).cpu().numpy()
+    assert np.all(hq[~active] == 0)
+    assert _q8_1_close(hq, hq_ref, h_ref, active, I)
+    # F16: the dequantized q8_1 values d16 * q of the same rows
+    hf = g.gguf_mul_mat_id(*args, out_type=g.F16).float().cpu().numpy()
+    deq = oracle.dequantize_f32(oracle.Q8_1, hq, I).astype(np.float16).astype(np.float32)
+    np.testing.assert_array_equal(hf, deq)
+    # the tensor-core path on the same inputs
+    with _vec_off(g):
+        hb2 = g.gguf_mul_mat_id(*args).float().cpu().numpy()
+    assert_close(hb2[active], hb[active], TOL_BF16, f"vec vs tensor-core gate_up T {T}")
+
+
+@pytest.mark.parametrize("wt", [oracle.Q6_K, oracle.Q4_K, oracle.Q8_0])
+@pytest.mark.parametrize("T", [1, 5, 16])
+def test_vec_down_from_oracle_h(g, wt, T):
+    E, K, H, I = 4, 3, 512, 256
+    bank_d = _bank(wt, E, H, I, 950 + T, False)
+    sd = bank_d.nbytes // E
+    ids, rw = synth.routes(T, E, K, seed=T + 7)
+    ids[0] = [2, 2, 0]
+    if T > 1:
+        ids[1, 1] = -1
+        rw[1, 0] = 0.0
+    hq = oracle.quantize_q8_1(synth.normal((T * K, I), 1.0, seed=T + 8))
+    ref = oracle.moe_down(wt, bank_d, E, sd, H, I, hq, ids, rw)
+    args = (_u8(bank_d), wt, E, sd, H, I, _u8(hq), _u8(ids), g.DOWN_WEIGHTED_SUM)
+    y = g.gguf_mul_mat_id(*args, route_w=_u8(rw), xt=g.Q8_1, out_type=g.F32).cpu().numpy()
+    assert_close(y, ref, TOL_F32, f"vec down type {wt} T {T}")
+    with _vec_off(g):
+        y2 = g.gguf_mul_mat_id(*args, route_w=_u8(rw), xt=g.Q8_1, out_type=g.F32).cpu().numpy()
+    assert_close(y2, ref, TOL_F32, f"tensor-core down type {wt} T {T}")
+
+
+@pytest.mark.parametrize("T", [1, 2, 16])
+@pytest.mark.parametrize("down", [oracle.Q6_K, oracle.Q4_K])
+def test_vec_moe_ffn_end_to_end(g, T, down):
+    E, K, H, I = 6, 4, 256, 256
+    bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 1000 + T, False)
+    bank_d = _bank(down, E, H, I, 1100 + T, False)
+    sgu, sd = bank_gu.nbytes // E, bank_d.nbytes // E
+    ids, rw = synth.routes(T, E, K, seed=T + 20)
+    ids[0, :2] = [3, 3]
+    if T > 1:
+        ids[1, 0] = -1
+        ids[1, 1] = E + 2              # out of range: inactive, counted
+        rw[1, 2] = 0.0
+    x = synth.activations(T, H, seed=T + 21, dtype=torch.bfloat16)
+    xq = oracle.quantize_q8_1(x.float().numpy())
+    _, hq = oracle.moe_gate_up(oracle.Q4_K, bank_gu, E, sgu, 2 * I, H, xq, ids)
+    ref = oracle.moe_down(down, bank_d, E, sd, H, I, hq, ids, rw)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    args = (_u8(bank_gu), g.Q4_K, sgu, _u8(bank_d), down, sd, E, H, I, x.to(DEV), _u8(ids), _u8(rw))
+    y = g.gguf_moe_ffn(*args, dev_status=status).float().cpu().numpy()
+    assert_close_moe_e2e(y, ref, f"vec moe ffn T {T} down {down}")
+    assert int(status.item()) == (1 if T > 1 else 0)
+    with _vec_off(g):
+        y2 = g.gguf_moe_ffn(*args).float().cpu().numpy()
+    assert_close_moe_e2e(y2, ref, f"tensor-core moe ffn T {T} down {down}")
+
+
+def test_vec_moe_full_size_decode(g):
+    # the full-size expert banks (E = 256, top-8, H = 2048, I = 512) at 16
+    # decode tokens through the vector path, every token against the oracle
+    E, K, H, I, T = 256, 8, 2048, 512, 16
+    bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 700, True)
+    bank_d = _bank(oracle.Q6_K, E, H, I, 701, True)
+    sgu, sd = bank_gu.nbytes // E, bank_d.nbytes // E
+    ids, rw = synth.routes(T, E, K, seed=3)
+    x = synth.activations(T, H, seed=4, dtype=torch.bfloat16)
+    y = g.gguf_moe_ffn(_u8(bank_gu), g.Q4_K, sgu, _u8(bank_d), g.Q6_K, sd, E, H, I, x.to(DEV), _u8(ids), _u8(rw))
+    y = y.float().cpu().numpy()
+    xq = oracle.quantize_q8_1(x.float().numpy())
+    _, hq = oracle.moe_gate_up(oracle.Q4_K, bank_gu, E, sgu, 2 * I, H, xq, ids, nthreads=8)
+    ref = oracle.moe_down(oracle.Q6_K, bank_d, E, sd, H, I, hq, ids, rw, nthreads=8)
+    assert_close_moe_e2e(y, ref, "vec moe full size")
