@@ -473,6 +473,26 @@ def secondary(torch, g, synth, dev, stream, hbm_peak, tf_peak, peak_kind):
             "frac_of_int8_mma_peak": round(ops / (ms * 1e-3) / 1e12 / p_int8, 3),
             "note": "routed-row int8-equivalent ops 2*T*top_k*(2I*H + H*I) / time; gate_up Q4_K + SwiGLU + q8_1, "
                     "down Q6_K + weighted sum"}
+        # the same expert block at decode token counts: the route-batched MMVQ path (each routed
+        # expert's rows read once per route); GB/s of the routed experts' packed weights
+        for Td in (1, 16):
+            ids_np, rw_np = synth.routes(Td, E, K_, seed=11 + Td)
+            ids_d, rw_d = torch.from_numpy(ids_np).to(dev), torch.from_numpy(rw_np).to(dev)
+            xd = synth.activations(Td, H, seed=12, dtype=torch.bfloat16).to(dev)
+            yd = torch.empty((Td, H), dtype=torch.bfloat16, device=dev)
+            args_d = g.moe_ffn_args(wgu, g.Q4_K, gu_stride, wdn, g.Q6_K, dn_stride, E, H, I, xd, g.BF16, ids_d, K_,
+                                    rw_d, yd, g.BF16, None)
+            ws_d = torch.empty(max(g.gguf_moe_ffn_ws_size(args_d), 16), dtype=torch.uint8, device=dev)
+
+            def moe_dec():
+                g.gguf_moe_ffn(wgu, g.Q4_K, gu_stride, wdn, g.Q6_K, dn_stride, E, H, I, xd, ids_d, rw_d, out=yd,
+                               ws=ws_d)
+            ms = _time_eager(torch, stream, moe_dec, 20, flush)
+            routed = Td * K_ * (gu_stride + dn_stride)   # each route reads its expert's matrices once
+            out[f"moe_ffn_decode_e256_top8_t{Td}"] = {
+                "us": round(ms * 1e3, 2), "routed_weight_mb": round(routed / 1e6, 2),
+                "gbs": round(routed / (ms * 1e-3) / 1e9, 1), "frac": round(routed / (ms * 1e-3) / 1e9 / hbm_peak, 3),
+                "note": "route-batched MMVQ path (quantize, route marks, gate_up, SwiGLU, q8_1, down, weighted sum)"}
         del wgu, wdn, x, y, ws
 
         # dequantize (a whole Q4_K / Q6_K matrix to bf16) and get_rows (8192 random rows of a Q6_K

@@ -55,6 +55,8 @@ __global__ void moe_count_kernel(const int32_t *__restrict__ ids, const float *_
 // -1 for a skipped one (same rules as moe_count_kernel; no grouping needed)
 __global__ void moe_mark_kernel(const int32_t *__restrict__ ids, const float *__restrict__ rw, int64_t R, int64_t E,
                                 int skip_zero_w, int32_t *__restrict__ pos, int32_t *__restrict__ dev_status) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= R) return;
     const int32_t e = ids[r];
@@ -128,6 +130,8 @@ template <int V>
 __global__ void moe_finalize_kernel(const float *__restrict__ z, const int32_t *__restrict__ pos,
                                     const float *__restrict__ route_w, int64_t T, int64_t top_k, int64_t n,
                                     void *__restrict__ y, int yt) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // z comes from the previous kernel
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * V;
     if (i >= T * n) return;
     const int64_t t = i / n, c = i - t * n;
@@ -157,6 +161,8 @@ __global__ void moe_finalize_kernel(const float *__restrict__ z, const int32_t *
 // of the tensor-core epilogue), rounded to bf16, the activation dtype
 __global__ void moe_swiglu_kernel(const float *__restrict__ z, const int32_t *__restrict__ pos, int64_t R, int64_t I,
                                   uint16_t *__restrict__ h) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // z comes from the previous kernel
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= R * I) return;
     const int64_t r = i / I, j = i - r * I;
@@ -169,6 +175,22 @@ __global__ void moe_swiglu_kernel(const float *__restrict__ z, const int32_t *__
 }
 
 // ---------------------------------------------------------------- host side
+
+// a 1-D launch that may start while the previous kernel of the stream
+// finishes (the kernel waits on griddepcontrol before reading its inputs)
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kern)(KArgs...), int64_t blocks, unsigned threads, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 static size_t a256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -300,24 +322,20 @@ cudaError_t launch_moe_finalize(const float *z, const int32_t *pos, const float 
     const int64_t count = T * n;
     if (count == 0) return cudaSuccess;
     if (n % 4 == 0)   // z rows are 16-byte aligned (workspace base 256-aligned, n % 4 == 0)
-        moe_finalize_kernel<4><<<(unsigned)((count / 4 + 255) / 256), 256, 0, s>>>(z, pos, route_w, T, top_k, n, y, yt);
-    else
-        moe_finalize_kernel<1><<<(unsigned)((count + 255) / 256), 256, 0, s>>>(z, pos, route_w, T, top_k, n, y, yt);
-    return cudaGetLastError();
+        return launch_pdl(moe_finalize_kernel<4>, (count / 4 + 255) / 256, 256, s, z, pos, route_w, T, top_k, n, y, yt);
+    return launch_pdl(moe_finalize_kernel<1>, (count + 255) / 256, 256, s, z, pos, route_w, T, top_k, n, y, yt);
 }
 
 cudaError_t launch_moe_swiglu(const float *z, const int32_t *pos, int64_t R, int64_t I, uint16_t *h, cudaStream_t s) {
     const int64_t count = R * I;
     if (count == 0) return cudaSuccess;
-    moe_swiglu_kernel<<<(unsigned)((count + 255) / 256), 256, 0, s>>>(z, pos, R, I, h);
-    return cudaGetLastError();
+    return launch_pdl(moe_swiglu_kernel, (count + 255) / 256, 256, s, z, pos, R, I, h);
 }
 
 cudaError_t moe_mark(const int32_t *ids, const float *rw, int64_t R, int64_t E, bool skip_zero_w, int32_t *status,
                      int32_t *pos, cudaStream_t s) {
     if (R == 0) return cudaSuccess;
-    moe_mark_kernel<<<(unsigned)((R + 255) / 256), 256, 0, s>>>(ids, rw, R, E, skip_zero_w ? 1 : 0, pos, status);
-    return cudaGetLastError();
+    return launch_pdl(moe_mark_kernel, (R + 255) / 256, 256, s, ids, rw, R, E, skip_zero_w ? 1 : 0, pos, status);
 }
 
 }  // namespace gg
