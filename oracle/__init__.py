@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gguf_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libgguf_oracle.so")
 
-F32, F16, Q8_0, Q8_1, Q4_K, Q6_K, BF16 = 0, 1, 8, 9, 12, 14, 30
+F32, F16, Q4_0, Q8_0, Q8_1, Q4_K, Q5_K, Q6_K, BF16 = 0, 1, 2, 8, 9, 12, 13, 14, 30
 
 
 def build(force: bool = False) -> str:

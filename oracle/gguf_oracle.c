@@ -1,6 +1,6 @@
 /*
  * gguf_oracle.c -- plain, slow, scalar CPU oracle for the GGUF block-quantized
- * matmul path (q8_1 activations x Q8_0 / Q4_K / Q6_K weights).
+ * matmul path (q8_1 activations x Q8_0 / Q4_0 / Q4_K / Q5_K / Q6_K weights).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or runs
  * this file: only tests/, __graft_entry__.smoke() and the cpu_baseline leg of
@@ -25,14 +25,21 @@
  *
  * Readings where the pages are silent (the pages name the formats but never
  * print their bytes):
- *  - Byte layouts of Q8_0 / q8_1 / Q4_K / Q6_K follow the public GGUF
+ *  - Q4_0 and Q5_K are two of the further tensor types the pages list
+ *    (FreeToken PR #690, "Tensor types"; transformers PR #45977, supported
+ *    quant types of GgufLinear).
+ *  - Byte layouts of Q8_0 / q8_1 / Q4_0 / Q4_K / Q5_K / Q6_K follow the public GGUF
  *    convention, so that blocks stay GGUF-compatible.  Layout parity with real
  *    GGUF files is unpinned (no GGUF file or gguf-py exists here); everything
  *    else is pinned by the tests in tests/test_oracle_*.py.
  *  - q8_1: d = amax / 127 (one IEEE fp32 division), q = roundf(x / d) (half
  *    away from zero), s = fp16(d * (float)sum(q)) with the fp32 d.
- *  - dequantized value order: Q4_K  a = d*s; b = dmin*m; v = a*q - b;
- *                             Q6_K  v = (d*sc) * (q - 32);   Q8_0  v = d*q.
+ *  - dequantized value order: Q4_K, Q5_K  a = d*s; b = dmin*m; v = a*q - b;
+ *                             Q6_K  v = (d*sc) * (q - 32);   Q8_0  v = d*q;
+ *                             Q4_0  v = d * (q - 8).
+ *  - block dots: symmetric formats with an integer offset (Q4_0: 8, Q6_K: 32)
+ *    take the offset into the exact integer sum; affine formats with a float
+ *    min (Q4_K, Q5_K) combine the min with the activation block's stored s.
  *  - matmul reference: the blockwise formula evaluated in fp64 on the stored
  *    (fp16) fields, e.g. Q4_K y = sum_j (d*s_j*d_a*S_j - dmin*m_j*s_a).
  *  - weight quantizers (test-input generators only; the GPU never quantizes
@@ -127,8 +134,8 @@ static void wr16(uint8_t *p, uint16_t v) { p[0] = (uint8_t)(v & 0xff); p[1] = (u
 int64_t orc_block_elems(int type) {
     switch (type) {
     case ORC_F32: case ORC_F16: case ORC_BF16: return 1;
-    case ORC_Q8_0: case ORC_Q8_1: return 32;
-    case ORC_Q4_K: case ORC_Q6_K: return 256;
+    case ORC_Q8_0: case ORC_Q8_1: case ORC_Q4_0: return 32;
+    case ORC_Q4_K: case ORC_Q5_K: case ORC_Q6_K: return 256;
     default: return 0;
     }
 }
@@ -139,7 +146,9 @@ int64_t orc_block_bytes(int type) {
     case ORC_F16: case ORC_BF16: return 2;
     case ORC_Q8_0: return 34;  /* fp16 d, int8 q[32] */
     case ORC_Q8_1: return 36;  /* fp16 d, fp16 s, int8 q[32] */
+    case ORC_Q4_0: return 18;  /* fp16 d, u8 qs[16] */
     case ORC_Q4_K: return 144; /* fp16 d, fp16 dmin, u8 scales[12], u8 qs[128] */
+    case ORC_Q5_K: return 176; /* fp16 d, fp16 dmin, u8 scales[12], u8 qh[32], u8 qs[128] */
     case ORC_Q6_K: return 210; /* u8 ql[128], u8 qh[64], i8 scales[16], fp16 d */
     default: return 0;
     }
@@ -154,7 +163,7 @@ int64_t orc_row_size(int type, int64_t k) {
 /* sub-block length of the per-block integer dot products */
 int64_t orc_sub_elems(int type) {
     switch (type) {
-    case ORC_Q8_0: case ORC_Q4_K: return 32;
+    case ORC_Q8_0: case ORC_Q4_0: case ORC_Q4_K: case ORC_Q5_K: return 32;
     case ORC_Q6_K: return 16;
     default: return 0;
     }
@@ -196,6 +205,28 @@ static int q4_k_q(const uint8_t *b, int i) {
     int c = i / 64, r = i % 64;
     uint8_t byte = qs[32 * c + (r % 32)];
     return r < 32 ? (byte & 15) : (byte >> 4);
+}
+
+/* Q4_0 block: 32 unsigned 4-bit quants; byte qs[l] (l = 0..15) holds value l
+ * in its low nibble and value l + 16 in its high nibble; value = d * (q - 8). */
+static float q4_0_d(const uint8_t *b) { return orc_f16_to_f32(rd16(b)); }
+static int q4_0_q(const uint8_t *b, int i) {
+    uint8_t byte = b[2 + (i % 16)];
+    return i < 16 ? (byte & 15) : (byte >> 4);
+}
+
+/* Q5_K super-block: the header (d, dmin, 12 scale bytes) is packed exactly as
+ * Q4_K's, so q4_k_d / q4_k_dmin / q4_k_scale_min read it too.  Value i takes
+ * its low 4 bits from qs (at byte 48) as Q4_K takes its quant from qs at 16,
+ * and its fifth bit from qh[i % 32] (at byte 16), bit i / 32 -- the sub-block
+ * index.  q in 0..31; value = d*s_j*q - dmin*m_j.                           */
+static int q5_k_q(const uint8_t *b, int i) {
+    const uint8_t *qs = b + 48, *qh = b + 16;
+    int c = i / 64, r = i % 64;
+    uint8_t byte = qs[32 * c + (r % 32)];
+    int lo = r < 32 ? (byte & 15) : (byte >> 4);
+    int hi = (qh[i % 32] >> (i / 32)) & 1;
+    return lo | (hi << 4);
 }
 
 /* Q6_K super-block.  Half h = i / 128 uses ql + 64h, qh + 32h, sc + 8h.  For
@@ -331,6 +362,84 @@ static void quantize_block_q4_k(const float *x, uint8_t *out) {
     }
 }
 
+/* Q4_0: the value v of largest magnitude sets d = v / -8 (so that v maps to
+ * q - 8 = -8); q = clamp(roundf(x / d) + 8, 0, 15) with the stored (fp16) d. */
+static void quantize_block_q4_0(const float *x, uint8_t *out) {
+    float amax = 0.0f, vmax = 0.0f;
+    for (int i = 0; i < 32; i++) {
+        float a = fabsf(x[i]);
+        if (a > amax) { amax = a; vmax = x[i]; }
+    }
+    uint16_t dh = orc_f32_to_f16(vmax / -8.0f);
+    float df = orc_f16_to_f32(dh);
+    memset(out, 0, 18);
+    wr16(out, dh);
+    for (int i = 0; i < 32; i++) {
+        int q = 8;
+        if (df != 0.0f) q = (int)roundf(x[i] / df) + 8;
+        if (q < 0) q = 0;
+        if (q > 15) q = 15;
+        out[2 + (i % 16)] |= (uint8_t)(i < 16 ? q : q << 4);
+    }
+}
+
+/* Q5_K: as Q4_K with 32 levels: scale_j = (hi - lo) / 31, q in 0..31, the low
+ * 4 bits packed as Q4_K's quants (at byte 48) and bit 4 of value i set as bit
+ * i / 32 of qh[i % 32].                                                      */
+static void quantize_block_q5_k(const float *x, uint8_t *out) {
+    float scale[8], minv[8];
+    float maxscale = 0.0f, maxmin = 0.0f;
+    for (int j = 0; j < 8; j++) {
+        float lo = 0.0f, hi = x[32 * j];
+        for (int i = 0; i < 32; i++) {
+            float v = x[32 * j + i];
+            if (v < lo) lo = v;
+            if (v > hi) hi = v;
+        }
+        scale[j] = (hi - lo) / 31.0f;
+        minv[j] = -lo;
+        if (scale[j] > maxscale) maxscale = scale[j];
+        if (minv[j] > maxmin) maxmin = minv[j];
+    }
+    float d = maxscale / 63.0f, dmin = maxmin / 63.0f;
+    int s6[8], m6[8];
+    for (int j = 0; j < 8; j++) {
+        int s = d > 0.0f ? (int)roundf(scale[j] / d) : 0;
+        int m = dmin > 0.0f ? (int)roundf(minv[j] / dmin) : 0;
+        s6[j] = s > 63 ? 63 : s;
+        m6[j] = m > 63 ? 63 : m;
+    }
+    uint16_t dh = orc_f32_to_f16(d), dminh = orc_f32_to_f16(dmin);
+    float df = orc_f16_to_f32(dh), dminf = orc_f16_to_f32(dminh);
+    memset(out, 0, 176);
+    wr16(out, dh);
+    wr16(out + 2, dminh);
+    uint8_t *sc = out + 4;
+    for (int j = 0; j < 8; j++) {
+        if (j < 4) {
+            sc[j] |= (uint8_t)s6[j];
+            sc[j + 4] |= (uint8_t)m6[j];
+        } else {
+            sc[j + 4] |= (uint8_t)((s6[j] & 15) | ((m6[j] & 15) << 4));
+            sc[j - 4] |= (uint8_t)((s6[j] >> 4) << 6);
+            sc[j] |= (uint8_t)((m6[j] >> 4) << 6);
+        }
+    }
+    uint8_t *qh = out + 16, *qs = out + 48;
+    for (int i = 0; i < 256; i++) {
+        int j = i / 32;
+        float denom = df * (float)s6[j];
+        int q = 0;
+        if (denom > 0.0f) q = (int)roundf((x[i] + dminf * (float)m6[j]) / denom);
+        if (q < 0) q = 0;
+        if (q > 31) q = 31;
+        int c = i / 64, r = i % 64;
+        if (r < 32) qs[32 * c + r] |= (uint8_t)(q & 15);
+        else qs[32 * c + r - 32] |= (uint8_t)((q & 15) << 4);
+        qh[i % 32] |= (uint8_t)((q >> 4) << (i / 32));
+    }
+}
+
 /* Q6_K: per sub-block j of 16, scale_j = amax_j / 31; d = max scale / 127;
  * sc_j = roundf(scale_j / d); q = clamp(roundf(x / (d_h * sc_j)), -32, 31) + 32. */
 static void quantize_block_q6_k(const float *x, uint8_t *out) {
@@ -385,7 +494,9 @@ int orc_quantize_weights(int type, const float *w, int64_t n, int64_t k, uint8_t
             uint8_t *o = out + r * rs + b * bb;
             switch (type) {
             case ORC_Q8_0: quantize_block_q8_0(x, o); break;
+            case ORC_Q4_0: quantize_block_q4_0(x, o); break;
             case ORC_Q4_K: quantize_block_q4_k(x, o); break;
+            case ORC_Q5_K: quantize_block_q5_k(x, o); break;
             case ORC_Q6_K: quantize_block_q6_k(x, o); break;
             case ORC_Q8_1: orc_quantize_q8_1_block(x, o); break;
             default: return -1;
@@ -409,6 +520,14 @@ static float dequant_value(int type, const uint8_t *blk, int i) {
         float a = q4_k_d(blk) * (float)s;
         float b = q4_k_dmin(blk) * (float)m;
         return a * (float)q4_k_q(blk, i) - b;
+    }
+    case ORC_Q4_0: return q4_0_d(blk) * (float)(q4_0_q(blk, i) - 8);
+    case ORC_Q5_K: {
+        int s, m;
+        q4_k_scale_min(blk, i / 32, &s, &m);
+        float a = q4_k_d(blk) * (float)s;
+        float b = q4_k_dmin(blk) * (float)m;
+        return a * (float)q5_k_q(blk, i) - b;
     }
     case ORC_Q6_K: {
         float a = q6_k_d(blk) * (float)q6_k_scale(blk, i);
@@ -435,6 +554,12 @@ static double dequant_value_f64(int type, const uint8_t *blk, int i) {
         int s, m;
         q4_k_scale_min(blk, i / 32, &s, &m);
         return (double)q4_k_d(blk) * s * q4_k_q(blk, i) - (double)q4_k_dmin(blk) * m;
+    }
+    case ORC_Q4_0: return (double)q4_0_d(blk) * (q4_0_q(blk, i) - 8);
+    case ORC_Q5_K: {
+        int s, m;
+        q4_k_scale_min(blk, i / 32, &s, &m);
+        return (double)q4_k_d(blk) * s * q5_k_q(blk, i) - (double)q4_k_dmin(blk) * m;
     }
     case ORC_Q6_K: return (double)q6_k_d(blk) * q6_k_scale(blk, i) * (q6_k_q(blk, i) - 32);
     default: return NAN;
@@ -504,7 +629,9 @@ static int32_t block_dot(int type, const uint8_t *wb, int64_t first, const uint8
         int qw;
         switch (type) {
         case ORC_Q8_0: qw = q8_0_q(wb, i); break;
+        case ORC_Q4_0: qw = q4_0_q(wb, i) - 8; break;
         case ORC_Q4_K: qw = q4_k_q(wb, i); break;
+        case ORC_Q5_K: qw = q5_k_q(wb, i); break;
         case ORC_Q6_K: qw = q6_k_q(wb, i) - 32; break;
         default: qw = 0;
         }
@@ -535,8 +662,8 @@ int orc_block_dots(int type, const uint8_t *w, int64_t n, int64_t k, const uint8
 /* ------------------------------------------------------------------------ */
 
 /* y = sum over the row's sub-blocks of the combination of stored fields:
- *   Q8_0: d_w * d_a * S
- *   Q4_K: d * s_j * d_a * S_j - dmin * m_j * s_a
+ *   Q8_0, Q4_0: d_w * d_a * S      (Q4_0: S over q - 8)
+ *   Q4_K, Q5_K: d * s_j * d_a * S_j - dmin * m_j * s_a
  *   Q6_K: d * sc_j * d_a * S_j
  * with d_a, s_a the q8_1 fields of the 32-block holding sub-block j.         */
 static double dot_row(int type, const uint8_t *wrow, int64_t k, const uint8_t *xrow) {
@@ -551,7 +678,9 @@ static double dot_row(int type, const uint8_t *wrow, int64_t k, const uint8_t *x
             double S = block_dot(type, wb, b * be, xrow, j);
             if (type == ORC_Q8_0) {
                 y += (double)q8_0_d(wb) * da * S;
-            } else if (type == ORC_Q4_K) {
+            } else if (type == ORC_Q4_0) {
+                y += (double)q4_0_d(wb) * da * S;
+            } else if (type == ORC_Q4_K || type == ORC_Q5_K) {
                 int s, m;
                 q4_k_scale_min(wb, j, &s, &m);
                 y += (double)q4_k_d(wb) * s * da * S - (double)q4_k_dmin(wb) * m * sa;

@@ -85,7 +85,9 @@ def _parse_blocks(name):
 
 
 @pytest.mark.parametrize("fname,tname,k", [("q8_0_hand_block.txt", "Q8_0", 32),
+                                           ("q4_0_hand_blocks.txt", "Q4_0", 32),
                                            ("q4_k_hand_blocks.txt", "Q4_K", 256),
+                                           ("q5_k_hand_blocks.txt", "Q5_K", 256),
                                            ("q6_k_hand_blocks.txt", "Q6_K", 256)])
 def test_hand_built_blocks(orc, fname, tname, k):
     t = getattr(orc, tname)
@@ -238,6 +240,59 @@ def test_q6_k_roundtrip_bound_and_codes(orc):
     assert lows == set(range(16)) and highs == set(range(4))
 
 
+def test_q4_0_roundtrip_bound_and_codes(orc):
+    w = synth.normal((32, 1024), 0.02, seed=8) * synth.lognormal_row_scale(32, seed=9)
+    p = orc.quantize_weights(orc.Q4_0, w)
+    dq = orc.dequantize_f32(orc.Q4_0, p, 1024).reshape(32, 32, 32).astype(np.float64)
+    wb = w.reshape(32, 32, 32).astype(np.float64)
+    blocks = p.reshape(32, 32, 18)
+    dh = np.abs(blocks[:, :, 0:2].copy().view(np.float16)[..., 0].astype(np.float64))[..., None]
+    err = np.abs(dq - wb)
+    # codes 0..15 are q - 8 = -8..7: the extreme value v sets d = v / -8, so every
+    # value lies within 8 steps of 0 (fp16 d: 2^-11 relative); values that do
+    # not reach the +8 side are rounded to the nearest step (half a step), those
+    # beyond +7.5 steps are clamped to +7 (at most 1 + 2^-9 steps)
+    assert np.all(err <= dh * (1.0 + 2.0 ** -9) + 1e-30)
+    r = np.abs(wb) / np.where(dh == 0, 1, dh)
+    inner = r < 7.4
+    assert np.all(err[inner] <= 0.5 * dh.repeat(32, axis=2)[inner] * (1 + 1e-6))
+    # the extreme value of each block is reproduced up to the fp16 rounding of d
+    amax = np.abs(wb).max(axis=2)
+    ext = np.take_along_axis(dq, np.abs(wb).argmax(axis=2)[..., None], axis=2)[..., 0]
+    assert np.all(np.abs(np.abs(ext) - amax) <= amax * 2.0 ** -11 * 1.001)
+    qs = blocks[:, :, 2:]
+    codes = set(np.unique(qs & 15)) | set(np.unique(qs >> 4))
+    assert codes == set(range(16))
+
+
+def test_q5_k_roundtrip_bound_and_codes(orc):
+    w = synth.normal((64, 2048), 0.02, seed=10) * synth.lognormal_row_scale(64, seed=12)
+    p = orc.quantize_weights(orc.Q5_K, w)
+    dq = orc.dequantize_f32(orc.Q5_K, p, 2048)
+    wb = w.reshape(64, 8, 8, 32)
+    lo = np.minimum(0, wb.min(axis=3))
+    step = (wb.max(axis=3) - lo) / 31.0
+    # as for Q4_K, with 31 steps per sub-block
+    d = step.max(axis=2, keepdims=True) / 63.0
+    dmin = (-lo).max(axis=2, keepdims=True) / 63.0
+    ed, edm = np.maximum(d * 2.0 ** -11, 2.0 ** -25), np.maximum(dmin * 2.0 ** -11, 2.0 ** -25)
+    grid_off = 0.5 * d + 63 * ed
+    min_off = 0.5 * dmin + 63 * edm
+    bound = 0.5 * (step + grid_off) + 31 * grid_off + min_off
+    err = np.abs(dq.reshape(64, 8, 8, 32) - wb).max(axis=3)
+    assert np.all(err <= bound * 1.001)
+    # the fifth bit halves the Q4_K step: the mean error is well below Q4_K's
+    e4 = np.abs(orc.dequantize_f32(orc.Q4_K, orc.quantize_weights(orc.Q4_K, w), 2048) - w).mean()
+    assert np.abs(dq - w).mean() < 0.6 * e4
+    blocks = p.reshape(-1, 176)
+    qh, qs = blocks[:, 16:48], blocks[:, 48:]
+    codes = set()
+    for j in range(8):
+        nib = (qs[:, 32 * (j // 2):32 * (j // 2) + 32] >> (4 * (j % 2))) & 15
+        codes |= set(np.unique(nib | (((qh >> j) & 1) << 4)))
+    assert codes == set(range(32))
+
+
 def test_layout_each_quant_nibble_moves_one_value(orc):
     """Perturbing one quant field changes exactly one dequantized value, and
     across a block every value is hit once (pins that the layout is a bijection)."""
@@ -260,6 +315,37 @@ def test_layout_each_quant_nibble_moves_one_value(orc):
                 assert changed.size == 1, (t, pos, shift, changed)
                 hit[changed[0]] += 1
         assert np.all(hit == 1), t
+    # Q4_0: the low bit of each nibble of qs moves exactly one of the 32 values
+    base = bytearray(18)
+    base[0:2] = bytes.fromhex("003c")
+    ref = orc.dequantize_f32(orc.Q4_0, np.frombuffer(bytes(base), np.uint8).reshape(1, -1), 32)[0]
+    hit = np.zeros(32, dtype=np.int32)
+    for pos in range(2, 18):
+        for shift in (0, 4):
+            b = bytearray(base)
+            b[pos] ^= (1 << shift)
+            v = orc.dequantize_f32(orc.Q4_0, np.frombuffer(bytes(b), np.uint8).reshape(1, -1), 32)[0]
+            changed = np.nonzero(v != ref)[0]
+            assert changed.size == 1
+            hit[changed[0]] += 1
+    assert np.all(hit == 1)
+    # Q5_K: each nibble of qs and each bit of qh moves exactly one value; each
+    # set covers all 256 values once
+    base = bytearray(176)
+    base[0:2] = bytes.fromhex("003c")
+    base[4:16] = bytes([1, 1, 1, 1, 0, 0, 0, 0, 1, 1, 1, 1])
+    ref = orc.dequantize_f32(orc.Q5_K, np.frombuffer(bytes(base), np.uint8).reshape(1, -1), 256)[0]
+    for positions, bits in [(range(48, 176), (0, 4)), (range(16, 48), range(8))]:
+        hit = np.zeros(256, dtype=np.int32)
+        for pos in positions:
+            for bit in bits:
+                b = bytearray(base)
+                b[pos] ^= (1 << bit)
+                v = orc.dequantize_f32(orc.Q5_K, np.frombuffer(bytes(b), np.uint8).reshape(1, -1), 256)[0]
+                changed = np.nonzero(v != ref)[0]
+                assert changed.size == 1, (pos, bit, changed)
+                hit[changed[0]] += 1
+        assert np.all(hit == 1)
     # Q6_K high-bit bytes: each 2-bit pair moves exactly one value
     base = bytearray(210)
     base[192:208] = bytes([1] * 16)
@@ -278,7 +364,7 @@ def test_layout_each_quant_nibble_moves_one_value(orc):
 
 
 def test_dequantize_out_dtypes_are_rne(orc):
-    for t, k in [(orc.Q8_0, 256), (orc.Q4_K, 512), (orc.Q6_K, 512)]:
+    for t, k in [(orc.Q8_0, 256), (orc.Q4_0, 256), (orc.Q4_K, 512), (orc.Q5_K, 512), (orc.Q6_K, 512)]:
         p = synth.safe_blocks(t, 16, k, seed=21)
         f = orc.dequantize(t, p, k, orc.F32)
         h = orc.dequantize(t, p, k, orc.F16)
@@ -286,7 +372,7 @@ def test_dequantize_out_dtypes_are_rne(orc):
         np.testing.assert_array_equal(h, f.astype(np.float16).view(np.uint16))
         np.testing.assert_array_equal(b, torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
         # the fp32 values are exact: they equal the fp64 evaluation of the same fields
-        np.testing.assert_array_equal(f.astype(np.float64), orc.dequantize_f64(t, p, k)) if t != orc.Q4_K else None
+        np.testing.assert_array_equal(f.astype(np.float64), orc.dequantize_f64(t, p, k)) if t not in (orc.Q4_K, orc.Q5_K) else None
 
 
 def test_get_rows_is_row_gather_of_dequantize(orc):

@@ -18,9 +18,9 @@ from gguf_block_quantized_quantize_gb300 import synth
 def _unit_scale_blocks(orc, t, n, k, seed):
     """Random quants with every scale 1 (and min 0): dequant == the raw quants."""
     p = synth.safe_blocks(t, n, k, seed).reshape(n, -1, orc.block_bytes(t)).copy()
-    if t == orc.Q8_0:
+    if t in (orc.Q8_0, orc.Q4_0):
         p[:, :, 0:2] = [0x00, 0x3C]
-    elif t == orc.Q4_K:
+    elif t in (orc.Q4_K, orc.Q5_K):
         p[:, :, 0:4] = [0x00, 0x3C, 0x00, 0x00]
         p[:, :, 4:16] = [1, 1, 1, 1, 0, 0, 0, 0, 1, 1, 1, 1]
     elif t == orc.Q6_K:
@@ -29,12 +29,12 @@ def _unit_scale_blocks(orc, t, n, k, seed):
     return np.ascontiguousarray(p.reshape(n, -1))
 
 
-@pytest.mark.parametrize("tname", ["Q8_0", "Q4_K", "Q6_K"])
+@pytest.mark.parametrize("tname", ["Q8_0", "Q4_0", "Q4_K", "Q5_K", "Q6_K"])
 def test_block_dots_brute_force(orc, tname):
     t = getattr(orc, tname)
     k, n, m = 512, 6, 3
     w = _unit_scale_blocks(orc, t, n, k, seed=31)
-    qw = orc.dequantize_f32(t, w, k).astype(np.int64)      # raw quants (q, q or q-32)
+    qw = orc.dequantize_f32(t, w, k).astype(np.int64)      # raw quants (q, q - 8, q or q - 32)
     assert np.all(qw == orc.dequantize_f32(t, w, k))      # integral
     xq = orc.quantize_q8_1(synth.normal((m, k), 1.0, seed=32))
     _, _, qa = orc.q8_1_fields(xq)
@@ -53,7 +53,7 @@ def test_block_dots_brute_force(orc, tname):
         assert np.all(got == 32 * 127 * 127)
 
 
-@pytest.mark.parametrize("tname", ["Q8_0", "Q6_K"])
+@pytest.mark.parametrize("tname", ["Q8_0", "Q4_0", "Q6_K"])
 def test_blockwise_equals_dequant_dot(orc, tname):
     t = getattr(orc, tname)
     k = 1024
@@ -66,19 +66,21 @@ def test_blockwise_equals_dequant_dot(orc, tname):
     assert np.all(np.abs(y - ref) <= 1e-13 * scale)
 
 
-def test_blockwise_q4_k_min_term(orc):
-    """Q4_K: blockwise y = dequant-dot + sum_j dmin*m_j*(d_a*sum(q_a) - s_a), and the
-    difference is bounded by the fp16 rounding of d_a and s_a."""
+@pytest.mark.parametrize("tname", ["Q4_K", "Q5_K"])
+def test_blockwise_affine_min_term(orc, tname):
+    """Q4_K / Q5_K: blockwise y = dequant-dot + sum_j dmin*m_j*(d_a*sum(q_a) - s_a),
+    and the difference is bounded by the fp16 rounding of d_a and s_a."""
+    t = getattr(orc, tname)
     k = 1024
-    w = synth.safe_blocks(orc.Q4_K, 16, k, seed=43)
+    w = synth.safe_blocks(t, 16, k, seed=43)
     xq = orc.quantize_q8_1(synth.normal((4, k), 1.0, seed=44))
-    y = orc.mul_mat(orc.Q4_K, w, k, xq)
-    ref = orc.mul_mat_dequant_f64(orc.Q4_K, w, k, xq)
+    y = orc.mul_mat(t, w, k, xq)
+    ref = orc.mul_mat_dequant_f64(t, w, k, xq)
     # bound: |d_a sum q - s_a| <= |sum q| * |d_a| * 2^-10 per 32-block (two fp16 roundings)
     dbits, sbits, qa = orc.q8_1_fields(xq)
     da = dbits.view(np.float16).astype(np.float64)
     qsum = np.abs(qa.astype(np.int64).sum(axis=2))
-    blk = w.reshape(16, -1, 144)
+    blk = w.reshape(16, -1, orc.block_bytes(t))
     dmin = blk[:, :, 2:4].copy().view(np.float16)[..., 0].astype(np.float64)   # [n, nsb]
     per_block = (qsum * np.abs(da) * 2.0 ** -10 + 1e-300)                       # [m, k/32]
     bound = (per_block.reshape(4, 1, -1, 8).sum(axis=3) * dmin[None] * 63).sum(axis=2)
@@ -86,7 +88,8 @@ def test_blockwise_q4_k_min_term(orc):
     assert np.abs(y - ref).max() > 0        # the term is real, not identically zero
 
 
-@pytest.mark.parametrize("tname,tol", [("Q8_0", 0.02), ("Q4_K", 0.15), ("Q6_K", 0.05)])
+@pytest.mark.parametrize("tname,tol", [("Q8_0", 0.02), ("Q4_0", 0.12), ("Q4_K", 0.15), ("Q5_K", 0.08),
+                                       ("Q6_K", 0.05)])
 def test_quantized_matmul_tracks_fp32(orc, tname, tol):
     t = getattr(orc, tname)
     k = 2048
