@@ -17,6 +17,8 @@ constexpr int Q8_0_BYTES = 34;     // fp16 d, int8 q[32]
 constexpr int Q8_1_BYTES = 36;     // fp16 d, fp16 s, int8 q[32]
 constexpr int Q4_K_BYTES = 144;    // fp16 d, fp16 dmin, scales[12], qs[128]
 constexpr int Q6_K_BYTES = 210;    // ql[128], qh[64], scales[16], fp16 d
+constexpr int Q4_0_BYTES = 18;     // fp16 d, qs[16] (value l low nibble, l + 16 high)
+constexpr int Q5_K_BYTES = 176;    // fp16 d, fp16 dmin, scales[12], qh[32], qs[128]
 
 __device__ __forceinline__ float h2f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
@@ -45,6 +47,25 @@ __device__ __forceinline__ uint16_t ld_u16(const uint8_t *p) { return *reinterpr
 
 // Read 8 bytes at a 2-byte-aligned address as two words, touching only bytes
 // in [p - 2, p + 10): aligned words plus a funnel shift when p % 4 == 2.
+// Exactly the 4*N bytes at the 2-byte-aligned p, as N words; reads only
+// [p - 2, p + 4N) (aligned words, the last two bytes by a 16-bit load).
+template <int N>
+__device__ __forceinline__ void ldw_a2(const uint8_t *p, uint32_t (&o)[N]) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    if ((a & 2) == 0) {
+#pragma unroll
+        for (int i = 0; i < N; i++) o[i] = ld_u32(p + 4 * i);
+    } else {
+        const uint8_t *b = p - 2;
+        uint32_t w[N + 1];
+#pragma unroll
+        for (int i = 0; i < N; i++) w[i] = ld_u32(b + 4 * i);
+        w[N] = ld_u16(b + 4 * N);
+#pragma unroll
+        for (int i = 0; i < N; i++) o[i] = __funnelshift_r(w[i], w[i + 1], 16);
+    }
+}
+
 __device__ __forceinline__ void ld8_a2(const uint8_t *p, uint32_t &lo, uint32_t &hi) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(p);
     const uint8_t *base = reinterpret_cast<const uint8_t *>(a & ~uintptr_t(3));
@@ -73,11 +94,13 @@ __device__ __forceinline__ void q4k_scale_min(const uint32_t sc[3], int j, int &
 }
 
 __host__ __device__ constexpr int64_t block_elems(int t) {
-    return (t == GGUF_Q8_0 || t == GGUF_Q8_1) ? 32 : (t == GGUF_Q4_K || t == GGUF_Q6_K) ? 256
+    return (t == GGUF_Q8_0 || t == GGUF_Q8_1 || t == GGUF_Q4_0) ? 32
+         : (t == GGUF_Q4_K || t == GGUF_Q5_K || t == GGUF_Q6_K) ? 256
          : (t == GGUF_F32 || t == GGUF_F16 || t == GGUF_BF16) ? 1 : 0;
 }
 __host__ __device__ constexpr int64_t block_bytes(int t) {
     return t == GGUF_Q8_0 ? 34 : t == GGUF_Q8_1 ? 36 : t == GGUF_Q4_K ? 144 : t == GGUF_Q6_K ? 210
+         : t == GGUF_Q4_0 ? 18 : t == GGUF_Q5_K ? 176
          : t == GGUF_F32 ? 4 : (t == GGUF_F16 || t == GGUF_BF16) ? 2 : 0;
 }
 

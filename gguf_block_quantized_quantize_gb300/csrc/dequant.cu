@@ -3,14 +3,16 @@
 // dequantize and get_rows are the ops of the same names in FreeToken PR #690
 // "serve GGUF checkpoints on vendored ggml-cuda kernels" (section "Vendored
 // ggml", paragraph "Our own code next to it").  Values are computed in fp32 in
-// the order  Q4_K: a = d*s; b = dmin*m; a*q - b;  Q6_K: (d*sc)*(q-32);
-// Q8_0 / q8_1: d*q  and rounded to the output dtype (RNE).  Every product
-// above is exact in fp32, so the only rounding is the Q4_K subtraction.
+// the order  Q4_K, Q5_K: a = d*s; b = dmin*m; a*q - b;  Q6_K: (d*sc)*(q-32);
+// Q8_0 / q8_1: d*q;  Q4_0: d*(q-8)  and rounded to the output dtype (RNE).
+// Every product above is exact in fp32, so the only rounding is the Q4_K /
+// Q5_K subtraction.
 //
 // One thread produces one 32-value piece of a row:
-//   Q8_0 / q8_1 : one block (one run of 32 values)
-//   Q4_K        : sub-block j of a super-block (values [32j, +32): the low or
-//                 high nibbles of the 32 quant bytes of chunk j / 2)
+//   Q8_0 / q8_1 / Q4_0 : one block (one run of 32 values)
+//   Q4_K / Q5_K : sub-block j of a super-block (values [32j, +32): the low or
+//                 high nibbles of the 32 quant bytes of chunk j / 2; Q5_K adds
+//                 bit j of the 32 high-bit bytes)
 //   Q6_K        : runs [128h + 32g + l0, +8) for g = 0..3 of a super-block
 #include "common.cuh"
 #include "internal.h"
@@ -71,26 +73,51 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
         }
         if (zero) for (int i = 0; i < 32; i++) v[i] = 0.0f;
         store_run<OT>(out, obase + p * 32, v, 32);
-    } else if (WT == GGUF_Q4_K) {
+    } else if (WT == GGUF_Q4_0) {
+        // block p: byte l of the 16 quant bytes holds value l (low nibble) and
+        // value l + 16 (high nibble); blocks are only 2-byte aligned
+        const uint8_t *blk = row + p * Q4_0_BYTES;
+        const float d = h2f(ld_u16(blk));
+        uint32_t qw[4];
+        ldw_a2<4>(blk + 2, qw);
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const int byte = (int)((qw[i >> 2] >> (8 * (i & 3))) & 0xff);
+            v[i] = __fmul_rn(d, (float)((byte & 15) - 8));
+            v[16 + i] = __fmul_rn(d, (float)((byte >> 4) - 8));
+        }
+        if (zero) for (int i = 0; i < 32; i++) v[i] = 0.0f;
+        store_run<OT>(out, obase + p * 32, v, 32);
+    } else if (WT == GGUF_Q4_K || WT == GGUF_Q5_K) {
         // sub-block j = p % 8 of super-block p / 8: the low (j even) or high
-        // (j odd) nibbles of the 32 quant bytes of chunk j / 2, written as one
+        // (j odd) nibbles of the 32 quant bytes of chunk j / 2 (Q5_K: plus bit
+        // j of the 32 high-bit bytes as the fifth bit), written as one
         // contiguous run of 32 values
+        constexpr bool K5 = WT == GGUF_Q5_K;
         const int64_t sb = p >> 3;
         const int j = (int)(p & 7), c = j >> 1, sh = 4 * (j & 1);
-        const uint8_t *blk = row + sb * Q4_K_BYTES;
+        const uint8_t *blk = row + sb * (K5 ? Q5_K_BYTES : Q4_K_BYTES);
+        const int qoff = K5 ? 48 : 16;
         const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
-        const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
-        const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
+        const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + qoff + 32 * c);
+        const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + qoff + 16 + 32 * c);
+        uint4 h0 = make_uint4(0u, 0u, 0u, 0u), h1 = h0;
+        if (K5) {
+            h0 = *reinterpret_cast<const uint4 *>(blk + 16);
+            h1 = *reinterpret_cast<const uint4 *>(blk + 32);
+        }
         const uint32_t sc[3] = {hdr.y, hdr.z, hdr.w};
         const float d = h2f(hdr.x & 0xffff), dmin = h2f(hdr.x >> 16);
         int s, m;
         q4k_scale_min(sc, j, s, m);
         const float a = __fmul_rn(d, (float)s), b = __fmul_rn(dmin, (float)m);
         const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
         for (int i = 0; i < 32; i++) {
-            const int nib = (qw[i >> 2] >> (8 * (i & 3) + sh)) & 15;
-            v[i] = __fsub_rn(__fmul_rn(a, (float)nib), b);
+            int q = (qw[i >> 2] >> (8 * (i & 3) + sh)) & 15;
+            if (K5) q |= (int)((hw[i >> 2] >> (8 * (i & 3) + j)) & 1) << 4;
+            v[i] = __fsub_rn(__fmul_rn(a, (float)q), b);
         }
         if (zero) for (int i = 0; i < 32; i++) v[i] = 0.0f;
         store_run<OT>(out, obase + sb * 256 + 32 * j, v, 32);
@@ -155,11 +182,16 @@ __global__ void block_dots_kernel(const uint8_t *__restrict__ w, int64_t n, int6
         int qw;
         if (WT == GGUF_Q8_0) {
             qw = (int8_t)row[(kk / 32) * Q8_0_BYTES + 2 + (kk % 32)];
-        } else if (WT == GGUF_Q4_K) {
-            const uint8_t *blk = row + (kk / 256) * Q4_K_BYTES;
+        } else if (WT == GGUF_Q4_0) {
+            const uint8_t byte = row[(kk / 32) * Q4_0_BYTES + 2 + (kk % 16)];
+            qw = ((kk % 32) < 16 ? (byte & 15) : (byte >> 4)) - 8;
+        } else if (WT == GGUF_Q4_K || WT == GGUF_Q5_K) {
+            constexpr bool K5 = WT == GGUF_Q5_K;
+            const uint8_t *blk = row + (kk / 256) * (K5 ? Q5_K_BYTES : Q4_K_BYTES);
             const int i = (int)(kk % 256), cc = i / 64, rr = i % 64;
-            const uint8_t byte = blk[16 + 32 * cc + (rr % 32)];
+            const uint8_t byte = blk[(K5 ? 48 : 16) + 32 * cc + (rr % 32)];
             qw = rr < 32 ? (byte & 15) : (byte >> 4);
+            if (K5) qw |= ((blk[16 + (i % 32)] >> (i / 32)) & 1) << 4;
         } else {
             const uint8_t *blk = row + (kk / 256) * Q6_K_BYTES;
             const int i = (int)(kk % 256), h = i / 128, o = i % 128, l = o % 32, g4 = o / 32;
@@ -183,7 +215,9 @@ cudaError_t launch_dequantize(const uint8_t *w, int wt, int64_t rows, int64_t k,
     switch (wt) {
     case GGUF_Q8_0: DQT(GGUF_Q8_0); break;
     case GGUF_Q8_1: DQT(GGUF_Q8_1); break;
+    case GGUF_Q4_0: DQT(GGUF_Q4_0); break;
     case GGUF_Q4_K: DQT(GGUF_Q4_K); break;
+    case GGUF_Q5_K: DQT(GGUF_Q5_K); break;
     case GGUF_Q6_K: DQT(GGUF_Q6_K); break;
     default: return cudaErrorInvalidValue;
     }
@@ -214,7 +248,9 @@ cudaError_t launch_block_dots(const uint8_t *w, int wt, int64_t n, int64_t k, co
     const int64_t rb = k / block_elems(wt) * block_bytes(wt);
     switch (wt) {
     case GGUF_Q8_0: block_dots_kernel<GGUF_Q8_0><<<grid, 256, 0, s>>>(w, n, k, rb, xq, m, sums); break;
+    case GGUF_Q4_0: block_dots_kernel<GGUF_Q4_0><<<grid, 256, 0, s>>>(w, n, k, rb, xq, m, sums); break;
     case GGUF_Q4_K: block_dots_kernel<GGUF_Q4_K><<<grid, 256, 0, s>>>(w, n, k, rb, xq, m, sums); break;
+    case GGUF_Q5_K: block_dots_kernel<GGUF_Q5_K><<<grid, 256, 0, s>>>(w, n, k, rb, xq, m, sums); break;
     case GGUF_Q6_K: block_dots_kernel<GGUF_Q6_K><<<grid, 256, 0, s>>>(w, n, k, rb, xq, m, sums); break;
     default: return cudaErrorInvalidValue;
     }

@@ -28,15 +28,18 @@ gguf_status report(gguf_status st, const char *msg);
 // q8_1 quantization (xq may be null); also writes the fp16 tensor-core operand
 // xh[m][pitch] = fp16(d16*q) when xh != nullptr, and its low part
 // xl = fp16(d16*q - xh) when xl != nullptr.  pitch > k appends the Q4_K
-// min-term correction columns (see op_pitch) and zero padding.
+// / Q5_K min-term correction columns (see op_pitch) and zero padding.
 cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int64_t ldx, uint8_t *xq,
                                  uint16_t *xh, uint16_t *xl, cudaStream_t s, int64_t pitch = 0);
 // the same fp16 operand(s) from q8_1 rows
 cudaError_t launch_q8_1_to_f16(const uint8_t *xq, int64_t m, int64_t k, uint16_t *xh, uint16_t *xl, cudaStream_t s,
                                int64_t pitch = 0);
-// Row length of the tensor-core operand for weight type wt: k, plus for Q4_K
-// one min-term correction column per 32-block, rounded up to the 64-value K step.
-inline int64_t op_pitch(int wt, int64_t k) { return wt == GGUF_Q4_K ? (k + k / 32 + 63) / 64 * 64 : k; }
+// Row length of the tensor-core operand for weight type wt: k, plus for the
+// affine K-quants (Q4_K, Q5_K) one min-term correction column per 32-block,
+// rounded up to the 64-value K step.
+inline int64_t op_pitch(int wt, int64_t k) {
+    return (wt == GGUF_Q4_K || wt == GGUF_Q5_K) ? (k + k / 32 + 63) / 64 * 64 : k;
+}
 
 cudaError_t launch_dequantize(const uint8_t *w, int wt, int64_t rows, int64_t k, const int32_t *ids,
                               int64_t table_rows, void *out, int ot, cudaStream_t s);

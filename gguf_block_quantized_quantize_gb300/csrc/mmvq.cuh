@@ -1,9 +1,9 @@
 // MMVQ: quantized weight x q8_1 activation product for small token counts
 // (decode).  y[m][n] = sum over the row's sub-blocks of an exact int32 block
 // dot product combined with the fp32 block scales:
-//   Q8_0: d_w * d_a * S
-//   Q4_K: d * s_j * d_a * S_j - dmin * m_j * s_a
-//   Q6_K: d * sc_j * d_a * S_j
+//   Q8_0, Q4_0: d_w * d_a * S          (Q4_0: S over q - 8)
+//   Q4_K, Q5_K: d * s_j * d_a * S_j - dmin * m_j * s_a
+//   Q6_K:       d * sc_j * d_a * S_j
 // (FreeToken PR #690 "serve GGUF checkpoints on vendored ggml-cuda kernels",
 // section "Vendored ggml": q8_1 activations, fp32 accumulation, results in the
 // activation dtype; MMVQ serves the small batches, section "Changes").
@@ -14,7 +14,7 @@
 // coalesced loads, and the arithmetic per byte is kept small enough to hide
 // under those loads:
 //   * K is split across the threads of a CTA: thread t owns "piece" t of every
-//     row (64 values for Q4_K / Q6_K, 32 for Q8_0).  Its q8_1 activation quants
+//     row (64 values for the K-quants, 32 for Q8_0 / Q4_0).  Its q8_1 activation quants
 //     for that piece are loaded once into registers and reused for every row
 //     the CTA visits, so activations cost no bandwidth in the row loop.  For
 //     8 tokens, two threads share a piece and take 4 tokens each, which halves
@@ -246,6 +246,111 @@ struct Q80Piece {
     }
 };
 
+// Q4_0 with staged loads, as Q8_0: a warp's 32 pieces are 32 consecutive
+// 18-byte blocks (only 2-byte aligned), one contiguous span of up to 576
+// bytes read with 16-byte loads of its aligned cover plus 2-byte loads of a
+// tail.  The offset 8 of the quants enters the exact integer sum through the
+// activation block's quant sum: S = sum(q * q_a) - 8 * sum(q_a).
+struct Q40Piece {
+    static constexpr int VALUES = 32;
+    static constexpr bool STAGED = true;
+    static constexpr int STAGE_CHUNKS = 38;   // 16-byte chunks of a warp's buffer (576 + 14 bytes)
+    struct Pos {
+        int64_t p;       // piece = block index in the row
+        int lane;
+        int span_off;    // byte offset of the warp's span in the row
+        int span_len;    // bytes of the span (32 / TG blocks, fewer at the end of the row)
+        int fld;         // byte offset of the piece's block in the span
+    };
+    struct W { uint4 c[2]; uint32_t t; uint32_t head; };
+    struct Wf { uint32_t q[4]; uint32_t d; };
+    template <int M>
+    struct A {
+        int q[M][8];     // activation quants, 4 per word
+        float f[M];      // d_a
+        int sum[M];      // 8 * sum of the block's quants
+    };
+    template <int TG>
+    static __device__ __forceinline__ Pos pos(int64_t p, int tg, int64_t k) {
+        constexpr int PW = 32 / TG;
+        const int64_t w = p / PW, left = k / 32 - PW * w;
+        Pos q;
+        q.p = p;
+        q.lane = (int)((p * TG + tg) & 31);
+        q.span_off = (int)(w * PW * Q4_0_BYTES);
+        q.span_len = (int)((left < PW ? (left > 0 ? left : 0) : PW) * Q4_0_BYTES);
+        q.fld = (int)(p % PW) * Q4_0_BYTES;
+        return q;
+    }
+    static __device__ __forceinline__ void load(W &w, const uint8_t *row, const Pos &q) {
+        const uint8_t *a = row + q.span_off;
+        const uint32_t head = (uint32_t)(reinterpret_cast<uintptr_t>(a) & 15);
+        const uint4 *c0 = reinterpret_cast<const uint4 *>(a - head);
+        const int full = (int)(head + q.span_len) >> 4;
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const int c = q.lane + 32 * i;
+            w.c[i] = c < full ? __ldg(c0 + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        const int tail = (int)((head + q.span_len) & 15) >> 1;
+        w.t = q.lane < tail ? ld_u16(reinterpret_cast<const uint8_t *>(c0 + full) + 2 * q.lane) : 0u;
+        w.head = head;
+    }
+    static __device__ __forceinline__ void prepare(const W &w, const Pos &q, uint4 *buf, Wf &f) {
+        const int full = (int)(w.head + q.span_len) >> 4;
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const int c = q.lane + 32 * i;
+            if (c < full) buf[c] = w.c[i];
+        }
+        const int tail = (int)((w.head + q.span_len) & 15) >> 1;
+        if (q.lane < tail) reinterpret_cast<uint16_t *>(buf + full)[q.lane] = (uint16_t)w.t;
+        __syncwarp();
+        const uint8_t *blk = reinterpret_cast<const uint8_t *>(buf) + w.head + q.fld;
+        f.d = *reinterpret_cast<const uint16_t *>(blk);
+        lds16_a2(blk + 2, f.q);
+        __syncwarp();   // every lane holds its block before the buffer is rewritten
+    }
+    template <int M>
+    static __device__ __forceinline__ void load_act(A<M> &a, const uint8_t *xq, int64_t xrb, int m_act,
+                                                    const Pos &q, bool valid) {
+#pragma unroll
+        for (int mm = 0; mm < M; mm++) {
+            const bool on = valid && mm < m_act;
+            const uint8_t *blk = xq + mm * xrb + (valid ? q.p : 0) * Q8_1_BYTES;
+            a.f[mm] = on ? h2f(ld_u16(blk)) : 0.0f;
+            int sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const int v = on ? (int)ld_u32(blk + 4 + 4 * i) : 0;
+                a.q[mm][i] = v;
+                sum = dp4a_ss(v, 0x01010101, sum);
+            }
+            a.sum[mm] = 8 * sum;
+        }
+    }
+    template <int M>
+    static __device__ __forceinline__ void dot(const Wf &w, const A<M> &a, const Pos &, float (&acc)[M]) {
+        const float d = h2f((uint16_t)w.d);
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            lo[i] = w.q[i] & 0x0F0F0F0Fu;          // values 4i .. 4i+3
+            hi[i] = (w.q[i] >> 4) & 0x0F0F0F0Fu;   // values 16 + 4i ..
+        }
+#pragma unroll
+        for (int mm = 0; mm < M; mm++) {
+            int S = -a.sum[mm];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                S = dp4a_us(lo[i], a.q[mm][i], S);
+                S = dp4a_us(hi[i], a.q[mm][4 + i], S);
+            }
+            acc[mm] = fmaf(d * a.f[mm], (float)S, acc[mm]);
+        }
+    }
+};
+
 // Q4_K, 64-value pieces: piece p is chunk c = p%4 of super-block p/4, i.e. the
 // 32 quant bytes at 16 + 32c whose low nibbles are sub-block 2c and whose high
 // nibbles are sub-block 2c+1 (values 64c .. 64c+63).  One thread loads the
@@ -330,6 +435,88 @@ struct Q4KPiece {
         for (int i = 0; i < 8; i++) {
             lo[i] = raw[i] & 0x0F0F0F0Fu;
             hi[i] = raw[i] & 0xF0F0F0F0u;
+        }
+#pragma unroll
+        for (int mm = 0; mm < M; mm++) {
+            int S0 = 0, S1 = 0;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                S0 = dp4a_us(lo[i], a.q[mm][i], S0);
+                S1 = dp4a_us(hi[i], a.q[mm][8 + i], S1);
+            }
+            float v = ds0 * (a.f[mm][0] * (float)S0);
+            v = fmaf(ds1, a.f[mm][1] * (float)S1, v);
+            v = fmaf(-dmin, fmaf(fm0, a.f[mm][2], fm1 * a.f[mm][3]), v);
+            acc[mm] += v;
+        }
+    }
+};
+
+// Q5_K, 64-value pieces as Q4_K: piece p is chunk c = p%4 of super-block p/4
+// (176 bytes, 16-byte aligned): the same 16-byte header, the 32 quant bytes at
+// 48 + 32c, and all 32 high-bit bytes at 16, of which the piece takes bits 2c
+// (its low-nibble sub-block) and 2c + 1 (its high-nibble one).  Five 16-byte
+// loads per piece; the four pieces of a super-block sit in adjacent lanes, so
+// a warp still reads each high-bit byte from DRAM once.
+struct Q5KPiece {
+    static constexpr int VALUES = 64;
+    static constexpr bool STAGED = false;
+    static constexpr int STAGE_CHUNKS = 1;
+    struct Pos {
+        int64_t sb;                // super-block index in the row
+        int c;                     // chunk
+        uint32_t sel_r, sel_w;     // scale-byte selectors, as Q4KPiece
+        uint32_t m1, m2, m3, m4;
+    };
+    struct W { uint4 h, h0, h1, a, b; };
+    template <int M> using A = Q4KPiece::A<M>;
+    static __device__ __forceinline__ Pos pos(int64_t p) {
+        const Q4KPiece::Pos k4 = Q4KPiece::pos(p);
+        Pos q;
+        q.sb = p >> 2;
+        q.c = k4.c;
+        q.sel_r = k4.sel_r;
+        q.sel_w = k4.sel_w;
+        q.m1 = k4.m1;
+        q.m2 = k4.m2;
+        q.m3 = k4.m3;
+        q.m4 = k4.m4;
+        return q;
+    }
+    static __device__ __forceinline__ void load(W &w, const uint8_t *row, const Pos &q) {
+        const uint8_t *blk = row + q.sb * Q5_K_BYTES;
+        w.h = __ldg(reinterpret_cast<const uint4 *>(blk));
+        w.h0 = __ldg(reinterpret_cast<const uint4 *>(blk + 16));
+        w.h1 = __ldg(reinterpret_cast<const uint4 *>(blk + 32));
+        w.a = __ldg(reinterpret_cast<const uint4 *>(blk + 48 + 32 * q.c));
+        w.b = __ldg(reinterpret_cast<const uint4 *>(blk + 64 + 32 * q.c));
+    }
+    template <int M>
+    static __device__ __forceinline__ void load_act(A<M> &a, const uint8_t *xq, int64_t xrb, int m_act,
+                                                    const Pos &q, bool valid) {
+        Q4KPiece::Pos k4{};
+        k4.off = q.sb * Q4_K_BYTES;   // Q4KPiece::load_act locates the q8_1 blocks from off and c
+        k4.c = q.c;
+        Q4KPiece::load_act<M>(a, xq, xrb, m_act, k4, valid);
+    }
+    template <int M>
+    static __device__ __forceinline__ void dot(const W &w, const A<M> &a, const Pos &q, float (&acc)[M]) {
+        const float d = h2f(w.h.x & 0xffff), dmin = h2f(w.h.x >> 16);
+        const uint32_t r = __byte_perm(w.h.y, w.h.z, q.sel_r);
+        const uint32_t wq = __byte_perm(w.h.w, 0u, q.sel_w);
+        const uint32_t sm = (r & q.m1) | ((r >> 2) & q.m2) | (wq & q.m3) | ((wq >> 4) & q.m4);
+        const float ds0 = d * (float)(sm & 0xff);
+        const float ds1 = d * (float)((sm >> 8) & 0xff);
+        const float fm0 = (float)((sm >> 16) & 0xff), fm1 = (float)(sm >> 24);
+        const uint32_t raw[8] = {w.a.x, w.a.y, w.a.z, w.a.w, w.b.x, w.b.y, w.b.z, w.b.w};
+        const uint32_t qh[8] = {w.h0.x, w.h0.y, w.h0.z, w.h0.w, w.h1.x, w.h1.y, w.h1.z, w.h1.w};
+        const int sh = 2 * q.c;
+        uint32_t lo[8], hi[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const uint32_t hb = qh[i] >> sh;   // bit 0 of each byte: sub-block 2c, bit 1: 2c + 1
+            lo[i] = (raw[i] & 0x0F0F0F0Fu) | ((hb << 4) & 0x10101010u);
+            hi[i] = ((raw[i] >> 4) & 0x0F0F0F0Fu) | ((hb << 3) & 0x10101010u);
         }
 #pragma unroll
         for (int mm = 0; mm < M; mm++) {
@@ -730,11 +917,17 @@ inline cudaError_t launch_mmvq_pt(const MmvqSegs &sg, int64_t k, const uint8_t *
 cudaError_t launch_mmvq_q8_0(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
 cudaError_t launch_mmvq_q4_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
 cudaError_t launch_mmvq_q6_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
+cudaError_t launch_mmvq_q4_0(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
+cudaError_t launch_mmvq_q5_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
 cudaError_t launch_mmvq_routes_q8_0(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,
                                     int64_t routes, float *z, cudaStream_t s);
 cudaError_t launch_mmvq_routes_q4_k(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,
                                     int64_t routes, float *z, cudaStream_t s);
 cudaError_t launch_mmvq_routes_q6_k(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,
+                                    int64_t routes, float *z, cudaStream_t s);
+cudaError_t launch_mmvq_routes_q4_0(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,
+                                    int64_t routes, float *z, cudaStream_t s);
+cudaError_t launch_mmvq_routes_q5_k(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,
                                     int64_t routes, float *z, cudaStream_t s);
 
 }  // namespace gg

@@ -1,0 +1,18 @@
+// MMVQ instantiations for Q4_0 weights (see mmvq.cuh).
+#include "mmvq.cuh"
+
+namespace gg {
+
+cudaError_t launch_mmvq_q4_0(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s) {
+    const int64_t n = sg.rows();
+    // the Q8_0 configuration (32-value staged pieces): 5..8 tokens as two
+    // threads per piece below 4096 rows
+    return launch_mmvq_pt<Q40Piece>(sg, k, xq, m, yt, s, k / 32 * Q4_0_BYTES, MmvqTune{false, false, n < 4096});
+}
+
+cudaError_t launch_mmvq_routes_q4_0(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,
+                                    int64_t routes, float *z, cudaStream_t s) {
+    return launch_mmvq_routes_pt<Q40Piece>(bank, rt, n, k, k / 32 * Q4_0_BYTES, xq, routes, z, s);
+}
+
+}  // namespace gg

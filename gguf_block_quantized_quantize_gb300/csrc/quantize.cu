@@ -55,7 +55,7 @@ __device__ __forceinline__ void write_f16_operand(float d16, const int q[8], uin
     if (lo) *reinterpret_cast<uint4 *>(lo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
-// Min-term correction columns of the operand rows (Q4_K weights).  The fp16
+// Min-term correction columns of the operand rows (Q4_K / Q5_K weights).  The fp16
 // operand d16 * q gives the min term of a 32-block as dmin * m * d16 * sum(q);
 // the blockwise formula uses the stored s instead.  Column k + b of a row
 // holds c_b = d16 * sum(q) - s (the weight side holds dmin * m for that

@@ -47,7 +47,7 @@ struct TgParams {
     // weights
     const uint8_t *w;
     int64_t expert_stride, rb, n, k;
-    int64_t kx;  // activation operand row length: k, plus the Q4_K min-term correction columns
+    int64_t kx;  // activation operand row length: k, plus the Q4_K / Q5_K min-term correction columns
     // dense tiles
     int64_t m;
     int tiles_n, tiles_m, tiles_total, ks_per_split;
@@ -64,7 +64,7 @@ struct TgParams {
     // gate_up outputs (any may be null)
     uint8_t *hq;
     uint16_t *hbf, *h16, *h16lo;
-    int64_t hpitch;  // row length of h16 / h16lo: I, plus correction columns when the down weights are Q4_K
+    int64_t hpitch;  // row length of h16 / h16lo: I, plus correction columns when the down weights are Q4_K / Q5_K
 };
 
 template <int BN, bool PRECISE, int MODE>
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             };
 #pragma unroll
             for (int dd = 0; dd < DEPTH; dd++) load_step(u[dd], d.k0 + dd);
-            // one task: unpack (weight steps) or the Q4_K min-term correction
+            // one task: unpack (weight steps) or the Q4_K / Q5_K min-term correction
             // values dmin * m_j of 8 sub-blocks per chunk (steps past the weights)
             auto task = [&](const U &u, int i, int ks, uint32_t (&hi)[VW / 2], uint32_t (&lo)[VW / 2]) {
 #pragma unroll
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                         if (PRECISE) pack_split<VW>(v, hi, lo);
                         else pack_single<VW>(v, hi);
                     }
-                } else if (WT == GGUF_Q4_K) {
+                } else if (WT == GGUF_Q4_K || WT == GGUF_Q5_K) {
                     // chunk c of this step holds the corrections of super-block
                     // (ks * 64 - k) / 64 + c of the row
                     const int64_t nsb = p.k / 256;
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                     for (int e = 0; e < U::CHUNKS; e++) {
                         const int64_t sb = sb0 + U::chunk(part, e);
                         uint4 hdr = make_uint4(0, 0, 0, 0);
-                        if (sb < nsb) hdr = *reinterpret_cast<const uint4 *>(wrow[i] + sb * Q4_K_BYTES);
+                        if (sb < nsb) hdr = *reinterpret_cast<const uint4 *>(wrow[i] + sb * block_bytes(WT));
                         const uint32_t sc[3] = {hdr.y, hdr.z, hdr.w};
                         const float dmin = h2f(hdr.x >> 16);
 #pragma unroll
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                                     p.h16[rt * p.hpitch + icol] = vh;
                                     if (p.h16lo) p.h16lo[rt * p.hpitch + icol] = f2h_rn(v - h2f(vh));
                                     if (p.hpitch > idim) {
-                                        // min-term correction column of this q8_1 block (Q4_K down
+                                        // min-term correction column of this q8_1 block (Q4_K / Q5_K down
                                         // weights), and the zero padding of the row (written once,
                                         // by the first column tile)
                                         if (lane == 0) {

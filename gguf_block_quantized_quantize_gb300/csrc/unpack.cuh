@@ -1,4 +1,5 @@
-// Weight unpack for the tensor-core GEMM: packed Q4_K / Q6_K / Q8_0 bytes of a
+// Weight unpack for the tensor-core GEMM: packed Q4_K / Q5_K / Q6_K / Q8_0 /
+// Q4_0 bytes of a
 // weight row -> fp16 operand values (each the exact fp32 value of the block
 // formula rounded once, or packed-half math where the product is rounded to a
 // 16-bit output anyway), stored as 16-byte chunks of a 128-byte-swizzled
@@ -7,7 +8,8 @@
 // Unit of work ("task"): one weight row, one 64-value K-step, one of PARTS
 // parts of it (halves for Q4_K and Q8_0, quarters for Q6_K); a task yields
 // CHUNKS 8-value chunks (16-byte fp16 chunks of the swizzled row), chunk e of
-// part j at position chunk(j, e) of the row.  Consecutive lanes take the parts
+// part j at position chunk(j, e) of the row.  (Halves for Q4_K, Q5_K, Q8_0
+// and Q4_0.)  Consecutive lanes take the parts
 // of one row, so a warp-wide load reads contiguous bytes of 16 (8) rows, and
 // every packed byte is read once.
 #pragma once
@@ -16,26 +18,7 @@
 
 namespace gg {
 
-// ---------------------------------------------------------------- packed-byte loads
-
-// Exactly the 4*N bytes at the 2-byte-aligned p, as N words; reads only
-// [p - 2, p + 4N) (aligned words, the last two bytes by a 16-bit load).
-template <int N>
-__device__ __forceinline__ void ldw_a2(const uint8_t *p, uint32_t (&o)[N]) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    if ((a & 2) == 0) {
-#pragma unroll
-        for (int i = 0; i < N; i++) o[i] = ld_u32(p + 4 * i);
-    } else {
-        const uint8_t *b = p - 2;
-        uint32_t w[N + 1];
-#pragma unroll
-        for (int i = 0; i < N; i++) w[i] = ld_u32(b + 4 * i);
-        w[N] = ld_u16(b + 4 * N);
-#pragma unroll
-        for (int i = 0; i < N; i++) o[i] = __funnelshift_r(w[i], w[i + 1], 16);
-    }
-}
+// ---------------------------------------------------------------- packed-byte helpers
 
 // exact small integer -> float: 2^23 + byte, then subtract
 __device__ __forceinline__ float byte_to_f(uint32_t word, int byte, float bias) {
@@ -220,6 +203,121 @@ struct KQ<GGUF_Q8_0> {
 #pragma unroll
             for (int p = 0; p < 2; p++)
                 out[2 * i + p] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(bytes_to_h2_1024(u, p)), k1152), d2));
+        }
+    }
+};
+
+// Q5_K: as Q4_K (the same header; quant bytes at 48 instead of 16), and half
+// j also takes high-bit bytes [16j, +16) (at byte 16 of the block), whose bits
+// 2c and 2c + 1 are the fifth bits of the low- and high-nibble sub-blocks.
+template <>
+struct KQ<GGUF_Q5_K> {
+    static constexpr int PARTS = 2, CHUNKS = 4;
+    static __device__ __forceinline__ int chunk(int j, int e) { return e < 2 ? 2 * j + e : 2 + 2 * j + e; }
+    uint4 hdr, q, qh;
+    __device__ __forceinline__ void load(const uint8_t *row, int ks, int j, int64_t) {
+        const uint8_t *blk = row + (int64_t)(ks >> 2) * Q5_K_BYTES;
+        hdr = *reinterpret_cast<const uint4 *>(blk);
+        qh = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * j);
+        q = *reinterpret_cast<const uint4 *>(blk + 48 + 32 * (ks & 3) + 16 * j);
+    }
+    __device__ __forceinline__ void scales(int ks, float &a0, float &b0, float &a1, float &b1) const {
+        const uint32_t sc[3] = {hdr.y, hdr.z, hdr.w};
+        const float d = h2f(hdr.x & 0xffff), dmin = h2f(hdr.x >> 16);
+        int s, m;
+        q4k_scale_min(sc, 2 * (ks & 3), s, m);
+        a0 = __fmul_rn(d, (float)s);
+        b0 = __fmul_rn(dmin, (float)m);
+        q4k_scale_min(sc, 2 * (ks & 3) + 1, s, m);
+        a1 = __fmul_rn(d, (float)s);
+        b1 = __fmul_rn(dmin, (float)m);
+    }
+    // 5-bit quants of the low / high nibble sub-block, 4 per word
+    __device__ __forceinline__ void quants(int ks, int h, uint32_t &lo, uint32_t &hi) const {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        const uint32_t b[4] = {qh.x, qh.y, qh.z, qh.w};
+        const uint32_t hb = b[h] >> (2 * (ks & 3));
+        lo = (w[h] & 0x0F0F0F0Fu) | ((hb << 4) & 0x10101010u);
+        hi = ((w[h] >> 4) & 0x0F0F0F0Fu) | ((hb << 3) & 0x10101010u);
+    }
+    __device__ __forceinline__ void unpack_f32(int ks, float (&v)[32]) const {
+        float a0, b0, a1, b1;
+        scales(ks, a0, b0, a1, b1);
+#pragma unroll
+        for (int h = 0; h < 4; h++) {
+            uint32_t lo, hi;
+            quants(ks, h, lo, hi);
+#pragma unroll
+            for (int b = 0; b < 4; b++) {
+                v[4 * h + b] = fmaf(a0, byte_to_f(lo, b, -8388608.0f), -b0);   // a * q exact, one rounding
+                v[16 + 4 * h + b] = fmaf(a1, byte_to_f(hi, b, -8388608.0f), -b1);
+            }
+        }
+    }
+    __device__ __forceinline__ void unpack_h2(int ks, uint32_t (&out)[16]) const {
+        float a0, b0, a1, b1;
+        scales(ks, a0, b0, a1, b1);
+        const __half2 a02 = __float2half2_rn(a0), nb02 = __float2half2_rn(-b0);
+        const __half2 a12 = __float2half2_rn(a1), nb12 = __float2half2_rn(-b1);
+        const __half2 k1024 = __float2half2_rn(1024.0f);
+#pragma unroll
+        for (int h = 0; h < 4; h++) {
+            uint32_t lo, hi;
+            quants(ks, h, lo, hi);
+#pragma unroll
+            for (int p = 0; p < 2; p++) {
+                out[2 * h + p] = h2_as_u32(__hfma2(__hsub2(u32_as_h2(bytes_to_h2_1024(lo, p)), k1024), a02, nb02));
+                out[8 + 2 * h + p] = h2_as_u32(__hfma2(__hsub2(u32_as_h2(bytes_to_h2_1024(hi, p)), k1024), a12, nb12));
+            }
+        }
+    }
+};
+
+// Q4_0: as Q8_0, K-step ks is blocks 2ks (chunks 0..3) and 2ks + 1 (chunks
+// 4..7, absent past the end when K % 64 == 32); half j is block 2ks + j, whose
+// 16 quant bytes hold values 0..15 in the low nibbles and 16..31 in the high.
+template <>
+struct KQ<GGUF_Q4_0> {
+    static constexpr int PARTS = 2, CHUNKS = 4;
+    static __device__ __forceinline__ int chunk(int j, int e) { return 4 * j + e; }
+    uint32_t q[4], dw;
+    __device__ __forceinline__ void load(const uint8_t *row, int ks, int j, int64_t kblocks) {
+        const int64_t b = 2 * (int64_t)ks + j;
+        if (b < kblocks) {
+            const uint8_t *blk = row + b * Q4_0_BYTES;
+            dw = ld_u16(blk);
+            ldw_a2<4>(blk + 2, q);
+        } else {
+            dw = 0u;
+#pragma unroll
+            for (int i = 0; i < 4; i++) q[i] = 0u;
+        }
+    }
+    // d * (q - 8) is exact in fp32
+    __device__ __forceinline__ void unpack_f32(int, float (&v)[32]) const {
+        const float d = h2f((uint16_t)dw);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint32_t lo = q[i] & 0x0F0F0F0Fu, hi = (q[i] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+            for (int b = 0; b < 4; b++) {
+                v[4 * i + b] = __fmul_rn(d, byte_to_f(lo, b, -8388616.0f));
+                v[16 + 4 * i + b] = __fmul_rn(d, byte_to_f(hi, b, -8388616.0f));
+            }
+        }
+    }
+    // q - 8 is exact in fp16 and the product is rounded once, as above
+    __device__ __forceinline__ void unpack_h2(int, uint32_t (&out)[16]) const {
+        const __half2 d2 = __halves2half2(__ushort_as_half((uint16_t)dw), __ushort_as_half((uint16_t)dw));
+        const __half2 k1032 = __float2half2_rn(1032.0f);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint32_t lo = q[i] & 0x0F0F0F0Fu, hi = (q[i] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+            for (int p = 0; p < 2; p++) {
+                out[2 * i + p] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(bytes_to_h2_1024(lo, p)), k1032), d2));
+                out[8 + 2 * i + p] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(bytes_to_h2_1024(hi, p)), k1032), d2));
+            }
         }
     }
 };

@@ -43,6 +43,9 @@ def test_type_table(g):
     assert L.gguf_type_block_elems(g.Q6_K) == 256 and L.gguf_type_block_bytes(g.Q6_K) == 210
     assert L.gguf_type_block_elems(g.Q8_0) == 32 and L.gguf_type_block_bytes(g.Q8_0) == 34
     assert L.gguf_type_block_elems(g.Q8_1) == 32 and L.gguf_type_block_bytes(g.Q8_1) == 36
+    assert L.gguf_type_block_elems(g.Q4_0) == 32 and L.gguf_type_block_bytes(g.Q4_0) == 18
+    assert L.gguf_type_block_elems(g.Q5_K) == 256 and L.gguf_type_block_bytes(g.Q5_K) == 176
+    assert g.gguf_row_size(g.Q4_0, 4128) == 2322 and g.gguf_row_size(g.Q5_K, 2048) == 1408
     assert g.gguf_row_size(g.Q4_K, 4096) == 2304 and g.gguf_row_size(g.Q6_K, 3072) == 2520
     assert g.gguf_row_size(g.Q4_K, 100) == -1 and L.gguf_type_block_bytes(99) == 0
 
@@ -60,7 +63,7 @@ def _mm(g, **kw):
 
 
 def test_mul_mat_rejects_bad_arguments(g):
-    assert _mm(g, wt=2) == 2                       # Q4_0: unsupported type
+    assert _mm(g, wt=3) == 2                       # Q4_1: unsupported type
     assert _mm(g, xt=g.Q6_K) == 2
     assert _mm(g, yt=g.Q8_0) == 2
     assert _mm(g, k=100) == 3                      # not a multiple of 256
@@ -88,7 +91,7 @@ def test_other_entry_points_reject_bad_arguments(g):
     assert L.gguf_quantize_q8_1(FAKE, g.Q8_0, 4, 64, 64, FAKE, None) == 2
     assert L.gguf_quantize_q8_1(FAKE, g.F32, 4, 40, 40, FAKE, None) == 3
     assert L.gguf_quantize_q8_1(FAKE, g.F32, 4, 64, 32, FAKE, None) == 1
-    assert L.gguf_dequantize(FAKE, 2, 4, 64, FAKE, g.F32, None) == 2
+    assert L.gguf_dequantize(FAKE, 3, 4, 64, FAKE, g.F32, None) == 2     # Q4_1: not supported
     assert L.gguf_dequantize(FAKE, g.Q6_K, 4, 300, FAKE, g.F32, None) == 3
     assert L.gguf_dequantize(FAKE, g.Q6_K, 4, 256, FAKE, g.Q8_0, None) == 2
     assert L.gguf_get_rows(FAKE, g.Q6_K, 4, 256, None, 3, FAKE, g.F32, None) == 1

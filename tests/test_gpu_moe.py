@@ -231,6 +231,25 @@ def test_gate_up_h512(g, path):
     assert same.mean() > 0.995, same.mean()
 
 
+@pytest.mark.parametrize("wt", [oracle.Q4_0, oracle.Q5_K, oracle.Q8_0, oracle.Q6_K])
+def test_gate_up_bank_types(g, path, wt):
+    """gate_up with every weight type of the bank, through both paths: the
+    bf16 h against the oracle's, inactive routes zero."""
+    E, K, H, I, T = 4, 3, 512, 128, 21
+    bank_gu = _bank(wt, E, 2 * I, H, 300 + wt, False)
+    sgu = bank_gu.nbytes // E
+    ids, _ = synth.routes(T, E, K, seed=wt)
+    ids[0] = [2, 2, 2]
+    ids[1, 0] = -1
+    x = synth.activations(T, H, seed=wt + 1, dtype=torch.bfloat16)
+    h_ref, _ = oracle.moe_gate_up(wt, bank_gu, E, sgu, 2 * I, H, oracle.quantize_q8_1(x.float().numpy()), ids)
+    active = ids.reshape(-1) >= 0
+    hb = g.gguf_mul_mat_id(_u8(bank_gu), wt, E, sgu, 2 * I, H, x.to(DEV), _u8(ids), g.GATE_UP_SWIGLU)
+    hb = hb.float().cpu().numpy()
+    assert np.all(hb[~active] == 0)
+    assert_close(hb[active], h_ref[active], TOL_BF16, f"gate_up type {wt} ({path})")
+
+
 # ---------------------------------------------------------------- vector path (few tokens)
 
 class _vec_off:
@@ -290,7 +309,7 @@ def test_vec_gate_up_outputs(g, T):
     assert_close(hb2[active], hb[active], TOL_BF16, f"vec vs tensor-core gate_up T {T}")
 
 
-@pytest.mark.parametrize("wt", [oracle.Q6_K, oracle.Q4_K, oracle.Q8_0])
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K])
 @pytest.mark.parametrize("T", [1, 5, 16])
 def test_vec_down_from_oracle_h(g, wt, T):
     E, K, H, I = 4, 3, 512, 256
@@ -312,7 +331,7 @@ def test_vec_down_from_oracle_h(g, wt, T):
 
 
 @pytest.mark.parametrize("T", [1, 2, 16])
-@pytest.mark.parametrize("down", [oracle.Q6_K, oracle.Q4_K])
+@pytest.mark.parametrize("down", [oracle.Q6_K, oracle.Q4_K, oracle.Q5_K, oracle.Q4_0])
 def test_vec_moe_ffn_end_to_end(g, T, down):
     E, K, H, I = 6, 4, 256, 256
     bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 1000 + T, False)
