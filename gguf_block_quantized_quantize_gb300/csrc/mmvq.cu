@@ -33,9 +33,9 @@ cudaError_t launch_mmvq(const MmvqSegs &sg, int wt, int64_t k, const uint8_t *xq
 }
 
 bool mmvq_routes_supported(int wt, int64_t k) {
-    const int64_t values = (wt == GGUF_Q8_0 || wt == GGUF_Q4_0) ? 32 : 64;
+    const int64_t values = wt == GGUF_Q8_0 ? 32 : 64;   // values per thread's piece
     return (wt == GGUF_Q8_0 || wt == GGUF_Q4_0 || wt == GGUF_Q4_K || wt == GGUF_Q5_K || wt == GGUF_Q6_K) && k > 0 &&
-           k / values <= 256;
+           (k + values - 1) / values <= 256;
 }
 
 cudaError_t launch_mmvq_routes(int wt, const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k,

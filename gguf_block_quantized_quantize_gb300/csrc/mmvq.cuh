@@ -14,7 +14,7 @@
 // coalesced loads, and the arithmetic per byte is kept small enough to hide
 // under those loads:
 //   * K is split across the threads of a CTA: thread t owns "piece" t of every
-//     row (64 values for the K-quants, 32 for Q8_0 / Q4_0).  Its q8_1 activation quants
+//     row (64 values for the K-quants and Q4_0, 32 for Q8_0).  Its q8_1 activation quants
 //     for that piece are loaded once into registers and reused for every row
 //     the CTA visits, so activations cost no bandwidth in the row loop.  For
 //     8 tokens, two threads share a piece and take 4 tokens each, which halves
@@ -246,40 +246,44 @@ struct Q80Piece {
     }
 };
 
-// Q4_0 with staged loads, as Q8_0: a warp's 32 pieces are 32 consecutive
-// 18-byte blocks (only 2-byte aligned), one contiguous span of up to 576
-// bytes read with 16-byte loads of its aligned cover plus 2-byte loads of a
-// tail.  The offset 8 of the quants enters the exact integer sum through the
-// activation block's quant sum: S = sum(q * q_a) - 8 * sum(q_a).
+// Q4_0 with staged loads, as Q8_0, two blocks per piece: piece p is blocks 2p
+// and 2p + 1 (the second absent at the end of a row of an odd number of
+// blocks), so a warp's 32 pieces are 64 consecutive 18-byte blocks (only
+// 2-byte aligned), one contiguous span of up to 1152 bytes read with 16-byte
+// loads of its aligned cover plus 2-byte loads of a tail.  The offset 8 of
+// the quants enters the exact integer sum through the activation block's
+// quant sum: S = sum(q * q_a) - 8 * sum(q_a).
 struct Q40Piece {
-    static constexpr int VALUES = 32;
+    static constexpr int VALUES = 64;
     static constexpr bool STAGED = true;
-    static constexpr int STAGE_CHUNKS = 38;   // 16-byte chunks of a warp's buffer (576 + 14 bytes)
+    static constexpr int STAGE_CHUNKS = 74;   // 16-byte chunks of a warp's buffer (1152 + 14 bytes, + reads)
     struct Pos {
-        int64_t p;       // piece = block index in the row
+        int64_t p;       // piece: blocks 2p, 2p + 1 of the row
         int lane;
         int span_off;    // byte offset of the warp's span in the row
-        int span_len;    // bytes of the span (32 / TG blocks, fewer at the end of the row)
-        int fld;         // byte offset of the piece's block in the span
+        int span_len;    // bytes of the span (64 / TG blocks, fewer at the end of the row)
+        int fld;         // byte offset of the piece's first block in the span
+        bool two;        // block 2p + 1 exists
     };
-    struct W { uint4 c[2]; uint32_t t; uint32_t head; };
-    struct Wf { uint32_t q[4]; uint32_t d; };
+    struct W { uint4 c[3]; uint32_t t; uint32_t head; };
+    struct Wf { uint32_t q[8]; uint32_t d; };   // quants of both blocks; d = d0 | d1 << 16
     template <int M>
     struct A {
-        int q[M][8];     // activation quants, 4 per word
-        float f[M];      // d_a
-        int sum[M];      // 8 * sum of the block's quants
+        int q[M][16];    // activation quants of both blocks, 4 per word
+        float f[M][2];   // d_a of each block
+        int sum[M][2];   // 8 * sum of each block's quants
     };
     template <int TG>
     static __device__ __forceinline__ Pos pos(int64_t p, int tg, int64_t k) {
-        constexpr int PW = 32 / TG;
-        const int64_t w = p / PW, left = k / 32 - PW * w;
+        constexpr int PW = 32 / TG, BW = 2 * PW;   // pieces, blocks per warp
+        const int64_t nb = k / 32, w = p / PW, left = nb - BW * w;   // blocks of the row from the span start
         Pos q;
         q.p = p;
         q.lane = (int)((p * TG + tg) & 31);
-        q.span_off = (int)(w * PW * Q4_0_BYTES);
-        q.span_len = (int)((left < PW ? (left > 0 ? left : 0) : PW) * Q4_0_BYTES);
-        q.fld = (int)(p % PW) * Q4_0_BYTES;
+        q.span_off = (int)(w * BW * Q4_0_BYTES);
+        q.span_len = (int)((left < BW ? (left > 0 ? left : 0) : BW) * Q4_0_BYTES);
+        q.fld = (int)(p % PW) * 2 * Q4_0_BYTES;
+        q.two = 2 * p + 1 < nb;
         return q;
     }
     static __device__ __forceinline__ void load(W &w, const uint8_t *row, const Pos &q) {
@@ -288,7 +292,7 @@ struct Q40Piece {
         const uint4 *c0 = reinterpret_cast<const uint4 *>(a - head);
         const int full = (int)(head + q.span_len) >> 4;
 #pragma unroll
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < 3; i++) {
             const int c = q.lane + 32 * i;
             w.c[i] = c < full ? __ldg(c0 + c) : make_uint4(0u, 0u, 0u, 0u);
         }
@@ -299,7 +303,7 @@ struct Q40Piece {
     static __device__ __forceinline__ void prepare(const W &w, const Pos &q, uint4 *buf, Wf &f) {
         const int full = (int)(w.head + q.span_len) >> 4;
 #pragma unroll
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < 3; i++) {
             const int c = q.lane + 32 * i;
             if (c < full) buf[c] = w.c[i];
         }
@@ -307,46 +311,64 @@ struct Q40Piece {
         if (q.lane < tail) reinterpret_cast<uint16_t *>(buf + full)[q.lane] = (uint16_t)w.t;
         __syncwarp();
         const uint8_t *blk = reinterpret_cast<const uint8_t *>(buf) + w.head + q.fld;
-        f.d = *reinterpret_cast<const uint16_t *>(blk);
-        lds16_a2(blk + 2, f.q);
-        __syncwarp();   // every lane holds its block before the buffer is rewritten
+        uint32_t lo[4], hi[4];
+        lds16_a2(blk + 2, lo);
+        lds16_a2(blk + 20, hi);
+        const uint32_t d0 = *reinterpret_cast<const uint16_t *>(blk);
+        const uint32_t d1 = *reinterpret_cast<const uint16_t *>(blk + 18);
+        // an absent second block (bytes past the span) contributes nothing
+        f.d = d0 | ((q.two ? d1 : 0u) << 16);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            f.q[i] = lo[i];
+            f.q[4 + i] = q.two ? hi[i] : 0u;
+        }
+        __syncwarp();   // every lane holds its blocks before the buffer is rewritten
     }
     template <int M>
     static __device__ __forceinline__ void load_act(A<M> &a, const uint8_t *xq, int64_t xrb, int m_act,
                                                     const Pos &q, bool valid) {
 #pragma unroll
         for (int mm = 0; mm < M; mm++) {
-            const bool on = valid && mm < m_act;
-            const uint8_t *blk = xq + mm * xrb + (valid ? q.p : 0) * Q8_1_BYTES;
-            a.f[mm] = on ? h2f(ld_u16(blk)) : 0.0f;
-            int sum = 0;
 #pragma unroll
-            for (int i = 0; i < 8; i++) {
-                const int v = on ? (int)ld_u32(blk + 4 + 4 * i) : 0;
-                a.q[mm][i] = v;
-                sum = dp4a_ss(v, 0x01010101, sum);
+            for (int b = 0; b < 2; b++) {
+                const bool on = valid && mm < m_act && (b == 0 || q.two);
+                const uint8_t *blk = xq + mm * xrb + (on ? 2 * q.p + b : 0) * Q8_1_BYTES;
+                a.f[mm][b] = on ? h2f(ld_u16(blk)) : 0.0f;
+                int sum = 0;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const int v = on ? (int)ld_u32(blk + 4 + 4 * i) : 0;
+                    a.q[mm][8 * b + i] = v;
+                    sum = dp4a_ss(v, 0x01010101, sum);
+                }
+                a.sum[mm][b] = 8 * sum;
             }
-            a.sum[mm] = 8 * sum;
         }
     }
     template <int M>
     static __device__ __forceinline__ void dot(const Wf &w, const A<M> &a, const Pos &, float (&acc)[M]) {
-        const float d = h2f((uint16_t)w.d);
-        uint32_t lo[4], hi[4];
+        const float d[2] = {h2f((uint16_t)(w.d & 0xffff)), h2f((uint16_t)(w.d >> 16))};
+        uint32_t lo[8], hi[8];
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            lo[i] = w.q[i] & 0x0F0F0F0Fu;          // values 4i .. 4i+3
+        for (int i = 0; i < 8; i++) {
+            lo[i] = w.q[i] & 0x0F0F0F0Fu;          // values 4i .. 4i+3 of the block
             hi[i] = (w.q[i] >> 4) & 0x0F0F0F0Fu;   // values 16 + 4i ..
         }
 #pragma unroll
         for (int mm = 0; mm < M; mm++) {
-            int S = -a.sum[mm];
+            float v = acc[mm];
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
-                S = dp4a_us(lo[i], a.q[mm][i], S);
-                S = dp4a_us(hi[i], a.q[mm][4 + i], S);
+            for (int b = 0; b < 2; b++) {
+                int S = -a.sum[mm][b];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    S = dp4a_us(lo[4 * b + i], a.q[mm][8 * b + i], S);
+                    S = dp4a_us(hi[4 * b + i], a.q[mm][8 * b + 4 + i], S);
+                }
+                v = fmaf(d[b] * a.f[mm][b], (float)S, v);
             }
-            acc[mm] = fmaf(d * a.f[mm], (float)S, acc[mm]);
+            acc[mm] = v;
         }
     }
 };
@@ -706,7 +728,7 @@ __global__ void __launch_bounds__(MAXT) mmvq_kernel(const MmvqSegs sg, int64_t k
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     const int tg = tid % TG;
     const int64_t piece = tid / TG;
-    const int64_t P = k / PT::VALUES;
+    const int64_t P = (k + PT::VALUES - 1) / PT::VALUES;   // a last partial piece (Q4_0) counts
     const bool valid = piece < P;
     const typename PT::Pos pos = [&] {
         if constexpr (PT::STAGED) return PT::template pos<TG>(piece, tg, k);   // lanes past the row still copy their share
@@ -816,7 +838,7 @@ template <class PT, int M, int TG, int R, int MAXT>
 inline cudaError_t launch_mmvq_cfg(const MmvqSegs &sg, int64_t k, int64_t rb, const uint8_t *xq, int64_t m, int yt,
                                    cudaStream_t s) {
     const int64_t n = sg.rows();
-    const int64_t P = k / PT::VALUES;
+    const int64_t P = (k + PT::VALUES - 1) / PT::VALUES;
     const int nthr = (int)((P * TG + 31) / 32 * 32);
     if (nthr > MAXT) return cudaErrorInvalidValue;
     auto kern = sg.nseg > 1 ? mmvq_kernel<PT, M, TG, R, MAXT, true> : mmvq_kernel<PT, M, TG, R, MAXT, false>;
@@ -845,7 +867,7 @@ template <class PT>
 inline cudaError_t launch_mmvq_routes_pt(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k,
                                          int64_t rb, const uint8_t *xq, int64_t routes, float *z, cudaStream_t s) {
     if (routes <= 0 || n <= 0) return cudaSuccess;
-    const int64_t P = k / PT::VALUES;
+    const int64_t P = (k + PT::VALUES - 1) / PT::VALUES;
     if (P > 256 || routes > 65535) return cudaErrorInvalidValue;
     const int nthr = (int)((P + 31) / 32 * 32);
     auto kern = mmvq_kernel<PT, 1, 1, 2, 256, false, true>;
@@ -887,7 +909,7 @@ struct MmvqTune {
 template <class PT>
 inline cudaError_t launch_mmvq_pt(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s,
                                   int64_t rb, MmvqTune t) {
-    const int64_t P = k / PT::VALUES;
+    const int64_t P = (k + PT::VALUES - 1) / PT::VALUES;
     if (P <= 256) {
         if (m <= 1) {
             if (t.r1_m1) return launch_mmvq_cfg<PT, 1, 1, 1, 256>(sg, k, rb, xq, m, yt, s);

@@ -250,6 +250,20 @@ def test_gate_up_bank_types(g, path, wt):
     assert_close(hb[active], h_ref[active], TOL_BF16, f"gate_up type {wt} ({path})")
 
 
+def test_vec_down_q4_0_odd_blocks(g):
+    # a Q4_0 down bank with I = 96 (three blocks per row): the route-batched
+    # MMVQ's last piece holds one block
+    E, K, H, I, T = 3, 2, 256, 96, 5
+    bank_d = _bank(oracle.Q4_0, E, H, I, 77, True)
+    sd = bank_d.nbytes // E
+    ids, rw = synth.routes(T, E, K, seed=78)
+    hq = oracle.quantize_q8_1(synth.normal((T * K, I), 1.0, seed=79))
+    ref = oracle.moe_down(oracle.Q4_0, bank_d, E, sd, H, I, hq, ids, rw)
+    y = g.gguf_mul_mat_id(_u8(bank_d), oracle.Q4_0, E, sd, H, I, _u8(hq), _u8(ids), g.DOWN_WEIGHTED_SUM,
+                          route_w=_u8(rw), xt=g.Q8_1, out_type=g.F32).cpu().numpy()
+    assert_close(y, ref, TOL_F32, "vec down Q4_0 I=96")
+
+
 # ---------------------------------------------------------------- vector path (few tokens)
 
 class _vec_off:

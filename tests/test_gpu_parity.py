@@ -166,6 +166,19 @@ def test_mmvq_k_range_bf16(g, wt, k, m):
     assert_close(y.float().cpu().numpy(), ref, TOL_BF16, f"mmvq bf16 type {wt} k {k} m {m}")
 
 
+@pytest.mark.parametrize("k", [32, 96, 2080, 16352])
+@pytest.mark.parametrize("m", [1, 3, 5, 8])
+def test_mmvq_q4_0_odd_block_count(g, k, m):
+    # Q4_0 pieces are block pairs: an odd number of blocks per row leaves a
+    # last piece of one block (k = 32: a single half piece; 16352: 511 blocks)
+    n = 197
+    w = _weights(oracle.Q4_0, n, k, seed=k + m, safe=True)
+    x = synth.activations(m, k, seed=k - m, dtype=torch.float32)
+    ref = oracle.mul_mat(oracle.Q4_0, w, k, oracle.quantize_q8_1(x.numpy()))
+    y = g.gguf_mul_mat(_u8(w), oracle.Q4_0, n, k, x.to(DEV)).cpu().numpy()
+    assert_close(y, ref, TOL_F32, f"mmvq Q4_0 k {k} m {m}")
+
+
 @pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K])
 @pytest.mark.parametrize("k", [256, 1024, 3072, 8192])
 @pytest.mark.parametrize("m", [5, 8])
