@@ -337,7 +337,7 @@ def run_ours(args, rank, world, torch, dev):
 # decode MMVQ launches, averaged over the step's launches, from the ncu capture
 # summarized in profiles/mmvq_q4_k_decode.md; None whenever the kernel has
 # changed since the capture.
-MMVQ_TRAFFIC = 21277344
+MMVQ_TRAFFIC = 21277120
 
 
 def run_e2e(args, g, torch, dev, dec, per_step):
@@ -516,6 +516,34 @@ def secondary(torch, g, synth, dev, stream, hbm_peak, tf_peak, peak_kind):
             "us": round(ms * 1e3, 2), "gbs": round(by / (ms * 1e-3) / 1e9, 1),
             "frac": round(by / (ms * 1e-3) / 1e9 / hbm_peak, 3), "bytes": by}
         del table, ids, y
+
+        # decode MMVQ of every weight type: 14336 x 4096 at 1 and 8 tokens (pre-quantized q8_1,
+        # bf16 out), graph-timed with the weights rotating over more than 4x L2; GB/s of weights
+        n, k = 14336, 4096
+        types = {}
+        for tname, wt in (("q4_0", g.Q4_0), ("q4_k", g.Q4_K), ("q5_k", g.Q5_K), ("q6_k", g.Q6_K), ("q8_0", g.Q8_0)):
+            wb = n * g.gguf_row_size(wt, k)
+            copies = [synth.safe_blocks_device(wt, n, k, seed=20 + i, device=dev) for i in range(int(4 * l2 // wb) + 2)]
+            res = {}
+            for m in (1, 8):
+                xq = g.gguf_quantize_q8_1(synth.activations(m, k, seed=m, dtype=torch.bfloat16).to(dev))
+                y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+                wsz = torch.empty(max(g.gguf_mul_mat_ws_size(wt, n, k, g.Q8_1, m, g.BF16), 16), dtype=torch.uint8,
+                                  device=dev)
+                idx = [0]
+
+                def one():
+                    idx[0] = (idx[0] + 1) % len(copies)
+                    g.gguf_mul_mat(copies[idx[0]], wt, n, k, xq, xt=g.Q8_1, m=m, out=y, ws=wsz)
+                one()
+                graphs = _capture(torch, stream, lambda: [one() for _ in range(16)], (len(copies) + 15) // 16)
+                us = _time_graphs(torch, stream, graphs, 4 * len(graphs), warm=2) * 1e3 / 16
+                res[f"m{m}"] = {"us": round(us, 2), "gbs": round(wb / us / 1e3, 1), "frac": round(wb / us / 1e3 / hbm_peak, 3)}
+                del graphs
+            types[tname] = res
+            del copies
+        out["mmvq_types_14336x4096"] = dict(types, note="GB/s of packed weights; q8_1 input, bf16 out, graph-timed, "
+                                                         "weights rotating past L2")
 
         # Llama-3.2-3B-shaped decode step: 28 layers of q/k/o/gate/up (Q4_K) and v/down (Q6_K), tied
         # Q6_K embedding / LM head 128256 x 3072 via get_rows + MMVQ; all linears at M in {1, 8, 32}
