@@ -10,7 +10,7 @@ on every machine):
   * activations  ~ N(0, 1) in fp32 / bf16 / fp16
   * routes       top_k distinct experts per token, uniform; weights are the
                  softmax of top_k N(0, 1) logits
-  * safe blocks  random packed Q8_0 / Q4_0 / Q4_K / Q5_K / Q6_K bytes whose fp16 scale fields
+  * safe blocks  random packed Q8_0 / Q4_0 / Q4_K / Q5_K / Q6_K / MXFP4 bytes whose fp16 scale fields
                  are finite and of the size quantized N(0, 0.02) weights have,
                  so that no value overflows (the "random-but-safe packed bytes"
                  of FreeToken PR #196, section "Testing")
@@ -20,10 +20,10 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-F32, F16, Q4_0, Q8_0, Q8_1, Q4_K, Q5_K, Q6_K, BF16 = 0, 1, 2, 8, 9, 12, 13, 14, 30
+F32, F16, Q4_0, Q8_0, Q8_1, Q4_K, Q5_K, Q6_K, BF16, MXFP4 = 0, 1, 2, 8, 9, 12, 13, 14, 30, 39
 
-BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q8_1: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256}
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q8_1: 36, Q4_K: 144, Q5_K: 176, Q6_K: 210}
+BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q8_1: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256, MXFP4: 32}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q8_1: 36, Q4_K: 144, Q5_K: 176, Q6_K: 210, MXFP4: 17}
 
 
 def row_bytes(t: int, k: int) -> int:
@@ -77,6 +77,10 @@ def safe_blocks(t: int, rows: int, k: int, seed: int) -> np.ndarray:
         # fp16 d at 0..1 (either sign); 16 nibble bytes random
         d = rng.uniform(2.0e-3, 1.2e-2, size=(rows, nb)) * rng.choice([-1.0, 1.0], size=(rows, nb))
         blk[:, :, 0:2] = _f16_bits(d).reshape(rows, nb, 1).view(np.uint8).reshape(rows, nb, 2)
+    elif t == MXFP4:
+        # E8M0 exponent byte at 0: block scales 2^-9 .. 2^-3, the range of quantized N(0, 0.02)
+        # weights; the 16 code bytes random
+        blk[:, :, 0] = rng.integers(118, 125, size=(rows, nb), dtype=np.uint8)
     elif t == Q5_K:
         # fp16 d at 0..1, fp16 dmin at 2..3 (non-negative); scale, high-bit and quant bytes random
         d = rng.uniform(1.0e-5, 1.0e-4, size=(rows, nb))
@@ -126,6 +130,8 @@ def safe_blocks_device(t: int, rows: int, k: int, seed: int, device) -> torch.Te
         field([1.5e-4, -2.5e-4, 3.5e-4, -4.5e-4], 0, 2)
     elif t == Q4_0:
         field([4.0e-3, -6.0e-3, 8.0e-3, -1.0e-2], 0, 2)
+    elif t == MXFP4:
+        blk[:, :, 0] = torch.randint(118, 125, (rows, nb), dtype=torch.uint8, device=device, generator=g)
     elif t == Q5_K:
         field([1.5e-5, 3.0e-5, 5.5e-5, 8.0e-5], 0, 2)
         field([0.0, 3.0e-4, 6.0e-4, 9.0e-4], 2, 4)

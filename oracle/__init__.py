@@ -20,6 +20,7 @@ _SRC = os.path.join(_HERE, "gguf_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libgguf_oracle.so")
 
 F32, F16, Q4_0, Q8_0, Q8_1, Q4_K, Q5_K, Q6_K, BF16 = 0, 1, 2, 8, 9, 12, 13, 14, 30
+MXFP4 = 39
 
 
 def build(force: bool = False) -> str:

@@ -1,6 +1,7 @@
 /*
  * gguf_oracle.c -- plain, slow, scalar CPU oracle for the GGUF block-quantized
- * matmul path (q8_1 activations x Q8_0 / Q4_0 / Q4_K / Q5_K / Q6_K weights).
+ * matmul path (q8_1 activations x Q8_0 / Q4_0 / Q4_K / Q5_K / Q6_K / MXFP4
+ * weights).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or runs
  * this file: only tests/, __graft_entry__.smoke() and the cpu_baseline leg of
@@ -25,6 +26,11 @@
  *
  * Readings where the pages are silent (the pages name the formats but never
  * print their bytes):
+ *  - MXFP4 is another type the pages list (FreeToken PR #690, "Tensor types").
+ *    Its values are OCP microscaling FP4: e2m1 codes (sign, 2-bit exponent,
+ *    1-bit mantissa) scaled by the block's E8M0 exponent, 2^(e - 127); the
+ *    GGUF block is {u8 e, u8 qs[16]} with Q4_0's nibble order.  E8M0 code 255
+ *    (NaN in the OCP definition) is read as the exponent 128 like any other.
  *  - Q4_0 and Q5_K are two of the further tensor types the pages list
  *    (FreeToken PR #690, "Tensor types"; transformers PR #45977, supported
  *    quant types of GgufLinear).
@@ -36,10 +42,13 @@
  *    away from zero), s = fp16(d * (float)sum(q)) with the fp32 d.
  *  - dequantized value order: Q4_K, Q5_K  a = d*s; b = dmin*m; v = a*q - b;
  *                             Q6_K  v = (d*sc) * (q - 32);   Q8_0  v = d*q;
- *                             Q4_0  v = d * (q - 8).
+ *                             Q4_0  v = d * (q - 8);
+ *                             MXFP4 v = e2m1(q) * 2^(e - 127), one exact product.
  *  - block dots: symmetric formats with an integer offset (Q4_0: 8, Q6_K: 32)
  *    take the offset into the exact integer sum; affine formats with a float
  *    min (Q4_K, Q5_K) combine the min with the activation block's stored s.
+ *    MXFP4's integer quant is 2 * e2m1(q) (exact, in -12..12) against the
+ *    block factor 2^(e - 128).
  *  - matmul reference: the blockwise formula evaluated in fp64 on the stored
  *    (fp16) fields, e.g. Q4_K y = sum_j (d*s_j*d_a*S_j - dmin*m_j*s_a).
  *  - weight quantizers (test-input generators only; the GPU never quantizes
@@ -134,7 +143,7 @@ static void wr16(uint8_t *p, uint16_t v) { p[0] = (uint8_t)(v & 0xff); p[1] = (u
 int64_t orc_block_elems(int type) {
     switch (type) {
     case ORC_F32: case ORC_F16: case ORC_BF16: return 1;
-    case ORC_Q8_0: case ORC_Q8_1: case ORC_Q4_0: return 32;
+    case ORC_Q8_0: case ORC_Q8_1: case ORC_Q4_0: case ORC_MXFP4: return 32;
     case ORC_Q4_K: case ORC_Q5_K: case ORC_Q6_K: return 256;
     default: return 0;
     }
@@ -147,6 +156,7 @@ int64_t orc_block_bytes(int type) {
     case ORC_Q8_0: return 34;  /* fp16 d, int8 q[32] */
     case ORC_Q8_1: return 36;  /* fp16 d, fp16 s, int8 q[32] */
     case ORC_Q4_0: return 18;  /* fp16 d, u8 qs[16] */
+    case ORC_MXFP4: return 17; /* u8 e (E8M0), u8 qs[16] (e2m1 codes) */
     case ORC_Q4_K: return 144; /* fp16 d, fp16 dmin, u8 scales[12], u8 qs[128] */
     case ORC_Q5_K: return 176; /* fp16 d, fp16 dmin, u8 scales[12], u8 qh[32], u8 qs[128] */
     case ORC_Q6_K: return 210; /* u8 ql[128], u8 qh[64], i8 scales[16], fp16 d */
@@ -163,7 +173,7 @@ int64_t orc_row_size(int type, int64_t k) {
 /* sub-block length of the per-block integer dot products */
 int64_t orc_sub_elems(int type) {
     switch (type) {
-    case ORC_Q8_0: case ORC_Q4_0: case ORC_Q4_K: case ORC_Q5_K: return 32;
+    case ORC_Q8_0: case ORC_Q4_0: case ORC_Q4_K: case ORC_Q5_K: case ORC_MXFP4: return 32;
     case ORC_Q6_K: return 16;
     default: return 0;
     }
@@ -214,6 +224,23 @@ static int q4_0_q(const uint8_t *b, int i) {
     uint8_t byte = b[2 + (i % 16)];
     return i < 16 ? (byte & 15) : (byte >> 4);
 }
+
+/* MXFP4 block: byte 0 is the E8M0 exponent e, bytes 1..16 hold 32 e2m1 codes
+ * in Q4_0's order (byte 1 + l: code of value l low, of value l + 16 high).
+ * e2m1 code c: sign c >> 3, exponent E = (c >> 1) & 3, mantissa M = c & 1;
+ * magnitude M / 2 when E = 0 (subnormal), else 2^(E - 1) * (1 + M / 2).     */
+static int mxfp4_e(const uint8_t *b) { return b[0]; }
+static int mxfp4_code(const uint8_t *b, int i) {
+    uint8_t byte = b[1 + (i % 16)];
+    return i < 16 ? (byte & 15) : (byte >> 4);
+}
+static double e2m1_value(int c) {
+    int E = (c >> 1) & 3, M = c & 1;
+    double mag = E == 0 ? 0.5 * M : ldexp(1.0 + 0.5 * M, E - 1);
+    return (c & 8) ? -mag : mag;
+}
+/* the integer quant 2 * e2m1(c), exact in -12..12 */
+static int mxfp4_q(const uint8_t *b, int i) { return (int)(2.0 * e2m1_value(mxfp4_code(b, i))); }
 
 /* Q5_K super-block: the header (d, dmin, 12 scale bytes) is packed exactly as
  * Q4_K's, so q4_k_d / q4_k_dmin / q4_k_scale_min read it too.  Value i takes
@@ -383,6 +410,32 @@ static void quantize_block_q4_0(const float *x, uint8_t *out) {
     }
 }
 
+/* MXFP4: the smallest e in 0..254 with 6 * 2^(e - 127) >= amax (0 for an
+ * all-zero block), then per value the e2m1 code of the nearest magnitude of
+ * |x| / 2^(e - 127) (ties to the larger), with x's sign.                     */
+static void quantize_block_mxfp4(const float *x, uint8_t *out) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; i++) {
+        double a = fabs((double)x[i]);
+        if (a > amax) amax = a;
+    }
+    int e = 0;
+    while (e < 254 && 6.0 * ldexp(1.0, e - 127) < amax) e++;
+    memset(out, 0, 17);
+    out[0] = (uint8_t)e;
+    double s = ldexp(1.0, e - 127);
+    for (int i = 0; i < 32; i++) {
+        double r = fabs((double)x[i]) / s;
+        int best = 0;
+        for (int c = 1; c < 8; c++) {
+            double dc = fabs(e2m1_value(c) - r), db = fabs(e2m1_value(best) - r);
+            if (dc <= db) best = c;
+        }
+        if (x[i] < 0.0f && best != 0) best |= 8;
+        out[1 + (i % 16)] |= (uint8_t)(i < 16 ? best : best << 4);
+    }
+}
+
 /* Q5_K: as Q4_K with 32 levels: scale_j = (hi - lo) / 31, q in 0..31, the low
  * 4 bits packed as Q4_K's quants (at byte 48) and bit 4 of value i set as bit
  * i / 32 of qh[i % 32].                                                      */
@@ -495,6 +548,7 @@ int orc_quantize_weights(int type, const float *w, int64_t n, int64_t k, uint8_t
             switch (type) {
             case ORC_Q8_0: quantize_block_q8_0(x, o); break;
             case ORC_Q4_0: quantize_block_q4_0(x, o); break;
+            case ORC_MXFP4: quantize_block_mxfp4(x, o); break;
             case ORC_Q4_K: quantize_block_q4_k(x, o); break;
             case ORC_Q5_K: quantize_block_q5_k(x, o); break;
             case ORC_Q6_K: quantize_block_q6_k(x, o); break;
@@ -522,6 +576,7 @@ static float dequant_value(int type, const uint8_t *blk, int i) {
         return a * (float)q4_k_q(blk, i) - b;
     }
     case ORC_Q4_0: return q4_0_d(blk) * (float)(q4_0_q(blk, i) - 8);
+    case ORC_MXFP4: return ldexpf((float)e2m1_value(mxfp4_code(blk, i)), mxfp4_e(blk) - 127);
     case ORC_Q5_K: {
         int s, m;
         q4_k_scale_min(blk, i / 32, &s, &m);
@@ -556,6 +611,7 @@ static double dequant_value_f64(int type, const uint8_t *blk, int i) {
         return (double)q4_k_d(blk) * s * q4_k_q(blk, i) - (double)q4_k_dmin(blk) * m;
     }
     case ORC_Q4_0: return (double)q4_0_d(blk) * (q4_0_q(blk, i) - 8);
+    case ORC_MXFP4: return ldexp(e2m1_value(mxfp4_code(blk, i)), mxfp4_e(blk) - 127);
     case ORC_Q5_K: {
         int s, m;
         q4_k_scale_min(blk, i / 32, &s, &m);
@@ -630,6 +686,7 @@ static int32_t block_dot(int type, const uint8_t *wb, int64_t first, const uint8
         switch (type) {
         case ORC_Q8_0: qw = q8_0_q(wb, i); break;
         case ORC_Q4_0: qw = q4_0_q(wb, i) - 8; break;
+        case ORC_MXFP4: qw = mxfp4_q(wb, i); break;
         case ORC_Q4_K: qw = q4_k_q(wb, i); break;
         case ORC_Q5_K: qw = q5_k_q(wb, i); break;
         case ORC_Q6_K: qw = q6_k_q(wb, i) - 32; break;
@@ -663,6 +720,7 @@ int orc_block_dots(int type, const uint8_t *w, int64_t n, int64_t k, const uint8
 
 /* y = sum over the row's sub-blocks of the combination of stored fields:
  *   Q8_0, Q4_0: d_w * d_a * S      (Q4_0: S over q - 8)
+ *   MXFP4:      2^(e - 128) * d_a * S   (S over 2 * e2m1(q))
  *   Q4_K, Q5_K: d * s_j * d_a * S_j - dmin * m_j * s_a
  *   Q6_K: d * sc_j * d_a * S_j
  * with d_a, s_a the q8_1 fields of the 32-block holding sub-block j.         */
@@ -680,6 +738,8 @@ static double dot_row(int type, const uint8_t *wrow, int64_t k, const uint8_t *x
                 y += (double)q8_0_d(wb) * da * S;
             } else if (type == ORC_Q4_0) {
                 y += (double)q4_0_d(wb) * da * S;
+            } else if (type == ORC_MXFP4) {
+                y += ldexp(1.0, mxfp4_e(wb) - 128) * da * S;
             } else if (type == ORC_Q4_K || type == ORC_Q5_K) {
                 int s, m;
                 q4_k_scale_min(wb, j, &s, &m);

@@ -88,6 +88,7 @@ def _parse_blocks(name):
                                            ("q4_0_hand_blocks.txt", "Q4_0", 32),
                                            ("q4_k_hand_blocks.txt", "Q4_K", 256),
                                            ("q5_k_hand_blocks.txt", "Q5_K", 256),
+                                           ("mxfp4_hand_blocks.txt", "MXFP4", 32),
                                            ("q6_k_hand_blocks.txt", "Q6_K", 256)])
 def test_hand_built_blocks(orc, fname, tname, k):
     t = getattr(orc, tname)
@@ -293,6 +294,44 @@ def test_q5_k_roundtrip_bound_and_codes(orc):
     assert codes == set(range(32))
 
 
+def test_mxfp4_codes_are_the_ocp_e2m1_values(orc):
+    """Every e2m1 code at scale 1 against the OCP table of FP4 E2M1 values,
+    and the scale as an exact power of two over the whole E8M0 range."""
+    table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    codes = bytes([l | ((l ^ 8) << 4) for l in range(16)])      # value l: code l; value 16 + l: code l ^ 8
+    for e in range(0, 255):
+        raw = np.frombuffer(bytes([e]) + codes, np.uint8).reshape(1, -1)
+        v64 = orc.dequantize_f64(orc.MXFP4, raw, 32)[0]
+        v32 = orc.dequantize_f32(orc.MXFP4, raw, 32)[0]
+        for l in range(16):
+            want = (table[l & 7] if l < 8 else -table[l & 7]) * 2.0 ** (e - 127)
+            assert v64[l] == want and v64[16 + l] == -want, (e, l)
+            # fp32: the same product, exact while it fits, inf past the fp32 range
+            w32 = np.float32(want) if abs(want) < 3.4028234663852886e38 else np.float32(np.copysign(np.inf, want))
+            assert v32[l] == w32, (e, l, v32[l], w32)
+
+
+def test_mxfp4_roundtrip_bound_and_codes(orc):
+    w = synth.normal((32, 1024), 0.02, seed=13) * synth.lognormal_row_scale(32, seed=14)
+    p = orc.quantize_weights(orc.MXFP4, w)
+    blocks = p.reshape(32, 32, 17)
+    e = blocks[:, :, 0].astype(np.float64)
+    s = 2.0 ** (e - 127)
+    wb = np.abs(w.reshape(32, 32, 32)).astype(np.float64)
+    # the chosen scale is the smallest power of two with 6 * s >= amax
+    amax = wb.max(axis=2)
+    assert np.all(6 * s >= amax) and np.all(6 * s / 2 < amax)
+    dq = orc.dequantize_f32(orc.MXFP4, p, 1024).reshape(32, 32, 32).astype(np.float64)
+    # nearest e2m1 magnitude: within half the widest gap of the grid (1.0 between 4 and 6)
+    # below 4 s, and half a gap elsewhere: gaps are 0.5 below 2, 1 from 2 to 4, 2 from 4 to 6
+    r = wb / s[..., None]
+    half_gap = np.where(r <= 2, 0.25, np.where(r <= 4, 0.5, 1.0))
+    assert np.all(np.abs(np.abs(dq) - wb) <= half_gap * s[..., None] * (1 + 1e-12))
+    assert np.all((np.sign(dq) == np.sign(w.reshape(32, 32, 32))) | (dq == 0))
+    codes = set(np.unique(blocks[:, :, 1:] & 15)) | set(np.unique(blocks[:, :, 1:] >> 4))
+    assert codes >= set(range(1, 8)) | set(range(9, 16))
+
+
 def test_layout_each_quant_nibble_moves_one_value(orc):
     """Perturbing one quant field changes exactly one dequantized value, and
     across a block every value is hit once (pins that the layout is a bijection)."""
@@ -329,6 +368,21 @@ def test_layout_each_quant_nibble_moves_one_value(orc):
             assert changed.size == 1
             hit[changed[0]] += 1
     assert np.all(hit == 1)
+    # MXFP4: every bit of every code (all codes 1 = 0.5, so the sign bit moves
+    # the value too) moves exactly one of the 32 values
+    base = bytearray([127] + [0x11] * 16)
+    ref = orc.dequantize_f32(orc.MXFP4, np.frombuffer(bytes(base), np.uint8).reshape(1, -1), 32)[0]
+    for bit in range(4):
+        hit = np.zeros(32, dtype=np.int32)
+        for pos in range(1, 17):
+            for shift in (0, 4):
+                b = bytearray(base)
+                b[pos] ^= (1 << (bit + shift))
+                v = orc.dequantize_f32(orc.MXFP4, np.frombuffer(bytes(b), np.uint8).reshape(1, -1), 32)[0]
+                changed = np.nonzero(v != ref)[0]
+                assert changed.size == 1, (bit, pos, shift)
+                hit[changed[0]] += 1
+        assert np.all(hit == 1), bit
     # Q5_K: each nibble of qs and each bit of qh moves exactly one value; each
     # set covers all 256 values once
     base = bytearray(176)
@@ -364,7 +418,8 @@ def test_layout_each_quant_nibble_moves_one_value(orc):
 
 
 def test_dequantize_out_dtypes_are_rne(orc):
-    for t, k in [(orc.Q8_0, 256), (orc.Q4_0, 256), (orc.Q4_K, 512), (orc.Q5_K, 512), (orc.Q6_K, 512)]:
+    for t, k in [(orc.Q8_0, 256), (orc.Q4_0, 256), (orc.Q4_K, 512), (orc.Q5_K, 512), (orc.Q6_K, 512),
+                 (orc.MXFP4, 256)]:
         p = synth.safe_blocks(t, 16, k, seed=21)
         f = orc.dequantize(t, p, k, orc.F32)
         h = orc.dequantize(t, p, k, orc.F16)

@@ -26,15 +26,17 @@ def _unit_scale_blocks(orc, t, n, k, seed):
     elif t == orc.Q6_K:
         p[:, :, 192:208] = 1
         p[:, :, 208:210] = [0x00, 0x3C]
+    elif t == orc.MXFP4:
+        p[:, :, 0] = 128            # scale 2: the value is the integer quant 2 * e2m1
     return np.ascontiguousarray(p.reshape(n, -1))
 
 
-@pytest.mark.parametrize("tname", ["Q8_0", "Q4_0", "Q4_K", "Q5_K", "Q6_K"])
+@pytest.mark.parametrize("tname", ["Q8_0", "Q4_0", "Q4_K", "Q5_K", "Q6_K", "MXFP4"])
 def test_block_dots_brute_force(orc, tname):
     t = getattr(orc, tname)
     k, n, m = 512, 6, 3
     w = _unit_scale_blocks(orc, t, n, k, seed=31)
-    qw = orc.dequantize_f32(t, w, k).astype(np.int64)      # raw quants (q, q - 8, q or q - 32)
+    qw = orc.dequantize_f32(t, w, k).astype(np.int64)      # raw quants (q, q - 8, q, q - 32 or 2 * e2m1)
     assert np.all(qw == orc.dequantize_f32(t, w, k))      # integral
     xq = orc.quantize_q8_1(synth.normal((m, k), 1.0, seed=32))
     _, _, qa = orc.q8_1_fields(xq)
@@ -53,7 +55,7 @@ def test_block_dots_brute_force(orc, tname):
         assert np.all(got == 32 * 127 * 127)
 
 
-@pytest.mark.parametrize("tname", ["Q8_0", "Q4_0", "Q6_K"])
+@pytest.mark.parametrize("tname", ["Q8_0", "Q4_0", "Q6_K", "MXFP4"])
 def test_blockwise_equals_dequant_dot(orc, tname):
     t = getattr(orc, tname)
     k = 1024
@@ -89,7 +91,7 @@ def test_blockwise_affine_min_term(orc, tname):
 
 
 @pytest.mark.parametrize("tname,tol", [("Q8_0", 0.02), ("Q4_0", 0.12), ("Q4_K", 0.15), ("Q5_K", 0.08),
-                                       ("Q6_K", 0.05)])
+                                       ("Q6_K", 0.05), ("MXFP4", 0.2)])
 def test_quantized_matmul_tracks_fp32(orc, tname, tol):
     t = getattr(orc, tname)
     k = 2048
