@@ -521,7 +521,8 @@ def secondary(torch, g, synth, dev, stream, hbm_peak, tf_peak, peak_kind):
         # bf16 out), graph-timed with the weights rotating over more than 4x L2; GB/s of weights
         n, k = 14336, 4096
         types = {}
-        for tname, wt in (("q4_0", g.Q4_0), ("q4_k", g.Q4_K), ("q5_k", g.Q5_K), ("q6_k", g.Q6_K), ("q8_0", g.Q8_0)):
+        for tname, wt in (("q4_0", g.Q4_0), ("q4_k", g.Q4_K), ("q5_k", g.Q5_K), ("q6_k", g.Q6_K), ("q8_0", g.Q8_0),
+                          ("mxfp4", g.MXFP4)):
             wb = n * g.gguf_row_size(wt, k)
             copies = [synth.safe_blocks_device(wt, n, k, seed=20 + i, device=dev) for i in range(int(4 * l2 // wb) + 2)]
             res = {}

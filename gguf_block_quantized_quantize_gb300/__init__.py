@@ -16,7 +16,7 @@ import os
 
 import torch
 
-F32, F16, Q4_0, Q8_0, Q8_1, Q4_K, Q5_K, Q6_K, BF16 = 0, 1, 2, 8, 9, 12, 13, 14, 30
+F32, F16, Q4_0, Q8_0, Q8_1, Q4_K, Q5_K, Q6_K, BF16, MXFP4 = 0, 1, 2, 8, 9, 12, 13, 14, 30, 39
 GATE_UP_SWIGLU, DOWN_WEIGHTED_SUM = 0, 1
 Q8_1_BYTES = 36   # one q8_1 block: fp16 d, fp16 s, 32 int8 quants (a q8_1 row is k / 32 blocks)
 

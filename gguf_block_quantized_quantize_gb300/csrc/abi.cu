@@ -112,7 +112,8 @@ int64_t option_mmvq_tc_max_m() { return g_mmvq_tc_max_m; }
 
 static bool is_float(int t) { return t == GGUF_F32 || t == GGUF_F16 || t == GGUF_BF16; }
 static bool is_weight(int t) {
-    return t == GGUF_Q8_0 || t == GGUF_Q4_0 || t == GGUF_Q4_K || t == GGUF_Q5_K || t == GGUF_Q6_K;
+    return t == GGUF_Q8_0 || t == GGUF_Q4_0 || t == GGUF_Q4_K || t == GGUF_Q5_K || t == GGUF_Q6_K ||
+           t == GGUF_MXFP4;
 }
 static int64_t esize(int t) { return t == GGUF_F32 ? 4 : 2; }
 static int64_t row_size(int t, int64_t k) {

@@ -19,6 +19,7 @@ constexpr int Q4_K_BYTES = 144;    // fp16 d, fp16 dmin, scales[12], qs[128]
 constexpr int Q6_K_BYTES = 210;    // ql[128], qh[64], scales[16], fp16 d
 constexpr int Q4_0_BYTES = 18;     // fp16 d, qs[16] (value l low nibble, l + 16 high)
 constexpr int Q5_K_BYTES = 176;    // fp16 d, fp16 dmin, scales[12], qh[32], qs[128]
+constexpr int MXFP4_BYTES = 17;    // u8 E8M0 exponent, qs[16] e2m1 codes (Q4_0's nibble order)
 
 __device__ __forceinline__ float h2f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
@@ -93,14 +94,66 @@ __device__ __forceinline__ void q4k_scale_min(const uint32_t sc[3], int j, int &
     }
 }
 
+// ---------------------------------------------------------------- MXFP4 helpers
+// An MXFP4 value is e2m1(code) * 2^(e - 127).  Kernels carry the integer quant
+// k = 2 * e2m1(code) (-12..12, exact) and the block factor 2^(e - 128).
+
+// 2^(e - 128) for an E8M0 code e (exact: 2^-128 and 2^-127 are fp32 subnormals)
+__device__ __forceinline__ float e8m0_half(uint32_t e) {
+    return e >= 2 ? __uint_as_float((e - 1) << 23) : __uint_as_float(0x00200000u << e);
+}
+
+// The four e2m1 codes in the nibbles of the low 16 bits of s -> four bytes
+// 16 + k (4..28), byte n from nibble n.  PRMT in its default mode takes table
+// byte (code & 7) for a selector nibble whose top bit is clear and, where it
+// is set, the replicated sign bit of that byte (0: the table bytes are
+// non-negative).  So p holds k for the codes with the sign bit clear and q
+// (sign bits flipped) |k| for the others, never both in one byte, and
+// 16 + p - q needs no carry between bytes.
+__device__ __forceinline__ uint32_t mxfp4_biased4(uint32_t s) {
+    constexpr uint32_t T0 = 0x03020100u, T1 = 0x0C080604u;   // |k| of codes 0..7: 0 1 2 3 4 6 8 12
+    const uint32_t s16 = s & 0xffffu;
+    uint32_t p, q;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p) : "r"(T0), "r"(T1), "r"(s16));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(q) : "r"(T0), "r"(T1), "r"(s16 ^ 0x8888u));
+    return p + 0x10101010u - q;
+}
+
+// The 17 bytes of an MXFP4 block at any address p: the exponent byte e and the
+// 16 code bytes as four words.  Reads only [p - 3, p + 17): four aligned words
+// from p rounded down to 4, then single bytes up to p + 16.
+__device__ __forceinline__ void ld_mxfp4_block(const uint8_t *p, uint32_t &e, uint32_t (&q)[4]) {
+    const int off = (int)(reinterpret_cast<uintptr_t>(p) & 3);
+    const uint8_t *b = p - off;
+    uint32_t w[5];
+#pragma unroll
+    for (int i = 0; i < 4; i++) w[i] = ld_u32(b + 4 * i);
+    uint32_t t = 0;
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        if (i <= off) t |= (uint32_t)b[16 + i] << (8 * i);
+    w[4] = t;
+    e = (w[0] >> (8 * off)) & 0xffu;
+    const int s = off + 1;   // the code bytes start at b + s
+#pragma unroll
+    for (int j = 0; j < 4; j++) q[j] = s == 4 ? w[j + 1] : __funnelshift_r(w[j], w[j + 1], 8 * s);
+}
+
+// k = 2 * e2m1(code) for one code, by its fields (sign, exponent, mantissa)
+__device__ __forceinline__ int mxfp4_k(uint32_t c) {
+    const int c7 = (int)(c & 7);
+    const int mag = c7 < 4 ? c7 : (2 + (c7 & 1)) << ((c7 >> 1) - 1);
+    return (c & 8) ? -mag : mag;
+}
+
 __host__ __device__ constexpr int64_t block_elems(int t) {
-    return (t == GGUF_Q8_0 || t == GGUF_Q8_1 || t == GGUF_Q4_0) ? 32
+    return (t == GGUF_Q8_0 || t == GGUF_Q8_1 || t == GGUF_Q4_0 || t == GGUF_MXFP4) ? 32
          : (t == GGUF_Q4_K || t == GGUF_Q5_K || t == GGUF_Q6_K) ? 256
          : (t == GGUF_F32 || t == GGUF_F16 || t == GGUF_BF16) ? 1 : 0;
 }
 __host__ __device__ constexpr int64_t block_bytes(int t) {
     return t == GGUF_Q8_0 ? 34 : t == GGUF_Q8_1 ? 36 : t == GGUF_Q4_K ? 144 : t == GGUF_Q6_K ? 210
-         : t == GGUF_Q4_0 ? 18 : t == GGUF_Q5_K ? 176
+         : t == GGUF_Q4_0 ? 18 : t == GGUF_Q5_K ? 176 : t == GGUF_MXFP4 ? 17
          : t == GGUF_F32 ? 4 : (t == GGUF_F16 || t == GGUF_BF16) ? 2 : 0;
 }
 

@@ -4,12 +4,13 @@
 // "serve GGUF checkpoints on vendored ggml-cuda kernels" (section "Vendored
 // ggml", paragraph "Our own code next to it").  Values are computed in fp32 in
 // the order  Q4_K, Q5_K: a = d*s; b = dmin*m; a*q - b;  Q6_K: (d*sc)*(q-32);
-// Q8_0 / q8_1: d*q;  Q4_0: d*(q-8)  and rounded to the output dtype (RNE).
+// Q8_0 / q8_1: d*q;  Q4_0: d*(q-8);  MXFP4: +-(2^(e-128) * |2 e2m1(q)|)  and
+// rounded to the output dtype (RNE).
 // Every product above is exact in fp32, so the only rounding is the Q4_K /
 // Q5_K subtraction.
 //
 // One thread produces one 32-value piece of a row:
-//   Q8_0 / q8_1 / Q4_0 : one block (one run of 32 values)
+//   Q8_0 / q8_1 / Q4_0 / MXFP4 : one block (one run of 32 values)
 //   Q4_K / Q5_K : sub-block j of a super-block (values [32j, +32): the low or
 //                 high nibbles of the 32 quant bytes of chunk j / 2; Q5_K adds
 //                 bit j of the 32 high-bit bytes)
@@ -85,6 +86,22 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
             const int byte = (int)((qw[i >> 2] >> (8 * (i & 3))) & 0xff);
             v[i] = __fmul_rn(d, (float)((byte & 15) - 8));
             v[16 + i] = __fmul_rn(d, (float)((byte >> 4) - 8));
+        }
+        if (zero) for (int i = 0; i < 32; i++) v[i] = 0.0f;
+        store_run<OT>(out, obase + p * 32, v, 32);
+    } else if (WT == GGUF_MXFP4) {
+        // block p (17 bytes, any alignment): e2m1 code of value l in the low
+        // nibble of code byte l, of value l + 16 in the high one
+        uint32_t e, qw[4];
+        ld_mxfp4_block(row + p * MXFP4_BYTES, e, qw);
+        const float d = e8m0_half(e);
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const uint32_t byte = (qw[i >> 2] >> (8 * (i & 3))) & 0xff;
+            const int k0 = mxfp4_k(byte & 15), k1 = mxfp4_k(byte >> 4);
+            const float a0 = __fmul_rn(d, (float)(k0 < 0 ? -k0 : k0)), a1 = __fmul_rn(d, (float)(k1 < 0 ? -k1 : k1));
+            v[i] = (byte & 8) ? -a0 : a0;
+            v[16 + i] = (byte & 0x80) ? -a1 : a1;
         }
         if (zero) for (int i = 0; i < 32; i++) v[i] = 0.0f;
         store_run<OT>(out, obase + p * 32, v, 32);
@@ -185,6 +202,9 @@ __global__ void block_dots_kernel(const uint8_t *__restrict__ w, int64_t n, int6
         } else if (WT == GGUF_Q4_0) {
             const uint8_t byte = row[(kk / 32) * Q4_0_BYTES + 2 + (kk % 16)];
             qw = ((kk % 32) < 16 ? (byte & 15) : (byte >> 4)) - 8;
+        } else if (WT == GGUF_MXFP4) {
+            const uint8_t byte = row[(kk / 32) * MXFP4_BYTES + 1 + (kk % 16)];
+            qw = mxfp4_k((kk % 32) < 16 ? (byte & 15) : (byte >> 4));
         } else if (WT == GGUF_Q4_K || WT == GGUF_Q5_K) {
             constexpr bool K5 = WT == GGUF_Q5_K;
             const uint8_t *blk = row + (kk / 256) * (K5 ? Q5_K_BYTES : Q4_K_BYTES);
@@ -218,6 +238,7 @@ cudaError_t launch_dequantize(const uint8_t *w, int wt, int64_t rows, int64_t k,
     case GGUF_Q4_0: DQT(GGUF_Q4_0); break;
     case GGUF_Q4_K: DQT(GGUF_Q4_K); break;
     case GGUF_Q5_K: DQT(GGUF_Q5_K); break;
+    case GGUF_MXFP4: DQT(GGUF_MXFP4); break;
     case GGUF_Q6_K: DQT(GGUF_Q6_K); break;
     default: return cudaErrorInvalidValue;
     }
@@ -251,6 +272,7 @@ cudaError_t launch_block_dots(const uint8_t *w, int wt, int64_t n, int64_t k, co
     case GGUF_Q4_0: block_dots_kernel<GGUF_Q4_0><<<grid, 256, 0, s>>>(w, n, k, rb, xq, m, sums); break;
     case GGUF_Q4_K: block_dots_kernel<GGUF_Q4_K><<<grid, 256, 0, s>>>(w, n, k, rb, xq, m, sums); break;
     case GGUF_Q5_K: block_dots_kernel<GGUF_Q5_K><<<grid, 256, 0, s>>>(w, n, k, rb, xq, m, sums); break;
+    case GGUF_MXFP4: block_dots_kernel<GGUF_MXFP4><<<grid, 256, 0, s>>>(w, n, k, rb, xq, m, sums); break;
     case GGUF_Q6_K: block_dots_kernel<GGUF_Q6_K><<<grid, 256, 0, s>>>(w, n, k, rb, xq, m, sums); break;
     default: return cudaErrorInvalidValue;
     }

@@ -125,6 +125,7 @@ cudaError_t launch_mmq(const uint8_t *w, int wt, int64_t n, int64_t k, const uin
     case GGUF_Q8_0: return launch_mmq_ot<GGUF_Q8_0>(w, n, k, xh, xl, m, y, yt, ldy, yacc, s);
     case GGUF_Q4_0: return launch_mmq_ot<GGUF_Q4_0>(w, n, k, xh, xl, m, y, yt, ldy, yacc, s);
     case GGUF_Q5_K: return launch_mmq_ot<GGUF_Q5_K>(w, n, k, xh, xl, m, y, yt, ldy, yacc, s);
+    case GGUF_MXFP4: return launch_mmq_ot<GGUF_MXFP4>(w, n, k, xh, xl, m, y, yt, ldy, yacc, s);
     default: return cudaErrorInvalidValue;
     }
 }

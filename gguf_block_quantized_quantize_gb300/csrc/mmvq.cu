@@ -28,14 +28,15 @@ cudaError_t launch_mmvq(const MmvqSegs &sg, int wt, int64_t k, const uint8_t *xq
     case GGUF_Q6_K: return launch_mmvq_q6_k(sg, k, xq, m, yt, s);
     case GGUF_Q4_0: return launch_mmvq_q4_0(sg, k, xq, m, yt, s);
     case GGUF_Q5_K: return launch_mmvq_q5_k(sg, k, xq, m, yt, s);
+    case GGUF_MXFP4: return launch_mmvq_mxfp4(sg, k, xq, m, yt, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
 bool mmvq_routes_supported(int wt, int64_t k) {
     const int64_t values = wt == GGUF_Q8_0 ? 32 : 64;   // values per thread's piece
-    return (wt == GGUF_Q8_0 || wt == GGUF_Q4_0 || wt == GGUF_Q4_K || wt == GGUF_Q5_K || wt == GGUF_Q6_K) && k > 0 &&
-           (k + values - 1) / values <= 256;
+    return (wt == GGUF_Q8_0 || wt == GGUF_Q4_0 || wt == GGUF_Q4_K || wt == GGUF_Q5_K || wt == GGUF_Q6_K ||
+            wt == GGUF_MXFP4) && k > 0 && (k + values - 1) / values <= 256;
 }
 
 cudaError_t launch_mmvq_routes(int wt, const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k,
@@ -46,6 +47,7 @@ cudaError_t launch_mmvq_routes(int wt, const uint8_t *bank, const MmvqRoutes &rt
     case GGUF_Q4_K: return launch_mmvq_routes_q4_k(bank, rt, n, k, xq, routes, z, s);
     case GGUF_Q4_0: return launch_mmvq_routes_q4_0(bank, rt, n, k, xq, routes, z, s);
     case GGUF_Q5_K: return launch_mmvq_routes_q5_k(bank, rt, n, k, xq, routes, z, s);
+    case GGUF_MXFP4: return launch_mmvq_routes_mxfp4(bank, rt, n, k, xq, routes, z, s);
     default: return launch_mmvq_routes_q6_k(bank, rt, n, k, xq, routes, z, s);
     }
 }

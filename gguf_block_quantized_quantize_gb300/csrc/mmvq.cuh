@@ -2,6 +2,7 @@
 // (decode).  y[m][n] = sum over the row's sub-blocks of an exact int32 block
 // dot product combined with the fp32 block scales:
 //   Q8_0, Q4_0: d_w * d_a * S          (Q4_0: S over q - 8)
+//   MXFP4:      2^(e - 128) * d_a * S  (S over k = 2 * e2m1(q))
 //   Q4_K, Q5_K: d * s_j * d_a * S_j - dmin * m_j * s_a
 //   Q6_K:       d * sc_j * d_a * S_j
 // (FreeToken PR #690 "serve GGUF checkpoints on vendored ggml-cuda kernels",
@@ -14,7 +15,7 @@
 // coalesced loads, and the arithmetic per byte is kept small enough to hide
 // under those loads:
 //   * K is split across the threads of a CTA: thread t owns "piece" t of every
-//     row (64 values for the K-quants and Q4_0, 32 for Q8_0).  Its q8_1 activation quants
+//     row (64 values for the K-quants, Q4_0 and MXFP4, 32 for Q8_0).  Its q8_1 activation quants
 //     for that piece are loaded once into registers and reused for every row
 //     the CTA visits, so activations cost no bandwidth in the row loop.  For
 //     8 tokens, two threads share a piece and take 4 tokens each, which halves
@@ -366,6 +367,138 @@ struct Q40Piece {
                     S = dp4a_us(lo[4 * b + i], a.q[mm][8 * b + i], S);
                     S = dp4a_us(hi[4 * b + i], a.q[mm][8 * b + 4 + i], S);
                 }
+                v = fmaf(d[b] * a.f[mm][b], (float)S, v);
+            }
+            acc[mm] = v;
+        }
+    }
+};
+
+// 16 bytes at any shared-memory address as four words (aligned words plus a
+// funnel shift)
+__device__ __forceinline__ void lds16_a1(const uint8_t *p, uint32_t (&o)[4]) {
+    const uint32_t *b = reinterpret_cast<const uint32_t *>(reinterpret_cast<uintptr_t>(p) & ~uintptr_t(3));
+    const int sh = 8 * (int)(reinterpret_cast<uintptr_t>(p) & 3);
+    uint32_t w[5];
+#pragma unroll
+    for (int i = 0; i < 5; i++) w[i] = b[i];
+#pragma unroll
+    for (int i = 0; i < 4; i++) o[i] = __funnelshift_r(w[i], w[i + 1], sh);
+}
+
+// MXFP4 as Q4_0: two 17-byte blocks per piece (the second absent at the end of
+// a row of an odd number of blocks), a warp's 64 blocks staged as one span of
+// up to 1088 bytes; the blocks have no alignment at all, so the span's tail
+// is read byte by byte.  Codes become biased bytes 16 + k (mxfp4_biased4), in
+// the order (l, l + 16, l + 1, l + 17) that one 16-bit selector gives; the
+// activation words are interleaved the same way once, when they are loaded,
+// and S = sum((16 + k) * q_a) - 16 * sum(q_a) is exact.
+struct MX4Piece {
+    static constexpr int VALUES = 64;
+    static constexpr bool STAGED = true;
+    static constexpr int STAGE_CHUNKS = 72;   // 16-byte chunks of a warp's buffer (1088 + 15 bytes, + reads)
+    using Pos = Q40Piece::Pos;
+    struct W { uint4 c[3]; uint32_t t; uint32_t head; };
+    struct Wf { uint32_t q[8]; uint32_t e; };   // code words of both blocks; e = e0 | e1 << 8
+    template <int M>
+    struct A {
+        int q[M][16];    // activation quants of both blocks, interleaved as the biased codes
+        float f[M][2];   // d_a of each block
+        int sum[M][2];   // 16 * sum of each block's quants
+    };
+    template <int TG>
+    static __device__ __forceinline__ Pos pos(int64_t p, int tg, int64_t k) {
+        constexpr int PW = 32 / TG, BW = 2 * PW;
+        const int64_t nb = k / 32, w = p / PW, left = nb - BW * w;
+        Pos q;
+        q.p = p;
+        q.lane = (int)((p * TG + tg) & 31);
+        q.span_off = (int)(w * BW * MXFP4_BYTES);
+        q.span_len = (int)((left < BW ? (left > 0 ? left : 0) : BW) * MXFP4_BYTES);
+        q.fld = (int)(p % PW) * 2 * MXFP4_BYTES;
+        q.two = 2 * p + 1 < nb;
+        return q;
+    }
+    static __device__ __forceinline__ void load(W &w, const uint8_t *row, const Pos &q) {
+        const uint8_t *a = row + q.span_off;
+        const uint32_t head = (uint32_t)(reinterpret_cast<uintptr_t>(a) & 15);
+        const uint4 *c0 = reinterpret_cast<const uint4 *>(a - head);
+        const int full = (int)(head + q.span_len) >> 4;
+#pragma unroll
+        for (int i = 0; i < 3; i++) {
+            const int c = q.lane + 32 * i;
+            w.c[i] = c < full ? __ldg(c0 + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        const int tail = (int)((head + q.span_len) & 15);   // bytes
+        w.t = q.lane < tail ? (uint32_t)reinterpret_cast<const uint8_t *>(c0 + full)[q.lane] : 0u;
+        w.head = head;
+    }
+    static __device__ __forceinline__ void prepare(const W &w, const Pos &q, uint4 *buf, Wf &f) {
+        const int full = (int)(w.head + q.span_len) >> 4;
+#pragma unroll
+        for (int i = 0; i < 3; i++) {
+            const int c = q.lane + 32 * i;
+            if (c < full) buf[c] = w.c[i];
+        }
+        const int tail = (int)((w.head + q.span_len) & 15);
+        if (q.lane < tail) reinterpret_cast<uint8_t *>(buf + full)[q.lane] = (uint8_t)w.t;
+        __syncwarp();
+        const uint8_t *blk = reinterpret_cast<const uint8_t *>(buf) + w.head + q.fld;
+        uint32_t lo[4], hi[4];
+        lds16_a1(blk + 1, lo);
+        lds16_a1(blk + 1 + MXFP4_BYTES, hi);
+        f.e = (uint32_t)blk[0] | ((uint32_t)blk[MXFP4_BYTES] << 8);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            f.q[i] = lo[i];
+            f.q[4 + i] = hi[i];   // an absent second block meets zero activations
+        }
+        __syncwarp();   // every lane holds its blocks before the buffer is rewritten
+    }
+    template <int M>
+    static __device__ __forceinline__ void load_act(A<M> &a, const uint8_t *xq, int64_t xrb, int m_act,
+                                                    const Pos &q, bool valid) {
+#pragma unroll
+        for (int mm = 0; mm < M; mm++) {
+#pragma unroll
+            for (int b = 0; b < 2; b++) {
+                const bool on = valid && mm < m_act && (b == 0 || q.two);
+                const uint8_t *blk = xq + mm * xrb + (on ? 2 * q.p + b : 0) * Q8_1_BYTES;
+                a.f[mm][b] = on ? h2f(ld_u16(blk)) : 0.0f;
+                int x[8], sum = 0;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    x[i] = on ? (int)ld_u32(blk + 4 + 4 * i) : 0;
+                    sum = dp4a_ss(x[i], 0x01010101, sum);
+                }
+                // code word j covers values 4j..4j+3 (low nibbles) and 16+4j.. (high):
+                // its two selectors give (4j, 16+4j, 4j+1, 17+4j), (4j+2, 18+4j, 4j+3, 19+4j)
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    a.q[mm][8 * b + 2 * j] = (int)__byte_perm((uint32_t)x[j], (uint32_t)x[4 + j], 0x5140);
+                    a.q[mm][8 * b + 2 * j + 1] = (int)__byte_perm((uint32_t)x[j], (uint32_t)x[4 + j], 0x7362);
+                }
+                a.sum[mm][b] = 16 * sum;
+            }
+        }
+    }
+    template <int M>
+    static __device__ __forceinline__ void dot(const Wf &w, const A<M> &a, const Pos &, float (&acc)[M]) {
+        const float d[2] = {e8m0_half(w.e & 0xff), e8m0_half((w.e >> 8) & 0xff)};
+        uint32_t u[16];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            u[2 * i] = mxfp4_biased4(w.q[i]);
+            u[2 * i + 1] = mxfp4_biased4(w.q[i] >> 16);
+        }
+#pragma unroll
+        for (int mm = 0; mm < M; mm++) {
+            float v = acc[mm];
+#pragma unroll
+            for (int b = 0; b < 2; b++) {
+                int S = -a.sum[mm][b];
+#pragma unroll
+                for (int i = 0; i < 8; i++) S = dp4a_us(u[8 * b + i], a.q[mm][8 * b + i], S);
                 v = fmaf(d[b] * a.f[mm][b], (float)S, v);
             }
             acc[mm] = v;
@@ -941,6 +1074,7 @@ cudaError_t launch_mmvq_q4_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, i
 cudaError_t launch_mmvq_q6_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
 cudaError_t launch_mmvq_q4_0(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
 cudaError_t launch_mmvq_q5_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
+cudaError_t launch_mmvq_mxfp4(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
 cudaError_t launch_mmvq_routes_q8_0(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,
                                     int64_t routes, float *z, cudaStream_t s);
 cudaError_t launch_mmvq_routes_q4_k(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,
@@ -951,5 +1085,7 @@ cudaError_t launch_mmvq_routes_q4_0(const uint8_t *bank, const MmvqRoutes &rt, i
                                     int64_t routes, float *z, cudaStream_t s);
 cudaError_t launch_mmvq_routes_q5_k(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,
                                     int64_t routes, float *z, cudaStream_t s);
+cudaError_t launch_mmvq_routes_mxfp4(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k,
+                                     const uint8_t *xq, int64_t routes, float *z, cudaStream_t s);
 
 }  // namespace gg

@@ -260,6 +260,7 @@ static cudaError_t launch_moe_mode(int wt, const TgParams &p, int64_t rows, cuda
     case GGUF_Q8_0: return tg_launch<GGUF_Q8_0, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, p, grid, s);
     case GGUF_Q4_0: return tg_launch<GGUF_Q4_0, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, p, grid, s);
     case GGUF_Q5_K: return tg_launch<GGUF_Q5_K, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, p, grid, s);
+    case GGUF_MXFP4: return tg_launch<GGUF_MXFP4, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, p, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }

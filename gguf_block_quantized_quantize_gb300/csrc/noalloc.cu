@@ -46,7 +46,8 @@ static gguf_status noalloc_scratch(uint8_t **out) {
 
 static bool is_float_t(int t) { return t == GGUF_F32 || t == GGUF_F16 || t == GGUF_BF16; }
 static bool is_weight_t(int t) {
-    return t == GGUF_Q8_0 || t == GGUF_Q4_0 || t == GGUF_Q4_K || t == GGUF_Q5_K || t == GGUF_Q6_K;
+    return t == GGUF_Q8_0 || t == GGUF_Q4_0 || t == GGUF_Q4_K || t == GGUF_Q5_K || t == GGUF_Q6_K ||
+           t == GGUF_MXFP4;
 }
 static bool aligned_to(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -57,7 +58,7 @@ using namespace gg;
 extern "C" gguf_status gguf_mul_mat_noalloc(const void *w, int wt, int64_t n, int64_t k, const void *x, int xt,
                                             int64_t m, int64_t ldx, void *y, int yt, int64_t ldy,
                                             gguf_stream_t stream) {
-    if (!is_weight_t(wt)) return report(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat_noalloc: weight type not Q8_0/Q4_0/Q4_K/Q5_K/Q6_K");
+    if (!is_weight_t(wt)) return report(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat_noalloc: weight type not Q8_0/Q4_0/Q4_K/Q5_K/Q6_K/MXFP4");
     if (!is_float_t(xt)) return report(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat_noalloc: x type is not F32/BF16/F16");
     if (!is_float_t(yt)) return report(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat_noalloc: y type is not F32/BF16/F16");
     if (n < 0 || k < 0 || m < 0) return report(GGUF_ERR_INVALID_ARG, "mul_mat_noalloc: negative size");

@@ -1,5 +1,5 @@
 // Weight unpack for the tensor-core GEMM: packed Q4_K / Q5_K / Q6_K / Q8_0 /
-// Q4_0 bytes of a
+// Q4_0 / MXFP4 bytes of a
 // weight row -> fp16 operand values (each the exact fp32 value of the block
 // formula rounded once, or packed-half math where the product is rounded to a
 // 16-bit output anyway), stored as 16-byte chunks of a 128-byte-swizzled
@@ -8,8 +8,8 @@
 // Unit of work ("task"): one weight row, one 64-value K-step, one of PARTS
 // parts of it (halves for Q4_K and Q8_0, quarters for Q6_K); a task yields
 // CHUNKS 8-value chunks (16-byte fp16 chunks of the swizzled row), chunk e of
-// part j at position chunk(j, e) of the row.  (Halves for Q4_K, Q5_K, Q8_0
-// and Q4_0.)  Consecutive lanes take the parts
+// part j at position chunk(j, e) of the row.  (Halves for Q4_K, Q5_K, Q8_0,
+// Q4_0 and MXFP4.)  Consecutive lanes take the parts
 // of one row, so a warp-wide load reads contiguous bytes of 16 (8) rows, and
 // every packed byte is read once.
 #pragma once
@@ -319,6 +319,48 @@ struct KQ<GGUF_Q4_0> {
                 out[8 + 2 * i + p] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(bytes_to_h2_1024(hi, p)), k1032), d2));
             }
         }
+    }
+};
+
+// MXFP4: as Q4_0, K-step ks is blocks 2ks and 2ks + 1 (absent past the end when
+// K % 64 == 32), half j block 2ks + j: 17 bytes at any address, the E8M0
+// exponent then the codes of values 0..15 (low nibbles) and 16..31 (high).
+template <>
+struct KQ<GGUF_MXFP4> {
+    static constexpr int PARTS = 2, CHUNKS = 4;
+    static __device__ __forceinline__ int chunk(int j, int e) { return 4 * j + e; }
+    uint32_t q[4], e;
+    __device__ __forceinline__ void load(const uint8_t *row, int ks, int j, int64_t kblocks) {
+        const int64_t b = 2 * (int64_t)ks + j;
+        if (b < kblocks) {
+            ld_mxfp4_block(row + b * MXFP4_BYTES, e, q);
+        } else {
+            e = 0u;
+#pragma unroll
+            for (int i = 0; i < 4; i++) q[i] = 0x88888888u;   // code 8: -0
+        }
+    }
+    // 2^(e - 128) * k, exact in fp32 (or inf past its range)
+    __device__ __forceinline__ void unpack_f32(int, float (&v)[32]) const {
+        const float d = e8m0_half(e);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            // biased bytes of values (4i, 16+4i, 4i+1, 17+4i) and (4i+2, 18+4i, 4i+3, 19+4i)
+            const uint32_t u0 = mxfp4_biased4(q[i]), u1 = mxfp4_biased4(q[i] >> 16);
+            const uint32_t lo = __byte_perm(u0, u1, 0x6420), hi = __byte_perm(u0, u1, 0x7531);
+#pragma unroll
+            for (int b = 0; b < 4; b++) {
+                v[4 * i + b] = __fmul_rn(d, byte_to_f(lo, b, -8388624.0f));
+                v[16 + 4 * i + b] = __fmul_rn(d, byte_to_f(hi, b, -8388624.0f));
+            }
+        }
+    }
+    // the block factor can lie outside the fp16 range: round the exact fp32 values once
+    __device__ __forceinline__ void unpack_h2(int ks, uint32_t (&out)[16]) const {
+        float v[32];
+        unpack_f32(ks, v);
+#pragma unroll
+        for (int i = 0; i < 16; i++) out[i] = pack_h2(v[2 * i], v[2 * i + 1]);
     }
 };
 

@@ -4,8 +4,8 @@
  *
  * The library computes the hot path of a GGUF serving engine: activations in
  * fp32 / bf16 / fp16 are quantized to q8_1 blocks of 32 and multiplied against
- * Q8_0 / Q4_0 / Q4_K / Q5_K / Q6_K weight blocks with per-block integer dot
- * products and an
+ * Q8_0 / Q4_0 / Q4_K / Q5_K / Q6_K / MXFP4 weight blocks with per-block integer
+ * dot products and an
  * fp32 scale / min combination; results come back in the activation dtype
  * with fp32 accumulation (FreeToken PR #690 "serve GGUF checkpoints on
  * vendored ggml-cuda kernels", section "Vendored ggml", list "What the ggml
@@ -31,7 +31,7 @@
  *     come back as GGUF_ERR_CUDA.
  *   - Weight buffers must start on a 16-byte boundary.  Rows are packed back
  *     to back ([rows][row_size] bytes).  K must be a multiple of the type's
- *     block (32 for Q8_0 / Q4_0 / q8_1, 256 for Q4_K / Q5_K / Q6_K: K-quant super-blocks span
+ *     block (32 for Q8_0 / Q4_0 / MXFP4 / q8_1, 256 for Q4_K / Q5_K / Q6_K: K-quant super-blocks span
  *     256 values, 1Cat-vLLM "GGUF on V100: implementation and acceptance control",
  *     section "TP/EP decision").  Offsets are 64-bit: no 2^31-block limit
  *     (FreeToken issue #671, "Known issues").  No kernel reads past the last
@@ -54,8 +54,10 @@
  *   Q5_K 176 B / 256 values: Q4_K's 16-byte header, 32 B of fifth bits (value
  *                            i: bit i/32 of byte i%32), 128 B of low 4 bits
  *                            as Q4_K's quants            v = d*scale_j*q - dmin*min_j
- * Q4_0 and Q5_K are two of the further tensor types the pages list (FreeToken
- * PR #690, "Tensor types"; transformers PR #45977, GgufLinear quant types).
+ *   MXFP4 17 B / 32 values : E8M0 exponent e, 16 B of e2m1 codes in Q4_0's
+ *                            order (OCP microscaling FP4)   v = e2m1(q)*2^(e-127)
+ * Q4_0, Q5_K and MXFP4 are further tensor types the pages list (FreeToken PR
+ * #690, "Tensor types"; transformers PR #45977, GgufLinear quant types).
  */
 #ifndef GGUF_GB300_H
 #define GGUF_GB300_H
@@ -79,7 +81,8 @@ typedef enum {
     GGUF_Q4_K = 12,
     GGUF_Q5_K = 13,
     GGUF_Q6_K = 14,
-    GGUF_BF16 = 30
+    GGUF_BF16 = 30,
+    GGUF_MXFP4 = 39
 } gguf_type;
 
 typedef enum {
@@ -122,11 +125,13 @@ gguf_status gguf_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int6
  * gguf_dequantize -- packed weights to float (FreeToken PR #690, op
  * "dequantize"; same-type float inputs are copied, types without a converter
  * are rejected: same page, summary of the later commits under "Validation").
- *   w   : [rows][row_size(wt, k)] bytes, wt in {Q8_0, Q4_0, Q4_K, Q5_K, Q6_K, Q8_1,
- *         F32, F16, BF16}
+ *   w   : [rows][row_size(wt, k)] bytes, wt in {Q8_0, Q4_0, Q4_K, Q5_K, Q6_K, MXFP4,
+ *         Q8_1, F32, F16, BF16}
  *   out : [rows][k] of type ot in {F32, F16, BF16}
  * Values are computed in fp32 in the order  Q4_K, Q5_K: a = d*s; b = dmin*m;
- * a*q - b;  Q6_K: (d*sc)*(q-32);  Q8_0 / q8_1: d*q;  Q4_0: d*(q-8);  then rounded to ot with
+ * a*q - b;  Q6_K: (d*sc)*(q-32);  Q8_0 / q8_1: d*q;  Q4_0: d*(q-8);  MXFP4:
+ * 2^(e-128) * (2*e2m1(q)), negated for a code with the sign bit (so code 8
+ * gives -0);  then rounded to ot with
  * round-to-nearest-even.  Bit-exact.  Float-to-float calls convert (RNE).
  */
 gguf_status gguf_dequantize(const void *w, int wt, int64_t rows, int64_t k, void *out, int ot,
@@ -144,7 +149,7 @@ gguf_status gguf_get_rows(const void *table, int tt, int64_t rows, int64_t k, co
 
 /*
  * gguf_mul_mat -- y[m][n] = sum_k W[n][k] * X[m][k] for a packed weight W
- * [n][k] (wt in {Q8_0, Q4_0, Q4_K, Q5_K, Q6_K}) and activations X [m][k].
+ * [n][k] (wt in {Q8_0, Q4_0, Q4_K, Q5_K, Q6_K, MXFP4}) and activations X [m][k].
  *   x  : [m][ldx] of type xt in {F32, BF16, F16} (quantized to q8_1 inside,
  *        into ws), or xt = GGUF_Q8_1: pre-quantized rows of row_size(Q8_1,k)
  *        bytes (ldx is then ignored) -- the way one q8_1 quantization serves
@@ -324,8 +329,9 @@ gguf_status gguf_moe_ffn(const gguf_moe_ffn_args *args, void *ws, size_t ws_byte
 
 /*
  * gguf_debug_block_dots -- test hook: the exact int32 dot product of every
- * weight sub-block (32 values for Q8_0 / Q4_0 / Q4_K / Q5_K, 16 for Q6_K; Q4_0
- * and Q6_K quants enter with their offsets 8 and 32 subtracted) with the matching
+ * weight sub-block (32 values for Q8_0 / Q4_0 / Q4_K / Q5_K / MXFP4, 16 for Q6_K;
+ * Q4_0 and Q6_K quants enter with their offsets 8 and 32 subtracted, MXFP4
+ * codes as 2 * e2m1) with the matching
  * q8_1 activation quants.  sums : [m][n][k / sub] int32.  Bit-exact.
  */
 gguf_status gguf_debug_block_dots(const void *w, int wt, int64_t n, int64_t k, const void *xq, int64_t m,

@@ -46,6 +46,8 @@ def test_type_table(g):
     assert L.gguf_type_block_elems(g.Q4_0) == 32 and L.gguf_type_block_bytes(g.Q4_0) == 18
     assert L.gguf_type_block_elems(g.Q5_K) == 256 and L.gguf_type_block_bytes(g.Q5_K) == 176
     assert g.gguf_row_size(g.Q4_0, 4128) == 2322 and g.gguf_row_size(g.Q5_K, 2048) == 1408
+    assert L.gguf_type_block_elems(g.MXFP4) == 32 and L.gguf_type_block_bytes(g.MXFP4) == 17
+    assert g.gguf_row_size(g.MXFP4, 4128) == 2193
     assert g.gguf_row_size(g.Q4_K, 4096) == 2304 and g.gguf_row_size(g.Q6_K, 3072) == 2520
     assert g.gguf_row_size(g.Q4_K, 100) == -1 and L.gguf_type_block_bytes(99) == 0
 

@@ -39,10 +39,10 @@ def _weights(wt, n, k, seed, safe=False):
     return oracle.quantize_weights(wt, synth.normal((n, k), 0.02, seed))
 
 
-@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K])
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.MXFP4])
 @pytest.mark.parametrize("m", [9, 16, 17, 32, 64, 100, 128, 256, 300])
 def test_mmq_bf16_shapes(g, wt, m):
-    n, k = 300, 1056 if wt in (oracle.Q8_0, oracle.Q4_0) else 1024   # ragged n; Q8_0 / Q4_0 k % 64 == 32
+    n, k = 300, 1056 if wt in (oracle.Q8_0, oracle.Q4_0, oracle.MXFP4) else 1024   # ragged n; k % 64 == 32 where it can
     w = _weights(wt, n, k, seed=m, safe=(m % 2 == 1))
     x = synth.activations(m, k, seed=m + 1, dtype=torch.bfloat16)
     ref = oracle.mul_mat(wt, w, k, oracle.quantize_q8_1(x.float().numpy()))
@@ -51,7 +51,7 @@ def test_mmq_bf16_shapes(g, wt, m):
     assert_close(y.float().cpu().numpy(), ref, TOL_BF16, f"mmq type {wt} m {m}")
 
 
-@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K])
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.MXFP4])
 @pytest.mark.parametrize("m", [12, 40, 200])
 def test_mmq_fp32_output(g, wt, m):
     n, k = 257, 2048

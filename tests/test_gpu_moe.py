@@ -231,7 +231,7 @@ def test_gate_up_h512(g, path):
     assert same.mean() > 0.995, same.mean()
 
 
-@pytest.mark.parametrize("wt", [oracle.Q4_0, oracle.Q5_K, oracle.Q8_0, oracle.Q6_K])
+@pytest.mark.parametrize("wt", [oracle.Q4_0, oracle.Q5_K, oracle.Q8_0, oracle.Q6_K, oracle.MXFP4])
 def test_gate_up_bank_types(g, path, wt):
     """gate_up with every weight type of the bank, through both paths: the
     bf16 h against the oracle's, inactive routes zero."""
@@ -250,18 +250,19 @@ def test_gate_up_bank_types(g, path, wt):
     assert_close(hb[active], h_ref[active], TOL_BF16, f"gate_up type {wt} ({path})")
 
 
-def test_vec_down_q4_0_odd_blocks(g):
-    # a Q4_0 down bank with I = 96 (three blocks per row): the route-batched
-    # MMVQ's last piece holds one block
+@pytest.mark.parametrize("wt", [oracle.Q4_0, oracle.MXFP4])
+def test_vec_down_two_block_pieces_odd_blocks(g, wt):
+    # a Q4_0 / MXFP4 down bank with I = 96 (three blocks per row): the
+    # route-batched MMVQ's last piece holds one block
     E, K, H, I, T = 3, 2, 256, 96, 5
-    bank_d = _bank(oracle.Q4_0, E, H, I, 77, True)
+    bank_d = _bank(wt, E, H, I, 77, True)
     sd = bank_d.nbytes // E
     ids, rw = synth.routes(T, E, K, seed=78)
     hq = oracle.quantize_q8_1(synth.normal((T * K, I), 1.0, seed=79))
-    ref = oracle.moe_down(oracle.Q4_0, bank_d, E, sd, H, I, hq, ids, rw)
-    y = g.gguf_mul_mat_id(_u8(bank_d), oracle.Q4_0, E, sd, H, I, _u8(hq), _u8(ids), g.DOWN_WEIGHTED_SUM,
+    ref = oracle.moe_down(wt, bank_d, E, sd, H, I, hq, ids, rw)
+    y = g.gguf_mul_mat_id(_u8(bank_d), wt, E, sd, H, I, _u8(hq), _u8(ids), g.DOWN_WEIGHTED_SUM,
                           route_w=_u8(rw), xt=g.Q8_1, out_type=g.F32).cpu().numpy()
-    assert_close(y, ref, TOL_F32, "vec down Q4_0 I=96")
+    assert_close(y, ref, TOL_F32, f"vec down type {wt} I=96")
 
 
 # ---------------------------------------------------------------- vector path (few tokens)
@@ -323,7 +324,7 @@ def test_vec_gate_up_outputs(g, T):
     assert_close(hb2[active], hb[active], TOL_BF16, f"vec vs tensor-core gate_up T {T}")
 
 
-@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K])
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.MXFP4])
 @pytest.mark.parametrize("T", [1, 5, 16])
 def test_vec_down_from_oracle_h(g, wt, T):
     E, K, H, I = 4, 3, 512, 256
@@ -345,7 +346,7 @@ def test_vec_down_from_oracle_h(g, wt, T):
 
 
 @pytest.mark.parametrize("T", [1, 2, 16])
-@pytest.mark.parametrize("down", [oracle.Q6_K, oracle.Q4_K, oracle.Q5_K, oracle.Q4_0])
+@pytest.mark.parametrize("down", [oracle.Q6_K, oracle.Q4_K, oracle.Q5_K, oracle.Q4_0, oracle.MXFP4])
 def test_vec_moe_ffn_end_to_end(g, T, down):
     E, K, H, I = 6, 4, 256, 256
     bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 1000 + T, False)

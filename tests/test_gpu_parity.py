@@ -80,11 +80,11 @@ def _weights(wt, n, k, seed, safe=False):
     return oracle.quantize_weights(wt, synth.normal((n, k), 0.02, seed) * synth.lognormal_row_scale(n, seed + 1))
 
 
-@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K])
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.MXFP4])
 @pytest.mark.parametrize("safe", [False, True])
 @pytest.mark.parametrize("ot", [oracle.F32, oracle.BF16, oracle.F16])
 def test_dequantize_bit_exact(g, wt, safe, ot):
-    n, k = 37, 800 if wt in (oracle.Q8_0, oracle.Q4_0) else 768
+    n, k = 37, 800 if wt in (oracle.Q8_0, oracle.Q4_0, oracle.MXFP4) else 768
     w = _weights(wt, n, k, seed=7, safe=safe)
     ref = oracle.dequantize(wt, w, k, ot)
     out = g.gguf_dequantize(_u8(w), wt, n, k, out_dtype={0: torch.float32, 30: torch.bfloat16, 1: torch.float16}[ot])
@@ -93,18 +93,18 @@ def test_dequantize_bit_exact(g, wt, safe, ot):
                                   ref.view(np.uint32) if ot == oracle.F32 else ref)
 
 
-@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K])
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.MXFP4])
 def test_dequantize_odd_rows_unaligned_blocks(g, wt):
     # K = one block per row: Q6_K (210 B), Q8_0 (34 B) and Q4_0 (18 B) rows
-    # alternate alignment
-    k = 32 if wt in (oracle.Q8_0, oracle.Q4_0) else 256
+    # alternate alignment; MXFP4 rows (17 B) start at every byte offset
+    k = 32 if wt in (oracle.Q8_0, oracle.Q4_0, oracle.MXFP4) else 256
     w = _weights(wt, 33, k, seed=8, safe=True)
     ref = oracle.dequantize(wt, w, k, oracle.F32)
     got = g.gguf_dequantize(_u8(w), wt, 33, k).cpu().numpy()
     np.testing.assert_array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
-@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K])
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.MXFP4])
 def test_get_rows_bit_exact(g, wt):
     rows, k = 1000, 512
     w = _weights(wt, rows, k, seed=9, safe=True)
@@ -126,7 +126,7 @@ def test_get_rows_llama_embedding_shape(g):
 
 # ---------------------------------------------------------------- block dots
 
-@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K])
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.MXFP4])
 def test_block_dots_bit_exact(g, wt):
     n, k, m = 19, 1024, 3
     w = _weights(wt, n, k, seed=11, safe=True)
@@ -139,7 +139,7 @@ def test_block_dots_bit_exact(g, wt):
 
 # ---------------------------------------------------------------- mul_mat (MMVQ)
 
-@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K])
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.MXFP4])
 @pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 8])
 @pytest.mark.parametrize("safe", [False, True])
 def test_mmvq_fp32(g, wt, m, safe):
@@ -151,7 +151,7 @@ def test_mmvq_fp32(g, wt, m, safe):
     assert_close(y, ref, TOL_F32, f"mmvq type {wt} m {m}")
 
 
-@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K])
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.MXFP4])
 @pytest.mark.parametrize("k", [256, 768, 3072, 8192, 16384])
 @pytest.mark.parametrize("m", [1, 4, 7])
 def test_mmvq_k_range_bf16(g, wt, k, m):
@@ -166,17 +166,19 @@ def test_mmvq_k_range_bf16(g, wt, k, m):
     assert_close(y.float().cpu().numpy(), ref, TOL_BF16, f"mmvq bf16 type {wt} k {k} m {m}")
 
 
+@pytest.mark.parametrize("wt", [oracle.Q4_0, oracle.MXFP4])
 @pytest.mark.parametrize("k", [32, 96, 2080, 16352])
 @pytest.mark.parametrize("m", [1, 3, 5, 8])
-def test_mmvq_q4_0_odd_block_count(g, k, m):
-    # Q4_0 pieces are block pairs: an odd number of blocks per row leaves a
-    # last piece of one block (k = 32: a single half piece; 16352: 511 blocks)
+def test_mmvq_two_block_pieces_odd_block_count(g, wt, k, m):
+    # Q4_0 / MXFP4 pieces are block pairs: an odd number of blocks per row
+    # leaves a last piece of one block (k = 32: a single half piece; 16352:
+    # 511 blocks); MXFP4 rows of an odd number of blocks start at odd bytes
     n = 197
-    w = _weights(oracle.Q4_0, n, k, seed=k + m, safe=True)
+    w = _weights(wt, n, k, seed=k + m, safe=True)
     x = synth.activations(m, k, seed=k - m, dtype=torch.float32)
-    ref = oracle.mul_mat(oracle.Q4_0, w, k, oracle.quantize_q8_1(x.numpy()))
-    y = g.gguf_mul_mat(_u8(w), oracle.Q4_0, n, k, x.to(DEV)).cpu().numpy()
-    assert_close(y, ref, TOL_F32, f"mmvq Q4_0 k {k} m {m}")
+    ref = oracle.mul_mat(wt, w, k, oracle.quantize_q8_1(x.numpy()))
+    y = g.gguf_mul_mat(_u8(w), wt, n, k, x.to(DEV)).cpu().numpy()
+    assert_close(y, ref, TOL_F32, f"mmvq type {wt} k {k} m {m}")
 
 
 @pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K])
@@ -301,7 +303,8 @@ def test_mmvq_tensor_core_q6_k_exact_integer_sums(g, m, n):
 
 
 @pytest.mark.parametrize("wt,n,k", [(oracle.Q6_K, 40000, 3072), (oracle.Q4_K, 20000, 3072),
-                                    (oracle.Q5_K, 20000, 3072), (oracle.Q4_0, 20000, 4096)])
+                                    (oracle.Q5_K, 20000, 3072), (oracle.Q4_0, 20000, 4096),
+                                    (oracle.MXFP4, 20000, 4128)])
 @pytest.mark.parametrize("m", [1, 2, 8])
 def test_mmvq_tall_sampled(g, wt, n, k, m):
     # tall matrices take the R = 1 / R = 4 row groupings; rows sampled for the oracle

@@ -32,7 +32,7 @@ def _u8(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
-@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K])
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.MXFP4])
 @pytest.mark.parametrize("m", [1, 3, 6, 8, 40])
 def test_segments_match_oracle(g, wt, m):
     k = 1024

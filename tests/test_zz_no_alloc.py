@@ -33,7 +33,7 @@ def _u8(a):
 
 
 @pytest.mark.parametrize("wt,n,k", [(oracle.Q4_K, 1000, 4096), (oracle.Q6_K, 333, 2048), (oracle.Q8_0, 517, 16384),
-                                    (oracle.Q4_0, 301, 4128), (oracle.Q5_K, 257, 2048)])
+                                    (oracle.Q4_0, 301, 4128), (oracle.Q5_K, 257, 2048), (oracle.MXFP4, 263, 4128)])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_noalloc_matches_mul_mat_on_consecutive_calls(g, wt, n, k, dtype):
     w = _u8(oracle.quantize_weights(wt, synth.normal((n, k), 0.02, seed=n)))
