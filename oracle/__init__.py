@@ -59,6 +59,7 @@ def lib():
             "orc_dequantize_row": (i32, [i32, p, i64, p]),
             "orc_dequantize_row_f64": (i32, [i32, p, i64, p]),
             "orc_dequantize": (i32, [i32, p, i64, i64, p, i32]),
+            "orc_moe_plain": (i32, [i32, p, i64, i64, i64, i64, p, p, i64, i64, p]),
             "orc_get_rows": (i32, [i32, p, i64, i64, p, i64, p, i32]),
             "orc_block_dots": (i32, [i32, p, i64, i64, p, i64, p]),
             "orc_mul_mat": (i32, [i32, p, i64, i64, p, i64, p]),
@@ -238,6 +239,20 @@ def moe_down(wt: int, bank: np.ndarray, n_experts: int, stride: int, n_out: int,
     t0, t1 = tokens if tokens is not None else (0, n_tokens)
     _ok(lib().orc_moe_down(wt, _ptr(bank), n_experts, stride, n_out, i_dim, _ptr(hq), _ptr(ids), _ptr(rw),
                            n_tokens, top_k, _ptr(y), t0, t1, nthreads), "moe_down")
+    return y
+
+
+def moe_plain(wt: int, bank: np.ndarray, n_experts: int, stride: int, n: int, k: int, xq: np.ndarray,
+              ids: np.ndarray) -> np.ndarray:
+    """fp64 y[T * top_k, n]: route r = t * top_k + j gives W[ids[t, j]] . xq[t]
+    (zero row for an inactive route)."""
+    bank = np.ascontiguousarray(bank, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    n_tokens, top_k = ids.shape
+    y = np.zeros((n_tokens * top_k, n), dtype=np.float64)
+    _ok(lib().orc_moe_plain(wt, _ptr(bank), n_experts, stride, n, k, _ptr(xq), _ptr(ids), n_tokens, top_k, _ptr(y)),
+        "moe_plain")
     return y
 
 

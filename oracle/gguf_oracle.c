@@ -933,3 +933,23 @@ int orc_moe_down(int wt, const uint8_t *bank, int64_t n_experts, int64_t stride,
         for (int t = 0; t < nthreads; t++) pthread_join(th[t], NULL);
     return 0;
 }
+
+/* mul_mat_id without the weighted sum: y[r] = W[ids[r]] . xq[r / top_k] for
+ * every route r = t * top_k + j (x rows per token, shared by the token's
+ * routes), in fp64; an inactive route (id < 0 or >= E) gives a zero row.    */
+int orc_moe_plain(int wt, const uint8_t *bank, int64_t n_experts, int64_t stride, int64_t n, int64_t k,
+                  const uint8_t *xq, const int32_t *ids, int64_t n_tokens, int64_t top_k, double *y) {
+    int64_t rs = orc_row_size(wt, k), xrs = k / 32 * 36;
+    if (rs < 0 || k % 32) return -1;
+    for (int64_t r = 0; r < n_tokens * top_k; r++) {
+        int32_t e = ids[r];
+        for (int64_t c = 0; c < n; c++) {
+            if (e < 0 || e >= n_experts) {
+                y[r * n + c] = 0.0;
+                continue;
+            }
+            y[r * n + c] = dot_row(wt, bank + (int64_t)e * stride + c * rs, k, xq + (r / top_k) * xrs);
+        }
+    }
+    return 0;
+}

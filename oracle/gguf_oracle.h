@@ -49,6 +49,9 @@ int orc_moe_down(int wt, const uint8_t *bank, int64_t n_experts, int64_t stride,
                  const uint8_t *hq, const int32_t *ids, const float *route_w, int64_t n_tokens, int64_t top_k,
                  double *y, int64_t t0, int64_t t1, int nthreads);
 
+int orc_moe_plain(int wt, const uint8_t *bank, int64_t n_experts, int64_t stride, int64_t n, int64_t k,
+                  const uint8_t *xq, const int32_t *ids, int64_t n_tokens, int64_t top_k, double *y);
+
 #ifdef __cplusplus
 }
 #endif

@@ -174,3 +174,30 @@ def test_route_recipe(orc):
     assert ids.min() >= 0 and ids.max() < 256
     np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=1e-6)
     assert np.all(w > 0)
+
+
+def test_moe_plain_rows(orc):
+    """mul_mat_id without the weighted sum: each active route's row equals the
+    dense product of its expert with its token's row; the route-weighted sum
+    of the rows equals moe_down fed the token rows per route; inactive routes
+    are zero rows."""
+    E, T, K, n, k = 3, 5, 2, 64, 512
+    bank = np.concatenate([orc.quantize_weights(orc.Q4_K, synth.normal((n, k), 0.02, seed=80 + e)) for e in range(E)])
+    stride = bank.nbytes // E
+    xq = orc.quantize_q8_1(synth.normal((T, k), 1.0, seed=84))
+    ids, rw = synth.routes(T, E, K, seed=85)
+    ids[0] = [2, 2]
+    ids[1, 1] = -1
+    ids[2, 0] = E + 1
+    y = orc.moe_plain(orc.Q4_K, bank, E, stride, n, k, xq, ids)
+    assert y.shape == (T * K, n)
+    for t in range(T):
+        for j in range(K):
+            r, e = t * K + j, ids[t, j]
+            if 0 <= e < E:
+                np.testing.assert_array_equal(y[r], orc.mul_mat(orc.Q4_K, bank[e * n:(e + 1) * n], k, xq[t:t + 1])[0])
+            else:
+                assert np.all(y[r] == 0)
+    ref = orc.moe_down(orc.Q4_K, bank, E, stride, n, k, np.repeat(xq, K, axis=0), ids, rw)
+    got = (y.reshape(T, K, n) * rw.astype(np.float64)[:, :, None]).sum(axis=1)
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-300)
