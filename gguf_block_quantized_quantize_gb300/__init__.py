@@ -17,7 +17,7 @@ import os
 import torch
 
 F32, F16, Q4_0, Q8_0, Q8_1, Q4_K, Q5_K, Q6_K, BF16, MXFP4 = 0, 1, 2, 8, 9, 12, 13, 14, 30, 39
-GATE_UP_SWIGLU, DOWN_WEIGHTED_SUM = 0, 1
+GATE_UP_SWIGLU, DOWN_WEIGHTED_SUM, PLAIN = 0, 1, 2
 Q8_1_BYTES = 36   # one q8_1 block: fp16 d, fp16 s, 32 int8 quants (a q8_1 row is k / 32 blocks)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -262,7 +262,7 @@ def gguf_mul_mat_id(w: torch.Tensor, wt: int, n_experts: int, expert_stride: int
                     ids: torch.Tensor, mode: int, route_w: torch.Tensor | None = None, xt: int | None = None,
                     out_type: int | None = None, out: torch.Tensor | None = None,
                     dev_status: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
-    """MoE expert product (see include/gguf_gb300.h for the two modes)."""
+    """MoE expert product (see include/gguf_gb300.h for the three modes)."""
     n_tokens, top_k = ids.shape
     if xt is None:
         xt = _TYPE_OF[x.dtype]
@@ -277,7 +277,8 @@ def gguf_mul_mat_id(w: torch.Tensor, wt: int, n_experts: int, expert_stride: int
                 out = torch.empty((n_tokens * top_k, gguf_row_size(Q8_1, i_dim)), dtype=torch.uint8, device=x.device)
         else:
             yt = BF16 if out_type is None else out_type
-            out = torch.empty((n_tokens, n), dtype=_DTYPE_OF[yt], device=x.device)
+            rows = n_tokens * top_k if mode == PLAIN else n_tokens
+            out = torch.empty((rows, n), dtype=_DTYPE_OF[yt], device=x.device)
     else:
         yt = out_type if out_type is not None else (Q8_1 if out.dtype == torch.uint8 else _TYPE_OF[out.dtype])
     args = moe_args(w, wt, n_experts, expert_stride, n, k, x, xt, n_tokens, ldx, ids, top_k, route_w, mode, out,

@@ -360,8 +360,8 @@ static gguf_status check_moe(const gguf_moe_args *a) {
         if (a->n % 128) return fail(GGUF_ERR_SHAPE, "mul_mat_id gate_up: n = 2*I must be a multiple of 128");
         if (a->yt != GGUF_BF16 && a->yt != GGUF_Q8_1 && a->yt != GGUF_F16)
             return fail(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat_id gate_up: out type %d is not BF16/Q8_1/F16", a->yt);
-    } else if (a->mode == GGUF_MOE_DOWN_WEIGHTED_SUM) {
-        if (!is_float(a->yt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat_id down: out type %d", a->yt);
+    } else if (a->mode == GGUF_MOE_DOWN_WEIGHTED_SUM || a->mode == GGUF_MOE_PLAIN) {
+        if (!is_float(a->yt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "mul_mat_id: out type %d", a->yt);
     } else {
         return fail(GGUF_ERR_INVALID_ARG, "mul_mat_id: unknown mode %d", a->mode);
     }
@@ -396,9 +396,10 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
     const int bn = moe_bn(R, a->n_experts);
     cudaError_t e;
     const bool vec = moe_vec(a->n_tokens, a->wt, a->k);
+    const bool plain = a->mode == GGUF_MOE_PLAIN;
     if (vec) {
         // route-batched MMVQ: each active route reads its expert's rows once
-        const int64_t rows = a->mode == GGUF_MOE_GATE_UP_SWIGLU ? a->n_tokens : R;
+        const int64_t rows = a->mode == GGUF_MOE_DOWN_WEIGHTED_SUM ? R : a->n_tokens;
         const uint8_t *xq = (const uint8_t *)a->x;
         if (a->xt != GGUF_Q8_1) {
             if ((e = launch_quantize_q8_1(a->x, a->xt, rows, a->k, a->ldx, (uint8_t *)w.xh, nullptr, nullptr, s)) != cudaSuccess)
@@ -406,9 +407,16 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
             xq = (const uint8_t *)w.xh;
         }
         const bool gu = a->mode == GGUF_MOE_GATE_UP_SWIGLU;
-        if ((e = moe_mark(a->ids, gu ? nullptr : a->route_w, R, a->n_experts, !gu, a->dev_status, w.pos, s)) != cudaSuccess)
+        const bool weighted = a->mode == GGUF_MOE_DOWN_WEIGHTED_SUM;
+        if ((e = moe_mark(a->ids, weighted ? a->route_w : nullptr, R, a->n_experts, weighted, a->dev_status, w.pos, s)) !=
+            cudaSuccess)
             return cuda_status(e, "mul_mat_id routes");
-        const MmvqRoutes rt{a->ids, w.pos, a->expert_stride, a->top_k, gu ? 0 : 1};
+        const MmvqRoutes rt{a->ids, w.pos, a->expert_stride, a->top_k, weighted ? 1 : 0};
+        if (plain) {
+            if ((e = launch_mmvq_routes(a->wt, (const uint8_t *)a->w, rt, a->n, a->k, xq, R, w.z, s)) != cudaSuccess)
+                return cuda_status(e, "mul_mat_id");
+            return cuda_status(launch_moe_plain_store(w.z, w.pos, R, a->n, a->y, a->yt, s), "mul_mat_id store");
+        }
         if (!gu) {
             if ((e = launch_mmvq_routes(a->wt, (const uint8_t *)a->w, rt, a->n, a->k, xq, R, w.z, s)) != cudaSuccess)
                 return cuda_status(e, "mul_mat_id down");
@@ -437,6 +445,16 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
                                a->yt == GGUF_BF16 ? (uint16_t *)a->y : nullptr,
                                a->yt == GGUF_F16 ? (uint16_t *)a->y : nullptr, nullptr, a->n / 2, s);
         return cuda_status(e, "mul_mat_id gate_up");
+    }
+    if (plain) {   // token rows, one output row per route
+        if ((e = to_f16_operand(a->x, a->xt, a->n_tokens, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), s)) != cudaSuccess)
+            return cuda_status(e, "mul_mat_id quantize");
+        if ((e = moe_group(a->ids, nullptr, R, a->n_experts, false, a->dev_status, w, bn, s)) != cudaSuccess)
+            return cuda_status(e, "mul_mat_id grouping");
+        if ((e = launch_moe_down((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, w.xl, a->top_k, R,
+                                 a->n_experts, w, w.z, a->yt == GGUF_F32, s, true)) != cudaSuccess)
+            return cuda_status(e, "mul_mat_id");
+        return cuda_status(launch_moe_plain_store(w.z, w.pos, R, a->n, a->y, a->yt, s), "mul_mat_id store");
     }
     if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), s)) != cudaSuccess) return cuda_status(e, "mul_mat_id quantize");
     if ((e = moe_group(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id grouping");

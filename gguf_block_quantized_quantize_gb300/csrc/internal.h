@@ -129,7 +129,10 @@ cudaError_t launch_moe_gate_up(const uint8_t *w, int wt, int64_t expert_stride, 
                                int64_t hpitch, cudaStream_t s);
 cudaError_t launch_moe_down(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
                             const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
-                            const MoeWs &ws, float *z, bool precise, cudaStream_t s);
+                            const MoeWs &ws, float *z, bool precise, cudaStream_t s, bool x_by_token = false);
+// y[R][n] (out dtype) from the per-route rows z, zero rows for skipped routes (pos < 0)
+cudaError_t launch_moe_plain_store(const float *z, const int32_t *pos, int64_t R, int64_t n, void *y, int yt,
+                                   cudaStream_t s);
 cudaError_t launch_moe_finalize(const float *z, const int32_t *pos, const float *route_w, int64_t T, int64_t top_k,
                                 int64_t n, void *y, int yt, cudaStream_t s);
 

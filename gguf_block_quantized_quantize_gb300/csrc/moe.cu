@@ -306,17 +306,38 @@ cudaError_t launch_moe_gate_up(const uint8_t *w, int wt, int64_t expert_stride, 
 }
 
 // down: z[R][n] = W[e] . x[route] for every grouped route; xh / xl: route
-// rows [R][kx] (xl only in the precise mode)
+// rows [R][kx] (xl only in the precise mode), or token rows [R / top_k][kx]
+// when x_by_token (every route of a token reads the token's row)
 cudaError_t launch_moe_down(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
                             const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
-                            const MoeWs &ws, float *z, bool precise, cudaStream_t s) {
+                            const MoeWs &ws, float *z, bool precise, cudaStream_t s, bool x_by_token) {
     (void)E;
     if (R == 0) return cudaSuccess;
     TgParams p = moe_params(w, wt, expert_stride, n, k, xh, xl, top_k, ws);
     p.tiles_x = (int)((n + TG_BM - 1) / TG_BM);
     p.yacc = z;
-    p.m = R / top_k;  // tokens; the operand has R = top_k * m rows
-    return precise ? launch_moe_mode<TG_MOE_DOWN, true>(wt, p, R, s) : launch_moe_mode<TG_MOE_DOWN, false>(wt, p, R, s);
+    p.m = R / top_k;  // tokens; the operand has R = top_k * m rows (m when x_by_token)
+    p.x_by_token = x_by_token ? 1 : 0;
+    const int64_t rows = x_by_token ? p.m : R;
+    return precise ? launch_moe_mode<TG_MOE_DOWN, true>(wt, p, rows, s)
+                   : launch_moe_mode<TG_MOE_DOWN, false>(wt, p, rows, s);
+}
+
+// y[r][c] = z[r][c] for an active route, 0 for a skipped one (out dtype)
+__global__ void moe_plain_store_kernel(const float *__restrict__ z, const int32_t *__restrict__ pos, int64_t R,
+                                       int64_t n, void *__restrict__ y, int yt) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // z comes from the previous kernel
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= R * n) return;
+    store_out(y, yt, i, pos[i / n] >= 0 ? z[i] : 0.0f);
+}
+
+cudaError_t launch_moe_plain_store(const float *z, const int32_t *pos, int64_t R, int64_t n, void *y, int yt,
+                                   cudaStream_t s) {
+    const int64_t count = R * n;
+    if (count == 0) return cudaSuccess;
+    return launch_pdl(moe_plain_store_kernel, (count + 255) / 256, 256, s, z, pos, R, n, y, yt);
 }
 
 // y[T][n] = the route-weighted sum of each token's z rows (out dtype)

@@ -58,6 +58,7 @@ struct TgParams {
     // gathered activation rows (MoE)
     const uint16_t *xh, *xl;
     int64_t top_k;
+    int x_by_token;   // MoE down mode: route r reads operand row r / top_k (its token's) instead of row r
     const int32_t *route_list, *offsets, *counts, *tile_expert, *tile_start, *n_tiles;
     const float *route_w;
     int tiles_x;
@@ -196,7 +197,8 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             // tile::gather4 per operand; slots past the routes read row
             // `rows` of the operand, out of range, i.e. zeros
             static_assert(BN == 128, "the MoE gather assigns 4 rows to each of 32 lanes");
-            const int32_t oob = (int32_t)(MODE == TG_MOE_GATE_UP ? p.m : p.top_k * p.m);
+            const bool by_token = MODE == TG_MOE_GATE_UP || p.x_by_token;
+            const int32_t oob = (int32_t)(by_token ? p.m : p.top_k * p.m);
             int it = 0, last = 0;
             for (int t = blockIdx.x; t < tiles_total && !*abort_flag; t += gridDim.x) {
                 const TgTile d = tg_tile<MODE, BN>(p, t, KS);
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                 for (int i = 0; i < 4; i++) {
                     const int j = 4 * lane + i;
                     const int r = j < d.n_eff ? p.route_list[d.route0 + j] : -1;
-                    rows[i] = r < 0 ? oob : (int32_t)(MODE == TG_MOE_GATE_UP ? r / p.top_k : r);
+                    rows[i] = r < 0 ? oob : (int32_t)(by_token ? r / p.top_k : r);
                 }
                 for (int ks = 0; ks < KS; ks++, it++) {
                     const int s = it % ST;

@@ -227,6 +227,7 @@ gguf_status gguf_mul_mat_noalloc(const void *w, int wt, int64_t n, int64_t k, co
 /* mul_mat_id modes */
 #define GGUF_MOE_GATE_UP_SWIGLU 0   /* h[r] = silu(gate) * up, rounded to bf16, out as BF16 or Q8_1 */
 #define GGUF_MOE_DOWN_WEIGHTED_SUM 1 /* y[t] = sum_k route_w[t][k] * (W[e] . x[route]) */
+#define GGUF_MOE_PLAIN 2             /* y[route] = W[e] . x[token]: one row per route, no weighting */
 
 /*
  * Arguments of gguf_mul_mat_id (MoE experts).
@@ -242,17 +243,23 @@ gguf_status gguf_mul_mat_noalloc(const void *w, int wt, int64_t n, int64_t k, co
  *                     DOWN: route rows [n_tokens * top_k][ldx] (BF16) or q8_1
  *                     rows [n_tokens * top_k][row_size(Q8_1, k)], route
  *                     r = t * top_k + j.
+ *                     PLAIN: token rows as for GATE_UP; every route of token
+ *                     t reads row t.
  *   ids             : [n_tokens][top_k] int32 expert ids; id < 0 or >= n_experts
  *                     marks an inactive route (skipped, never read), and a token
  *                     may name the same expert more than once (FreeToken issue
  *                     #671, "Known issues").
  *   route_w         : [n_tokens][top_k] fp32 weights (DOWN; NULL means 1.0).
- *                     A route whose weight is 0 is skipped.
+ *                     A route whose weight is 0 is skipped.  PLAIN ignores it.
  *   y, yt           : GATE_UP: [n_tokens * top_k][n/2] of yt = BF16, Q8_1 (q8_1
  *                     rows of row_size(Q8_1, n/2) bytes) or F16 (the dequantized
  *                     q8_1 values d16*q, the form the down GEMM consumes);
  *                     inactive routes get zero rows.  n must be a multiple of 128.
  *                     DOWN: [n_tokens][n] of yt = F32, BF16 or F16.
+ *                     PLAIN: [n_tokens * top_k][n] of yt = F32, BF16 or F16,
+ *                     row r = t * top_k + j; inactive routes get zero rows.
+ *                     (The generic mul_mat_id without a fused epilogue, for
+ *                     experts whose output the caller combines itself.)
  *   workspace       : 256-byte aligned, gguf_mul_mat_id_ws_size(args) bytes.
  *   dev_status      : optional device int32; the count of ids >= n_experts is
  *                     added to it (never a trap, never a host sync).

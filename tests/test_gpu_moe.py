@@ -265,6 +265,39 @@ def test_vec_down_two_block_pieces_odd_blocks(g, wt):
     assert_close(y, ref, TOL_F32, f"vec down type {wt} I=96")
 
 
+@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K, oracle.MXFP4])
+@pytest.mark.parametrize("out_type", ["f32", "bf16"])
+def test_plain_rows(g, path, wt, out_type):
+    """mul_mat_id without the weighted sum: one output row per route against
+    the oracle; inactive and out-of-range ids give zero rows and the latter
+    are counted; route weights are ignored."""
+    E, K, n, k, T = 4, 3, 256, 512, 21
+    bank = _bank(wt, E, n, k, 400 + wt, False)
+    stride = bank.nbytes // E
+    ids, rw = synth.routes(T, E, K, seed=wt + 3)
+    ids[0] = [1, 1, 1]
+    ids[1, 2] = -1
+    ids[2, 0] = E + 5
+    rw[3, 0] = 0.0                      # a weight of 0 does not skip a PLAIN route
+    x = synth.activations(T, k, seed=wt + 4, dtype=torch.float32 if out_type == "f32" else torch.bfloat16)
+    ref = oracle.moe_plain(wt, bank, E, stride, n, k, oracle.quantize_q8_1(x.float().numpy()), ids)
+    active = ((ids >= 0) & (ids < E)).reshape(-1)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = g.gguf_mul_mat_id(_u8(bank), wt, E, stride, n, k, x.to(DEV), _u8(ids), g.PLAIN, route_w=_u8(rw),
+                          out_type=g.F32 if out_type == "f32" else g.BF16, dev_status=status)
+    assert y.shape == (T * K, n)
+    y = y.float().cpu().numpy()
+    assert np.all(y[~active] == 0)
+    assert_close(y[active], ref[active], TOL_F32 if out_type == "f32" else TOL_BF16, f"plain type {wt} ({path})")
+    np.testing.assert_array_equal(y[0], y[1])          # the same expert and token
+    assert int(status.item()) == 1
+    # pre-quantized token rows give the same result
+    xq = g.gguf_quantize_q8_1(x.to(DEV))
+    y2 = g.gguf_mul_mat_id(_u8(bank), wt, E, stride, n, k, xq, _u8(ids), g.PLAIN, xt=g.Q8_1,
+                           out_type=g.F32 if out_type == "f32" else g.BF16).float().cpu().numpy()
+    np.testing.assert_array_equal(y2, y)
+
+
 # ---------------------------------------------------------------- vector path (few tokens)
 
 class _vec_off:
