@@ -837,7 +837,7 @@ struct Q6KPiece {
 // (or of its token), the fp32 output row r of sg.y[0]; skipped routes
 // (pos[r] < 0) exit at once.  M = 1, one segment.
 template <class PT, int M, int TG, int R, int MAXT, bool MULTI, bool ROUTES = false>
-__global__ void __launch_bounds__(MAXT) mmvq_kernel(const MmvqSegs sg, int64_t k, int64_t rb,
+__global__ void __launch_bounds__(MAXT, MAXT == 32 ? 16 : 1) mmvq_kernel(const MmvqSegs sg, int64_t k, int64_t rb,
                                                    const uint8_t *__restrict__ xq, int m_act, int yt,
                                                    const MmvqRoutes rt) {
     const int64_t n = sg.rows();
@@ -995,7 +995,10 @@ inline cudaError_t launch_mmvq_cfg(const MmvqSegs &sg, int64_t k, int64_t rb, co
 }
 
 // the route-batched launch: CTAs of one route over its rows (two per group),
-// as many per route as fill the GPU once
+// as many per route as fill the GPU once.  Rows of at most 32 pieces (one
+// warp; MoE down rows of 512 values have 8) take a one-warp instance whose
+// buffers are sized for one warp and whose registers are capped for 16
+// resident CTAs per SM, so many more rows are in flight.
 template <class PT>
 inline cudaError_t launch_mmvq_routes_pt(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k,
                                          int64_t rb, const uint8_t *xq, int64_t routes, float *z, cudaStream_t s) {
@@ -1003,11 +1006,13 @@ inline cudaError_t launch_mmvq_routes_pt(const uint8_t *bank, const MmvqRoutes &
     const int64_t P = (k + PT::VALUES - 1) / PT::VALUES;
     if (P > 256 || routes > 65535) return cudaErrorInvalidValue;
     const int nthr = (int)((P + 31) / 32 * 32);
-    auto kern = mmvq_kernel<PT, 1, 1, 2, 256, false, true>;
+    const bool one_warp = nthr == 32;
+    constexpr int R = 2;
+    auto kern = one_warp ? mmvq_kernel<PT, 1, 1, 2, 32, false, true> : mmvq_kernel<PT, 1, 1, 2, 256, false, true>;
     cudaError_t e = cudaSuccess;
     const int per_sm = kernel_occupancy(reinterpret_cast<const void *>(kern), nthr, 0, &e);
     if (per_sm == 0) return e;
-    const int64_t groups = (n + 1) / 2;
+    const int64_t groups = (n + R - 1) / R;
     int64_t bx = ((int64_t)device_info().sm_count * per_sm + routes - 1) / routes;
     if (bx > groups) bx = groups;
     if (bx < 1) bx = 1;
