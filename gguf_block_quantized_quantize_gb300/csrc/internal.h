@@ -78,6 +78,7 @@ struct MmvqRoutes {
     int64_t expert_stride;   // bytes between the experts' matrices
     int64_t top_k;           // route slots per token
     int x_per_route;         // activation row of route r: r (1) or its token r / top_k (0)
+    int pack;                // > 1: one-warp CTAs treat this many consecutive rows as one (set by the launcher)
 };
 // z[r][n] (fp32) = W[ids[r]] . q8_1 activation row of route r, for every route
 // slot r < routes with pos[r] >= 0 (W: the expert bank, [n][k] of type wt per

@@ -835,9 +835,13 @@ struct Q6KPiece {
 // ROUTES: MoE route slots, one per grid row (blockIdx.y = r): the weights are
 // expert ids[r] of the bank sg.w[0], the activations the q8_1 row of route r
 // (or of its token), the fp32 output row r of sg.y[0]; skipped routes
-// (pos[r] < 0) exit at once.  M = 1, one segment.
+// (pos[r] < 0) exit at once.  M = 1, one segment.  With rt.pack = G > 1 (one
+// warp, rows of 32 / G whole pieces) G consecutive rows of the expert, which
+// are contiguous, are loaded and staged as one row of G * k values; lane l
+// takes piece l % (32 / G) of row l / (32 / G) and the lanes of each row are
+// reduced on their own.
 template <class PT, int M, int TG, int R, int MAXT, bool MULTI, bool ROUTES = false>
-__global__ void __launch_bounds__(MAXT, MAXT == 32 ? 16 : 1) mmvq_kernel(const MmvqSegs sg, int64_t k, int64_t rb,
+__global__ void __launch_bounds__(MAXT, MAXT == 32 ? 12 : 1) mmvq_kernel(const MmvqSegs sg, int64_t k, int64_t rb,
                                                    const uint8_t *__restrict__ xq, int m_act, int yt,
                                                    const MmvqRoutes rt) {
     const int64_t n = sg.rows();
@@ -854,6 +858,9 @@ __global__ void __launch_bounds__(MAXT, MAXT == 32 ? 16 : 1) mmvq_kernel(const M
         y0 = reinterpret_cast<float *>(y0) + r * n;
         xq += (rt.x_per_route ? r : r / rt.top_k) * ((k / 32) * Q8_1_BYTES);
     }
+    int G = 1;   // rows per (virtual) row
+    if constexpr (ROUTES) G = rt.pack > 1 ? rt.pack : 1;
+    const int64_t nv = n / G, kv = k * G, rbv = rb * G;
     constexpr int V = R * M;
     static_assert(V * TG <= 32 && (V & (V - 1)) == 0, "R*M must be a power of two <= 32/TG");
     __shared__ float red[2][MAXT / 32][TG * V];
@@ -861,11 +868,18 @@ __global__ void __launch_bounds__(MAXT, MAXT == 32 ? 16 : 1) mmvq_kernel(const M
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     const int tg = tid % TG;
     const int64_t piece = tid / TG;
-    const int64_t P = (k + PT::VALUES - 1) / PT::VALUES;   // a last partial piece (Q4_0) counts
+    const int64_t P = (kv + PT::VALUES - 1) / PT::VALUES;   // a last partial piece (Q4_0) counts
+    const int64_t Pr = (k + PT::VALUES - 1) / PT::VALUES;   // pieces of one real row
     const bool valid = piece < P;
     const typename PT::Pos pos = [&] {
-        if constexpr (PT::STAGED) return PT::template pos<TG>(piece, tg, k);   // lanes past the row still copy their share
+        if constexpr (PT::STAGED) return PT::template pos<TG>(piece, tg, kv);   // lanes past the row still copy their share
         else return PT::pos(valid ? piece : 0);
+    }();
+    // the piece's place in its real row, which locates its activations
+    const typename PT::Pos posr = [&] {
+        if (G == 1) return pos;
+        if constexpr (PT::STAGED) return PT::template pos<TG>(piece % Pr, tg, k);
+        else return PT::pos(piece % Pr);
     }();
     const int64_t stride = (int64_t)gridDim.x * R;
     int64_t n0 = (int64_t)blockIdx.x * R;
@@ -875,7 +889,7 @@ __global__ void __launch_bounds__(MAXT, MAXT == 32 ? 16 : 1) mmvq_kernel(const M
         if (!valid && !PT::STAGED) return;
         if constexpr (!MULTI) {
 #pragma unroll
-            for (int r = 0; r < R; r++) PT::load(dst[r], w0 + (base + r < n ? base + r : n - 1) * rb, pos);
+            for (int r = 0; r < R; r++) PT::load(dst[r], w0 + (base + r < nv ? base + r : nv - 1) * rbv, pos);
         } else {
             // one lookup per group; a group that crosses a segment end (or the
             // last row) takes the per-row lookup
@@ -896,14 +910,14 @@ __global__ void __launch_bounds__(MAXT, MAXT == 32 ? 16 : 1) mmvq_kernel(const M
     };
     // weights never change: the first rows are requested before waiting for
     // the kernel that wrote the activations
-    if (n0 < n) load_rows(wa, n0);
+    if (n0 < nv) load_rows(wa, n0);
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     typename PT::template A<M> act;
     const int m_mine = m_act - tg * M;  // tokens of this thread (may be <= 0)
     PT::template load_act<M>(act, xq + (int64_t)tg * M * ((k / 32) * Q8_1_BYTES), (k / 32) * Q8_1_BYTES,
-                             m_mine, pos, valid);
+                             m_mine, posr, valid);
 
     int buf = 0;
     auto process = [&](const typename PT::W (&cur)[R], int64_t r0) {
@@ -935,13 +949,24 @@ __global__ void __launch_bounds__(MAXT, MAXT == 32 ? 16 : 1) mmvq_kernel(const M
                 for (int mm = 0; mm < M; mm++) part[r * M + mm] = acc[mm];
             }
         }
+        if constexpr (ROUTES) {
+            if (G > 1) {   // lanes [l - l % Pr, +Pr) hold the pieces of real row (r0 + r) * G + l / Pr
+#pragma unroll
+                for (int r = 0; r < R; r++) {
+                    float v = part[r];
+                    for (int o = (int)Pr / 2; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane % Pr == 0 && r0 + r < nv) store_row(0, (r0 + r) * G + lane / Pr, v);
+                }
+                return;
+            }
+        }
         int idx;
         const float tot = butterfly_tg<V, TG>(part, lane, idx);
         const bool writer = butterfly_writer<V, TG>(lane);
         if (nw == 1) {
             if (writer) {
                 const int r = idx / M, tok = tg * M + idx % M;
-                if (r0 + r < n && tok < m_act) store_row(tok, r0 + r, tot);
+                if (r0 + r < nv && tok < m_act) store_row(tok, r0 + r, tot);
             }
         } else {
             if (writer) red[buf][warp][tg * V + idx] = tot;
@@ -950,18 +975,18 @@ __global__ void __launch_bounds__(MAXT, MAXT == 32 ? 16 : 1) mmvq_kernel(const M
                 float sum = 0.0f;
                 for (int j = 0; j < nw; j++) sum += red[buf][j][tid];
                 const int g = tid / V, i = tid % V, r = i / M, tok = g * M + i % M;
-                if (r0 + r < n && tok < m_act) store_row(tok, r0 + r, sum);
+                if (r0 + r < nv && tok < m_act) store_row(tok, r0 + r, sum);
             }
             buf ^= 1;
         }
     };
     // two register sets in turn: the next rows load while the current compute
-    while (n0 < n) {
-        if (n0 + stride < n) load_rows(wb, n0 + stride);
+    while (n0 < nv) {
+        if (n0 + stride < nv) load_rows(wb, n0 + stride);
         process(wa, n0);
         n0 += stride;
-        if (n0 >= n) break;
-        if (n0 + stride < n) load_rows(wa, n0 + stride);
+        if (n0 >= nv) break;
+        if (n0 + stride < nv) load_rows(wa, n0 + stride);
         process(wb, n0);
         n0 += stride;
     }
@@ -997,8 +1022,9 @@ inline cudaError_t launch_mmvq_cfg(const MmvqSegs &sg, int64_t k, int64_t rb, co
 // the route-batched launch: CTAs of one route over its rows (two per group),
 // as many per route as fill the GPU once.  Rows of at most 32 pieces (one
 // warp; MoE down rows of 512 values have 8) take a one-warp instance whose
-// buffers are sized for one warp and whose registers are capped for 16
-// resident CTAs per SM, so many more rows are in flight.
+// buffers are sized for one warp, with registers for 12 resident CTAs per SM
+// (3 warps per SM sub-partition: up to 168 registers, no spills), and rows of
+// 32 / G whole pieces are packed G to a warp-row (rt.pack).
 template <class PT>
 inline cudaError_t launch_mmvq_routes_pt(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k,
                                          int64_t rb, const uint8_t *xq, int64_t routes, float *z, cudaStream_t s) {
@@ -1008,11 +1034,15 @@ inline cudaError_t launch_mmvq_routes_pt(const uint8_t *bank, const MmvqRoutes &
     const int nthr = (int)((P + 31) / 32 * 32);
     const bool one_warp = nthr == 32;
     constexpr int R = 2;
+    // rows of 32 / G whole pieces: G rows per warp-row (all 32 lanes busy)
+    MmvqRoutes rtp = rt;
+    rtp.pack = 1;
+    if (one_warp && k % PT::VALUES == 0 && P <= 16 && 32 % P == 0 && n % (32 / P) == 0) rtp.pack = (int)(32 / P);
     auto kern = one_warp ? mmvq_kernel<PT, 1, 1, 2, 32, false, true> : mmvq_kernel<PT, 1, 1, 2, 256, false, true>;
     cudaError_t e = cudaSuccess;
     const int per_sm = kernel_occupancy(reinterpret_cast<const void *>(kern), nthr, 0, &e);
     if (per_sm == 0) return e;
-    const int64_t groups = (n + R - 1) / R;
+    const int64_t groups = (n / rtp.pack + R - 1) / R;
     int64_t bx = ((int64_t)device_info().sm_count * per_sm + routes - 1) / routes;
     if (bx > groups) bx = groups;
     if (bx < 1) bx = 1;
@@ -1027,7 +1057,7 @@ inline cudaError_t launch_mmvq_routes_pt(const uint8_t *bank, const MmvqRoutes &
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, sg, k, rb, xq, 1, (int)GGUF_F32, rt);
+    return cudaLaunchKernelEx(&cfg, kern, sg, k, rb, xq, 1, (int)GGUF_F32, rtp);
 }
 
 // Configuration by token count (measured on GB300, Q4_K / Q6_K rows of 3072 ..
