@@ -105,7 +105,7 @@ static int64_t g_mmvq_tc_min_m = 5;
 // MoE calls of at most this many tokens take the route-batched MMVQ (vector)
 // path; the workspace reserves its buffers up to MOE_VEC_CAP tokens
 constexpr int64_t MOE_VEC_CAP = 256;
-static int64_t g_moe_vec_max_tokens = 128;
+static int64_t g_moe_vec_max_tokens = 256;
 int64_t option_mmvq_tc() { return g_mmvq_tc; }
 int64_t option_mmvq_tc_min_m() { return g_mmvq_tc_min_m; }
 int64_t option_mmvq_tc_max_m() { return g_mmvq_tc_max_m; }

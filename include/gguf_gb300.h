@@ -266,7 +266,7 @@ gguf_status gguf_mul_mat_noalloc(const void *w, int wt, int64_t n, int64_t k, co
  * The intermediate h is kept in the activation dtype (bf16) and then quantized
  * to q8_1 (FreeToken PR #690, section "Changes": the intermediates stay in the
  * activation dtype).
- * Path: up to option "moe_vec_max_tokens" tokens (default 128) the call runs
+ * Path: up to option "moe_vec_max_tokens" tokens (default 256) the call runs
  * the route-batched MMVQ (one launch over all route slots, each reading its
  * expert's rows once with exact int32 block sums; FreeToken PR #690, section
  * "Changes": MoE takes MMVQ for small batches and MMQ above, with the
@@ -355,10 +355,10 @@ gguf_status gguf_debug_block_dots(const void *w, int wt, int64_t n, int64_t k, c
  *   "mmvq_tc_min_m": fewest tokens that take the tensor-core MMVQ, 1 .. 8
  *                   (default 5).
  *   "moe_vec_max_tokens": mul_mat_id / moe_ffn calls of at most this many
- *                   tokens take the route-batched MMVQ; 0 .. 256, default 128
- *                   (the measured crossover with the grouped GEMM on GB300
- *                   for the E=256, top-8 expert block: 3x faster at 1..16
- *                   tokens, even at 128, slower from 192).
+ *                   tokens take the route-batched MMVQ; 0 .. 256, default 256
+ *                   (measured on GB300 for the E=256, top-8 expert block:
+ *                   4-6x faster than the grouped GEMM at 1..16 tokens,
+ *                   2.3x at 128, still 1.3x at 256).
  *   "mmvq_tc_max_m": Q4_K products of 9 up to this many tokens stay on the
  *                   tensor-core MMVQ (2 or 4 n-tiles of 8 tokens) instead
  *                   of MMQ; 8 .. 32, default 16 (the measured crossover on
