@@ -107,3 +107,34 @@ def test_other_entry_points_reject_bad_arguments(g):
     assert L.gguf_set_option(b"moe_vec_max_tokens", 257) != 0 and L.gguf_get_option(b"moe_vec_max_tokens") == 256
     assert L.gguf_get_option(b"mmvq_tc_max_m") == 16
     assert L.gguf_set_option(b"mmvq_tc_max_m", 64) != 0 and L.gguf_get_option(b"mmvq_tc_max_m") == 16
+
+
+def _moe(g, **kw):
+    """gguf_mul_mat_id on fake device pointers: only the synchronous argument
+    checks run (every call below fails validation before any launch, or has
+    no tokens)."""
+    a = dict(w=0x10000, wt=g.Q4_K, n_experts=4, expert_stride=256 * 144, n=256, k=256, x=0x20000, xt=g.BF16,
+             n_tokens=3, ldx=256, ids=0x30000, top_k=2, route_w=0, mode=g.PLAIN, y=0x40000, yt=g.F32,
+             dev_status=0)
+    a.update(kw)
+    args = g.MoeArgs(a["w"], a["wt"], a["n_experts"], a["expert_stride"], a["n"], a["k"], a["x"], a["xt"],
+                     a["n_tokens"], a["ldx"], a["ids"], a["top_k"], a["route_w"], a["mode"], a["y"], a["yt"],
+                     a["dev_status"])
+    L = g.load_library()
+    return L.gguf_mul_mat_id(ctypes.byref(args), FAKE, 0, None)
+
+
+def test_mul_mat_id_modes_and_types(g):
+    assert g.GATE_UP_SWIGLU == 0 and g.DOWN_WEIGHTED_SUM == 1 and g.PLAIN == 2
+    assert _moe(g, mode=3) == 1                       # unknown mode
+    assert _moe(g, yt=g.Q8_1) == 2                    # PLAIN rows are float
+    assert _moe(g, mode=g.DOWN_WEIGHTED_SUM, yt=g.Q8_1) == 2
+    assert _moe(g, wt=3) == 2                         # Q4_1: not a supported bank type
+    assert _moe(g, k=100) == 3                        # not a multiple of the Q4_K block
+    assert _moe(g, expert_stride=256 * 144 - 16) == 1  # stride below n * row_size
+    assert _moe(g, n_tokens=0) == 0                   # no tokens: nothing to do
+    # the remaining valid PLAIN call fails only on the (absent) workspace
+    assert _moe(g) == 5 and "workspace" in g.load_library().gguf_last_error().decode()
+    for wt, k in ((g.Q4_0, 96), (g.MXFP4, 96), (g.Q5_K, 256), (g.Q8_0, 64)):
+        stride = -(-256 * g.gguf_row_size(wt, k) // 16) * 16
+        assert _moe(g, wt=wt, k=k, ldx=k, expert_stride=stride) == 5, wt
