@@ -438,3 +438,18 @@ def test_get_rows_is_row_gather_of_dequantize(orc):
     # out-of-range ids give zero rows
     z = orc.get_rows(orc.Q6_K, p, 512, np.array([-1, 40], dtype=np.int32), orc.F32)
     assert np.all(z == 0)
+
+
+@pytest.mark.parametrize("tname", ["Q8_0", "Q4_0", "Q4_K", "Q5_K", "Q6_K", "MXFP4"])
+def test_safe_blocks_give_weight_sized_finite_values(orc, tname):
+    """The random-but-safe packed blocks (host and device generators; the
+    device one runs on the CPU here) dequantize to finite values of the size
+    quantized N(0, 0.02) weights have, so no test or bench input overflows."""
+    t = getattr(orc, tname)
+    k = 512
+    for blocks in (synth.safe_blocks(t, 64, k, seed=90),
+                   synth.safe_blocks_device(t, 64, k, seed=91, device="cpu").numpy()):
+        assert blocks.shape == (64, synth.row_bytes(t, k))
+        v = orc.dequantize_f64(t, np.ascontiguousarray(blocks), k)
+        assert np.all(np.isfinite(v))
+        assert 1e-4 < np.abs(v).max() < 1.0, (tname, np.abs(v).max())
