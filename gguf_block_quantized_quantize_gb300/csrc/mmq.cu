@@ -77,6 +77,10 @@ static cudaError_t launch_dense(const uint8_t *w, int64_t n, int64_t k, const ui
     if (tiles > INT32_MAX) return cudaErrorInvalidValue;
     p.tiles_n = (int)tiles_n;
     p.tiles_m = (int)tiles_m;
+    // weights that do not stay in L2 across a pass over the weight tiles (the
+    // LM head: 417 MB of Q6_K) are read once per activation tile in the
+    // weight-fastest order; activation-fastest reads each once
+    p.m_fast = (tiles_m > 1 && n * p.rb > (int64_t)(64 << 20)) ? 1 : 0;
     p.tiles_total = (int)tiles;
     p.ks_per_split = kps;
     p.y = y;

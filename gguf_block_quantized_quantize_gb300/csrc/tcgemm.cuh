@@ -51,6 +51,7 @@ struct TgParams {
     // dense tiles
     int64_t m;
     int tiles_n, tiles_m, tiles_total, ks_per_split;
+    int m_fast;   // dense tile order: the activation tile index varies fastest (weights larger than L2)
     void *y;
     int yt;
     int64_t ldy;
@@ -99,8 +100,12 @@ __device__ __forceinline__ TgTile tg_tile(const TgParams &p, int t, int KS) {
     TgTile d{};
     if (MODE == TG_DENSE) {
         const int nm = p.tiles_n * p.tiles_m;
-        d.row0 = (int64_t)(t % p.tiles_n) * TG_BM;
-        d.m0 = (int64_t)((t / p.tiles_n) % p.tiles_m) * BN;
+        // m_fast: the CTAs of one wave share few weight tiles, each read from DRAM
+        // once and from L2 by the CTAs of its other activation tiles
+        const int tn = p.m_fast ? (t / p.tiles_m) % p.tiles_n : t % p.tiles_n;
+        const int tm = p.m_fast ? t % p.tiles_m : (t / p.tiles_n) % p.tiles_m;
+        d.row0 = (int64_t)tn * TG_BM;
+        d.m0 = (int64_t)tm * BN;
         d.k0 = (t / nm) * p.ks_per_split;
         d.k1 = d.k0 + p.ks_per_split < KS ? d.k0 + p.ks_per_split : KS;
         d.n_eff = BN;
