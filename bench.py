@@ -295,9 +295,7 @@ def run_ours(args, rank, world, torch, dev):
     clk = clocks.stop()
     n_mmvq = dec.mmvq_launches_per_step()
     ms_mmvq = ms_mmvq_step / n_mmvq
-    ms_total = _max_over_ranks(ms_total, world, torch, dev)
-    ms_step = ms_total / args.steps
-    value = per_step * world / (ms_step * 1e-3) / 1e9
+    ms_step, value = _job_rate(ms_total, args.steps, per_step, world, torch, dev)
     achieved = (mmvq_bytes / n_mmvq) / (ms_mmvq * 1e-3) / 1e9
 
     # per (shape, M) detail: each MMVQ alone, 16 launches per graph
@@ -683,6 +681,14 @@ def _max_over_ranks(v, world, torch, dev):
     t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _job_rate(ms_total, steps, bytes_per_step, world, torch, dev):
+    """Whole-job rate of `world` replicas: every rank processed bytes_per_step
+    per step, and the job took the slowest rank's time.  Returns (ms per step,
+    GB/s over all ranks)."""
+    ms_step = _max_over_ranks(ms_total, world, torch, dev) / steps
+    return ms_step, bytes_per_step * world / (ms_step * 1e-3) / 1e9
 
 
 def main(argv=None):
