@@ -21,9 +21,12 @@ import numpy as np
 import torch
 
 F32, F16, Q4_0, Q8_0, Q8_1, Q4_K, Q5_K, Q6_K, BF16, MXFP4 = 0, 1, 2, 8, 9, 12, 13, 14, 30, 39
+Q4_1, Q5_0, Q5_1 = 3, 6, 7
 
-BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q8_1: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256, MXFP4: 32}
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q8_1: 36, Q4_K: 144, Q5_K: 176, Q6_K: 210, MXFP4: 17}
+BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q8_1: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256, MXFP4: 32, Q4_1: 32, Q5_0: 32,
+               Q5_1: 32}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q8_1: 36, Q4_K: 144, Q5_K: 176, Q6_K: 210, MXFP4: 17, Q4_1: 20, Q5_0: 22,
+               Q5_1: 24}
 
 
 def row_bytes(t: int, k: int) -> int:
@@ -76,6 +79,17 @@ def safe_blocks(t: int, rows: int, k: int, seed: int) -> np.ndarray:
     elif t == Q4_0:
         # fp16 d at 0..1 (either sign); 16 nibble bytes random
         d = rng.uniform(2.0e-3, 1.2e-2, size=(rows, nb)) * rng.choice([-1.0, 1.0], size=(rows, nb))
+        blk[:, :, 0:2] = _f16_bits(d).reshape(rows, nb, 1).view(np.uint8).reshape(rows, nb, 2)
+    elif t in (Q4_1, Q5_1):
+        # fp16 d at 0..1 (positive), fp16 m at 2..3 (the block minimum, negative); the rest random
+        levels = 15 if t == Q4_1 else 31
+        d = rng.uniform(4.0, 8.0, size=(rows, nb)) * 0.02 / levels
+        m = -rng.uniform(0.03, 0.07, size=(rows, nb))
+        blk[:, :, 0:2] = _f16_bits(d).reshape(rows, nb, 1).view(np.uint8).reshape(rows, nb, 2)
+        blk[:, :, 2:4] = _f16_bits(m).reshape(rows, nb, 1).view(np.uint8).reshape(rows, nb, 2)
+    elif t == Q5_0:
+        # fp16 d at 0..1 (either sign); high-bit and quant bytes random
+        d = rng.uniform(1.0e-3, 6.0e-3, size=(rows, nb)) * rng.choice([-1.0, 1.0], size=(rows, nb))
         blk[:, :, 0:2] = _f16_bits(d).reshape(rows, nb, 1).view(np.uint8).reshape(rows, nb, 2)
     elif t == MXFP4:
         # E8M0 exponent byte at 0: block scales 2^-9 .. 2^-3, the range of quantized N(0, 0.02)
@@ -132,6 +146,12 @@ def safe_blocks_device(t: int, rows: int, k: int, seed: int, device) -> torch.Te
         field([4.0e-3, -6.0e-3, 8.0e-3, -1.0e-2], 0, 2)
     elif t == MXFP4:
         blk[:, :, 0] = torch.randint(118, 125, (rows, nb), dtype=torch.uint8, device=device, generator=g)
+    elif t in (Q4_1, Q5_1):
+        levels = 15 if t == Q4_1 else 31
+        field([0.1 / levels, 0.12 / levels, 0.14 / levels, 0.16 / levels], 0, 2)
+        field([-0.035, -0.045, -0.055, -0.065], 2, 4)
+    elif t == Q5_0:
+        field([2.0e-3, -3.0e-3, 4.0e-3, -5.0e-3], 0, 2)
     elif t == Q5_K:
         field([1.5e-5, 3.0e-5, 5.5e-5, 8.0e-5], 0, 2)
         field([0.0, 3.0e-4, 6.0e-4, 9.0e-4], 2, 4)

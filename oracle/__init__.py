@@ -21,6 +21,7 @@ _LIB_PATH = os.path.join(_HERE, "libgguf_oracle.so")
 
 F32, F16, Q4_0, Q8_0, Q8_1, Q4_K, Q5_K, Q6_K, BF16 = 0, 1, 2, 8, 9, 12, 13, 14, 30
 MXFP4 = 39
+Q4_1, Q5_0, Q5_1 = 3, 6, 7
 
 
 def build(force: bool = False) -> str:

@@ -1,7 +1,7 @@
 /*
  * gguf_oracle.c -- plain, slow, scalar CPU oracle for the GGUF block-quantized
- * matmul path (q8_1 activations x Q8_0 / Q4_0 / Q4_K / Q5_K / Q6_K / MXFP4
- * weights).
+ * matmul path (q8_1 activations x Q8_0 / Q4_0 / Q4_1 / Q5_0 / Q5_1 / Q4_K /
+ * Q5_K / Q6_K / MXFP4 weights).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or runs
  * this file: only tests/, __graft_entry__.smoke() and the cpu_baseline leg of
@@ -31,6 +31,11 @@
  *    1-bit mantissa) scaled by the block's E8M0 exponent, 2^(e - 127); the
  *    GGUF block is {u8 e, u8 qs[16]} with Q4_0's nibble order.  E8M0 code 255
  *    (NaN in the OCP definition) is read as the exponent 128 like any other.
+ *  - Q4_1, Q5_0 and Q5_1 are listed there too.  Their public GGUF blocks of 32:
+ *    Q4_1 {fp16 d, fp16 m, qs[16]}, value d*q + m; Q5_0 {fp16 d, qh[4],
+ *    qs[16]}, value d*(q - 16); Q5_1 {fp16 d, fp16 m, qh[4], qs[16]}, value
+ *    d*q + m.  The nibbles are in Q4_0's order; the fifth bit of value i is
+ *    bit i of qh read as a little-endian 32-bit word.
  *  - Q4_0 and Q5_K are two of the further tensor types the pages list
  *    (FreeToken PR #690, "Tensor types"; transformers PR #45977, supported
  *    quant types of GgufLinear).
@@ -42,11 +47,13 @@
  *    away from zero), s = fp16(d * (float)sum(q)) with the fp32 d.
  *  - dequantized value order: Q4_K, Q5_K  a = d*s; b = dmin*m; v = a*q - b;
  *                             Q6_K  v = (d*sc) * (q - 32);   Q8_0  v = d*q;
- *                             Q4_0  v = d * (q - 8);
+ *                             Q4_0  v = d * (q - 8);   Q5_0  v = d * (q - 16);
+ *                             Q4_1, Q5_1  v = d*q + m (one rounding);
  *                             MXFP4 v = e2m1(q) * 2^(e - 127), one exact product.
- *  - block dots: symmetric formats with an integer offset (Q4_0: 8, Q6_K: 32)
- *    take the offset into the exact integer sum; affine formats with a float
- *    min (Q4_K, Q5_K) combine the min with the activation block's stored s.
+ *  - block dots: symmetric formats with an integer offset (Q4_0: 8, Q5_0: 16,
+ *    Q6_K: 32) take the offset into the exact integer sum; affine formats with
+ *    a float min (Q4_K, Q5_K: -dmin*m_j; Q4_1, Q5_1: +m) combine the min with
+ *    the activation block's stored s.
  *    MXFP4's integer quant is 2 * e2m1(q) (exact, in -12..12) against the
  *    block factor 2^(e - 128).
  *  - matmul reference: the blockwise formula evaluated in fp64 on the stored
@@ -143,7 +150,8 @@ static void wr16(uint8_t *p, uint16_t v) { p[0] = (uint8_t)(v & 0xff); p[1] = (u
 int64_t orc_block_elems(int type) {
     switch (type) {
     case ORC_F32: case ORC_F16: case ORC_BF16: return 1;
-    case ORC_Q8_0: case ORC_Q8_1: case ORC_Q4_0: case ORC_MXFP4: return 32;
+    case ORC_Q8_0: case ORC_Q8_1: case ORC_Q4_0: case ORC_MXFP4:
+    case ORC_Q4_1: case ORC_Q5_0: case ORC_Q5_1: return 32;
     case ORC_Q4_K: case ORC_Q5_K: case ORC_Q6_K: return 256;
     default: return 0;
     }
@@ -157,6 +165,9 @@ int64_t orc_block_bytes(int type) {
     case ORC_Q8_1: return 36;  /* fp16 d, fp16 s, int8 q[32] */
     case ORC_Q4_0: return 18;  /* fp16 d, u8 qs[16] */
     case ORC_MXFP4: return 17; /* u8 e (E8M0), u8 qs[16] (e2m1 codes) */
+    case ORC_Q4_1: return 20;  /* fp16 d, fp16 m, u8 qs[16] */
+    case ORC_Q5_0: return 22;  /* fp16 d, u8 qh[4], u8 qs[16] */
+    case ORC_Q5_1: return 24;  /* fp16 d, fp16 m, u8 qh[4], u8 qs[16] */
     case ORC_Q4_K: return 144; /* fp16 d, fp16 dmin, u8 scales[12], u8 qs[128] */
     case ORC_Q5_K: return 176; /* fp16 d, fp16 dmin, u8 scales[12], u8 qh[32], u8 qs[128] */
     case ORC_Q6_K: return 210; /* u8 ql[128], u8 qh[64], i8 scales[16], fp16 d */
@@ -173,7 +184,8 @@ int64_t orc_row_size(int type, int64_t k) {
 /* sub-block length of the per-block integer dot products */
 int64_t orc_sub_elems(int type) {
     switch (type) {
-    case ORC_Q8_0: case ORC_Q4_0: case ORC_Q4_K: case ORC_Q5_K: case ORC_MXFP4: return 32;
+    case ORC_Q8_0: case ORC_Q4_0: case ORC_Q4_K: case ORC_Q5_K: case ORC_MXFP4:
+    case ORC_Q4_1: case ORC_Q5_0: case ORC_Q5_1: return 32;
     case ORC_Q6_K: return 16;
     default: return 0;
     }
@@ -224,6 +236,18 @@ static int q4_0_q(const uint8_t *b, int i) {
     uint8_t byte = b[2 + (i % 16)];
     return i < 16 ? (byte & 15) : (byte >> 4);
 }
+
+/* Q4_1 / Q5_0 / Q5_1 blocks of 32.  The quant bytes qs (16) hold value l in
+ * the low nibble of qs[l] and value l + 16 in the high one; Q5_0 / Q5_1 add
+ * bit i of the little-endian word qh as bit 4 of value i.                    */
+static int qs_nibble(const uint8_t *qs, int i) { return i < 16 ? (qs[i] & 15) : (qs[i - 16] >> 4); }
+static int qh_bit(const uint8_t *qh, int i) { return (qh[i / 8] >> (i % 8)) & 1; }
+static float q41_d(const uint8_t *b) { return orc_f16_to_f32(rd16(b)); }
+static float q41_m(const uint8_t *b) { return orc_f16_to_f32(rd16(b + 2)); }
+static int q4_1_q(const uint8_t *b, int i) { return qs_nibble(b + 4, i); }
+static float q5_0_d(const uint8_t *b) { return orc_f16_to_f32(rd16(b)); }
+static int q5_0_q(const uint8_t *b, int i) { return qs_nibble(b + 6, i) | (qh_bit(b + 2, i) << 4); }
+static int q5_1_q(const uint8_t *b, int i) { return qs_nibble(b + 8, i) | (qh_bit(b + 4, i) << 4); }
 
 /* MXFP4 block: byte 0 is the E8M0 exponent e, bytes 1..16 hold 32 e2m1 codes
  * in Q4_0's order (byte 1 + l: code of value l low, of value l + 16 high).
@@ -410,6 +434,52 @@ static void quantize_block_q4_0(const float *x, uint8_t *out) {
     }
 }
 
+/* Q4_1 / Q5_1 (levels = 15 / 31): m = min x, d = (max x - m) / levels; the
+ * stored fp16 d_h, m_h; q = clamp(roundf((x - m_h) / d_h), 0, levels).
+ * Q5_0: the value v of largest magnitude sets d = v / -16;
+ * q = clamp(roundf(x / d_h) + 16, 0, 31).                                   */
+static void quantize_block_affine32(const float *x, uint8_t *out, int levels, int with_qh) {
+    float lo = x[0], hi = x[0];
+    for (int i = 1; i < 32; i++) {
+        if (x[i] < lo) lo = x[i];
+        if (x[i] > hi) hi = x[i];
+    }
+    uint16_t dh = orc_f32_to_f16((hi - lo) / (float)levels), mh = orc_f32_to_f16(lo);
+    float df = orc_f16_to_f32(dh), mf = orc_f16_to_f32(mh);
+    int bytes = with_qh ? 24 : 20;
+    memset(out, 0, (size_t)bytes);
+    wr16(out, dh);
+    wr16(out + 2, mh);
+    uint8_t *qh = out + 4, *qs = out + (with_qh ? 8 : 4);
+    for (int i = 0; i < 32; i++) {
+        int q = 0;
+        if (df > 0.0f) q = (int)roundf((x[i] - mf) / df);
+        if (q < 0) q = 0;
+        if (q > levels) q = levels;
+        qs[i % 16] |= (uint8_t)(i < 16 ? (q & 15) : (q & 15) << 4);
+        if (with_qh) qh[i / 8] |= (uint8_t)(((q >> 4) & 1) << (i % 8));
+    }
+}
+static void quantize_block_q5_0(const float *x, uint8_t *out) {
+    float amax = 0.0f, vmax = 0.0f;
+    for (int i = 0; i < 32; i++) {
+        float a = fabsf(x[i]);
+        if (a > amax) { amax = a; vmax = x[i]; }
+    }
+    uint16_t dh = orc_f32_to_f16(vmax / -16.0f);
+    float df = orc_f16_to_f32(dh);
+    memset(out, 0, 22);
+    wr16(out, dh);
+    for (int i = 0; i < 32; i++) {
+        int q = 16;
+        if (df != 0.0f) q = (int)roundf(x[i] / df) + 16;
+        if (q < 0) q = 0;
+        if (q > 31) q = 31;
+        out[6 + (i % 16)] |= (uint8_t)(i < 16 ? (q & 15) : (q & 15) << 4);
+        out[2 + i / 8] |= (uint8_t)(((q >> 4) & 1) << (i % 8));
+    }
+}
+
 /* MXFP4: the smallest e in 0..254 with 6 * 2^(e - 127) >= amax (0 for an
  * all-zero block), then per value the e2m1 code of the nearest magnitude of
  * |x| / 2^(e - 127) (ties to the larger), with x's sign.                     */
@@ -549,6 +619,9 @@ int orc_quantize_weights(int type, const float *w, int64_t n, int64_t k, uint8_t
             case ORC_Q8_0: quantize_block_q8_0(x, o); break;
             case ORC_Q4_0: quantize_block_q4_0(x, o); break;
             case ORC_MXFP4: quantize_block_mxfp4(x, o); break;
+            case ORC_Q4_1: quantize_block_affine32(x, o, 15, 0); break;
+            case ORC_Q5_1: quantize_block_affine32(x, o, 31, 1); break;
+            case ORC_Q5_0: quantize_block_q5_0(x, o); break;
             case ORC_Q4_K: quantize_block_q4_k(x, o); break;
             case ORC_Q5_K: quantize_block_q5_k(x, o); break;
             case ORC_Q6_K: quantize_block_q6_k(x, o); break;
@@ -577,6 +650,9 @@ static float dequant_value(int type, const uint8_t *blk, int i) {
     }
     case ORC_Q4_0: return q4_0_d(blk) * (float)(q4_0_q(blk, i) - 8);
     case ORC_MXFP4: return ldexpf((float)e2m1_value(mxfp4_code(blk, i)), mxfp4_e(blk) - 127);
+    case ORC_Q4_1: return q41_d(blk) * (float)q4_1_q(blk, i) + q41_m(blk);
+    case ORC_Q5_0: return q5_0_d(blk) * (float)(q5_0_q(blk, i) - 16);
+    case ORC_Q5_1: return q41_d(blk) * (float)q5_1_q(blk, i) + q41_m(blk);
     case ORC_Q5_K: {
         int s, m;
         q4_k_scale_min(blk, i / 32, &s, &m);
@@ -612,6 +688,9 @@ static double dequant_value_f64(int type, const uint8_t *blk, int i) {
     }
     case ORC_Q4_0: return (double)q4_0_d(blk) * (q4_0_q(blk, i) - 8);
     case ORC_MXFP4: return ldexp(e2m1_value(mxfp4_code(blk, i)), mxfp4_e(blk) - 127);
+    case ORC_Q4_1: return (double)q41_d(blk) * q4_1_q(blk, i) + (double)q41_m(blk);
+    case ORC_Q5_0: return (double)q5_0_d(blk) * (q5_0_q(blk, i) - 16);
+    case ORC_Q5_1: return (double)q41_d(blk) * q5_1_q(blk, i) + (double)q41_m(blk);
     case ORC_Q5_K: {
         int s, m;
         q4_k_scale_min(blk, i / 32, &s, &m);
@@ -687,6 +766,9 @@ static int32_t block_dot(int type, const uint8_t *wb, int64_t first, const uint8
         case ORC_Q8_0: qw = q8_0_q(wb, i); break;
         case ORC_Q4_0: qw = q4_0_q(wb, i) - 8; break;
         case ORC_MXFP4: qw = mxfp4_q(wb, i); break;
+        case ORC_Q4_1: qw = q4_1_q(wb, i); break;
+        case ORC_Q5_0: qw = q5_0_q(wb, i) - 16; break;
+        case ORC_Q5_1: qw = q5_1_q(wb, i); break;
         case ORC_Q4_K: qw = q4_k_q(wb, i); break;
         case ORC_Q5_K: qw = q5_k_q(wb, i); break;
         case ORC_Q6_K: qw = q6_k_q(wb, i) - 32; break;
@@ -721,6 +803,8 @@ int orc_block_dots(int type, const uint8_t *w, int64_t n, int64_t k, const uint8
 /* y = sum over the row's sub-blocks of the combination of stored fields:
  *   Q8_0, Q4_0: d_w * d_a * S      (Q4_0: S over q - 8)
  *   MXFP4:      2^(e - 128) * d_a * S   (S over 2 * e2m1(q))
+ *   Q5_0:       d_w * d_a * S           (S over q - 16)
+ *   Q4_1, Q5_1: d * d_a * S + m * s_a
  *   Q4_K, Q5_K: d * s_j * d_a * S_j - dmin * m_j * s_a
  *   Q6_K: d * sc_j * d_a * S_j
  * with d_a, s_a the q8_1 fields of the 32-block holding sub-block j.         */
@@ -740,6 +824,10 @@ static double dot_row(int type, const uint8_t *wrow, int64_t k, const uint8_t *x
                 y += (double)q4_0_d(wb) * da * S;
             } else if (type == ORC_MXFP4) {
                 y += ldexp(1.0, mxfp4_e(wb) - 128) * da * S;
+            } else if (type == ORC_Q5_0) {
+                y += (double)q5_0_d(wb) * da * S;
+            } else if (type == ORC_Q4_1 || type == ORC_Q5_1) {
+                y += (double)q41_d(wb) * da * S + (double)q41_m(wb) * sa;
             } else if (type == ORC_Q4_K || type == ORC_Q5_K) {
                 int s, m;
                 q4_k_scale_min(wb, j, &s, &m);

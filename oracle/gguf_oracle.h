@@ -12,7 +12,7 @@ extern "C" {
 #endif
 
 /* ggml type numbering (public GGUF convention) */
-enum { ORC_F32 = 0, ORC_F16 = 1, ORC_Q4_0 = 2, ORC_Q8_0 = 8, ORC_Q8_1 = 9, ORC_Q4_K = 12, ORC_Q5_K = 13, ORC_Q6_K = 14, ORC_BF16 = 30,
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_Q4_0 = 2, ORC_Q4_1 = 3, ORC_Q5_0 = 6, ORC_Q5_1 = 7, ORC_Q8_0 = 8, ORC_Q8_1 = 9, ORC_Q4_K = 12, ORC_Q5_K = 13, ORC_Q6_K = 14, ORC_BF16 = 30,
        ORC_MXFP4 = 39 };
 
 float orc_f16_to_f32(uint16_t h);

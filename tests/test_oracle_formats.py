@@ -89,12 +89,13 @@ def _parse_blocks(name):
                                            ("q4_k_hand_blocks.txt", "Q4_K", 256),
                                            ("q5_k_hand_blocks.txt", "Q5_K", 256),
                                            ("mxfp4_hand_blocks.txt", "MXFP4", 32),
+                                           ("q4_1_q5_0_q5_1_hand_blocks.txt", None, 32),
                                            ("q6_k_hand_blocks.txt", "Q6_K", 256)])
 def test_hand_built_blocks(orc, fname, tname, k):
-    t = getattr(orc, tname)
     blocks = _parse_blocks(fname)
     assert blocks
     for b in blocks:
+        t = getattr(orc, tname if tname is not None else b["type"])
         raw = np.frombuffer(b["hex"], dtype=np.uint8).reshape(1, -1)
         assert raw.shape[1] == orc.block_bytes(t)
         got = orc.dequantize_f32(t, raw, k)[0]
@@ -440,7 +441,7 @@ def test_get_rows_is_row_gather_of_dequantize(orc):
     assert np.all(z == 0)
 
 
-@pytest.mark.parametrize("tname", ["Q8_0", "Q4_0", "Q4_K", "Q5_K", "Q6_K", "MXFP4"])
+@pytest.mark.parametrize("tname", ["Q8_0", "Q4_0", "Q4_K", "Q5_K", "Q6_K", "MXFP4", "Q4_1", "Q5_0", "Q5_1"])
 def test_safe_blocks_give_weight_sized_finite_values(orc, tname):
     """The random-but-safe packed blocks (host and device generators; the
     device one runs on the CPU here) dequantize to finite values of the size
@@ -453,3 +454,68 @@ def test_safe_blocks_give_weight_sized_finite_values(orc, tname):
         v = orc.dequantize_f64(t, np.ascontiguousarray(blocks), k)
         assert np.all(np.isfinite(v))
         assert 1e-4 < np.abs(v).max() < 1.0, (tname, np.abs(v).max())
+
+
+
+@pytest.mark.parametrize("tname,levels", [("Q4_1", 15), ("Q5_1", 31)])
+def test_q4_1_q5_1_roundtrip_bound_and_codes(orc, tname, levels):
+    t = getattr(orc, tname)
+    w = synth.normal((32, 1024), 0.02, seed=15) * synth.lognormal_row_scale(32, seed=16)
+    p = orc.quantize_weights(t, w)
+    dq = orc.dequantize_f64(t, p, 1024).reshape(32, 32, 32)
+    wb = w.reshape(32, 32, 32).astype(np.float64)
+    step = (wb.max(axis=2) - wb.min(axis=2)) / levels
+    # half a step, plus the fp16 roundings of d (times up to `levels`) and of m
+    ed = np.maximum(step * 2.0 ** -11, 2.0 ** -25)
+    em = np.maximum(np.abs(wb.min(axis=2)) * 2.0 ** -11, 2.0 ** -25)
+    bound = 0.5 * (step + ed) + levels * ed + em
+    assert np.all(np.abs(dq - wb).max(axis=2) <= bound * 1.001)
+    codes = orc.dequantize_f64(t, _unit_scale(orc, t, p), 1024)
+    assert set(np.unique(codes).astype(int)) == set(range(levels + 1))
+
+
+def test_q5_0_roundtrip_bound_and_codes(orc):
+    w = synth.normal((32, 1024), 0.02, seed=17) * synth.lognormal_row_scale(32, seed=18)
+    p = orc.quantize_weights(orc.Q5_0, w)
+    dq = orc.dequantize_f64(orc.Q5_0, p, 1024).reshape(32, 32, 32)
+    wb = w.reshape(32, 32, 32).astype(np.float64)
+    dh = np.abs(p.reshape(32, 32, 22)[:, :, 0:2].copy().view(np.float16)[..., 0].astype(np.float64))[..., None]
+    # as Q4_0 with 16 steps each side: within a step (1 + 2^-9 for the clamp at +15)
+    assert np.all(np.abs(dq - wb) <= dh * (1.0 + 2.0 ** -9) + 1e-30)
+    codes = orc.dequantize_f64(orc.Q5_0, _unit_scale(orc, orc.Q5_0, p), 1024)
+    assert set(np.unique(codes).astype(int)) == set(range(-16, 16))
+
+
+def _unit_scale(orc, t, p):
+    """The same quants with d = 1 (and m = 0): dequantize gives the raw codes."""
+    b = p.reshape(p.shape[0], -1, orc.block_bytes(t)).copy()
+    b[:, :, 0:2] = [0x00, 0x3C]
+    if t in (orc.Q4_1, orc.Q5_1):
+        b[:, :, 2:4] = 0
+    return np.ascontiguousarray(b.reshape(p.shape[0], -1))
+
+
+@pytest.mark.parametrize("tname", ["Q4_1", "Q5_0", "Q5_1"])
+def test_q4_1_q5_0_q5_1_layout_bijection(orc, tname):
+    """Every quant bit (nibble bits and high bits) moves exactly one of the 32
+    values, and each set of bits covers all 32 once."""
+    t = getattr(orc, tname)
+    nb = orc.block_bytes(t)
+    qs0 = {"Q4_1": 4, "Q5_0": 6, "Q5_1": 8}[tname]
+    qh0 = {"Q4_1": None, "Q5_0": 2, "Q5_1": 4}[tname]
+    base = bytearray(nb)
+    base[0:2] = bytes.fromhex("003c")
+    ref = orc.dequantize_f32(t, np.frombuffer(bytes(base), np.uint8).reshape(1, -1), 32)[0]
+    groups = [[(pos, bit) for pos in range(qs0, qs0 + 16) for bit in (0, 4)]]
+    if qh0 is not None:
+        groups.append([(pos, bit) for pos in range(qh0, qh0 + 4) for bit in range(8)])
+    for group in groups:
+        hit = np.zeros(32, dtype=np.int32)
+        for pos, bit in group:
+            b = bytearray(base)
+            b[pos] ^= (1 << bit)
+            v = orc.dequantize_f32(t, np.frombuffer(bytes(b), np.uint8).reshape(1, -1), 32)[0]
+            changed = np.nonzero(v != ref)[0]
+            assert changed.size == 1, (tname, pos, bit)
+            hit[changed[0]] += 1
+        assert np.all(hit == 1)

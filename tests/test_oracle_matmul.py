@@ -28,10 +28,14 @@ def _unit_scale_blocks(orc, t, n, k, seed):
         p[:, :, 208:210] = [0x00, 0x3C]
     elif t == orc.MXFP4:
         p[:, :, 0] = 128            # scale 2: the value is the integer quant 2 * e2m1
+    elif t == orc.Q5_0:
+        p[:, :, 0:2] = [0x00, 0x3C]
+    elif t in (orc.Q4_1, orc.Q5_1):
+        p[:, :, 0:4] = [0x00, 0x3C, 0x00, 0x00]   # d = 1, m = 0
     return np.ascontiguousarray(p.reshape(n, -1))
 
 
-@pytest.mark.parametrize("tname", ["Q8_0", "Q4_0", "Q4_K", "Q5_K", "Q6_K", "MXFP4"])
+@pytest.mark.parametrize("tname", ["Q8_0", "Q4_0", "Q4_K", "Q5_K", "Q6_K", "MXFP4", "Q4_1", "Q5_0", "Q5_1"])
 def test_block_dots_brute_force(orc, tname):
     t = getattr(orc, tname)
     k, n, m = 512, 6, 3
@@ -55,7 +59,7 @@ def test_block_dots_brute_force(orc, tname):
         assert np.all(got == 32 * 127 * 127)
 
 
-@pytest.mark.parametrize("tname", ["Q8_0", "Q4_0", "Q6_K", "MXFP4"])
+@pytest.mark.parametrize("tname", ["Q8_0", "Q4_0", "Q6_K", "MXFP4", "Q5_0"])
 def test_blockwise_equals_dequant_dot(orc, tname):
     t = getattr(orc, tname)
     k = 1024
@@ -91,7 +95,8 @@ def test_blockwise_affine_min_term(orc, tname):
 
 
 @pytest.mark.parametrize("tname,tol", [("Q8_0", 0.02), ("Q4_0", 0.12), ("Q4_K", 0.15), ("Q5_K", 0.08),
-                                       ("Q6_K", 0.05), ("MXFP4", 0.2)])
+                                       ("Q6_K", 0.05), ("MXFP4", 0.2), ("Q4_1", 0.12), ("Q5_0", 0.08),
+                                       ("Q5_1", 0.06)])
 def test_quantized_matmul_tracks_fp32(orc, tname, tol):
     t = getattr(orc, tname)
     k = 2048
@@ -201,3 +206,24 @@ def test_moe_plain_rows(orc):
     ref = orc.moe_down(orc.Q4_K, bank, E, stride, n, k, np.repeat(xq, K, axis=0), ids, rw)
     got = (y.reshape(T, K, n) * rw.astype(np.float64)[:, :, None]).sum(axis=1)
     np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-300)
+
+
+
+@pytest.mark.parametrize("tname", ["Q4_1", "Q5_1"])
+def test_blockwise_plus_min_term(orc, tname):
+    """Q4_1 / Q5_1: blockwise y = dequant-dot - sum_b m_b*(d_a*sum(q_a) - s_a):
+    the +m term uses the stored s_a, so the difference is bounded by its fp16
+    rounding, and is real."""
+    t = getattr(orc, tname)
+    k = 1024
+    w = synth.safe_blocks(t, 16, k, seed=48)
+    xq = orc.quantize_q8_1(synth.normal((4, k), 1.0, seed=49))
+    y = orc.mul_mat(t, w, k, xq)
+    ref = orc.mul_mat_dequant_f64(t, w, k, xq)
+    dbits, _, qa = orc.q8_1_fields(xq)
+    da = dbits.view(np.float16).astype(np.float64)
+    qsum = np.abs(qa.astype(np.int64).sum(axis=2))
+    m = np.abs(w.reshape(16, -1, orc.block_bytes(t))[:, :, 2:4].copy().view(np.float16)[..., 0].astype(np.float64))
+    bound = (qsum[:, None, :] * np.abs(da)[:, None, :] * 2.0 ** -10 * m[None]).sum(axis=2)
+    assert np.all(np.abs(y - ref) <= bound + 1e-12)
+    assert np.abs(y - ref).max() > 0
