@@ -51,6 +51,7 @@ def lib():
             "orc_f32_to_f16": (ctypes.c_uint16, [ctypes.c_float]),
             "orc_bf16_to_f32": (ctypes.c_float, [ctypes.c_uint16]),
             "orc_f32_to_bf16": (ctypes.c_uint16, [ctypes.c_float]),
+            "orc_f64_to_bf16": (ctypes.c_uint16, [ctypes.c_double]),
             "orc_block_elems": (i64, [i32]),
             "orc_block_bytes": (i64, [i32]),
             "orc_row_size": (i64, [i32, i64]),
@@ -118,6 +119,11 @@ def f16_value(bits: int) -> float:
 
 def bf16_bits(x: float) -> int:
     return lib().orc_f32_to_bf16(x)
+
+
+def bf16_bits_f64(x: float) -> int:
+    """fp64 -> bf16 bits, rounded once (no fp32 step)."""
+    return lib().orc_f64_to_bf16(x)
 
 
 def bf16_value(bits: int) -> float:

@@ -123,10 +123,11 @@ float orc_bf16_to_f32(uint16_t h) {
     return f;
 }
 
-uint16_t orc_f32_to_bf16(float f) {
+/* round-to-nearest-even of an fp64 value to bf16, in one step (no fp32 hop) */
+uint16_t orc_f64_to_bf16(double f) {
     if (isnan(f)) return 0x7fc0;
     uint16_t sign = signbit(f) ? 0x8000 : 0;
-    double a = fabs((double)f);
+    double a = fabs(f);
     if (a == 0.0) return sign;
     int e;
     (void)frexp(a, &e);
@@ -139,6 +140,9 @@ uint16_t orc_f32_to_bf16(float f) {
     if (r < 128.0) return sign | (uint16_t)r; /* subnormal */
     return sign | (uint16_t)(((e + 127) << 7) | ((int)r - 128));
 }
+
+/* every fp32 value is an fp64 value: the same rounding */
+uint16_t orc_f32_to_bf16(float f) { return orc_f64_to_bf16((double)f); }
 
 static uint16_t rd16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
 static void wr16(uint8_t *p, uint16_t v) { p[0] = (uint8_t)(v & 0xff); p[1] = (uint8_t)(v >> 8); }
@@ -938,8 +942,9 @@ static void *moe_gu_worker(void *arg) {
             for (int64_t i = 0; i < I; i++) {
                 double g = dot_row(j->wt, we + i * rs, j->h, j->xq + t * xrs);
                 double u = dot_row(j->wt, we + (I + i) * rs, j->h, j->xq + t * xrs);
-                /* the intermediate is kept in the activation dtype (bf16) */
-                hrow[i] = orc_bf16_to_f32(orc_f32_to_bf16((float)(silu_f64(g) * u)));
+                /* the intermediate is kept in the activation dtype (bf16): the
+                 * fp64 value rounded once, with no fp32 step in between */
+                hrow[i] = orc_bf16_to_f32(orc_f64_to_bf16(silu_f64(g) * u));
             }
         }
         if (j->hbuf) memcpy(j->hbuf + r * I, hrow, sizeof(float) * (size_t)I);

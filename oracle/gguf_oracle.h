@@ -19,6 +19,7 @@ float orc_f16_to_f32(uint16_t h);
 uint16_t orc_f32_to_f16(float f);
 float orc_bf16_to_f32(uint16_t h);
 uint16_t orc_f32_to_bf16(float f);
+uint16_t orc_f64_to_bf16(double f);
 
 int64_t orc_block_elems(int type);
 int64_t orc_block_bytes(int type);

@@ -123,8 +123,26 @@ def test_mul_mat_row_subset_and_threads(orc):
 # --------------------------------------------------------------------------
 
 def _bf16_round(a):
-    import torch
-    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).float().numpy()
+    """fp64 -> nearest bf16 value (ties to even), rounded once: 8 significant
+    bits, by exact power-of-two scaling and numpy's round-half-even."""
+    a = np.asarray(a, dtype=np.float64)
+    _, e = np.frexp(a)                       # a = m * 2^e, 0.5 <= |m| < 1
+    e = np.maximum(e, -125)                  # below the normal range the quantum stays 2^-133
+    return np.ldexp(np.round(np.ldexp(a, 8 - e)), e - 8)
+
+
+def _bf16_round_via_f32(a):
+    """The same after an fp32 step: differs from _bf16_round when the fp32
+    value lands on a bf16 tie that the fp64 value was not on."""
+    return _bf16_round(np.asarray(a, dtype=np.float64).astype(np.float32).astype(np.float64))
+
+
+def _q8_0_rows(d_bits, q):
+    """Q8_0 rows of one block each: fp16 scale bits d_bits[i], int8 quants q[i]."""
+    out = np.zeros((len(d_bits), 34), np.uint8)
+    out[:, 0:2] = np.array(d_bits, np.uint16).astype("<u2").view(np.uint8).reshape(-1, 2)
+    out[:, 2:] = np.array(q, np.int8).view(np.uint8)
+    return out
 
 
 def test_moe_single_expert_is_dense_swiglu(orc):
@@ -142,6 +160,40 @@ def test_moe_single_expert_is_dense_swiglu(orc):
     np.testing.assert_array_equal(hq, orc.quantize_q8_1(h))
     y = orc.moe_down(orc.Q6_K, wd, 1, wd.nbytes, H, I, hq, ids, rw)
     np.testing.assert_allclose(y, 0.75 * orc.mul_mat(orc.Q6_K, wd, I, hq), rtol=1e-15, atol=1e-300)
+
+
+def test_moe_swiglu_rounds_fp64_to_bf16_once(orc):
+    """h = bf16(silu(g) * u) is one rounding of the fp64 value.  The first three
+    gate / up row pairs are hand-picked so that silu(g) * u lies off a bf16 tie
+    that its fp32 rounding lands on exactly: an fp32 step in between would
+    round those three the other way."""
+    H, I = 32, 32
+    rng = np.random.default_rng(81)
+    # (gate d, gate q, up d, up q) against x = e_0, whose q8_1 block is d = fp16(1/127), q_0 = 127
+    picked = [(0x240F, -49, 0x2085, -111), (0x2054, -13, 0x2340, -86), (0x1BCA, 44, 0x1D46, -27)]
+    dg = [p[0] for p in picked] + [0x2000] * (I - 3)
+    du = [p[2] for p in picked] + [0x2000] * (I - 3)
+    qg = rng.integers(-127, 128, (I, 32))
+    qu = rng.integers(-127, 128, (I, 32))
+    for i, p in enumerate(picked):
+        qg[i] = 0; qu[i] = 0
+        qg[i, 0] = p[1]; qu[i, 0] = p[3]
+    bank = np.concatenate([_q8_0_rows(dg, qg), _q8_0_rows(du, qu)]).reshape(-1)
+    x = np.zeros((1, H), np.float32)
+    x[0, 0] = 1.0
+    xq = orc.quantize_q8_1(x)
+    h, _ = orc.moe_gate_up(orc.Q8_0, bank, 1, bank.nbytes, 2 * I, H, xq, np.zeros((1, 1), np.int32))
+    # independent expectation: fp64 dot of the dequantized rows and activation, textbook SiLU
+    d_x = np.float16(np.float32(1.0) / np.float32(127.0)).astype(np.float64)
+    wg = np.array(dg, np.uint16).view(np.float16).astype(np.float64)[:, None] * qg
+    wu = np.array(du, np.uint16).view(np.float16).astype(np.float64)[:, None] * qu
+    xv = np.zeros(H)
+    xv[0] = d_x * 127.0
+    g, u = wg @ xv, wu @ xv
+    v = g / (1.0 + np.exp(-g)) * u
+    np.testing.assert_array_equal(h[0], _bf16_round(v))
+    # the pin is sensitive: an fp32 step would change exactly the picked rows here
+    assert np.all(_bf16_round_via_f32(v[:3]) != _bf16_round(v[:3]))
 
 
 def test_moe_repeated_and_inactive_routes(orc):
