@@ -149,6 +149,18 @@ def gguf_get_option(key: str) -> int:
     return int(load_library().gguf_get_option(key.encode()))
 
 
+def _check_x_rows(x: torch.Tensor, xt: int, k: int, what: str):
+    """The C ABI reads x as rows of k values (or q8_1 bytes) with a row stride:
+    the values of a row must be adjacent, and q8_1 rows packed back to back."""
+    if x.dim() != 2:
+        raise ValueError(f"{what}: x must be a 2-D tensor")
+    if xt == Q8_1:
+        if x.shape[0] > 1 and x.stride(0) != k // 32 * Q8_1_BYTES or x.shape[1] > 1 and x.stride(1) != 1:
+            raise ValueError(f"{what}: q8_1 rows of x must be contiguous")
+    elif x.shape[1] > 1 and x.stride(1) != 1:
+        raise ValueError(f"{what}: the values of a row of x must be contiguous (stride(1) == 1)")
+
+
 def gguf_quantize_q8_1(x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
     """x [m, k] (fp32 / bf16 / fp16, rows may be strided) -> q8_1 bytes [m, k/32*36]."""
     m, k = x.shape
@@ -192,6 +204,7 @@ def gguf_mul_mat(w: torch.Tensor, wt: int, n: int, k: int, x: torch.Tensor, xt: 
         xt = _TYPE_OF[x.dtype]
     if m is None:
         m = x.shape[0]
+    _check_x_rows(x, xt, k, "gguf_mul_mat")
     ldx = x.stride(0) if xt != Q8_1 else k // 32 * Q8_1_BYTES
     if out is None:
         if out_dtype is None:
@@ -216,6 +229,7 @@ def gguf_mul_mat_segments(wt: int, k: int, x: torch.Tensor, segments, xt: int | 
         xt = _TYPE_OF[x.dtype]
     if m is None:
         m = x.shape[0]
+    _check_x_rows(x, xt, k, "gguf_mul_mat_segments")
     ldx = x.stride(0) if xt != Q8_1 else k // 32 * Q8_1_BYTES
     outs = [o for (_, _, o) in segments]
     yt = _TYPE_OF[outs[0].dtype]
@@ -238,6 +252,7 @@ def gguf_mul_mat_noalloc(w: torch.Tensor, wt: int, n: int, k: int, x: torch.Tens
     inside the call; calls that overlap on one device race on the scratch)."""
     xt = _TYPE_OF[x.dtype]
     m = x.shape[0]
+    _check_x_rows(x, xt, k, "gguf_mul_mat_noalloc")
     if out is None:
         out = torch.empty((m, n), dtype=out_dtype or x.dtype, device=x.device)
     if out.stride(1) != 1:
@@ -266,6 +281,7 @@ def gguf_mul_mat_id(w: torch.Tensor, wt: int, n_experts: int, expert_stride: int
     n_tokens, top_k = ids.shape
     if xt is None:
         xt = _TYPE_OF[x.dtype]
+    _check_x_rows(x, xt, k, "gguf_mul_mat_id")
     ldx = x.stride(0) if xt != Q8_1 else gguf_row_size(Q8_1, k)
     if out is None:
         if mode == GATE_UP_SWIGLU:
@@ -309,6 +325,7 @@ def gguf_moe_ffn(w_gate_up: torch.Tensor, gate_up_type: int, gate_up_stride: int
     """The whole MoE expert block: y = sum_k w_k * down_e(silu(gate_e x) * up_e x)."""
     n_tokens, top_k = ids.shape
     xt = _TYPE_OF[x.dtype] if x.dtype != torch.uint8 else Q8_1
+    _check_x_rows(x, xt, hidden, "gguf_moe_ffn")
     if out is None:
         out = torch.empty((n_tokens, hidden), dtype=x.dtype if xt != Q8_1 else torch.bfloat16, device=x.device)
     args = moe_ffn_args(w_gate_up, gate_up_type, gate_up_stride, w_down, down_type, down_stride, n_experts, hidden,

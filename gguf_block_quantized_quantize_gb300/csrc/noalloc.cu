@@ -6,7 +6,10 @@
 // two calls that overlap in time on the same device (two streams, two host
 // threads) race on it.  The first call on a device looks its address up
 // (cudaGetSymbolAddress), which must not happen during stream capture: make
-// one ordinary call per device first.
+// one ordinary call per device first.  The address is kept for the life of
+// the process: it is not valid across cudaDeviceReset (the module may load
+// elsewhere in the new context), so a process that resets a device must not
+// call this entry point on that device afterwards.
 #include <stdio.h>
 
 #include <mutex>
@@ -70,7 +73,8 @@ extern "C" gguf_status gguf_mul_mat_noalloc(const void *w, int wt, int64_t n, in
                       "mul_mat_noalloc: the fixed scratch serves m <= 8 and k <= 16384 only; use gguf_mul_mat");
     const size_t need = (size_t)m * (size_t)(k / 32) * 36;
     if (need > NOALLOC_SCRATCH_BYTES) return report(GGUF_ERR_WORKSPACE, "mul_mat_noalloc: scratch too small");
-    if (m == 0 || n == 0 || k == 0) return GGUF_OK;
+    if (m == 0 || n == 0) return GGUF_OK;   // nothing to compute: pointers are not looked at
+    if (k == 0) return report(GGUF_ERR_SHAPE, "mul_mat_noalloc: k must be positive");
     if (!w || !x || !y) return report(GGUF_ERR_INVALID_ARG, "mul_mat_noalloc: null pointer");
     const size_t xs = xt == GGUF_F32 ? 4 : 2, ys = yt == GGUF_F32 ? 4 : 2;
     if (!aligned_to(w, 16) || !aligned_to(x, xs) || !aligned_to(y, ys))

@@ -214,10 +214,13 @@ gguf_status gguf_mul_mat_segments(int wt, const gguf_segment *segs, int nseg, in
  * {F32, BF16, F16}; the result is the same MMVQ computation that gguf_mul_mat
  * runs for these sizes under the default options.
  * Errors: GGUF_ERR_WORKSPACE when m > 8 or k > 16384 (use gguf_mul_mat);
- * otherwise as gguf_mul_mat.  Nothing has to be cleared between calls: every
+ * otherwise as gguf_mul_mat (m == 0 or n == 0 is a no-op; k == 0 with work
+ * to do is GGUF_ERR_SHAPE).  Nothing has to be cleared between calls: every
  * scratch byte that is read was written by the same call.
  * The first call on each device looks up the scratch address; make it before
- * any stream capture.  The scratch is shared by every caller on the device:
+ * any stream capture.  The address is kept until the process exits and does
+ * not survive cudaDeviceReset: do not call this entry point on a device after
+ * resetting it.  The scratch is shared by every caller on the device:
  * calls that overlap in time (other streams, other host threads) race on it
  * and must be serialized by the caller.
  */

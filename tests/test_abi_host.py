@@ -138,3 +138,35 @@ def test_mul_mat_id_modes_and_types(g):
     for wt, k in ((g.Q4_0, 96), (g.MXFP4, 96), (g.Q5_K, 256), (g.Q8_0, 64)):
         stride = -(-256 * g.gguf_row_size(wt, k) // 16) * 16
         assert _moe(g, wt=wt, k=k, ldx=k, expert_stride=stride) == 5, wt
+
+
+def test_noalloc_argument_checks(g):
+    L = g.load_library()
+
+    def na(**kw):
+        a = dict(w=FAKE, wt=g.Q4_K, n=16, k=256, x=FAKE, xt=g.BF16, m=4, ldx=256, y=FAKE, yt=g.BF16, ldy=16)
+        a.update(kw)
+        return L.gguf_mul_mat_noalloc(a["w"], a["wt"], a["n"], a["k"], a["x"], a["xt"], a["m"], a["ldx"], a["y"],
+                                      a["yt"], a["ldy"], None)
+    assert na(k=0, ldx=0) == 3                 # k == 0 with rows to compute: as gguf_mul_mat
+    assert _mm(g, k=0, ldx=0) == 3
+    assert na(m=0) == 0 and na(n=0) == 0       # empty products are no-ops
+    assert na(m=9) == 5 and na(k=16640, ldx=16640) == 5   # beyond the fixed scratch
+    assert na(xt=g.Q8_1) == 2
+    assert na(ldx=128) == 1
+
+
+def test_binding_rejects_strided_rows(g):
+    import torch
+    # checked before any pointer reaches the library (CPU tensors, nothing launched)
+    xt = torch.zeros(256, 4, dtype=torch.bfloat16).t()          # [4, 256] with stride(1) == 4
+    w = torch.zeros(16 * 144, dtype=torch.uint8)
+    for fn in (lambda: g.gguf_mul_mat(w, g.Q4_K, 16, 256, xt),
+               lambda: g.gguf_mul_mat_noalloc(w, g.Q4_K, 16, 256, xt),
+               lambda: g.gguf_mul_mat_segments(g.Q4_K, 256, xt, [(w, 16, torch.zeros(4, 16, dtype=torch.bfloat16))])):
+        with pytest.raises(ValueError):
+            fn()
+    # q8_1 rows with a gap between them
+    xq = torch.zeros(4, 2 * 288, dtype=torch.uint8)[:, :288]
+    with pytest.raises(ValueError):
+        g.gguf_mul_mat(w, g.Q4_K, 16, 256, xq, xt=g.Q8_1)
