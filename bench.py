@@ -36,6 +36,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# the headline metric's name, as the benchmark configuration states it
+METRIC = "GGUF matmul: weight-read HBM GB/s (MMVQ) and int8 TOPS (MMQ/MoE) on 1 GB300"
 DECODE_SHAPES = [(4096, 4096), (14336, 4096)]
 DECODE_MS = [1, 2, 4, 8]
 
@@ -315,10 +317,10 @@ def run_ours(args, rank, world, torch, dev):
     e2e = run_e2e(args, g, torch, dev, dec, per_step)
 
     result = {
-        "metric": "GGUF matmul: weight-read HBM GB/s (MMVQ) and int8 TOPS (MMQ/MoE) on 1 GB300",
+        "metric": METRIC,
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "u8", "data": "synthetic",
+        "dtype": "int8 dot, fp32 combine", "data": "synthetic",
         "config": {"workload": "decode MMVQ: Q4_K 4096x4096 and 14336x4096, bf16 activations M in {1,2,4,8}; "
                                "step = one bf16->q8_1 quantize of the 15 activation rows, then per M one "
                                "segment-table MMVQ launch over both weight matrices (each M-row slice shared by "
@@ -327,7 +329,7 @@ def run_ours(args, rank, world, torch, dev):
                    "weights": "random-but-safe packed Q4_K blocks", "parallelism": f"replicas x{world}"},
         "weight_bytes_per_step": weight_bytes, "bytes_per_step": per_step,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": MMVQ_TRAFFIC,
+                     "frac": round(achieved / hbm_peak, 4), "traffic": mmvq_traffic(),
                      "kernel": "MMVQ (dp4a mmvq_kernel for M<=4, int8 tensor-core for M=8), one segment-table launch "
                                "per M over both matrices; 4 launches per step, mean",
                      "peak_source": f"{peak_kind} hbm_gbs"},
@@ -342,10 +344,27 @@ def run_ours(args, rank, world, torch, dev):
 
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# decode MMVQ launches, averaged over the step's launches, from the ncu capture
-# summarized in profiles/mmvq_q4_k_decode.md; None whenever the kernel or the
-# launch set has changed since the capture.
-MMVQ_TRAFFIC = 42522432
+# decode MMVQ launches, averaged over the step's four segment launches, from one
+# ncu capture of this bench's decode step:
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none
+#       -k regex:mmvq -s 20 -c 8 python bench.py --steps 3 --warmup 3 --no-secondary --no-cpu-baseline
+# together with the SHA-256 of the MMVQ sources it was taken on.  The bench
+# reports the figure only while those sources are unchanged, and null otherwise.
+MMVQ_TRAFFIC = {"bytes": 42521216, "sources_sha256": "0627c8c65d4c787fb10028dd7a08665f2963cf50d104160b49e9dde838a012c1"}
+MMVQ_SOURCES = ("mmvq.cuh", "mmvq_mma.cuh", "mmvq_mma_q6k.cuh", "mmvq.cu", "mmvq_q4_k.cu", "common.cuh")
+
+
+def mmvq_sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for name in MMVQ_SOURCES:
+        with open(os.path.join(ROOT, "gguf_block_quantized_quantize_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def mmvq_traffic():
+    return MMVQ_TRAFFIC["bytes"] if MMVQ_TRAFFIC["sources_sha256"] == mmvq_sources_sha256() else None
 
 
 def run_e2e(args, g, torch, dev, dec, per_step):
@@ -452,6 +471,8 @@ def secondary(torch, g, synth, dev, stream, hbm_peak, tf_peak, peak_kind):
             ms = _time_eager(torch, stream, lambda: g.gguf_mul_mat(w, wt, n, k, x, out=y, ws=ws), 5, flush)
             tops = 2.0 * m * n * k / (ms * 1e-3) / 1e12
             out[name] = {"ms": round(ms, 4), "tops": round(tops, 1),
+                         "rate": "algorithmic 2*m*n*k ops/s (int8-equivalent); computed as fp16 tcgen05 MMAs of "
+                                 "the dequantized operands",
                          "roofline": {"bound": "tensor", "achieved": round(tops, 1), "peak": tf_peak,
                                       "unit": "TFLOP/s", "frac": round(tops / tf_peak, 4),
                                       "note": f"fp16 tcgen05 MMA; peak = {peak_kind} bf16 (same rate as fp16)"},
@@ -479,8 +500,8 @@ def secondary(torch, g, synth, dev, stream, hbm_peak, tf_peak, peak_kind):
             "ms": round(ms, 4), "tops": round(ops / (ms * 1e-3) / 1e12, 1),
             "frac_of_bf16_peak": round(ops / (ms * 1e-3) / 1e12 / tf_peak, 4),
             "frac_of_int8_mma_peak": round(ops / (ms * 1e-3) / 1e12 / p_int8, 3),
-            "note": "routed-row int8-equivalent ops 2*T*top_k*(2I*H + H*I) / time; gate_up Q4_K + SwiGLU + q8_1, "
-                    "down Q6_K + weighted sum"}
+            "note": "routed-row int8-equivalent ops 2*T*top_k*(2I*H + H*I) / time, computed as fp16 tcgen05 MMAs "
+                    "of the dequantized operands; gate_up Q4_K + SwiGLU + q8_1, down Q6_K + weighted sum"}
         # the same expert block at decode token counts: the route-batched MMVQ path (each routed
         # expert's rows read once per route); GB/s of the routed experts' packed weights
         for Td in (1, 16):
@@ -593,30 +614,42 @@ def llama_decode(torch, g, synth, dev, stream, hbm_peak):
         def mm(w, wt, n, k, xq, out):
             g.gguf_mul_mat(w, wt, n, k, xq, xt=g.Q8_1, m=m, out=out, ws=ws)
 
+        def seg(wt, k, xq, parts):   # weight matrices of one type on one input: one call
+            g.gguf_mul_mat_segments(wt, k, xq, [(ly_w, n, o) for (ly_w, n, o) in parts], xt=g.Q8_1, m=m, ws=ws)
+
         def step():
             g.gguf_get_rows(emb, Q6, V, D, ids, out=h)           # token embedding rows
             for ly in layers:
                 g.gguf_quantize_q8_1(act_d, out=xq_d)              # attention input, shared by q, k, v
-                for nm in ("q", "k", "v"):
-                    _, wt, n, k = next(s for s in layer_shapes if s[0] == nm)
-                    mm(ly[nm], wt, n, k, xq_d, outs[nm])
+                seg(Q4, D, xq_d, [(ly["q"], D, outs["q"]), (ly["k"], KV, outs["k"])])
+                mm(ly["v"], Q6, KV, D, xq_d, outs["v"])
                 g.gguf_quantize_q8_1(act_d, out=xq_d)              # attention output
                 mm(ly["o"], Q4, D, D, xq_d, outs["o"])
                 g.gguf_quantize_q8_1(act_d, out=xq_d)              # FFN input, shared by gate and up
-                mm(ly["gate"], Q4, F, D, xq_d, outs["gate"])
-                mm(ly["up"], Q4, F, D, xq_d, outs["up"])
+                seg(Q4, D, xq_d, [(ly["gate"], F, outs["gate"]), (ly["up"], F, outs["up"])])
                 g.gguf_quantize_q8_1(act_f, out=xq_f)              # FFN hidden
                 mm(ly["down"], Q6, D, F, xq_f, outs["down"])
             g.gguf_quantize_q8_1(act_d, out=xq_d)
             mm(emb, Q6, V, D, xq_d, logits)                        # tied LM head
 
-        step()
-        torch.cuda.synchronize()
-        gr = _capture(torch, stream, step, 1)
-        ms = _time_graphs(torch, stream, gr, 10, warm=2)
-        gbs = wbytes / (ms * 1e-3) / 1e9
-        res.append({"m": m, "ms": round(ms, 4), "weight_gb": round(wbytes / 1e9, 3), "gbs": round(gbs, 1),
-                    "frac": round(gbs / hbm_peak, 3), "path": "MMVQ" if m <= 8 else "MMQ"})
+        # M = 32 runs under the default dispatch, and once more with the Q4_K
+        # products on the 4-n-tile tensor-core MMVQ instead of MMQ
+        variants = [("default", None)] + ([("mmvq_tc_max_m=32", 32)] if m > 16 else [])
+        for label, tc_max in variants:
+            saved = g.gguf_get_option("mmvq_tc_max_m")
+            if tc_max is not None:
+                g.gguf_set_option("mmvq_tc_max_m", tc_max)
+            try:
+                step()
+                torch.cuda.synchronize()
+                gr = _capture(torch, stream, step, 1)
+                ms = _time_graphs(torch, stream, gr, 10, warm=2)
+            finally:
+                g.gguf_set_option("mmvq_tc_max_m", saved)
+            gbs = wbytes / (ms * 1e-3) / 1e9
+            res.append({"m": m, "dispatch": label, "ms": round(ms, 4), "weight_gb": round(wbytes / 1e9, 3),
+                        "gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 3)})
+            del gr
     return res
 
 
@@ -657,7 +690,7 @@ def run_reference(args, rank, world):
     v = statistics.median(p["value"] for p in per)
     cb = dict(per[-1])
     cb["value"] = v
-    return {"impl": "reference", "metric": "GGUF matmul: weight-read HBM GB/s (MMVQ) and int8 TOPS (MMQ/MoE) on 1 GB300",
+    return {"impl": "reference", "metric": METRIC,
             "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "decode MMVQ: Q4_K 4096x4096 and 14336x4096, bf16 activations M in {1,2,4,8}; "

@@ -26,7 +26,8 @@ LIB_PATH = os.path.join(_HERE, "libgguf_gb300.so")
 _DTYPE_OF = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}
 _TYPE_OF = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 
-_STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED_TYPE", 3: "SHAPE", 4: "ALIGNMENT", 5: "WORKSPACE", 6: "CUDA"}
+_STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED_TYPE", 3: "SHAPE", 4: "ALIGNMENT", 5: "WORKSPACE", 6: "CUDA",
+           7: "DEVICE"}
 
 
 class GgufError(RuntimeError):
@@ -82,6 +83,8 @@ SIGNATURES = {
     "gguf_debug_block_dots": (_i, [_p, _i, _i64, _i64, _p, _i64, _p, _p]),
     "gguf_set_option": (_i, [ctypes.c_char_p, _i64]),
     "gguf_get_option": (_i64, [ctypes.c_char_p]),
+    "gguf_device_errors": (_i, [ctypes.POINTER(ctypes.c_int32), _i, _p]),
+    "gguf_device_errors_async": (_i, [_p, _i, _p]),
 }
 
 _lib = None
@@ -334,6 +337,22 @@ def gguf_moe_ffn(w_gate_up: torch.Tensor, gate_up_type: int, gate_up_stride: int
     if ws is None:
         ws = _workspace(need, x.device)
     _check(load_library().gguf_moe_ffn(ctypes.byref(args), _ptr(ws), 0 if ws is None else ws.numel(), _stream()))
+    return out
+
+
+def gguf_device_errors(clear: bool = True) -> int:
+    """Error word of the tensor-core kernels after the current stream's work;
+    raises GgufError (status DEVICE) when a kernel gave up a bounded wait."""
+    v = ctypes.c_int32(0)
+    _check(load_library().gguf_device_errors(ctypes.byref(v), 1 if clear else 0, _stream()))
+    return int(v.value)
+
+
+def gguf_device_errors_async(out: torch.Tensor, clear: bool = True) -> torch.Tensor:
+    """Stream-ordered copy of the error word into the int32 device tensor ``out``."""
+    if out.dtype != torch.int32 or out.numel() < 1:
+        raise ValueError("gguf_device_errors_async: out must be an int32 tensor with one element")
+    _check(load_library().gguf_device_errors_async(_ptr(out), 1 if clear else 0, _stream()))
     return out
 
 

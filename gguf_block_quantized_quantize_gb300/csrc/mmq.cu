@@ -16,21 +16,34 @@
 // Tiles of 128 weight rows x BN activation rows, persistent over the GPU; small
 // token counts split K across CTAs (fp32 partial sums in the workspace, then a
 // conversion pass) so that every SM has work.
+#include <stdio.h>
+
 #include <mutex>
 
 #include "tcgemm.cuh"
 
 namespace gg {
 
-__device__ int g_tg_error;  // nonzero after a timed-out wait (diagnostics)
+// Error word of the tensor-core kernels: a CTA whose bounded wait gives up ORs
+// in the bit of its role (1 operand-B loads, 2 MMA issue, 4 weight unpack,
+// 8 epilogue, 16 accumulator hand-over, 32 packed-weight loads) and exits.
+// gguf_device_errors reads it back.
+__device__ int g_tg_error;
 
 int *tg_error_word() {
     static int *ptr[64] = {};
+    static std::mutex mu;
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (!ptr[dev]) cudaGetSymbolAddress(reinterpret_cast<void **>(&ptr[dev]), g_tg_error);
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptr[dev] && cudaGetSymbolAddress(reinterpret_cast<void **>(&ptr[dev]), g_tg_error) != cudaSuccess)
+        ptr[dev] = nullptr;
     return ptr[dev];
+}
+
+// *dst = the error word (stream-ordered); clear: reset it to 0 in the same step
+__global__ void tg_error_take_kernel(int32_t *dst, int clear) {
+    *dst = clear ? atomicExch(&g_tg_error, 0) : atomicOr(&g_tg_error, 0);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -151,3 +164,48 @@ cudaError_t launch_convert_rows(const float *yacc, int64_t m, int64_t n, void *y
 }
 
 }  // namespace gg
+
+using namespace gg;
+
+static gguf_status device_error_status(int v) {
+    if (v == 0) return GGUF_OK;
+    char msg[256];
+    snprintf(msg, sizeof(msg),
+             "device_errors: a tensor-core kernel gave up a bounded wait (flags 0x%x:%s%s%s%s%s%s); outputs of "
+             "the calls since the last check are not valid",
+             v, (v & 1) ? " operand loads" : "", (v & 2) ? " MMA issue" : "", (v & 4) ? " weight unpack" : "",
+             (v & 8) ? " epilogue" : "", (v & 16) ? " accumulator hand-over" : "", (v & 32) ? " packed-weight loads" : "");
+    return report(GGUF_ERR_DEVICE, msg);
+}
+
+extern "C" gguf_status gguf_device_errors(int32_t *flags, int clear, gguf_stream_t stream) {
+    if (!flags) return report(GGUF_ERR_INVALID_ARG, "device_errors: null flags");
+    *flags = 0;
+    int *word = tg_error_word();
+    if (!word) return report(GGUF_ERR_CUDA, "device_errors: the error word of the current device is not reachable");
+    cudaStream_t s = (cudaStream_t)stream;
+    int v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, word, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && clear) e = cudaMemsetAsync(word, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        char msg[256];
+        snprintf(msg, sizeof(msg), "device_errors: CUDA error %d (%s)", (int)e, cudaGetErrorString(e));
+        return report(GGUF_ERR_CUDA, msg);
+    }
+    *flags = v;
+    return device_error_status(v);
+}
+
+extern "C" gguf_status gguf_device_errors_async(int32_t *dev_flags, int clear, gguf_stream_t stream) {
+    if (!dev_flags) return report(GGUF_ERR_INVALID_ARG, "device_errors_async: null flags");
+    if (reinterpret_cast<uintptr_t>(dev_flags) % 4) return report(GGUF_ERR_ALIGNMENT, "device_errors_async: flags must be 4-byte aligned");
+    tg_error_take_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(dev_flags, clear ? 1 : 0);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        char msg[256];
+        snprintf(msg, sizeof(msg), "device_errors_async: CUDA error %d (%s)", (int)e, cudaGetErrorString(e));
+        return report(GGUF_ERR_CUDA, msg);
+    }
+    return GGUF_OK;
+}

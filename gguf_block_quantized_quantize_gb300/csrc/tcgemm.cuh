@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xbuf) + S::XBUF);
     uint64_t *full_a = bars, *full_b = bars + ST, *empty = bars + 2 * ST;
     uint64_t *tfull = bars + 3 * ST, *tempty = bars + 3 * ST + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * ST + 4);
+    uint64_t *drain = bars + 3 * ST + 4;  // completion of every MMA this CTA issued
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * ST + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -156,6 +157,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             tc::mbar_init(&tfull[b], 1);
             tc::mbar_init(&tempty[b], 128);
         }
+        tc::mbar_init(drain, 1);
         *abort_flag = 0;
         tc::fence_barrier_init();
         tc::prefetch_tmap(&map_hi);
@@ -273,6 +275,10 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                 }
                 tc::mma_commit(&tfull[b]);
             }
+            // every MMA issued so far has finished before TMEM is released (after
+            // an abort the epilogue no longer waits for them)
+            tc::mma_commit(drain);
+            if (!tc::mbar_wait(drain, 0)) fail(2);
         }
     } else if (warp < 2 + TG_PRODUCERS / 32) {
         // ================= A producers: thread p takes part p % PARTS of tile
@@ -561,7 +567,9 @@ inline cudaError_t tg_launch(const CUtensorMap &mh, const CUtensorMap &ml, const
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    kern<<<grid, TG_THREADS, S::SMEM, s>>>(mh, ml, p, tg_error_word());
+    int *err = tg_error_word();
+    if (!err) return cudaErrorInvalidSymbol;
+    kern<<<grid, TG_THREADS, S::SMEM, s>>>(mh, ml, p, err);
     return cudaGetLastError();
 }
 

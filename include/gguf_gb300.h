@@ -92,7 +92,8 @@ typedef enum {
     GGUF_ERR_SHAPE = 3,            /* K not a multiple of the block, or sizes inconsistent */
     GGUF_ERR_ALIGNMENT = 4,        /* a buffer or stride breaks the alignment rule */
     GGUF_ERR_WORKSPACE = 5,        /* ws smaller than the *_ws_size query */
-    GGUF_ERR_CUDA = 6              /* a CUDA runtime / launch error; see gguf_last_error() */
+    GGUF_ERR_CUDA = 6,             /* a CUDA runtime / launch error; see gguf_last_error() */
+    GGUF_ERR_DEVICE = 7            /* a kernel gave up a bounded wait (gguf_device_errors) */
 } gguf_status;
 
 /* Thread-local message describing the last non-OK status of this thread. */
@@ -370,6 +371,32 @@ gguf_status gguf_debug_block_dots(const void *w, int wt, int64_t n, int64_t k, c
  */
 gguf_status gguf_set_option(const char *key, int64_t value);
 int64_t gguf_get_option(const char *key);
+
+/*
+ * gguf_device_errors -- the error word of the tensor-core kernels (MMQ and the
+ * grouped MoE GEMMs) on the current device.  Those kernels bound every wait
+ * of their pipeline (one second); a CTA whose wait gives up sets the bit of
+ * its role, stops its work and exits, so the call that launched it has
+ * already returned GGUF_OK while its output is incomplete.  The prior art
+ * turned faults into errors the caller can see (FreeToken issue #671 "MoE
+ * cache, CPU experts and GGUF support", section "Known issues"); this query is
+ * how such a timeout reaches the caller.
+ *   flags  : host int32; receives the word (0 when every kernel finished).
+ *   clear  : nonzero resets the word to 0 after reading it.
+ *   stream : the word is read after all work queued on `stream` (the call
+ *            synchronizes that stream).
+ * Returns GGUF_OK when the word is 0, GGUF_ERR_DEVICE when a bit is set (the
+ * message names the roles: 1 operand loads, 2 MMA issue, 4 weight unpack,
+ * 8 epilogue, 16 accumulator hand-over, 32 packed-weight loads),
+ * GGUF_ERR_INVALID_ARG for a null flags pointer.
+ *
+ * gguf_device_errors_async -- the same read (and optional reset) as a
+ * stream-ordered device step with no host synchronization: the word is
+ * written to the device int32 *dev_flags when the stream reaches it.  Usable
+ * inside CUDA graph capture.
+ */
+gguf_status gguf_device_errors(int32_t *flags, int clear, gguf_stream_t stream);
+gguf_status gguf_device_errors_async(int32_t *dev_flags, int clear, gguf_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -170,3 +170,12 @@ def test_binding_rejects_strided_rows(g):
     xq = torch.zeros(4, 2 * 288, dtype=torch.uint8)[:, :288]
     with pytest.raises(ValueError):
         g.gguf_mul_mat(w, g.Q4_K, 16, 256, xq, xt=g.Q8_1)
+
+
+def test_device_error_query_arguments(g):
+    L = g.load_library()
+    # null flags: refused before any CUDA call
+    assert L.gguf_device_errors(None, 1, None) == 1
+    assert L.gguf_device_errors_async(None, 1, None) == 1
+    assert L.gguf_device_errors_async(ctypes.c_void_p(0x10002), 1, None) == 4
+    assert g._STATUS[7] == "DEVICE"

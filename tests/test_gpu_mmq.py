@@ -121,3 +121,16 @@ def test_mmq_lm_head_q6_k_full_size_sampled(g):
     got = y[torch.from_numpy(toks).to(DEV)][:, torch.from_numpy(rows).to(DEV)].float().cpu().numpy()
     assert np.all(np.isfinite(got))
     assert_close(got, ref, TOL_BF16, "Q6_K 248320x2048 @ 2048")
+
+
+def test_device_error_word_is_clear_after_mmq(g):
+    """A normal tensor-core call leaves the error word of the bounded waits at 0."""
+    g.gguf_device_errors(clear=True)
+    n, k, m = 1000, 2048, 300
+    w = _u8(_weights(oracle.Q4_K, n, k, seed=9, safe=True))
+    for dt in (torch.bfloat16, torch.float32):
+        g.gguf_mul_mat(w, oracle.Q4_K, n, k, synth.activations(m, k, seed=10, dtype=dt).to(DEV))
+    assert g.gguf_device_errors(clear=False) == 0
+    flag = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    g.gguf_device_errors_async(flag, clear=True)
+    assert int(flag.item()) == 0

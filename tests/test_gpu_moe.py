@@ -420,3 +420,49 @@ def test_vec_moe_full_size_decode(g):
     _, hq = oracle.moe_gate_up(oracle.Q4_K, bank_gu, E, sgu, 2 * I, H, xq, ids, nthreads=8)
     ref = oracle.moe_down(oracle.Q6_K, bank_d, E, sd, H, I, hq, ids, rw, nthreads=8)
     assert_close_moe_e2e(y, ref, "vec moe full size")
+
+
+def _e2e_error_stats(y, ref):
+    from _util import rel_err
+    e = rel_err(y, ref)
+    q = np.percentile(e, [50, 99, 99.9, 99.99])
+    return {"max": float(e.max()), "p50": float(q[0]), "p99": float(q[1]), "p99.9": float(q[2]),
+            "p99.99": float(q[3]), "frac_gt_1e-2": float((e > 1e-2).mean()), "frac_gt_3e-3": float((e > 3e-3).mean()),
+            "n": int(e.size)}
+
+
+@pytest.mark.parametrize("T,vec", [(8192, False), (256, True)])
+def test_moe_full_size_error_distribution(g, T, vec):
+    """Per-element error of the fused FFN against the full oracle chain on the
+    full-size expert block (E = 256, top-8, H = 2048, I = 512): 64 tokens,
+    the first 16, the last 16 and 32 spread between (printed with -s)."""
+    E, K, H, I = 256, 8, 2048, 512
+    bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 700, True)
+    bank_d = _bank(oracle.Q6_K, E, H, I, 701, True)
+    sgu, sd = bank_gu.nbytes // E, bank_d.nbytes // E
+    ids, rw = synth.routes(T, E, K, seed=2)
+    x = synth.activations(T, H, seed=1, dtype=torch.bfloat16)
+    saved = g.gguf_get_option("moe_vec_max_tokens")
+    g.gguf_set_option("moe_vec_max_tokens", 256 if vec else 0)
+    try:
+        y = g.gguf_moe_ffn(_u8(bank_gu), g.Q4_K, sgu, _u8(bank_d), g.Q6_K, sd, E, H, I, x.to(DEV), _u8(ids),
+                           _u8(rw)).float().cpu().numpy()
+    finally:
+        g.gguf_set_option("moe_vec_max_tokens", saved)
+    toks = sorted(set(list(range(16)) + list(range(T - 16, T)) +
+                      np.random.default_rng(5).choice(np.arange(16, T - 16), 32, replace=False).tolist()))
+    xq = oracle.quantize_q8_1(x[toks].float().numpy())
+    sub_ids, sub_rw = ids[toks], rw[toks]
+    _, hq = oracle.moe_gate_up(oracle.Q4_K, bank_gu, E, sgu, 2 * I, H, xq, sub_ids, nthreads=16)
+    ref = oracle.moe_down(oracle.Q6_K, bank_d, E, sd, H, I, hq, sub_ids, sub_rw, nthreads=16)
+    st = _e2e_error_stats(y[toks], ref)
+    print(f"\nmoe e2e error T={T} {'vector' if vec else 'tensor-core'}: {st}")
+    assert_close_moe_e2e(y[toks], ref, f"moe e2e T={T}")
+
+
+def test_device_error_word_is_clear_after_moe(g, path):
+    g.gguf_device_errors(clear=True)
+    E, K, H, I, T, bank_gu, _, ids, rw, x = _small_case()
+    sgu = bank_gu.nbytes // E
+    g.gguf_mul_mat_id(_u8(bank_gu), g.Q4_K, E, sgu, 2 * I, H, x.to(DEV), _u8(ids), g.GATE_UP_SWIGLU)
+    assert g.gguf_device_errors(clear=True) == 0
