@@ -106,6 +106,8 @@ static int64_t g_mmvq_tc_min_m = 5;
 // path; the workspace reserves its buffers up to MOE_VEC_CAP tokens
 constexpr int64_t MOE_VEC_CAP = 256;
 static int64_t g_moe_vec_max_tokens = 256;
+static int64_t g_mmq_stage = 1;
+int64_t option_mmq_stage() { return g_mmq_stage; }
 int64_t option_mmvq_tc() { return g_mmvq_tc; }
 int64_t option_mmvq_tc_min_m() { return g_mmvq_tc_min_m; }
 int64_t option_mmvq_tc_max_m() { return g_mmvq_tc_max_m; }
@@ -336,9 +338,9 @@ static gguf_status check_bank(const char *what, const void *w, int wt, int64_t E
 static MoeWs moe_call_layout(const gguf_moe_args *a, void *base) {
     const int64_t R = a->n_tokens * a->top_k;
     const int64_t kx = op_pitch(a->wt, a->k);
+    // the grouped GEMMs' fp16 operand holds one row per route, in grouped order
     if (a->mode == GGUF_MOE_GATE_UP_SWIGLU)
-        return moe_ws_layout(base, a->n_experts, R, a->n_tokens * kx, 0, 0, false,
-                             a->n_tokens <= MOE_VEC_CAP ? a->n : 0);
+        return moe_ws_layout(base, a->n_experts, R, R * kx, 0, 0, false, a->n_tokens <= MOE_VEC_CAP ? a->n : 0);
     return moe_ws_layout(base, a->n_experts, R, R * kx, R * a->n, 0, false);
 }
 
@@ -372,10 +374,14 @@ static gguf_status check_moe(const gguf_moe_args *a) {
     return GGUF_OK;
 }
 
-static cudaError_t to_f16_operand(const void *x, int xt, int64_t rows, int64_t k, int64_t ldx, uint16_t *xh,
-                                  uint16_t *xl, int64_t pitch, cudaStream_t s) {
-    return xt == GGUF_Q8_1 ? launch_q8_1_to_f16((const uint8_t *)x, rows, k, xh, xl, s, pitch)
-                           : launch_quantize_q8_1(x, xt, rows, k, ldx, nullptr, xh, xl, s, pitch);
+// the fp16 operand of the grouped GEMMs: row i (grouped order) is x row
+// route_list[i] / rdiv (rdiv = top_k: token rows; 1: route rows)
+static cudaError_t to_f16_operand(const void *x, int xt, int64_t R, int64_t k, int64_t ldx, uint16_t *xh,
+                                  uint16_t *xl, int64_t pitch, const MoeWs &w, int64_t E, int32_t rdiv,
+                                  cudaStream_t s) {
+    return xt == GGUF_Q8_1
+               ? launch_q8_1_to_f16((const uint8_t *)x, R, k, xh, xl, s, pitch, w.route_list, rdiv, w.offsets + E)
+               : launch_quantize_q8_1(x, xt, R, k, ldx, nullptr, xh, xl, s, pitch, w.route_list, rdiv, w.offsets + E);
 }
 
 size_t gguf_mul_mat_id_ws_size(const gguf_moe_args *args) {
@@ -438,26 +444,31 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
         const int64_t idim = a->n / 2;
         const size_t ybytes = a->yt == GGUF_Q8_1 ? (size_t)(R * row_size(GGUF_Q8_1, idim)) : (size_t)(R * idim * 2);
         if ((e = cudaMemsetAsync(a->y, 0, ybytes, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id");
-        if ((e = to_f16_operand(a->x, a->xt, a->n_tokens, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), s)) != cudaSuccess) return cuda_status(e, "mul_mat_id quantize");
         if ((e = moe_group(a->ids, nullptr, R, a->n_experts, false, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id grouping");
+        if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), w, a->n_experts,
+                                (int32_t)a->top_k, s)) != cudaSuccess)
+            return cuda_status(e, "mul_mat_id quantize");
         e = launch_moe_gate_up((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, w.xl, a->top_k, R,
                                a->n_experts, w, a->yt == GGUF_Q8_1 ? (uint8_t *)a->y : nullptr,
                                a->yt == GGUF_BF16 ? (uint16_t *)a->y : nullptr,
-                               a->yt == GGUF_F16 ? (uint16_t *)a->y : nullptr, nullptr, a->n / 2, s);
+                               a->yt == GGUF_F16 ? (uint16_t *)a->y : nullptr, nullptr, a->n / 2, false, s);
         return cuda_status(e, "mul_mat_id gate_up");
     }
     if (plain) {   // token rows, one output row per route
-        if ((e = to_f16_operand(a->x, a->xt, a->n_tokens, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), s)) != cudaSuccess)
-            return cuda_status(e, "mul_mat_id quantize");
         if ((e = moe_group(a->ids, nullptr, R, a->n_experts, false, a->dev_status, w, bn, s)) != cudaSuccess)
             return cuda_status(e, "mul_mat_id grouping");
+        if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), w, a->n_experts,
+                                (int32_t)a->top_k, s)) != cudaSuccess)
+            return cuda_status(e, "mul_mat_id quantize");
         if ((e = launch_moe_down((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, w.xl, a->top_k, R,
-                                 a->n_experts, w, w.z, a->yt == GGUF_F32, s, true)) != cudaSuccess)
+                                 a->n_experts, w, w.z, a->yt == GGUF_F32, s)) != cudaSuccess)
             return cuda_status(e, "mul_mat_id");
         return cuda_status(launch_moe_plain_store(w.z, w.pos, R, a->n, a->y, a->yt, s), "mul_mat_id store");
     }
-    if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), s)) != cudaSuccess) return cuda_status(e, "mul_mat_id quantize");
     if ((e = moe_group(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id grouping");
+    if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), w, a->n_experts, 1, s)) !=
+        cudaSuccess)
+        return cuda_status(e, "mul_mat_id quantize");
     if ((e = launch_moe_down((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, w.xl, a->top_k, R,
                              a->n_experts, w, w.z, a->yt == GGUF_F32, s)) != cudaSuccess)
         return cuda_status(e, "mul_mat_id down");
@@ -467,7 +478,7 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
 
 static MoeWs ffn_layout(const gguf_moe_ffn_args *a, void *base) {
     const int64_t R = a->n_tokens * a->top_k;
-    return moe_ws_layout(base, a->n_experts, R, a->n_tokens * op_pitch(a->gate_up_type, a->hidden),
+    return moe_ws_layout(base, a->n_experts, R, R * op_pitch(a->gate_up_type, a->hidden),
                          R * a->hidden, R * op_pitch(a->down_type, a->inter), a->yt == GGUF_F32,
                          a->n_tokens <= MOE_VEC_CAP ? 2 * a->inter : 0);
 }
@@ -525,12 +536,14 @@ gguf_status gguf_moe_ffn(const gguf_moe_ffn_args *a, void *ws, size_t ws_bytes, 
         return cuda_status(launch_moe_finalize(w.z, w.pos, a->route_w, a->n_tokens, a->top_k, a->hidden, a->y, a->yt, s),
                            "moe_ffn finalize");
     }
-    if ((e = to_f16_operand(a->x, a->xt, a->n_tokens, a->hidden, a->ldx, w.xh, w.xl, op_pitch(a->gate_up_type, a->hidden), s)) != cudaSuccess) return cuda_status(e, "moe_ffn quantize");
     // one grouping serves both GEMMs; a route of weight 0 contributes nothing and is skipped by both
     if ((e = moe_group(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "moe_ffn grouping");
+    if ((e = to_f16_operand(a->x, a->xt, R, a->hidden, a->ldx, w.xh, w.xl, op_pitch(a->gate_up_type, a->hidden), w,
+                            a->n_experts, (int32_t)a->top_k, s)) != cudaSuccess)
+        return cuda_status(e, "moe_ffn quantize");
     if ((e = launch_moe_gate_up((const uint8_t *)a->w_gate_up, a->gate_up_type, a->gate_up_stride, 2 * a->inter,
                                 a->hidden, w.xh, w.xl, a->top_k, R, a->n_experts, w, nullptr, nullptr, w.h16, w.h16lo,
-                                op_pitch(a->down_type, a->inter), s)) != cudaSuccess)
+                                op_pitch(a->down_type, a->inter), true, s)) != cudaSuccess)
         return cuda_status(e, "moe_ffn gate_up");
     if ((e = launch_moe_down((const uint8_t *)a->w_down, a->down_type, a->down_stride, a->hidden, a->inter, w.h16,
                              w.h16lo, a->top_k, R, a->n_experts, w, w.z, a->yt == GGUF_F32, s)) != cudaSuccess)
@@ -580,6 +593,10 @@ gguf_status gguf_set_option(const char *key, int64_t value) {
         g_mmq_enable = value != 0;
         return GGUF_OK;
     }
+    if (!strcmp(key, "mmq_stage")) {
+        g_mmq_stage = value != 0;
+        return GGUF_OK;
+    }
     return fail(GGUF_ERR_INVALID_ARG, "set_option: unknown key '%s'", key);
 }
 
@@ -591,6 +608,7 @@ int64_t gguf_get_option(const char *key) {
     if (!strcmp(key, "mmvq_tc_min_m")) return g_mmvq_tc_min_m;
     if (!strcmp(key, "moe_vec_max_tokens")) return g_moe_vec_max_tokens;
     if (!strcmp(key, "mmvq_tc_max_m")) return g_mmvq_tc_max_m;
+    if (!strcmp(key, "mmq_stage")) return g_mmq_stage;
     return -1;
 }
 

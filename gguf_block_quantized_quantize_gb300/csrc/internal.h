@@ -29,11 +29,15 @@ gguf_status report(gguf_status st, const char *msg);
 // xh[m][pitch] = fp16(d16*q) when xh != nullptr, and its low part
 // xl = fp16(d16*q - xh) when xl != nullptr.  pitch > k appends the Q4_K
 // / Q5_K min-term correction columns (see op_pitch) and zero padding.
+// rmap (optional, device): output row r is input row rmap[r] / rdiv, for the
+// rows r < *rcount (device); the rows past it are not written.
 cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int64_t ldx, uint8_t *xq,
-                                 uint16_t *xh, uint16_t *xl, cudaStream_t s, int64_t pitch = 0);
+                                 uint16_t *xh, uint16_t *xl, cudaStream_t s, int64_t pitch = 0,
+                                 const int32_t *rmap = nullptr, int32_t rdiv = 1, const int32_t *rcount = nullptr);
 // the same fp16 operand(s) from q8_1 rows
 cudaError_t launch_q8_1_to_f16(const uint8_t *xq, int64_t m, int64_t k, uint16_t *xh, uint16_t *xl, cudaStream_t s,
-                               int64_t pitch = 0);
+                               int64_t pitch = 0, const int32_t *rmap = nullptr, int32_t rdiv = 1,
+                               const int32_t *rcount = nullptr);
 // Row length of the tensor-core operand for weight type wt: k, plus for the
 // affine K-quants (Q4_K, Q5_K) one min-term correction column per 32-block,
 // rounded up to the 64-value K step.
@@ -53,6 +57,9 @@ int64_t option_mmvq_tc_min_m();
 // option "mmvq_tc_max_m" (default 32): Q4_K products of 9..this many tokens run
 // as one tensor-core MMVQ launch instead of MMQ
 int64_t option_mmvq_tc_max_m();
+// option "mmq_stage" (default 1): the tensor-core GEMM stages packed weight
+// rows in shared memory with bulk tensor copies where their layout allows
+int64_t option_mmq_stage();
 // whether m (> 8) tokens of K-long Q4_K rows take the tensor-core MMVQ
 bool mmvq_tc_wide(int wt, int64_t k, int64_t m);
 
@@ -127,10 +134,10 @@ cudaError_t moe_mark(const int32_t *ids, const float *rw, int64_t R, int64_t E, 
 cudaError_t launch_moe_gate_up(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
                                const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
                                const MoeWs &ws, uint8_t *hq, uint16_t *hbf, uint16_t *h16, uint16_t *h16lo,
-                               int64_t hpitch, cudaStream_t s);
+                               int64_t hpitch, bool h16_grouped, cudaStream_t s);
 cudaError_t launch_moe_down(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
                             const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
-                            const MoeWs &ws, float *z, bool precise, cudaStream_t s, bool x_by_token = false);
+                            const MoeWs &ws, float *z, bool precise, cudaStream_t s);
 // y[R][n] (out dtype) from the per-route rows z, zero rows for skipped routes (pos < 0)
 cudaError_t launch_moe_plain_store(const float *z, const int32_t *pos, int64_t R, int64_t n, void *y, int yt,
                                    cudaStream_t s);

@@ -64,10 +64,11 @@ template <int WT, int BN, bool PRECISE, int OT>
 static cudaError_t launch_dense(const uint8_t *w, int64_t n, int64_t k, const uint16_t *xh, const uint16_t *xl,
                                 int64_t m, void *y, int64_t ldy, float *yacc, cudaStream_t s) {
     const int64_t kx = op_pitch(WT, k);
-    CUtensorMap mh, ml;
+    CUtensorMap mh, ml, mw;
     cudaError_t e = tg_make_map(&mh, xh, m, kx, BN);
     if (e != cudaSuccess) return e;
     ml = mh;
+    mw = mh;
     if (PRECISE && (e = tg_make_map(&ml, xl, m, kx, BN)) != cudaSuccess) return e;
     TgParams p{};
     p.w = w;
@@ -76,6 +77,8 @@ static cudaError_t launch_dense(const uint8_t *w, int64_t n, int64_t k, const ui
     p.k = k;
     p.kx = kx;
     p.m = m;
+    if (option_mmq_stage())
+        tg_plan_staging(p, &mw, WT, w, n, 1, 0, k, TG_BM, tg_base_bytes<WT, BN, PRECISE, TG_DENSE>());
     const int64_t tiles_n = (n + TG_BM - 1) / TG_BM, tiles_m = (m + BN - 1) / BN;
     const int KS = (int)((kx + TG_BK - 1) / TG_BK);
     const int sms = device_info().sm_count;
@@ -84,7 +87,8 @@ static cudaError_t launch_dense(const uint8_t *w, int64_t n, int64_t k, const ui
         const int64_t base = tiles_n * tiles_m;
         while (base * splits < sms && (KS + splits) / (splits + 1) >= 4) splits++;
     }
-    const int kps = (KS + splits - 1) / splits;
+    int kps = (KS + splits - 1) / splits;
+    if (p.pstages > 0 && p.pchunked) kps = (kps + 3) / 4 * 4;   // splits start on a staged chunk
     splits = (KS + kps - 1) / kps;
     const int64_t tiles = tiles_n * tiles_m * splits;
     if (tiles > INT32_MAX) return cudaErrorInvalidValue;
@@ -102,7 +106,7 @@ static cudaError_t launch_dense(const uint8_t *w, int64_t n, int64_t k, const ui
     p.yacc = splits > 1 ? yacc : nullptr;
     if (splits > 1 && (e = cudaMemsetAsync(yacc, 0, sizeof(float) * (size_t)(m * n), s)) != cudaSuccess) return e;
     const int grid = (int)(tiles < sms ? tiles : sms);
-    e = tg_launch<WT, BN, PRECISE, TG_DENSE, OT>(mh, ml, p, grid, s);
+    e = tg_launch<WT, BN, PRECISE, TG_DENSE, OT>(mh, ml, mw, p, grid, s);
     if (e != cudaSuccess || splits == 1) return e;
     return launch_convert_rows(yacc, m, n, y, OT, ldy, s);
 }

@@ -19,14 +19,19 @@
 // CTAs past the device-side tile count exit at once.
 //
 // GEMM tile: 128 weight rows x BN routes x 64 K per stage, the same fp16
-// tcgen05 engine as the dense MMQ.  The activation rows of a tile are gathered
-// by TMA tile::gather4 (token rows for gate_up, route rows for down); the last
-// tile of an expert issues the MMA with N rounded up to 16 only.
+// tcgen05 engine as the dense MMQ.  The activation rows of a tile are loaded
+// as one 2-D box per K-step; the last tile of an expert issues the MMA with N
+// rounded up to 16 only.
+// The activation operand is written in grouped route order (the conversion
+// to the fp16 operand reads each row through route_list), so an expert's
+// routes are consecutive rows and a tile loads them with plain 2-D bulk
+// tensor copies instead of per-row gathers.
 //   gate_up : the A tile holds 64 gate rows i and the 64 matching up rows I+i,
 //             so the epilogue has g and u of the same (route, i): it computes
 //             h = silu(g) * u in fp32, rounds it to bf16 (the activation dtype),
 //             quantizes each 32 consecutive i (one warp) to a q8_1 block, and
-//             writes q8_1 / bf16 / fp16 (d16*q, the operand of the down GEMM).
+//             writes q8_1 / bf16 (per route) or fp16 (d16*q, the operand of the
+//             down GEMM, in grouped order).
 //   down    : z[route][n] = W_down[e] . h_route (fp32, plain stores); a last
 //             pass sums each token's routes in slot order, y[t] = sum_k w_k z,
 //             so the result is deterministic and needs no atomics.
@@ -245,22 +250,30 @@ cudaError_t moe_group(const int32_t *ids, const float *rw, int64_t R, int64_t E,
     return cudaGetLastError();
 }
 
-// rows: operand rows (tokens for gate_up, routes for down), each p.kx fp16;
-// the gather reads one-row boxes of 64 values
-template <int MODE, bool PRECISE>
-static cudaError_t launch_moe_mode(int wt, const TgParams &p, int64_t rows, cudaStream_t s) {
-    CUtensorMap mh{}, ml{};
-    cudaError_t e = tg_make_map(&mh, p.xh, rows, p.kx, 1);
-    if (e == cudaSuccess && PRECISE) e = tg_make_map(&ml, p.xl, rows, p.kx, 1);
+// rows: operand rows in grouped route order (R), each p.kx fp16; a tile
+// reads 64 values of its 128 consecutive rows per K-step
+template <int WT, int MODE, bool PRECISE>
+static cudaError_t launch_moe_wt(TgParams p, int64_t rows, int64_t n_experts, cudaStream_t s) {
+    CUtensorMap mh{}, ml{}, mw{};
+    cudaError_t e = tg_make_map(&mh, p.xh, rows, p.kx, MOE_BN);
+    if (e == cudaSuccess && PRECISE) e = tg_make_map(&ml, p.xl, rows, p.kx, MOE_BN);
     if (e != cudaSuccess) return e;
+    if (option_mmq_stage())   // gate_up buffers: 64 gate rows and the 64 matching up rows
+        tg_plan_staging(p, &mw, WT, p.w, p.n, n_experts, p.expert_stride, p.k, MODE == TG_MOE_GATE_UP ? 64 : TG_BM,
+                        tg_base_bytes<WT, MOE_BN, PRECISE, MODE>());
     const int grid = device_info().sm_count;  // persistent; CTAs beyond the device-side tile count exit
+    return tg_launch<WT, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, mw, p, grid, s);
+}
+
+template <int MODE, bool PRECISE>
+static cudaError_t launch_moe_mode(int wt, const TgParams &p, int64_t rows, int64_t n_experts, cudaStream_t s) {
     switch (wt) {
-    case GGUF_Q4_K: return tg_launch<GGUF_Q4_K, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, p, grid, s);
-    case GGUF_Q6_K: return tg_launch<GGUF_Q6_K, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, p, grid, s);
-    case GGUF_Q8_0: return tg_launch<GGUF_Q8_0, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, p, grid, s);
-    case GGUF_Q4_0: return tg_launch<GGUF_Q4_0, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, p, grid, s);
-    case GGUF_Q5_K: return tg_launch<GGUF_Q5_K, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, p, grid, s);
-    case GGUF_MXFP4: return tg_launch<GGUF_MXFP4, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, p, grid, s);
+    case GGUF_Q4_K: return launch_moe_wt<GGUF_Q4_K, MODE, PRECISE>(p, rows, n_experts, s);
+    case GGUF_Q6_K: return launch_moe_wt<GGUF_Q6_K, MODE, PRECISE>(p, rows, n_experts, s);
+    case GGUF_Q8_0: return launch_moe_wt<GGUF_Q8_0, MODE, PRECISE>(p, rows, n_experts, s);
+    case GGUF_Q4_0: return launch_moe_wt<GGUF_Q4_0, MODE, PRECISE>(p, rows, n_experts, s);
+    case GGUF_Q5_K: return launch_moe_wt<GGUF_Q5_K, MODE, PRECISE>(p, rows, n_experts, s);
+    case GGUF_MXFP4: return launch_moe_wt<GGUF_MXFP4, MODE, PRECISE>(p, rows, n_experts, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -291,36 +304,32 @@ static TgParams moe_params(const uint8_t *w, int wt, int64_t expert_stride, int6
 cudaError_t launch_moe_gate_up(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
                                const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
                                const MoeWs &ws, uint8_t *hq, uint16_t *hbf, uint16_t *h16, uint16_t *h16lo,
-                               int64_t hpitch, cudaStream_t s) {
-    (void)E;
+                               int64_t hpitch, bool h16_grouped, cudaStream_t s) {
     if (R == 0) return cudaSuccess;
     TgParams p = moe_params(w, wt, expert_stride, n, k, xh, xl, top_k, ws);
+    p.h16_grouped = h16_grouped ? 1 : 0;
     p.hpitch = hpitch < n / 2 ? n / 2 : hpitch;
     p.tiles_x = (int)(n / 2 / 64);
     p.hq = hq;
     p.hbf = hbf;
     p.h16 = h16;
     p.h16lo = h16lo;
-    p.m = R / top_k;  // token rows of the operand
-    return launch_moe_mode<TG_MOE_GATE_UP, true>(wt, p, p.m, s);
+    p.m = R / top_k;
+    return launch_moe_mode<TG_MOE_GATE_UP, true>(wt, p, R, E, s);
 }
 
-// down: z[R][n] = W[e] . x[route] for every grouped route; xh / xl: route
-// rows [R][kx] (xl only in the precise mode), or token rows [R / top_k][kx]
-// when x_by_token (every route of a token reads the token's row)
+// down: z[R][n] = W[e] . x[route] for every grouped route; xh / xl: the
+// operand rows in grouped route order [R][kx] (xl only in the precise mode)
 cudaError_t launch_moe_down(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
                             const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
-                            const MoeWs &ws, float *z, bool precise, cudaStream_t s, bool x_by_token) {
-    (void)E;
+                            const MoeWs &ws, float *z, bool precise, cudaStream_t s) {
     if (R == 0) return cudaSuccess;
     TgParams p = moe_params(w, wt, expert_stride, n, k, xh, xl, top_k, ws);
     p.tiles_x = (int)((n + TG_BM - 1) / TG_BM);
     p.yacc = z;
-    p.m = R / top_k;  // tokens; the operand has R = top_k * m rows (m when x_by_token)
-    p.x_by_token = x_by_token ? 1 : 0;
-    const int64_t rows = x_by_token ? p.m : R;
-    return precise ? launch_moe_mode<TG_MOE_DOWN, true>(wt, p, rows, s)
-                   : launch_moe_mode<TG_MOE_DOWN, false>(wt, p, rows, s);
+    p.m = R / top_k;
+    return precise ? launch_moe_mode<TG_MOE_DOWN, true>(wt, p, R, E, s)
+                   : launch_moe_mode<TG_MOE_DOWN, false>(wt, p, R, E, s);
 }
 
 // y[r][c] = z[r][c] for an active route, 0 for a skipped one (out dtype)

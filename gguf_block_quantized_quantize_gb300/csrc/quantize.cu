@@ -73,11 +73,19 @@ __device__ __forceinline__ void write_correction(uint16_t *hi_row, uint16_t *lo_
     }
 }
 
+// Row map of the permuted operand (MoE): output row r is input row
+// rmap[r] / rdiv; rows at or past *rcount are not written.
+struct RowMap {
+    const int32_t *rmap;
+    int32_t rdiv;
+    const int32_t *rcount;
+};
+
 template <int XT, bool VEC>
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restrict__ x, int64_t m, int64_t k,
                                                             int64_t ldx, uint8_t *__restrict__ xq,
                                                             uint16_t *__restrict__ xh, uint16_t *__restrict__ xl,
-                                                            int64_t pitch) {
+                                                            int64_t pitch, RowMap map) {
     // launched as a programmatic dependent: let the next kernel start its own
     // independent prefetch, and wait for the previous kernel before touching
     // memory it may still read or write
@@ -88,12 +96,17 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restri
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t blk = g >> 2;
     const int j = (int)(g & 3);
-    const bool active = blk < total;
+    bool active = blk < total;
     const int64_t row = active ? blk / nb : 0;
     const int64_t b = active ? blk - row * nb : 0;
+    int64_t src = row;
+    if (map.rmap != nullptr) {   // uniform over the 4 threads of a block
+        active = active && row < *map.rcount;
+        src = active ? map.rmap[row] / map.rdiv : 0;
+    }
 
     float v[8];
-    if (active) load8<XT, VEC>(x, row * ldx + b * QK8 + 8 * j, v);
+    if (active) load8<XT, VEC>(x, src * ldx + b * QK8 + 8 * j, v);
     else {
 #pragma unroll
         for (int i = 0; i < 8; i++) v[i] = 0.0f;
@@ -138,13 +151,19 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restri
 
 __global__ void __launch_bounds__(256) q8_1_to_f16_kernel(const uint8_t *__restrict__ xq, int64_t m, int64_t k,
                                                           uint16_t *__restrict__ xh, uint16_t *__restrict__ xl,
-                                                          int64_t pitch) {
+                                                          int64_t pitch, RowMap map) {
     const int64_t nb = k / QK8;
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t blk = g >> 2;
     const int j = (int)(g & 3);
     if (blk >= m * nb) return;
-    const uint8_t *p = xq + blk * Q8_1_BYTES;
+    int64_t src_blk = blk;
+    if (map.rmap != nullptr) {
+        const int64_t r = blk / nb;
+        if (r >= *map.rcount) return;
+        src_blk = (int64_t)(map.rmap[r] / map.rdiv) * nb + (blk - r * nb);
+    }
+    const uint8_t *p = xq + src_blk * Q8_1_BYTES;
     const float d16 = h2f(ld_u16(p));
     const uint32_t w0 = ld_u32(p + 4 + 8 * j), w1 = ld_u32(p + 8 + 8 * j);
     int q[8];
@@ -160,7 +179,8 @@ __global__ void __launch_bounds__(256) q8_1_to_f16_kernel(const uint8_t *__restr
 }
 
 cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int64_t ldx, uint8_t *xq,
-                                 uint16_t *xh, uint16_t *xl, cudaStream_t s, int64_t pitch) {
+                                 uint16_t *xh, uint16_t *xl, cudaStream_t s, int64_t pitch, const int32_t *rmap,
+                                 int32_t rdiv, const int32_t *rcount) {
     if (pitch < k) pitch = k;
     const int64_t threads = m * (k / QK8) * 4;
     if (threads == 0) return cudaSuccess;
@@ -176,7 +196,8 @@ cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, in
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-#define QLAUNCH(XT, V) (void)cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<XT, V>, x, m, k, ldx, xq, xh, xl, pitch)
+    const RowMap map{rmap, rdiv < 1 ? 1 : rdiv, rcount};
+#define QLAUNCH(XT, V) (void)cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<XT, V>, x, m, k, ldx, xq, xh, xl, pitch, map)
     if (xt == GGUF_F32) { if (vec) QLAUNCH(GGUF_F32, true); else QLAUNCH(GGUF_F32, false); }
     else if (xt == GGUF_BF16) { if (vec) QLAUNCH(GGUF_BF16, true); else QLAUNCH(GGUF_BF16, false); }
     else { if (vec) QLAUNCH(GGUF_F16, true); else QLAUNCH(GGUF_F16, false); }
@@ -185,11 +206,12 @@ cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, in
 }
 
 cudaError_t launch_q8_1_to_f16(const uint8_t *xq, int64_t m, int64_t k, uint16_t *xh, uint16_t *xl, cudaStream_t s,
-                               int64_t pitch) {
+                               int64_t pitch, const int32_t *rmap, int32_t rdiv, const int32_t *rcount) {
     if (pitch < k) pitch = k;
     const int64_t threads = m * (k / QK8) * 4;
     if (threads == 0) return cudaSuccess;
-    q8_1_to_f16_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(xq, m, k, xh, xl, pitch);
+    q8_1_to_f16_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(xq, m, k, xh, xl, pitch,
+                                                                        RowMap{rmap, rdiv < 1 ? 1 : rdiv, rcount});
     return cudaGetLastError();
 }
 

@@ -5,8 +5,13 @@
 // Operands (all fp16, K-major, 128-byte swizzled rows of 64 values):
 //   A = weight rows, unpacked in registers from the packed GGUF blocks
 //       (unpack.cuh) by 8 producer warps; per K-step a thread takes one part
-//       (half or quarter) of one or two rows, consecutive lanes sharing a
-//       row, so that each warp-wide load reads 16 (8) rows of contiguous bytes;
+//       (half or quarter) of one or two rows.  Where the weight rows can be
+//       described to TMA (row bytes a multiple of 16, or a few rows together),
+//       the packed bytes of 128 rows x one 256-value chunk (or whole short
+//       rows) are staged in a ring of shared-memory buffers by bulk tensor
+//       copies and the producers unpack from there; otherwise they load the
+//       packed bytes from global memory themselves, consecutive lanes sharing
+//       a row so that each warp-wide load reads 16 (8) rows of contiguous bytes;
 //   B = activation rows (the fp16 form d16 * q of q8_1 values), loaded by TMA:
 //       tiles (dense) or tile::gather4 of the routed rows (MoE; 4 rows per copy).
 // Precision modes:
@@ -17,12 +22,13 @@
 //           and three MMAs per K step, A_hi B_hi + A_hi B_lo + A_lo B_hi: the
 //           result matches the exact blockwise value to about 1e-6.  Used for
 //           fp32 outputs and for the MoE intermediate, which is re-quantized.
-// Roles (448 threads):
+// Roles (480 threads):
 //   warp 0      B producer (dense: one elected lane; MoE: lane i gathers rows 4i .. 4i+3)
 //   warp 1      TMEM allocator + the MMA-issuing thread (two accumulators)
 //   warps 2-9   A producers
 //   warps 10-13 epilogue (TMEM lane quadrant = warp % 4), overlapping the next
 //               tile's mainloop
+//   warp 14     packed-weight loader (one elected lane issues the bulk copies)
 // Every wait is bounded (1 s); a timeout sets the error word and the CTA exits.
 #pragma once
 
@@ -38,7 +44,22 @@ namespace gg {
 constexpr int TG_BM = 128;
 constexpr int TG_BK = 64;
 constexpr int TG_PRODUCERS = 256;
-constexpr int TG_THREADS = 64 + TG_PRODUCERS + 128;
+constexpr int TG_GROUPS = 2;   // producer groups, each building every TG_GROUPS-th K-step
+constexpr int TG_THREADS = 64 + TG_PRODUCERS + 128 + 32;
+constexpr int TG_LOADER_WARP = 14;
+constexpr int TG_MAX_PSTAGES = 8;
+constexpr int TG_SMEM_MAX = 232448;   // dynamic shared memory a CTA may opt in to
+
+// Packed bytes of one 256-value chunk of a weight row, and the width of the
+// 16-byte-aligned window that always covers one (a chunk that starts inside a
+// 16-byte word needs up to 16 - gcd(bytes, 16) more).
+__host__ __device__ constexpr int tg_chunk_bytes(int wt) {
+    return wt == GGUF_Q4_K ? 144 : wt == GGUF_Q5_K ? 176 : wt == GGUF_Q6_K ? 210 : wt == GGUF_Q8_0 ? 272
+         : wt == GGUF_Q4_0 ? 144 : wt == GGUF_MXFP4 ? 136 : 0;
+}
+__host__ __device__ constexpr int tg_chunk_pitch(int wt) {
+    return wt == GGUF_Q6_K ? 224 : wt == GGUF_MXFP4 ? 144 : tg_chunk_bytes(wt);
+}
 constexpr int TG_A_BYTES = TG_BM * TG_BK * 2;  // one fp16 operand tile, 16 KB
 
 enum { TG_DENSE = 0, TG_MOE_GATE_UP = 1, TG_MOE_DOWN = 2 };
@@ -59,7 +80,6 @@ struct TgParams {
     // gathered activation rows (MoE)
     const uint16_t *xh, *xl;
     int64_t top_k;
-    int x_by_token;   // MoE down mode: route r reads operand row r / top_k (its token's) instead of row r
     const int32_t *route_list, *offsets, *counts, *tile_expert, *tile_start, *n_tiles;
     const float *route_w;
     int tiles_x;
@@ -67,19 +87,34 @@ struct TgParams {
     uint8_t *hq;
     uint16_t *hbf, *h16, *h16lo;
     int64_t hpitch;  // row length of h16 / h16lo: I, plus correction columns when the down weights are Q4_K / Q5_K
+    int h16_grouped;  // h16 / h16lo rows in grouped route order (the fused down GEMM's operand); 0: route order
+    // staged packed weights (pstages == 0: the producers load from global memory)
+    int pstages;         // buffers in the ring
+    int pkc;             // K-steps per staged chunk (4: one 256-value chunk; or every weight K-step of a row)
+    int pchunked;        // 1: chunks of 256 values in an aligned window; 0: whole rows
+    int pgroup;          // rows per line of the tensor map (whole rows whose byte length is not a multiple of 16)
+    int64_t ppitch;      // bytes between rows in a buffer
+    int64_t pstage_bytes;
+    int64_t pb256;       // packed bytes per 256 values
 };
 
-template <int BN, bool PRECISE, int MODE>
+template <int WT, int BN, bool PRECISE, int MODE>
 struct TgShape {
     static constexpr int OPS = PRECISE ? 2 : 1;
     static constexpr int A_STAGE = OPS * TG_A_BYTES;
     static constexpr int B_STAGE = OPS * BN * TG_BK * 2;
     // gate_up exchange: gate and up values of 64 rows x 32 routes, fp32
     static constexpr int XBUF = MODE == TG_MOE_GATE_UP ? 2 * 64 * 32 * 4 : 0;
-    static constexpr int FIXED = 1024 + XBUF + 512 + BN * 8;
-    static constexpr int STAGES_RAW = (220 * 1024 - FIXED) / (A_STAGE + B_STAGE);
+    static constexpr int BAR_BYTES = 1024;
+    static constexpr int FIXED = 1024 + XBUF + BAR_BYTES + BN * 8;
+    // room kept for two buffers of staged packed weights: 128 rows x one chunk
+    // window, or (MoE down, fast mode) whole rows of up to 432 bytes
+    static constexpr int PCHUNK = (TG_BM * tg_chunk_pitch(WT) + 1023) / 1024 * 1024;
+    static constexpr int PRES = (MODE == TG_MOE_DOWN && !PRECISE && 2 * PCHUNK < 110592) ? 110592 : 2 * PCHUNK;
+    static constexpr int STAGES_RAW = (TG_SMEM_MAX - FIXED - PRES) / (A_STAGE + B_STAGE);
     static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
-    static constexpr int SMEM = FIXED + STAGES * (A_STAGE + B_STAGE);
+    static_assert(STAGES >= 2, "at least two operand stages");
+    static constexpr int BASE = FIXED + STAGES * (A_STAGE + B_STAGE);   // bytes before the packed ring
     static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
 };
 
@@ -125,20 +160,24 @@ __device__ __forceinline__ TgTile tg_tile(const TgParams &p, int t, int KS) {
 
 template <int WT, int BN, bool PRECISE, int MODE, int OT>
 __global__ void __launch_bounds__(TG_THREADS, 1)
-    tg_kernel(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo, const TgParams p,
-              int *err) {
-    using S = TgShape<BN, PRECISE, MODE>;
+    tg_kernel(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo,
+              const __grid_constant__ CUtensorMap map_w, const TgParams p, int *err) {
+    using S = TgShape<WT, BN, PRECISE, MODE>;
     constexpr int ST = S::STAGES;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived from smem_raw by pointer arithmetic so
+    // that loads through it compile to shared-memory loads
+    uint8_t *smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = smem;                             // [ST][OPS][16 KB]
     uint8_t *sB = smem + ST * S::A_STAGE;           // [ST][OPS][BN * 128]
-    float *xbuf = reinterpret_cast<float *>(sB + ST * S::B_STAGE);
+    uint8_t *sP = sB + ST * S::B_STAGE;             // [pstages][pstage_bytes] packed weights
+    float *xbuf = reinterpret_cast<float *>(sP + (int64_t)p.pstages * p.pstage_bytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xbuf) + S::XBUF);
     uint64_t *full_a = bars, *full_b = bars + ST, *empty = bars + 2 * ST;
     uint64_t *tfull = bars + 3 * ST, *tempty = bars + 3 * ST + 2;
     uint64_t *drain = bars + 3 * ST + 4;  // completion of every MMA this CTA issued
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * ST + 5);
+    uint64_t *pfull = bars + 3 * ST + 5, *pempty = pfull + TG_MAX_PSTAGES;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(pempty + TG_MAX_PSTAGES);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -149,7 +188,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
 
     if (tid == 0) {
         for (int s = 0; s < ST; s++) {
-            tc::mbar_init(&full_a[s], TG_PRODUCERS);
+            tc::mbar_init(&full_a[s], TG_PRODUCERS / TG_GROUPS);
             tc::mbar_init(&full_b[s], 1);
             tc::mbar_init(&empty[s], 1);
         }
@@ -158,10 +197,15 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             tc::mbar_init(&tempty[b], 128);
         }
         tc::mbar_init(drain, 1);
+        for (int s = 0; s < p.pstages; s++) {
+            tc::mbar_init(&pfull[s], 1);
+            tc::mbar_init(&pempty[s], TG_PRODUCERS / 32);
+        }
         *abort_flag = 0;
         tc::fence_barrier_init();
         tc::prefetch_tmap(&map_hi);
         if (PRECISE) tc::prefetch_tmap(&map_lo);
+        if (p.pstages > 0) tc::prefetch_tmap(&map_w);
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, S::TMEM_COLS);
@@ -200,44 +244,30 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                         tc::mbar_wait(&full_b[i % ST], (uint32_t)(i / ST) & 1u);
             }
         } else {
-            // gather: lane i loads rows 4i .. 4i+3 of the tile with one
-            // tile::gather4 per operand; slots past the routes read row
-            // `rows` of the operand, out of range, i.e. zeros
-            static_assert(BN == 128, "the MoE gather assigns 4 rows to each of 32 lanes");
-            const bool by_token = MODE == TG_MOE_GATE_UP || p.x_by_token;
-            const int32_t oob = (int32_t)(by_token ? p.m : p.top_k * p.m);
-            int it = 0, last = 0;
-            for (int t = blockIdx.x; t < tiles_total && !*abort_flag; t += gridDim.x) {
-                const TgTile d = tg_tile<MODE, BN>(p, t, KS);
-                int32_t rows[4];
-#pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    const int j = 4 * lane + i;
-                    const int r = j < d.n_eff ? p.route_list[d.route0 + j] : -1;
-                    rows[i] = r < 0 ? oob : (int32_t)(by_token ? r / p.top_k : r);
-                }
-                for (int ks = 0; ks < KS; ks++, it++) {
-                    const int s = it % ST;
-                    const uint32_t ph = (uint32_t)(it / ST) & 1u;
-                    if (*abort_flag) break;
-                    bool ok = true;
-                    if (lane == 0) {
-                        ok = tc::mbar_wait(&empty[s], ph ^ 1u);
-                        if (ok) tc::mbar_arrive_expect_tx(&full_b[s], (uint32_t)S::B_STAGE);
+            // MoE: the operand rows are in grouped (expert-sorted) route order, so
+            // a tile's routes are consecutive rows from route0; rows past the
+            // expert's routes belong to the next expert and only fill MMA columns
+            // the epilogue ignores (rows past the operand read as zeros)
+            if (lane == 0) {
+                int it = 0, last = 0;
+                for (int t = blockIdx.x; t < tiles_total && !*abort_flag; t += gridDim.x) {
+                    const TgTile d = tg_tile<MODE, BN>(p, t, KS);
+                    for (int ks = 0; ks < KS; ks++, it++) {
+                        const int s = it % ST;
+                        const uint32_t ph = (uint32_t)(it / ST) & 1u;
+                        if (*abort_flag) break;
+                        if (!tc::mbar_wait(&empty[s], ph ^ 1u)) { fail(1); break; }
+                        tc::mbar_arrive_expect_tx(&full_b[s], (uint32_t)S::B_STAGE);
+                        uint8_t *dst = sB + s * S::B_STAGE;
+                        tc::tma_load_2d(dst, &map_hi, &full_b[s], ks * TG_BK, d.route0);
+                        if (PRECISE) tc::tma_load_2d(dst + BN * TG_BK * 2, &map_lo, &full_b[s], ks * TG_BK, d.route0);
+                        last = it + 1;
                     }
-                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                    if (!ok) { if (lane == 0) fail(1); break; }
-                    uint8_t *dst = sB + s * S::B_STAGE + lane * 4 * 128;
-                    tc::tma_gather4(dst, &map_hi, &full_b[s], ks * TG_BK, rows[0], rows[1], rows[2], rows[3]);
-                    if (PRECISE)
-                        tc::tma_gather4(dst + BN * TG_BK * 2, &map_lo, &full_b[s], ks * TG_BK, rows[0], rows[1], rows[2],
-                                        rows[3]);
-                    last = it + 1;
                 }
+                if (*abort_flag)  // copies already issued land before the CTA exits
+                    for (int i = last - ST < 0 ? 0 : last - ST; i < last; i++)
+                        tc::mbar_wait(&full_b[i % ST], (uint32_t)(i / ST) & 1u);
             }
-            if (*abort_flag && lane == 0)  // copies already issued land before the CTA exits
-                for (int i = last - ST < 0 ? 0 : last - ST; i < last; i++)
-                    tc::mbar_wait(&full_b[i % ST], (uint32_t)(i / ST) & 1u);
         }
     } else if (warp == 1) {
         // ================= MMA issuer
@@ -281,25 +311,87 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             if (!tc::mbar_wait(drain, 0)) fail(2);
         }
     } else if (warp < 2 + TG_PRODUCERS / 32) {
-        // ================= A producers: thread p takes part p % PARTS of tile
-        // rows p / PARTS + RP * i (RP = 256 / PARTS rows per pass); one
-        // warp-wide load covers 32 / PARTS rows of contiguous bytes
+        // ================= A producers.  The 8 warps form TG_GROUPS groups;
+        // group g builds the A tiles of the K-steps whose running index is g
+        // modulo TG_GROUPS, so that several K-steps are unpacked at once.  In a
+        // group, thread p takes part p % PARTS of tile rows p / PARTS + RP * i
+        // (RP = threads per group / PARTS rows per pass).
         using U = KQ<WT>;
-        constexpr int PARTS = U::PARTS, RP = TG_PRODUCERS / PARTS, TPT = TG_BM / RP;
+        constexpr int GW = (TG_PRODUCERS / 32) / TG_GROUPS;   // warps per group
+        constexpr int PARTS = U::PARTS, RP = 32 * GW / PARTS, TPT = TG_BM / RP;
         constexpr int VW = 8 * U::CHUNKS;  // fp32 values per task
-        // K-steps loaded ahead: 4 for the MoE GEMMs (latency-bound gathers of
-        // expert rows); 2 for the dense MMQ, where deeper unrolling cost more
-        // in instruction-cache misses than it hid
-        constexpr int DEPTH = MODE == TG_DENSE ? 2 : 4;
+        // own K-steps loaded ahead from global memory (unstaged rows): the next
+        // one, TG_GROUPS K-steps later in the stream
+        constexpr int DEPTH = 1;
         // lane -> (row, part): each group of 8 lanes takes one part of 8
         // different rows, so a 16-byte swizzled store is conflict-free within
         // every 8-lane phase, and the parts of a row are in the same warp so a
         // warp-wide load still reads whole 32-byte sectors
-        const int pw = warp - 2, pl = lane;
+        const int grp = (warp - 2) / GW, pw = (warp - 2) % GW, pl = lane;
         const int part = (pl >> 3) % PARTS;
         const int r0 = (32 / PARTS) * pw + (pl & 7) + 8 * (pl / (8 * PARTS));
         const int64_t kblocks = p.k / 32;
-        int it = 0;
+        // one task: unpack (weight steps) or the Q4_K / Q5_K min-term correction
+        // values dmin * m_j of 8 sub-blocks per chunk (steps past the weights)
+        auto task = [&](const U &u, bool live_i, const uint8_t *wrow_i, int ks, uint32_t (&hi)[VW / 2],
+                        uint32_t (&lo)[VW / 2]) {
+#pragma unroll
+            for (int w = 0; w < VW / 2; w++) { hi[w] = 0u; lo[w] = 0u; }
+            if (!live_i) return;
+            if (ks < KS_W) {
+                if (H2) {
+                    u.unpack_h2(ks, hi);
+                } else {
+                    float v[VW];
+                    u.unpack_f32(ks, v);
+                    if (PRECISE) pack_split<VW>(v, hi, lo);
+                    else pack_single<VW>(v, hi);
+                }
+            } else if (WT == GGUF_Q4_K || WT == GGUF_Q5_K) {
+                // chunk c of this step holds the corrections of super-block
+                // (ks * 64 - k) / 64 + c of the row
+                const int64_t nsb = p.k / 256;
+                const int64_t sb0 = ((int64_t)ks * TG_BK - p.k) / 8;
+                float v[VW];
+#pragma unroll
+                for (int e = 0; e < U::CHUNKS; e++) {
+                    const int64_t sb = sb0 + U::chunk(part, e);
+                    uint4 hdr = make_uint4(0, 0, 0, 0);
+                    if (sb < nsb) hdr = *reinterpret_cast<const uint4 *>(wrow_i + sb * block_bytes(WT));
+                    const uint32_t sc[3] = {hdr.y, hdr.z, hdr.w};
+                    const float dmin = h2f(hdr.x >> 16);
+#pragma unroll
+                    for (int jj = 0; jj < 8; jj++) {
+                        int sv, mv;
+                        q4k_scale_min(sc, jj, sv, mv);
+                        v[8 * e + jj] = sb < nsb ? __fmul_rn(dmin, (float)mv) : 0.0f;
+                    }
+                }
+                pack_single<VW>(v, hi);
+            }
+        };
+        // K-step ks (running index itk): wait for its stage, then unpack and
+        // store one task at a time (few live registers), signal the MMA
+        auto produce = [&](const U (&uu)[TPT], const bool (&live)[TPT], const uint8_t *const (&wrow)[TPT], int ks,
+                           int itk) -> bool {
+            const int s = itk % ST;
+            const uint32_t ph = (uint32_t)(itk / ST) & 1u;
+            if (*abort_flag) return false;
+            if (!tc::mbar_wait(&empty[s], ph ^ 1u)) { fail(4); return false; }
+            uint8_t *tile = sA + s * S::A_STAGE;
+#pragma unroll
+            for (int i = 0; i < TPT; i++) {
+                uint32_t hi[VW / 2], lo[VW / 2];
+                task(uu[i], live[i], wrow[i], ks, hi, lo);
+                store_sw128_task<U>(tile, r0 + RP * i, part, hi);
+                if (PRECISE) store_sw128_task<U>(tile + TG_A_BYTES, r0 + RP * i, part, lo);
+            }
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(&full_a[s]);
+            return true;
+        };
+        int it0 = 0;   // running index of the tile's first K-step
+        int pc = 0;    // staged chunks consumed
         for (int t = blockIdx.x; t < tiles_total && !*abort_flag; t += gridDim.x) {
             const TgTile d = tg_tile<MODE, BN>(p, t, KS);
             bool live[TPT];
@@ -320,85 +412,64 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                 wrow[i] = wbase + (live[i] ? row : 0) * p.rb;
             }
             const int kw1 = d.k1 < KS_W ? d.k1 : KS_W;  // weight K steps of this tile
-            U u[DEPTH][TPT];                             // tasks of steps ks .. ks + DEPTH - 1
-            auto load_step = [&](U (&uu)[TPT], int ks) {
-                if (ks >= kw1) return;
-#pragma unroll
-                for (int i = 0; i < TPT; i++)
-                    if (live[i]) uu[i].load(wrow[i], ks, part, kblocks);
-            };
-#pragma unroll
-            for (int dd = 0; dd < DEPTH; dd++) load_step(u[dd], d.k0 + dd);
-            // one task: unpack (weight steps) or the Q4_K / Q5_K min-term correction
-            // values dmin * m_j of 8 sub-blocks per chunk (steps past the weights)
-            auto task = [&](const U &u, int i, int ks, uint32_t (&hi)[VW / 2], uint32_t (&lo)[VW / 2]) {
-#pragma unroll
-                for (int w = 0; w < VW / 2; w++) { hi[w] = 0u; lo[w] = 0u; }
-                if (!live[i]) return;
-                if (ks < KS_W) {
-                    if (H2) {
-                        u.unpack_h2(ks, hi);
-                    } else {
-                        float v[VW];
-                        u.unpack_f32(ks, v);
-                        if (PRECISE) pack_split<VW>(v, hi, lo);
-                        else pack_single<VW>(v, hi);
-                    }
-                } else if (WT == GGUF_Q4_K || WT == GGUF_Q5_K) {
-                    // chunk c of this step holds the corrections of super-block
-                    // (ks * 64 - k) / 64 + c of the row
-                    const int64_t nsb = p.k / 256;
-                    const int64_t sb0 = ((int64_t)ks * TG_BK - p.k) / 8;
-                    float v[VW];
-#pragma unroll
-                    for (int e = 0; e < U::CHUNKS; e++) {
-                        const int64_t sb = sb0 + U::chunk(part, e);
-                        uint4 hdr = make_uint4(0, 0, 0, 0);
-                        if (sb < nsb) hdr = *reinterpret_cast<const uint4 *>(wrow[i] + sb * block_bytes(WT));
-                        const uint32_t sc[3] = {hdr.y, hdr.z, hdr.w};
-                        const float dmin = h2f(hdr.x >> 16);
-#pragma unroll
-                        for (int jj = 0; jj < 8; jj++) {
-                            int sv, mv;
-                            q4k_scale_min(sc, jj, sv, mv);
-                            v[8 * e + jj] = sb < nsb ? __fmul_rn(dmin, (float)mv) : 0.0f;
-                        }
-                    }
-                    pack_single<VW>(v, hi);
-                }
-            };
-            auto produce = [&](const U (&uu)[TPT], int ks) -> bool {
-                const int s = it % ST;
-                const uint32_t ph = (uint32_t)(it / ST) & 1u;
-                it++;
-                uint32_t hi[TPT][VW / 2], lo[TPT][VW / 2];
-#pragma unroll
-                for (int i = 0; i < TPT; i++) task(uu[i], i, ks, hi[i], lo[i]);
-                if (*abort_flag) return false;
-                if (!tc::mbar_wait(&empty[s], ph ^ 1u)) { fail(4); return false; }
-                uint8_t *tile = sA + s * S::A_STAGE;
-#pragma unroll
-                for (int i = 0; i < TPT; i++) {
-                    store_sw128_task<U>(tile, r0 + RP * i, part, hi[i]);
-                    if (PRECISE) store_sw128_task<U>(tile + TG_A_BYTES, r0 + RP * i, part, lo[i]);
-                }
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(&full_a[s]);
-                return true;
-            };
+            // this group's first K-step of the tile
+            const int kfirst = d.k0 + ((grp - it0) % TG_GROUPS + TG_GROUPS) % TG_GROUPS;
             bool ok = true;
-            for (int ks = d.k0; ks < d.k1 && ok; ks += DEPTH) {
+            if (p.pstages > 0) {
+                // staged: chunk c of the tile's weight steps waits in buffer pc % pstages
+                const int PS = p.pstages;
+                int ks = kfirst;
+                for (int c = d.k0 / p.pkc; c * p.pkc < kw1 && ok; c++, pc++) {
+                    const int ps = pc % PS;
+                    const int c1 = (c + 1) * p.pkc < kw1 ? (c + 1) * p.pkc : kw1;
+                    if (!tc::mbar_wait(&pfull[ps], (uint32_t)(pc / PS) & 1u)) { fail(4); ok = false; break; }
+                    // row i of the buffer, offset so that the type's block
+                    // arithmetic on a K-step of the row lands in the buffer
+                    const int64_t x0 = p.pchunked ? (int64_t)c * p.pb256 / 16 * 16 : 0;
+                    const uint8_t *buf = sP + (int64_t)ps * p.pstage_bytes;
+                    const uint8_t *vrow[TPT];
 #pragma unroll
-                for (int dd = 0; dd < DEPTH; dd++) {
-                    if (ok && ks + dd < d.k1) {
-                        ok = produce(u[dd], ks + dd);
-                        load_step(u[dd], ks + dd + DEPTH);  // DEPTH K-steps ahead
+                    for (int i = 0; i < TPT; i++) vrow[i] = buf + (int64_t)(r0 + RP * i) * p.ppitch - x0;
+                    for (; ks < c1 && ok; ks += TG_GROUPS) {
+                        U u[TPT];
+#pragma unroll
+                        for (int i = 0; i < TPT; i++)
+                            if (live[i]) u[i].load(vrow[i], ks, part, kblocks);
+                        ok = produce(u, live, wrow, ks, it0 + ks - d.k0);
+                    }
+                    __syncwarp();   // every lane's reads of the buffer are done
+                    if (lane == 0) tc::mbar_arrive(&pempty[ps]);
+                }
+                // steps past the weights (correction columns)
+                for (; ks < d.k1 && ok; ks += TG_GROUPS) {
+                    U u[TPT];
+                    ok = produce(u, live, wrow, ks, it0 + ks - d.k0);
+                }
+            } else {
+                U u[DEPTH][TPT];   // tasks of this group's next DEPTH K-steps
+                auto load_step = [&](U (&uu)[TPT], int ks) {
+                    if (ks >= kw1) return;
+#pragma unroll
+                    for (int i = 0; i < TPT; i++)
+                        if (live[i]) uu[i].load(wrow[i], ks, part, kblocks);
+                };
+#pragma unroll
+                for (int dd = 0; dd < DEPTH; dd++) load_step(u[dd], kfirst + TG_GROUPS * dd);
+                for (int ks = kfirst; ks < d.k1 && ok; ks += TG_GROUPS * DEPTH) {
+#pragma unroll
+                    for (int dd = 0; dd < DEPTH; dd++) {
+                        const int kk = ks + TG_GROUPS * dd;
+                        if (ok && kk < d.k1) {
+                            ok = produce(u[dd], live, wrow, kk, it0 + kk - d.k0);
+                            load_step(u[dd], kk + TG_GROUPS * DEPTH);   // DEPTH own K-steps ahead
+                        }
                     }
                 }
             }
             if (!ok) break;
+            it0 += d.k1 - d.k0;
         }
-    } else {
+    } else if (warp < TG_LOADER_WARP) {
         // ================= epilogue
         const int q = warp & 3;
         int i = 0;
@@ -498,23 +569,25 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                                     }
                                 }
                                 if (p.h16) {
+                                    // the fused down GEMM's operand: rows in grouped order
+                                    const int64_t hr = p.h16_grouped ? (int64_t)d.route0 + j : rt;
                                     const float v = h2f(dh) * (float)qv;
                                     const uint16_t vh = f2h_rn(v);
-                                    p.h16[rt * p.hpitch + icol] = vh;
-                                    if (p.h16lo) p.h16lo[rt * p.hpitch + icol] = f2h_rn(v - h2f(vh));
+                                    p.h16[hr * p.hpitch + icol] = vh;
+                                    if (p.h16lo) p.h16lo[hr * p.hpitch + icol] = f2h_rn(v - h2f(vh));
                                     if (p.hpitch > idim) {
                                         // min-term correction column of this q8_1 block (Q4_K / Q5_K down
                                         // weights), and the zero padding of the row (written once,
                                         // by the first column tile)
                                         if (lane == 0) {
                                             const uint16_t sh = f2h_rn(__fmul_rn(dq, (float)sum));
-                                            p.h16[rt * p.hpitch + idim + icol / 32] = f2h_rn(h2f(dh) * (float)sum - h2f(sh));
-                                            if (p.h16lo) p.h16lo[rt * p.hpitch + idim + icol / 32] = 0;
+                                            p.h16[hr * p.hpitch + idim + icol / 32] = f2h_rn(h2f(dh) * (float)sum - h2f(sh));
+                                            if (p.h16lo) p.h16lo[hr * p.hpitch + idim + icol / 32] = 0;
                                         }
                                         if (d.row0 == 0 && hb == 0)
                                             for (int64_t c2 = idim + idim / 32 + lane; c2 < p.hpitch; c2 += 32) {
-                                                p.h16[rt * p.hpitch + c2] = 0;
-                                                if (p.h16lo) p.h16lo[rt * p.hpitch + c2] = 0;
+                                                p.h16[hr * p.hpitch + c2] = 0;
+                                                if (p.h16lo) p.h16lo[hr * p.hpitch + c2] = 0;
                                             }
                                     }
                                 }
@@ -528,6 +601,39 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             tc::mbar_arrive(&tempty[b]);
             if (!ok) break;
         }
+    } else if (lane == 0 && p.pstages > 0) {
+        // ================= packed-weight loader: chunk c of a tile (K-steps
+        // [c * pkc, (c + 1) * pkc) of its weight steps) into buffer pc % pstages:
+        // the 16-byte-aligned window of the chunk's bytes of 128 rows (64 gate
+        // + 64 up rows for gate_up), or whole rows
+        const int PS = p.pstages;
+        int pc = 0, last = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < tiles_total && ok && !*abort_flag; t += gridDim.x) {
+            const TgTile d = tg_tile<MODE, BN>(p, t, KS);
+            const int kw1 = d.k1 < KS_W ? d.k1 : KS_W;
+            const int32_t z = MODE == TG_DENSE ? 0 : d.e;
+            for (int c = d.k0 / p.pkc; c * p.pkc < kw1; c++, pc++) {
+                const int ps = pc % PS;
+                if (*abort_flag) { ok = false; break; }
+                if (!tc::mbar_wait(&pempty[ps], ((uint32_t)(pc / PS) & 1u) ^ 1u)) { fail(32); ok = false; break; }
+                tc::mbar_arrive_expect_tx(&pfull[ps], (uint32_t)(TG_BM * p.ppitch));
+                uint8_t *dst = sP + (int64_t)ps * p.pstage_bytes;
+                // x in 8-byte elements of the tensor map
+                const int32_t x = p.pchunked ? (int32_t)((int64_t)c * p.pb256 / 16 * 2) : 0;
+                if (MODE == TG_MOE_GATE_UP) {
+                    tc::tma_load_3d(dst, &map_w, &pfull[ps], x, (int32_t)(d.row0 / p.pgroup), z);
+                    tc::tma_load_3d(dst + 64 * p.ppitch, &map_w, &pfull[ps], x,
+                                    (int32_t)((p.n / 2 + d.row0) / p.pgroup), z);
+                } else {
+                    tc::tma_load_3d(dst, &map_w, &pfull[ps], x, (int32_t)(d.row0 / p.pgroup), z);
+                }
+                last = pc + 1;
+            }
+        }
+        if (*abort_flag)  // copies already issued land before the CTA exits
+            for (int i = last - PS < 0 ? 0 : last - PS; i < last; i++)
+                tc::mbar_wait(&pfull[i % PS], (uint32_t)(i / PS) & 1u);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -554,23 +660,84 @@ inline cudaError_t tg_make_map(CUtensorMap *map, const uint16_t *base, int64_t r
 
 int *tg_error_word();
 
+// Staging of the packed weight rows (sets the p.p* fields and the tensor map;
+// p.pstages = 0 when the rows cannot be staged, and the producers then load
+// from global memory).  The weights are E matrices of `rows` rows of k values,
+// expert_stride bytes apart (E = 1: one matrix); a buffer holds 128 rows,
+// taken as boxes of box_rows rows.  base_bytes: shared memory the kernel uses
+// before the ring.
+//   chunked : row bytes a multiple of 16 and k a multiple of 256; a buffer is
+//             the 16-byte-aligned window over one 256-value chunk of the rows;
+//   rows    : otherwise, whole rows, taken g at a time so that a line of the
+//             tensor map is a multiple of 16 bytes (g * row bytes <= 2048).
+inline void tg_plan_staging(TgParams &p, CUtensorMap *map, int wt, const uint8_t *w, int64_t rows, int64_t E,
+                            int64_t expert_stride, int64_t k, int box_rows, int base_bytes) {
+    p.pstages = 0;
+    p.pkc = 1;
+    p.pgroup = 1;
+    auto enc = tensor_map_encoder();
+    const int64_t rb = k / block_elems(wt) * block_bytes(wt);
+    const int ksw = (int)((k + TG_BK - 1) / TG_BK);
+    if (!enc || rb <= 0 || (reinterpret_cast<uintptr_t>(w) & 15) || (E > 1 && expert_stride % 16)) return;
+    int g = 1, chunked = 0;
+    int64_t pitch = 0;
+    if (rb % 16 == 0 && k % 256 == 0 && tg_chunk_pitch(wt) > 0) {
+        chunked = 1;
+        pitch = tg_chunk_pitch(wt);
+    } else {
+        while ((g * rb) % 16) g *= 2;
+        if (g > 16 || rows % g || box_rows % g || g * rb > 2048) return;
+        pitch = rb;
+    }
+    // a box that fills part of a buffer (gate_up: 64 gate rows, then 64 up rows)
+    // must leave the next box 128-byte aligned
+    if (box_rows < TG_BM && (box_rows * pitch) % 128) return;
+    const int64_t stage = (TG_BM * pitch + 1023) / 1024 * 1024;
+    int64_t ps = (TG_SMEM_MAX - base_bytes) / stage;
+    if (ps > TG_MAX_PSTAGES) ps = TG_MAX_PSTAGES;
+    if (ps < 2) return;
+    const int64_t line = chunked ? rb : g * rb;   // bytes of one line of the map
+    cuuint64_t gdim[3] = {(cuuint64_t)(line / 8), (cuuint64_t)(rows / g), (cuuint64_t)E};
+    cuuint64_t gstride[2] = {(cuuint64_t)line, (cuuint64_t)(E > 1 ? expert_stride : rows * rb)};
+    cuuint32_t box[3] = {(cuuint32_t)((chunked ? pitch : line) / 8), (cuuint32_t)(box_rows / g), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint8_t *>(w), gdim, gstride, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return;
+    p.pstages = (int)ps;
+    p.pkc = chunked ? 4 : ksw;
+    p.pchunked = chunked;
+    p.pgroup = g;
+    p.ppitch = pitch;
+    p.pstage_bytes = stage;
+    p.pb256 = tg_chunk_bytes(wt);
+}
+
 template <int WT, int BN, bool PRECISE, int MODE, int OT>
-inline cudaError_t tg_launch(const CUtensorMap &mh, const CUtensorMap &ml, const TgParams &p, int grid,
-                             cudaStream_t s) {
-    using S = TgShape<BN, PRECISE, MODE>;
+inline cudaError_t tg_launch(const CUtensorMap &mh, const CUtensorMap &ml, const CUtensorMap &mw, const TgParams &p,
+                             int grid, cudaStream_t s) {
+    using S = TgShape<WT, BN, PRECISE, MODE>;
     auto kern = tg_kernel<WT, BN, PRECISE, MODE, OT>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TG_SMEM_MAX);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     int *err = tg_error_word();
     if (!err) return cudaErrorInvalidSymbol;
-    kern<<<grid, TG_THREADS, S::SMEM, s>>>(mh, ml, p, err);
+    const int64_t smem = S::BASE + (int64_t)p.pstages * p.pstage_bytes;
+    if (smem > TG_SMEM_MAX) return cudaErrorInvalidValue;
+    kern<<<grid, TG_THREADS, (size_t)smem, s>>>(mh, ml, mw, p, err);
     return cudaGetLastError();
+}
+
+template <int WT, int BN, bool PRECISE, int MODE>
+constexpr int tg_base_bytes() {
+    return TgShape<WT, BN, PRECISE, MODE>::BASE;
 }
 
 }  // namespace gg

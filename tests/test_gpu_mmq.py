@@ -134,3 +134,33 @@ def test_device_error_word_is_clear_after_mmq(g):
     flag = torch.full((1,), -1, dtype=torch.int32, device=DEV)
     g.gguf_device_errors_async(flag, clear=True)
     assert int(flag.item()) == 0
+
+
+@pytest.fixture
+def stage_option(g):
+    saved = g.gguf_get_option("mmq_stage")
+    yield
+    g.gguf_set_option("mmq_stage", saved)
+
+
+# shapes whose packed rows the GEMM stages in shared memory by bulk tensor
+# copies: 256-value chunks (row bytes a multiple of 16) or whole short rows
+@pytest.mark.parametrize("wt,n,k", [(oracle.Q4_K, 300, 1024), (oracle.Q5_K, 257, 2048), (oracle.Q6_K, 300, 2048),
+                                    (oracle.Q6_K, 200, 512), (oracle.Q8_0, 333, 1024), (oracle.Q4_0, 129, 1024),
+                                    (oracle.MXFP4, 300, 1024)])
+@pytest.mark.parametrize("m,dtype", [(12, torch.bfloat16), (100, torch.bfloat16), (300, torch.bfloat16),
+                                     (40, torch.float32), (200, torch.float32)])
+def test_mmq_staged_weights_against_oracle(g, stage_option, wt, n, k, m, dtype):
+    w = _weights(wt, n, k, seed=m + n, safe=(m % 2 == 0))
+    x = synth.activations(m, k, seed=m + 7, dtype=dtype)
+    ref = oracle.mul_mat(wt, w, k, oracle.quantize_q8_1(x.float().numpy()))
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    ys = []
+    for stage in (1, 0):
+        g.gguf_set_option("mmq_stage", stage)
+        y = g.gguf_mul_mat(_u8(w), wt, n, k, x.to(DEV)).float().cpu().numpy()
+        assert_close(y, ref, tol, f"mmq staged={stage} type {wt} n {n} k {k} m {m}")
+        ys.append(y)
+    # both ways feed the MMA the same operand values; only the order of the
+    # fp32 accumulation may differ between the split-K partial sums
+    assert_close(ys[0], ys[1], 1e-5 if dtype == torch.float32 else TOL_BF16, "staged vs global loads")

@@ -466,3 +466,36 @@ def test_device_error_word_is_clear_after_moe(g, path):
     sgu = bank_gu.nbytes // E
     g.gguf_mul_mat_id(_u8(bank_gu), g.Q4_K, E, sgu, 2 * I, H, x.to(DEV), _u8(ids), g.GATE_UP_SWIGLU)
     assert g.gguf_device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("H,I,down", [(256, 256, oracle.Q6_K), (2048, 512, oracle.Q6_K), (512, 256, oracle.Q4_K)])
+def test_moe_staged_weights(g, H, I, down):
+    """The grouped GEMMs with packed weight rows staged by bulk tensor copies
+    (option mmq_stage, the default) and loaded by the producer warps: both
+    against the oracle chain, and against each other."""
+    E, K, T = 7, 4, 300
+    bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 900, True)
+    bank_d = _bank(down, E, H, I, 901, True)
+    sgu, sd = bank_gu.nbytes // E, bank_d.nbytes // E
+    ids, rw = synth.routes(T, E, K, seed=31)
+    ids[0] = [2, 2, 5, 5]
+    ids[1, 1] = -1
+    x = synth.activations(T, H, seed=32, dtype=torch.bfloat16)
+    xq = oracle.quantize_q8_1(x.float().numpy())
+    _, hq = oracle.moe_gate_up(oracle.Q4_K, bank_gu, E, sgu, 2 * I, H, xq, ids, nthreads=8)
+    ref = oracle.moe_down(down, bank_d, E, sd, H, I, hq, ids, rw, nthreads=8)
+    saved = (g.gguf_get_option("mmq_stage"), g.gguf_get_option("moe_vec_max_tokens"))
+    g.gguf_set_option("moe_vec_max_tokens", 0)
+    ys = []
+    try:
+        for stage in (1, 0):
+            g.gguf_set_option("mmq_stage", stage)
+            y = g.gguf_moe_ffn(_u8(bank_gu), g.Q4_K, sgu, _u8(bank_d), down, sd, E, H, I, x.to(DEV), _u8(ids),
+                               _u8(rw)).float().cpu().numpy()
+            assert_close_moe_e2e(y, ref, f"moe staged={stage} H {H} I {I}")
+            ys.append(y)
+    finally:
+        g.gguf_set_option("mmq_stage", saved[0])
+        g.gguf_set_option("moe_vec_max_tokens", saved[1])
+    # the same operand values either way, and a fixed order of the sums
+    np.testing.assert_array_equal(ys[0], ys[1])
