@@ -107,7 +107,12 @@ static int64_t g_mmvq_tc_min_m = 5;
 constexpr int64_t MOE_VEC_CAP = 256;
 static int64_t g_moe_vec_max_tokens = 256;
 static int64_t g_mmq_stage = 1;
+static int64_t g_moe_deterministic = 1;
+static int64_t g_mmq_bn_max = 256;
+int64_t option_mmq_bn_max() { return g_mmq_bn_max; }
+static int64_t g_moe_down_precise = 1;
 int64_t option_mmq_stage() { return g_mmq_stage; }
+int64_t option_moe_deterministic() { return g_moe_deterministic; }
 int64_t option_mmvq_tc() { return g_mmvq_tc; }
 int64_t option_mmvq_tc_min_m() { return g_mmvq_tc_min_m; }
 int64_t option_mmvq_tc_max_m() { return g_mmvq_tc_max_m; }
@@ -341,7 +346,29 @@ static MoeWs moe_call_layout(const gguf_moe_args *a, void *base) {
     // the grouped GEMMs' fp16 operand holds one row per route, in grouped order
     if (a->mode == GGUF_MOE_GATE_UP_SWIGLU)
         return moe_ws_layout(base, a->n_experts, R, R * kx, 0, 0, false, a->n_tokens <= MOE_VEC_CAP ? a->n : 0);
-    return moe_ws_layout(base, a->n_experts, R, R * kx, R * a->n, 0, false);
+    return moe_ws_layout(base, a->n_experts, R, R * kx, R * ((a->n + 127) / 128 * 128), 0, false);
+}
+
+// The grouped down GEMM with the expert-weighted sum: fp32 atomics into the
+// zeroed token rows (the first T * n floats of the z buffer) and one
+// conversion to the output dtype; or, with option moe_deterministic, the
+// per-route rows z and the slot-order sum.
+static cudaError_t grouped_down_sum(const uint8_t *wd, int wt, int64_t stride, int64_t n, int64_t k,
+                                    const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t T, int64_t E,
+                                    const MoeWs &w, const int32_t *ids, const float *route_w, void *y, int yt,
+                                    bool precise, cudaStream_t s) {
+    const int64_t R = T * top_k;
+    cudaError_t e;
+    if (g_moe_deterministic) {
+        if ((e = launch_moe_down(wd, wt, stride, n, k, xh, xl, top_k, R, E, w, w.z, precise, s)) != cudaSuccess)
+            return e;
+        return launch_moe_finalize(w.z, w.pos, ids, w.offsets, route_w, T, top_k, n, y, yt, s);
+    }
+    if ((e = cudaMemsetAsync(w.z, 0, sizeof(float) * (size_t)(T * n), s)) != cudaSuccess) return e;
+    if ((e = launch_moe_down(wd, wt, stride, n, k, xh, xl, top_k, R, E, w, w.z, precise, s, w.z, route_w)) !=
+        cudaSuccess)
+        return e;
+    return launch_convert_rows(w.z, T, n, y, yt, n, s);
 }
 
 // the route-batched MMVQ path: few tokens, and weight rows it takes
@@ -421,12 +448,14 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
         if (plain) {
             if ((e = launch_mmvq_routes(a->wt, (const uint8_t *)a->w, rt, a->n, a->k, xq, R, w.z, s)) != cudaSuccess)
                 return cuda_status(e, "mul_mat_id");
-            return cuda_status(launch_moe_plain_store(w.z, w.pos, R, a->n, a->y, a->yt, s), "mul_mat_id store");
+            return cuda_status(launch_moe_plain_store(w.z, w.pos, nullptr, nullptr, R, a->n, a->y, a->yt, s),
+                               "mul_mat_id store");
         }
         if (!gu) {
             if ((e = launch_mmvq_routes(a->wt, (const uint8_t *)a->w, rt, a->n, a->k, xq, R, w.z, s)) != cudaSuccess)
                 return cuda_status(e, "mul_mat_id down");
-            return cuda_status(launch_moe_finalize(w.z, w.pos, a->route_w, a->n_tokens, a->top_k, a->n, a->y, a->yt, s),
+            return cuda_status(launch_moe_finalize(w.z, w.pos, nullptr, nullptr, a->route_w, a->n_tokens, a->top_k, a->n,
+                                                   a->y, a->yt, s),
                                "mul_mat_id finalize");
         }
         const int64_t idim = a->n / 2;
@@ -463,23 +492,24 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
         if ((e = launch_moe_down((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, w.xl, a->top_k, R,
                                  a->n_experts, w, w.z, a->yt == GGUF_F32, s)) != cudaSuccess)
             return cuda_status(e, "mul_mat_id");
-        return cuda_status(launch_moe_plain_store(w.z, w.pos, R, a->n, a->y, a->yt, s), "mul_mat_id store");
+        return cuda_status(launch_moe_plain_store(w.z, w.pos, a->ids, w.offsets, R, a->n, a->y, a->yt, s),
+                           "mul_mat_id store");
     }
     if ((e = moe_group(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id grouping");
     if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), w, a->n_experts, 1, s)) !=
         cudaSuccess)
         return cuda_status(e, "mul_mat_id quantize");
-    if ((e = launch_moe_down((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, w.xl, a->top_k, R,
-                             a->n_experts, w, w.z, a->yt == GGUF_F32, s)) != cudaSuccess)
-        return cuda_status(e, "mul_mat_id down");
-    return cuda_status(launch_moe_finalize(w.z, w.pos, a->route_w, a->n_tokens, a->top_k, a->n, a->y, a->yt, s),
-                       "mul_mat_id finalize");
+    return cuda_status(grouped_down_sum((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, w.xl,
+                                        a->top_k, a->n_tokens, a->n_experts, w, a->ids, a->route_w, a->y, a->yt,
+                                        a->yt == GGUF_F32, s),
+                       "mul_mat_id down");
 }
 
 static MoeWs ffn_layout(const gguf_moe_ffn_args *a, void *base) {
     const int64_t R = a->n_tokens * a->top_k;
     return moe_ws_layout(base, a->n_experts, R, R * op_pitch(a->gate_up_type, a->hidden),
-                         R * a->hidden, R * op_pitch(a->down_type, a->inter), a->yt == GGUF_F32,
+                         R * ((a->hidden + 127) / 128 * 128), R * op_pitch(a->down_type, a->inter),
+                         a->yt == GGUF_F32 || g_moe_down_precise,
                          a->n_tokens <= MOE_VEC_CAP ? 2 * a->inter : 0);
 }
 
@@ -533,7 +563,8 @@ gguf_status gguf_moe_ffn(const gguf_moe_ffn_args *a, void *ws, size_t ws_bytes, 
                                     MmvqRoutes{a->ids, w.pos, a->down_stride, a->top_k, 1}, a->hidden, a->inter, hq, R,
                                     w.z, s)) != cudaSuccess)
             return cuda_status(e, "moe_ffn down");
-        return cuda_status(launch_moe_finalize(w.z, w.pos, a->route_w, a->n_tokens, a->top_k, a->hidden, a->y, a->yt, s),
+        return cuda_status(launch_moe_finalize(w.z, w.pos, nullptr, nullptr, a->route_w, a->n_tokens, a->top_k,
+                                               a->hidden, a->y, a->yt, s),
                            "moe_ffn finalize");
     }
     // one grouping serves both GEMMs; a route of weight 0 contributes nothing and is skipped by both
@@ -545,11 +576,10 @@ gguf_status gguf_moe_ffn(const gguf_moe_ffn_args *a, void *ws, size_t ws_bytes, 
                                 a->hidden, w.xh, w.xl, a->top_k, R, a->n_experts, w, nullptr, nullptr, w.h16, w.h16lo,
                                 op_pitch(a->down_type, a->inter), true, s)) != cudaSuccess)
         return cuda_status(e, "moe_ffn gate_up");
-    if ((e = launch_moe_down((const uint8_t *)a->w_down, a->down_type, a->down_stride, a->hidden, a->inter, w.h16,
-                             w.h16lo, a->top_k, R, a->n_experts, w, w.z, a->yt == GGUF_F32, s)) != cudaSuccess)
-        return cuda_status(e, "moe_ffn down");
-    return cuda_status(launch_moe_finalize(w.z, w.pos, a->route_w, a->n_tokens, a->top_k, a->hidden, a->y, a->yt, s),
-                       "moe_ffn finalize");
+    return cuda_status(grouped_down_sum((const uint8_t *)a->w_down, a->down_type, a->down_stride, a->hidden, a->inter,
+                                        w.h16, w.h16lo, a->top_k, a->n_tokens, a->n_experts, w, a->ids, a->route_w,
+                                        a->y, a->yt, a->yt == GGUF_F32 || g_moe_down_precise, s),
+                       "moe_ffn down");
 }
 
 gguf_status gguf_debug_block_dots(const void *w, int wt, int64_t n, int64_t k, const void *xq, int64_t m,
@@ -597,6 +627,19 @@ gguf_status gguf_set_option(const char *key, int64_t value) {
         g_mmq_stage = value != 0;
         return GGUF_OK;
     }
+    if (!strcmp(key, "moe_deterministic")) {
+        g_moe_deterministic = value != 0;
+        return GGUF_OK;
+    }
+    if (!strcmp(key, "mmq_bn_max")) {
+        if (value != 128 && value != 256) return fail(GGUF_ERR_INVALID_ARG, "set_option: mmq_bn_max must be 128 or 256");
+        g_mmq_bn_max = value;
+        return GGUF_OK;
+    }
+    if (!strcmp(key, "moe_down_precise")) {
+        g_moe_down_precise = value != 0;
+        return GGUF_OK;
+    }
     return fail(GGUF_ERR_INVALID_ARG, "set_option: unknown key '%s'", key);
 }
 
@@ -609,6 +652,9 @@ int64_t gguf_get_option(const char *key) {
     if (!strcmp(key, "moe_vec_max_tokens")) return g_moe_vec_max_tokens;
     if (!strcmp(key, "mmvq_tc_max_m")) return g_mmvq_tc_max_m;
     if (!strcmp(key, "mmq_stage")) return g_mmq_stage;
+    if (!strcmp(key, "moe_deterministic")) return g_moe_deterministic;
+    if (!strcmp(key, "moe_down_precise")) return g_moe_down_precise;
+    if (!strcmp(key, "mmq_bn_max")) return g_mmq_bn_max;
     return -1;
 }
 

@@ -60,6 +60,9 @@ int64_t option_mmvq_tc_max_m();
 // option "mmq_stage" (default 1): the tensor-core GEMM stages packed weight
 // rows in shared memory with bulk tensor copies where their layout allows
 int64_t option_mmq_stage();
+// option "mmq_bn_max" (128 or 256, default 256): widest activation tile of the
+// dense MMQ; tiles of at most 128 rows keep the weight operand in TMEM
+int64_t option_mmq_bn_max();
 // whether m (> 8) tokens of K-long Q4_K rows take the tensor-core MMVQ
 bool mmvq_tc_wide(int wt, int64_t k, int64_t m);
 
@@ -137,11 +140,21 @@ cudaError_t launch_moe_gate_up(const uint8_t *w, int wt, int64_t expert_stride, 
                                int64_t hpitch, bool h16_grouped, cudaStream_t s);
 cudaError_t launch_moe_down(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
                             const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
-                            const MoeWs &ws, float *z, bool precise, cudaStream_t s);
+                            const MoeWs &ws, float *z, bool precise, cudaStream_t s, float *ysum = nullptr,
+                            const float *route_w = nullptr);
+// option "moe_deterministic" (default 1): 1 keeps the grouped down GEMM's
+// per-route rows and sums each token's routes in slot order afterwards (the
+// same bits on every run); 0 adds the weighted rows into the token rows with
+// fp32 atomics in the GEMM's epilogue
+int64_t option_moe_deterministic();
 // y[R][n] (out dtype) from the per-route rows z, zero rows for skipped routes (pos < 0)
-cudaError_t launch_moe_plain_store(const float *z, const int32_t *pos, int64_t R, int64_t n, void *y, int yt,
-                                   cudaStream_t s);
-cudaError_t launch_moe_finalize(const float *z, const int32_t *pos, const float *route_w, int64_t T, int64_t top_k,
-                                int64_t n, void *y, int yt, cudaStream_t s);
+cudaError_t launch_moe_plain_store(const float *z, const int32_t *pos, const int32_t *ids, const int32_t *offsets,
+                                   int64_t R, int64_t n, void *y, int yt, cudaStream_t s);
+// y[T][n] = sum over each token's active routes of route_w * z row (in slot
+// order); z rows in route order (offsets == nullptr) or in grouped order, route
+// r at offsets[ids[r]] + pos[r]
+cudaError_t launch_moe_finalize(const float *z, const int32_t *pos, const int32_t *ids, const int32_t *offsets,
+                                const float *route_w, int64_t T, int64_t top_k, int64_t n, void *y, int yt,
+                                cudaStream_t s);
 
 }  // namespace gg

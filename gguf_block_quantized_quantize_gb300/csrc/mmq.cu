@@ -122,7 +122,7 @@ static cudaError_t launch_mmq_bn(const uint8_t *w, int64_t n, int64_t k, const u
     if (m <= 16) return launch_dense<WT, 16, false, OT>(w, n, k, xh, xl, m, y, ldy, yacc, s);
     if (m <= 32) return launch_dense<WT, 32, false, OT>(w, n, k, xh, xl, m, y, ldy, yacc, s);
     if (m <= 64) return launch_dense<WT, 64, false, OT>(w, n, k, xh, xl, m, y, ldy, yacc, s);
-    if (m <= 128) return launch_dense<WT, 128, false, OT>(w, n, k, xh, xl, m, y, ldy, yacc, s);
+    if (m <= 128 || option_mmq_bn_max() <= 128) return launch_dense<WT, 128, false, OT>(w, n, k, xh, xl, m, y, ldy, yacc, s);
     return launch_dense<WT, 256, false, OT>(w, n, k, xh, xl, m, y, ldy, yacc, s);
     }
 }

@@ -128,11 +128,15 @@ __global__ void moe_scatter_kernel(const int32_t *__restrict__ ids, const int32_
     if (p >= 0) route_list[offsets[ids[r]] + p] = (int32_t)r;
 }
 
-// y[t][c] = sum over the token's route slots k (in order) of w_k * z[t*top_k + k][c];
-// routes that were not grouped (inactive id, or weight 0) have pos = -1 and no z row
-// V consecutive columns per thread (V = 4 when n % 4 == 0: 16-byte loads)
+// y[t][c] = sum over the token's route slots k (in order) of w_k * z(t*top_k + k, c);
+// routes that were not grouped (inactive id, or weight 0) have pos = -1 and no z row.
+// z is [R][n] in route order, or, with offsets, the grouped GEMM's layout:
+// route r at its grouped position g = offsets[ids[r]] + pos[r], column c at
+// ((c / 128) * R + g) * 128 + c % 128.  V consecutive columns per thread
+// (V = 4 when n % 4 == 0: 16-byte loads)
 template <int V>
 __global__ void moe_finalize_kernel(const float *__restrict__ z, const int32_t *__restrict__ pos,
+                                    const int32_t *__restrict__ ids, const int32_t *__restrict__ offsets,
                                     const float *__restrict__ route_w, int64_t T, int64_t top_k, int64_t n,
                                     void *__restrict__ y, int yt) {
     asm volatile("griddepcontrol.wait;" ::: "memory");   // z comes from the previous kernel
@@ -145,17 +149,25 @@ __global__ void moe_finalize_kernel(const float *__restrict__ z, const int32_t *
     for (int v = 0; v < V; v++) acc[v] = 0.0f;
     for (int64_t k = 0; k < top_k; k++) {
         const int64_t r = t * top_k + k;
-        if (pos[r] < 0) continue;
+        const int32_t pr = pos[r];
+        if (pr < 0) continue;
         const float w = route_w ? route_w[r] : 1.0f;
+        // grouped rows are stored in 128-column blocks of R rows
+        const int64_t zi = offsets ? ((((c >> 7) * T * top_k) + offsets[ids[r]] + pr) << 7) + (c & 127) : r * n + c;
         if (V == 4) {
-            const float4 zv = *reinterpret_cast<const float4 *>(z + r * n + c);
+            const float4 zv = *reinterpret_cast<const float4 *>(z + zi);
             acc[0] = fmaf(w, zv.x, acc[0]);
             acc[1] = fmaf(w, zv.y, acc[1]);
             acc[2] = fmaf(w, zv.z, acc[2]);
             acc[3] = fmaf(w, zv.w, acc[3]);
         } else {
 #pragma unroll
-            for (int v = 0; v < V; v++) acc[v] = fmaf(w, z[r * n + c + v], acc[v]);
+            for (int v = 0; v < V; v++) {
+                const int64_t cv = c + v;
+                const int64_t zv = offsets ? ((((cv >> 7) * T * top_k) + offsets[ids[r]] + pr) << 7) + (cv & 127)
+                                           : r * n + cv;
+                acc[v] = fmaf(w, z[zv], acc[v]);
+            }
         }
     }
 #pragma unroll
@@ -318,45 +330,59 @@ cudaError_t launch_moe_gate_up(const uint8_t *w, int wt, int64_t expert_stride, 
     return launch_moe_mode<TG_MOE_GATE_UP, true>(wt, p, R, E, s);
 }
 
-// down: z[R][n] = W[e] . x[route] for every grouped route; xh / xl: the
-// operand rows in grouped route order [R][kx] (xl only in the precise mode)
+// down: z[R][n] = W[e] . x[route] for every grouped route, or, with ysum,
+// ysum[t][n] += route_w[r] * (W[e] . x[route]) (fp32 atomics into zeroed token
+// rows); xh / xl: the operand rows in grouped route order [R][kx] (xl only in
+// the precise mode)
 cudaError_t launch_moe_down(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
                             const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
-                            const MoeWs &ws, float *z, bool precise, cudaStream_t s) {
+                            const MoeWs &ws, float *z, bool precise, cudaStream_t s, float *ysum,
+                            const float *route_w) {
     if (R == 0) return cudaSuccess;
     TgParams p = moe_params(w, wt, expert_stride, n, k, xh, xl, top_k, ws);
     p.tiles_x = (int)((n + TG_BM - 1) / TG_BM);
     p.yacc = z;
+    p.zrows = R;
+    p.ysum = ysum;
+    p.route_w = route_w;
     p.m = R / top_k;
     return precise ? launch_moe_mode<TG_MOE_DOWN, true>(wt, p, R, E, s)
                    : launch_moe_mode<TG_MOE_DOWN, false>(wt, p, R, E, s);
 }
 
-// y[r][c] = z[r][c] for an active route, 0 for a skipped one (out dtype)
-__global__ void moe_plain_store_kernel(const float *__restrict__ z, const int32_t *__restrict__ pos, int64_t R,
-                                       int64_t n, void *__restrict__ y, int yt) {
+// y[r][c] = z(r, c) for an active route, 0 for a skipped one (out dtype); the
+// layouts of z as in the finalize
+__global__ void moe_plain_store_kernel(const float *__restrict__ z, const int32_t *__restrict__ pos,
+                                       const int32_t *__restrict__ ids, const int32_t *__restrict__ offsets,
+                                       int64_t R, int64_t n, void *__restrict__ y, int yt) {
     asm volatile("griddepcontrol.wait;" ::: "memory");   // z comes from the previous kernel
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= R * n) return;
-    store_out(y, yt, i, pos[i / n] >= 0 ? z[i] : 0.0f);
+    const int64_t r = i / n, c = i - r * n;
+    const int32_t pr = pos[r];
+    const int64_t zi = offsets ? ((((c >> 7) * R) + (pr >= 0 ? offsets[ids[r]] + pr : 0)) << 7) + (c & 127) : i;
+    store_out(y, yt, i, pr >= 0 ? z[zi] : 0.0f);
 }
 
-cudaError_t launch_moe_plain_store(const float *z, const int32_t *pos, int64_t R, int64_t n, void *y, int yt,
-                                   cudaStream_t s) {
+cudaError_t launch_moe_plain_store(const float *z, const int32_t *pos, const int32_t *ids, const int32_t *offsets,
+                                   int64_t R, int64_t n, void *y, int yt, cudaStream_t s) {
     const int64_t count = R * n;
     if (count == 0) return cudaSuccess;
-    return launch_pdl(moe_plain_store_kernel, (count + 255) / 256, 256, s, z, pos, R, n, y, yt);
+    return launch_pdl(moe_plain_store_kernel, (count + 255) / 256, 256, s, z, pos, ids, offsets, R, n, y, yt);
 }
 
 // y[T][n] = the route-weighted sum of each token's z rows (out dtype)
-cudaError_t launch_moe_finalize(const float *z, const int32_t *pos, const float *route_w, int64_t T, int64_t top_k,
-                                int64_t n, void *y, int yt, cudaStream_t s) {
+cudaError_t launch_moe_finalize(const float *z, const int32_t *pos, const int32_t *ids, const int32_t *offsets,
+                                const float *route_w, int64_t T, int64_t top_k, int64_t n, void *y, int yt,
+                                cudaStream_t s) {
     const int64_t count = T * n;
     if (count == 0) return cudaSuccess;
     if (n % 4 == 0)   // z rows are 16-byte aligned (workspace base 256-aligned, n % 4 == 0)
-        return launch_pdl(moe_finalize_kernel<4>, (count / 4 + 255) / 256, 256, s, z, pos, route_w, T, top_k, n, y, yt);
-    return launch_pdl(moe_finalize_kernel<1>, (count + 255) / 256, 256, s, z, pos, route_w, T, top_k, n, y, yt);
+        return launch_pdl(moe_finalize_kernel<4>, (count / 4 + 255) / 256, 256, s, z, pos, ids, offsets, route_w, T,
+                          top_k, n, y, yt);
+    return launch_pdl(moe_finalize_kernel<1>, (count + 255) / 256, 256, s, z, pos, ids, offsets, route_w, T, top_k, n,
+                      y, yt);
 }
 
 cudaError_t launch_moe_swiglu(const float *z, const int32_t *pos, int64_t R, int64_t I, uint16_t *h, cudaStream_t s) {

@@ -76,7 +76,10 @@ struct TgParams {
     void *y;
     int yt;
     int64_t ldy;
-    float *yacc;  // split-K partial sums [m][n] (dense) or the per-route outputs [R][n] (MoE down)
+    float *yacc;  // split-K partial sums [m][n] (dense), or the MoE down per-route outputs in grouped
+                  // order, as ceil(n / 128) blocks [zrows][128]
+    float *ysum;  // MoE down with the fused weighted sum: fp32 token rows [T][n], zeroed before the call
+    int64_t zrows;  // MoE down: rows (routes) of one 128-column block of yacc
     // gathered activation rows (MoE)
     const uint16_t *xh, *xl;
     int64_t top_k;
@@ -101,21 +104,30 @@ struct TgParams {
 template <int WT, int BN, bool PRECISE, int MODE>
 struct TgShape {
     static constexpr int OPS = PRECISE ? 2 : 1;
-    static constexpr int A_STAGE = OPS * TG_A_BYTES;
+    // tiles of at most 128 activation rows keep the unpacked weight operand in
+    // tensor memory (beside the two accumulators); wider tiles in shared memory
+    static constexpr bool ATM = BN <= 128;
+    static constexpr int A_COL0 = 2 * BN;   // first TMEM column of the A stages
+    static constexpr int A_STAGE = ATM ? 0 : OPS * TG_A_BYTES;
     static constexpr int B_STAGE = OPS * BN * TG_BK * 2;
-    // gate_up exchange: gate and up values of 64 rows x 32 routes, fp32
-    static constexpr int XBUF = MODE == TG_MOE_GATE_UP ? 2 * 64 * 32 * 4 : 0;
+    // gate_up exchange: gate and up values of 64 rows x 32 routes, fp32;
+    // down: two 32-route x 128-column fp32 buffers of the bulk output stores
+    static constexpr int XBUF = MODE == TG_MOE_GATE_UP ? 2 * 64 * 32 * 4 : MODE == TG_MOE_DOWN ? 2 * 32 * 128 * 4 : 0;
     static constexpr int BAR_BYTES = 1024;
     static constexpr int FIXED = 1024 + XBUF + BAR_BYTES + BN * 8;
     // room kept for two buffers of staged packed weights: 128 rows x one chunk
     // window, or (MoE down, fast mode) whole rows of up to 432 bytes
     static constexpr int PCHUNK = (TG_BM * tg_chunk_pitch(WT) + 1023) / 1024 * 1024;
-    static constexpr int PRES = (MODE == TG_MOE_DOWN && !PRECISE && 2 * PCHUNK < 110592) ? 110592 : 2 * PCHUNK;
+    static constexpr int PRES = (MODE == TG_MOE_DOWN && 2 * PCHUNK < 110592) ? 110592 : 2 * PCHUNK;
     static constexpr int STAGES_RAW = (TG_SMEM_MAX - FIXED - PRES) / (A_STAGE + B_STAGE);
-    static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
+    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;   // B stages (and A stages in shared memory)
     static_assert(STAGES >= 2, "at least two operand stages");
     static constexpr int BASE = FIXED + STAGES * (A_STAGE + B_STAGE);   // bytes before the packed ring
-    static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+    // A stages: in TMEM, OPS x 32 columns each (64 fp16 of K per row)
+    static constexpr int STA_RAW = ATM ? (512 - A_COL0) / (32 * OPS) : STAGES;
+    static constexpr int STA = STA_RAW > 8 ? 8 : STA_RAW;
+    static_assert(STA >= 2, "at least two A stages");
+    static constexpr int TMEM_COLS = ATM ? 512 : (2 * BN < 32 ? 32 : 2 * BN);
 };
 
 __device__ __forceinline__ void tg_named_bar(int id, int count) {
@@ -163,7 +175,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
     tg_kernel(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo,
               const __grid_constant__ CUtensorMap map_w, const TgParams p, int *err) {
     using S = TgShape<WT, BN, PRECISE, MODE>;
-    constexpr int ST = S::STAGES;
+    constexpr int ST = S::STAGES, STA = S::STA;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, derived from smem_raw by pointer arithmetic so
     // that loads through it compile to shared-memory loads
@@ -173,10 +185,11 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
     uint8_t *sP = sB + ST * S::B_STAGE;             // [pstages][pstage_bytes] packed weights
     float *xbuf = reinterpret_cast<float *>(sP + (int64_t)p.pstages * p.pstage_bytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xbuf) + S::XBUF);
-    uint64_t *full_a = bars, *full_b = bars + ST, *empty = bars + 2 * ST;
-    uint64_t *tfull = bars + 3 * ST, *tempty = bars + 3 * ST + 2;
-    uint64_t *drain = bars + 3 * ST + 4;  // completion of every MMA this CTA issued
-    uint64_t *pfull = bars + 3 * ST + 5, *pempty = pfull + TG_MAX_PSTAGES;
+    uint64_t *full_a = bars, *empty_a = bars + STA;            // A stages (TMEM or shared memory)
+    uint64_t *full_b = bars + 2 * STA, *empty_b = full_b + ST;  // B stages
+    uint64_t *tfull = empty_b + ST, *tempty = tfull + 2;
+    uint64_t *drain = tfull + 4;  // completion of every MMA this CTA issued
+    uint64_t *pfull = drain + 1, *pempty = pfull + TG_MAX_PSTAGES;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(pempty + TG_MAX_PSTAGES);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -187,10 +200,13 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
     constexpr bool H2 = !PRECISE && OT != GGUF_F32 && MODE == TG_DENSE;
 
     if (tid == 0) {
-        for (int s = 0; s < ST; s++) {
+        for (int s = 0; s < STA; s++) {
             tc::mbar_init(&full_a[s], TG_PRODUCERS / TG_GROUPS);
+            tc::mbar_init(&empty_a[s], 1);
+        }
+        for (int s = 0; s < ST; s++) {
             tc::mbar_init(&full_b[s], 1);
-            tc::mbar_init(&empty[s], 1);
+            tc::mbar_init(&empty_b[s], 1);
         }
         for (int b = 0; b < 2; b++) {
             tc::mbar_init(&tfull[b], 1);
@@ -231,7 +247,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                         const int s = it % ST;
                         const uint32_t ph = (uint32_t)(it / ST) & 1u;
                         if (*abort_flag) break;
-                        if (!tc::mbar_wait(&empty[s], ph ^ 1u)) { fail(1); break; }
+                        if (!tc::mbar_wait(&empty_b[s], ph ^ 1u)) { fail(1); break; }
                         tc::mbar_arrive_expect_tx(&full_b[s], (uint32_t)S::B_STAGE);
                         uint8_t *dst = sB + s * S::B_STAGE;
                         tc::tma_load_2d(dst, &map_hi, &full_b[s], ks * TG_BK, (int32_t)d.m0);
@@ -256,7 +272,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                         const int s = it % ST;
                         const uint32_t ph = (uint32_t)(it / ST) & 1u;
                         if (*abort_flag) break;
-                        if (!tc::mbar_wait(&empty[s], ph ^ 1u)) { fail(1); break; }
+                        if (!tc::mbar_wait(&empty_b[s], ph ^ 1u)) { fail(1); break; }
                         tc::mbar_arrive_expect_tx(&full_b[s], (uint32_t)S::B_STAGE);
                         uint8_t *dst = sB + s * S::B_STAGE;
                         tc::tma_load_2d(dst, &map_hi, &full_b[s], ks * TG_BK, d.route0);
@@ -283,25 +299,40 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                 const int n_mma = MODE == TG_DENSE ? BN : ((d.n_eff + 15) / 16) * 16;
                 const uint32_t idesc = tc::idesc_f16_f32(TG_BM, n_mma);
                 for (int ks = d.k0; ks < d.k1; ks++, it++) {
-                    const int s = it % ST;
-                    const uint32_t ph = (uint32_t)(it / ST) & 1u;
+                    const int s = it % ST, sa = it % STA;
+                    const uint32_t ph = (uint32_t)(it / ST) & 1u, pha = (uint32_t)(it / STA) & 1u;
                     if (*abort_flag) break;
-                    if (!tc::mbar_wait(&full_a[s], ph) || !tc::mbar_wait(&full_b[s], ph)) { fail(2); break; }
+                    if (!tc::mbar_wait(&full_a[sa], pha) || !tc::mbar_wait(&full_b[s], ph)) { fail(2); break; }
                     tc::tc_fence_after();
-                    const uint32_t a0 = tc::smem_u32(sA + s * S::A_STAGE);
                     const uint32_t b0 = tc::smem_u32(sB + s * S::B_STAGE);
+                    if constexpr (S::ATM) {
+                        // A hi (and lo) in TMEM columns of stage sa; 8 columns per K = 16
+                        const uint32_t a0 = tmem + (uint32_t)(S::A_COL0 + sa * 32 * S::OPS);
 #pragma unroll
-                    for (int kk = 0; kk < TG_BK / 16; kk++) {
-                        const uint32_t acc_in = (ks != d.k0 || kk != 0) ? 1u : 0u;
-                        tc::mma_f16(acc, tc::sw128_desc(a0 + 32 * kk), tc::sw128_desc(b0 + 32 * kk), idesc, acc_in);
-                        if (PRECISE) {
-                            tc::mma_f16(acc, tc::sw128_desc(a0 + 32 * kk),
-                                        tc::sw128_desc(b0 + BN * TG_BK * 2 + 32 * kk), idesc, 1u);
-                            tc::mma_f16(acc, tc::sw128_desc(a0 + TG_A_BYTES + 32 * kk), tc::sw128_desc(b0 + 32 * kk),
-                                        idesc, 1u);
+                        for (int kk = 0; kk < TG_BK / 16; kk++) {
+                            const uint32_t acc_in = (ks != d.k0 || kk != 0) ? 1u : 0u;
+                            tc::mma_f16_ts(acc, a0 + 8 * kk, tc::sw128_desc(b0 + 32 * kk), idesc, acc_in);
+                            if (PRECISE) {
+                                tc::mma_f16_ts(acc, a0 + 8 * kk, tc::sw128_desc(b0 + BN * TG_BK * 2 + 32 * kk), idesc, 1u);
+                                tc::mma_f16_ts(acc, a0 + 32 + 8 * kk, tc::sw128_desc(b0 + 32 * kk), idesc, 1u);
+                            }
+                        }
+                    } else {
+                        const uint32_t a0 = tc::smem_u32(sA + sa * S::A_STAGE);
+#pragma unroll
+                        for (int kk = 0; kk < TG_BK / 16; kk++) {
+                            const uint32_t acc_in = (ks != d.k0 || kk != 0) ? 1u : 0u;
+                            tc::mma_f16(acc, tc::sw128_desc(a0 + 32 * kk), tc::sw128_desc(b0 + 32 * kk), idesc, acc_in);
+                            if (PRECISE) {
+                                tc::mma_f16(acc, tc::sw128_desc(a0 + 32 * kk),
+                                            tc::sw128_desc(b0 + BN * TG_BK * 2 + 32 * kk), idesc, 1u);
+                                tc::mma_f16(acc, tc::sw128_desc(a0 + TG_A_BYTES + 32 * kk),
+                                            tc::sw128_desc(b0 + 32 * kk), idesc, 1u);
+                            }
                         }
                     }
-                    tc::mma_commit(&empty[s]);
+                    tc::mma_commit(&empty_a[sa]);
+                    tc::mma_commit(&empty_b[s]);
                 }
                 tc::mma_commit(&tfull[b]);
             }
@@ -311,6 +342,146 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             if (!tc::mbar_wait(drain, 0)) fail(2);
         }
     } else if (warp < 2 + TG_PRODUCERS / 32) {
+      if constexpr (S::ATM) {
+        // ================= A producers, operand in TMEM.  Warp w writes the
+        // TMEM lane quadrant w % 4: a thread owns tile row 32 * (w % 4) + lane
+        // and writes all 64 values of its row per K-step; the 4 warps of group
+        // (w - 2) / 4 take the K-steps whose running index is the group
+        // modulo TG_GROUPS.
+        using U = KQ<WT>;
+        constexpr int PARTS = U::PARTS, VW = 8 * U::CHUNKS;
+        const int grp = (warp - 2) >> 2;
+        const int r = 32 * (warp & 3) + lane;
+        const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
+        const int64_t kblocks = p.k / 32;
+        // part j of K-step ks of this row (zeros for a row past the matrix), or
+        // the Q4_K / Q5_K min-term correction values of the steps past the weights
+        auto part_values = [&](const U &u, bool live, const uint8_t *wrow, int ks, int j, uint32_t (&hi)[VW / 2],
+                               uint32_t (&lo)[VW / 2]) {
+#pragma unroll
+            for (int w = 0; w < VW / 2; w++) { hi[w] = 0u; lo[w] = 0u; }
+            if (!live) return;
+            if (ks < KS_W) {
+                if (H2) {
+                    u.unpack_h2(ks, hi);
+                } else {
+                    float v[VW];
+                    u.unpack_f32(ks, v);
+                    if (PRECISE) pack_split<VW>(v, hi, lo);
+                    else pack_single<VW>(v, hi);
+                }
+            } else if (WT == GGUF_Q4_K || WT == GGUF_Q5_K) {
+                const int64_t nsb = p.k / 256;
+                const int64_t sb0 = ((int64_t)ks * TG_BK - p.k) / 8;
+                float v[VW];
+#pragma unroll
+                for (int e = 0; e < U::CHUNKS; e++) {
+                    const int64_t sb = sb0 + U::chunk(j, e);
+                    uint4 hdr = make_uint4(0, 0, 0, 0);
+                    if (sb < nsb) hdr = *reinterpret_cast<const uint4 *>(wrow + sb * block_bytes(WT));
+                    const uint32_t sc[3] = {hdr.y, hdr.z, hdr.w};
+                    const float dmin = h2f(hdr.x >> 16);
+#pragma unroll
+                    for (int jj = 0; jj < 8; jj++) {
+                        int sv, mv;
+                        q4k_scale_min(sc, jj, sv, mv);
+                        v[8 * e + jj] = sb < nsb ? __fmul_rn(dmin, (float)mv) : 0.0f;
+                    }
+                }
+                pack_single<VW>(v, hi);
+            }
+        };
+        // K-step ks (running index itk) of this row into its TMEM A stage
+        auto produce_row = [&](const U (&uu)[PARTS], bool live, const uint8_t *wrow, int ks, int itk) -> bool {
+            const int sa = itk % STA;
+            const uint32_t pha = (uint32_t)(itk / STA) & 1u;
+            // warp-uniform outcome: the TMEM stores below are warp-collective
+            bool ok = !*abort_flag && tc::mbar_wait(&empty_a[sa], pha ^ 1u);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) { if (lane == 0) fail(4); return false; }
+            tc::tc_fence_after();
+            const uint32_t acol = tmem + tlane + (uint32_t)(S::A_COL0 + sa * 32 * S::OPS);
+#pragma unroll
+            for (int j = 0; j < PARTS; j++) {
+                uint32_t hi[VW / 2], lo[VW / 2];
+                part_values(uu[j], live, wrow, ks, j, hi, lo);
+#pragma unroll
+                for (int e = 0; e < U::CHUNKS; e++) {
+                    const uint32_t c = acol + 4 * U::chunk(j, e);
+                    tc::tmem_st_32x32b_x4(c, hi[4 * e], hi[4 * e + 1], hi[4 * e + 2], hi[4 * e + 3]);
+                    if (PRECISE) tc::tmem_st_32x32b_x4(c + 32, lo[4 * e], lo[4 * e + 1], lo[4 * e + 2], lo[4 * e + 3]);
+                }
+            }
+            tc::tmem_st_wait();
+            tc::tc_fence_before();
+            tc::mbar_arrive(&full_a[sa]);
+            return true;
+        };
+        int it0 = 0, pc = 0;
+        for (int t = blockIdx.x; t < tiles_total && !*abort_flag; t += gridDim.x) {
+            const TgTile d = tg_tile<MODE, BN>(p, t, KS);
+            // this thread's weight row (gate_up: rows 0..63 gate, 64..127 the matching up rows)
+            int64_t row;
+            bool live;
+            if (MODE == TG_MOE_GATE_UP) {
+                row = r < 64 ? d.row0 + r : p.n / 2 + d.row0 + (r - 64);
+                live = (r < 64 ? d.row0 + r : d.row0 + (r - 64)) < p.n / 2;
+            } else {
+                row = d.row0 + r;
+                live = row < p.n;
+            }
+            const uint8_t *wrow = p.w + (MODE == TG_DENSE ? 0 : (int64_t)d.e * p.expert_stride) + (live ? row : 0) * p.rb;
+            const int kw1 = d.k1 < KS_W ? d.k1 : KS_W;
+            const int kfirst = d.k0 + ((grp - it0) % TG_GROUPS + TG_GROUPS) % TG_GROUPS;
+            bool ok = true;
+            int ks = kfirst;
+            if (p.pstages > 0) {
+                const int PS = p.pstages;
+                for (int c = d.k0 / p.pkc; c * p.pkc < kw1 && ok; c++, pc++) {
+                    const int ps = pc % PS;
+                    const int c1 = (c + 1) * p.pkc < kw1 ? (c + 1) * p.pkc : kw1;
+                    ok = __all_sync(0xffffffffu, tc::mbar_wait(&pfull[ps], (uint32_t)(pc / PS) & 1u));
+                    if (!ok) { if (lane == 0) fail(4); break; }
+                    // the row in the buffer, offset so that the type's block
+                    // arithmetic on a K-step lands in the buffer
+                    const int64_t x0 = p.pchunked ? (int64_t)c * p.pb256 / 16 * 16 : 0;
+                    const uint8_t *vrow = sP + (int64_t)ps * p.pstage_bytes + (int64_t)r * p.ppitch - x0;
+                    for (; ks < c1 && ok; ks += TG_GROUPS) {
+                        U uu[PARTS];
+#pragma unroll
+                        for (int j = 0; j < PARTS; j++)
+                            if (live) uu[j].load(vrow, ks, j, kblocks);
+                        ok = produce_row(uu, live, wrow, ks, it0 + ks - d.k0);
+                    }
+                    __syncwarp();   // every lane's reads of the buffer are done
+                    if (lane == 0) tc::mbar_arrive(&pempty[ps]);
+                }
+            } else {
+                // the next own K-step's bytes are loaded while this one is unpacked
+                U un[PARTS];
+                auto load_row = [&](U (&uu)[PARTS], int kk) {
+                    if (kk >= kw1 || !live) return;
+#pragma unroll
+                    for (int j = 0; j < PARTS; j++) uu[j].load(wrow, kk, j, kblocks);
+                };
+                load_row(un, ks);
+                for (; ks < kw1 && ok; ks += TG_GROUPS) {
+                    U uu[PARTS];
+#pragma unroll
+                    for (int j = 0; j < PARTS; j++) uu[j] = un[j];
+                    load_row(un, ks + TG_GROUPS);
+                    ok = produce_row(uu, live, wrow, ks, it0 + ks - d.k0);
+                }
+            }
+            // steps past the weights (correction columns)
+            for (; ks < d.k1 && ok; ks += TG_GROUPS) {
+                U uu[PARTS];
+                ok = produce_row(uu, live, wrow, ks, it0 + ks - d.k0);
+            }
+            if (!ok) break;
+            it0 += d.k1 - d.k0;
+        }
+      } else {
         // ================= A producers.  The 8 warps form TG_GROUPS groups;
         // group g builds the A tiles of the K-steps whose running index is g
         // modulo TG_GROUPS, so that several K-steps are unpacked at once.  In a
@@ -374,10 +545,10 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
         // store one task at a time (few live registers), signal the MMA
         auto produce = [&](const U (&uu)[TPT], const bool (&live)[TPT], const uint8_t *const (&wrow)[TPT], int ks,
                            int itk) -> bool {
-            const int s = itk % ST;
-            const uint32_t ph = (uint32_t)(itk / ST) & 1u;
+            const int s = itk % STA;
+            const uint32_t ph = (uint32_t)(itk / STA) & 1u;
             if (*abort_flag) return false;
-            if (!tc::mbar_wait(&empty[s], ph ^ 1u)) { fail(4); return false; }
+            if (!tc::mbar_wait(&empty_a[s], ph ^ 1u)) { fail(4); return false; }
             uint8_t *tile = sA + s * S::A_STAGE;
 #pragma unroll
             for (int i = 0; i < TPT; i++) {
@@ -469,17 +640,32 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             if (!ok) break;
             it0 += d.k1 - d.k0;
         }
+      }
     } else if (warp < TG_LOADER_WARP) {
         // ================= epilogue
         const int q = warp & 3;
         int i = 0;
+        int ochunk = 0;   // MoE down: bulk output stores issued (staging buffer ochunk & 1)
         for (int t = blockIdx.x; t < tiles_total; t += gridDim.x, i++) {
             const TgTile d = tg_tile<MODE, BN>(p, t, KS);
             const int b = i & 1;
-            const bool ok = tc::mbar_wait(&tfull[b], (uint32_t)(i >> 1) & 1u);
-            if (!ok) fail(8);
+            // MoE: the tile's route ids (and route weights), lane l holding routes
+            // l, 32 + l, ...; loaded before the wait for the accumulator
+            int rtv[MODE == TG_DENSE ? 1 : BN / 32];
+            float wv[MODE == TG_DENSE ? 1 : BN / 32];
+            if (MODE != TG_DENSE) {
+#pragma unroll
+                for (int c = 0; c < BN / 32; c++) {
+                    const bool in = 32 * c + lane < d.n_eff;
+                    rtv[c] = in ? p.route_list[d.route0 + 32 * c + lane] : 0;
+                    wv[c] = (MODE == TG_MOE_DOWN && p.ysum && p.route_w && in) ? p.route_w[rtv[c]] : 1.0f;
+                }
+            }
+            // warp-uniform outcome: the TMEM loads below are warp-collective
+            const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&tfull[b], (uint32_t)(i >> 1) & 1u));
+            if (!ok && lane == 0) fail(8);
             tc::tc_fence_after();
-            const bool go = ok && !*abort_flag;
+            const bool go = __all_sync(0xffffffffu, ok && !*abort_flag);
             if (MODE == TG_DENSE) {
                 const int64_t orow = d.row0 + 32 * q + lane;
 #pragma unroll 1
@@ -500,21 +686,54 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                 }
             } else if (MODE == TG_MOE_DOWN) {
                 const int64_t orow = d.row0 + 32 * q + lane;
-#pragma unroll 1
-                for (int c = 0; c * 32 < d.n_eff && go; c++) {
-                    uint32_t rr[32];
-                    // the chunk's 32 route ids, one per lane, loaded together
-                    const int rt_l = 32 * c + lane < d.n_eff ? p.route_list[d.route0 + 32 * c + lane] : 0;
-                    tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + 32 * c), rr);
-                    tc::tmem_ld_wait();
 #pragma unroll
-                    for (int jj = 0; jj < 32; jj++) {
-                        if (32 * c + jj < d.n_eff) {  // uniform within the warp
-                            // route rt's output row; the weighted sum over a token's
-                            // routes is taken afterwards in a fixed order
-                            const int rt = __shfl_sync(0xffffffffu, rt_l, jj);
-                            if (orow < p.n) p.yacc[(int64_t)rt * p.n + orow] = __uint_as_float(rr[jj]);
+                for (int c = 0; c < BN / 32; c++) {
+                    // the chunk count is the same in the 4 warps (they meet at named
+                    // barriers); a warp whose wait failed skips the work only
+                    if (c * 32 >= d.n_eff) break;
+                    uint32_t rr[32];
+                    const int rt_l = rtv[c];
+                    const float w_l = wv[c];
+                    const int rows = d.n_eff - 32 * c < 32 ? d.n_eff - 32 * c : 32;
+                    float *ob = xbuf + (ochunk & 1) * (32 * 128);
+                    if (!p.ysum) {
+                        // the buffer's previous bulk store has read it
+                        if (warp == 10 && lane == 0) tc::bulk_wait_read<1>();
+                        tg_named_bar(2, 128);
+                    }
+                    if (go) {
+                        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + 32 * c), rr);
+                        tc::tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 32; jj++) rr[jj] = 0u;
+                    }
+                    if (p.ysum) {
+#pragma unroll
+                        for (int jj = 0; jj < 32; jj++) {
+                            if (go && jj < rows) {  // uniform within the warp
+                                // fused weighted sum: w * (W_e . h_route) added into the
+                                // token's fp32 row (the 32 lanes: 128 consecutive bytes)
+                                const int rt = __shfl_sync(0xffffffffu, rt_l, jj);
+                                const float wr = __shfl_sync(0xffffffffu, w_l, jj);
+                                if (orow < p.n)
+                                    atomicAdd(&p.ysum[(int64_t)(rt / p.top_k) * p.n + orow], wr * __uint_as_float(rr[jj]));
+                            }
                         }
+                    } else {
+                        // the routes' output values in 128-column blocks, routes at their
+                        // grouped positions: the chunk's rows of this column block are one
+                        // contiguous run, written by one bulk copy from the staging buffer
+#pragma unroll
+                        for (int jj = 0; jj < 32; jj++) ob[jj * 128 + 32 * q + lane] = __uint_as_float(rr[jj]);
+                        tc::fence_proxy_async_smem();
+                        tg_named_bar(2, 128);
+                        if (warp == 10 && lane == 0 && go) {
+                            float *dst = p.yacc + (((int64_t)(d.row0 >> 7) * p.zrows + d.route0 + 32 * c) << 7);
+                            tc::bulk_store(dst, ob, (uint32_t)rows * 512u);
+                            tc::bulk_commit();
+                        }
+                        ochunk++;
                     }
                 }
             } else {
@@ -538,8 +757,11 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                     }
                     tg_named_bar(1, 128);
                     if (any) {
-                        // the chunk's 32 route ids, one per lane, loaded together
-                        const int rt_l = 32 * c + lane < d.n_eff ? p.route_list[d.route0 + 32 * c + lane] : 0;
+                        // this chunk's route ids (a register array indexed by the loop count)
+                        int rt_l = rtv[0];
+#pragma unroll
+                        for (int cc = 1; cc < BN / 32; cc++)
+                            if (c == cc) rt_l = rtv[cc];
 #pragma unroll 2
                         for (int jj = q; jj < 32; jj += 4) {
                             const int j = 32 * c + jj;
@@ -601,6 +823,8 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             tc::mbar_arrive(&tempty[b]);
             if (!ok) break;
         }
+        // bulk output stores finish before the CTA's shared memory is released
+        if (MODE == TG_MOE_DOWN && warp == 10 && lane == 0) tc::bulk_wait_all();
     } else if (lane == 0 && p.pstages > 0) {
         // ================= packed-weight loader: chunk c of a tile (K-steps
         // [c * pkc, (c + 1) * pkc) of its weight steps) into buffer pc % pstages:

@@ -484,8 +484,10 @@ def test_moe_staged_weights(g, H, I, down):
     xq = oracle.quantize_q8_1(x.float().numpy())
     _, hq = oracle.moe_gate_up(oracle.Q4_K, bank_gu, E, sgu, 2 * I, H, xq, ids, nthreads=8)
     ref = oracle.moe_down(down, bank_d, E, sd, H, I, hq, ids, rw, nthreads=8)
-    saved = (g.gguf_get_option("mmq_stage"), g.gguf_get_option("moe_vec_max_tokens"))
+    saved = (g.gguf_get_option("mmq_stage"), g.gguf_get_option("moe_vec_max_tokens"),
+             g.gguf_get_option("moe_deterministic"))
     g.gguf_set_option("moe_vec_max_tokens", 0)
+    g.gguf_set_option("moe_deterministic", 1)
     ys = []
     try:
         for stage in (1, 0):
@@ -497,5 +499,36 @@ def test_moe_staged_weights(g, H, I, down):
     finally:
         g.gguf_set_option("mmq_stage", saved[0])
         g.gguf_set_option("moe_vec_max_tokens", saved[1])
+        g.gguf_set_option("moe_deterministic", saved[2])
     # the same operand values either way, and a fixed order of the sums
     np.testing.assert_array_equal(ys[0], ys[1])
+
+
+def test_moe_deterministic_option(g):
+    """Option moe_deterministic = 1: per-route rows summed in slot order, the
+    same bits on every run; the default fused atomic sum agrees with it to
+    fp32 rounding of the sum's order (then bf16 output rounding)."""
+    E, K, H, I, T = 9, 8, 512, 256, 400
+    bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 950, True)
+    bank_d = _bank(oracle.Q6_K, E, H, I, 951, True)
+    sgu, sd = bank_gu.nbytes // E, bank_d.nbytes // E
+    ids, rw = synth.routes(T, E, K, seed=41)
+    x = synth.activations(T, H, seed=42, dtype=torch.float32).to(DEV)
+    args = (_u8(bank_gu), g.Q4_K, sgu, _u8(bank_d), g.Q6_K, sd, E, H, I, x, _u8(ids), _u8(rw))
+    saved = (g.gguf_get_option("moe_deterministic"), g.gguf_get_option("moe_vec_max_tokens"))
+    g.gguf_set_option("moe_vec_max_tokens", 0)
+    try:
+        g.gguf_set_option("moe_deterministic", 1)
+        y1 = g.gguf_moe_ffn(*args).cpu().numpy()
+        y2 = g.gguf_moe_ffn(*args).cpu().numpy()
+        g.gguf_set_option("moe_deterministic", 0)
+        y3 = g.gguf_moe_ffn(*args).cpu().numpy()
+    finally:
+        g.gguf_set_option("moe_deterministic", saved[0])
+        g.gguf_set_option("moe_vec_max_tokens", saved[1])
+    np.testing.assert_array_equal(y1, y2)
+    assert_close(y3, y1, 1e-5, "atomic vs slot-order weighted sum")
+    xq = oracle.quantize_q8_1(x.cpu().numpy())
+    _, hq = oracle.moe_gate_up(oracle.Q4_K, bank_gu, E, sgu, 2 * I, H, xq, ids, nthreads=8)
+    ref = oracle.moe_down(oracle.Q6_K, bank_d, E, sd, H, I, hq, ids, rw, nthreads=8)
+    assert_close_moe_e2e(y3, ref, "moe fp32 out, fused sum")
