@@ -110,7 +110,7 @@ static int64_t g_mmq_stage = 1;
 static int64_t g_moe_deterministic = 1;
 static int64_t g_mmq_bn_max = 256;
 int64_t option_mmq_bn_max() { return g_mmq_bn_max; }
-static int64_t g_moe_down_precise = 1;
+static int64_t g_moe_down_precise = 0;
 int64_t option_mmq_stage() { return g_mmq_stage; }
 int64_t option_moe_deterministic() { return g_moe_deterministic; }
 int64_t option_mmvq_tc() { return g_mmvq_tc; }

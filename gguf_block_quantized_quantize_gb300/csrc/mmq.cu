@@ -105,8 +105,10 @@ static cudaError_t launch_dense(const uint8_t *w, int64_t n, int64_t k, const ui
     p.ldy = ldy;
     p.yacc = splits > 1 ? yacc : nullptr;
     if (splits > 1 && (e = cudaMemsetAsync(yacc, 0, sizeof(float) * (size_t)(m * n), s)) != cudaSuccess) return e;
+    CUtensorMap my = mh;
+    p.ystore = (splits == 1 && tg_make_out_map(&my, y, OT, n, m, ldy)) ? 1 : 0;
     const int grid = (int)(tiles < sms ? tiles : sms);
-    e = tg_launch<WT, BN, PRECISE, TG_DENSE, OT>(mh, ml, mw, p, grid, s);
+    e = tg_launch<WT, BN, PRECISE, TG_DENSE, OT>(mh, ml, mw, my, p, grid, s);
     if (e != cudaSuccess || splits == 1) return e;
     return launch_convert_rows(yacc, m, n, y, OT, ldy, s);
 }

@@ -274,7 +274,7 @@ static cudaError_t launch_moe_wt(TgParams p, int64_t rows, int64_t n_experts, cu
         tg_plan_staging(p, &mw, WT, p.w, p.n, n_experts, p.expert_stride, p.k, MODE == TG_MOE_GATE_UP ? 64 : TG_BM,
                         tg_base_bytes<WT, MOE_BN, PRECISE, MODE>());
     const int grid = device_info().sm_count;  // persistent; CTAs beyond the device-side tile count exit
-    return tg_launch<WT, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, mw, p, grid, s);
+    return tg_launch<WT, MOE_BN, PRECISE, MODE, GGUF_F32>(mh, ml, mw, mh, p, grid, s);
 }
 
 template <int MODE, bool PRECISE>

@@ -80,6 +80,7 @@ struct TgParams {
                   // order, as ceil(n / 128) blocks [zrows][128]
     float *ysum;  // MoE down with the fused weighted sum: fp32 token rows [T][n], zeroed before the call
     int64_t zrows;  // MoE down: rows (routes) of one 128-column block of yacc
+    int ystore;     // dense: the output is written by bulk tensor stores through map_y
     // gathered activation rows (MoE)
     const uint16_t *xh, *xl;
     int64_t top_k;
@@ -111,8 +112,12 @@ struct TgShape {
     static constexpr int A_STAGE = ATM ? 0 : OPS * TG_A_BYTES;
     static constexpr int B_STAGE = OPS * BN * TG_BK * 2;
     // gate_up exchange: gate and up values of 64 rows x 32 routes, fp32;
-    // down: two 32-route x 128-column fp32 buffers of the bulk output stores
-    static constexpr int XBUF = MODE == TG_MOE_GATE_UP ? 2 * 64 * 32 * 4 : MODE == TG_MOE_DOWN ? 2 * 32 * 128 * 4 : 0;
+    // down: two 32-route x 128-column fp32 buffers of the bulk output stores;
+    // dense: two 32 x 32 output boxes per epilogue warp (fp32 outputs are the
+    // precise mode, 16-bit outputs the fast one)
+    static constexpr int XBUF = MODE == TG_MOE_GATE_UP ? 2 * 64 * 32 * 4
+                              : MODE == TG_MOE_DOWN    ? 2 * 32 * 128 * 4
+                                                       : 4 * 2 * 32 * 32 * (PRECISE ? 4 : 2);
     static constexpr int BAR_BYTES = 1024;
     static constexpr int FIXED = 1024 + XBUF + BAR_BYTES + BN * 8;
     // room kept for two buffers of staged packed weights: 128 rows x one chunk
@@ -173,7 +178,8 @@ __device__ __forceinline__ TgTile tg_tile(const TgParams &p, int t, int KS) {
 template <int WT, int BN, bool PRECISE, int MODE, int OT>
 __global__ void __launch_bounds__(TG_THREADS, 1)
     tg_kernel(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo,
-              const __grid_constant__ CUtensorMap map_w, const TgParams p, int *err) {
+              const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_y, const TgParams p,
+              int *err) {
     using S = TgShape<WT, BN, PRECISE, MODE>;
     constexpr int ST = S::STAGES, STA = S::STA;
     extern __shared__ uint8_t smem_raw[];
@@ -673,6 +679,30 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                     uint32_t rr[32];
                     tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + 32 * c), rr);
                     tc::tmem_ld_wait();
+                    if (p.ystore) {
+                        // this warp's 32 weight rows x 32 activation rows as one box:
+                        // element (activation row jj, weight row lane) in the output
+                        // dtype, then one bulk tensor store (edges past m, n clipped)
+                        constexpr int ES = OT == GGUF_F32 ? 4 : 2;
+                        uint8_t *ob = reinterpret_cast<uint8_t *>(xbuf) + (q * 2 + (ochunk & 1)) * (32 * 32 * ES);
+                        if (lane == 0) tc::bulk_wait_read<1>();   // the box's previous store has read it
+                        __syncwarp();
+#pragma unroll
+                        for (int jj = 0; jj < 32; jj++) {
+                            const float v = __uint_as_float(rr[jj]);
+                            if (OT == GGUF_F32) reinterpret_cast<float *>(ob)[jj * 32 + lane] = v;
+                            else if (OT == GGUF_BF16) reinterpret_cast<uint16_t *>(ob)[jj * 32 + lane] = f2bf_rn(v);
+                            else reinterpret_cast<uint16_t *>(ob)[jj * 32 + lane] = f2h_rn(v);
+                        }
+                        tc::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tc::tma_store_2d(&map_y, ob, (int32_t)(d.row0 + 32 * q), (int32_t)(d.m0 + 32 * c));
+                            tc::bulk_commit();
+                        }
+                        ochunk++;
+                        continue;
+                    }
                     if (orow < p.n) {
 #pragma unroll
                         for (int jj = 0; jj < 32; jj++) {
@@ -824,7 +854,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             if (!ok) break;
         }
         // bulk output stores finish before the CTA's shared memory is released
-        if (MODE == TG_MOE_DOWN && warp == 10 && lane == 0) tc::bulk_wait_all();
+        if (lane == 0) tc::bulk_wait_all();
     } else if (lane == 0 && p.pstages > 0) {
         // ================= packed-weight loader: chunk c of a tile (K-steps
         // [c * pkc, (c + 1) * pkc) of its weight steps) into buffer pc % pstages:
@@ -884,6 +914,24 @@ inline cudaError_t tg_make_map(CUtensorMap *map, const uint16_t *base, int64_t r
 
 int *tg_error_word();
 
+// the output y[m][ldy] (element type ot) as a 2-D tensor map with 32 x 32
+// boxes, for the dense epilogue's bulk tensor stores; false when its base or
+// row stride is not 16-byte aligned
+inline bool tg_make_out_map(CUtensorMap *map, void *y, int ot, int64_t n, int64_t m, int64_t ldy) {
+    auto enc = tensor_map_encoder();
+    const int64_t es = ot == GGUF_F32 ? 4 : 2;
+    if (!enc || (reinterpret_cast<uintptr_t>(y) & 15) || (ldy * es) % 16 || n <= 0 || m <= 0) return false;
+    cuuint64_t gdim[2] = {(cuuint64_t)n, (cuuint64_t)m};
+    cuuint64_t gstride[1] = {(cuuint64_t)(ldy * es)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt = ot == GGUF_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : ot == GGUF_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return enc(map, dt, 2, y, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Staging of the packed weight rows (sets the p.p* fields and the tensor map;
 // p.pstages = 0 when the rows cannot be staged, and the producers then load
 // from global memory).  The weights are E matrices of `rows` rows of k values,
@@ -939,8 +987,8 @@ inline void tg_plan_staging(TgParams &p, CUtensorMap *map, int wt, const uint8_t
 }
 
 template <int WT, int BN, bool PRECISE, int MODE, int OT>
-inline cudaError_t tg_launch(const CUtensorMap &mh, const CUtensorMap &ml, const CUtensorMap &mw, const TgParams &p,
-                             int grid, cudaStream_t s) {
+inline cudaError_t tg_launch(const CUtensorMap &mh, const CUtensorMap &ml, const CUtensorMap &mw, const CUtensorMap &my,
+                             const TgParams &p, int grid, cudaStream_t s) {
     using S = TgShape<WT, BN, PRECISE, MODE>;
     auto kern = tg_kernel<WT, BN, PRECISE, MODE, OT>;
     static bool attr_set[64] = {};
@@ -955,7 +1003,7 @@ inline cudaError_t tg_launch(const CUtensorMap &mh, const CUtensorMap &ml, const
     if (!err) return cudaErrorInvalidSymbol;
     const int64_t smem = S::BASE + (int64_t)p.pstages * p.pstage_bytes;
     if (smem > TG_SMEM_MAX) return cudaErrorInvalidValue;
-    kern<<<grid, TG_THREADS, (size_t)smem, s>>>(mh, ml, mw, p, err);
+    kern<<<grid, TG_THREADS, (size_t)smem, s>>>(mh, ml, mw, my, p, err);
     return cudaGetLastError();
 }
 
