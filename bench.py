@@ -127,13 +127,14 @@ class Decode:
     activations shares one quantization).  Weight copies rotate over more
     than 4x L2 per shape, so no launch finds its weights in L2.
 
-    Each M runs as one segment-table launch over both weight matrices (four
-    MMVQ launches per step).  They depend only on the quantized rows, so a step
-    runs them on four CUDA streams, which overlaps the start and end of one
-    launch with the others'; `serial` keeps them on one stream (the per-kernel
-    roofline is timed that way).  Measured on GB300: 59.4 us per step on four
-    streams with segment launches, 61.2 on two streams with eight per-matrix
-    launches; serially 63.1 against 66.0 us."""
+    Each M is one segment-table MMVQ launch over both weight matrices (four
+    MMVQ launches per step).  They depend only on the quantized rows, so the
+    step issues them as one gguf_mul_mat_batch call: a chain of programmatic
+    dependent launches in which each starts as the previous one drains, closed
+    by an empty ordinary launch.  Measured on GB300 before the batch call: 59.4
+    us per step on four CUDA streams, 63.1 us serially.  `mode` selects the
+    batch (default), four streams ("streams") or serial segment calls
+    ("serial")."""
 
     def __init__(self, torch, g, synth, dev):
         self.g = g
@@ -178,25 +179,26 @@ class Decode:
         self.counters[(n, k)] = (c + 1) % pool.shape[0]
         return pool[c]
 
-    def _products(self, ms):
-        g = self.g
-        for m in ms:
-            for (n, k) in DECODE_SHAPES:   # both weight matrices read this M's q8_1 slice
-                g.gguf_mul_mat(self.weight(n, k), g.Q4_K, n, k, self.xqs[m], xt=g.Q8_1, m=m, out=self.ys[(n, m)],
-                               ws=self.ws)
-
     def _segments(self, ms):   # one call (and launch) per M for both weight matrices
         g = self.g
         for m in ms:
             segs = [(self.weight(n, k), n, self.ys[(n, m)]) for (n, k) in DECODE_SHAPES]
             g.gguf_mul_mat_segments(g.Q4_K, self.k, self.xqs[m], segs, xt=g.Q8_1, m=m, ws=self.ws)
 
-    def step(self, quantize=True, x_all=None, serial=False, segments=True):
+    def _batch(self, ms):   # one call: the M-products as chained launches
+        self.g.gguf_mul_mat_batch(self.g.Q4_K, self.k,
+                                  [(self.xqs[m], [(self.weight(n, k), n, self.ys[(n, m)]) for (n, k) in DECODE_SHAPES])
+                                   for m in ms])
+
+    def step(self, quantize=True, x_all=None, mode="batch"):
         g, torch = self.g, self.torch
         if quantize:
             g.gguf_quantize_q8_1(self.x_all if x_all is None else x_all, out=self.xq_all)
-        run = self._segments if segments else self._products
-        if serial:
+        if mode == "batch":
+            self._batch(DECODE_MS)
+            return
+        run = self._segments
+        if mode == "serial":
             run(DECODE_MS)
             return
         # M = 4 on the current stream, M = 8, 2 and 1 on one side stream each
@@ -213,11 +215,12 @@ class Decode:
             join.record(side)
             main.wait_event(join)
 
-    def mmvq_launches_per_step(self, segments=True):
-        return len(DECODE_MS) * (1 if segments else len(DECODE_SHAPES))
+    def mmvq_launches_per_step(self):
+        return len(DECODE_MS)
 
     def launches_per_step(self, quantize=True):
-        return self.mmvq_launches_per_step() + (1 if quantize else 0)
+        # the MMVQ launches, the empty launch that closes the batch, the quantize
+        return self.mmvq_launches_per_step() + 1 + (1 if quantize else 0)
 
     def bytes_per_step(self):
         """Algorithmic bytes: packed weights + bf16 x read + q8_1 write + q8_1 read per product + y write."""
@@ -272,7 +275,7 @@ def run_ours(args, rank, world, torch, dev):
     nph = min(dec.n_phase, 8)
     with torch.cuda.stream(stream):
         graphs = _capture(torch, stream, dec.step, nph)
-        mgraphs = _capture(torch, stream, lambda: dec.step(quantize=False, serial=True), nph)
+        mgraphs = _capture(torch, stream, lambda: dec.step(quantize=False), nph)
     torch.cuda.synchronize()
     per_step, weight_bytes, mmvq_bytes = dec.bytes_per_step()
 
@@ -294,6 +297,11 @@ def run_ours(args, rank, world, torch, dev):
     ms_total = ev0.elapsed_time(ev1)
     # the dominant kernel alone (MMVQ on the same q8_1 inputs, same rotation, same stream)
     ms_mmvq_step = _time_graphs(torch, stream, mgraphs, max(args.steps, 20))
+    # for comparison: the same four launches as separate segment calls (no chaining)
+    with torch.cuda.stream(stream):
+        sgraphs = _capture(torch, stream, lambda: dec.step(quantize=False, mode="serial"), nph)
+    ms_mmvq_serial = _time_graphs(torch, stream, sgraphs, max(args.steps, 20))
+    del sgraphs
     clk = clocks.stop()
     n_mmvq = dec.mmvq_launches_per_step()
     ms_mmvq = ms_mmvq_step / n_mmvq
@@ -324,15 +332,17 @@ def run_ours(args, rank, world, torch, dev):
         "config": {"workload": "decode MMVQ: Q4_K 4096x4096 and 14336x4096, bf16 activations M in {1,2,4,8}; "
                                "step = one bf16->q8_1 quantize of the 15 activation rows, then per M one "
                                "segment-table MMVQ launch over both weight matrices (each M-row slice shared by "
-                               "both), the four launches on 4 CUDA streams after the quantize",
+                               "both), the four launches chained in one gguf_mul_mat_batch call",
                    "l2": "weight copies rotate over >4x L2 per shape (inputs larger than L2)",
                    "weights": "random-but-safe packed Q4_K blocks", "parallelism": f"replicas x{world}"},
         "weight_bytes_per_step": weight_bytes, "bytes_per_step": per_step,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": mmvq_traffic(),
                      "kernel": "MMVQ (dp4a mmvq_kernel for M<=4, int8 tensor-core for M=8), one segment-table launch "
-                               "per M over both matrices; 4 launches per step, mean",
-                     "peak_source": f"{peak_kind} hbm_gbs"},
+                               "per M over both matrices, the 4 launches chained in one gguf_mul_mat_batch call; "
+                               "total bytes / total time of the 4",
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "frac_unchained": round(mmvq_bytes / (ms_mmvq_serial * 1e-3) / 1e9 / hbm_peak, 4)},
         "detail": detail,
         "gpu_launches": args.steps * dec.launches_per_step(),
         "clocks": clk,
@@ -371,9 +381,8 @@ def run_e2e(args, g, torch, dev, dec, per_step):
     """Same workload through the public API with host buffers: each step copies
     its activations from pinned host memory and reads its outputs back.  The
     loop is bound by host calls, so it issues the fewest: one quantize, one
-    gguf_mul_mat_segments call per M (both weight matrices), one copy each way,
-    all on one stream (a second stream's events cost more host time than the
-    overlap saves here)."""
+    gguf_mul_mat_batch call (all M-products), one copy each way, on one
+    stream."""
     hx = dec.x_all.cpu().pin_memory()
     hy = torch.empty(dec.y_all.shape, dtype=dec.y_all.dtype).pin_memory()
     dx = torch.empty_like(dec.x_all)
@@ -383,7 +392,7 @@ def run_e2e(args, g, torch, dev, dec, per_step):
 
     def step():
         dx.copy_(hx, non_blocking=True)
-        dec.step(x_all=dx, serial=True, segments=True)
+        dec.step(x_all=dx)
         hy.copy_(dec.y_all, non_blocking=True)
 
     with torch.cuda.stream(stream):

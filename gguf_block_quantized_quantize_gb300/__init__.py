@@ -43,6 +43,14 @@ class Segment(ctypes.Structure):
     _fields_ = [("w", ctypes.c_void_p), ("n", ctypes.c_int64), ("y", ctypes.c_void_p), ("ldy", ctypes.c_int64)]
 
 
+class MmJob(ctypes.Structure):
+    _fields_ = [("segs", ctypes.POINTER(Segment)), ("nseg", ctypes.c_int), ("xq", ctypes.c_void_p),
+                ("m", ctypes.c_int64)]
+
+
+MAX_BATCH_JOBS = 8
+
+
 class MoeArgs(ctypes.Structure):
     _fields_ = [("w", ctypes.c_void_p), ("wt", ctypes.c_int), ("n_experts", ctypes.c_int64),
                 ("expert_stride", ctypes.c_int64), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
@@ -76,6 +84,7 @@ SIGNATURES = {
     "gguf_mul_mat_noalloc": (_i, [_p, _i, _i64, _i64, _p, _i, _i64, _i64, _p, _i, _i64, _p]),
     "gguf_mul_mat_segments_ws_size": (_sz, [_i, ctypes.POINTER(Segment), _i, _i64, _i, _i64, _i]),
     "gguf_mul_mat_segments": (_i, [_i, ctypes.POINTER(Segment), _i, _i64, _p, _i, _i64, _i64, _i, _p, _sz, _p]),
+    "gguf_mul_mat_batch": (_i, [_i, _i64, ctypes.POINTER(MmJob), _i, _i, _p]),
     "gguf_mul_mat_id_ws_size": (_sz, [ctypes.POINTER(MoeArgs)]),
     "gguf_mul_mat_id": (_i, [ctypes.POINTER(MoeArgs), _p, _sz, _p]),
     "gguf_moe_ffn_ws_size": (_sz, [ctypes.POINTER(MoeFfnArgs)]),
@@ -245,6 +254,31 @@ def gguf_mul_mat_segments(wt: int, k: int, x: torch.Tensor, segments, xt: int | 
         ws = _workspace(int(lib.gguf_mul_mat_segments_ws_size(wt, arr, len(segments), k, xt, m, yt)), x.device)
     _check(lib.gguf_mul_mat_segments(wt, arr, len(segments), k, _ptr(x), xt, m, ldx, yt, _ptr(ws),
                                      0 if ws is None else ws.numel(), _stream()))
+    return outs
+
+
+def gguf_mul_mat_batch(wt: int, k: int, jobs):
+    """Decode-sized products on q8_1 rows, one chained launch per job:
+    ``jobs`` is a list of (xq [m, row bytes] uint8, [(w, n, out), ...]).  The
+    outputs share one dtype; they are returned per job."""
+    arrs, cjobs, outs = [], [], []
+    yt = None
+    for xq, segs in jobs:
+        if xq.dim() != 2 or (xq.shape[0] > 1 and xq.stride(0) != k // 32 * Q8_1_BYTES):
+            raise ValueError("gguf_mul_mat_batch: q8_1 rows of xq must be contiguous")
+        for (_, _, o) in segs:
+            t = _TYPE_OF[o.dtype]
+            if o.stride(1) != 1 or (yt is not None and t != yt):
+                raise ValueError("gguf_mul_mat_batch: outputs need contiguous rows and one dtype")
+            yt = t
+        arr = (Segment * len(segs))(*[Segment(_ptr(w), n, _ptr(o), o.stride(0)) for (w, n, o) in segs])
+        arrs.append(arr)
+        cjobs.append(MmJob(arr, len(segs), _ptr(xq), xq.shape[0]))
+        outs.append([o for (_, _, o) in segs])
+    if not cjobs:
+        return outs
+    carr = (MmJob * len(cjobs))(*cjobs)
+    _check(_lib_fast().gguf_mul_mat_batch(wt, k, carr, len(cjobs), yt, _stream()))
     return outs
 
 

@@ -109,6 +109,7 @@ static int64_t g_moe_vec_max_tokens = 256;
 static int64_t g_mmq_stage = 1;
 static int64_t g_moe_deterministic = 1;
 static int64_t g_mmq_bn_max = 256;
+static int64_t g_mmq_split_k = 1;   // small m: split K across CTAs (fp32 partial sums) to fill the GPU
 int64_t option_mmq_bn_max() { return g_mmq_bn_max; }
 static int64_t g_moe_down_precise = 0;
 int64_t option_mmq_stage() { return g_mmq_stage; }
@@ -267,7 +268,7 @@ static gguf_status mul_mat_impl(int wt, const gguf_segment *segs, int nseg, int6
             xl = (uint16_t *)wp;
             wp += align256((size_t)(m * kx * 2));
         }
-        float *yacc = m <= 256 ? (float *)wp : nullptr;
+        float *yacc = (m <= 256 && g_mmq_split_k) ? (float *)wp : nullptr;
         cudaError_t e = xt == GGUF_Q8_1 ? launch_q8_1_to_f16((const uint8_t *)x, m, k, xh, xl, s, kx)
                                         : launch_quantize_q8_1(x, xt, m, k, ldx, nullptr, xh, xl, s, kx);
         if (e != cudaSuccess) return cuda_status(e, what);
@@ -324,6 +325,62 @@ size_t gguf_mul_mat_segments_ws_size(int wt, const gguf_segment *segs, int nseg,
 gguf_status gguf_mul_mat_segments(int wt, const gguf_segment *segs, int nseg, int64_t k, const void *x, int xt,
                                   int64_t m, int64_t ldx, int yt, void *ws, size_t ws_bytes, gguf_stream_t stream) {
     return mul_mat_impl(wt, segs, nseg, k, x, xt, m, ldx, yt, ws, ws_bytes, stream, "mul_mat_segments");
+}
+
+gguf_status gguf_mul_mat_batch(int wt, int64_t k, const gguf_mm_job *jobs, int njobs, int yt, gguf_stream_t stream) {
+    const char *what = "mul_mat_batch";
+    if (!is_weight(wt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "%s: weight type %d not supported", what, wt);
+    if (!is_float(yt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "%s: y type %d is not F32/BF16/F16", what, yt);
+    if (njobs < 0 || njobs > GGUF_MAX_BATCH_JOBS || (njobs > 0 && !jobs))
+        return fail(GGUF_ERR_INVALID_ARG, "%s: %d jobs (0..%d)", what, njobs, GGUF_MAX_BATCH_JOBS);
+    if (k < 0) return fail(GGUF_ERR_INVALID_ARG, "%s: negative size", what);
+    if (row_size(wt, k) < 0) return fail(GGUF_ERR_SHAPE, "%s: k=%lld not a multiple of the block of type %d", what, (long long)k, wt);
+    // validate every job before launching any
+    MmvqSegs sgs[GGUF_MAX_BATCH_JOBS];
+    int live = 0;
+    for (int j = 0; j < njobs; j++) {
+        const gguf_mm_job &jb = jobs[j];
+        if (jb.nseg < 1 || jb.nseg > GGUF_MAX_SEGMENTS || !jb.segs)
+            return fail(GGUF_ERR_INVALID_ARG, "%s: job %d has %d segments (1..%d)", what, j, jb.nseg, GGUF_MAX_SEGMENTS);
+        if (jb.m < 0) return fail(GGUF_ERR_INVALID_ARG, "%s: job %d: negative m", what, j);
+        MmvqSegs &sg = sgs[j];
+        sg = MmvqSegs{};
+        for (int i = 0; i < MMVQ_MAX_SEGS; i++) sg.end[i] = INT64_MAX;
+        int64_t acc = 0;
+        for (int i = 0; i < jb.nseg; i++) {
+            const gguf_segment &g = jb.segs[i];
+            if (g.n < 0 || g.ldy < g.n) return fail(GGUF_ERR_INVALID_ARG, "%s: job %d segment %d: bad n / ldy", what, j, i);
+            if (g.n == 0) continue;
+            if (!g.w || !g.y) return fail(GGUF_ERR_INVALID_ARG, "%s: job %d: null pointer", what, j);
+            if (!aligned(g.w, 16) || !aligned(g.y, esize(yt)))
+                return fail(GGUF_ERR_ALIGNMENT, "%s: job %d: weight base must be 16-byte aligned, y element-aligned", what, j);
+            acc += g.n;
+            sg.end[sg.nseg] = acc;
+            sg.w[sg.nseg] = (const uint8_t *)g.w;
+            sg.y[sg.nseg] = g.y;
+            sg.ldy[sg.nseg] = g.ldy;
+            sg.nseg++;
+        }
+        if (jb.m == 0 || acc == 0) continue;   // nothing to compute
+        if (k == 0) return fail(GGUF_ERR_SHAPE, "%s: k must be positive", what);
+        if (!jb.xq || !aligned(jb.xq, 4)) return fail(GGUF_ERR_ALIGNMENT, "%s: job %d: q8_1 input null or misaligned", what, j);
+        if (use_mmq(wt, jb.m, k) || (jb.m > 8 && !mmvq_tc_wide(wt, k, jb.m)))
+            return fail(GGUF_ERR_INVALID_ARG, "%s: job %d: m=%lld is not decode-sized (the MMVQ range)", what, j,
+                        (long long)jb.m);
+        live++;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    int pos = 0;
+    for (int j = 0; j < njobs; j++) {
+        MmvqSegs &sg = sgs[j];
+        if (jobs[j].m == 0 || sg.nseg == 0) continue;
+        sg.chain = live == 1 ? 0 : (pos == 0 ? 1 : 2);
+        pos++;
+        cudaError_t e = launch_mmvq(sg, wt, k, (const uint8_t *)jobs[j].xq, jobs[j].m, yt, s);
+        if (e != cudaSuccess) return cuda_status(e, what);
+    }
+    if (live > 1) return cuda_status(launch_mmvq_join(s), what);
+    return GGUF_OK;
 }
 
 // ---------------------------------------------------------------- MoE
@@ -636,6 +693,10 @@ gguf_status gguf_set_option(const char *key, int64_t value) {
         g_mmq_bn_max = value;
         return GGUF_OK;
     }
+    if (!strcmp(key, "mmq_split_k")) {
+        g_mmq_split_k = value != 0;
+        return GGUF_OK;
+    }
     if (!strcmp(key, "moe_down_precise")) {
         g_moe_down_precise = value != 0;
         return GGUF_OK;
@@ -655,6 +716,7 @@ int64_t gguf_get_option(const char *key) {
     if (!strcmp(key, "moe_deterministic")) return g_moe_deterministic;
     if (!strcmp(key, "moe_down_precise")) return g_moe_down_precise;
     if (!strcmp(key, "mmq_bn_max")) return g_mmq_bn_max;
+    if (!strcmp(key, "mmq_split_k")) return g_mmq_split_k;
     return -1;
 }
 

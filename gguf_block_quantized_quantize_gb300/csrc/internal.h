@@ -76,6 +76,10 @@ struct MmvqSegs {
     const uint8_t *w[MMVQ_MAX_SEGS];
     void *y[MMVQ_MAX_SEGS];
     int64_t ldy[MMVQ_MAX_SEGS];
+    // programmatic dependent launch: 0 a launch on its own; 1 the first launch
+    // of a batch whose launches share inputs written before the batch; 2 a
+    // later launch of such a batch (see mmvq_pdl_enter)
+    int chain;
     __host__ __device__ int64_t rows() const { return end[nseg - 1]; }
 };
 // one segment: W[n][k] -> y[.][ldy]
@@ -101,6 +105,9 @@ bool mmvq_routes_supported(int wt, int64_t k);
 // for every segment s: y_s[m][ldy_s] (yt) = W_s (wt) . q8_1 rows xq[m] ; m <= 8,
 // or m <= 32 when mmvq_tc_wide(wt, k, m)
 cudaError_t launch_mmvq(const MmvqSegs &sg, int wt, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s);
+// an empty kernel launched without programmatic serialization: the end of a
+// batch of chained launches (sg.chain 1, 2, ...)
+cudaError_t launch_mmvq_join(cudaStream_t s);
 
 // tensor-core MMQ: y[m][ldy] = W[n][k] . xh[m][k] (fp16 operand rows; fp32
 // outputs also need the low parts xl).  yacc (optional, fp32 [m][n]) lets small

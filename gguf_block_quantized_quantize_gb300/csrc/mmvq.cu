@@ -33,6 +33,15 @@ cudaError_t launch_mmvq(const MmvqSegs &sg, int wt, int64_t k, const uint8_t *xq
     }
 }
 
+__global__ void mmvq_join_kernel() {}
+
+// an ordinary (non-programmatic) launch: it starts only after all earlier work
+// of the stream has completed, which closes a batch of chained MMVQ launches
+cudaError_t launch_mmvq_join(cudaStream_t s) {
+    mmvq_join_kernel<<<1, 32, 0, s>>>();
+    return cudaGetLastError();
+}
+
 bool mmvq_routes_supported(int wt, int64_t k) {
     const int64_t values = wt == GGUF_Q8_0 ? 32 : 64;   // values per thread's piece
     return (wt == GGUF_Q8_0 || wt == GGUF_Q4_0 || wt == GGUF_Q4_K || wt == GGUF_Q5_K || wt == GGUF_Q6_K ||

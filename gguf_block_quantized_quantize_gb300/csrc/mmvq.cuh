@@ -63,6 +63,25 @@ __device__ __forceinline__ void load_act_q8_0(ActPiece<M> &a, const uint8_t *xq,
     }
 }
 
+// Programmatic dependent launch of an MMVQ kernel.  chain 0 (alone): let the
+// next kernel launch, then wait for the kernel that wrote the activations.
+// chain 1 (first of a batch): wait first, then let the batch's next kernel
+// launch: its inputs were written before the batch, so it may read them at
+// once.  chain 2 (later in a batch): let the next launch and read at once.
+// The batch ends with an ordinary launch of an empty kernel, which starts only
+// after every kernel before it has completed.
+__device__ __forceinline__ void mmvq_pdl_enter(int chain) {
+    if (chain == 1) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    } else if (chain == 2) {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    } else {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
+}
+
 template <int V>
 __device__ __forceinline__ float butterfly(float (&v)[V], int lane) {
     constexpr int LOG = V == 1 ? 0 : V == 2 ? 1 : V == 4 ? 2 : V == 8 ? 3 : V == 16 ? 4 : 5;
@@ -911,8 +930,8 @@ __global__ void __launch_bounds__(MAXT, MAXT == 32 ? 12 : 1) mmvq_kernel(const M
     // weights never change: the first rows are requested before waiting for
     // the kernel that wrote the activations
     if (n0 < nv) load_rows(wa, n0);
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if constexpr (!ROUTES) mmvq_pdl_enter(sg.chain);
+    else asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // routes waited above
 
     typename PT::template A<M> act;
     const int m_mine = m_act - tg * M;  // tokens of this thread (may be <= 0)

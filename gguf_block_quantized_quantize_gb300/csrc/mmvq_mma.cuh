@@ -116,8 +116,7 @@ __global__ void __launch_bounds__(NT == 1 ? 512 : 256, 1)
     int64_t tile = blockIdx.x;
     MmaW wa, wb;
     if (sb_lo < sb_hi && tile < n_tiles) load_item(wa, tile, sb_lo);
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    mmvq_pdl_enter(sg.chain);
 
     // ---- q8_1 rows into shared memory (quants of block b at b * 40 + 8), d_a and s_a pairs
     for (int i = tid; i < TOK * nblk; i += blockDim.x) {

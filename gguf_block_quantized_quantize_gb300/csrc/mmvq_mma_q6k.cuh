@@ -132,8 +132,7 @@ __global__ void __launch_bounds__(256, 2)
     int64_t tile = blockIdx.x;
     Q6Raw wa, wb;
     if (sb_lo < sb_hi && tile < n_tiles) load_item(wa, tile, sb_lo);
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    mmvq_pdl_enter(sg.chain);
 
     // ---- q8_1 rows into shared memory (quants of block b at b * 40 + 8),
     // d_a per block and 32 * (sum of the quants) per 16-value group

@@ -228,6 +228,35 @@ gguf_status gguf_mul_mat_segments(int wt, const gguf_segment *segs, int nseg, in
 gguf_status gguf_mul_mat_noalloc(const void *w, int wt, int64_t n, int64_t k, const void *x, int xt, int64_t m,
                                  int64_t ldx, void *y, int yt, int64_t ldy, gguf_stream_t stream);
 
+/*
+ * gguf_mul_mat_batch -- several decode-sized products of one weight type and
+ * K in one call, each a gguf_mul_mat_segments on q8_1 rows that were written
+ * before the call: job j computes y_s[m_j][n_s] = Xq_j . W_s^T for its
+ * segments.  The pages' decode step issues one MMVQ per weight (FreeToken PR
+ * #690, section "Vendored ggml", MMVQ for small batches); a batch of such
+ * products is launched as one chain of kernels (programmatic dependent launch)
+ * in which each kernel after the first starts as the previous one drains, so
+ * the GPU pays the start-up and tail of a launch once for the batch.
+ *   jobs[njobs] : host array, njobs <= GGUF_MAX_BATCH_JOBS; each job's xq is
+ *                 [m][row_size(GGUF_Q8_1, k)] bytes (4-byte aligned) and its
+ *                 m is decode-sized (the MMVQ range of gguf_mul_mat: at most
+ *                 option "mmvq_max_m" rows, Q4_K up to "mmvq_tc_max_m");
+ *                 segments as in gguf_mul_mat_segments.
+ * The jobs run concurrently: no job may write memory that another job of the
+ * batch reads or writes (its y may not be another job's xq).  The call ends
+ * with an ordinary launch, so work queued after it sees every job complete.
+ * No workspace.  Errors as gguf_mul_mat_segments; GGUF_ERR_INVALID_ARG for a
+ * job outside the MMVQ range; nothing is launched unless every job is valid.
+ */
+#define GGUF_MAX_BATCH_JOBS 8
+typedef struct gguf_mm_job {
+    const gguf_segment *segs;  /* host array of the job's weight segments */
+    int nseg;                  /* 1 .. GGUF_MAX_SEGMENTS */
+    const void *xq;            /* q8_1 activation rows */
+    int64_t m;                 /* rows of xq */
+} gguf_mm_job;
+gguf_status gguf_mul_mat_batch(int wt, int64_t k, const gguf_mm_job *jobs, int njobs, int yt, gguf_stream_t stream);
+
 /* mul_mat_id modes */
 #define GGUF_MOE_GATE_UP_SWIGLU 0   /* h[r] = silu(gate) * up, rounded to bf16, out as BF16 or Q8_1 */
 #define GGUF_MOE_DOWN_WEIGHTED_SUM 1 /* y[t] = sum_k route_w[t][k] * (W[e] . x[route]) */

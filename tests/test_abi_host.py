@@ -183,3 +183,24 @@ def test_device_error_query_arguments(g):
     assert L.gguf_device_errors_async(None, 1, None) == 1
     assert L.gguf_device_errors_async(ctypes.c_void_p(0x10002), 1, None) == 4
     assert g._STATUS[7] == "DEVICE"
+
+
+def test_mul_mat_batch_argument_checks(g):
+    L = g.load_library()
+    seg = g.Segment(FAKE, 16, FAKE, 16)
+    segs = (g.Segment * 1)(seg)
+    def job(m, nseg=1, xq=0x20000):
+        return g.MmJob(segs, nseg, ctypes.c_void_p(xq), m)
+    def run(jobs, wt=None, k=256, yt=None):
+        arr = (g.MmJob * max(len(jobs), 1))(*jobs) if jobs else None
+        return L.gguf_mul_mat_batch(g.Q4_K if wt is None else wt, k, arr, len(jobs), g.BF16 if yt is None else yt, None)
+    assert run([]) == 0                                    # no jobs: nothing to do
+    assert run([job(4)] * 9) == 1                          # more than GGUF_MAX_BATCH_JOBS
+    assert run([job(4, nseg=0)]) == 1
+    assert run([job(4)], wt=3) == 2                        # Q4_1: unsupported
+    assert run([job(4)], yt=g.Q8_0) == 2
+    assert run([job(4)], k=100) == 3
+    assert run([job(4), job(64)]) == 1                     # m = 64 is not decode-sized
+    assert "decode-sized" in L.gguf_last_error().decode()
+    assert run([job(4, xq=0x20002)]) == 4                  # q8_1 rows must be 4-byte aligned
+    assert run([job(0)]) == 0                              # empty jobs are skipped

@@ -118,3 +118,31 @@ def test_segments_reject_bad_count(g):
     with pytest.raises(g.GgufError) as e:
         g.gguf_mul_mat_segments(oracle.Q4_K, 256, x, [(w, 8, y)] * 9)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0])
+def test_mul_mat_batch_matches_segment_calls(g, wt):
+    """A batch of decode-sized jobs (chained launches) gives exactly what the
+    same jobs give as separate segment calls, and the oracle's products; a
+    kernel queued after the batch sees every job's output."""
+    k = 2048
+    shapes = [(300, 1), (1000, 2)]
+    ws = {n: _u8(oracle.quantize_weights(wt, synth.normal((n, k), 0.02, seed=n + s))) for n, s in shapes}
+    jobs, refs, sep = [], [], []
+    for j, m in enumerate((1, 2, 4, 8, 3)):
+        x = synth.activations(m, k, seed=40 + j, dtype=torch.bfloat16)
+        xq = g.gguf_quantize_q8_1(x.to(DEV))
+        outs = [torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=DEV) for n, _ in shapes]
+        jobs.append((xq, [(ws[n], n, o) for (n, _), o in zip(shapes, outs)]))
+        xq_ref = oracle.quantize_q8_1(x.float().numpy())
+        refs.append([oracle.mul_mat(wt, ws[n].cpu().numpy(), k, xq_ref) for n, _ in shapes])
+        sep.append([torch.empty((m, n), dtype=torch.bfloat16, device=DEV) for n, _ in shapes])
+        g.gguf_mul_mat_segments(wt, k, xq, [(ws[n], n, o) for (n, _), o in zip(shapes, sep[-1])], xt=g.Q8_1, m=m)
+    outs = g.gguf_mul_mat_batch(wt, k, jobs)
+    sums = [sum(o.float().sum() for o in job_outs) for job_outs in outs]   # queued right after the batch
+    torch.cuda.synchronize()
+    for j, job_outs in enumerate(outs):
+        for o, s, r in zip(job_outs, sep[j], refs[j]):
+            assert torch.equal(o, s), f"job {j}: batch differs from the segment call"
+            assert_close(o.float().cpu().numpy(), r, TOL_BF16, f"batch job {j}")
+        assert torch.isfinite(sums[j])
