@@ -666,45 +666,198 @@ def llama_decode(torch, g, synth, dev, stream, hbm_peak):
 # CPU baseline: the oracle on a bounded sample of the same workload
 # --------------------------------------------------------------------------
 
-def cpu_baseline(budget_s: float = 15.0):
-    import oracle
+class OracleDecode:
+    """The decode MMVQ workload (Q4_K 4096x4096 and 14336x4096, bf16
+    activations at M = 1, 2, 4, 8) on the oracle: one step quantizes each M's
+    rows to q8_1 and computes all eight products in fp64, like the GPU step."""
+
+    def __init__(self):
+        import oracle
+        import torch
+        from gguf_block_quantized_quantize_gb300 import synth
+        self.o = oracle
+        k = DECODE_SHAPES[0][1]
+        self.k = k
+        self.w = {n: synth.safe_blocks(oracle.Q4_K, n, k, seed=n) for (n, _) in DECODE_SHAPES}
+        self.x = {m: synth.activations(m, k, seed=100 + m, dtype=torch.bfloat16).float().numpy() for m in DECODE_MS}
+        rb, qb = oracle.row_size(oracle.Q4_K, k), oracle.row_size(oracle.Q8_1, k)
+        # the GPU step's algorithmic bytes: packed weights, bf16 x read, q8_1 written and read, bf16 y
+        self.bytes = sum(m * k * 2 + m * qb + sum(n * rb + m * qb + m * n * 2 for (n, _) in DECODE_SHAPES)
+                         for m in DECODE_MS)
+
+    def step(self, nthreads):
+        """Seconds per (n, M) product (its quantize included) and in total."""
+        o, per = self.o, {}
+        t_all = time.perf_counter()
+        for m in DECODE_MS:
+            t0 = time.perf_counter()
+            xq = o.quantize_q8_1(self.x[m])
+            tq = time.perf_counter() - t0
+            for i, (n, _) in enumerate(DECODE_SHAPES):
+                t0 = time.perf_counter()
+                o.mul_mat(o.Q4_K, self.w[n], self.k, xq, nthreads=nthreads)
+                per[f"{n}x{self.k}_m{m}"] = time.perf_counter() - t0 + (tq if i == 0 else 0.0)
+        return per, time.perf_counter() - t_all
+
+
+def _sub_rows(n, frac):
+    return max(1, min(n, int(round(n * frac))))
+
+
+def _time_rows(o, wt, w, k, xq, frac, nthreads):
+    """Seconds for all rows of W . xq, extrapolated from the first n * frac rows."""
+    n = w.shape[0]
+    r = _sub_rows(n, frac)
+    t0 = time.perf_counter()
+    o.mul_mat(wt, w[:r], k, xq, nthreads=nthreads)
+    return (time.perf_counter() - t0) * n / r
+
+
+def cpu_baseline():
+    """The oracle (scalar C, fp64 accumulation of the blockwise sums) on this
+    host's cores, one entry per workload, single-threaded and on every core.
+    The decode MMVQ step and the Q8_0 product run in full; the prefill MMQ
+    products, the MoE block and the Llama-shaped step run on seeded row, token
+    or layer subsets and are extrapolated linearly (the oracle's cost is
+    proportional to rows x tokens); each entry states its sample.  The line's
+    value is the decode MMVQ step on every core, in the GPU step's unit."""
+    import oracle as o
+    import torch
     from gguf_block_quantized_quantize_gb300 import synth
 
     cores = os.cpu_count() or 1
-    n, k, m = 4096, 4096, 8
-    w = synth.safe_blocks(oracle.Q4_K, n, k, seed=n)
-    x = synth.activations(m, k, seed=108, dtype=__import__("torch").bfloat16).float().numpy()
-    rows = 64
-    done_bytes, t0 = 0, time.perf_counter()
-    rb = oracle.row_size(oracle.Q4_K, k)
-    while time.perf_counter() - t0 < budget_s and rows <= n:
-        xq = oracle.quantize_q8_1(x)
-        oracle.mul_mat(oracle.Q4_K, w[:rows], k, xq, nthreads=cores)
-        done_bytes += rows * rb + m * k * 2 + 2 * xq.nbytes + m * rows * 2
-        rows = min(n, rows * 2) if rows < n else n + 1
-    dt = time.perf_counter() - t0
-    return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"Q4_K 4096x4096 x M=8 bf16 (q8_1 quantize + blockwise fp64 matmul), row subsets of "
-                      f"64..4096 rows for ~{budget_s:.0f} s on {cores} threads"}
+    t_begin = time.perf_counter()
+    out = {}
+
+    # Q8_0 512 x 1024, fp32 activations M = 8, fp32 out: in full, 5 calls each
+    n, k, m = 512, 1024, 8
+    w = synth.safe_blocks(o.Q8_0, n, k, seed=1)
+    x = synth.activations(m, k, seed=2, dtype=torch.float32).numpy()
+    e = {"sample": "in full (q8_1 quantize + fp64 blockwise product), median of 5 calls"}
+    for label, nt in (("1t", 1), ("all", cores)):
+        ts = []
+        for _ in range(5):
+            t0 = time.perf_counter()
+            o.mul_mat(o.Q8_0, w, k, o.quantize_q8_1(x), nthreads=nt)
+            ts.append(time.perf_counter() - t0)
+        e[f"us_{label}"] = round(statistics.median(ts) * 1e6, 1)
+    out["q8_0_512x1024_m8_f32"] = e
+
+    # decode MMVQ: the whole step, single-threaded and on every core
+    dec = OracleDecode()
+    e = {"sample": "in full: q8_1 quantize of each M + all 8 products per step", "bytes_per_step": dec.bytes}
+    for label, nt in (("1t", 1), ("all", cores)):
+        per, tot = dec.step(nt)
+        e[f"ms_{label}"] = round(tot * 1e3, 2)
+        e[f"gbs_{label}"] = round(dec.bytes / tot / 1e9, 4)
+        e[f"product_ms_{label}"] = {kk: round(v * 1e3, 2) for kk, v in per.items()}
+    out["decode_mmvq_q4_k"] = e
+    headline = e["gbs_all"]
+
+    # prefill MMQ: row subsets, the q8_1 quantize of all tokens timed in full
+    for name, wt, n, k, m, fr1, fra in (("mmq_q4_k_8192x2048_m8192", o.Q4_K, 8192, 2048, 8192, 4, 8),
+                                        ("mmq_q6_k_248320x2048_m2048", o.Q6_K, 248320, 2048, 2048, 16, 16)):
+        x = synth.activations(m, k, seed=3, dtype=torch.bfloat16).float().numpy()
+        t0 = time.perf_counter()
+        xq = o.quantize_q8_1(x)
+        tq = time.perf_counter() - t0
+        w = synth.safe_blocks(wt, max(fr1, fra * cores), k, seed=n)
+        e = {"quantize_s": round(tq, 3)}
+        for label, nt, rows in (("1t", 1, fr1), ("all", cores, fra * cores)):
+            t0 = time.perf_counter()
+            o.mul_mat(wt, w[:rows], k, xq, nthreads=nt)
+            t = tq + (time.perf_counter() - t0) * n / rows
+            e[f"s_{label}"] = round(t, 2)
+            e[f"tops_{label}"] = round(2.0 * m * n * k / t / 1e12, 6)
+        e["sample"] = (f"rows 0..{fr1} (1 thread) and 0..{fra * cores} (all cores) of {n}, each x all {m} tokens, "
+                       f"time x {n} / rows + the full quantize")
+        out[name] = e
+        del w, x, xq
+
+    # MoE FFN: all routes of a token subset through gate_up (Q4_K) + SwiGLU + q8_1 and down (Q6_K) +
+    # weighted sum; ops as on the GPU, 2 * T * top_k * (2I * H + H * I)
+    E, H, I, T, K_ = 256, 2048, 512, 8192, 8
+    wgu = synth.safe_blocks(o.Q4_K, E * 2 * I, H, seed=5)
+    wdn = synth.safe_blocks(o.Q6_K, E * H, I, seed=6)
+    gs, ds = 2 * I * o.row_size(o.Q4_K, H), H * o.row_size(o.Q6_K, I)
+    ids, rw = synth.routes(T, E, K_, seed=7)
+    ops = 2.0 * T * K_ * (2 * I * H + H * I)
+    e = {}
+    for label, nt, ts in (("1t", 1, 2), ("all", cores, 4 * cores)):
+        x = synth.activations(ts, H, seed=8, dtype=torch.bfloat16).float().numpy()
+        t0 = time.perf_counter()
+        xq = o.quantize_q8_1(x)
+        _, hq = o.moe_gate_up(o.Q4_K, wgu, E, gs, 2 * I, H, xq, ids[:ts], nthreads=nt)
+        o.moe_down(o.Q6_K, wdn, E, ds, H, I, hq, ids[:ts], rw[:ts], nthreads=nt)
+        t = (time.perf_counter() - t0) * T / ts
+        e[f"s_{label}"] = round(t, 2)
+        e[f"tops_{label}"] = round(ops / t / 1e12, 6)
+        e[f"tokens_{label}"] = ts
+    e["sample"] = f"the first tokens_1t / tokens_all of {T} tokens (all {K_} routes each), time x {T} / tokens"
+    out["moe_ffn_e256_top8_h2048_i512_t8192"] = e
+    del wgu, wdn
+
+    # Llama-3.2-3B-shaped decode step: one layer's seven linears (+ the four q8_1 quantizes) stand
+    # for all 28 (same shapes, same cost), the LM head on a row subset; GB/s of all 28 layers'
+    # weights + the head, as on the GPU
+    L, D, F, V, KV = 28, 3072, 8192, 128256, 1024
+    shapes = [("q", o.Q4_K, D, D), ("k", o.Q4_K, KV, D), ("v", o.Q6_K, KV, D), ("o", o.Q4_K, D, D),
+              ("gate", o.Q4_K, F, D), ("up", o.Q4_K, F, D), ("down", o.Q6_K, D, F)]
+    layer = {nm: synth.safe_blocks(wt, n, k, seed=1000 + i) for i, (nm, wt, n, k) in enumerate(shapes)}
+    head_rows = max(_sub_rows(V, 1.0 / 16), 1)
+    head = synth.safe_blocks(o.Q6_K, head_rows, D, seed=2000)
+    wbytes = L * sum(v.nbytes for v in layer.values()) + V * o.row_size(o.Q6_K, D)
+    rows = []
+    for m in (1, 8, 32):
+        xd = synth.activations(m, D, seed=m, dtype=torch.bfloat16).float().numpy()
+        xf = synth.activations(m, F, seed=m + 1, dtype=torch.bfloat16).float().numpy()
+        r = {"m": m}
+        for label, nt, frac, hfrac in (("1t", 1, 1.0 / 16, 1.0 / 16), ("all", cores, 1.0, 1.0)):
+            t0 = time.perf_counter()
+            xqd = o.quantize_q8_1(xd)
+            t_layer = 3 * (time.perf_counter() - t0)   # three quantizes of D-long rows per layer
+            t0 = time.perf_counter()
+            xqf = o.quantize_q8_1(xf)
+            t_layer += time.perf_counter() - t0
+            for nm, wt, n, k in shapes:
+                t_layer += _time_rows(o, wt, layer[nm], k, xqf if k == F else xqd, frac, nt)
+            t_head = _time_rows(o, o.Q6_K, head, D, xqd, hfrac, nt) * V / head_rows
+            t = L * t_layer + t_head
+            r[f"ms_{label}"] = round(t * 1e3, 1)
+            r[f"gbs_{label}"] = round(wbytes / t / 1e9, 4)
+        rows.append(r)
+    out["llama32_3b_decode_linears"] = {
+        "steps": rows, "weight_gb": round(wbytes / 1e9, 3),
+        "sample": f"one layer's 7 linears x {L} (1 thread: rows 0..n/16 of each, x 16) + LM head rows "
+                  f"0..{head_rows} of {V} (1 thread: 0..{_sub_rows(head_rows, 1.0 / 16)}), scaled to {V}"}
+
+    return {"value": headline, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"decode MMVQ step in full (Q4_K 4096x4096 and 14336x4096 x M in {{1,2,4,8}}, q8_1 quantize "
+                      f"+ fp64 blockwise products) on {cores} threads; per-workload entries in 'workloads'",
+            "wall_s": round(time.perf_counter() - t_begin, 1), "workloads": out}
 
 
 def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is the whole decode MMVQ step
+    (the headline workload, in full) on every host core."""
     if rank != 0:
         return None
-    per = []
+    cores = os.cpu_count() or 1
+    dec = OracleDecode()
     for _ in range(args.warmup):
-        cpu_baseline(budget_s=2.0)
-    for _ in range(args.steps):
-        per.append(cpu_baseline(budget_s=max(2.0, 30.0 / max(args.steps, 1))))
-    v = statistics.median(p["value"] for p in per)
-    cb = dict(per[-1])
-    cb["value"] = v
+        dec.step(cores)
+    t = [dec.step(cores)[1] for _ in range(args.steps)]
+    ms = statistics.median(t) * 1e3
+    v = round(dec.bytes / (ms * 1e-3) / 1e9, 4)
+    sample = (f"decode MMVQ step in full per step (Q4_K 4096x4096 and 14336x4096 x M in {{1,2,4,8}}, q8_1 quantize + "
+              f"fp64 blockwise products) on {cores} threads")
     return {"impl": "reference", "metric": METRIC,
             "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "decode MMVQ: Q4_K 4096x4096 and 14336x4096, bf16 activations M in {1,2,4,8}; "
-                                   "oracle on a bounded row sample per step"},
-            "cpu_baseline": cb,
+                                   "oracle on the host cores"},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -1087,6 +1087,7 @@ inline cudaError_t launch_mmvq_routes_pt(const uint8_t *bank, const MmvqRoutes &
 // pieces (32-value pieces of K > 8192) use 512-thread CTAs.
 struct MmvqTune {
     bool r4_m1;        // M = 1: R = 4 instead of 2
+    bool r8_m1;        // M = 1: R = 8 (overrides r4_m1)
     bool r1_m1;        // M = 1: R = 1 (overrides r4_m1)
     bool tg2_m8;       // 5..8 tokens: two threads per piece
     bool r4_m2;        // 2 tokens: R = 4 instead of 2
@@ -1100,6 +1101,7 @@ inline cudaError_t launch_mmvq_pt(const MmvqSegs &sg, int64_t k, const uint8_t *
     if (P <= 256) {
         if (m <= 1) {
             if (t.r1_m1) return launch_mmvq_cfg<PT, 1, 1, 1, 256>(sg, k, rb, xq, m, yt, s);
+            if (t.r8_m1) return launch_mmvq_cfg<PT, 1, 1, 8, 256>(sg, k, rb, xq, m, yt, s);
             if (t.r4_m1) return launch_mmvq_cfg<PT, 1, 1, 4, 256>(sg, k, rb, xq, m, yt, s);
             return launch_mmvq_cfg<PT, 1, 1, 2, 256>(sg, k, rb, xq, m, yt, s);
         }

@@ -5,7 +5,7 @@ namespace gg {
 
 cudaError_t launch_mmvq_mxfp4(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt, cudaStream_t s) {
     // Q4_0's configuration (the same two-block staged pieces)
-    return launch_mmvq_pt<MX4Piece>(sg, k, xq, m, yt, s, k / 32 * MXFP4_BYTES, MmvqTune{false, false, false, false, true});
+    return launch_mmvq_pt<MX4Piece>(sg, k, xq, m, yt, s, k / 32 * MXFP4_BYTES, MmvqTune{false, false, false, false, false, true});
 }
 
 cudaError_t launch_mmvq_routes_mxfp4(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k,

@@ -13,8 +13,10 @@ cudaError_t launch_mmvq_q4_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, i
     if (m > 8) return mma_q4k_fits(k, m) ? launch_mmvq_mma_q4k(sg, k, xq, m, yt, s) : cudaErrorInvalidValue;
     if (m >= option_mmvq_tc_min_m() && n >= 2048 && option_mmvq_tc() && mma_q4k_fits(k, m))
         return launch_mmvq_mma_q4k(sg, k, xq, m, yt, s);
+    // one token: 8 rows in flight per thread on matrices of 8192 rows or more
+    // (GB300, 18432 rows of 4096: 9.5 us against 11.0 with 4 rows)
     return launch_mmvq_pt<Q4KPiece>(sg, k, xq, m, yt, s, k / 256 * Q4_K_BYTES,
-                                    MmvqTune{n >= 8192, false, true, true, true});
+                                    MmvqTune{n >= 8192, n >= 8192, false, true, true, true});
 }
 
 bool mmvq_tc_wide(int wt, int64_t k, int64_t m) {

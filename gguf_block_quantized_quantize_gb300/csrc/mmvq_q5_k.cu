@@ -8,7 +8,7 @@ cudaError_t launch_mmvq_q5_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, i
     // flight per register set for 1 and 3..4 tokens, four for 2 tokens
     // (14336 rows: 11.2 -> 10.3 us), and 5..8 tokens on one thread per piece
     // (29.2 -> 24.7 us; two threads with 4 tokens each are slower here)
-    return launch_mmvq_pt<Q5KPiece>(sg, k, xq, m, yt, s, k / 256 * Q5_K_BYTES, MmvqTune{false, false, false, true, false});
+    return launch_mmvq_pt<Q5KPiece>(sg, k, xq, m, yt, s, k / 256 * Q5_K_BYTES, MmvqTune{false, false, false, false, true, false});
 }
 
 cudaError_t launch_mmvq_routes_q5_k(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,

@@ -12,7 +12,7 @@ cudaError_t launch_mmvq_q6_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, i
     if (m >= option_mmvq_tc_min_m() && m <= 8 && n >= Q6K_TC_MIN_ROWS && option_mmvq_tc() && mma_q6k_fits(k, m))
         return launch_mmvq_mma_q6k(sg, k, xq, m, yt, s);
     // 5..8 tokens: two threads per piece below 2048 rows; 2 tokens: four rows per group (measured)
-    return launch_mmvq_pt<Q6KPiece>(sg, k, xq, m, yt, s, k / 256 * Q6_K_BYTES, MmvqTune{false, false, n < 2048, n >= 2048, false});
+    return launch_mmvq_pt<Q6KPiece>(sg, k, xq, m, yt, s, k / 256 * Q6_K_BYTES, MmvqTune{false, false, false, n < 2048, n >= 2048, false});
 }
 
 cudaError_t launch_mmvq_routes_q6_k(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k, const uint8_t *xq,

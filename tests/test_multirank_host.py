@@ -64,3 +64,15 @@ def test_reference_arm_runs_on_rank_0_only():
     class A:
         steps, warmup = 1, 3
     assert bench.run_reference(A(), 1, 2) is None     # other ranks exit without work
+
+
+def test_reference_arm_line_on_rank_0():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class A:
+        steps, warmup = 1, 0
+    res = bench.run_reference(A(), 0, 1)
+    assert res["impl"] == "reference" and res["unit"] == "GB/s" and res["value"] > 0
+    assert res["cpu_baseline"]["value"] == res["value"] and res["cpu_baseline"]["kind"] == "oracle"
+    assert res["e2e"] == {"value": res["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
