@@ -112,6 +112,9 @@ static int64_t g_mmq_bn_max = 256;
 static int64_t g_mmq_split_k = 1;   // small m: split K across CTAs (fp32 partial sums) to fill the GPU
 int64_t option_mmq_bn_max() { return g_mmq_bn_max; }
 static int64_t g_moe_down_precise = 0;
+// gate_up GEMM of the grouped MoE path: 1 hi + lo operands (three MMAs per K
+// step), 0 one fp16 operand per side
+static int64_t g_moe_gate_up_precise = 1;
 int64_t option_mmq_stage() { return g_mmq_stage; }
 int64_t option_moe_deterministic() { return g_moe_deterministic; }
 int64_t option_mmvq_tc() { return g_mmvq_tc; }
@@ -458,14 +461,16 @@ static gguf_status check_moe(const gguf_moe_args *a) {
     return GGUF_OK;
 }
 
-// the fp16 operand of the grouped GEMMs: row i (grouped order) is x row
-// route_list[i] / rdiv (rdiv = top_k: token rows; 1: route rows)
+// the fp16 operand of the grouped GEMMs in grouped route order: x row i
+// feeds the routes i * fan + j, j < fan (fan = top_k: token rows; 1: route
+// rows), each written at its expert offset + slot
 static cudaError_t to_f16_operand(const void *x, int xt, int64_t R, int64_t k, int64_t ldx, uint16_t *xh,
-                                  uint16_t *xl, int64_t pitch, const MoeWs &w, int64_t E, int32_t rdiv,
+                                  uint16_t *xl, int64_t pitch, const MoeWs &w, const int32_t *ids, int32_t fan,
                                   cudaStream_t s) {
+    const int64_t rows = R / fan;
     return xt == GGUF_Q8_1
-               ? launch_q8_1_to_f16((const uint8_t *)x, R, k, xh, xl, s, pitch, w.route_list, rdiv, w.offsets + E)
-               : launch_quantize_q8_1(x, xt, R, k, ldx, nullptr, xh, xl, s, pitch, w.route_list, rdiv, w.offsets + E);
+               ? launch_q8_1_to_f16((const uint8_t *)x, rows, k, xh, xl, s, pitch, ids, w.pos, w.offsets, fan)
+               : launch_quantize_q8_1(x, xt, rows, k, ldx, nullptr, xh, xl, s, pitch, ids, w.pos, w.offsets, fan);
 }
 
 size_t gguf_mul_mat_id_ws_size(const gguf_moe_args *args) {
@@ -531,10 +536,11 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
         const size_t ybytes = a->yt == GGUF_Q8_1 ? (size_t)(R * row_size(GGUF_Q8_1, idim)) : (size_t)(R * idim * 2);
         if ((e = cudaMemsetAsync(a->y, 0, ybytes, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id");
         if ((e = moe_group(a->ids, nullptr, R, a->n_experts, false, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id grouping");
-        if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), w, a->n_experts,
+        uint16_t *xl = g_moe_gate_up_precise ? w.xl : nullptr;
+        if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, xl, op_pitch(a->wt, a->k), w, a->ids,
                                 (int32_t)a->top_k, s)) != cudaSuccess)
             return cuda_status(e, "mul_mat_id quantize");
-        e = launch_moe_gate_up((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, w.xl, a->top_k, R,
+        e = launch_moe_gate_up((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, xl, a->top_k, R,
                                a->n_experts, w, a->yt == GGUF_Q8_1 ? (uint8_t *)a->y : nullptr,
                                a->yt == GGUF_BF16 ? (uint16_t *)a->y : nullptr,
                                a->yt == GGUF_F16 ? (uint16_t *)a->y : nullptr, nullptr, a->n / 2, false, s);
@@ -543,7 +549,7 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
     if (plain) {   // token rows, one output row per route
         if ((e = moe_group(a->ids, nullptr, R, a->n_experts, false, a->dev_status, w, bn, s)) != cudaSuccess)
             return cuda_status(e, "mul_mat_id grouping");
-        if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), w, a->n_experts,
+        if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), w, a->ids,
                                 (int32_t)a->top_k, s)) != cudaSuccess)
             return cuda_status(e, "mul_mat_id quantize");
         if ((e = launch_moe_down((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, w.xl, a->top_k, R,
@@ -553,7 +559,7 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
                            "mul_mat_id store");
     }
     if ((e = moe_group(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "mul_mat_id grouping");
-    if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), w, a->n_experts, 1, s)) !=
+    if ((e = to_f16_operand(a->x, a->xt, R, a->k, a->ldx, w.xh, w.xl, op_pitch(a->wt, a->k), w, a->ids, 1, s)) !=
         cudaSuccess)
         return cuda_status(e, "mul_mat_id quantize");
     return cuda_status(grouped_down_sum((const uint8_t *)a->w, a->wt, a->expert_stride, a->n, a->k, w.xh, w.xl,
@@ -626,11 +632,12 @@ gguf_status gguf_moe_ffn(const gguf_moe_ffn_args *a, void *ws, size_t ws_bytes, 
     }
     // one grouping serves both GEMMs; a route of weight 0 contributes nothing and is skipped by both
     if ((e = moe_group(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w, bn, s)) != cudaSuccess) return cuda_status(e, "moe_ffn grouping");
-    if ((e = to_f16_operand(a->x, a->xt, R, a->hidden, a->ldx, w.xh, w.xl, op_pitch(a->gate_up_type, a->hidden), w,
-                            a->n_experts, (int32_t)a->top_k, s)) != cudaSuccess)
+    uint16_t *xl = g_moe_gate_up_precise ? w.xl : nullptr;
+    if ((e = to_f16_operand(a->x, a->xt, R, a->hidden, a->ldx, w.xh, xl, op_pitch(a->gate_up_type, a->hidden), w,
+                            a->ids, (int32_t)a->top_k, s)) != cudaSuccess)
         return cuda_status(e, "moe_ffn quantize");
     if ((e = launch_moe_gate_up((const uint8_t *)a->w_gate_up, a->gate_up_type, a->gate_up_stride, 2 * a->inter,
-                                a->hidden, w.xh, w.xl, a->top_k, R, a->n_experts, w, nullptr, nullptr, w.h16, w.h16lo,
+                                a->hidden, w.xh, xl, a->top_k, R, a->n_experts, w, nullptr, nullptr, w.h16, w.h16lo,
                                 op_pitch(a->down_type, a->inter), true, s)) != cudaSuccess)
         return cuda_status(e, "moe_ffn gate_up");
     return cuda_status(grouped_down_sum((const uint8_t *)a->w_down, a->down_type, a->down_stride, a->hidden, a->inter,
@@ -701,6 +708,10 @@ gguf_status gguf_set_option(const char *key, int64_t value) {
         g_moe_down_precise = value != 0;
         return GGUF_OK;
     }
+    if (!strcmp(key, "moe_gate_up_precise")) {
+        g_moe_gate_up_precise = value != 0;
+        return GGUF_OK;
+    }
     return fail(GGUF_ERR_INVALID_ARG, "set_option: unknown key '%s'", key);
 }
 
@@ -715,6 +726,7 @@ int64_t gguf_get_option(const char *key) {
     if (!strcmp(key, "mmq_stage")) return g_mmq_stage;
     if (!strcmp(key, "moe_deterministic")) return g_moe_deterministic;
     if (!strcmp(key, "moe_down_precise")) return g_moe_down_precise;
+    if (!strcmp(key, "moe_gate_up_precise")) return g_moe_gate_up_precise;
     if (!strcmp(key, "mmq_bn_max")) return g_mmq_bn_max;
     if (!strcmp(key, "mmq_split_k")) return g_mmq_split_k;
     return -1;

@@ -29,15 +29,19 @@ gguf_status report(gguf_status st, const char *msg);
 // xh[m][pitch] = fp16(d16*q) when xh != nullptr, and its low part
 // xl = fp16(d16*q - xh) when xl != nullptr.  pitch > k appends the Q4_K
 // / Q5_K min-term correction columns (see op_pitch) and zero padding.
-// rmap (optional, device): output row r is input row rmap[r] / rdiv, for the
-// rows r < *rcount (device); the rows past it are not written.
+// ids (optional, device; with the MoE grouping's pos and offsets): the fp16
+// operand is written in grouped route order, input row i feeding the routes
+// r = i * fan + j (j < fan); an active route (pos[r] >= 0) goes to operand
+// row offsets[ids[r]] + pos[r], a skipped one nowhere.  Each input row is
+// quantized once.
 cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int64_t ldx, uint8_t *xq,
                                  uint16_t *xh, uint16_t *xl, cudaStream_t s, int64_t pitch = 0,
-                                 const int32_t *rmap = nullptr, int32_t rdiv = 1, const int32_t *rcount = nullptr);
+                                 const int32_t *ids = nullptr, const int32_t *pos = nullptr,
+                                 const int32_t *offsets = nullptr, int32_t fan = 1);
 // the same fp16 operand(s) from q8_1 rows
 cudaError_t launch_q8_1_to_f16(const uint8_t *xq, int64_t m, int64_t k, uint16_t *xh, uint16_t *xl, cudaStream_t s,
-                               int64_t pitch = 0, const int32_t *rmap = nullptr, int32_t rdiv = 1,
-                               const int32_t *rcount = nullptr);
+                               int64_t pitch = 0, const int32_t *ids = nullptr, const int32_t *pos = nullptr,
+                               const int32_t *offsets = nullptr, int32_t fan = 1);
 // Row length of the tensor-core operand for weight type wt: k, plus for the
 // affine K-quants (Q4_K, Q5_K) one min-term correction column per 32-block,
 // rounded up to the 64-value K step.

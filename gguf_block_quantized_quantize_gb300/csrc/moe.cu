@@ -23,9 +23,9 @@
 // as one 2-D box per K-step; the last tile of an expert issues the MMA with N
 // rounded up to 16 only.
 // The activation operand is written in grouped route order (the conversion
-// to the fp16 operand reads each row through route_list), so an expert's
-// routes are consecutive rows and a tile loads them with plain 2-D bulk
-// tensor copies instead of per-row gathers.
+// quantizes each token row once and writes it to the grouped row of each of
+// its active routes), so an expert's routes are consecutive rows and a tile
+// loads them with plain 2-D bulk tensor copies instead of per-row gathers.
 //   gate_up : the A tile holds 64 gate rows i and the 64 matching up rows I+i,
 //             so the epilogue has g and u of the same (route, i): it computes
 //             h = silu(g) * u in fp32, rounds it to bf16 (the activation dtype),
@@ -311,8 +311,9 @@ static TgParams moe_params(const uint8_t *w, int wt, int64_t expert_stride, int6
     return p;
 }
 
-// gate_up (+ SwiGLU + q8_1): the intermediate is re-quantized, so the product
-// runs in the precise (hi + lo) mode; xh / xl: token rows [T][k]
+// gate_up (+ SwiGLU + q8_1); xh / xl: the operand rows in grouped route order
+// [R][kx]; with xl (the low parts) the product runs in the precise (hi + lo)
+// mode, else on one fp16 operand per side
 cudaError_t launch_moe_gate_up(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
                                const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
                                const MoeWs &ws, uint8_t *hq, uint16_t *hbf, uint16_t *h16, uint16_t *h16lo,
@@ -327,13 +328,14 @@ cudaError_t launch_moe_gate_up(const uint8_t *w, int wt, int64_t expert_stride, 
     p.h16 = h16;
     p.h16lo = h16lo;
     p.m = R / top_k;
-    return launch_moe_mode<TG_MOE_GATE_UP, true>(wt, p, R, E, s);
+    return xl ? launch_moe_mode<TG_MOE_GATE_UP, true>(wt, p, R, E, s)
+              : launch_moe_mode<TG_MOE_GATE_UP, false>(wt, p, R, E, s);
 }
 
 // down: z[R][n] = W[e] . x[route] for every grouped route, or, with ysum,
-// ysum[t][n] += route_w[r] * (W[e] . x[route]) (fp32 atomics into zeroed token
-// rows); xh / xl: the operand rows in grouped route order [R][kx] (xl only in
-// the precise mode)
+// ysum[t][n] += route_w[r] * (W[e] . x[route]) into zeroed token rows (bulk
+// reduce-adds of the staged rows when n % 4 == 0, else fp32 atomics); xh / xl:
+// the operand rows in grouped route order [R][kx] (xl only in the precise mode)
 cudaError_t launch_moe_down(const uint8_t *w, int wt, int64_t expert_stride, int64_t n, int64_t k,
                             const uint16_t *xh, const uint16_t *xl, int64_t top_k, int64_t R, int64_t E,
                             const MoeWs &ws, float *z, bool precise, cudaStream_t s, float *ysum,
@@ -344,6 +346,7 @@ cudaError_t launch_moe_down(const uint8_t *w, int wt, int64_t expert_stride, int
     p.yacc = z;
     p.zrows = R;
     p.ysum = ysum;
+    p.ysum_bulk = ysum && n % 4 == 0 && (reinterpret_cast<uintptr_t>(ysum) & 15) == 0;
     p.route_w = route_w;
     p.m = R / top_k;
     return precise ? launch_moe_mode<TG_MOE_DOWN, true>(wt, p, R, E, s)

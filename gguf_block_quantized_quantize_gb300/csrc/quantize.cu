@@ -73,19 +73,39 @@ __device__ __forceinline__ void write_correction(uint16_t *hi_row, uint16_t *lo_
     }
 }
 
-// Row map of the permuted operand (MoE): output row r is input row
-// rmap[r] / rdiv; rows at or past *rcount are not written.
-struct RowMap {
-    const int32_t *rmap;
-    int32_t rdiv;
-    const int32_t *rcount;
+// Scatter of the permuted operand (MoE): input row i feeds the routes
+// r = i * fan + j (j < fan); an active route (pos[r] >= 0) is written to row
+// offsets[ids[r]] + pos[r] of the output (grouped route order), a skipped one
+// nowhere.  ids == nullptr: output row i is input row i.
+struct RowScatter {
+    const int32_t *ids, *pos, *offsets;
+    int32_t fan;
 };
+
+// the fp16 operand row(s) of one 8-value group: row i, or every active
+// route's grouped row
+__device__ __forceinline__ void write_operand_rows(const RowScatter &map, int64_t row, int64_t k, int64_t pitch,
+                                                   int64_t b, int j, float d16, const int q[8], int sum,
+                                                   uint16_t s16, uint16_t *xh, uint16_t *xl) {
+    for (int f = 0; f < (map.ids ? map.fan : 1); f++) {
+        int64_t orow = row;
+        if (map.ids) {
+            const int64_t r = row * map.fan + f;
+            const int32_t pr = map.pos[r];
+            if (pr < 0) continue;
+            orow = (int64_t)map.offsets[map.ids[r]] + pr;
+        }
+        write_f16_operand(d16, q, xh + orow * pitch + b * QK8 + 8 * j, xl ? xl + orow * pitch + b * QK8 + 8 * j : nullptr);
+        if (pitch > k)
+            write_correction(xh + orow * pitch, xl ? xl + orow * pitch : nullptr, k, pitch, b, j, d16, sum, s16);
+    }
+}
 
 template <int XT, bool VEC>
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restrict__ x, int64_t m, int64_t k,
                                                             int64_t ldx, uint8_t *__restrict__ xq,
                                                             uint16_t *__restrict__ xh, uint16_t *__restrict__ xl,
-                                                            int64_t pitch, RowMap map) {
+                                                            int64_t pitch, RowScatter map) {
     // launched as a programmatic dependent: let the next kernel start its own
     // independent prefetch, and wait for the previous kernel before touching
     // memory it may still read or write
@@ -96,17 +116,12 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restri
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t blk = g >> 2;
     const int j = (int)(g & 3);
-    bool active = blk < total;
+    const bool active = blk < total;
     const int64_t row = active ? blk / nb : 0;
     const int64_t b = active ? blk - row * nb : 0;
-    int64_t src = row;
-    if (map.rmap != nullptr) {   // uniform over the 4 threads of a block
-        active = active && row < *map.rcount;
-        src = active ? map.rmap[row] / map.rdiv : 0;
-    }
 
     float v[8];
-    if (active) load8<XT, VEC>(x, src * ldx + b * QK8 + 8 * j, v);
+    if (active) load8<XT, VEC>(x, row * ldx + b * QK8 + 8 * j, v);
     else {
 #pragma unroll
         for (int i = 0; i < 8; i++) v[i] = 0.0f;
@@ -141,46 +156,34 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restri
             *reinterpret_cast<uint32_t *>(o) = (uint32_t)dh | ((uint32_t)sh << 16);
         }
     }
-    if (xh != nullptr) {
-        write_f16_operand(h2f(dh), q, xh + row * pitch + b * QK8 + 8 * j, xl ? xl + row * pitch + b * QK8 + 8 * j : nullptr);
-        if (pitch > k)
-            write_correction(xh + row * pitch, xl ? xl + row * pitch : nullptr, k, pitch, b, j, h2f(dh), sum,
-                             f2h_rn(__fmul_rn(d, (float)sum)));
-    }
+    if (xh != nullptr)
+        write_operand_rows(map, row, k, pitch, b, j, h2f(dh), q, sum, f2h_rn(__fmul_rn(d, (float)sum)), xh, xl);
 }
 
 __global__ void __launch_bounds__(256) q8_1_to_f16_kernel(const uint8_t *__restrict__ xq, int64_t m, int64_t k,
                                                           uint16_t *__restrict__ xh, uint16_t *__restrict__ xl,
-                                                          int64_t pitch, RowMap map) {
+                                                          int64_t pitch, RowScatter map) {
     const int64_t nb = k / QK8;
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t blk = g >> 2;
     const int j = (int)(g & 3);
     if (blk >= m * nb) return;
-    int64_t src_blk = blk;
-    if (map.rmap != nullptr) {
-        const int64_t r = blk / nb;
-        if (r >= *map.rcount) return;
-        src_blk = (int64_t)(map.rmap[r] / map.rdiv) * nb + (blk - r * nb);
-    }
-    const uint8_t *p = xq + src_blk * Q8_1_BYTES;
+    const uint8_t *p = xq + blk * Q8_1_BYTES;
     const float d16 = h2f(ld_u16(p));
     const uint32_t w0 = ld_u32(p + 4 + 8 * j), w1 = ld_u32(p + 8 + 8 * j);
     int q[8];
 #pragma unroll
     for (int i = 0; i < 4; i++) { q[i] = (int8_t)(w0 >> (8 * i)); q[4 + i] = (int8_t)(w1 >> (8 * i)); }
     const int64_t row = blk / nb, b = blk - row * nb;
-    write_f16_operand(d16, q, xh + row * pitch + b * QK8 + 8 * j, xl ? xl + row * pitch + b * QK8 + 8 * j : nullptr);
-    if (pitch > k) {
-        int sum = 0;
+    int sum = 0;
+    if (pitch > k)
         for (int t = 0; t < 32; t++) sum += (int8_t)p[4 + t];
-        write_correction(xh + row * pitch, xl ? xl + row * pitch : nullptr, k, pitch, b, j, d16, sum, ld_u16(p + 2));
-    }
+    write_operand_rows(map, row, k, pitch, b, j, d16, q, sum, ld_u16(p + 2), xh, xl);
 }
 
 cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int64_t ldx, uint8_t *xq,
-                                 uint16_t *xh, uint16_t *xl, cudaStream_t s, int64_t pitch, const int32_t *rmap,
-                                 int32_t rdiv, const int32_t *rcount) {
+                                 uint16_t *xh, uint16_t *xl, cudaStream_t s, int64_t pitch, const int32_t *ids,
+                                 const int32_t *pos, const int32_t *offsets, int32_t fan) {
     if (pitch < k) pitch = k;
     const int64_t threads = m * (k / QK8) * 4;
     if (threads == 0) return cudaSuccess;
@@ -196,7 +199,7 @@ cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, in
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const RowMap map{rmap, rdiv < 1 ? 1 : rdiv, rcount};
+    const RowScatter map{ids, pos, offsets, fan < 1 ? 1 : fan};
 #define QLAUNCH(XT, V) (void)cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<XT, V>, x, m, k, ldx, xq, xh, xl, pitch, map)
     if (xt == GGUF_F32) { if (vec) QLAUNCH(GGUF_F32, true); else QLAUNCH(GGUF_F32, false); }
     else if (xt == GGUF_BF16) { if (vec) QLAUNCH(GGUF_BF16, true); else QLAUNCH(GGUF_BF16, false); }
@@ -206,12 +209,13 @@ cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, in
 }
 
 cudaError_t launch_q8_1_to_f16(const uint8_t *xq, int64_t m, int64_t k, uint16_t *xh, uint16_t *xl, cudaStream_t s,
-                               int64_t pitch, const int32_t *rmap, int32_t rdiv, const int32_t *rcount) {
+                               int64_t pitch, const int32_t *ids, const int32_t *pos, const int32_t *offsets,
+                               int32_t fan) {
     if (pitch < k) pitch = k;
     const int64_t threads = m * (k / QK8) * 4;
     if (threads == 0) return cudaSuccess;
     q8_1_to_f16_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(xq, m, k, xh, xl, pitch,
-                                                                        RowMap{rmap, rdiv < 1 ? 1 : rdiv, rcount});
+                                                                        RowScatter{ids, pos, offsets, fan < 1 ? 1 : fan});
     return cudaGetLastError();
 }
 

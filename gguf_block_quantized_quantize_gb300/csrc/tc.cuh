@@ -117,6 +117,14 @@ __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_
                  "r"(smem_u32(ssrc)), "r"(bytes)
                  : "memory");
 }
+// bytes (a multiple of 16; both addresses 16-byte aligned) of fp32 values in
+// shared memory added element by element into global memory, performed at L2
+__device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, const float *ssrc, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(gdst)),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // wait until at most N of the thread's bulk groups still read shared memory
 template <int N>

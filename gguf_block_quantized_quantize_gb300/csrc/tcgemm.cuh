@@ -79,6 +79,8 @@ struct TgParams {
     float *yacc;  // split-K partial sums [m][n] (dense), or the MoE down per-route outputs in grouped
                   // order, as ceil(n / 128) blocks [zrows][128]
     float *ysum;  // MoE down with the fused weighted sum: fp32 token rows [T][n], zeroed before the call
+    int ysum_bulk;  // 1: the weighted rows are added by bulk reduce-adds (n % 4 == 0, ysum 16-byte aligned);
+                    // 0: by scalar fp32 atomics
     int64_t zrows;  // MoE down: rows (routes) of one 128-column block of yacc
     int ystore;     // dense: the output is written by bulk tensor stores through map_y
     // gathered activation rows (MoE)
@@ -716,6 +718,9 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                 }
             } else if (MODE == TG_MOE_DOWN) {
                 const int64_t orow = d.row0 + 32 * q + lane;
+                // the chunk's rows leave through a staging buffer: bulk copies into z,
+                // or bulk reduce-adds of the weighted rows into the token rows
+                const bool staged = !p.ysum || p.ysum_bulk;
 #pragma unroll
                 for (int c = 0; c < BN / 32; c++) {
                     // the chunk count is the same in the 4 warps (they meet at named
@@ -726,9 +731,10 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                     const float w_l = wv[c];
                     const int rows = d.n_eff - 32 * c < 32 ? d.n_eff - 32 * c : 32;
                     float *ob = xbuf + (ochunk & 1) * (32 * 128);
-                    if (!p.ysum) {
-                        // the buffer's previous bulk store has read it
-                        if (warp == 10 && lane == 0) tc::bulk_wait_read<1>();
+                    if (staged) {
+                        // the buffer's previous bulk copies have read it (each lane of
+                        // warp 10 waits for its own)
+                        if (warp == 10) tc::bulk_wait_read<1>();
                         tg_named_bar(2, 128);
                     }
                     if (go) {
@@ -738,7 +744,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
 #pragma unroll
                         for (int jj = 0; jj < 32; jj++) rr[jj] = 0u;
                     }
-                    if (p.ysum) {
+                    if (!staged) {
 #pragma unroll
                         for (int jj = 0; jj < 32; jj++) {
                             if (go && jj < rows) {  // uniform within the warp
@@ -755,13 +761,27 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                         // grouped positions: the chunk's rows of this column block are one
                         // contiguous run, written by one bulk copy from the staging buffer
 #pragma unroll
-                        for (int jj = 0; jj < 32; jj++) ob[jj * 128 + 32 * q + lane] = __uint_as_float(rr[jj]);
+                        for (int jj = 0; jj < 32; jj++) {
+                            const float wr = __shfl_sync(0xffffffffu, w_l, jj);   // 1 without ysum
+                            ob[jj * 128 + 32 * q + lane] = wr * __uint_as_float(rr[jj]);
+                        }
                         tc::fence_proxy_async_smem();
                         tg_named_bar(2, 128);
-                        if (warp == 10 && lane == 0 && go) {
-                            float *dst = p.yacc + (((int64_t)(d.row0 >> 7) * p.zrows + d.route0 + 32 * c) << 7);
-                            tc::bulk_store(dst, ob, (uint32_t)rows * 512u);
-                            tc::bulk_commit();
+                        if (warp == 10 && go) {
+                            if (p.ysum) {
+                                // lane l adds route row l (weighted) into its token's row:
+                                // the tile's columns, clipped at n
+                                if (lane < rows) {
+                                    const int64_t cols = p.n - d.row0 < 128 ? p.n - d.row0 : 128;
+                                    tc::bulk_reduce_add_f32(p.ysum + (int64_t)(rt_l / p.top_k) * p.n + d.row0,
+                                                            ob + lane * 128, (uint32_t)cols * 4u);
+                                }
+                                tc::bulk_commit();
+                            } else if (lane == 0) {
+                                float *dst = p.yacc + (((int64_t)(d.row0 >> 7) * p.zrows + d.route0 + 32 * c) << 7);
+                                tc::bulk_store(dst, ob, (uint32_t)rows * 512u);
+                                tc::bulk_commit();
+                            }
                         }
                         ochunk++;
                     }
@@ -802,7 +822,9 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                                 const int il = 32 * hb + lane;
                                 const int64_t icol = d.row0 + il;  // column of h
                                 const float gv = xg[jj * 64 + il], uv = xu[jj * 64 + il];
-                                const float hf = gv / (1.0f + expf(-gv)) * uv;
+                                // silu in fp32 with the fast exponential and division (a few ulp of
+                                // fp32, far below the bf16 rounding of h that follows)
+                                const float hf = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
                                 const uint16_t hbits = f2bf_rn(hf);
                                 const float hx = bf2f(hbits);  // the intermediate in the activation dtype
                                 if (p.hbf) p.hbf[rt * idim + icol] = hbits;
@@ -853,8 +875,9 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             tc::mbar_arrive(&tempty[b]);
             if (!ok) break;
         }
-        // bulk output stores finish before the CTA's shared memory is released
-        if (lane == 0) tc::bulk_wait_all();
+        // bulk output copies finish before the CTA's shared memory is released
+        // (each lane waits for the groups it committed)
+        tc::bulk_wait_all();
     } else if (lane == 0 && p.pstages > 0) {
         // ================= packed-weight loader: chunk c of a tile (K-steps
         // [c * pkc, (c + 1) * pkc) of its weight steps) into buffer pc % pstages:

@@ -396,6 +396,26 @@ gguf_status gguf_debug_block_dots(const void *w, int wt, int64_t n, int64_t k, c
  *                   tensor-core MMVQ (2 or 4 n-tiles of 8 tokens) instead
  *                   of MMQ; 8 .. 32, default 16 (the measured crossover on
  *                   GB300: 4 n-tiles are not faster than MMQ).
+ *   "mmq_stage"   : 1 (default) lets the tensor-core GEMMs (MMQ and the
+ *                   grouped MoE GEMMs) stage packed weight rows in shared
+ *                   memory by bulk tensor copies where the rows' layout allows
+ *                   it; 0 has the producer warps load them from global memory.
+ *   "mmq_bn_max"  : widest activation tile of the dense MMQ, 128 or 256
+ *                   (default 256).  Tiles of at most 128 rows keep the weight
+ *                   operand in tensor memory.
+ *   "mmq_split_k" : 1 (default) lets MMQ calls with few output tiles split K
+ *                   across CTAs (fp32 partial sums, then one conversion).
+ *   "moe_deterministic": 1 (default) keeps the grouped down GEMM's per-route
+ *                   rows and sums each token's routes in slot order afterwards
+ *                   (the same bits on every run); 0 adds the weighted rows into
+ *                   fp32 token rows inside the GEMM's epilogue (bulk
+ *                   reduce-adds, or fp32 atomics when n % 4 != 0), whose
+ *                   summation order varies from run to run.
+ *   "moe_down_precise": 1 runs the grouped down GEMM on hi + lo operands for
+ *                   16-bit outputs too (fp32 outputs always do); default 0.
+ *   "moe_gate_up_precise": 1 (default) runs the grouped gate_up GEMM on hi + lo
+ *                   operands (three MMAs per K step); 0 on one fp16 operand
+ *                   per side.
  * Returns GGUF_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 gguf_status gguf_set_option(const char *key, int64_t value);

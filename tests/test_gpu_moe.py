@@ -71,7 +71,18 @@ def _small_case(safe=False):
     return E, K, H, I, T, bank_gu, bank_d, ids, rw, x
 
 
-def test_gate_up_swiglu_bf16_and_q8_1(g, path):
+@pytest.fixture(params=[1, 0])
+def gate_up_precise(request, g):
+    """The grouped gate_up GEMM on hi + lo operands (option
+    moe_gate_up_precise = 1, three MMAs per K step) and on one fp16 operand
+    per side (0)."""
+    saved = g.gguf_get_option("moe_gate_up_precise")
+    g.gguf_set_option("moe_gate_up_precise", request.param)
+    yield request.param
+    g.gguf_set_option("moe_gate_up_precise", saved)
+
+
+def test_gate_up_swiglu_bf16_and_q8_1(g, path, gate_up_precise):
     E, K, H, I, T, bank_gu, _, ids, rw, x = _small_case()
     sgu = bank_gu.nbytes // E
     xq = oracle.quantize_q8_1(x.float().numpy())
@@ -432,24 +443,28 @@ def _e2e_error_stats(y, ref):
             "n": int(e.size)}
 
 
-@pytest.mark.parametrize("T,vec", [(8192, False), (256, True)])
-def test_moe_full_size_error_distribution(g, T, vec):
+@pytest.mark.parametrize("T,vec,precise", [(8192, False, 1), (8192, False, 0), (256, True, 1)])
+def test_moe_full_size_error_distribution(g, T, vec, precise):
     """Per-element error of the fused FFN against the full oracle chain on the
     full-size expert block (E = 256, top-8, H = 2048, I = 512): 64 tokens,
-    the first 16, the last 16 and 32 spread between (printed with -s)."""
+    the first 16, the last 16 and 32 spread between (printed with -s); the
+    tensor-core path with the gate_up GEMM on hi + lo operands and on one
+    fp16 operand per side."""
     E, K, H, I = 256, 8, 2048, 512
     bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 700, True)
     bank_d = _bank(oracle.Q6_K, E, H, I, 701, True)
     sgu, sd = bank_gu.nbytes // E, bank_d.nbytes // E
     ids, rw = synth.routes(T, E, K, seed=2)
     x = synth.activations(T, H, seed=1, dtype=torch.bfloat16)
-    saved = g.gguf_get_option("moe_vec_max_tokens")
+    saved = (g.gguf_get_option("moe_vec_max_tokens"), g.gguf_get_option("moe_gate_up_precise"))
     g.gguf_set_option("moe_vec_max_tokens", 256 if vec else 0)
+    g.gguf_set_option("moe_gate_up_precise", precise)
     try:
         y = g.gguf_moe_ffn(_u8(bank_gu), g.Q4_K, sgu, _u8(bank_d), g.Q6_K, sd, E, H, I, x.to(DEV), _u8(ids),
                            _u8(rw)).float().cpu().numpy()
     finally:
-        g.gguf_set_option("moe_vec_max_tokens", saved)
+        g.gguf_set_option("moe_vec_max_tokens", saved[0])
+        g.gguf_set_option("moe_gate_up_precise", saved[1])
     toks = sorted(set(list(range(16)) + list(range(T - 16, T)) +
                       np.random.default_rng(5).choice(np.arange(16, T - 16), 32, replace=False).tolist()))
     xq = oracle.quantize_q8_1(x[toks].float().numpy())
@@ -457,8 +472,12 @@ def test_moe_full_size_error_distribution(g, T, vec):
     _, hq = oracle.moe_gate_up(oracle.Q4_K, bank_gu, E, sgu, 2 * I, H, xq, sub_ids, nthreads=16)
     ref = oracle.moe_down(oracle.Q6_K, bank_d, E, sd, H, I, hq, sub_ids, sub_rw, nthreads=16)
     st = _e2e_error_stats(y[toks], ref)
-    print(f"\nmoe e2e error T={T} {'vector' if vec else 'tensor-core'}: {st}")
-    assert_close_moe_e2e(y[toks], ref, f"moe e2e T={T}", TOL_MOE_E2E_ELEM_VEC if vec else TOL_MOE_E2E_ELEM)
+    print(f"\nmoe e2e error T={T} {'vector' if vec else 'tensor-core'} gate_up precise={precise}: {st}")
+    # one fp16 operand per side in gate_up (opt-in): measured max 2.0e-2, p99 8.6e-3
+    # elementwise at this size, against 1.0e-2 / 3.4e-3 on hi + lo operands; only
+    # the per-token norm-wise bound is asserted for it
+    tol = TOL_MOE_E2E_ELEM_VEC if vec else (TOL_MOE_E2E_ELEM if precise else None)
+    assert_close_moe_e2e(y[toks], ref, f"moe e2e T={T}", tol)
 
 
 def test_device_error_word_is_clear_after_moe(g, path):
@@ -506,9 +525,10 @@ def test_moe_staged_weights(g, H, I, down):
 
 
 def test_moe_deterministic_option(g):
-    """Option moe_deterministic = 1: per-route rows summed in slot order, the
-    same bits on every run; the default fused atomic sum agrees with it to
-    fp32 rounding of the sum's order (then bf16 output rounding)."""
+    """Option moe_deterministic = 1 (the default): per-route rows summed in
+    slot order, the same bits on every run; 0: the weighted rows added into
+    the token rows by bulk reduce-adds in the down GEMM's epilogue, which
+    agrees with it to fp32 rounding of the sum's order."""
     E, K, H, I, T = 9, 8, 512, 256, 400
     bank_gu = _bank(oracle.Q4_K, E, 2 * I, H, 950, True)
     bank_d = _bank(oracle.Q6_K, E, H, I, 951, True)
@@ -533,3 +553,36 @@ def test_moe_deterministic_option(g):
     _, hq = oracle.moe_gate_up(oracle.Q4_K, bank_gu, E, sgu, 2 * I, H, xq, ids, nthreads=8)
     ref = oracle.moe_down(oracle.Q6_K, bank_d, E, sd, H, I, hq, ids, rw, nthreads=8)
     assert_close_moe_e2e(y3, ref, "moe fp32 out, fused sum")
+
+
+@pytest.mark.parametrize("n", [510, 500])
+def test_down_fused_sum_row_lengths(g, n):
+    """The fused weighted sum (option moe_deterministic = 0) for output rows
+    whose length is a multiple of 4 (bulk reduce-adds of 16-byte runs) and one
+    that is not (fp32 atomics), against the oracle; a partial last column tile
+    in both."""
+    E, K, T, I = 6, 4, 150, 256
+    packed = _bank(oracle.Q6_K, E, n, I, 960, safe=True).reshape(E, -1)
+    sd = (packed.shape[1] + 15) // 16 * 16     # expert matrices on 16-byte boundaries
+    bank_d = np.zeros((E, sd), dtype=np.uint8)
+    bank_d[:, :packed.shape[1]] = packed
+    bank_d = bank_d.reshape(-1)
+    ids, rw = synth.routes(T, E, K, seed=43)
+    ids[0] = [3, 3, 1, 1]
+    ids[1, 2] = -1
+    rw[2, 1] = 0.0
+    hq = oracle.quantize_q8_1(synth.normal((T * K, I), 1.0, seed=44))
+    ref = oracle.moe_down(oracle.Q6_K, bank_d, E, sd, n, I, hq, ids, rw)
+    saved = (g.gguf_get_option("moe_deterministic"), g.gguf_get_option("moe_vec_max_tokens"))
+    g.gguf_set_option("moe_vec_max_tokens", 0)
+    try:
+        out = {}
+        for det in (1, 0):
+            g.gguf_set_option("moe_deterministic", det)
+            out[det] = g.gguf_mul_mat_id(_u8(bank_d), g.Q6_K, E, sd, n, I, _u8(hq), _u8(ids), g.DOWN_WEIGHTED_SUM,
+                                         route_w=_u8(rw), xt=g.Q8_1, out_type=g.F32).cpu().numpy()
+    finally:
+        g.gguf_set_option("moe_deterministic", saved[0])
+        g.gguf_set_option("moe_vec_max_tokens", saved[1])
+    assert_close(out[0], ref, TOL_F32, f"fused weighted sum n={n}")
+    assert_close(out[0], out[1], 1e-5, f"fused vs slot-order sum n={n}")
