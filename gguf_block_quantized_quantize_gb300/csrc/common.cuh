@@ -35,7 +35,28 @@ __device__ __forceinline__ void store_out(void *out, int ot, int64_t idx, float 
 }
 
 // signed x signed 4-way byte dot product with accumulate
+// Exact fp32 value of an integer on the full-rate pipes instead of the
+// conversion unit (a quarter of the FMA rate or less): the bits of
+// 1.5 * 2^23 + v are that float exactly while |v| < 2^22 (every per-block
+// dot sum here: at most 32 * 255 * 127 in magnitude), and so are those of
+// 2^23 + b for a byte b.
+constexpr float kI2fBias = 12582912.0f;   // 1.5 * 2^23
+__device__ __forceinline__ float i2f_bits(int v) { return __int_as_float(0x4B400000 + v); }   // = kI2fBias + v
+__device__ __forceinline__ float i2f22(int v) { return i2f_bits(v) - kI2fBias; }
+// byte i of w as an exact float
+__device__ __forceinline__ float u8f(uint32_t w, int i) {
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, (uint32_t)i | (4u << 4) | (4u << 8) | (7u << 12))) - 8388608.0f;
+}
+
 __device__ __forceinline__ int dp4a_ss(int a, int b, int c) { return __dp4a(a, b, c); }
+
+// asynchronous 4-byte global -> shared copy (both 4-byte aligned); the thread's
+// copies are complete after cp_async_wait_all
+__device__ __forceinline__ void cp_async4(void *sdst, const void *gsrc) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(sdst)), "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // unsigned (a) x signed (b) 4-way byte dot product with accumulate
 __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
     int d;

@@ -261,7 +261,7 @@ struct Q80Piece {
             int S = 0;
 #pragma unroll
             for (int i = 0; i < 8; i++) S = dp4a_ss((int)w.q[i], a.q[mm][i], S);
-            acc[mm] = fmaf(d * a.f[mm], (float)S, acc[mm]);
+            acc[mm] = fmaf(d * a.f[mm], i2f22(S), acc[mm]);
         }
     }
 };
@@ -386,7 +386,7 @@ struct Q40Piece {
                     S = dp4a_us(lo[4 * b + i], a.q[mm][8 * b + i], S);
                     S = dp4a_us(hi[4 * b + i], a.q[mm][8 * b + 4 + i], S);
                 }
-                v = fmaf(d[b] * a.f[mm][b], (float)S, v);
+                v = fmaf(d[b] * a.f[mm][b], i2f22(S), v);
             }
             acc[mm] = v;
         }
@@ -518,7 +518,7 @@ struct MX4Piece {
                 int S = -a.sum[mm][b];
 #pragma unroll
                 for (int i = 0; i < 8; i++) S = dp4a_us(u[8 * b + i], a.q[mm][8 * b + i], S);
-                v = fmaf(d[b] * a.f[mm][b], (float)S, v);
+                v = fmaf(d[b] * a.f[mm][b], i2f22(S), v);
             }
             acc[mm] = v;
         }
@@ -599,10 +599,10 @@ struct Q4KPiece {
         const uint32_t wq = __byte_perm(w.h.w, 0u, q.sel_w);
         // bytes (s0, s1, m0, m1), each 6 bits
         const uint32_t sm = (r & q.m1) | ((r >> 2) & q.m2) | (wq & q.m3) | ((wq >> 4) & q.m4);
-        const float ds0 = d * (float)(sm & 0xff);
+        const float ds0 = d * u8f(sm, 0);
         // high nibbles are used in place (16 * q), so their scale carries 1/16 (exact)
-        const float ds1 = d * (float)((sm >> 8) & 0xff) * 0.0625f;
-        const float fm0 = (float)((sm >> 16) & 0xff), fm1 = (float)(sm >> 24);
+        const float ds1 = d * u8f(sm, 1) * 0.0625f;
+        const float fm0 = u8f(sm, 2), fm1 = u8f(sm, 3);
         const uint32_t raw[8] = {w.a.x, w.a.y, w.a.z, w.a.w, w.b.x, w.b.y, w.b.z, w.b.w};
         uint32_t lo[8], hi[8];
 #pragma unroll
@@ -618,8 +618,8 @@ struct Q4KPiece {
                 S0 = dp4a_us(lo[i], a.q[mm][i], S0);
                 S1 = dp4a_us(hi[i], a.q[mm][8 + i], S1);
             }
-            float v = ds0 * (a.f[mm][0] * (float)S0);
-            v = fmaf(ds1, a.f[mm][1] * (float)S1, v);
+            float v = ds0 * (a.f[mm][0] * i2f22(S0));
+            v = fmaf(ds1, a.f[mm][1] * i2f22(S1), v);
             v = fmaf(-dmin, fmaf(fm0, a.f[mm][2], fm1 * a.f[mm][3]), v);
             acc[mm] += v;
         }
@@ -679,9 +679,9 @@ struct Q5KPiece {
         const uint32_t r = __byte_perm(w.h.y, w.h.z, q.sel_r);
         const uint32_t wq = __byte_perm(w.h.w, 0u, q.sel_w);
         const uint32_t sm = (r & q.m1) | ((r >> 2) & q.m2) | (wq & q.m3) | ((wq >> 4) & q.m4);
-        const float ds0 = d * (float)(sm & 0xff);
-        const float ds1 = d * (float)((sm >> 8) & 0xff);
-        const float fm0 = (float)((sm >> 16) & 0xff), fm1 = (float)(sm >> 24);
+        const float ds0 = d * u8f(sm, 0);
+        const float ds1 = d * u8f(sm, 1);
+        const float fm0 = u8f(sm, 2), fm1 = u8f(sm, 3);
         const uint32_t raw[8] = {w.a.x, w.a.y, w.a.z, w.a.w, w.b.x, w.b.y, w.b.z, w.b.w};
         const uint32_t qh[8] = {w.h0.x, w.h0.y, w.h0.z, w.h0.w, w.h1.x, w.h1.y, w.h1.z, w.h1.w};
         const int sh = 2 * q.c;
@@ -700,8 +700,8 @@ struct Q5KPiece {
                 S0 = dp4a_us(lo[i], a.q[mm][i], S0);
                 S1 = dp4a_us(hi[i], a.q[mm][8 + i], S1);
             }
-            float v = ds0 * (a.f[mm][0] * (float)S0);
-            v = fmaf(ds1, a.f[mm][1] * (float)S1, v);
+            float v = ds0 * (a.f[mm][0] * i2f22(S0));
+            v = fmaf(ds1, a.f[mm][1] * i2f22(S1), v);
             v = fmaf(-dmin, fmaf(fm0, a.f[mm][2], fm1 * a.f[mm][3]), v);
             acc[mm] += v;
         }
@@ -820,7 +820,7 @@ struct Q6KPiece {
         const float d = h2f((uint16_t)w.d);
         float dsc[4];
 #pragma unroll
-        for (int g = 0; g < 4; g++) dsc[g] = d * (float)(int)(int8_t)((w.sc >> (8 * g)) & 0xff);
+        for (int g = 0; g < 4; g++) dsc[g] = d * i2f22((int)(int8_t)((w.sc >> (8 * g)) & 0xff));
         uint32_t u[4][4];
 #pragma unroll
         for (int i = 0; i < 4; i++) {
@@ -838,7 +838,7 @@ struct Q6KPiece {
                 int S = -a.sum[mm][g];
 #pragma unroll
                 for (int i = 0; i < 4; i++) S = dp4a_us(u[g][i], a.q[mm][4 * g + i], S);
-                v = fmaf(dsc[g], a.f[mm][g] * (float)S, v);
+                v = fmaf(dsc[g], a.f[mm][g] * i2f22(S), v);
             }
             acc[mm] += v;
         }

@@ -45,7 +45,7 @@ __device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32
 // Shared-memory layout (bytes) for rows of nblk = K/32 q8_1 blocks; the
 // warps' partial sums of up to `grp` tiles are kept before one reduction.
 struct MmaSmem {
-    int64_t xs, xs_pitch, da, saf, red, total;
+    int64_t xs, xs_pitch, da, saf, red, hdr, total;
 };
 __host__ __device__ inline MmaSmem mma_smem_layout(int64_t k, int nw, int grp, int nt) {
     const int64_t nblk = k / 32, nsb = k / 256, tok = 8 * (int64_t)nt;
@@ -55,7 +55,9 @@ __host__ __device__ inline MmaSmem mma_smem_layout(int64_t k, int nw, int grp, i
     L.da = L.xs + tok * L.xs_pitch;                         // float [nblk][8*nt]: d_a
     L.saf = L.da + nblk * tok * 4;                          // uint32 [nsb][nt][32]: s_a pairs for the min MMA
     L.red = L.saf + nsb * nt * 32 * 4;                      // float4 [2][grp][nw][nt][32]
-    L.total = L.red + 2 * (int64_t)grp * nw * nt * 32 * 16;
+    L.hdr = L.red;                                          // uint32 [8*nt][nblk] block headers while staging
+    const int64_t red_end = L.red + 2 * (int64_t)grp * nw * nt * 32 * 16, hdr_end = L.hdr + tok * nblk * 4;
+    L.total = red_end > hdr_end ? red_end : hdr_end;
     return L;
 }
 
@@ -118,33 +120,37 @@ __global__ void __launch_bounds__(NT == 1 ? 512 : 256, 1)
     if (sb_lo < sb_hi && tile < n_tiles) load_item(wa, tile, sb_lo);
     mmvq_pdl_enter(sg.chain);
 
-    // ---- q8_1 rows into shared memory (quants of block b at b * 40 + 8), d_a and s_a pairs
+    // ---- q8_1 rows into shared memory: asynchronous 4-byte copies, all of a
+    // thread's in flight at once (quants of block b at b * 40 + 8, the block's
+    // (d, s) word into hdr); zeros for the token rows past m_act
+    uint32_t *hdr = reinterpret_cast<uint32_t *>(smem + L.hdr);
     for (int i = tid; i < TOK * nblk; i += blockDim.x) {
         const int tok = i / nblk, b = i - tok * nblk;
         uint32_t *dst = reinterpret_cast<uint32_t *>(xs + tok * pitch + b * 40 + 8);
         if (tok < m_act) {
-            const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + tok * xrb + (int64_t)b * Q8_1_BYTES + 4);
+            const uint8_t *src = xq + tok * xrb + (int64_t)b * Q8_1_BYTES;
+            cp_async4(hdr + i, src);
 #pragma unroll
-            for (int j = 0; j < 8; j++) dst[j] = src[j];
+            for (int j = 0; j < 8; j++) cp_async4(dst + j, src + 4 + 4 * j);
         } else {
+            hdr[i] = 0u;
 #pragma unroll
             for (int j = 0; j < 8; j++) dst[j] = 0u;
         }
     }
+    cp_async_wait_all();
+    __syncthreads();
+    // d_a as fp32 [block][token] and the s_a pairs of the min-term MMA [sb][nt][lane]
     for (int i = tid; i < nblk * TOK; i += blockDim.x) {
         const int b = i / TOK, tok = i % TOK;
-        da[i] = tok < m_act ? h2f(ld_u16(xq + tok * xrb + (int64_t)b * Q8_1_BYTES)) : 0.0f;
+        da[i] = h2f((uint16_t)(hdr[tok * nblk + b] & 0xffffu));
     }
-    for (int i = tid; i < nsb * NT * 32; i += blockDim.x) {   // [sb][nt][lane]
+    for (int i = tid; i < nsb * NT * 32; i += blockDim.x) {
         const int s = i / (NT * 32), l = i & 31, tok = 8 * ((i >> 5) % NT) + (l >> 2), tt = l & 3;
-        uint32_t v = 0u;
-        if (tok < m_act) {
-            const uint8_t *b = xq + tok * xrb + (int64_t)(s * 8 + 2 * tt) * Q8_1_BYTES;
-            v = (uint32_t)ld_u16(b + 2) | ((uint32_t)ld_u16(b + Q8_1_BYTES + 2) << 16);
-        }
-        saf[i] = v;
+        const uint32_t *h = hdr + tok * nblk + s * 8 + 2 * tt;
+        saf[i] = (h[0] >> 16) | (h[1] & 0xffff0000u);
     }
-    __syncthreads();
+    __syncthreads();   // hdr (the reduction area) is free again
 
     const uint8_t *xg = xs + g * pitch + 8 + 8 * t;   // this lane's B bytes: token 8nt + g, values 8t .. 8t+7
     const __half2 bias = __floats2half2_rn(-1024.0f, -1024.0f);
@@ -168,8 +174,8 @@ __global__ void __launch_bounds__(NT == 1 ? 512 : 256, 1)
 #pragma unroll
         for (int c = 0; c < 4; c++) {
             const uint32_t sc = __shfl_sync(0xffffffffu, sp, (lane & ~3) | c);
-            const float sl0 = (float)(sc & 0xff), sh0 = (float)((sc >> 8) & 0xff);
-            const float sl1 = (float)((sc >> 16) & 0xff), sh1 = (float)(sc >> 24);
+            const float sl0 = u8f(sc, 0), sh0 = u8f(sc, 1);
+            const float sl1 = u8f(sc, 2), sh1 = u8f(sc, 3);
             const int bl = sb * 8 + 2 * c;   // block of the low nibbles; bl + 1 of the high ones
             const uint2 x0 = W.q0[c], x1 = W.q1[c];
             const uint32_t lo00 = x0.x & 0x0F0F0F0Fu, lo10 = x1.x & 0x0F0F0F0Fu;
@@ -186,14 +192,14 @@ __global__ void __launch_bounds__(NT == 1 ? 512 : 256, 1)
                 const float2 dL = *reinterpret_cast<const float2 *>(da + bl * TOK + 8 * nt + 2 * t);
                 const float2 dH = *reinterpret_cast<const float2 *>(da + (bl + 1) * TOK + 8 * nt + 2 * t);
                 // accumulator i: row g (i < 2) or g+8, token 8nt + 2t + (i & 1)
-                u[nt][0] = fmaf(sl0, dL.x * (float)sL[0], u[nt][0]);
-                u[nt][1] = fmaf(sl0, dL.y * (float)sL[1], u[nt][1]);
-                u[nt][2] = fmaf(sl1, dL.x * (float)sL[2], u[nt][2]);
-                u[nt][3] = fmaf(sl1, dL.y * (float)sL[3], u[nt][3]);
-                u[nt][0] = fmaf(sh0, dH.x * (float)sH[0], u[nt][0]);
-                u[nt][1] = fmaf(sh0, dH.y * (float)sH[1], u[nt][1]);
-                u[nt][2] = fmaf(sh1, dH.x * (float)sH[2], u[nt][2]);
-                u[nt][3] = fmaf(sh1, dH.y * (float)sH[3], u[nt][3]);
+                u[nt][0] = fmaf(sl0, dL.x * i2f22(sL[0]), u[nt][0]);
+                u[nt][1] = fmaf(sl0, dL.y * i2f22(sL[1]), u[nt][1]);
+                u[nt][2] = fmaf(sl1, dL.x * i2f22(sL[2]), u[nt][2]);
+                u[nt][3] = fmaf(sl1, dL.y * i2f22(sL[3]), u[nt][3]);
+                u[nt][0] = fmaf(sh0, dH.x * i2f22(sH[0]), u[nt][0]);
+                u[nt][1] = fmaf(sh0, dH.y * i2f22(sH[1]), u[nt][1]);
+                u[nt][2] = fmaf(sh1, dH.x * i2f22(sH[2]), u[nt][2]);
+                u[nt][3] = fmaf(sh1, dH.y * i2f22(sH[3]), u[nt][3]);
             }
         }
         // min term: A = m_2t, m_2t+1 of rows g, g+8 at k-slots 2t, 2t+1 (exact fp16 integers)
