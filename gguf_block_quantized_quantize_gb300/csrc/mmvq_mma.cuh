@@ -1,4 +1,4 @@
-// Tensor-core MMVQ for 5..32 tokens (Q4_K weights): the per-block int32 dot
+// Tensor-core MMVQ for 5..32 tokens (Q4_K and Q5_K weights): the per-block int32 dot
 // products of the blockwise formula run on warp-level int8 MMAs
 // (mma.sync m16n8k32 s8 x s8 -> s32).  One MMA is one 32-value block of 16
 // weight rows against 8 tokens (one n-tile; 2 or 4 n-tiles share the weight
@@ -9,7 +9,10 @@
 // At 8 tokens the dp4a form needs 16 dp4a per token per 64 weights, which
 // GB300's int8 rate cannot issue as fast as HBM delivers the weights; here the
 // operands need one LOP3 per 4 weights (Q4_K nibbles are non-negative int8)
-// and the q8_1 quants are the B fragments as they are.
+// and the q8_1 quants are the B fragments as they are.  Q5_K adds the fifth
+// bit of each quant from its 32 high-bit bytes (bit 2c of byte i for value i
+// of sub-block 2c, bit 2c + 1 for sub-block 2c + 1): the quants stay
+// non-negative int8 (0..31), so the same MMA and scale arithmetic apply.
 // The min term of a super-block is one fp16 MMA: A = the rows' 8 six-bit
 // mins, B = the 8 blocks' stored fp16 s_a (products exact in fp32).
 //
@@ -61,17 +64,26 @@ __host__ __device__ inline MmaSmem mma_smem_layout(int64_t k, int nw, int grp, i
     return L;
 }
 
-struct MmaW {
+struct MmaWBase {
     uint4 h0, h1;        // headers of rows g and g+8
-    uint2 q0[4], q1[4];  // bytes [32c + 8t, +8) of each chunk c, rows g and g+8
+    uint2 q0[4], q1[4];  // quant bytes [32c + 8t, +8) of each chunk c, rows g and g+8
+};
+template <int WT>
+struct MmaW : MmaWBase {};
+template <>
+struct MmaW<GGUF_Q5_K> : MmaWBase {
+    uint2 qh0, qh1;      // high-bit bytes [8t, +8) of rows g and g+8
 };
 
-// NT: n-tiles of 8 tokens (8*NT tokens at most)
-template <int NT>
+// WT: Q4_K or Q5_K; NT: n-tiles of 8 tokens (8*NT tokens at most)
+template <int WT, int NT>
 __global__ void __launch_bounds__(NT == 1 ? 512 : 256, 1)
-    mmvq_mma_q4k_kernel(const MmvqSegs sg, int64_t k, int64_t rb, const uint8_t *__restrict__ xq, int m_act, int yt,
-                        int grp) {
+    mmvq_mma_kq_kernel(const MmvqSegs sg, int64_t k, int64_t rb, const uint8_t *__restrict__ xq, int m_act, int yt,
+                       int grp) {
     constexpr int TOK = 8 * NT;
+    constexpr bool Q5 = WT == GGUF_Q5_K;
+    constexpr int SB_BYTES = Q5 ? Q5_K_BYTES : Q4_K_BYTES;
+    constexpr int QOFF = Q5 ? 48 : 16;   // the quant bytes follow the header (and Q5_K's 32 high-bit bytes)
     const int64_t n = sg.rows();
     extern __shared__ __align__(16) uint8_t smem[];
     const int nw = blockDim.x >> 5;
@@ -95,28 +107,32 @@ __global__ void __launch_bounds__(NT == 1 ? 512 : 256, 1)
     // row base pointers of the tile being loaded (looked up once per tile)
     int64_t cached_tile = -1;
     const uint8_t *base0 = nullptr, *base1 = nullptr;
-    auto load_item = [&](MmaW &W, int64_t tile, int sb) {
+    auto load_item = [&](MmaW<WT> &W, int64_t tile, int sb) {
         if (tile != cached_tile) {
             const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
             base0 = seg_row(sg, r0 < n ? r0 : n - 1, rb);
             base1 = seg_row(sg, r1 < n ? r1 : n - 1, rb);
             cached_tile = tile;
         }
-        const uint8_t *b0 = base0 + sb * Q4_K_BYTES;
-        const uint8_t *b1 = base1 + sb * Q4_K_BYTES;
+        const uint8_t *b0 = base0 + sb * SB_BYTES;
+        const uint8_t *b1 = base1 + sb * SB_BYTES;
         W.h0 = __ldg(reinterpret_cast<const uint4 *>(b0));
         W.h1 = __ldg(reinterpret_cast<const uint4 *>(b1));
+        if constexpr (Q5) {
+            W.qh0 = __ldg(reinterpret_cast<const uint2 *>(b0 + 16 + 8 * t));
+            W.qh1 = __ldg(reinterpret_cast<const uint2 *>(b1 + 16 + 8 * t));
+        }
 #pragma unroll
         for (int c = 0; c < 4; c++) {
-            W.q0[c] = __ldg(reinterpret_cast<const uint2 *>(b0 + 16 + 32 * c + 8 * t));
-            W.q1[c] = __ldg(reinterpret_cast<const uint2 *>(b1 + 16 + 32 * c + 8 * t));
+            W.q0[c] = __ldg(reinterpret_cast<const uint2 *>(b0 + QOFF + 32 * c + 8 * t));
+            W.q1[c] = __ldg(reinterpret_cast<const uint2 *>(b1 + QOFF + 32 * c + 8 * t));
         }
     };
 
     // the first item's weights are requested before waiting for the kernel
     // that wrote the activations
     int64_t tile = blockIdx.x;
-    MmaW wa, wb;
+    MmaW<WT> wa, wb;
     if (sb_lo < sb_hi && tile < n_tiles) load_item(wa, tile, sb_lo);
     mmvq_pdl_enter(sg.chain);
 
@@ -156,7 +172,7 @@ __global__ void __launch_bounds__(NT == 1 ? 512 : 256, 1)
     const __half2 bias = __floats2half2_rn(-1024.0f, -1024.0f);
 
     // one (tile, super-block) item; partial sums of rows g, g+8 x tokens 8nt + 2t, +1 into acc[nt]
-    auto process = [&](const MmaW &W, int sb, float (&acc)[NT][4]) {
+    auto process = [&](const MmaW<WT> &W, int sb, float (&acc)[NT][4]) {
         const float d0 = h2f(W.h0.x & 0xffff), dm0 = h2f(W.h0.x >> 16);
         const float d1 = h2f(W.h1.x & 0xffff), dm1 = h2f(W.h1.x >> 16);
         // (s, m) of sub-blocks 2t, 2t+1 for rows g and g+8 as bytes (s0, s1, m0, m1)
@@ -178,10 +194,22 @@ __global__ void __launch_bounds__(NT == 1 ? 512 : 256, 1)
             const float sl1 = u8f(sc, 2), sh1 = u8f(sc, 3);
             const int bl = sb * 8 + 2 * c;   // block of the low nibbles; bl + 1 of the high ones
             const uint2 x0 = W.q0[c], x1 = W.q1[c];
-            const uint32_t lo00 = x0.x & 0x0F0F0F0Fu, lo10 = x1.x & 0x0F0F0F0Fu;
-            const uint32_t lo01 = x0.y & 0x0F0F0F0Fu, lo11 = x1.y & 0x0F0F0F0Fu;
-            const uint32_t hi00 = (x0.x >> 4) & 0x0F0F0F0Fu, hi10 = (x1.x >> 4) & 0x0F0F0F0Fu;
-            const uint32_t hi01 = (x0.y >> 4) & 0x0F0F0F0Fu, hi11 = (x1.y >> 4) & 0x0F0F0F0Fu;
+            uint32_t lo00 = x0.x & 0x0F0F0F0Fu, lo10 = x1.x & 0x0F0F0F0Fu;
+            uint32_t lo01 = x0.y & 0x0F0F0F0Fu, lo11 = x1.y & 0x0F0F0F0Fu;
+            uint32_t hi00 = (x0.x >> 4) & 0x0F0F0F0Fu, hi10 = (x1.x >> 4) & 0x0F0F0F0Fu;
+            uint32_t hi01 = (x0.y >> 4) & 0x0F0F0F0Fu, hi11 = (x1.y >> 4) & 0x0F0F0F0Fu;
+            if constexpr (Q5) {   // fifth bits: bit 2c of each high-bit byte (low nibbles), 2c + 1 (high)
+                const uint32_t h00 = W.qh0.x >> (2 * c), h01 = W.qh0.y >> (2 * c);
+                const uint32_t h10 = W.qh1.x >> (2 * c), h11 = W.qh1.y >> (2 * c);
+                lo00 |= (h00 << 4) & 0x10101010u;
+                lo01 |= (h01 << 4) & 0x10101010u;
+                lo10 |= (h10 << 4) & 0x10101010u;
+                lo11 |= (h11 << 4) & 0x10101010u;
+                hi00 |= (h00 << 3) & 0x10101010u;
+                hi01 |= (h01 << 3) & 0x10101010u;
+                hi10 |= (h10 << 3) & 0x10101010u;
+                hi11 |= (h11 << 3) & 0x10101010u;
+            }
 #pragma unroll
             for (int nt = 0; nt < NT; nt++) {
                 const uint2 bL = *reinterpret_cast<const uint2 *>(xg + 8 * nt * pitch + bl * 40);
@@ -295,14 +323,14 @@ inline int mma_q4k_ntiles(int64_t m) { return m <= 8 ? 1 : m <= 16 ? 2 : 4; }
 // rows must fit in shared memory; m <= 32)
 inline bool mma_q4k_fits(int64_t k, int64_t m) { return m <= 32 && mma_q4k_group(k, mma_q4k_ntiles(m)) > 0; }
 
-template <int NT>
-inline cudaError_t launch_mmvq_mma_q4k_nt(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt,
-                                          cudaStream_t s) {
+template <int WT, int NT>
+inline cudaError_t launch_mmvq_mma_kq_nt(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt,
+                                         cudaStream_t s) {
     const int64_t n = sg.rows();
     const int nw = mma_q4k_warps(k, NT), grp = mma_q4k_group(k, NT);
     if (grp == 0) return cudaErrorInvalidValue;
     const MmaSmem L = mma_smem_layout(k, nw, grp, NT);
-    auto kern = mmvq_mma_q4k_kernel<NT>;
+    auto kern = mmvq_mma_kq_kernel<WT, NT>;
     cudaError_t e = cudaSuccess;
     const int per_sm = kernel_occupancy(reinterpret_cast<const void *>(kern), nw * 32, (size_t)L.total, &e);
     if (per_sm == 0) return e;
@@ -319,15 +347,22 @@ inline cudaError_t launch_mmvq_mma_q4k_nt(const MmvqSegs &sg, int64_t k, const u
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, sg, k, k / 256 * (int64_t)Q4_K_BYTES, xq, (int)m, yt, grp);
+    const int64_t rb = k / 256 * (int64_t)(WT == GGUF_Q5_K ? Q5_K_BYTES : Q4_K_BYTES);
+    return cudaLaunchKernelEx(&cfg, kern, sg, k, rb, xq, (int)m, yt, grp);
 }
 
-inline cudaError_t launch_mmvq_mma_q4k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt,
-                                       cudaStream_t s) {
-    switch (mma_q4k_ntiles(m)) {
-    case 1: return launch_mmvq_mma_q4k_nt<1>(sg, k, xq, m, yt, s);
-    case 2: return launch_mmvq_mma_q4k_nt<2>(sg, k, xq, m, yt, s);
-    default: return launch_mmvq_mma_q4k_nt<4>(sg, k, xq, m, yt, s);
+// Q4_K: 5..32 tokens (1, 2 or 4 n-tiles); Q5_K: 5..8 tokens (one n-tile)
+template <int WT>
+inline cudaError_t launch_mmvq_mma_kq(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt,
+                                      cudaStream_t s) {
+    if constexpr (WT == GGUF_Q5_K) {
+        return m <= 8 ? launch_mmvq_mma_kq_nt<WT, 1>(sg, k, xq, m, yt, s) : cudaErrorInvalidValue;
+    } else {
+        switch (mma_q4k_ntiles(m)) {
+        case 1: return launch_mmvq_mma_kq_nt<WT, 1>(sg, k, xq, m, yt, s);
+        case 2: return launch_mmvq_mma_kq_nt<WT, 2>(sg, k, xq, m, yt, s);
+        default: return launch_mmvq_mma_kq_nt<WT, 4>(sg, k, xq, m, yt, s);
+        }
     }
 }
 

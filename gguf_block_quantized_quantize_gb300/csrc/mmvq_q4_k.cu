@@ -10,9 +10,9 @@ cudaError_t launch_mmvq_q4_k(const MmvqSegs &sg, int64_t k, const uint8_t *xq, i
     // when the q8_1 rows fit in shared memory and there are enough 16-row
     // tiles to fill the GPU (below 2048 rows the per-CTA staging of the
     // activations outweighs it)
-    if (m > 8) return mma_q4k_fits(k, m) ? launch_mmvq_mma_q4k(sg, k, xq, m, yt, s) : cudaErrorInvalidValue;
+    if (m > 8) return mma_q4k_fits(k, m) ? launch_mmvq_mma_kq<GGUF_Q4_K>(sg, k, xq, m, yt, s) : cudaErrorInvalidValue;
     if (m >= option_mmvq_tc_min_m() && n >= 2048 && option_mmvq_tc() && mma_q4k_fits(k, m))
-        return launch_mmvq_mma_q4k(sg, k, xq, m, yt, s);
+        return launch_mmvq_mma_kq<GGUF_Q4_K>(sg, k, xq, m, yt, s);
     // one token: 8 rows in flight per thread on matrices of 8192 rows or more
     // (GB300, 18432 rows of 4096: 9.5 us against 11.0 with 4 rows)
     return launch_mmvq_pt<Q4KPiece>(sg, k, xq, m, yt, s, k / 256 * Q4_K_BYTES,

@@ -181,14 +181,14 @@ def test_mmvq_two_block_pieces_odd_block_count(g, wt, k, m):
     assert_close(y, ref, TOL_F32, f"mmvq type {wt} k {k} m {m}")
 
 
-@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K])
+@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.Q8_0, oracle.Q4_0])
 @pytest.mark.parametrize("k", [256, 1024, 3072, 8192])
 @pytest.mark.parametrize("m", [5, 8])
 def test_mmvq_tensor_core_vs_dp4a(g, wt, k, m):
-    # 5..8 tokens of Q4_K rows (n >= 2048) and of Q6_K rows (n >= 32768) run on
-    # the tensor-core MMVQ by default; the dp4a kernel (option mmvq_tc = 0)
-    # computes the same formula
-    n = 2100 if wt == oracle.Q4_K else 32768 + 37
+    # 5..8 tokens of Q4_K / Q5_K / Q8_0 / Q4_0 rows (n >= 2048) and of Q6_K
+    # rows (n >= 32768) run on the tensor-core MMVQ by default; the dp4a
+    # kernel (option mmvq_tc = 0) computes the same formula
+    n = 32768 + 37 if wt == oracle.Q6_K else 2100
     if wt == oracle.Q6_K and k > 1024:
         pytest.skip("tall Q6_K rows: k up to 1024 keeps the oracle fast")
     w = _weights(wt, n, k, seed=k + m)
@@ -258,6 +258,91 @@ def test_mmvq_tensor_core_exact_integer_sums(g, m):
     x = torch.from_numpy(xi.astype(np.float32))
     assert np.array_equal(oracle.mul_mat(oracle.Q4_K, w, k, oracle.quantize_q8_1(xi.astype(np.float32))), want)
     y = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x.to(DEV)).cpu().numpy()
+    assert np.array_equal(y.astype(np.float64), want), f"max diff {np.abs(y - want).max()}"
+
+
+def _q5_k_plain(q5):
+    # Q5_K rows with d = 1, dmin = 0, every sub-block scale 1 and min 0: the
+    # blocks hold the 5-bit quants themselves (value 64c + 32h + l of a block:
+    # low 4 bits in the nibble h of byte 32c + l, fifth bit in bit 2c + h of
+    # high-bit byte l)
+    n, k = q5.shape
+    v = q5.reshape(n, k // 256, 4, 2, 32).astype(np.uint8)     # [row][sb][c][h][l]
+    blk = np.zeros((n, k // 256, 176), np.uint8)
+    blk[:, :, 1] = 0x3C                                         # d = fp16 1.0
+    blk[:, :, 4:8] = 1
+    blk[:, :, 12:16] = 1
+    qh = np.zeros((n, k // 256, 32), np.uint8)
+    for c in range(4):
+        for h in range(2):
+            qh |= ((v[:, :, c, h, :] >> 4) & 1) << (2 * c + h)
+    blk[:, :, 16:48] = qh
+    blk[:, :, 48:] = ((v[:, :, :, 0, :] & 15) | ((v[:, :, :, 1, :] & 15) << 4)).reshape(n, k // 256, 128)
+    return blk.reshape(n, -1)
+
+
+@pytest.mark.parametrize("m", [5, 8])
+@pytest.mark.parametrize("n", [2048, 2061])
+def test_mmvq_tensor_core_q5_k_exact_integer_sums(g, m, n):
+    # Q5_K rows with unit scales, zero mins and integer activations whose every
+    # 32-block reaches 127 (d_a = 1, q = x): y is the integer product q5 . X,
+    # below 2^24, so the tensor-core MMVQ must match the int64 product bit for
+    # bit (2061 rows: a ragged last 16-row tile)
+    k = 1024
+    rng = np.random.default_rng(m + n)
+    q5 = rng.integers(0, 32, size=(n, k), dtype=np.int64)
+    xi = rng.integers(-127, 128, size=(m, k), dtype=np.int64)
+    xi[:, ::32] = 127
+    w = _q5_k_plain(q5)
+    assert np.array_equal(oracle.dequantize_f32(oracle.Q5_K, w, k), q5.astype(np.float32))
+    want = (xi @ q5.T).astype(np.float64)
+    assert np.abs(want).max() < 2 ** 24
+    y = g.gguf_mul_mat(_u8(w), oracle.Q5_K, n, k, torch.from_numpy(xi.astype(np.float32)).to(DEV)).cpu().numpy()
+    assert np.array_equal(y.astype(np.float64), want), f"max diff {np.abs(y - want).max()}"
+
+
+def _q8_0_plain(q8):
+    # Q8_0 rows with d = 1: the blocks hold the int8 quants themselves
+    n, k = q8.shape
+    blk = np.zeros((n, k // 32, 34), np.uint8)
+    blk[:, :, 1] = 0x3C                                         # d = fp16 1.0
+    blk[:, :, 2:] = q8.reshape(n, k // 32, 32).astype(np.int8).view(np.uint8)
+    return blk.reshape(n, -1)
+
+
+def _q4_0_plain(q4):
+    # Q4_0 rows with d = 1: value l of a block is q4 - 8, its nibble in byte
+    # l (low, l < 16) or l - 16 (high)
+    n, k = q4.shape
+    v = q4.reshape(n, k // 32, 2, 16).astype(np.uint8)
+    blk = np.zeros((n, k // 32, 18), np.uint8)
+    blk[:, :, 1] = 0x3C
+    blk[:, :, 2:] = v[:, :, 0, :] | (v[:, :, 1, :] << 4)
+    return blk.reshape(n, -1)
+
+
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0])
+@pytest.mark.parametrize("m", [5, 8])
+@pytest.mark.parametrize("n", [2048, 2061])
+def test_mmvq_tensor_core_small_block_exact_integer_sums(g, wt, m, n):
+    # Q8_0 / Q4_0 rows with d = 1 and integer activations whose every 32-block
+    # reaches 127 (d_a = 1, q = x): y is the integer product, below 2^24, so
+    # the tensor-core MMVQ must match the int64 product bit for bit (2061
+    # rows: a ragged last 16-row tile)
+    k = 512
+    rng = np.random.default_rng(m + n + wt)
+    if wt == oracle.Q8_0:
+        qv = rng.integers(-127, 128, size=(n, k), dtype=np.int64)
+        w, vals = _q8_0_plain(qv), qv
+    else:
+        qv = rng.integers(0, 16, size=(n, k), dtype=np.int64)
+        w, vals = _q4_0_plain(qv), qv - 8
+    xi = rng.integers(-127, 128, size=(m, k), dtype=np.int64)
+    xi[:, ::32] = 127
+    assert np.array_equal(oracle.dequantize_f32(wt, w, k), vals.astype(np.float32))
+    want = (xi @ vals.T).astype(np.float64)
+    assert np.abs(want).max() < 2 ** 24
+    y = g.gguf_mul_mat(_u8(w), wt, n, k, torch.from_numpy(xi.astype(np.float32)).to(DEV)).cpu().numpy()
     assert np.array_equal(y.astype(np.float64), want), f"max diff {np.abs(y - want).max()}"
 
 
