@@ -185,6 +185,14 @@ class Decode:
             segs = [(self.weight(n, k), n, self.ys[(n, m)]) for (n, k) in DECODE_SHAPES]
             g.gguf_mul_mat_segments(g.Q4_K, self.k, self.xqs[m], segs, xt=g.Q8_1, m=m, ws=self.ws)
 
+    def prepared_batches(self, count):
+        """`count` consecutive steps' batch calls with their arguments marshalled
+        once (the weight copies rotate as in the timed step)."""
+        return [self.g.PreparedBatch(self.g.Q4_K, self.k,
+                                     [(self.xqs[m], [(self.weight(n, k), n, self.ys[(n, m)]) for (n, k) in DECODE_SHAPES])
+                                      for m in DECODE_MS])
+                for _ in range(count)]
+
     def _batch(self, ms):   # one call: the M-products as chained launches
         self.g.gguf_mul_mat_batch(self.g.Q4_K, self.k,
                                   [(self.xqs[m], [(self.weight(n, k), n, self.ys[(n, m)]) for (n, k) in DECODE_SHAPES])
@@ -379,10 +387,11 @@ def mmvq_traffic():
 
 def run_e2e(args, g, torch, dev, dec, per_step):
     """Same workload through the public API with host buffers: each step copies
-    its activations from pinned host memory and reads its outputs back.  The
-    loop is bound by host calls, so it issues the fewest: one quantize, one
-    gguf_mul_mat_batch call (all M-products), one copy each way, on one
-    stream."""
+    its activations from pinned host memory, quantizes them, runs the four
+    M-products as one gguf_mul_mat_batch call and reads its outputs back, on
+    one stream.  The batch call's arguments are marshalled once per weight
+    phase (PreparedBatch), as an engine replaying its decode step would, so the
+    host issues four calls per step."""
     hx = dec.x_all.cpu().pin_memory()
     hy = torch.empty(dec.y_all.shape, dtype=dec.y_all.dtype).pin_memory()
     dx = torch.empty_like(dec.x_all)
@@ -390,9 +399,14 @@ def run_e2e(args, g, torch, dev, dec, per_step):
     h2d = hx.numel() * hx.element_size()
     d2h = hy.numel() * hy.element_size()
 
+    prepared = dec.prepared_batches(64)
+    it = [0]
+
     def step():
         dx.copy_(hx, non_blocking=True)
-        dec.step(x_all=dx)
+        g.gguf_quantize_q8_1(dx, out=dec.xq_all)
+        prepared[it[0] % len(prepared)].run()
+        it[0] += 1
         hy.copy_(dec.y_all, non_blocking=True)
 
     with torch.cuda.stream(stream):

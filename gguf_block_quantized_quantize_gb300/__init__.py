@@ -282,6 +282,31 @@ def gguf_mul_mat_batch(wt: int, k: int, jobs):
     return outs
 
 
+class PreparedBatch:
+    """The arguments of one gguf_mul_mat_batch call marshalled once (the
+    tensors are referenced, not copied): ``run()`` issues the call on the
+    current stream with no per-call argument building, as an engine that
+    replays the same decode step does.  Same ``jobs`` as gguf_mul_mat_batch."""
+
+    def __init__(self, wt: int, k: int, jobs):
+        self._keep, cjobs, yt = [], [], None
+        for xq, segs in jobs:
+            if xq.dim() != 2 or (xq.shape[0] > 1 and xq.stride(0) != k // 32 * Q8_1_BYTES):
+                raise ValueError("PreparedBatch: q8_1 rows of xq must be contiguous")
+            for (_, _, o) in segs:
+                t = _TYPE_OF[o.dtype]
+                if o.stride(1) != 1 or (yt is not None and t != yt):
+                    raise ValueError("PreparedBatch: outputs need contiguous rows and one dtype")
+                yt = t
+            arr = (Segment * len(segs))(*[Segment(_ptr(w), n, _ptr(o), o.stride(0)) for (w, n, o) in segs])
+            self._keep.append((xq, segs, arr))
+            cjobs.append(MmJob(arr, len(segs), _ptr(xq), xq.shape[0]))
+        self._args = (wt, k, (MmJob * len(cjobs))(*cjobs), len(cjobs), yt)
+
+    def run(self):
+        _check(_lib_fast().gguf_mul_mat_batch(*self._args, _stream()))
+
+
 def gguf_mul_mat_noalloc(w: torch.Tensor, wt: int, n: int, k: int, x: torch.Tensor,
                          out: torch.Tensor | None = None, out_dtype=None) -> torch.Tensor:
     """y[m, n] = x[m, k] @ W[n, k]^T for m <= 8, k <= 16384, with the q8_1

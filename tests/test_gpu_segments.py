@@ -146,3 +146,14 @@ def test_mul_mat_batch_matches_segment_calls(g, wt):
             assert torch.equal(o, s), f"job {j}: batch differs from the segment call"
             assert_close(o.float().cpu().numpy(), r, TOL_BF16, f"batch job {j}")
         assert torch.isfinite(sums[j])
+    # the same batch with its arguments marshalled once, run twice into cleared outputs
+    prep = g.PreparedBatch(wt, k, jobs)
+    for _ in range(2):
+        for job_outs in outs:
+            for o in job_outs:
+                o.fill_(float("nan"))
+        prep.run()
+        torch.cuda.synchronize()
+        for j, job_outs in enumerate(outs):
+            for o, s_ in zip(job_outs, sep[j]):
+                assert torch.equal(o, s_), f"prepared batch job {j} differs from the segment call"
