@@ -1,20 +1,23 @@
-// Tensor-core MMVQ for 5..8 tokens of Q8_0 and Q4_0 weights (32-value blocks
-// with one fp16 scale each): the per-block int32 dot products of the blockwise
+// Tensor-core MMVQ for 5..8 tokens of Q8_0, Q4_0 and MXFP4 weights (32-value
+// blocks with one scale each): the per-block int32 dot products of the blockwise
 // formula run on warp-level int8 MMAs (mma.sync m16n8k32 s8 x s8 -> s32), one
 // MMA per 32-value block of 16 weight rows against 8 tokens, so each s32
 // accumulator is exactly the block dot S of one (row, token) pair, and
 //   y += d_w * d_a * S
 // is applied per block in fp32, as in the dp4a kernel.  Q8_0 quants enter the
-// MMA as they are; Q4_0 nibbles enter unsigned (0..15) and the offset comes
-// off the exact sum, S = MMA - 8 * sum(q_a), with the activation blocks' quant
-// sums computed once per CTA.
+// MMA as they are; Q4_0 nibbles enter unsigned (0..15) and MXFP4 codes as the
+// biased bytes 16 + k (k = 2 e2m1, -12..12), and the offset comes off the exact
+// sum, S = MMA - OFF * sum(q_a) (OFF 8 or 16), with the activation blocks'
+// quant sums computed once per CTA.  MXFP4's scale is 2^(e - 128) of the
+// block's E8M0 byte e, since its values are k * 2^(e - 128).
 //
-// The blocks are 34 (Q8_0) or 18 (Q4_0) bytes, only 2-byte aligned, so an
-// item (16 rows x 8 blocks = 256 values) is copied into a per-warp shared-
-// memory buffer with 16-byte asynchronous copies (an item of a 16-byte-aligned
-// row of K % 256 == 0 values starts and ends on 16-byte boundaries: 272 / 144
-// bytes per row), double-buffered so the next item's copies are in flight
-// while this one computes; the lanes then read their fragments from there.
+// The blocks are 34 (Q8_0), 18 (Q4_0) or 17 (MXFP4) bytes, 2-byte aligned or
+// not at all, so an item (16 rows x 8 blocks, 16 for MXFP4) is copied into a
+// per-warp shared-memory buffer with 16-byte asynchronous copies (an item of a
+// 16-byte-aligned row whose K is a multiple of the item starts and ends on
+// 16-byte boundaries: 272 / 144 / 272 bytes per row), into a ring of NBUF
+// buffers so the next items' copies are in flight while one computes; the
+// lanes then read their fragments from there.
 // Work split and the q8_1 staging are those of the K-quant tensor-core kernel
 // (mmvq_mma.cuh): warp w takes items [w * nsb / NW, (w + 1) * nsb / NW) of
 // every 16-row tile, and the warps' partial sums are added in a fixed order.
@@ -28,18 +31,42 @@ namespace gg {
 
 template <int WT>
 struct SbTraits;
-// BB: block bytes; NBUF: item buffers per warp (NBUF - 1 items in flight
-// while one computes; Q4_0's smaller buffers let two CTAs share an SM)
+// BB: block bytes; NB: blocks per item; NBUF: item buffers per warp (NBUF - 1
+// items in flight while one computes; Q4_0's smaller buffers let two CTAs
+// share an SM); OFF: the offset of the quants entering the MMA
 template <>
 struct SbTraits<GGUF_Q8_0> {
-    static constexpr int BB = Q8_0_BYTES;   // 34
-    static constexpr int NBUF = 3;
+    static constexpr int BB = Q8_0_BYTES, NB = 8, NBUF = 3, OFF = 0;   // 34-byte blocks
 };
 template <>
 struct SbTraits<GGUF_Q4_0> {
-    static constexpr int BB = Q4_0_BYTES;   // 18
-    static constexpr int NBUF = 3;
+    static constexpr int BB = Q4_0_BYTES, NB = 8, NBUF = 3, OFF = 8;   // 18-byte blocks
 };
+template <>
+struct SbTraits<GGUF_MXFP4> {
+    static constexpr int BB = MXFP4_BYTES, NB = 16, NBUF = 3, OFF = 16;   // 17-byte blocks
+};
+
+// compile-time loop: f(std::integral_constant<int, I>) for I in [B, N)
+template <int B, int N, class F>
+__device__ __forceinline__ void unroll_c(F &&f) {
+    if constexpr (B < N) {
+        f(std::integral_constant<int, B>{});
+        unroll_c<B + 1, N>(f);
+    }
+}
+
+// 4 bytes at a shared-memory address p with p % 4 == O (compile-time):
+// aligned words and a funnel shift, reading [p - O, p - O + 8) when O != 0
+template <int O>
+__device__ __forceinline__ uint32_t lds4_at(const uint8_t *p) {
+    if constexpr (O == 0) {
+        return *reinterpret_cast<const uint32_t *>(p);
+    } else {
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(p - O);
+        return __funnelshift_r(w[0], w[1], 8 * O);
+    }
+}
 
 __device__ __forceinline__ void cp_async16(void *sdst, const void *gsrc) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(sdst)),
@@ -62,14 +89,21 @@ __device__ __forceinline__ uint32_t lds4(const uint8_t *p) {
     }
 }
 
-inline int64_t sb_item_bytes(int wt) { return 8 * (wt == GGUF_Q8_0 ? Q8_0_BYTES : Q4_0_BYTES); }
-inline int sb_nbuf(int wt) { return wt == GGUF_Q8_0 ? SbTraits<GGUF_Q8_0>::NBUF : SbTraits<GGUF_Q4_0>::NBUF; }
-inline int mma_sb_warps(int64_t k) {
-    const int nsb = (int)(k / 256);
+inline int sb_nb(int wt) { return wt == GGUF_MXFP4 ? SbTraits<GGUF_MXFP4>::NB : 8; }
+inline int64_t sb_item_bytes(int wt) {
+    return wt == GGUF_Q8_0 ? 8 * Q8_0_BYTES : wt == GGUF_Q4_0 ? 8 * Q4_0_BYTES : 16 * MXFP4_BYTES;
+}
+inline int sb_nbuf(int wt) {
+    return wt == GGUF_Q8_0 ? SbTraits<GGUF_Q8_0>::NBUF
+           : wt == GGUF_Q4_0 ? SbTraits<GGUF_Q4_0>::NBUF : SbTraits<GGUF_MXFP4>::NBUF;
+}
+// warps per CTA: at most 8, and at least one item of every tile each
+inline int mma_sb_warps(int wt, int64_t k) {
+    const int nsb = (int)(k / (32 * sb_nb(wt)));
     return nsb < 8 ? (nsb < 1 ? 1 : nsb) : 8;
 }
 // shared memory: the K-quant kernel's activation layout (one n-tile), the
-// activation blocks' quant sums times 8 (int32 [block][token]), then the
+// activation blocks' quant sums times OFF (int32 [block][token]), then the
 // per-warp item buffers (NBUF items of 16 rows each)
 __host__ __device__ inline int64_t mma_sb_qs_offset(int64_t k, int nw, int grp) {
     return (mma_smem_layout(k, nw, grp, 1).total + 15) / 16 * 16;
@@ -85,9 +119,9 @@ inline int64_t mma_sb_smem(int wt, int64_t k, int nw, int grp) {
 inline int mma_sb_group(int wt, int64_t k) {
     const int64_t two = 113 * 1024;   // two CTAs within an SM's 228 KB, 1 KB reserved per CTA
     for (int grp = 4; grp >= 1; grp /= 2)
-        if (mma_sb_smem(wt, k, mma_sb_warps(k), grp) <= two) return grp;
+        if (mma_sb_smem(wt, k, mma_sb_warps(wt, k), grp) <= two) return grp;
     for (int grp = 4; grp >= 1; grp /= 2)
-        if (mma_sb_smem(wt, k, mma_sb_warps(k), grp) <= (int64_t)device_info().smem_optin) return grp;
+        if (mma_sb_smem(wt, k, mma_sb_warps(wt, k), grp) <= (int64_t)device_info().smem_optin) return grp;
     return 0;
 }
 
@@ -95,8 +129,8 @@ template <int WT>
 __global__ void __launch_bounds__(256, 2)
     mmvq_mma_sb_kernel(const MmvqSegs sg, int64_t k, int64_t rb, const uint8_t *__restrict__ xq, int m_act, int yt,
                        int grp) {
-    constexpr int BB = SbTraits<WT>::BB;
-    constexpr int IB = 8 * BB;        // bytes of one row's item
+    constexpr int BB = SbTraits<WT>::BB, NB = SbTraits<WT>::NB, OFF = SbTraits<WT>::OFF;
+    constexpr int IB = NB * BB;       // bytes of one row's item
     constexpr int NCH = IB / 16;      // 16-byte chunks of one row's item
     constexpr int TOK = 8;
     constexpr int NBUF = SbTraits<WT>::NBUF;
@@ -112,7 +146,7 @@ __global__ void __launch_bounds__(256, 2)
     uint8_t *wbuf = smem + mma_sb_wbuf_offset(k, nw, grp) + (int64_t)warp * NBUF * 16 * IB;
 
     const int g = lane >> 2, t = lane & 3;
-    const int nblk = (int)(k / 32), nsb = (int)(k / 256);
+    const int nblk = (int)(k / 32), nsb = (int)(k / (32 * NB));
     const int64_t xrb = (int64_t)nblk * Q8_1_BYTES;
     const int pitch = (int)L.xs_pitch;
     const int64_t n_tiles = (n + 15) / 16;
@@ -189,12 +223,12 @@ __global__ void __launch_bounds__(256, 2)
     for (int i = tid; i < nblk * TOK; i += blockDim.x) {
         const int b = i / TOK, tok = i % TOK;
         da[i] = h2f((uint16_t)(hdr[tok * nblk + b] & 0xffffu));
-        if constexpr (WT == GGUF_Q4_0) {
+        if constexpr (OFF != 0) {
             const uint32_t *qw = reinterpret_cast<const uint32_t *>(xs + tok * pitch + b * 40 + 8);
             int sum = 0;
 #pragma unroll
             for (int j = 0; j < 8; j++) sum = __dp4a((int)qw[j], 0x01010101, sum);
-            qs8[i] = 8 * sum;
+            qs8[i] = OFF * sum;
         }
     }
     __syncthreads();   // hdr (the reduction area) is free again
@@ -211,42 +245,63 @@ __global__ void __launch_bounds__(256, 2)
 
         const uint8_t *w0 = wbuf + (cc % NBUF) * 16 * IB + g * IB;   // row g of the tile
         const uint8_t *w1 = w0 + 8 * IB;                     // row g + 8
-        // block b of the item; A4: its quant words are 4-byte aligned in the
-        // buffer (odd b: 34 b + 2 and 18 b + 2 are multiples of 4)
-        auto step = [&](int b, auto a4) {
-            constexpr bool A4 = decltype(a4)::value;
-            const int blk = sb * 8 + b;
-            const float dw0 = h2f(*reinterpret_cast<const uint16_t *>(w0 + b * BB));
-            const float dw1 = h2f(*reinterpret_cast<const uint16_t *>(w1 + b * BB));
+        // block B of the item (a compile-time constant, so the alignment of its
+        // words in the buffer is known: rows start on 16-byte boundaries)
+        auto step = [&](auto bc) {
+            constexpr int B = decltype(bc)::value;
+            const int blk = sb * NB + B;
+            float dw0, dw1;
             uint32_t a0, a1, a2, a3, b0, b1;
-            if constexpr (WT == GGUF_Q8_0) {
-                // quants 8t .. 8t+7 of the block (the same K order on both sides)
-                a0 = lds4<A4>(w0 + b * BB + 2 + 8 * t);
-                a2 = lds4<A4>(w0 + b * BB + 6 + 8 * t);
-                a1 = lds4<A4>(w1 + b * BB + 2 + 8 * t);
-                a3 = lds4<A4>(w1 + b * BB + 6 + 8 * t);
-                const uint2 bx = *reinterpret_cast<const uint2 *>(xg + blk * 40 + 8 * t);
-                b0 = bx.x;
-                b1 = bx.y;
+            if constexpr (WT == GGUF_MXFP4) {
+                dw0 = e8m0_half(w0[B * BB]);
+                dw1 = e8m0_half(w1[B * BB]);
+                // code bytes 4t .. 4t+3 (values 4t.. low, 16+4t.. high) as biased bytes in
+                // the order (4t, 16+4t, 4t+1, 17+4t), (4t+2, 18+4t, 4t+3, 19+4t)
+                constexpr int O = (B * BB + 1) & 3;
+                const uint32_t c0 = lds4_at<O>(w0 + B * BB + 1 + 4 * t);
+                const uint32_t c1 = lds4_at<O>(w1 + B * BB + 1 + 4 * t);
+                a0 = mxfp4_biased4(c0);
+                a2 = mxfp4_biased4(c0 >> 16);
+                a1 = mxfp4_biased4(c1);
+                a3 = mxfp4_biased4(c1 >> 16);
+                const uint32_t x0 = *reinterpret_cast<const uint32_t *>(xg + blk * 40 + 4 * t);
+                const uint32_t x1 = *reinterpret_cast<const uint32_t *>(xg + blk * 40 + 16 + 4 * t);
+                b0 = __byte_perm(x0, x1, 0x5140);
+                b1 = __byte_perm(x0, x1, 0x7362);
             } else {
-                // nibble bytes 4t .. 4t+3: values 4t.. (low) and 16+4t.. (high), unsigned
-                const uint32_t q0 = lds4<A4>(w0 + b * BB + 2 + 4 * t);
-                const uint32_t q1 = lds4<A4>(w1 + b * BB + 2 + 4 * t);
-                a0 = q0 & 0x0F0F0F0Fu;
-                a1 = q1 & 0x0F0F0F0Fu;
-                a2 = (q0 >> 4) & 0x0F0F0F0Fu;
-                a3 = (q1 >> 4) & 0x0F0F0F0Fu;
-                b0 = *reinterpret_cast<const uint32_t *>(xg + blk * 40 + 4 * t);
-                b1 = *reinterpret_cast<const uint32_t *>(xg + blk * 40 + 16 + 4 * t);
+                dw0 = h2f(*reinterpret_cast<const uint16_t *>(w0 + B * BB));
+                dw1 = h2f(*reinterpret_cast<const uint16_t *>(w1 + B * BB));
+                // the quant words are 4-byte aligned for odd B (34 B + 2 and 18 B + 2)
+                constexpr bool A4 = ((B * BB + 2) & 3) == 0;
+                if constexpr (WT == GGUF_Q8_0) {
+                    // quants 8t .. 8t+7 of the block (the same K order on both sides)
+                    a0 = lds4<A4>(w0 + B * BB + 2 + 8 * t);
+                    a2 = lds4<A4>(w0 + B * BB + 6 + 8 * t);
+                    a1 = lds4<A4>(w1 + B * BB + 2 + 8 * t);
+                    a3 = lds4<A4>(w1 + B * BB + 6 + 8 * t);
+                    const uint2 bx = *reinterpret_cast<const uint2 *>(xg + blk * 40 + 8 * t);
+                    b0 = bx.x;
+                    b1 = bx.y;
+                } else {
+                    // nibble bytes 4t .. 4t+3: values 4t.. (low) and 16+4t.. (high), unsigned
+                    const uint32_t q0 = lds4<A4>(w0 + B * BB + 2 + 4 * t);
+                    const uint32_t q1 = lds4<A4>(w1 + B * BB + 2 + 4 * t);
+                    a0 = q0 & 0x0F0F0F0Fu;
+                    a1 = q1 & 0x0F0F0F0Fu;
+                    a2 = (q0 >> 4) & 0x0F0F0F0Fu;
+                    a3 = (q1 >> 4) & 0x0F0F0F0Fu;
+                    b0 = *reinterpret_cast<const uint32_t *>(xg + blk * 40 + 4 * t);
+                    b1 = *reinterpret_cast<const uint32_t *>(xg + blk * 40 + 16 + 4 * t);
+                }
             }
             int S[4];
             mma_16832_s8(S, a0, a1, a2, a3, b0, b1);
-            if constexpr (WT == GGUF_Q4_0) {   // the offset 8 of every weight quant
-                const int2 q8 = *reinterpret_cast<const int2 *>(qs8 + blk * TOK + 2 * t);
-                S[0] -= q8.x;
-                S[1] -= q8.y;
-                S[2] -= q8.x;
-                S[3] -= q8.y;
+            if constexpr (OFF != 0) {   // the offset of every weight quant
+                const int2 qo = *reinterpret_cast<const int2 *>(qs8 + blk * TOK + 2 * t);
+                S[0] -= qo.x;
+                S[1] -= qo.y;
+                S[2] -= qo.x;
+                S[3] -= qo.y;
             }
             const float2 dd = *reinterpret_cast<const float2 *>(da + blk * TOK + 2 * t);
             // accumulator i: row g (i < 2) or g+8, token 2t + (i & 1)
@@ -255,11 +310,7 @@ __global__ void __launch_bounds__(256, 2)
             acc[2] = fmaf(dw1 * dd.x, i2f22(S[2]), acc[2]);
             acc[3] = fmaf(dw1 * dd.y, i2f22(S[3]), acc[3]);
         };
-#pragma unroll
-        for (int bp = 0; bp < 4; bp++) {
-            step(2 * bp, std::false_type{});
-            step(2 * bp + 1, std::true_type{});
-        }
+        unroll_c<0, NB>(step);
         __syncwarp();   // every lane is done with this buffer before it is refilled
         cc++;
 
@@ -296,11 +347,11 @@ __global__ void __launch_bounds__(256, 2)
     cp_async_wait_all();   // no copy outlives the CTA
 }
 
-// whether 5..8 tokens of K-long rows of type wt (Q8_0 / Q4_0) can take this
-// kernel: whole 256-value items, every segment's rows 16-byte aligned, the
-// buffers in shared memory
+// whether 5..8 tokens of K-long rows of type wt (Q8_0 / Q4_0 / MXFP4) can take
+// this kernel: whole items, every segment's rows 16-byte aligned, the buffers
+// in shared memory
 inline bool mma_sb_fits(int wt, const MmvqSegs &sg, int64_t k, int64_t m) {
-    if (m > 8 || k % 256 != 0) return false;
+    if (m > 8 || k % (32 * sb_nb(wt)) != 0) return false;
     for (int i = 0; i < sg.nseg; i++)
         if (reinterpret_cast<uintptr_t>(sg.w[i]) % 16 != 0) return false;
     return mma_sb_group(wt, k) > 0;
@@ -310,7 +361,7 @@ template <int WT>
 inline cudaError_t launch_mmvq_mma_sb(const MmvqSegs &sg, int64_t k, const uint8_t *xq, int64_t m, int yt,
                                       cudaStream_t s) {
     const int64_t n = sg.rows();
-    const int nw = mma_sb_warps(k), grp = mma_sb_group(WT, k);
+    const int nw = mma_sb_warps(WT, k), grp = mma_sb_group(WT, k);
     if (grp == 0) return cudaErrorInvalidValue;
     const size_t smem = (size_t)mma_sb_smem(WT, k, nw, grp);
     auto kern = mmvq_mma_sb_kernel<WT>;

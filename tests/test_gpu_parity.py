@@ -181,13 +181,14 @@ def test_mmvq_two_block_pieces_odd_block_count(g, wt, k, m):
     assert_close(y, ref, TOL_F32, f"mmvq type {wt} k {k} m {m}")
 
 
-@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.Q8_0, oracle.Q4_0])
+@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.Q8_0, oracle.Q4_0, oracle.MXFP4])
 @pytest.mark.parametrize("k", [256, 1024, 3072, 8192])
 @pytest.mark.parametrize("m", [5, 8])
 def test_mmvq_tensor_core_vs_dp4a(g, wt, k, m):
-    # 5..8 tokens of Q4_K / Q5_K / Q8_0 / Q4_0 rows (n >= 2048) and of Q6_K
-    # rows (n >= 32768) run on the tensor-core MMVQ by default; the dp4a
-    # kernel (option mmvq_tc = 0) computes the same formula
+    # 5..8 tokens of Q4_K / Q5_K / Q8_0 / Q4_0 / MXFP4 rows (n >= 2048; MXFP4
+    # rows of whole 512-value items) and of Q6_K rows (n >= 32768) run on the
+    # tensor-core MMVQ by default; the dp4a kernel (option mmvq_tc = 0)
+    # computes the same formula
     n = 32768 + 37 if wt == oracle.Q6_K else 2100
     if wt == oracle.Q6_K and k > 1024:
         pytest.skip("tall Q6_K rows: k up to 1024 keeps the oracle fast")
@@ -310,6 +311,18 @@ def _q8_0_plain(q8):
     return blk.reshape(n, -1)
 
 
+def _mxfp4_plain(codes):
+    # MXFP4 rows with exponent byte 128 (scale 2^(128-127) on e2m1, so a code's
+    # value is the integer 2 * e2m1(code)); code l of a block in byte l (low
+    # nibble, l < 16) or l - 16 (high)
+    n, k = codes.shape
+    v = codes.reshape(n, k // 32, 2, 16).astype(np.uint8)
+    blk = np.zeros((n, k // 32, 17), np.uint8)
+    blk[:, :, 0] = 128
+    blk[:, :, 1:] = v[:, :, 0, :] | (v[:, :, 1, :] << 4)
+    return blk.reshape(n, -1)
+
+
 def _q4_0_plain(q4):
     # Q4_0 rows with d = 1: value l of a block is q4 - 8, its nibble in byte
     # l (low, l < 16) or l - 16 (high)
@@ -321,22 +334,25 @@ def _q4_0_plain(q4):
     return blk.reshape(n, -1)
 
 
-@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0])
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.MXFP4])
 @pytest.mark.parametrize("m", [5, 8])
 @pytest.mark.parametrize("n", [2048, 2061])
 def test_mmvq_tensor_core_small_block_exact_integer_sums(g, wt, m, n):
-    # Q8_0 / Q4_0 rows with d = 1 and integer activations whose every 32-block
-    # reaches 127 (d_a = 1, q = x): y is the integer product, below 2^24, so
-    # the tensor-core MMVQ must match the int64 product bit for bit (2061
-    # rows: a ragged last 16-row tile)
+    # Q8_0 / Q4_0 rows with d = 1, MXFP4 rows with unit scale, and integer
+    # activations whose every 32-block reaches 127 (d_a = 1, q = x): y is the
+    # integer product, below 2^24, so the tensor-core MMVQ must match the
+    # int64 product bit for bit (2061 rows: a ragged last 16-row tile)
     k = 512
     rng = np.random.default_rng(m + n + wt)
     if wt == oracle.Q8_0:
         qv = rng.integers(-127, 128, size=(n, k), dtype=np.int64)
         w, vals = _q8_0_plain(qv), qv
-    else:
+    elif wt == oracle.Q4_0:
         qv = rng.integers(0, 16, size=(n, k), dtype=np.int64)
         w, vals = _q4_0_plain(qv), qv - 8
+    else:
+        w = _mxfp4_plain(rng.integers(0, 16, size=(n, k), dtype=np.int64))
+        vals = oracle.dequantize_f32(wt, w, k).astype(np.int64)
     xi = rng.integers(-127, 128, size=(m, k), dtype=np.int64)
     xi[:, ::32] = 127
     assert np.array_equal(oracle.dequantize_f32(wt, w, k), vals.astype(np.float32))
