@@ -493,7 +493,26 @@ def secondary(torch, g, synth, dev, stream, hbm_peak, tf_peak, peak_kind):
                              device=dev)
             ms = _time_eager(torch, stream, lambda: g.gguf_mul_mat(w, wt, n, k, x, out=y, ws=ws), 5, flush)
             tops = 2.0 * m * n * k / (ms * 1e-3) / 1e12
-            out[name] = {"ms": round(ms, 4), "tops": round(tops, 1),
+            # the alternative engine on the same product: dequantize to fp16 + one library GEMM
+            g.gguf_set_option("mmq_engine", 1)
+            try:
+                ws1 = torch.empty(max(g.gguf_mul_mat_ws_size(wt, n, k, g.BF16, m, g.BF16), 16), dtype=torch.uint8,
+                                  device=dev)
+                ms1 = _time_eager(torch, stream, lambda: g.gguf_mul_mat(w, wt, n, k, x, out=y, ws=ws1), 5, flush)
+                # with fp16 outputs the library GEMM writes them directly (no fp32 rows)
+                y16 = torch.empty((m, n), dtype=torch.float16, device=dev)
+                ms2 = _time_eager(torch, stream, lambda: g.gguf_mul_mat(w, wt, n, k, x, out=y16, ws=ws1), 5, flush)
+                lib_engine = {"ms": round(ms1, 4), "tops": round(2.0 * m * n * k / (ms1 * 1e-3) / 1e12, 1),
+                              "ms_f16_out": round(ms2, 4),
+                              "note": "option mmq_engine = 1: weights dequantized to fp16 in the workspace, then one "
+                                      "cuBLAS fp16 GEMM (fp32 accumulation) on the q8_1 operand, fp32 rows converted "
+                                      "to bf16; includes the dequantize"}
+                del ws1, y16
+            except Exception as exc:   # cuBLAS not loadable: reported, the fused number stands
+                lib_engine = {"unavailable": str(exc)[:200]}
+            finally:
+                g.gguf_set_option("mmq_engine", 0)
+            out[name] = {"ms": round(ms, 4), "tops": round(tops, 1), "library_engine": lib_engine,
                          "rate": "algorithmic 2*m*n*k ops/s (int8-equivalent); computed as fp16 tcgen05 MMAs of "
                                  "the dequantized operands",
                          "roofline": {"bound": "tensor", "achieved": round(tops, 1), "peak": tf_peak,

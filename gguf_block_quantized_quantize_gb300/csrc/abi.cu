@@ -110,6 +110,10 @@ static int64_t g_mmq_stage = 1;
 static int64_t g_moe_deterministic = 1;
 static int64_t g_mmq_bn_max = 256;
 static int64_t g_mmq_split_k = 1;   // small m: split K across CTAs (fp32 partial sums) to fill the GPU
+static int64_t g_mmq_engine = 0;    // 1: 16-bit-output prefill products as dequantize + library GEMM
+int64_t option_mmq_engine() { return g_mmq_engine; }
+// the library-GEMM engine takes this product
+static bool lib_engine(int64_t m, int64_t k, int yt) { return g_mmq_engine == 1 && yt != GGUF_F32 && m > 0 && k > 0; }
 int64_t option_mmq_bn_max() { return g_mmq_bn_max; }
 static int64_t g_moe_down_precise = 0;
 // gate_up GEMM of the grouped MoE path: 1 hi + lo operands (three MMAs per K
@@ -209,6 +213,9 @@ gguf_status gguf_get_rows(const void *table, int tt, int64_t rows, int64_t k, co
 
 size_t gguf_mul_mat_ws_size(int wt, int64_t n, int64_t k, int xt, int64_t m, int yt) {
     if (m <= 0 || k <= 0 || k % 32) return 0;
+    if (use_mmq(wt, m, k) && lib_engine(m, k, yt))   // fp16 activation rows, the fp16 weights, fp32 rows (BF16 out)
+        return align256((size_t)(m * k * 2)) + align256((size_t)(n * k * 2)) +
+               (yt == GGUF_BF16 ? align256((size_t)(m * n * 4)) : 0);
     if (use_mmq(wt, m, k)) {
         // fp16 operand rows (plus their low parts for fp32 outputs), plus fp32
         // partial sums when K is split across CTAs (small m)
@@ -261,6 +268,30 @@ static gguf_status mul_mat_impl(int wt, const gguf_segment *segs, int nseg, int6
     if (need > 0 && !aligned(ws, 16)) return fail(GGUF_ERR_ALIGNMENT, "%s: workspace must be 16-byte aligned", what);
     cudaStream_t s = (cudaStream_t)stream;
 
+    if (use_mmq(wt, m, k) && lib_engine(m, k, yt)) {
+        // dequantize + library GEMM: the activations' fp16 operand d16 * q (no
+        // min-term correction columns), each weight matrix dequantized to fp16
+        uint16_t *xh = (uint16_t *)ws;
+        uint16_t *wh = (uint16_t *)((uint8_t *)ws + align256((size_t)(m * k * 2)));
+        float *yf = (float *)((uint8_t *)wh + align256((size_t)(n_max * k * 2)));   // BF16 out: fp32 rows first
+        cudaError_t e = xt == GGUF_Q8_1 ? launch_q8_1_to_f16((const uint8_t *)x, m, k, xh, nullptr, s, k)
+                                        : launch_quantize_q8_1(x, xt, m, k, ldx, nullptr, xh, nullptr, s, k);
+        if (e != cudaSuccess) return cuda_status(e, what);
+        for (int i = 0; i < nseg; i++) {
+            if (segs[i].n == 0) continue;
+            if ((e = launch_dequantize((const uint8_t *)segs[i].w, wt, segs[i].n, k, nullptr, 0, wh, GGUF_F16, s)) !=
+                cudaSuccess)
+                return cuda_status(e, what);
+            e = yt == GGUF_BF16 ? library_gemm_f16(wh, xh, segs[i].n, m, k, yf, GGUF_F32, segs[i].n, s)
+                                : library_gemm_f16(wh, xh, segs[i].n, m, k, segs[i].y, yt, segs[i].ldy, s);
+            if (e == cudaErrorNotSupported)
+                return fail(GGUF_ERR_CUDA, "%s: option mmq_engine = 1 needs cuBLAS, which could not be loaded", what);
+            if (e == cudaSuccess && yt == GGUF_BF16)
+                e = launch_convert_rows(yf, m, segs[i].n, segs[i].y, yt, segs[i].ldy, s);
+            if (e != cudaSuccess) return cuda_status(e, what);
+        }
+        return GGUF_OK;
+    }
     if (use_mmq(wt, m, k)) {
         const int64_t kx = op_pitch(wt, k);
         uint8_t *wp = (uint8_t *)ws;
@@ -712,6 +743,11 @@ gguf_status gguf_set_option(const char *key, int64_t value) {
         g_moe_gate_up_precise = value != 0;
         return GGUF_OK;
     }
+    if (!strcmp(key, "mmq_engine")) {
+        if (value != 0 && value != 1) return fail(GGUF_ERR_INVALID_ARG, "set_option: mmq_engine must be 0 or 1");
+        g_mmq_engine = value;
+        return GGUF_OK;
+    }
     return fail(GGUF_ERR_INVALID_ARG, "set_option: unknown key '%s'", key);
 }
 
@@ -727,6 +763,7 @@ int64_t gguf_get_option(const char *key) {
     if (!strcmp(key, "moe_deterministic")) return g_moe_deterministic;
     if (!strcmp(key, "moe_down_precise")) return g_moe_down_precise;
     if (!strcmp(key, "moe_gate_up_precise")) return g_moe_gate_up_precise;
+    if (!strcmp(key, "mmq_engine")) return g_mmq_engine;
     if (!strcmp(key, "mmq_bn_max")) return g_mmq_bn_max;
     if (!strcmp(key, "mmq_split_k")) return g_mmq_split_k;
     return -1;

@@ -119,6 +119,14 @@ cudaError_t launch_mmvq_join(cudaStream_t s);
 cudaError_t launch_mmq(const uint8_t *w, int wt, int64_t n, int64_t k, const uint16_t *xh, const uint16_t *xl,
                        int64_t m, void *y, int yt, int64_t ldy, float *yacc, cudaStream_t s);
 cudaError_t launch_convert_rows(const float *yacc, int64_t m, int64_t n, void *y, int yt, int64_t ldy, cudaStream_t s);
+// the library-GEMM engine (libgemm.cu): y[m][ldy] (F32 / F16) = X[m][k] .
+// W[n][k]^T with fp16 operands and fp32 accumulation, by cuBLAS opened at run
+// time; cudaErrorNotSupported when cuBLAS cannot be loaded
+cudaError_t library_gemm_f16(const uint16_t *w, const uint16_t *x, int64_t n, int64_t m, int64_t k, void *y, int yt,
+                             int64_t ldy, cudaStream_t s);
+// option "mmq_engine" (default 0): 1 runs the prefill products with 16-bit
+// outputs as dequantize + library GEMM instead of the fused tensor-core MMQ
+int64_t option_mmq_engine();
 
 // ---- MoE (moe.cu)
 struct MoeWs {

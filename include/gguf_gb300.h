@@ -416,6 +416,19 @@ gguf_status gguf_debug_block_dots(const void *w, int wt, int64_t n, int64_t k, c
  *   "moe_gate_up_precise": 1 (default) runs the grouped gate_up GEMM on hi + lo
  *                   operands (three MMAs per K step); 0 on one fp16 operand
  *                   per side.
+ *   "mmq_engine"  : 0 (default) runs the prefill (MMQ-range) products on the
+ *                   fused tensor-core MMQ; 1 runs those with BF16 / F16
+ *                   outputs as dequantize (weights -> fp16) + one library GEMM
+ *                   (cuBLAS, opened at run time: GGUF_ERR_CUDA when it cannot
+ *                   be loaded) on the activations' fp16 q8_1 operand, the
+ *                   alternative engine FreeToken PR #196 ("Gains") races
+ *                   against MMQ.  Its workspace adds n * k * 2 bytes (the
+ *                   fp16 weights) and, for BF16 outputs, m * n * 4 (the GEMM
+ *                   writes fp32 rows that one pass converts), and its min
+ *                   terms use d_a * sum(q) instead
+ *                   of the stored s_a (about 1e-3 of the row rms), within
+ *                   the 16-bit output bound.  FP32 outputs keep the fused
+ *                   MMQ.
  * Returns GGUF_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 gguf_status gguf_set_option(const char *key, int64_t value);

@@ -115,6 +115,9 @@ def test_other_entry_points_reject_bad_arguments(g):
     assert L.gguf_set_option(b"moe_gate_up_precise", 0) == 0 and L.gguf_get_option(b"moe_gate_up_precise") == 0
     assert L.gguf_set_option(b"moe_gate_up_precise", 1) == 0
     assert L.gguf_get_option(b"mmq_bn_max") == 256 and L.gguf_get_option(b"mmq_split_k") == 1
+    assert L.gguf_get_option(b"mmq_engine") == 0 and L.gguf_set_option(b"mmq_engine", 2) != 0
+    assert L.gguf_set_option(b"mmq_engine", 1) == 0 and L.gguf_get_option(b"mmq_engine") == 1
+    assert L.gguf_set_option(b"mmq_engine", 0) == 0
 
 
 def _moe(g, **kw):

@@ -164,3 +164,44 @@ def test_mmq_staged_weights_against_oracle(g, stage_option, wt, n, k, m, dtype):
     # both ways feed the MMA the same operand values; only the order of the
     # fp32 accumulation may differ between the split-K partial sums
     assert_close(ys[0], ys[1], 1e-5 if dtype == torch.float32 else TOL_BF16, "staged vs global loads")
+
+
+@pytest.fixture
+def lib_engine(g):
+    """Option mmq_engine = 1 for the test: prefill products with 16-bit
+    outputs run as dequantize + library GEMM."""
+    g.gguf_set_option("mmq_engine", 1)
+    yield
+    g.gguf_set_option("mmq_engine", 0)
+
+
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.MXFP4])
+@pytest.mark.parametrize("m,out", [(64, torch.bfloat16), (300, torch.bfloat16), (129, torch.float16)])
+def test_mmq_library_engine_against_oracle_and_fused(g, lib_engine, wt, m, out):
+    # the dequantize + library GEMM engine against the oracle at the 16-bit
+    # bound, and against the fused tensor-core MMQ on the same inputs (the
+    # engines differ by accumulation order and, for Q4_K / Q5_K, the min term's
+    # use of d_a * sum(q) in place of the stored s_a)
+    n, k = 520, 1024
+    w = _weights(wt, n, k, seed=m + wt, safe=True)
+    x = synth.activations(m, k, seed=m, dtype=out)
+    ref = oracle.mul_mat(wt, w, k, oracle.quantize_q8_1(x.float().numpy()))
+    y1 = g.gguf_mul_mat(_u8(w), wt, n, k, x.to(DEV)).float().cpu().numpy()
+    g.gguf_set_option("mmq_engine", 0)
+    y0 = g.gguf_mul_mat(_u8(w), wt, n, k, x.to(DEV)).float().cpu().numpy()
+    assert_close(y1, ref, TOL_BF16, f"library engine type {wt} m {m}")
+    assert_close(y1, y0, TOL_BF16, f"library engine vs fused MMQ type {wt} m {m}")
+
+
+def test_mmq_library_engine_keeps_fp32_on_fused_path(g, lib_engine):
+    # fp32 outputs need the hi + lo operands of the fused MMQ: the option leaves
+    # them on it (the 1e-3 bound holds; split-K sums may differ in order only)
+    n, k, m = 300, 1024, 40
+    w = _weights(oracle.Q4_K, n, k, seed=7)
+    x = synth.activations(m, k, seed=8, dtype=torch.float32)
+    ref = oracle.mul_mat(oracle.Q4_K, w, k, oracle.quantize_q8_1(x.numpy()))
+    a = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x.to(DEV)).cpu().numpy()
+    g.gguf_set_option("mmq_engine", 0)
+    b = g.gguf_mul_mat(_u8(w), oracle.Q4_K, n, k, x.to(DEV)).cpu().numpy()
+    assert_close(a, ref, TOL_F32, "fp32 output with mmq_engine = 1")
+    assert_close(a, b, 1e-5, "fp32 output with and without the option")
