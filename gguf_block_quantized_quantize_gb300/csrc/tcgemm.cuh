@@ -812,7 +812,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
 #pragma unroll
                         for (int cc = 1; cc < BN / 32; cc++)
                             if (c == cc) rt_l = rtv[cc];
-#pragma unroll 2
+#pragma unroll 4
                         for (int jj = q; jj < 32; jj += 4) {
                             const int j = 32 * c + jj;
                             if (j >= d.n_eff) break;  // uniform within the warp
