@@ -147,26 +147,46 @@ __global__ void moe_finalize_kernel(const float *__restrict__ z, const int32_t *
     float acc[V];
 #pragma unroll
     for (int v = 0; v < V; v++) acc[v] = 0.0f;
-    for (int64_t k = 0; k < top_k; k++) {
-        const int64_t r = t * top_k + k;
-        const int32_t pr = pos[r];
-        if (pr < 0) continue;
-        const float w = route_w ? route_w[r] : 1.0f;
-        // grouped rows are stored in 128-column blocks of R rows
-        const int64_t zi = offsets ? ((((c >> 7) * T * top_k) + offsets[ids[r]] + pr) << 7) + (c & 127) : r * n + c;
+    // routes in groups of 8: every index and z load of a group is issued before
+    // the group's products are added, in slot order
+    constexpr int KG = 8;
+    for (int64_t k0 = 0; k0 < top_k; k0 += KG) {
+        int64_t zi[KG];
+        float wk[KG];
+#pragma unroll
+        for (int j = 0; j < KG; j++) {
+            const int64_t r = t * top_k + k0 + j;
+            const int32_t pr = k0 + j < top_k ? pos[r] : -1;
+            wk[j] = pr < 0 ? 0.0f : (route_w ? route_w[r] : 1.0f);
+            // grouped rows are stored in 128-column blocks of R rows
+            zi[j] = pr < 0 ? -1
+                           : offsets ? ((((c >> 7) * T * top_k) + offsets[ids[r]] + pr) << 7) + (c & 127) : r * n + c;
+        }
         if (V == 4) {
-            const float4 zv = *reinterpret_cast<const float4 *>(z + zi);
-            acc[0] = fmaf(w, zv.x, acc[0]);
-            acc[1] = fmaf(w, zv.y, acc[1]);
-            acc[2] = fmaf(w, zv.z, acc[2]);
-            acc[3] = fmaf(w, zv.w, acc[3]);
+            float4 zv[KG];
+#pragma unroll
+            for (int j = 0; j < KG; j++)
+                zv[j] = zi[j] < 0 ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : *reinterpret_cast<const float4 *>(z + zi[j]);
+#pragma unroll
+            for (int j = 0; j < KG; j++) {
+                if (zi[j] < 0) continue;   // a skipped route adds nothing (not even a zero)
+                acc[0] = fmaf(wk[j], zv[j].x, acc[0]);
+                acc[1] = fmaf(wk[j], zv[j].y, acc[1]);
+                acc[2] = fmaf(wk[j], zv[j].z, acc[2]);
+                acc[3] = fmaf(wk[j], zv[j].w, acc[3]);
+            }
         } else {
 #pragma unroll
-            for (int v = 0; v < V; v++) {
-                const int64_t cv = c + v;
-                const int64_t zv = offsets ? ((((cv >> 7) * T * top_k) + offsets[ids[r]] + pr) << 7) + (cv & 127)
-                                           : r * n + cv;
-                acc[v] = fmaf(w, z[zv], acc[v]);
+            for (int j = 0; j < KG; j++) {
+                if (zi[j] < 0) continue;
+                const int64_t r = t * top_k + k0 + j;
+#pragma unroll
+                for (int v = 0; v < V; v++) {
+                    const int64_t cv = c + v;
+                    const int64_t zv = offsets ? ((((cv >> 7) * T * top_k) + offsets[ids[r]] + pos[r]) << 7) + (cv & 127)
+                                               : r * n + cv;
+                    acc[v] = fmaf(wk[j], z[zv], acc[v]);
+                }
             }
         }
     }
