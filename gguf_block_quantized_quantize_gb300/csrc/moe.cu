@@ -56,6 +56,42 @@ __global__ void moe_count_kernel(const int32_t *__restrict__ ids, const float *_
     pos[r] = ok ? atomicAdd(&counts[e], 1) : -1;
 }
 
+// The same counts with a per-CTA histogram in shared memory (E <= 8192): each
+// CTA takes MOE_COUNT_CHUNK consecutive routes, gives each active one its
+// place among the CTA's routes of its expert, then adds the CTA's count of
+// every expert to counts[] once (one global atomic per expert and CTA instead
+// of one per route) and shifts its routes' places by the returned base.
+constexpr int MOE_COUNT_CHUNK = 4096;
+__global__ void __launch_bounds__(256) moe_count_smem_kernel(const int32_t *__restrict__ ids,
+                                                             const float *__restrict__ rw, int64_t R, int64_t E,
+                                                             int skip_zero_w, int32_t *__restrict__ counts,
+                                                             int32_t *__restrict__ pos,
+                                                             int32_t *__restrict__ dev_status) {
+    extern __shared__ int32_t hist[];   // [E] local counts, then the global bases
+    for (int64_t e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int64_t r0 = (int64_t)blockIdx.x * MOE_COUNT_CHUNK;
+    const int64_t r1 = r0 + MOE_COUNT_CHUNK < R ? r0 + MOE_COUNT_CHUNK : R;
+    int bad = 0;
+    for (int64_t r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+        const int32_t e = ids[r];
+        const bool ok = e >= 0 && e < E && !(skip_zero_w && rw != nullptr && rw[r] == 0.0f);
+        bad += e >= E;
+        pos[r] = ok ? atomicAdd(&hist[e], 1) : -1;
+    }
+    if (bad && dev_status != nullptr) atomicAdd(dev_status, bad);
+    __syncthreads();
+    for (int64_t e = threadIdx.x; e < E; e += blockDim.x) {
+        const int32_t c = hist[e];
+        hist[e] = c ? atomicAdd(&counts[e], c) : 0;
+    }
+    __syncthreads();
+    for (int64_t r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+        const int32_t p = pos[r];
+        if (p >= 0) pos[r] = p + hist[ids[r]];
+    }
+}
+
 // the route marks of the route-batched path: pos[r] = r for an active route,
 // -1 for a skipped one (same rules as moe_count_kernel; no grouping needed)
 __global__ void moe_mark_kernel(const int32_t *__restrict__ ids, const float *__restrict__ rw, int64_t R, int64_t E,
@@ -276,7 +312,11 @@ cudaError_t moe_group(const int32_t *ids, const float *rw, int64_t R, int64_t E,
     cudaError_t e = cudaMemsetAsync(w.counts, 0, sizeof(int32_t) * (size_t)E, s);
     if (e != cudaSuccess) return e;
     const unsigned g = (unsigned)((R + 255) / 256);
-    if (R > 0) moe_count_kernel<<<g, 256, 0, s>>>(ids, rw, R, E, skip_zero_w ? 1 : 0, w.counts, w.pos, status);
+    if (R > 0 && E <= 8192)
+        moe_count_smem_kernel<<<(unsigned)((R + MOE_COUNT_CHUNK - 1) / MOE_COUNT_CHUNK), 256, (size_t)E * 4, s>>>(
+            ids, rw, R, E, skip_zero_w ? 1 : 0, w.counts, w.pos, status);
+    else if (R > 0)
+        moe_count_kernel<<<g, 256, 0, s>>>(ids, rw, R, E, skip_zero_w ? 1 : 0, w.counts, w.pos, status);
     moe_scan_kernel<<<1, 1024, 0, s>>>(w.counts, E, bn, w.offsets, w.tile_expert, w.tile_start, w.n_tiles);
     if (R > 0) moe_scatter_kernel<<<g, 256, 0, s>>>(ids, w.pos, R, w.offsets, w.route_list);
     return cudaGetLastError();
