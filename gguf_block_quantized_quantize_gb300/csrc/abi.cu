@@ -650,8 +650,7 @@ gguf_status gguf_moe_ffn(const gguf_moe_ffn_args *a, void *ws, size_t ws_bytes, 
         if ((e = launch_mmvq_routes(a->gate_up_type, (const uint8_t *)a->w_gate_up,
                                     MmvqRoutes{a->ids, w.pos, a->gate_up_stride, a->top_k, 0}, 2 * a->inter, a->hidden,
                                     xq, R, w.zv, s)) != cudaSuccess ||
-            (e = launch_moe_swiglu(w.zv, w.pos, R, a->inter, w.hb, s)) != cudaSuccess ||
-            (e = launch_quantize_q8_1(w.hb, GGUF_BF16, R, a->inter, a->inter, hq, nullptr, nullptr, s)) != cudaSuccess)
+            (e = launch_moe_swiglu_q8_1(w.zv, w.pos, R, a->inter, hq, s)) != cudaSuccess)
             return cuda_status(e, "moe_ffn gate_up");
         if ((e = launch_mmvq_routes(a->down_type, (const uint8_t *)a->w_down,
                                     MmvqRoutes{a->ids, w.pos, a->down_stride, a->top_k, 1}, a->hidden, a->inter, hq, R,

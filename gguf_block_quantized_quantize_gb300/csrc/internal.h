@@ -147,6 +147,10 @@ MoeWs moe_ws_layout(void *base, int64_t E, int64_t R, int64_t xh_elems, int64_t 
 // h[r][j] = bf16(silu(g) * u) of the vector gate_up rows z[r] = (g[0..I), u[0..I));
 // zeros for skipped routes (pos[r] < 0)
 cudaError_t launch_moe_swiglu(const float *z, const int32_t *pos, int64_t R, int64_t I, uint16_t *h, cudaStream_t s);
+// the same h quantized to q8_1 rows hq[R][I / 32] in the same pass (the bits
+// that launch_moe_swiglu followed by the q8_1 quantize give)
+cudaError_t launch_moe_swiglu_q8_1(const float *z, const int32_t *pos, int64_t R, int64_t I, uint8_t *hq,
+                                  cudaStream_t s);
 int moe_bn(int64_t routes, int64_t experts);
 cudaError_t moe_group(const int32_t *ids, const float *rw, int64_t R, int64_t E, bool skip_zero_w, int32_t *status,
                       const MoeWs &w, int bn, cudaStream_t s);

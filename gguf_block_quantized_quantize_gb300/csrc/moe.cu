@@ -230,8 +230,8 @@ __global__ void moe_finalize_kernel(const float *__restrict__ z, const int32_t *
     for (int v = 0; v < V; v++) store_out(y, yt, i + v, acc[v]);
 }
 
-// SwiGLU of the route-batched gate_up: h = silu(g) * u in fp32 (the formula
-// of the tensor-core epilogue), rounded to bf16, the activation dtype
+// SwiGLU of the route-batched gate_up: h = silu(g) * u in fp32 (IEEE exp and
+// division), rounded to bf16, the activation dtype
 __global__ void moe_swiglu_kernel(const float *__restrict__ z, const int32_t *__restrict__ pos, int64_t R, int64_t I,
                                   uint16_t *__restrict__ h) {
     asm volatile("griddepcontrol.wait;" ::: "memory");   // z comes from the previous kernel
@@ -245,6 +245,61 @@ __global__ void moe_swiglu_kernel(const float *__restrict__ z, const int32_t *__
         bits = f2bf_rn(g / (1.0f + expf(-g)) * u);
     }
     h[i] = bits;
+}
+
+// The same SwiGLU and the q8_1 quantization of h in one pass (the down
+// product's input): four threads per 32-value block, each rounding 8 values
+// of h to bf16 and quantizing them by the rule of the q8_1 quantize kernel
+// (d = amax / 127, q = roundf(h / d), s = fp16(d * sum q)), so the blocks are
+// the bits that quantizing the bf16 rows gives.  Skipped routes get zero
+// blocks, as their zero rows would.
+__global__ void __launch_bounds__(256) moe_swiglu_q8_1_kernel(const float *__restrict__ z,
+                                                              const int32_t *__restrict__ pos, int64_t R, int64_t I,
+                                                              uint8_t *__restrict__ hq) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // z comes from the previous kernel
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int64_t nb = I / 32;
+    const int64_t gidx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t blk = gidx >> 2;
+    const int j = (int)(gidx & 3);
+    const bool in = blk < R * nb;
+    const int64_t r = in ? blk / nb : 0, b = in ? blk - r * nb : 0;
+    const bool on = in && pos[r] >= 0;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        float hx = 0.0f;
+        if (on) {
+            const int64_t c = b * 32 + 8 * j + i;
+            const float g = z[r * 2 * I + c], u = z[r * 2 * I + I + c];
+            hx = bf2f(f2bf_rn(g / (1.0f + expf(-g)) * u));
+        }
+        v[i] = hx;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float d = __fdiv_rn(amax, 127.0f);
+    int q[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        q[i] = (d != 0.0f) ? (int)roundf(__fdiv_rn(v[i], d)) : 0;
+        sum += q[i];
+    }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    if (!in) return;
+    uint8_t *o = hq + blk * Q8_1_BYTES;
+    const uint32_t w0 = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) | ((uint32_t)(q[3] & 0xff) << 24);
+    const uint32_t w1 = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) | ((uint32_t)(q[7] & 0xff) << 24);
+    reinterpret_cast<uint32_t *>(o + 4 + 8 * j)[0] = w0;
+    reinterpret_cast<uint32_t *>(o + 4 + 8 * j)[1] = w1;
+    if (j == 0) {
+        const uint16_t dh = f2h_rn(d), sh = f2h_rn(__fmul_rn(d, (float)sum));
+        *reinterpret_cast<uint32_t *>(o) = (uint32_t)dh | ((uint32_t)sh << 16);
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -446,6 +501,13 @@ cudaError_t launch_moe_finalize(const float *z, const int32_t *pos, const int32_
                           top_k, n, y, yt);
     return launch_pdl(moe_finalize_kernel<1>, (count + 255) / 256, 256, s, z, pos, ids, offsets, route_w, T, top_k, n,
                       y, yt);
+}
+
+cudaError_t launch_moe_swiglu_q8_1(const float *z, const int32_t *pos, int64_t R, int64_t I, uint8_t *hq,
+                                  cudaStream_t s) {
+    const int64_t threads = R * (I / 32) * 4;
+    if (threads == 0) return cudaSuccess;
+    return launch_pdl(moe_swiglu_q8_1_kernel, (threads + 255) / 256, 256, s, z, pos, R, I, hq);
 }
 
 cudaError_t launch_moe_swiglu(const float *z, const int32_t *pos, int64_t R, int64_t I, uint16_t *h, cudaStream_t s) {
