@@ -89,9 +89,14 @@ __device__ __forceinline__ uint32_t lds4(const uint8_t *p) {
     }
 }
 
-inline int sb_nb(int wt) { return wt == GGUF_MXFP4 ? SbTraits<GGUF_MXFP4>::NB : 8; }
+template <int WT>
+constexpr int sb_item_bytes_t() { return SbTraits<WT>::NB * SbTraits<WT>::BB; }
+inline int sb_nb(int wt) {
+    return wt == GGUF_Q8_0 ? SbTraits<GGUF_Q8_0>::NB : wt == GGUF_Q4_0 ? SbTraits<GGUF_Q4_0>::NB : SbTraits<GGUF_MXFP4>::NB;
+}
 inline int64_t sb_item_bytes(int wt) {
-    return wt == GGUF_Q8_0 ? 8 * Q8_0_BYTES : wt == GGUF_Q4_0 ? 8 * Q4_0_BYTES : 16 * MXFP4_BYTES;
+    return wt == GGUF_Q8_0 ? sb_item_bytes_t<GGUF_Q8_0>()
+           : wt == GGUF_Q4_0 ? sb_item_bytes_t<GGUF_Q4_0>() : sb_item_bytes_t<GGUF_MXFP4>();
 }
 inline int sb_nbuf(int wt) {
     return wt == GGUF_Q8_0 ? SbTraits<GGUF_Q8_0>::NBUF
