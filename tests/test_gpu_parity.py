@@ -345,7 +345,7 @@ def test_mmvq_tensor_core_small_block_exact_integer_sums(g, wt, m, n):
     k = 512
     rng = np.random.default_rng(m + n + wt)
     if wt == oracle.Q8_0:
-        qv = rng.integers(-127, 128, size=(n, k), dtype=np.int64)
+        qv = rng.integers(-128, 128, size=(n, k), dtype=np.int64)   # the full int8 range
         w, vals = _q8_0_plain(qv), qv
     elif wt == oracle.Q4_0:
         qv = rng.integers(0, 16, size=(n, k), dtype=np.int64)
