@@ -157,3 +157,33 @@ def test_mul_mat_batch_matches_segment_calls(g, wt):
         for j, job_outs in enumerate(outs):
             for o, s_ in zip(job_outs, sep[j]):
                 assert torch.equal(o, s_), f"prepared batch job {j} differs from the segment call"
+
+
+def test_decode_step_as_benchmarked_full_size_sampled(g):
+    """The benchmarked decode step itself: bench.py's Decode object (Q4_K
+    4096x4096 and 14336x4096, K = 4096, random packed blocks with safe scales,
+    copies rotating past L2), one q8_1 quantization of the 15 activation rows,
+    and the four M-products as one gguf_mul_mat_batch chain in the timed order.
+    Every output matrix is checked against the oracle on 256 sampled rows plus
+    the first and last, for every token."""
+    import bench
+
+    dec = bench.Decode(torch, g, synth, torch.device(DEV))
+    for y in dec.ys.values():
+        y.fill_(float("nan"))
+    dec.step()
+    torch.cuda.synchronize()
+    k = dec.k
+    for (n, kk) in bench.DECODE_SHAPES:
+        assert kk == k
+        base = synth.safe_blocks(oracle.Q4_K, n, k, seed=n)   # every rotating copy holds these bytes
+        assert torch.equal(dec.pools[(n, k)][0].cpu(), torch.from_numpy(base))
+        rows = np.sort(np.random.default_rng(n).choice(n, 256, replace=False))
+        rows[0], rows[-1] = 0, n - 1
+        for m in bench.DECODE_MS:
+            xq_ref = oracle.quantize_q8_1(dec.xs[m].float().cpu().numpy())
+            assert np.array_equal(dec.xqs[m].cpu().numpy(), xq_ref.reshape(m, -1)), f"q8_1 rows of M = {m}"
+            ref = oracle.mul_mat(oracle.Q4_K, base[rows], k, xq_ref)
+            y = dec.ys[(n, m)].float().cpu().numpy()
+            assert np.isfinite(y).all(), f"{n} x {k}, M = {m}: an output was not written"
+            assert_close(y[:, rows], ref, TOL_BF16, f"decode step {n} x {k}, M = {m}")
