@@ -394,10 +394,12 @@ def mmvq_traffic():
 def run_e2e(args, g, torch, dev, dec, per_step):
     """Same workload through the public API with host buffers: each step copies
     its activations from pinned host memory, quantizes them, runs the four
-    M-products as one gguf_mul_mat_batch call and reads its outputs back, on
-    one stream.  The batch call's arguments are marshalled once per weight
-    phase (PreparedBatch), as an engine replaying its decode step would, so the
-    host issues four calls per step."""
+    M-products as one gguf_mul_mat_batch call and copies its outputs back to
+    pinned host memory, on one stream.  Both copies go through gguf_copy_async
+    (on the SMs, chained with the step's launches; a copy-engine copy costs
+    about 5 us of latency and ends the chain).  The batch call's arguments are
+    marshalled once per weight phase (PreparedBatch), as an engine replaying
+    its decode step would, so the host issues four calls per step."""
     hx = dec.x_all.cpu().pin_memory()
     hy = torch.empty(dec.y_all.shape, dtype=dec.y_all.dtype).pin_memory()
     dx = torch.empty_like(dec.x_all)
@@ -409,11 +411,11 @@ def run_e2e(args, g, torch, dev, dec, per_step):
     it = [0]
 
     def step():
-        dx.copy_(hx, non_blocking=True)
+        g.gguf_copy(dx, hx)
         g.gguf_quantize_q8_1(dx, out=dec.xq_all)
         prepared[it[0] % len(prepared)].run()
         it[0] += 1
-        hy.copy_(dec.y_all, non_blocking=True)
+        g.gguf_copy(hy, dec.y_all)
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -427,7 +429,8 @@ def run_e2e(args, g, torch, dev, dec, per_step):
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / args.steps
     return {"value": round(per_step / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5)}
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5),
+            "copies": "gguf_copy_async: pinned host <-> device on the SMs, in the step's launch chain"}
 
 
 # --------------------------------------------------------------------------

@@ -78,6 +78,7 @@ SIGNATURES = {
     "gguf_row_size": (_i64, [_i, _i64]),
     "gguf_quantize_q8_1": (_i, [_p, _i, _i64, _i64, _i64, _p, _p]),
     "gguf_dequantize": (_i, [_p, _i, _i64, _i64, _p, _i, _p]),
+    "gguf_copy_async": (_i, [_p, _p, _i64, _p]),
     "gguf_get_rows": (_i, [_p, _i, _i64, _i64, _p, _i64, _p, _i, _p]),
     "gguf_mul_mat_ws_size": (_sz, [_i, _i64, _i64, _i, _i64, _i]),
     "gguf_mul_mat": (_i, [_p, _i, _i64, _i64, _p, _i, _i64, _i64, _p, _i, _i64, _p, _sz, _p]),
@@ -182,6 +183,22 @@ def gguf_quantize_q8_1(x: torch.Tensor, out: torch.Tensor | None = None) -> torc
         out = torch.empty((m, max(gguf_row_size(Q8_1, k), 0)), dtype=torch.uint8, device=x.device)
     _check(_lib_fast().gguf_quantize_q8_1(_ptr(x), _TYPE_OF[x.dtype], m, k, x.stride(0), _ptr(out), _stream()))
     return out
+
+
+def gguf_copy(dst: torch.Tensor, src: torch.Tensor) -> torch.Tensor:
+    """dst <- src on the current stream through gguf_copy_async (a copy on the
+    SMs): each tensor contiguous and on the GPU or in pinned host memory, both
+    the same number of bytes."""
+    for t, what in ((dst, "dst"), (src, "src")):
+        if not t.is_contiguous():
+            raise ValueError(f"gguf_copy: {what} must be contiguous")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"gguf_copy: {what} must be a CUDA tensor or pinned host memory")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("gguf_copy: dst and src differ in size")
+    _check(_lib_fast().gguf_copy_async(dst.data_ptr(), src.data_ptr(), nbytes, _stream()))
+    return dst
 
 
 def gguf_dequantize(w: torch.Tensor, wt: int, rows: int, k: int, out_dtype=torch.float32,

@@ -195,6 +195,31 @@ gguf_status gguf_dequantize(const void *w, int wt, int64_t rows, int64_t k, void
                        "dequantize");
 }
 
+// whether a kernel may read or write p: device or managed memory, or pinned
+// host memory mapped into the unified address space (pageable host memory is
+// not accessible, and a kernel touching it would fault)
+static bool device_accessible(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
+    return a.type == cudaMemoryTypeHost && a.devicePointer == p;
+}
+
+gguf_status gguf_copy_async(void *dst, const void *src, int64_t bytes, gguf_stream_t stream) {
+    if (bytes < 0) return fail(GGUF_ERR_INVALID_ARG, "copy_async: negative size");
+    if (bytes == 0) return GGUF_OK;
+    if (!dst || !src) return fail(GGUF_ERR_INVALID_ARG, "copy_async: null pointer");
+    if (!device_accessible(dst) || !device_accessible(src))
+        return fail(GGUF_ERR_INVALID_ARG, "copy_async: both buffers must be device, managed or pinned host memory");
+    const uintptr_t d = reinterpret_cast<uintptr_t>(dst), s = reinterpret_cast<uintptr_t>(src);
+    if (d < s + (uintptr_t)bytes && s < d + (uintptr_t)bytes)
+        return fail(GGUF_ERR_INVALID_ARG, "copy_async: the buffers overlap");
+    return cuda_status(launch_copy(dst, src, bytes, (cudaStream_t)stream), "copy_async");
+}
+
 gguf_status gguf_get_rows(const void *table, int tt, int64_t rows, int64_t k, const int32_t *ids, int64_t n_ids,
                           void *out, int ot, gguf_stream_t stream) {
     if (!is_float(ot)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "get_rows: out type %d is not F32/BF16/F16", ot);

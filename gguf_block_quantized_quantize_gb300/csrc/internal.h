@@ -25,6 +25,10 @@ int kernel_occupancy(const void *kern, int threads, size_t smem, cudaError_t *er
 // sets the thread-local message returned by gguf_last_error() and returns st
 gguf_status report(gguf_status st, const char *msg);
 
+// dst[0, bytes) = src[0, bytes) on the SMs, as a programmatic dependent launch;
+// both pointers device-accessible (copy.cu)
+cudaError_t launch_copy(void *dst, const void *src, int64_t bytes, cudaStream_t s);
+
 // q8_1 quantization (xq may be null); also writes the fp16 tensor-core operand
 // xh[m][pitch] = fp16(d16*q) when xh != nullptr, and its low part
 // xl = fp16(d16*q - xh) when xl != nullptr.  pitch > k appends the Q4_K

@@ -229,6 +229,25 @@ gguf_status gguf_mul_mat_noalloc(const void *w, int wt, int64_t n, int64_t k, co
                                  int64_t ldx, void *y, int yt, int64_t ldy, gguf_stream_t stream);
 
 /*
+ * gguf_copy_async -- dst[0, bytes) = src[0, bytes), stream-ordered.  Not a
+ * step of the pages' method: the host <-> device staging that an engine
+ * serving the decode step (FreeToken PR #690 "serve GGUF checkpoints on
+ * vendored ggml-cuda kernels") puts around it.  The copy runs on the SMs as a
+ * programmatic dependent launch, so it stays in the chain of the path's
+ * launches instead of ending it the way a copy-engine copy does.
+ *   dst, src : device, managed or pinned (page-locked) host memory, any
+ *              alignment (16-byte aligned pointers move 16 bytes per load);
+ *              the ranges may not overlap.  The caller keeps both alive until
+ *              the stream has passed the copy.
+ *   bytes    : >= 0 (0 is a no-op).
+ * Errors: GGUF_ERR_INVALID_ARG for a negative size, a null pointer,
+ * overlapping ranges or a buffer that is not device-accessible (pageable host
+ * memory is refused before anything is launched); GGUF_ERR_CUDA for a launch
+ * error.
+ */
+gguf_status gguf_copy_async(void *dst, const void *src, int64_t bytes, gguf_stream_t stream);
+
+/*
  * gguf_mul_mat_batch -- several decode-sized products of one weight type and
  * K in one call, each a gguf_mul_mat_segments on q8_1 rows that were written
  * before the call: job j computes y_s[m_j][n_s] = Xq_j . W_s^T for its

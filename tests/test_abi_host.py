@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gguf_gb300.h")
@@ -211,3 +212,19 @@ def test_mul_mat_batch_argument_checks(g):
     assert "decode-sized" in L.gguf_last_error().decode()
     assert run([job(4, xq=0x20002)]) == 4                  # q8_1 rows must be 4-byte aligned
     assert run([job(0)]) == 0                              # empty jobs are skipped
+
+
+def test_copy_argument_checks(g):
+    L = g.load_library()
+    assert L.gguf_copy_async(None, None, 0, None) == 0          # nothing to copy
+    assert L.gguf_copy_async(FAKE, FAKE, -1, None) == 1         # negative size
+    assert L.gguf_copy_async(None, FAKE, 16, None) == 1         # null pointer
+    # pageable host memory is not device-accessible: refused before any launch
+    buf = ctypes.create_string_buffer(64)
+    assert L.gguf_copy_async(ctypes.addressof(buf), ctypes.addressof(buf) + 32, 16, None) == 1
+    assert "device, managed or pinned" in L.gguf_last_error().decode()
+    # the binding refuses pageable and non-contiguous tensors and size mismatches
+    with pytest.raises(ValueError):
+        g.gguf_copy(torch.zeros(16, dtype=torch.uint8), torch.zeros(16, dtype=torch.uint8))
+    with pytest.raises(ValueError):
+        g.gguf_copy(torch.zeros(4, 4)[:, :2], torch.zeros(8))
