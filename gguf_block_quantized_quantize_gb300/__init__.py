@@ -48,6 +48,11 @@ class MmJob(ctypes.Structure):
                 ("m", ctypes.c_int64)]
 
 
+class MmJobTyped(ctypes.Structure):
+    _fields_ = [("wt", ctypes.c_int), ("k", ctypes.c_int64), ("segs", ctypes.POINTER(Segment)), ("nseg", ctypes.c_int),
+                ("xq", ctypes.c_void_p), ("m", ctypes.c_int64)]
+
+
 MAX_BATCH_JOBS = 8
 
 
@@ -79,6 +84,7 @@ SIGNATURES = {
     "gguf_quantize_q8_1": (_i, [_p, _i, _i64, _i64, _i64, _p, _p]),
     "gguf_dequantize": (_i, [_p, _i, _i64, _i64, _p, _i, _p]),
     "gguf_copy_async": (_i, [_p, _p, _i64, _p]),
+    "gguf_mul_mat_batch_typed": (_i, [ctypes.POINTER(MmJobTyped), _i, _i, _p]),
     "gguf_get_rows": (_i, [_p, _i, _i64, _i64, _p, _i64, _p, _i, _p]),
     "gguf_mul_mat_ws_size": (_sz, [_i, _i64, _i64, _i, _i64, _i]),
     "gguf_mul_mat": (_i, [_p, _i, _i64, _i64, _p, _i, _i64, _i64, _p, _i, _i64, _p, _sz, _p]),
@@ -296,6 +302,38 @@ def gguf_mul_mat_batch(wt: int, k: int, jobs):
         return outs
     carr = (MmJob * len(cjobs))(*cjobs)
     _check(_lib_fast().gguf_mul_mat_batch(wt, k, carr, len(cjobs), yt, _stream()))
+    return outs
+
+
+def _typed_jobs(jobs, what):
+    """ctypes typed jobs of [(wt, k, xq, [(w, n, out), ...]), ...]: the arrays
+    to keep alive, the jobs, the outputs per job and the one output type."""
+    keep, cjobs, outs, yt = [], [], [], None
+    for wt, k, xq, segs in jobs:
+        if xq.dim() != 2 or (xq.shape[0] > 1 and xq.stride(0) != k // 32 * Q8_1_BYTES):
+            raise ValueError(f"{what}: q8_1 rows of xq must be contiguous")
+        for (_, _, o) in segs:
+            t = _TYPE_OF[o.dtype]
+            if o.stride(1) != 1 or (yt is not None and t != yt):
+                raise ValueError(f"{what}: outputs need contiguous rows and one dtype")
+            yt = t
+        arr = (Segment * len(segs))(*[Segment(_ptr(w), n, _ptr(o), o.stride(0)) for (w, n, o) in segs])
+        keep.append((xq, segs, arr))
+        cjobs.append(MmJobTyped(wt, k, arr, len(segs), _ptr(xq), xq.shape[0]))
+        outs.append([o for (_, _, o) in segs])
+    return keep, cjobs, outs, yt
+
+
+def gguf_mul_mat_batch_typed(jobs):
+    """gguf_mul_mat_batch with the weight type and K per job: ``jobs`` is a
+    list of (wt, k, xq [m, row bytes] uint8, [(w, n, out), ...]).  The outputs
+    share one dtype; they are returned per job."""
+    keep, cjobs, outs, yt = _typed_jobs(jobs, "gguf_mul_mat_batch_typed")
+    if not cjobs:
+        return outs
+    carr = (MmJobTyped * len(cjobs))(*cjobs)
+    _check(_lib_fast().gguf_mul_mat_batch_typed(carr, len(cjobs), yt, _stream()))
+    del keep
     return outs
 
 

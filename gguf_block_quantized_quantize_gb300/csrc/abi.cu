@@ -386,19 +386,24 @@ gguf_status gguf_mul_mat_segments(int wt, const gguf_segment *segs, int nseg, in
     return mul_mat_impl(wt, segs, nseg, k, x, xt, m, ldx, yt, ws, ws_bytes, stream, "mul_mat_segments");
 }
 
-gguf_status gguf_mul_mat_batch(int wt, int64_t k, const gguf_mm_job *jobs, int njobs, int yt, gguf_stream_t stream) {
-    const char *what = "mul_mat_batch";
-    if (!is_weight(wt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "%s: weight type %d not supported", what, wt);
+// The batch of decode-sized products behind gguf_mul_mat_batch and
+// gguf_mul_mat_batch_typed: every job validated before any launch, then one
+// chain of programmatic dependent launches closed by an ordinary empty one.
+static gguf_status mul_mat_batch_impl(const char *what, const gguf_mm_job_typed *jobs, int njobs, int yt,
+                                      gguf_stream_t stream) {
     if (!is_float(yt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "%s: y type %d is not F32/BF16/F16", what, yt);
     if (njobs < 0 || njobs > GGUF_MAX_BATCH_JOBS || (njobs > 0 && !jobs))
         return fail(GGUF_ERR_INVALID_ARG, "%s: %d jobs (0..%d)", what, njobs, GGUF_MAX_BATCH_JOBS);
-    if (k < 0) return fail(GGUF_ERR_INVALID_ARG, "%s: negative size", what);
-    if (row_size(wt, k) < 0) return fail(GGUF_ERR_SHAPE, "%s: k=%lld not a multiple of the block of type %d", what, (long long)k, wt);
-    // validate every job before launching any
     MmvqSegs sgs[GGUF_MAX_BATCH_JOBS];
     int live = 0;
     for (int j = 0; j < njobs; j++) {
-        const gguf_mm_job &jb = jobs[j];
+        const gguf_mm_job_typed &jb = jobs[j];
+        const int wt = jb.wt;
+        const int64_t k = jb.k;
+        if (!is_weight(wt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "%s: job %d: weight type %d not supported", what, j, wt);
+        if (k < 0) return fail(GGUF_ERR_INVALID_ARG, "%s: job %d: negative size", what, j);
+        if (row_size(wt, k) < 0)
+            return fail(GGUF_ERR_SHAPE, "%s: job %d: k=%lld not a multiple of the block of type %d", what, j, (long long)k, wt);
         if (jb.nseg < 1 || jb.nseg > GGUF_MAX_SEGMENTS || !jb.segs)
             return fail(GGUF_ERR_INVALID_ARG, "%s: job %d has %d segments (1..%d)", what, j, jb.nseg, GGUF_MAX_SEGMENTS);
         if (jb.m < 0) return fail(GGUF_ERR_INVALID_ARG, "%s: job %d: negative m", what, j);
@@ -421,7 +426,7 @@ gguf_status gguf_mul_mat_batch(int wt, int64_t k, const gguf_mm_job *jobs, int n
             sg.nseg++;
         }
         if (jb.m == 0 || acc == 0) continue;   // nothing to compute
-        if (k == 0) return fail(GGUF_ERR_SHAPE, "%s: k must be positive", what);
+        if (k == 0) return fail(GGUF_ERR_SHAPE, "%s: job %d: k must be positive", what, j);
         if (!jb.xq || !aligned(jb.xq, 4)) return fail(GGUF_ERR_ALIGNMENT, "%s: job %d: q8_1 input null or misaligned", what, j);
         if (use_mmq(wt, jb.m, k) || (jb.m > 8 && !mmvq_tc_wide(wt, k, jb.m)))
             return fail(GGUF_ERR_INVALID_ARG, "%s: job %d: m=%lld is not decode-sized (the MMVQ range)", what, j,
@@ -435,11 +440,28 @@ gguf_status gguf_mul_mat_batch(int wt, int64_t k, const gguf_mm_job *jobs, int n
         if (jobs[j].m == 0 || sg.nseg == 0) continue;
         sg.chain = live == 1 ? 0 : (pos == 0 ? 1 : 2);
         pos++;
-        cudaError_t e = launch_mmvq(sg, wt, k, (const uint8_t *)jobs[j].xq, jobs[j].m, yt, s);
+        cudaError_t e = launch_mmvq(sg, jobs[j].wt, jobs[j].k, (const uint8_t *)jobs[j].xq, jobs[j].m, yt, s);
         if (e != cudaSuccess) return cuda_status(e, what);
     }
     if (live > 1) return cuda_status(launch_mmvq_join(s), what);
     return GGUF_OK;
+}
+
+gguf_status gguf_mul_mat_batch(int wt, int64_t k, const gguf_mm_job *jobs, int njobs, int yt, gguf_stream_t stream) {
+    const char *what = "mul_mat_batch";
+    if (!is_weight(wt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "%s: weight type %d not supported", what, wt);
+    if (!is_float(yt)) return fail(GGUF_ERR_UNSUPPORTED_TYPE, "%s: y type %d is not F32/BF16/F16", what, yt);
+    if (njobs < 0 || njobs > GGUF_MAX_BATCH_JOBS || (njobs > 0 && !jobs))
+        return fail(GGUF_ERR_INVALID_ARG, "%s: %d jobs (0..%d)", what, njobs, GGUF_MAX_BATCH_JOBS);
+    if (k < 0) return fail(GGUF_ERR_INVALID_ARG, "%s: negative size", what);
+    if (row_size(wt, k) < 0) return fail(GGUF_ERR_SHAPE, "%s: k=%lld not a multiple of the block of type %d", what, (long long)k, wt);
+    gguf_mm_job_typed tj[GGUF_MAX_BATCH_JOBS];
+    for (int j = 0; j < njobs; j++) tj[j] = gguf_mm_job_typed{wt, k, jobs[j].segs, jobs[j].nseg, jobs[j].xq, jobs[j].m};
+    return mul_mat_batch_impl(what, tj, njobs, yt, stream);
+}
+
+gguf_status gguf_mul_mat_batch_typed(const gguf_mm_job_typed *jobs, int njobs, int yt, gguf_stream_t stream) {
+    return mul_mat_batch_impl("mul_mat_batch_typed", jobs, njobs, yt, stream);
 }
 
 // ---------------------------------------------------------------- MoE

@@ -276,6 +276,24 @@ typedef struct gguf_mm_job {
 } gguf_mm_job;
 gguf_status gguf_mul_mat_batch(int wt, int64_t k, const gguf_mm_job *jobs, int njobs, int yt, gguf_stream_t stream);
 
+/*
+ * gguf_mul_mat_batch_typed -- gguf_mul_mat_batch with the weight type and K
+ * given per job, so products of different types on one input (a layer's q
+ * and k in Q4_K and its v in Q6_K, all on the attention input) run in one
+ * chain and none waits for another.  Same rules and errors as
+ * gguf_mul_mat_batch, checked per job (GGUF_ERR_UNSUPPORTED_TYPE /
+ * GGUF_ERR_SHAPE name the job); one output type yt for all jobs.
+ */
+typedef struct gguf_mm_job_typed {
+    int wt;                    /* the job's weight type */
+    int64_t k;                 /* the job's K */
+    const gguf_segment *segs;  /* host array of the job's weight segments */
+    int nseg;                  /* 1 .. GGUF_MAX_SEGMENTS */
+    const void *xq;            /* q8_1 activation rows, [m][row_size(GGUF_Q8_1, k)] */
+    int64_t m;                 /* rows of xq */
+} gguf_mm_job_typed;
+gguf_status gguf_mul_mat_batch_typed(const gguf_mm_job_typed *jobs, int njobs, int yt, gguf_stream_t stream);
+
 /* mul_mat_id modes */
 #define GGUF_MOE_GATE_UP_SWIGLU 0   /* h[r] = silu(gate) * up, rounded to bf16, out as BF16 or Q8_1 */
 #define GGUF_MOE_DOWN_WEIGHTED_SUM 1 /* y[t] = sum_k route_w[t][k] * (W[e] . x[route]) */

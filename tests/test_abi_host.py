@@ -228,3 +228,23 @@ def test_copy_argument_checks(g):
         g.gguf_copy(torch.zeros(16, dtype=torch.uint8), torch.zeros(16, dtype=torch.uint8))
     with pytest.raises(ValueError):
         g.gguf_copy(torch.zeros(4, 4)[:, :2], torch.zeros(8))
+
+
+def test_mul_mat_batch_typed_argument_checks(g):
+    L = g.load_library()
+    seg = g.Segment(FAKE, 16, FAKE, 16)
+    segs = (g.Segment * 1)(seg)
+    def job(wt, k, m, xq=0x20000):
+        return g.MmJobTyped(wt, k, segs, 1, ctypes.c_void_p(xq), m)
+    def run(jobs, yt=None):
+        arr = (g.MmJobTyped * max(len(jobs), 1))(*jobs) if jobs else None
+        return L.gguf_mul_mat_batch_typed(arr, len(jobs), g.BF16 if yt is None else yt, None)
+    assert run([]) == 0
+    assert run([job(g.Q4_K, 256, 4)] * 9) == 1              # more than GGUF_MAX_BATCH_JOBS
+    assert run([job(g.Q4_K, 256, 4), job(3, 256, 4)]) == 2  # the second job's type (Q4_1) is unsupported
+    assert "job 1" in L.gguf_last_error().decode()
+    assert run([job(g.Q4_K, 256, 4), job(g.Q6_K, 100, 4)]) == 3   # the second job's K is not whole blocks
+    assert run([job(g.Q4_K, 256, 4)], yt=g.Q8_0) == 2
+    assert run([job(g.Q6_K, 256, 64)]) == 1                 # m = 64 is not decode-sized
+    assert run([job(g.Q4_K, 256, 4, xq=0x20002)]) == 4      # q8_1 rows must be 4-byte aligned
+    assert run([job(g.Q4_K, 256, 0)]) == 0                  # empty jobs are skipped

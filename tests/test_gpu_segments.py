@@ -187,3 +187,36 @@ def test_decode_step_as_benchmarked_full_size_sampled(g):
             y = dec.ys[(n, m)].float().cpu().numpy()
             assert np.isfinite(y).all(), f"{n} x {k}, M = {m}: an output was not written"
             assert_close(y[:, rows], ref, TOL_BF16, f"decode step {n} x {k}, M = {m}")
+
+
+@pytest.mark.parametrize("m", [1, 2, 5, 8])
+def test_mul_mat_batch_typed_mixed_types(g, m):
+    """Products of different weight types and K on their q8_1 inputs in one
+    chain (a layer's q + k in Q4_K and v in Q6_K on the attention input, and a
+    Q8_0 product with another K): each job equals its separate segment call bit
+    for bit and matches the oracle."""
+    D, KV, k2 = 3072, 1024, 1024
+    wq = oracle.quantize_weights(oracle.Q4_K, synth.normal((D, D), 0.02, seed=1))
+    wk = oracle.quantize_weights(oracle.Q4_K, synth.normal((KV, D), 0.02, seed=2))
+    wv = oracle.quantize_weights(oracle.Q6_K, synth.normal((KV, D), 0.02, seed=3))
+    w8 = oracle.quantize_weights(oracle.Q8_0, synth.normal((300, k2), 0.02, seed=4))
+    x = synth.activations(m, D, seed=m, dtype=torch.bfloat16)
+    x2 = synth.activations(m, k2, seed=m + 9, dtype=torch.bfloat16)
+    xq, xq2 = g.gguf_quantize_q8_1(x.to(DEV)), g.gguf_quantize_q8_1(x2.to(DEV))
+    out = {nm: torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=DEV)
+           for nm, n in (("q", D), ("k", KV), ("v", KV), ("e", 300))}
+    dw = {nm: _u8(w) for nm, w in (("q", wq), ("k", wk), ("v", wv), ("e", w8))}
+    g.gguf_mul_mat_batch_typed([(oracle.Q4_K, D, xq, [(dw["q"], D, out["q"]), (dw["k"], KV, out["k"])]),
+                                (oracle.Q6_K, D, xq, [(dw["v"], KV, out["v"])]),
+                                (oracle.Q8_0, k2, xq2, [(dw["e"], 300, out["e"])])])
+    sep = {nm: torch.empty_like(o) for nm, o in out.items()}
+    g.gguf_mul_mat_segments(oracle.Q4_K, D, xq, [(dw["q"], D, sep["q"]), (dw["k"], KV, sep["k"])], xt=g.Q8_1, m=m)
+    g.gguf_mul_mat(dw["v"], oracle.Q6_K, KV, D, xq, xt=g.Q8_1, m=m, out=sep["v"])
+    g.gguf_mul_mat(dw["e"], oracle.Q8_0, 300, k2, xq2, xt=g.Q8_1, m=m, out=sep["e"])
+    torch.cuda.synchronize()
+    xr, xr2 = oracle.quantize_q8_1(x.float().numpy()), oracle.quantize_q8_1(x2.float().numpy())
+    refs = {"q": oracle.mul_mat(oracle.Q4_K, wq, D, xr), "k": oracle.mul_mat(oracle.Q4_K, wk, D, xr),
+            "v": oracle.mul_mat(oracle.Q6_K, wv, D, xr), "e": oracle.mul_mat(oracle.Q8_0, w8, k2, xr2)}
+    for nm in out:
+        assert torch.equal(out[nm], sep[nm]), f"{nm}: typed batch differs from the separate call"
+        assert_close(out[nm].float().cpu().numpy(), refs[nm], TOL_BF16, f"typed batch {nm} m={m}")
