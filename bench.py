@@ -572,7 +572,7 @@ def secondary(torch, g, synth, dev, stream, hbm_peak, tf_peak, peak_kind):
             out[f"moe_ffn_decode_e256_top8_t{Td}"] = {
                 "us": round(ms * 1e3, 2), "routed_weight_mb": round(routed / 1e6, 2),
                 "gbs": round(routed / (ms * 1e-3) / 1e9, 1), "frac": round(routed / (ms * 1e-3) / 1e9 / hbm_peak, 3),
-                "note": "route-batched MMVQ path (quantize, route marks, gate_up, SwiGLU, q8_1, down, weighted sum)"}
+                "note": "route-batched MMVQ path (quantize with the route marks, gate_up, SwiGLU + q8_1, down, weighted sum)"}
         del wgu, wdn, x, y, ws
 
         # dequantize (a whole Q4_K / Q6_K matrix to bf16) and get_rows (8192 random rows of a Q6_K

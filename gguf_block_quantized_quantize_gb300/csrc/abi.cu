@@ -573,17 +573,27 @@ gguf_status gguf_mul_mat_id(const gguf_moe_args *a, void *ws, size_t ws_bytes, g
     if (vec) {
         // route-batched MMVQ: each active route reads its expert's rows once
         const int64_t rows = a->mode == GGUF_MOE_DOWN_WEIGHTED_SUM ? R : a->n_tokens;
-        const uint8_t *xq = (const uint8_t *)a->x;
-        if (a->xt != GGUF_Q8_1) {
-            if ((e = launch_quantize_q8_1(a->x, a->xt, rows, a->k, a->ldx, (uint8_t *)w.xh, nullptr, nullptr, s)) != cudaSuccess)
-                return cuda_status(e, "mul_mat_id quantize");
-            xq = (const uint8_t *)w.xh;
-        }
         const bool gu = a->mode == GGUF_MOE_GATE_UP_SWIGLU;
         const bool weighted = a->mode == GGUF_MOE_DOWN_WEIGHTED_SUM;
-        if ((e = moe_mark(a->ids, weighted ? a->route_w : nullptr, R, a->n_experts, weighted, a->dev_status, w.pos, s)) !=
-            cudaSuccess)
+        // the route marks ride on the quantize launch when there is one
+        const uint8_t *xq = (const uint8_t *)a->x;
+        if (a->xt != GGUF_Q8_1) {
+            RouteMarks mk;
+            mk.ids = a->ids;
+            mk.rw = weighted ? a->route_w : nullptr;
+            mk.R = R;
+            mk.E = a->n_experts;
+            mk.skip_zero_w = weighted ? 1 : 0;
+            mk.pos = w.pos;
+            mk.status = a->dev_status;
+            if ((e = launch_quantize_q8_1(a->x, a->xt, rows, a->k, a->ldx, (uint8_t *)w.xh, nullptr, nullptr, s, 0,
+                                          nullptr, nullptr, nullptr, 1, mk)) != cudaSuccess)
+                return cuda_status(e, "mul_mat_id quantize");
+            xq = (const uint8_t *)w.xh;
+        } else if ((e = moe_mark(a->ids, weighted ? a->route_w : nullptr, R, a->n_experts, weighted, a->dev_status,
+                                 w.pos, s)) != cudaSuccess) {
             return cuda_status(e, "mul_mat_id routes");
+        }
         const MmvqRoutes rt{a->ids, w.pos, a->expert_stride, a->top_k, weighted ? 1 : 0};
         if (plain) {
             if ((e = launch_mmvq_routes(a->wt, (const uint8_t *)a->w, rt, a->n, a->k, xq, R, w.z, s)) != cudaSuccess)
@@ -685,14 +695,24 @@ gguf_status gguf_moe_ffn(const gguf_moe_ffn_args *a, void *ws, size_t ws_bytes, 
     if (moe_vec(a->n_tokens, a->gate_up_type, a->hidden) && mmvq_routes_supported(a->down_type, a->inter)) {
         // route-batched MMVQ for both products: x -> q8_1, gate_up rows per
         // route, SwiGLU -> bf16 -> q8_1, down rows per route, weighted sum
+        // the route marks ride on the quantize launch (one launch fewer)
         const uint8_t *xq = (const uint8_t *)a->x;
         if (a->xt != GGUF_Q8_1) {
-            if ((e = launch_quantize_q8_1(a->x, a->xt, a->n_tokens, a->hidden, a->ldx, (uint8_t *)w.xh, nullptr, nullptr, s)) != cudaSuccess)
+            RouteMarks mk;
+            mk.ids = a->ids;
+            mk.rw = a->route_w;
+            mk.R = R;
+            mk.E = a->n_experts;
+            mk.skip_zero_w = 1;
+            mk.pos = w.pos;
+            mk.status = a->dev_status;
+            if ((e = launch_quantize_q8_1(a->x, a->xt, a->n_tokens, a->hidden, a->ldx, (uint8_t *)w.xh, nullptr,
+                                          nullptr, s, 0, nullptr, nullptr, nullptr, 1, mk)) != cudaSuccess)
                 return cuda_status(e, "moe_ffn quantize");
             xq = (const uint8_t *)w.xh;
-        }
-        if ((e = moe_mark(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w.pos, s)) != cudaSuccess)
+        } else if ((e = moe_mark(a->ids, a->route_w, R, a->n_experts, true, a->dev_status, w.pos, s)) != cudaSuccess) {
             return cuda_status(e, "moe_ffn routes");
+        }
         uint8_t *hq = (uint8_t *)w.h16;   // q8_1 rows of h ([R][I / 32] blocks fit in the fp16 operand buffer)
         if ((e = launch_mmvq_routes(a->gate_up_type, (const uint8_t *)a->w_gate_up,
                                     MmvqRoutes{a->ids, w.pos, a->gate_up_stride, a->top_k, 0}, 2 * a->inter, a->hidden,

@@ -38,10 +38,21 @@ cudaError_t launch_copy(void *dst, const void *src, int64_t bytes, cudaStream_t 
 // r = i * fan + j (j < fan); an active route (pos[r] >= 0) goes to operand
 // row offsets[ids[r]] + pos[r], a skipped one nowhere.  Each input row is
 // quantized once.
+// The route marks of the MoE vector path, written by the same launch when
+// ids != nullptr: pos[r] = r for an active route, -1 for one whose expert id
+// is outside [0, E) or (skip_zero_w) whose weight is 0; every id >= E adds 1
+// to *status (when not null).  The quantization does not wait for them.
+struct RouteMarks {
+    const int32_t *ids = nullptr;
+    const float *rw = nullptr;
+    int64_t R = 0, E = 0;
+    int skip_zero_w = 0;
+    int32_t *pos = nullptr, *status = nullptr;
+};
 cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int64_t ldx, uint8_t *xq,
                                  uint16_t *xh, uint16_t *xl, cudaStream_t s, int64_t pitch = 0,
                                  const int32_t *ids = nullptr, const int32_t *pos = nullptr,
-                                 const int32_t *offsets = nullptr, int32_t fan = 1);
+                                 const int32_t *offsets = nullptr, int32_t fan = 1, const RouteMarks &marks = {});
 // the same fp16 operand(s) from q8_1 rows
 cudaError_t launch_q8_1_to_f16(const uint8_t *xq, int64_t m, int64_t k, uint16_t *xh, uint16_t *xl, cudaStream_t s,
                                int64_t pitch = 0, const int32_t *ids = nullptr, const int32_t *pos = nullptr,

@@ -105,7 +105,7 @@ template <int XT, bool VEC>
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restrict__ x, int64_t m, int64_t k,
                                                             int64_t ldx, uint8_t *__restrict__ xq,
                                                             uint16_t *__restrict__ xh, uint16_t *__restrict__ xl,
-                                                            int64_t pitch, RowScatter map) {
+                                                            int64_t pitch, RowScatter map, RouteMarks mk) {
     // launched as a programmatic dependent: let the next kernel start its own
     // independent prefetch, and wait for the previous kernel before touching
     // memory it may still read or write
@@ -114,6 +114,12 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restri
     const int64_t nb = k / QK8;
     const int64_t total = m * nb;
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (mk.ids != nullptr && g < mk.R) {   // the MoE route marks (see RouteMarks)
+        const int32_t e = mk.ids[g];
+        const bool ok = e >= 0 && e < mk.E && !(mk.skip_zero_w && mk.rw != nullptr && mk.rw[g] == 0.0f);
+        if (e >= mk.E && mk.status != nullptr) atomicAdd(mk.status, 1);
+        mk.pos[g] = ok ? (int32_t)g : -1;
+    }
     const int64_t blk = g >> 2;
     const int j = (int)(g & 3);
     const bool active = blk < total;
@@ -183,9 +189,10 @@ __global__ void __launch_bounds__(256) q8_1_to_f16_kernel(const uint8_t *__restr
 
 cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, int64_t ldx, uint8_t *xq,
                                  uint16_t *xh, uint16_t *xl, cudaStream_t s, int64_t pitch, const int32_t *ids,
-                                 const int32_t *pos, const int32_t *offsets, int32_t fan) {
+                                 const int32_t *pos, const int32_t *offsets, int32_t fan, const RouteMarks &marks) {
     if (pitch < k) pitch = k;
-    const int64_t threads = m * (k / QK8) * 4;
+    int64_t threads = m * (k / QK8) * 4;
+    if (marks.ids != nullptr && marks.R > threads) threads = marks.R;
     if (threads == 0) return cudaSuccess;
     const int64_t grid = (threads + 255) / 256;
     const int esz = xt == GGUF_F32 ? 4 : 2;
@@ -200,7 +207,8 @@ cudaError_t launch_quantize_q8_1(const void *x, int xt, int64_t m, int64_t k, in
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const RowScatter map{ids, pos, offsets, fan < 1 ? 1 : fan};
-#define QLAUNCH(XT, V) (void)cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<XT, V>, x, m, k, ldx, xq, xh, xl, pitch, map)
+#define QLAUNCH(XT, V) \
+    (void)cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<XT, V>, x, m, k, ldx, xq, xh, xl, pitch, map, marks)
     if (xt == GGUF_F32) { if (vec) QLAUNCH(GGUF_F32, true); else QLAUNCH(GGUF_F32, false); }
     else if (xt == GGUF_BF16) { if (vec) QLAUNCH(GGUF_BF16, true); else QLAUNCH(GGUF_BF16, false); }
     else { if (vec) QLAUNCH(GGUF_F16, true); else QLAUNCH(GGUF_F16, false); }
