@@ -860,7 +860,7 @@ struct Q6KPiece {
 // takes piece l % (32 / G) of row l / (32 / G) and the lanes of each row are
 // reduced on their own.
 template <class PT, int M, int TG, int R, int MAXT, bool MULTI, bool ROUTES = false>
-__global__ void __launch_bounds__(MAXT, MAXT == 32 ? 12 : 1) mmvq_kernel(const MmvqSegs sg, int64_t k, int64_t rb,
+__global__ void __launch_bounds__(MAXT, MAXT == 32 ? 16 : 1) mmvq_kernel(const MmvqSegs sg, int64_t k, int64_t rb,
                                                    const uint8_t *__restrict__ xq, int m_act, int yt,
                                                    const MmvqRoutes rt) {
     const int64_t n = sg.rows();
@@ -1041,9 +1041,12 @@ inline cudaError_t launch_mmvq_cfg(const MmvqSegs &sg, int64_t k, int64_t rb, co
 // the route-batched launch: CTAs of one route over its rows (two per group),
 // as many per route as fill the GPU once.  Rows of at most 32 pieces (one
 // warp; MoE down rows of 512 values have 8) take a one-warp instance whose
-// buffers are sized for one warp, with registers for 12 resident CTAs per SM
-// (3 warps per SM sub-partition: up to 168 registers, no spills), and rows of
-// 32 / G whole pieces are packed G to a warp-row (rt.pack).
+// buffers are sized for one warp, with registers for 16 resident CTAs per SM
+// (4 warps per SM sub-partition: up to 128 registers; only the Q6_K instance
+// spills, 40 bytes), and rows of 32 / G whole pieces are packed G to a
+// warp-row (rt.pack).  Measured on GB300 against 12 CTAs per SM (168
+// registers, no spills) for the E=256 top-8 expert block: 16 tokens 101 ->
+// 84 us, 256 tokens 1160 -> 910 us, 4 tokens 37.5 -> 39.6 us.
 template <class PT>
 inline cudaError_t launch_mmvq_routes_pt(const uint8_t *bank, const MmvqRoutes &rt, int64_t n, int64_t k,
                                          int64_t rb, const uint8_t *xq, int64_t routes, float *z, cudaStream_t s) {
