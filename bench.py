@@ -374,7 +374,7 @@ def run_ours(args, rank, world, torch, dev):
 #       -k regex:mmvq -s 20 -c 8 python bench.py --steps 3 --warmup 3 --no-secondary --no-cpu-baseline
 # together with the SHA-256 of the MMVQ sources it was taken on.  The bench
 # reports the figure only while those sources are unchanged, and null otherwise.
-MMVQ_TRAFFIC = {"bytes": 42527808, "sources_sha256": "350016baa1ae90e129a8d4814cad4cbca15d35b93168d0deb433339c6825d6a5"}
+MMVQ_TRAFFIC = {"bytes": 42528704, "sources_sha256": "dd07a10bbdcf3fa4f9dc5d2f3dd2b08587e824c26b5679504e2983bfda658b55"}
 MMVQ_SOURCES = ("mmvq.cuh", "mmvq_mma.cuh", "mmvq_mma_q6k.cuh", "mmvq.cu", "mmvq_q4_k.cu", "common.cuh")
 
 
